@@ -1,0 +1,386 @@
+"""Pins of the fp64 CPU oracle against facts that do not come from the oracle:
+number-format definitions checked against torch's own casts, a library attention
+routine (torch SDPA in float64) on tiny batches, closed forms, invariants of the
+method, and the values the source pages print (tests/golden/plan_points.json)."""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from helpers import bits16, oracle_args, oracle_decode, oracle_decode_planned, oracle_plan
+from paged_kv_decode_split_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "plan_points.json")
+
+
+# ------------------------------------------------------------------ number formats
+
+def test_e4m3fn_all_256_codes_match_torch():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3fn_to_double(b) for b in range(256)])
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got))
+    assert nan.sum() == 2  # 0x7F and 0xFF only: e4m3fn has no infinities
+    assert np.array_equal(ref[~nan], got[~nan])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9
+
+
+def test_bf16_and_fp16_all_codes_match_torch():
+    codes = torch.arange(65536, dtype=torch.int32).to(torch.int16)
+    for dt, fn in ((torch.bfloat16, oracle.bf16_to_double), (torch.float16, oracle.fp16_to_double)):
+        ref = codes.view(dt).to(torch.float64).numpy()
+        got = np.array([fn(b) for b in range(65536)])
+        nan = np.isnan(ref)
+        assert np.array_equal(nan, np.isnan(got))
+        assert np.array_equal(ref[~nan], got[~nan])
+
+
+# ------------------------------------------------------------ attention: library routine
+
+def _dequant(t: torch.Tensor, kv_dtype: str, scale: float) -> torch.Tensor:
+    if kv_dtype == "fp8":
+        return t.view(torch.float8_e4m3fn).to(torch.float64) * scale
+    return t.to(torch.float64)
+
+
+def sdpa_reference(w) -> torch.Tensor:
+    """Each request's keys gathered densely with torch indexing, then torch's
+    scaled_dot_product_attention in float64 with the end-aligned causal mask
+    (token i of L sees the first S-(L-1-i) keys); rows of padding, empty requests
+    and rows with no visible key are zero."""
+    n, G = w.num_seqs, w.num_q_heads // w.num_kv_heads
+    out = torch.zeros(w.num_tokens, w.num_q_heads, w.head_dim, dtype=torch.float64)
+    cu = w.cu_query_lens
+    for r in range(n):
+        S = int(w.context_lens[r])
+        rows = list(range(int(cu[r]), int(cu[r + 1]))) if cu is not None else [r]
+        L = len(rows)
+        if S <= 0 or L == 0:
+            continue
+        pages = w.block_tables[r, : -(-S // w.block_size)].long()
+        K = _dequant(w.k_cache[pages], w.kv_dtype, w.k_scale)  # [p, Hkv, bs, D]
+        V = _dequant(w.v_cache[pages], w.kv_dtype, w.v_scale)
+        K = K.permute(1, 0, 2, 3).reshape(w.num_kv_heads, -1, w.head_dim)[:, :S]
+        V = V.permute(1, 0, 2, 3).reshape(w.num_kv_heads, -1, w.head_dim)[:, :S]
+        K = K.repeat_interleave(G, dim=0)  # q head hq uses kv head hq // G
+        V = V.repeat_interleave(G, dim=0)
+        q = w.q[rows].to(torch.float64).permute(1, 0, 2)  # [Hq, L, D]
+        mask = torch.ones(L, S, dtype=torch.bool).tril(diagonal=S - L)
+        o = F.scaled_dot_product_attention(q, K, V, attn_mask=mask, scale=w.scale)
+        visible = mask.any(dim=1)
+        o[:, ~visible] = 0.0
+        out[rows] = o.permute(1, 0, 2)
+    return out
+
+
+CASES = [
+    dict(name="decode_bf16", lens=[17, 64, 200, 1000], ql=None, H=(8, 2), D=64, bs=16, kv="bf16"),
+    dict(name="decode_fp8", lens=[1, 33, 300], ql=None, H=(8, 1), D=128, bs=16, kv="fp8"),
+    dict(name="decode_fp16", lens=[5, 129], ql=None, H=(4, 4), D=64, bs=64, kv="fp16"),
+    dict(name="verify", lens=[40, 7, 130], ql=[3, 3, 3], H=(6, 1), D=64, bs=16, kv="bf16", pad=2),
+    dict(name="mixed", lens=[50, 0, 20, 9], ql=[1, 2, 20, 0], H=(4, 2), D=64, bs=16, kv="bf16",
+         pad=3),
+    dict(name="short_ctx", lens=[2, 3], ql=[4, 1], H=(2, 1), D=64, bs=16, kv="fp8", pad=1),
+]
+
+
+def _case(c, seed=0, **kw):
+    return wl.make_batch(c["name"], c["lens"], c["ql"], c["H"][0], c["H"][1], c["D"], c["bs"],
+                         c["kv"], seed=seed, pad_tokens=c.get("pad", 0), kv_scale=0.05, **kw)
+
+
+@pytest.mark.parametrize("c", CASES, ids=[c["name"] for c in CASES])
+def test_dense_matches_torch_sdpa(c):
+    w = _case(c)
+    got = oracle_decode(w)
+    ref = sdpa_reference(w).numpy()
+    assert np.abs(got - ref).max() < 1e-12
+
+
+def test_sdpa_reference_sees_the_per_token_causal_range():
+    # "short_ctx": request 0 has S=2 keys and L=4 tokens: tokens 0 and 1 see no key
+    # (S-(L-1-i) <= 0) and must be zero; tokens 2 and 3 see 1 and 2 keys.
+    w = _case(CASES[-1])
+    out = oracle_decode(w)
+    assert np.all(out[0] == 0) and np.all(out[1] == 0)
+    assert np.any(out[2] != 0) and np.any(out[3] != 0)
+
+
+# ------------------------------------------------------------------- closed forms
+
+def _single(S, L=1, H=(4, 2), D=64, bs=16, kv="bf16", seed=3):
+    return wl.make_batch("single", [S], None if L == 1 else [L], H[0], H[1], D, bs, kv,
+                         seed=seed, kv_scale=0.05)
+
+
+def test_one_key_returns_that_value_row():
+    w = _single(1)
+    out = oracle_decode(w)
+    page = int(w.block_tables[0, 0])
+    for hq in range(w.num_q_heads):
+        v = w.v_cache[page, hq // 2, 0].to(torch.float64).numpy()
+        assert np.array_equal(out[0, hq], v)
+
+
+def test_zero_query_gives_mean_of_visible_values():
+    w = _single(77, L=3)
+    w.q.zero_()
+    out = oracle_decode(w)
+    for i in range(3):
+        K = 77 - (3 - 1 - i)
+        pages = w.block_tables[0].long()
+        V = w.v_cache[pages].to(torch.float64).permute(1, 0, 2, 3).reshape(2, -1, 64)[:, :K]
+        for hq in range(4):
+            assert np.allclose(out[i, hq], V[hq // 2].mean(0).numpy(), atol=1e-13, rtol=0)
+
+
+def test_constant_values_give_that_constant():
+    w = _single(300, kv="fp8")
+    w.v_cache.fill_(0x38)  # e4m3fn 0x38 = 1.0
+    out = oracle_decode(w)
+    assert np.allclose(out, 1.0 * w.v_scale, atol=1e-14, rtol=0)
+
+
+def test_dominant_key_selects_its_value():
+    w = _single(100)
+    w.k_cache.zero_()
+    pages = w.block_tables[0].long()
+    j = 57
+    w.k_cache[pages[j // 16], :, j % 16] = w.q[0].reshape(2, 2, 64)[:, 0] * 64  # huge logit
+    out = oracle_decode(w)
+    v = w.v_cache[pages[j // 16], 0, j % 16].to(torch.float64).numpy()
+    assert np.allclose(out[0, 0], v, atol=1e-12)
+
+
+# -------------------------------------------------------------------- invariants
+
+def _repage(w, new_bs: int, seed: int):
+    """The same logical keys stored under another page size and a fresh random
+    physical page order."""
+    g = torch.Generator().manual_seed(seed)
+    n = w.num_seqs
+    dense_k, dense_v = [], []
+    for r in range(n):
+        S = int(w.context_lens[r])
+        p = -(-S // w.block_size) if S > 0 else 0
+        pages = w.block_tables[r, :p].long()
+        dense_k.append(w.k_cache[pages].permute(1, 0, 2, 3).reshape(w.num_kv_heads, -1, w.head_dim))
+        dense_v.append(w.v_cache[pages].permute(1, 0, 2, 3).reshape(w.num_kv_heads, -1, w.head_dim))
+    need = [(-(-int(s) // new_bs) if s > 0 else 0) for s in w.context_lens.tolist()]
+    nb = sum(need) + 5
+    perm = torch.randperm(nb, generator=g)
+    shape = (nb, w.num_kv_heads, new_bs, w.head_dim)
+    k = torch.full(shape, 0x7F if w.kv_dtype == "fp8" else 0, dtype=w.k_cache.dtype)
+    v = k.clone()
+    bt = torch.full((n, max(1, max(need))), -1, dtype=torch.int32)
+    at = 0
+    for r in range(n):
+        for b in range(need[r]):
+            page = int(perm[at]); at += 1
+            bt[r, b] = page
+            lo, hi = b * new_bs, min((b + 1) * new_bs, dense_k[r].shape[1])
+            k[page, :, : hi - lo] = dense_k[r][:, lo:hi]
+            v[page, :, : hi - lo] = dense_v[r][:, lo:hi]
+    return wl.Workload(w.name, w.q, k, v, w.kv_dtype, w.k_scale, w.v_scale, bt, w.context_lens,
+                       w.cu_query_lens, w.scale, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                       new_bs, w.budget, w.max_partitions)
+
+
+@pytest.mark.parametrize("c", CASES[:4], ids=[c["name"] for c in CASES[:4]])
+def test_output_independent_of_paging(c):
+    w = _case(c)
+    base = oracle_decode(w)
+    for i, bs in enumerate((16, 64, 128)):
+        other = oracle_decode(_repage(w, bs, seed=11 + i))
+        assert np.abs(other - base).max() < 1e-12
+
+
+def test_cu_arange_is_bitwise_the_no_cu_path():
+    w = _case(CASES[0])
+    a = oracle_decode(w)
+    w2 = wl.Workload(**{**w.__dict__, "cu_query_lens": torch.arange(5, dtype=torch.int32)})
+    b = oracle_decode(w2)
+    assert np.array_equal(a, b)
+
+
+def test_padding_rows_and_empty_requests_are_zero():
+    w = _case(CASES[4])  # lens [50, 0, 20, 9], ql [1, 2, 20, 0], 3 padding rows
+    out = oracle_decode(w)
+    cu = w.cu_query_lens.tolist()
+    assert np.all(out[cu[1]:cu[2]] == 0)          # request 1 has S = 0
+    assert np.all(out[cu[-1]:] == 0)             # graph padding rows
+    assert np.all(np.isfinite(out))
+    # request 2 (S=20, L=20): token 0 sees exactly one key -> that key's value
+    page = int(w.block_tables[2, 0])
+    t0 = cu[2]
+    for hq in range(4):
+        assert np.array_equal(out[t0, hq], w.v_cache[page, hq // 2, 0].to(torch.float64).numpy())
+
+
+def test_adding_a_padding_row_changes_no_other_row():
+    c = dict(CASES[3]); c["pad"] = 0
+    w = _case(c)
+    a = oracle_decode(w)
+    extra = torch.randn(5, w.num_q_heads, w.head_dim).to(w.q.dtype)
+    w2 = wl.Workload(**{**w.__dict__, "q": torch.cat([w.q, extra])})
+    b = oracle_decode(w2)
+    assert np.array_equal(a, b[: a.shape[0]]) and np.all(b[a.shape[0]:] == 0)
+
+
+@pytest.mark.parametrize("c", CASES, ids=[c["name"] for c in CASES])
+def test_merge_identity_for_any_split_count(c):
+    """Partial softmaxes over the plan's tasks plus the LSE merge give the dense
+    result, whatever the split count (1 ... 256) and the plan kind."""
+    w = _case(c)
+    dense = oracle_decode(w)
+    for P, W in ((1, 8), (2, 8), (7, 100), (256, 512), (256, 4096)):
+        for kind in (oracle.PLAN_PROPORTIONAL, oracle.PLAN_UNIFORM):
+            work, red = oracle_plan(w, W, kind, max_partitions=P)
+            got = oracle_decode_planned(w, work, red)
+            assert np.abs(got - dense).max() < 1e-12, (P, W, kind)
+
+
+def test_merge_identity_uses_every_partition():
+    # a plan whose tasks split a 1000-token request in several parts
+    w = _case(CASES[0])
+    work, red = oracle_plan(w, 4096, max_partitions=256)
+    assert red[3, 1] == 4
+    dense = oracle_decode(w)
+    bad = work.copy()
+    bad[red[3, 0], 2] -= 1  # drop the last tile of the first part
+    got = oracle_decode_planned(w, bad, red)
+    assert np.abs(got[3] - dense[3]).max() > 1e-3
+
+
+# ---------------------------------------------------------------------- work plan
+
+def test_golden_capacities():
+    g = json.load(open(GOLDEN))
+    for e in g["capacity"]:
+        assert oracle.plan_capacity(e["n"], e["num_kv_heads"], e["max_partitions"],
+                                    e["budget"]) == e["capacity"], e["cite"]
+
+
+def _lens(e):
+    if "context_lens" in e:
+        return e["context_lens"]
+    v, k = e["context_lens_repeat"]
+    return [v] * k
+
+
+def test_golden_partition_counts():
+    g = json.load(open(GOLDEN))
+    for e in g["partitions"]:
+        lens = np.array(_lens(e), dtype=np.int32)
+        want = e["parts"] if "parts" in e else [e["parts_repeat"][0]] * e["parts_repeat"][1]
+        _, red = oracle.plan(lens, None, e["num_kv_heads"], e["max_partitions"], e["budget"])
+        assert red[:, 1].tolist() == want, e["cite"]
+        if "same_with_max_partitions" in e:
+            _, red2 = oracle.plan(lens, None, e["num_kv_heads"], e["same_with_max_partitions"],
+                                  e["budget"])
+            assert red2[:, 1].tolist() == want, e["cite"]
+
+
+def test_golden_tile_counts():
+    g = json.load(open(GOLDEN))
+    for e in g["tiles"]:
+        for S, nt in zip(e["context_lens"], e["tiles"]):
+            work, red = oracle.plan(np.array([S], np.int32), None, 1, 100000, 10 ** 6)
+            p = red[0, 1]
+            assert p == nt  # one tile per partition when the budget is unbounded
+            assert work[p - 1, 2] == nt and work[0, 1] == 0
+
+
+def test_capacity_ceil_and_floor():
+    assert oracle.plan_capacity(1, 3, 256, 10) == 4      # ceil(10 / 3)
+    assert oracle.plan_capacity(32, 4, 256, 296) == 74
+    assert oracle.plan_capacity(512, 8, 256, 304) == 512  # never below the batch
+    assert oracle.plan_capacity(2, 1, 3, 512) == 6        # never above n * P
+
+
+def _check_plan(lens, qlens, Hkv, P, W, kind):
+    lens = np.asarray(lens, np.int32)
+    cu = None if qlens is None else np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    work, red = oracle.plan(lens, cu, Hkv, P, W, kind)
+    n, C = len(lens), work.shape[0]
+    ql = np.ones(n, int) if qlens is None else np.asarray(qlens)
+    active = (lens > 0) & (ql > 0)
+    parts = red[:, 1]
+    T = oracle.TILE
+    tiles = -(-lens.astype(np.int64) // T)
+    assert parts.sum() <= C
+    assert np.all(parts[~active] == 0)
+    assert np.all(parts[active] >= 1)
+    assert np.all(parts[active] <= np.minimum(P, tiles[active]))
+    assert np.array_equal(red[:, 0], np.concatenate([[0], np.cumsum(parts)[:-1]]))
+    for r in range(n):
+        f, p = red[r]
+        if p == 0:
+            continue
+        seg = work[f:f + p]
+        assert np.all(seg[:, 0] == r) and np.all(seg[:, 3] == lens[r])
+        assert seg[0, 1] == 0 and seg[-1, 2] == tiles[r]
+        assert np.all(seg[1:, 1] == seg[:-1, 2]) and np.all(seg[:, 2] > seg[:, 1])
+        sizes = seg[:, 2] - seg[:, 1]
+        assert sizes.max() - sizes.min() <= 1     # even chunking
+    assert np.all(work[parts.sum():, 0] == -1)
+    return work, red, active
+
+
+@pytest.mark.parametrize("kind", [oracle.PLAN_PROPORTIONAL, oracle.PLAN_UNIFORM])
+@pytest.mark.parametrize("seed", range(6))
+def test_plan_invariants_random(kind, seed):
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(1, 300))
+    lens = np.clip(np.round(np.exp(rng.normal(np.log(4096), 1.5, n))), 1, 131072).astype(np.int32)
+    lens[rng.random(n) < 0.1] = 0
+    qlens = None if seed % 2 == 0 else rng.integers(0, 5, n)
+    Hkv = int(rng.choice([1, 2, 4, 8]))
+    P = int(rng.choice([1, 8, 64, 256]))
+    W = int(rng.choice([296, 304, 512, 2048]))
+    work, red, active = _check_plan(lens, qlens, Hkv, P, W, kind)
+    parts = red[:, 1]
+    if kind == oracle.PLAN_PROPORTIONAL:
+        # monotone in context length among active requests
+        idx = np.where(active)[0]
+        order = idx[np.argsort(lens[idx], kind="stable")]
+        assert np.all(np.diff(parts[order]) >= 0)
+    else:
+        C = work.shape[0]
+        tiles = -(-lens.astype(np.int64) // oracle.TILE)
+        cap = min(P, C // max(1, active.sum()))
+        assert np.array_equal(parts[active], np.minimum(cap, tiles[active]))
+
+
+def test_plan_proportional_rule_by_hand():
+    # C = min(3*256, max(3, ceil(304/4))) = 76; n_act = 3; sum S = 11000
+    lens = np.array([1000, 2000, 8000], np.int32)
+    work, red = oracle.plan(lens, None, 4, 256, 304)
+    assert work.shape[0] == 76
+    # 1 + floor(73*S/11000): 1000 -> 7 (cap 4 tiles), 2000 -> 14 (cap 8), 8000 -> 54 (cap 32)
+    assert red[:, 1].tolist() == [4, 8, 32]
+    lens = np.array([100000, 5000, 300], np.int32)
+    _, red = oracle.plan(lens, None, 4, 256, 304)
+    # 1 + floor(73*S/105300): 100000 -> 70, 5000 -> 4, 300 -> 1
+    assert red[:, 1].tolist() == [70, 4, 1]
+    _, red = oracle.plan(lens, None, 4, 256, 304, kind=oracle.PLAN_UNIFORM)
+    # floor(76/3) = 25 each, capped by tiles: 391 -> 25, 20 -> 20, 2 -> 2
+    assert red[:, 1].tolist() == [25, 20, 2]
+
+
+def test_plan_skips_zero_length_and_rowless_requests():
+    lens = np.array([500, 0, 700, 300], np.int32)
+    cu = np.array([0, 1, 2, 2, 5], np.int32)   # request 2 owns no query row
+    work, red = oracle.plan(lens, cu, 1, 256, 16)
+    assert red[:, 1].tolist()[1:3] == [0, 0]
+    # n_act = 2, sum S = 800, C = 16: 1 + floor(14*500/800) = 9 -> 2 tiles; 1 + floor(14*300/800) = 6 -> 2
+    assert red[:, 1].tolist() == [2, 0, 0, 2]
+    assert red[:, 0].tolist() == [0, 2, 2, 2]
