@@ -1,0 +1,199 @@
+/*
+ * pa.h -- C ABI of libpa: paged-KV GQA decode attention with a
+ * context-proportional split-KV work plan, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (sources are web pages, cited by title and section):
+ *
+ *   [ATOM-2366] ROCm/ATOM pull 2366, "[MiniMax-M3] Route the paged decode to
+ *     aiter's FlyDSL kernel with work planner".  Section 1 (Motivation): a
+ *     planner hands each request a partition count proportional to its real
+ *     context length.  Section 3 (Design): the work budget is 2 x CU, the
+ *     partition ceiling 256; the plan depends on context_lens only, is built
+ *     once per forward, refreshed in place (no allocation, no device-to-host
+ *     copy) so it can be captured in a CUDA graph.  Section 5, "Planner drift
+ *     at the real ceiling": capacity = min(batch x max_partitions,
+ *     max(batch, 2 x CU / kv_heads)).  Review item 2: the plan stores per-task
+ *     begin/end tiles plus seq_ctx (word 3 of each 4-word task).  Review item
+ *     5: the capability gate (dtypes, block size, head_dim, int32 tables,
+ *     q heads divisible by kv heads, out shaped and typed like q).
+ *   [ATOM-2514] ROCm/ATOM pull 2514, "Fix(attention): adapt the FlyDSL paged
+ *     decode to aiter #5809 (explicit work plans)".  Motivation/Design: every
+ *     decode call takes an explicit plan with the default 2 x CU budget; more
+ *     than 4096 sequences is outside the planner's domain.
+ *   [RDNA-29] opengfx1030/vllm-rdna pull 29 (mixed and MTP-verify batches),
+ *     Change section 1 "Kernel: per-token causal decode": with cu_query_lens a
+ *     request owns L = cu[r+1]-cu[r] consecutive query rows; its token i
+ *     attends to the first S - (L - 1 - i) keys; rows past cu[num_seqs] and
+ *     rows of zero-length requests come out as zeros; without cu_query_lens
+ *     row r is request r's single token.
+ *
+ * For query row t of request r (token i), q head hq and kv head h = hq / G
+ * (G = Hq / Hkv), with K_t = S_r - (L_r - 1 - i) visible keys:
+ *     out[t, hq, :] = sum_j softmax_j(scale * <q[t,hq], k_j>) * v_j,  j < K_t,
+ * k_j / v_j the j-th key/value row of request r in kv head h, gathered through
+ * block_tables.  fp8 caches hold OCP float8 e4m3fn codes; a code c means
+ * e4m3fn(c) * k_scale (keys) or * v_scale (values).
+ *
+ * Data layouts (all row-major, contiguous, device memory unless stated):
+ *   q, out          [num_tokens, Hq, D]          bf16 or fp16; out has q's dtype
+ *   k_cache,v_cache [num_blocks, Hkv, block_size, D]  bf16, fp16 or e4m3fn bytes
+ *   block_tables    int32 [num_seqs, max_blocks_per_seq]; entry b of row r is
+ *                   the physical block holding keys [b*bs, (b+1)*bs) of r
+ *   context_lens    int32 [num_seqs]  KV length of each request (query tokens
+ *                   included)
+ *   cu_query_lens   int32 [num_seqs + 1] or NULL; nondecreasing, cu[0] == 0
+ *
+ * Work plan (device memory owned by the plan):
+ *   work_info   int32 [capacity][4] = (seq, tile_begin, tile_end, seq_ctx);
+ *               seq = -1 marks an unused slot.  A task covers keys
+ *               [tile_begin*256, min(tile_end*256, seq_ctx)).
+ *   reduce_info int32 [num_seqs][2] = (first_slot, num_parts); slots are
+ *               request-major, first_slot is the running sum of num_parts.
+ *   Rule (integer, int64 intermediates), with n_act the requests that have
+ *   S > 0 and at least one query row, and T = 256 tokens:
+ *     capacity C = min(n * P, max(n, ceil(W / Hkv)))
+ *     PROPORTIONAL: p_r = min(P, ceil(S_r/T), 1 + floor((C - n_act) * S_r / sum S))
+ *     UNIFORM:      p_r = min(P, ceil(S_r/T), floor(C / n_act))
+ *     inactive requests: p_r = 0.  Part j of request r covers tiles
+ *     [floor(j*nt/p), floor((j+1)*nt/p)), nt = ceil(S_r/T).
+ *   The proportional rule's integer form (reserve one partition per active
+ *   request, share the rest in proportion to S with floor rounding) and the
+ *   uniform comparator are this library's reading of the pages, which give no
+ *   closed integer form for either.
+ *
+ * Streams, ownership, capture: every call that takes a stream enqueues its
+ * work on that stream (a cudaStream_t passed as void*; NULL = legacy default
+ * stream) and returns without synchronising, unless stated.  The caller owns
+ * every tensor.  A plan owns its device buffers, allocated only by
+ * pa_plan_build and released by pa_plan_destroy; pa_plan_refresh and
+ * pa_decode never allocate and never wait on the host, so both may be
+ * captured in a CUDA graph.  One plan may be in flight on one stream at a time
+ * (its partial-result scratch is per plan).  pa_plan_refresh must run after
+ * every change of context_lens or cu_query_lens and before the pa_decode
+ * calls that use it; pa_decode detects a plan refreshed from other lengths and
+ * reports it through the device error word (PA_DEVERR_STALE_PLAN) rather than
+ * computing over the wrong key ranges.
+ *
+ * Errors: every function returns PA_OK or a negative PA_ERR_* status; nothing
+ * aborts, throws across the ABI, or falls back to another implementation.
+ * Problems only visible on the device (bad block-table entries, a stale plan,
+ * lengths beyond what the plan was built for) set bits in a sticky per-plan
+ * error word, read with pa_plan_read_errors.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = -1,   /* null pointer, negative size, misaligned pointer, bad code */
+  PA_ERR_UNSUPPORTED = -2,   /* outside the supported domain (dtype, D, block size, ...) */
+  PA_ERR_PLAN_MISMATCH = -3, /* call disagrees with the plan (shape, never refreshed, ...) */
+  PA_ERR_CUDA = -4,          /* a CUDA runtime/driver call failed (no device, launch error) */
+  PA_ERR_OOM = -5            /* device allocation failed in pa_plan_build */
+};
+
+/* Element types. */
+enum pa_dtype { PA_BF16 = 0, PA_FP16 = 1, PA_FP8_E4M3 = 2 };
+
+/* Plan kinds: the context-proportional plan, and the uniform comparator. */
+enum pa_plan_kind { PA_PLAN_PROPORTIONAL = 0, PA_PLAN_UNIFORM = 1 };
+
+/* Sticky device error bits. */
+#define PA_DEVERR_STALE_PLAN 0x1u    /* lengths differ from those of the last refresh */
+#define PA_DEVERR_BAD_PAGE 0x2u      /* a needed block-table entry is outside [0, num_blocks)
+                                        or past max_blocks_per_seq; its keys read as zeros */
+#define PA_DEVERR_PLAN_OVERFLOW 0x4u /* refresh saw a query length above max_query_len, more
+                                        than max_tokens rows, or a malformed cu_query_lens;
+                                        the plan was emptied (every output row becomes 0) */
+#define PA_DEVERR_TIMEOUT 0x8u       /* a bounded wait inside a kernel gave up */
+
+#define PA_TILE_TOKENS 256          /* partition tile, in tokens */
+#define PA_DEFAULT_MAX_PARTITIONS 256
+#define PA_MAX_SEQS 4096
+
+typedef struct pa_plan pa_plan; /* opaque */
+
+/* Creates a plan for batches of exactly num_seqs requests on device `device`
+ * and allocates its device buffers: work_info, reduce_info, the per-request
+ * snapshot of query lengths, the error word, and fp32 partial-result scratch
+ * sized for at most max_query_len query rows per request and max_tokens rows
+ * per call.  max_partitions <= 0 selects 256; budget <= 0 selects
+ * 2 x multiProcessorCount of the device ([ATOM-2514] Design, "default
+ * budget").  kind is a pa_plan_kind.  The plan is unusable by pa_decode until
+ * the first pa_plan_refresh.  Supported: 1 <= num_seqs <= 4096, Hq % Hkv == 0,
+ * head_dim in {64, 128, 256}.  Returns PA_ERR_OOM / PA_ERR_CUDA on device
+ * failures (nothing is leaked), PA_ERR_INVALID_ARG / PA_ERR_UNSUPPORTED on bad
+ * parameters.  On success *plan owns the buffers until pa_plan_destroy. */
+int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_q_heads, int num_kv_heads,
+                  int head_dim, int max_query_len, int max_tokens, int max_partitions, int budget,
+                  int kind);
+
+/* Recomputes the plan in place from the live device arrays context_lens
+ * [num_seqs] and cu_query_lens [num_seqs + 1] (NULL: one query row per
+ * request), on `stream`: one kernel, no allocation, no host synchronisation
+ * ([ATOM-2366] section 3, plan lifetime vs cudagraph).  Whether cu_query_lens
+ * was given is remembered: pa_decode must be called the same way. */
+int pa_plan_refresh(pa_plan* plan, const int32_t* context_lens, const int32_t* cu_query_lens,
+                    void* stream);
+
+/* Paged decode over the plan's tasks, then an LSE-weighted merge of each
+ * request's partial results ([ATOM-2366] sections 3 and 6 item 5: split
+ * attention tile, then the partial-softmax reduce).  Arguments follow the
+ * layouts above; num_q_heads, head_dim, num_kv_heads and num_seqs must equal
+ * the plan's.  q_dtype is PA_BF16 or PA_FP16; kv_dtype is PA_BF16 (q bf16),
+ * PA_FP16 (q fp16) or PA_FP8_E4M3 (q bf16 or fp16; the dot products then run
+ * on fp16 values, so |q| must stay below 65504).  k_scale / v_scale apply to
+ * fp8 caches only and must be finite.  block_size in {16, 64, 128};
+ * num_blocks * num_kv_heads * block_size < 2^31.  Without cu_query_lens
+ * num_tokens == num_seqs; with it, num_tokens >= 1 and rows past
+ * cu[num_seqs] are graph padding (written as zeros).  q, out, k_cache and
+ * v_cache must be 16-byte aligned.  Every output row is written.  Enqueues
+ * two kernels on `stream`; returns without waiting. */
+int pa_decode(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int num_q_heads,
+              int head_dim, const void* k_cache, const void* v_cache, int kv_dtype, float k_scale,
+              float v_scale, int num_blocks, int num_kv_heads, int block_size,
+              const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+              const int32_t* cu_query_lens, int num_seqs, float scale, void* out, void* stream);
+
+/* Host-side facts about a plan (any pointer may be NULL): its capacity C, the
+ * batch size, the budget W and ceiling P actually used, the plan kind, the
+ * device, and the bytes of device memory it owns. */
+int pa_plan_info(const pa_plan* plan, int* capacity, int* num_seqs, int* budget,
+                 int* max_partitions, int* kind, int* device, long long* device_bytes);
+
+/* Copies the current work_info (capacity x 4 int32) and reduce_info
+ * (num_seqs x 2 int32) to host memory, ordered after prior work on `stream`,
+ * and waits for the copy (synchronises `stream`; not capturable).  Either
+ * destination may be NULL.  For tests and diagnostics. */
+int pa_plan_download(const pa_plan* plan, int32_t* work_info, int32_t* reduce_info, void* stream);
+
+/* Reads the plan's sticky device error word (PA_DEVERR_* bits) into *errors,
+ * ordered after prior work on `stream`; waits for it (synchronises `stream`;
+ * not capturable).  clear != 0 resets the word to 0 afterwards. */
+int pa_plan_read_errors(pa_plan* plan, uint32_t* errors, int clear, void* stream);
+
+/* Profiling hook: when both are non-NULL, every later pa_decode records
+ * start_event immediately before its split-KV kernel and stop_event right
+ * after it, on the decode stream (cudaEvent_t values passed as void*; the
+ * caller owns them).  NULL, NULL turns it off. */
+int pa_plan_set_split_events(pa_plan* plan, void* start_event, void* stop_event);
+
+/* Releases the plan's device buffers and the plan (NULL is a no-op).  The
+ * caller must ensure no enqueued work still uses the plan. */
+int pa_plan_destroy(pa_plan* plan);
+
+/* A static, human-readable name for a status code. */
+const char* pa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -1,0 +1,429 @@
+// pa_api.cu -- the C ABI declared in include/pa.h: argument validation (the
+// capability gate of "[MiniMax-M3] Route the paged decode to aiter's FlyDSL
+// kernel with work planner", review item 5), plan memory, TMA descriptors and
+// the kernel launches.  Host code only; every step of the computation runs in
+// the kernels of pa_plan.cu, pa_split_d*.cu and pa_merge.cu.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "../../include/pa.h"
+#include "pa_internal.h"
+
+namespace {
+
+struct TmapSlot {
+  bool valid = false;
+  const void* ptr = nullptr;
+  int num_blocks = 0, Hkv = 0, bs = 0, D = 0, dtype = 0;
+  CUtensorMap map;
+};
+
+// Current-device guard: the ABI never leaves the caller's current device changed.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) return;
+    ok = (prev == dev) || (cudaSetDevice(dev) == cudaSuccess);
+  }
+  ~DeviceGuard() {
+    int cur;
+    if (ok && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+struct pa_plan {
+  int device, n, Hq, Hkv, D, max_qlen, max_tokens, P, W, kind, C;
+  long long rows_cap;
+  pa::PlanDev dev;
+  void* mem;
+  long long bytes;
+  int refreshed;  // 0: never; 1: without cu_query_lens; 2: with cu_query_lens
+  cudaEvent_t ev_start, ev_stop;
+  TmapSlot tmaps[8];
+  int tmap_next;
+};
+
+namespace pa {
+
+int split_box_row_bytes(int D, int kv_dtype) {
+  const int row = D * (kv_dtype == PA_FP8_E4M3 ? 1 : 2);
+  return row < 128 ? row : 128;
+}
+
+int split_box_rows(int D, int kv_dtype, int bs) {
+  const int ks = 16384 / (D * (kv_dtype == PA_FP8_E4M3 ? 1 : 2));  // keys per stage
+  return bs < ks ? bs : ks;
+}
+
+int split_row_groups(int max_qlen, int G) {
+  const long long rows = static_cast<long long>(max_qlen) * G;
+  if (rows <= 32) return static_cast<int>((rows + 7) / 8);
+  return 1;  // long prompt rows take several passes over their (short) key range
+}
+
+cudaError_t launch_split(const SplitParams& p, int C, int D, int kv_dtype, int row_groups,
+                         const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s) {
+  switch (D) {
+    case 64: return launch_split_d64(p, C, kv_dtype, row_groups, tk, tv, s);
+    case 128: return launch_split_d128(p, C, kv_dtype, row_groups, tk, tv, s);
+    default: return launch_split_d256(p, C, kv_dtype, row_groups, tk, tv, s);
+  }
+}
+
+}  // namespace pa
+
+namespace {
+
+// TMA view of a cache [num_blocks, Hkv, bs, D] as a 2-D tensor of
+// num_blocks*Hkv*bs rows x D elements; boxes of box_rows rows x one swizzle
+// span (128 bytes, or 64 for a 64-byte row), swizzled to match the kernel.
+int make_tmap(pa_plan* plan, const void* ptr, int num_blocks, int Hkv, int bs, int D, int dtype,
+              CUtensorMap* out) {
+  for (auto& s : plan->tmaps) {
+    if (s.valid && s.ptr == ptr && s.num_blocks == num_blocks && s.Hkv == Hkv && s.bs == bs &&
+        s.D == D && s.dtype == dtype) {
+      *out = s.map;
+      return PA_OK;
+    }
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return PA_ERR_CUDA;
+  const int esz = dtype == PA_FP8_E4M3 ? 1 : 2;
+  const int swb = pa::split_box_row_bytes(D, dtype);
+  CUtensorMapDataType dt = dtype == PA_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                           : dtype == PA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                              : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(D),
+                        static_cast<cuuint64_t>(num_blocks) * Hkv * bs};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * esz};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(swb / esz),
+                       static_cast<cuuint32_t>(pa::split_box_rows(D, dtype, bs))};
+  cuuint32_t estr[2] = {1, 1};
+  CUtensorMap m;
+  CUresult r = fn(&m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return PA_ERR_CUDA;
+  TmapSlot& s = plan->tmaps[plan->tmap_next];
+  plan->tmap_next = (plan->tmap_next + 1) % 8;
+  s.valid = true;
+  s.ptr = ptr;
+  s.num_blocks = num_blocks;
+  s.Hkv = Hkv;
+  s.bs = bs;
+  s.D = D;
+  s.dtype = dtype;
+  s.map = m;
+  *out = m;
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pa_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_PLAN_MISMATCH: return "PA_ERR_PLAN_MISMATCH";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    case PA_ERR_OOM: return "PA_ERR_OOM";
+    default: return "PA_ERR_UNKNOWN";
+  }
+}
+
+int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_q_heads, int num_kv_heads,
+                  int head_dim, int max_query_len, int max_tokens, int max_partitions, int budget,
+                  int kind) {
+  if (!plan) return PA_ERR_INVALID_ARG;
+  *plan = nullptr;
+  if (device < 0 || num_seqs < 1 || num_q_heads < 1 || num_kv_heads < 1 || max_query_len < 1 ||
+      max_tokens < 1)
+    return PA_ERR_INVALID_ARG;
+  if (kind != PA_PLAN_PROPORTIONAL && kind != PA_PLAN_UNIFORM) return PA_ERR_INVALID_ARG;
+  if (num_seqs > PA_MAX_SEQS) return PA_ERR_UNSUPPORTED;
+  if (num_q_heads % num_kv_heads != 0) return PA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
+  if (max_partitions <= 0) max_partitions = PA_DEFAULT_MAX_PARTITIONS;
+  if (max_partitions > 65536 || budget > (1 << 24)) return PA_ERR_UNSUPPORTED;
+
+  DeviceGuard guard(device);
+  if (!guard.ok) return PA_ERR_CUDA;
+  if (budget <= 0) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        sms <= 0)
+      return PA_ERR_CUDA;
+    budget = 2 * sms;
+  }
+  const long long per_head = (static_cast<long long>(budget) + num_kv_heads - 1) / num_kv_heads;
+  const long long lo = per_head > num_seqs ? per_head : num_seqs;
+  const long long hi = static_cast<long long>(num_seqs) * max_partitions;
+  const long long C = hi < lo ? hi : lo;
+  long long rows_cap = C * max_query_len;
+  const long long rows_alt = static_cast<long long>(max_partitions) * max_tokens;
+  if (rows_alt < rows_cap) rows_cap = rows_alt;
+  if (rows_cap < 1) rows_cap = 1;
+
+  const size_t n = static_cast<size_t>(num_seqs);
+  const size_t b_work = align256(static_cast<size_t>(C) * sizeof(int4));
+  const size_t b_prow = align256(static_cast<size_t>(C) * sizeof(int));
+  const size_t b_red = align256(n * sizeof(int2));
+  const size_t b_snap = align256(n * sizeof(int2));
+  const size_t b_err = 256;
+  const size_t b_po = align256(static_cast<size_t>(rows_cap) * num_q_heads * head_dim * 4);
+  const size_t b_pl = align256(static_cast<size_t>(rows_cap) * num_q_heads * 4);
+  const size_t total = b_work + b_prow + b_red + b_snap + b_err + b_po + b_pl;
+
+  pa_plan* pl = new (std::nothrow) pa_plan();
+  if (!pl) return PA_ERR_OOM;
+  void* mem = nullptr;
+  if (cudaMalloc(&mem, total) != cudaSuccess) {
+    cudaGetLastError();
+    delete pl;
+    return PA_ERR_OOM;
+  }
+  char* c = static_cast<char*>(mem);
+  pl->dev.work = reinterpret_cast<int4*>(c);
+  c += b_work;
+  pl->dev.part_row = reinterpret_cast<int*>(c);
+  c += b_prow;
+  pl->dev.reduce = reinterpret_cast<int2*>(c);
+  c += b_red;
+  pl->dev.snap = reinterpret_cast<int2*>(c);
+  c += b_snap;
+  pl->dev.err = reinterpret_cast<unsigned*>(c);
+  c += b_err;
+  pl->dev.part_o = reinterpret_cast<float*>(c);
+  c += b_po;
+  pl->dev.part_lse = reinterpret_cast<float*>(c);
+  if (cudaMemset(pl->dev.err, 0, sizeof(unsigned)) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    cudaFree(mem);
+    delete pl;
+    return PA_ERR_CUDA;
+  }
+  pl->device = device;
+  pl->n = num_seqs;
+  pl->Hq = num_q_heads;
+  pl->Hkv = num_kv_heads;
+  pl->D = head_dim;
+  pl->max_qlen = max_query_len;
+  pl->max_tokens = max_tokens;
+  pl->P = max_partitions;
+  pl->W = budget;
+  pl->kind = kind;
+  pl->C = static_cast<int>(C);
+  pl->rows_cap = rows_cap;
+  pl->mem = mem;
+  pl->bytes = static_cast<long long>(total);
+  pl->refreshed = 0;
+  pl->ev_start = pl->ev_stop = nullptr;
+  pl->tmap_next = 0;
+  *plan = pl;
+  return PA_OK;
+}
+
+int pa_plan_refresh(pa_plan* plan, const int32_t* context_lens, const int32_t* cu_query_lens,
+                    void* stream) {
+  if (!plan || !context_lens) return PA_ERR_INVALID_ARG;
+  DeviceGuard guard(plan->device);
+  if (!guard.ok) return PA_ERR_CUDA;
+  pa::PlanParams p;
+  p.context_lens = context_lens;
+  p.cu = cu_query_lens;
+  p.n = plan->n;
+  p.Hkv = plan->Hkv;
+  p.P = plan->P;
+  p.C = plan->C;
+  p.kind = plan->kind;
+  p.max_qlen = plan->max_qlen;
+  p.max_tokens = plan->max_tokens;
+  p.rows_cap = plan->rows_cap;
+  p.dev = plan->dev;
+  if (pa::launch_plan(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return PA_ERR_CUDA;
+  plan->refreshed = cu_query_lens ? 2 : 1;
+  return PA_OK;
+}
+
+int pa_decode(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int num_q_heads,
+              int head_dim, const void* k_cache, const void* v_cache, int kv_dtype, float k_scale,
+              float v_scale, int num_blocks, int num_kv_heads, int block_size,
+              const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+              const int32_t* cu_query_lens, int num_seqs, float scale, void* out, void* stream) {
+  if (!plan) return PA_ERR_INVALID_ARG;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return PA_ERR_INVALID_ARG;
+  if (num_tokens < 1 || num_blocks < 1 || max_blocks_per_seq < 1) return PA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+  if (q_dtype != PA_BF16 && q_dtype != PA_FP16) return PA_ERR_UNSUPPORTED;
+  if (kv_dtype != PA_BF16 && kv_dtype != PA_FP16 && kv_dtype != PA_FP8_E4M3)
+    return PA_ERR_UNSUPPORTED;
+  if ((kv_dtype == PA_BF16 && q_dtype != PA_BF16) || (kv_dtype == PA_FP16 && q_dtype != PA_FP16))
+    return PA_ERR_UNSUPPORTED;
+  if (kv_dtype == PA_FP8_E4M3 && (!std::isfinite(k_scale) || !std::isfinite(v_scale)))
+    return PA_ERR_INVALID_ARG;
+  if (block_size != 16 && block_size != 64 && block_size != 128) return PA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
+  if (num_kv_heads < 1 || num_q_heads % num_kv_heads != 0) return PA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_blocks) * num_kv_heads * block_size >= (1ll << 31))
+    return PA_ERR_UNSUPPORTED;
+  if (num_seqs != plan->n || num_q_heads != plan->Hq || num_kv_heads != plan->Hkv ||
+      head_dim != plan->D)
+    return PA_ERR_PLAN_MISMATCH;
+  if (plan->refreshed == 0 || (cu_query_lens != nullptr) != (plan->refreshed == 2))
+    return PA_ERR_PLAN_MISMATCH;
+  if (!cu_query_lens && num_tokens != num_seqs) return PA_ERR_INVALID_ARG;
+
+  DeviceGuard guard(plan->device);
+  if (!guard.ok) return PA_ERR_CUDA;
+  CUtensorMap tk, tv;
+  int st = make_tmap(plan, k_cache, num_blocks, num_kv_heads, block_size, head_dim, kv_dtype, &tk);
+  if (st != PA_OK) return st;
+  st = make_tmap(plan, v_cache, num_blocks, num_kv_heads, block_size, head_dim, kv_dtype, &tv);
+  if (st != PA_OK) return st;
+
+  const bool fp8 = kv_dtype == PA_FP8_E4M3;
+  pa::SplitParams sp;
+  sp.plan = plan->dev;
+  sp.q = q;
+  sp.out = out;
+  sp.block_tables = block_tables;
+  sp.context_lens = context_lens;
+  sp.cu = cu_query_lens;
+  sp.num_tokens = num_tokens;
+  sp.num_blocks = num_blocks;
+  sp.Hq = num_q_heads;
+  sp.Hkv = num_kv_heads;
+  sp.G = num_q_heads / num_kv_heads;
+  sp.bs = block_size;
+  sp.max_blocks = max_blocks_per_seq;
+  sp.n = num_seqs;
+  sp.total_rows = num_blocks * num_kv_heads * block_size;
+  sp.out_f16 = q_dtype == PA_FP16 ? 1 : 0;
+  sp.scale_log2 = static_cast<float>(static_cast<double>(scale) * (fp8 ? k_scale : 1.0) *
+                                     1.4426950408889634);
+  sp.v_scale = fp8 ? v_scale : 1.0f;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int wq = pa::split_row_groups(plan->max_qlen, sp.G);
+  if (plan->ev_start && cudaEventRecord(plan->ev_start, s) != cudaSuccess) return PA_ERR_CUDA;
+  if (pa::launch_split(sp, plan->C, head_dim, kv_dtype, wq, tk, tv, s) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (plan->ev_stop && cudaEventRecord(plan->ev_stop, s) != cudaSuccess) return PA_ERR_CUDA;
+
+  pa::MergeParams mp;
+  mp.plan = plan->dev;
+  mp.out = out;
+  mp.context_lens = context_lens;
+  mp.cu = cu_query_lens;
+  mp.num_tokens = num_tokens;
+  mp.n = num_seqs;
+  mp.Hq = num_q_heads;
+  mp.D = head_dim;
+  mp.out_f16 = sp.out_f16;
+  if (pa::launch_merge(mp, s) != cudaSuccess) return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+int pa_plan_info(const pa_plan* plan, int* capacity, int* num_seqs, int* budget,
+                 int* max_partitions, int* kind, int* device, long long* device_bytes) {
+  if (!plan) return PA_ERR_INVALID_ARG;
+  if (capacity) *capacity = plan->C;
+  if (num_seqs) *num_seqs = plan->n;
+  if (budget) *budget = plan->W;
+  if (max_partitions) *max_partitions = plan->P;
+  if (kind) *kind = plan->kind;
+  if (device) *device = plan->device;
+  if (device_bytes) *device_bytes = plan->bytes;
+  return PA_OK;
+}
+
+int pa_plan_download(const pa_plan* plan, int32_t* work_info, int32_t* reduce_info, void* stream) {
+  if (!plan) return PA_ERR_INVALID_ARG;
+  DeviceGuard guard(plan->device);
+  if (!guard.ok) return PA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (work_info && cudaMemcpyAsync(work_info, plan->dev.work,
+                                   static_cast<size_t>(plan->C) * sizeof(int4),
+                                   cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (reduce_info && cudaMemcpyAsync(reduce_info, plan->dev.reduce,
+                                     static_cast<size_t>(plan->n) * sizeof(int2),
+                                     cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+int pa_plan_read_errors(pa_plan* plan, uint32_t* errors, int clear, void* stream) {
+  if (!plan || !errors) return PA_ERR_INVALID_ARG;
+  DeviceGuard guard(plan->device);
+  if (!guard.ok) return PA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(errors, plan->dev.err, sizeof(unsigned), cudaMemcpyDeviceToHost, s) !=
+      cudaSuccess)
+    return PA_ERR_CUDA;
+  if (clear && cudaMemsetAsync(plan->dev.err, 0, sizeof(unsigned), s) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+int pa_plan_set_split_events(pa_plan* plan, void* start_event, void* stop_event) {
+  if (!plan) return PA_ERR_INVALID_ARG;
+  if ((start_event == nullptr) != (stop_event == nullptr)) return PA_ERR_INVALID_ARG;
+  plan->ev_start = static_cast<cudaEvent_t>(start_event);
+  plan->ev_stop = static_cast<cudaEvent_t>(stop_event);
+  return PA_OK;
+}
+
+int pa_plan_destroy(pa_plan* plan) {
+  if (!plan) return PA_OK;
+  int st = PA_OK;
+  {
+    DeviceGuard guard(plan->device);
+    if (!guard.ok || cudaFree(plan->mem) != cudaSuccess) st = PA_ERR_CUDA;
+  }
+  delete plan;
+  return st;
+}
+
+}  // extern "C"

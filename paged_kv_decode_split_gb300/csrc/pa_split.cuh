@@ -1,0 +1,535 @@
+// pa_split.cuh -- the split-KV paged decode kernel (one CTA per plan task and
+// kv head).
+//
+// What it computes ("[MiniMax-M3] Route the paged decode to aiter's FlyDSL
+// kernel with work planner", sections 1 and 3; vllm-rdna pull 29, Change 1):
+// task (r, tile_begin, tile_end, S) of the plan covers keys
+// [tile_begin*256, min(tile_end*256, S)) of request r.  For every query row of
+// r (token i of L, q head of kv head h) the CTA forms the partial softmax over
+// the task's keys that the row may see (key < S - (L-1-i)), and writes either
+// the finished output row (when r has a single partition) or a normalised
+// fp32 partial plus its log2-sum-exp for the merge kernel.
+//
+// GB300 mapping:
+//  * warp 0 is the producer: one lane walks the block table and issues TMA
+//    tile loads (cp.async.bulk.tensor.2d, 128-byte swizzle, L2 evict-first)
+//    of the K and V rows of each page into a 3-stage shared-memory ring,
+//    completion counted in bytes on a per-stage mbarrier;
+//  * the consumer warps form a (row group) x (key split) grid: warp (wq, wk)
+//    owns query rows [8wq, 8wq+8) of the pass and a 1/WK slice of every
+//    stage's keys, and keeps its own online-softmax state;
+//  * QK^T and PV run on the tensor cores as m16n8k16 MMAs in "swap-AB" form:
+//    16 keys (QK) or 16 head dims (PV) on M, the 8 query rows on N, so a GQA
+//    group of 8 fills N exactly.  P leaves the QK accumulator through
+//    movmatrix.trans straight into the PV B fragment (no shared memory);
+//  * fp8 e4m3 caches are converted in registers (cvt.f16x2.e4m3x2, exact) and
+//    multiplied in fp16; k_scale is folded into the logit scale and v_scale
+//    into the epilogue;
+//  * the key-split warps are merged through shared memory at the end of a pass.
+#pragma once
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+template <int D, int KVT, int WQ>
+struct SplitCfg {
+  static constexpr bool kFp8 = (KVT == PA_FP8_E4M3);
+  static constexpr bool kBf16Mma = (KVT == PA_BF16);
+  static constexpr int ESZ = kFp8 ? 1 : 2;            // bytes per cached element
+  static constexpr int ROW = D * ESZ;                 // bytes per key row
+  static constexpr int SWB = ROW < 128 ? ROW : 128;   // swizzle span = box row bytes
+  static constexpr int CB = ROW / SWB;                // column blocks per key row
+  static constexpr int KS = 16384 / ROW;              // keys per stage (16 KB per tensor)
+  static constexpr int NS = 3;                        // pipeline depth
+  static constexpr int WK0 = (WQ == 1) ? 4 : 2;
+  static constexpr int WK = (KS / 16 < WK0) ? KS / 16 : WK0;  // key-split warps
+  static constexpr int KW = KS / WK;                  // keys per warp per stage
+  static constexpr int MT = KW / 16;                  // 16-key tiles per warp per stage
+  static constexpr int NCW = WQ * WK;                 // consumer warps
+  static constexpr int THREADS = 32 * (1 + NCW);
+  static constexpr int TILE_BYTES = KS * ROW;         // one tensor, one stage
+  static constexpr int BLOCK_BYTES = KS * SWB;        // one column block of a tile
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K then V
+  static constexpr int DATA_BYTES = NS * STAGE_BYTES;
+  static constexpr int DP = D + 4;                    // padded exchange row, floats
+  static constexpr int EX_BYTES = WQ * WK * 8 * (DP + 2) * 4;
+  static constexpr int SMEM_BYTES = DATA_BYTES + 1024 + 2 * NS * 8;
+  static constexpr int MIN_BLOCKS = (THREADS <= 224) ? 2 : 1;
+  static_assert(KW % 16 == 0, "a warp handles whole 16-key tiles");
+  static_assert(EX_BYTES <= DATA_BYTES, "epilogue exchange reuses the stage ring");
+  static_assert(D % 32 == 0, "head_dim is a multiple of 32");
+};
+
+// Byte offset of 16-byte chunk `chunk` of row `row` inside a column block whose
+// base is aligned to the swizzle repeat: the TMA 128B (64B) swizzle XORs the
+// chunk index with address bits [9:7] ([8:7]).
+template <int SWB>
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  const uint32_t o = static_cast<uint32_t>(row * SWB + chunk * 16);
+  constexpr uint32_t mask = (SWB == 128) ? 7u : 3u;
+  return o ^ (((o >> 7) & mask) << 4);
+}
+
+template <int D, int KVT, int WQ>
+__global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT, WQ>::MIN_BLOCKS)
+    split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                 const SplitParams p) {
+  using Cfg = SplitCfg<D, KVT, WQ>;
+  constexpr int NQ = 8 * WQ;  // query rows per pass
+
+  const int slot = blockIdx.x;
+  const int h = blockIdx.y;
+  const int4 task = p.plan.work[slot];
+  const int r = task.x;
+  if (r < 0) return;  // unused slot
+
+  // A plan refreshed from other lengths: the merge kernel zeroes these rows
+  // and reports it; this task does nothing.
+  const int S = task.w;
+  const int row0 = p.cu ? p.cu[r] : r;
+  const int L = p.cu ? p.cu[r + 1] - row0 : 1;
+  const int2 snap = p.plan.snap[r];
+  if (snap.x != p.context_lens[r] || snap.y != L) return;
+
+  const int parts = p.plan.reduce[r].y;
+  const int prow_base = p.plan.part_row[slot];
+  const int G = p.G;
+  const int rows = L * G;                 // query rows of this request
+  const int npass = (rows + NQ - 1) / NQ;
+  const int kb = task.y * kTile;          // first key of the task
+  const int ke_task = min(task.z * kTile, S);
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  float* ex = reinterpret_cast<float*>(smem_raw + (base - raw));
+  const uint32_t bar_full = base + Cfg::DATA_BYTES;
+  const uint32_t bar_empty = bar_full + 8 * Cfg::NS;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cfg::NS; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, Cfg::NCW);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  // Last key any row of pass `pass` may see.
+  auto pass_key_end = [&](int pass) {
+    const int last_row = min(rows, (pass + 1) * NQ) - 1;
+    const int last_tok = last_row / G;
+    return min(ke_task, S - (L - 1 - last_tok));
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tmk);
+      prefetch_tmap(&tmv);
+    }
+    const uint64_t policy = l2_evict_first_policy();
+    const int bs = p.bs;
+    const int box_rows = bs < Cfg::KS ? bs : Cfg::KS;
+    const uint32_t box_bytes = static_cast<uint32_t>(box_rows * Cfg::SWB);
+    const int* bt = p.block_tables + static_cast<size_t>(r) * p.max_blocks;
+    const int npages = min((S + bs - 1) / bs, p.max_blocks);
+    auto bt_at = [&](int idx) { return idx < npages ? __ldg(bt + idx) : -1; };
+    int it = 0;
+    for (int pass = 0; pass < npass; ++pass) {
+      const int ke = pass_key_end(pass);
+      const int nst = ke > kb ? (ke - kb + Cfg::KS - 1) / Cfg::KS : 0;
+      int win = kb / bs;
+      int cur = bt_at(win + lane);
+      int nxt = bt_at(win + 32 + lane);
+      for (int s = 0; s < nst; ++s, ++it) {
+        const int buf = it % Cfg::NS;
+        if (it >= Cfg::NS) mbar_wait(bar_empty + 8 * buf, ((it / Cfg::NS) & 1) ^ 1, p.plan.err);
+        const int key0 = kb + s * Cfg::KS;
+        const int nkeys = min(Cfg::KS, ke - key0);
+        const int nbox = (nkeys + box_rows - 1) / box_rows;
+        const uint32_t kdst = base + buf * Cfg::STAGE_BYTES;
+        const uint32_t vdst = kdst + Cfg::TILE_BYTES;
+        if (lane == 0)
+          mbar_arrive_expect_tx(bar_full + 8 * buf, nbox * box_bytes * Cfg::CB * 2);
+        for (int b = 0; b < nbox; ++b) {
+          const int key = key0 + b * box_rows;
+          const int pidx = key / bs;
+          while (pidx >= win + 32) {  // slide the 32-entry block-table window
+            win += 32;
+            cur = nxt;
+            nxt = bt_at(win + 32 + lane);
+          }
+          const int page = __shfl_sync(0xffffffffu, cur, pidx - win);
+          if (lane == 0) {
+            int y;
+            if (page < 0 || page >= p.num_blocks || pidx >= p.max_blocks) {
+              atomicOr(p.plan.err, PA_DEVERR_BAD_PAGE);
+              y = p.total_rows;  // outside the tensor: the copy reads zeros
+            } else {
+              y = (page * p.Hkv + h) * bs + (key % bs);
+            }
+            const uint32_t off = static_cast<uint32_t>(b * box_rows * Cfg::SWB);
+#pragma unroll
+            for (int cb = 0; cb < Cfg::CB; ++cb) {
+              const int x = cb * (Cfg::SWB / Cfg::ESZ);
+              tma_load_2d(kdst + cb * Cfg::BLOCK_BYTES + off, &tmk, x, y, bar_full + 8 * buf, policy);
+              tma_load_2d(vdst + cb * Cfg::BLOCK_BYTES + off, &tmv, x, y, bar_full + 8 * buf, policy);
+            }
+          }
+        }
+      }
+      __syncthreads();  // pairs with the consumers' end-of-pass barrier
+    }
+    // Every issued stage was waited for by the consumers; re-check so that no
+    // copy can still be landing in shared memory when the CTA exits.
+    if (lane == 0) {
+      for (int k = (it > Cfg::NS ? it - Cfg::NS : 0); k < it; ++k)
+        mbar_wait(bar_full + 8 * (k % Cfg::NS), (k / Cfg::NS) & 1, p.plan.err);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int cw = warp - 1;
+  const int wq = cw % WQ;
+  const int wk = cw / WQ;
+  const int g = lane >> 2;  // MMA groupID
+  const int t = lane & 3;   // MMA thread-in-group
+  const float sl2 = p.scale_log2;
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  const int ct = threadIdx.x - 32;  // consumer thread index
+
+  int it = 0;
+  for (int pass = 0; pass < npass; ++pass) {
+    const int pass_base = pass * NQ;
+    const int ke = pass_key_end(pass);
+    const int nst = ke > kb ? (ke - kb + Cfg::KS - 1) / Cfg::KS : 0;
+
+    // Key limit of this thread's two accumulator columns (query rows).
+    int lim[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int n = pass_base + 8 * wq + 2 * t + e;
+      lim[e] = (n < rows) ? min(ke_task, S - (L - 1 - n / G)) : kb;
+    }
+
+    // Q^T as the B operand of QK^T: row n = groupID of this warp's 8 rows.
+    uint32_t qf[D / 16][2];
+    {
+      const int n = pass_base + 8 * wq + g;
+      const int tok = n / G;
+      const bool ok = n < rows && row0 + tok < p.num_tokens;
+      const size_t qoff = ok ? (static_cast<size_t>(row0 + tok) * p.Hq + h * G + n % G) * D : 0;
+      if constexpr (!Cfg::kFp8) {
+        const uint16_t* qp = static_cast<const uint16_t*>(p.q) + qoff;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          qf[ks][0] = ok ? *reinterpret_cast<const uint32_t*>(qp + 16 * ks + 2 * t) : 0u;
+          qf[ks][1] = ok ? *reinterpret_cast<const uint32_t*>(qp + 16 * ks + 2 * t + 8) : 0u;
+        }
+      } else {
+        // fp16 operands; head-dim order permuted to match the fp8 K fragment:
+        // k-step ks uses d = cb*SWB + t*(SWB/4) + 4j + {0,1 | 2,3}.
+        constexpr int KPB = Cfg::SWB / 16;  // k-steps per column block
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const int d = (ks / KPB) * Cfg::SWB + t * (Cfg::SWB / 4) + 4 * (ks % KPB);
+          float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
+          if (ok) {
+            const uint2 raw4 = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.q) + qoff + d);
+            if (p.out_f16) {
+              const __half2 a = *reinterpret_cast<const __half2*>(&raw4.x);
+              const __half2 b = *reinterpret_cast<const __half2*>(&raw4.y);
+              v0 = __low2float(a); v1 = __high2float(a); v2 = __low2float(b); v3 = __high2float(b);
+            } else {
+              const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&raw4.x);
+              const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw4.y);
+              v0 = __low2float(a); v1 = __high2float(a); v2 = __low2float(b); v3 = __high2float(b);
+            }
+          }
+          qf[ks][0] = pack2<false>(v0, v1);
+          qf[ks][1] = pack2<false>(v2, v3);
+        }
+      }
+    }
+
+    float m[2] = {NEG_INF, NEG_INF};
+    float l[2] = {0.f, 0.f};
+    float acc[D / 16][4];
+#pragma unroll
+    for (int dt = 0; dt < D / 16; ++dt) acc[dt][0] = acc[dt][1] = acc[dt][2] = acc[dt][3] = 0.f;
+
+    const bool warp_active = pass_base + 8 * wq < rows;
+
+    for (int s = 0; s < nst; ++s, ++it) {
+      const int buf = it % Cfg::NS;
+      mbar_wait(bar_full + 8 * buf, (it / Cfg::NS) & 1, p.plan.err);
+      const uint32_t kt = base + buf * Cfg::STAGE_BYTES;
+      const uint32_t vt = kt + Cfg::TILE_BYTES;
+      const int key0 = kb + s * Cfg::KS;
+
+      if (warp_active) {
+#pragma unroll 1
+        for (int mt = 0; mt < Cfg::MT; ++mt) {
+          const int rbase = wk * Cfg::KW + mt * 16;  // row of the tile's first key
+          const int kbase = key0 + rbase;
+          if (kbase >= ke) break;
+
+          // ---- S^T[16 keys x 8 rows] = K Q^T
+          float c[4] = {0.f, 0.f, 0.f, 0.f};
+          if constexpr (!Cfg::kFp8) {
+            const int lrow = rbase + (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int lchk = (lane >> 4) & 1;
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const int cb = ks / 4;                  // 64 elements per column block
+              const int chunk = (ks % 4) * 2 + lchk;
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4(kt + cb * Cfg::BLOCK_BYTES + swz<Cfg::SWB>(lrow, chunk), a0, a1, a2, a3);
+              mma16816<Cfg::kBf16Mma>(c, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+            }
+          } else {
+            constexpr int KPB = Cfg::SWB / 16;
+            constexpr int CPT = Cfg::SWB / 64;        // 16-byte chunks per thread per row
+#pragma unroll
+            for (int cb = 0; cb < Cfg::CB; ++cb) {
+              uint32_t wg[4 * CPT], wg8[4 * CPT];
+#pragma unroll
+              for (int k = 0; k < CPT; ++k) {
+                const uint4 x = lds128(kt + cb * Cfg::BLOCK_BYTES + swz<Cfg::SWB>(rbase + g, t * CPT + k));
+                const uint4 y = lds128(kt + cb * Cfg::BLOCK_BYTES + swz<Cfg::SWB>(rbase + g + 8, t * CPT + k));
+                wg[4 * k] = x.x; wg[4 * k + 1] = x.y; wg[4 * k + 2] = x.z; wg[4 * k + 3] = x.w;
+                wg8[4 * k] = y.x; wg8[4 * k + 1] = y.y; wg8[4 * k + 2] = y.z; wg8[4 * k + 3] = y.w;
+              }
+#pragma unroll
+              for (int j = 0; j < KPB; ++j) {
+                uint32_t a0, a1, a2, a3;
+                e4m3x4_to_f16x2x2(wg[j], a0, a2);
+                e4m3x4_to_f16x2x2(wg8[j], a1, a3);
+                mma16816<false>(c, a0, a1, a2, a3, qf[cb * KPB + j][0], qf[cb * KPB + j][1]);
+              }
+            }
+          }
+
+          // ---- online softmax (log2 domain); rows g and g+8 of the tile
+          const int k_lo = kbase + g;
+          float sv[4];
+          sv[0] = (k_lo < lim[0]) ? c[0] * sl2 : NEG_INF;
+          sv[1] = (k_lo < lim[1]) ? c[1] * sl2 : NEG_INF;
+          sv[2] = (k_lo + 8 < lim[0]) ? c[2] * sl2 : NEG_INF;
+          sv[3] = (k_lo + 8 < lim[1]) ? c[3] * sl2 : NEG_INF;
+          float mx0 = fmaxf(sv[0], sv[2]);
+          float mx1 = fmaxf(sv[1], sv[3]);
+#pragma unroll
+          for (int o = 4; o <= 16; o <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+          }
+          const float mn0 = fmaxf(m[0], mx0);
+          const float mn1 = fmaxf(m[1], mx1);
+          const float ref0 = (mn0 == NEG_INF) ? 0.f : mn0;
+          const float ref1 = (mn1 == NEG_INF) ? 0.f : mn1;
+          const float al0 = fast_exp2(m[0] - ref0);
+          const float al1 = fast_exp2(m[1] - ref1);
+          m[0] = mn0;
+          m[1] = mn1;
+          const float p0 = fast_exp2(sv[0] - ref0);
+          const float p1 = fast_exp2(sv[1] - ref1);
+          const float p2 = fast_exp2(sv[2] - ref0);
+          const float p3 = fast_exp2(sv[3] - ref1);
+          l[0] = l[0] * al0 + p0 + p2;
+          l[1] = l[1] * al1 + p1 + p3;
+#pragma unroll
+          for (int dt = 0; dt < D / 16; ++dt) {
+            acc[dt][0] *= al0;
+            acc[dt][1] *= al1;
+            acc[dt][2] *= al0;
+            acc[dt][3] *= al1;
+          }
+          // P^T (keys x rows) -> B fragment of PV: transpose the two 8x8 halves.
+          const uint32_t pb0 = movmatrix_trans(pack2<Cfg::kBf16Mma>(p0, p1));
+          const uint32_t pb1 = movmatrix_trans(pack2<Cfg::kBf16Mma>(p2, p3));
+
+          // ---- O^T[D x 8] += V^T P^T.  Keys past `ke` may hold stale or
+          // uninitialised shared memory: zero them so 0 * NaN cannot occur.
+          const bool tail = kbase + 16 > ke;
+          const int kq = kbase + 2 * t;  // keys of this thread's B/A k-pairs
+          const uint32_t m01 = (kq < ke ? 0x0000ffffu : 0u) | (kq + 1 < ke ? 0xffff0000u : 0u);
+          const uint32_t m89 = (kq + 8 < ke ? 0x0000ffffu : 0u) | (kq + 9 < ke ? 0xffff0000u : 0u);
+          if constexpr (!Cfg::kFp8) {
+            const int lrow = rbase + (lane & 7) + ((lane >> 4) & 1) * 8;
+            const int lchk = (lane >> 3) & 1;
+#pragma unroll
+            for (int dt = 0; dt < D / 16; ++dt) {
+              const int cb = dt / 4;
+              const int chunk = (dt % 4) * 2 + lchk;
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4_trans(vt + cb * Cfg::BLOCK_BYTES + swz<Cfg::SWB>(lrow, chunk), a0, a1, a2, a3);
+              if (tail) {
+                a0 &= m01; a1 &= m01; a2 &= m89; a3 &= m89;
+              }
+              mma16816<Cfg::kBf16Mma>(acc[dt], a0, a1, a2, a3, pb0, pb1);
+            }
+          } else {
+            // d = 32u + 4g + e:  e = 0 / 1 -> tile 2u rows g / g+8,
+            //                    e = 2 / 3 -> tile 2u+1 rows g / g+8.
+            const int ra = rbase + 2 * t;
+            const uint32_t z0 = (kq < ke) ? 0xffffffffu : 0u, z1 = (kq + 1 < ke) ? 0xffffffffu : 0u;
+            const uint32_t z8 = (kq + 8 < ke) ? 0xffffffffu : 0u, z9 = (kq + 9 < ke) ? 0xffffffffu : 0u;
+#pragma unroll
+            for (int u = 0; u < D / 32; ++u) {
+              const int byte = 32 * u + 4 * g;
+              const int cb = byte / Cfg::SWB;
+              const int inb = byte % Cfg::SWB;
+              const uint32_t blk = vt + cb * Cfg::BLOCK_BYTES;
+              const uint32_t wsub = static_cast<uint32_t>(inb & 15);
+              uint32_t w0 = lds32(blk + swz<Cfg::SWB>(ra, inb >> 4) + wsub);
+              uint32_t w1 = lds32(blk + swz<Cfg::SWB>(ra + 1, inb >> 4) + wsub);
+              uint32_t w8 = lds32(blk + swz<Cfg::SWB>(ra + 8, inb >> 4) + wsub);
+              uint32_t w9 = lds32(blk + swz<Cfg::SWB>(ra + 9, inb >> 4) + wsub);
+              if (tail) {
+                w0 &= z0; w1 &= z1; w8 &= z8; w9 &= z9;
+              }
+              uint32_t x0, x1, y0, y1, u0, u1, v0, v1;
+              e4m3x4_to_f16x2x2(prmt(w0, w1, 0x5140u), x0, x1);  // d+0, d+1; keys 2t,2t+1
+              e4m3x4_to_f16x2x2(prmt(w0, w1, 0x7362u), y0, y1);  // d+2, d+3
+              e4m3x4_to_f16x2x2(prmt(w8, w9, 0x5140u), u0, u1);  // keys 2t+8, 2t+9
+              e4m3x4_to_f16x2x2(prmt(w8, w9, 0x7362u), v0, v1);
+              mma16816<false>(acc[2 * u], x0, x1, u0, u1, pb0, pb1);
+              mma16816<false>(acc[2 * u + 1], y0, y1, v0, v1, pb0, pb1);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty + 8 * buf);
+    }
+
+    // ------------------------------------------------------------ epilogue
+#pragma unroll
+    for (int o = 4; o <= 16; o <<= 1) {
+      l[0] += __shfl_xor_sync(0xffffffffu, l[0], o);
+      l[1] += __shfl_xor_sync(0xffffffffu, l[1], o);
+    }
+    named_barrier_sync(1, Cfg::NCW * 32);  // all stage reads of this pass done
+
+    // exchange area: O [WQ][WK][8][DP], then m and l [WQ][WK][8]
+    float* ex_o = ex;
+    float* ex_m = ex + WQ * Cfg::WK * 8 * Cfg::DP;
+    float* ex_l = ex_m + WQ * Cfg::WK * 8;
+    const int wslot = (wq * Cfg::WK + wk) * 8;
+#pragma unroll
+    for (int dt = 0; dt < D / 16; ++dt) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        int d;
+        if constexpr (!Cfg::kFp8)
+          d = 16 * dt + g + 8 * hh;
+        else
+          d = 32 * (dt / 2) + 4 * g + 2 * (dt % 2) + hh;
+        ex_o[(wslot + 2 * t) * Cfg::DP + d] = acc[dt][2 * hh];
+        ex_o[(wslot + 2 * t + 1) * Cfg::DP + d] = acc[dt][2 * hh + 1];
+      }
+    }
+    if (g == 0) {
+      ex_m[wslot + 2 * t] = m[0];
+      ex_m[wslot + 2 * t + 1] = m[1];
+      ex_l[wslot + 2 * t] = l[0];
+      ex_l[wslot + 2 * t + 1] = l[1];
+    }
+    named_barrier_sync(1, Cfg::NCW * 32);
+
+    constexpr int D4 = D / 4;
+    for (int u = ct; u < WQ * 8 * D4; u += Cfg::NCW * 32) {
+      const int gq = u / (8 * D4);
+      const int col = (u / D4) % 8;
+      const int d4 = (u % D4) * 4;
+      const int n = pass_base + 8 * gq + col;
+      if (n >= rows) continue;
+      float M = NEG_INF;
+#pragma unroll
+      for (int k = 0; k < Cfg::WK; ++k) M = fmaxf(M, ex_m[(gq * Cfg::WK + k) * 8 + col]);
+      float lsum = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+      if (M != NEG_INF) {
+#pragma unroll
+        for (int k = 0; k < Cfg::WK; ++k) {
+          const int ws = (gq * Cfg::WK + k) * 8 + col;
+          const float w = fast_exp2(ex_m[ws] - M);
+          const float4 v = *reinterpret_cast<const float4*>(ex_o + ws * Cfg::DP + d4);
+          lsum += w * ex_l[ws];
+          o0 += w * v.x; o1 += w * v.y; o2 += w * v.z; o3 += w * v.w;
+        }
+      }
+      const float inv = lsum > 0.f ? p.v_scale / lsum : 0.f;
+      o0 *= inv; o1 *= inv; o2 *= inv; o3 *= inv;
+      const int tok = n / G;
+      const int hq = h * G + n % G;
+      if (parts == 1) {
+        const int trow = row0 + tok;
+        if (trow >= p.num_tokens) {
+          atomicOr(p.plan.err, PA_DEVERR_PLAN_OVERFLOW);
+          continue;
+        }
+        uint2 pk;
+        if (p.out_f16) {
+          pk.x = pack2<false>(o0, o1);
+          pk.y = pack2<false>(o2, o3);
+        } else {
+          pk.x = pack2<true>(o0, o1);
+          pk.y = pack2<true>(o2, o3);
+        }
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) +
+                                  (static_cast<size_t>(trow) * p.Hq + hq) * D + d4) = pk;
+      } else {
+        const size_t prow = static_cast<size_t>(prow_base + tok) * p.Hq + hq;
+        *reinterpret_cast<float4*>(p.plan.part_o + prow * D + d4) = make_float4(o0, o1, o2, o3);
+        if (d4 == 0) p.plan.part_lse[prow] = lsum > 0.f ? M + __log2f(lsum) : NEG_INF;
+      }
+    }
+    fence_proxy_async_smem();  // exchange writes precede the next pass's TMA writes
+    __syncthreads();           // pairs with the producer's end-of-pass barrier
+  }
+}
+
+template <int D, int KVT, int WQ>
+cudaError_t launch_split_cfg(const SplitParams& p, int C, const CUtensorMap& tk,
+                             const CUtensorMap& tv, cudaStream_t s) {
+  using Cfg = SplitCfg<D, KVT, WQ>;
+  auto kern = split_kernel<D, KVT, WQ>;
+  static bool attr_done = false;  // benign race: the attribute call is idempotent
+  if (!attr_done) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  dim3 grid(C, p.Hkv);
+  kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_split_d(const SplitParams& p, int C, int kv_dtype, int wq,
+                           const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s) {
+#define PA_SPLIT_CASE(KVT)                                                     \
+  switch (wq) {                                                                \
+    case 1: return launch_split_cfg<D, KVT, 1>(p, C, tk, tv, s);               \
+    case 2: return launch_split_cfg<D, KVT, 2>(p, C, tk, tv, s);               \
+    case 3: return launch_split_cfg<D, KVT, 3>(p, C, tk, tv, s);               \
+    default: return launch_split_cfg<D, KVT, 4>(p, C, tk, tv, s);              \
+  }
+  switch (kv_dtype) {
+    case PA_BF16: PA_SPLIT_CASE(PA_BF16)
+    case PA_FP16: PA_SPLIT_CASE(PA_FP16)
+    default: PA_SPLIT_CASE(PA_FP8_E4M3)
+  }
+#undef PA_SPLIT_CASE
+}
+
+}  // namespace pa

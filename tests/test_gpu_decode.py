@@ -1,0 +1,309 @@
+"""The CUDA decode path (planner + split-KV kernel + merge, through the C ABI)
+against the fp64 oracle, element by element.
+
+Tolerances (max |gpu - oracle| over every output element, outputs rounded to
+bf16/fp16): 1e-2 with 16-bit caches, 3e-2 with fp8-e4m3 caches, the oracle
+decoding the same fp8 bytes."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import oracle_decode
+from paged_kv_decode_split_gb300 import binding, workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 1e-2, "fp16": 1e-2, "fp8": 3e-2}
+
+
+@pytest.fixture(scope="module")
+def dev():
+    assert torch.cuda.is_available(), "the GPU tests need a CUDA device"
+    import __graft_entry__
+    __graft_entry__.build()
+    return torch.device("cuda", 0)
+
+
+def run(w, kind=binding.PROPORTIONAL, budget=None, max_partitions=None, out=None):
+    plan = binding.plan_for(w, kind, budget, max_partitions)
+    plan.refresh(w.context_lens, w.cu_query_lens)
+    o = binding.decode_workload(plan, w, out=out)
+    torch.cuda.synchronize()
+    return o, plan
+
+
+def max_diff(out: torch.Tensor, ref: np.ndarray) -> float:
+    got = out.float().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    return float(np.abs(got - ref).max()) if ref.size else 0.0
+
+
+def check(w, **kw):
+    out, plan = run(w, **kw)
+    ref = oracle_decode(w.to("cpu"))
+    d = max_diff(out, ref)
+    assert d <= TOL[w.kv_dtype], f"{w.name}: max|diff| {d}"
+    assert plan.read_errors() == 0
+    return out, ref, d
+
+
+def batch(dev, lens, ql=None, H=(8, 2), D=128, bs=16, kv="bf16", q="bf16", pad=0, seed=0, **kw):
+    return wl.make_batch("case", lens, ql, H[0], H[1], D, bs, kv, q, seed=seed, pad_tokens=pad,
+                         kv_scale=0.05, device=dev, **kw)
+
+
+# ---------------------------------------------------------------- small sweeps
+
+def test_tiny(dev):
+    for kind in (binding.PROPORTIONAL, binding.UNIFORM):
+        check(wl.tiny(0, dev), kind=kind)
+
+
+RAGGED = [1, 15, 17, 255, 256, 257, 700, 1500]
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("kv,q", [("bf16", "bf16"), ("fp16", "fp16"), ("fp8", "bf16"),
+                                  ("fp8", "fp16")])
+@pytest.mark.parametrize("bs", [16, 64, 128])
+def test_dtype_shape_sweep(dev, D, kv, q, bs):
+    check(batch(dev, RAGGED, H=(8, 2), D=D, bs=bs, kv=kv, q=q, seed=D + bs))
+
+
+@pytest.mark.parametrize("H", [(4, 4), (6, 1), (12, 2), (16, 2), (32, 4), (64, 8)])
+def test_gqa_group_sizes(dev, H):
+    check(batch(dev, [33, 600, 1200], H=H, D=128, kv="bf16", seed=H[0]))
+
+
+@pytest.mark.parametrize("P,W", [(1, 8), (2, 16), (4, 64), (16, 512), (256, 4096), (256, 296)])
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_split_count_sweep(dev, P, W, kv):
+    """The error must not grow with the number of partitions (the partials stay
+    fp32 and are merged by their log-sum-exp)."""
+    w = batch(dev, [9000, 40, 2600], H=(8, 1), D=128, kv=kv, seed=5, budget=W, max_partitions=P)
+    _, _, d = check(w)
+    assert d <= TOL[kv]
+
+
+# ---------------------------------------------------- multi-token rows (cu)
+
+def test_verify_rows_and_padding(dev):
+    w = batch(dev, [600, 40, 3000, 2], ql=[3, 3, 3, 3], H=(6, 1), D=256, bs=64, pad=5, seed=1)
+    out, _, _ = check(w)
+    assert torch.all(out[12:] == 0)
+
+
+def test_mixed_decode_and_prompt(dev):
+    w = batch(dev, [700, 100, 0, 900, 5], ql=[1, 100, 2, 1, 0], H=(12, 2), D=256, bs=64, pad=3,
+              seed=2)
+    out, _, _ = check(w)
+    cu = w.cu_query_lens.tolist()
+    assert torch.all(out[cu[2]:cu[3]] == 0)       # zero-length request
+    assert torch.all(out[cu[-1]:] == 0)          # graph padding rows
+
+
+def test_rows_with_no_visible_key_are_zero(dev):
+    w = batch(dev, [2, 300], ql=[5, 2], H=(8, 2), D=64, pad=1, seed=3)
+    out, _, _ = check(w)
+    assert torch.all(out[0:3] == 0)  # tokens 0..2 of request 0 see S-(L-1-i) <= 0 keys
+
+
+@pytest.mark.parametrize("ql", [2, 4, 8])
+def test_verify_row_groups(dev, ql):
+    check(batch(dev, [5000, 900, 64], ql=[ql] * 3, H=(8, 1), D=128, kv="fp8", seed=ql))
+
+
+def test_cu_arange_matches_no_cu(dev):
+    w = batch(dev, RAGGED, H=(8, 2), D=128, seed=9)
+    a, _ = run(w)
+    w2 = wl.Workload(**{**w.__dict__, "cu_query_lens": torch.arange(
+        len(RAGGED) + 1, dtype=torch.int32, device=dev)})
+    b, _ = run(w2)
+    assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------ robustness
+
+def _poison(w):
+    """NaN in every cache slot that no request may read: the tail of each
+    request's last page and every unused page."""
+    nan = 0x7F if w.kv_dtype == "fp8" else float("nan")
+    used = torch.zeros(w.k_cache.shape[0], dtype=torch.bool)
+    bs = w.block_size
+    for r, S in enumerate(w.context_lens.tolist()):
+        np_ = -(-S // bs)
+        pages = w.block_tables[r, :np_].long().cpu()
+        used[pages] = True
+        if S % bs:
+            last = int(pages[-1])
+            w.k_cache[last, :, S % bs:] = nan
+            w.v_cache[last, :, S % bs:] = nan
+    idx = (~used).nonzero().flatten().to(w.k_cache.device)
+    w.k_cache[idx] = nan
+    w.v_cache[idx] = nan
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_nan_poisoned_unread_slots(dev, kv):
+    w = batch(dev, [17, 300, 1000, 5], H=(8, 2), D=128, kv=kv, seed=4, pool_pages=200)
+    _poison(w)
+    check(w)
+
+
+def test_deterministic(dev):
+    w = wl.tiny(0, dev)
+    a, _ = run(w)
+    b, _ = run(w)
+    assert torch.equal(a, b)
+
+
+def test_stale_plan_is_reported_and_zeroed(dev):
+    w = batch(dev, [3000, 800, 1200], H=(8, 2), D=128, seed=6)
+    plan = binding.plan_for(w)
+    plan.refresh(w.context_lens)
+    w.context_lens[1] += 1  # a draft step bumps a length without re-planning
+    out = binding.decode_workload(plan, w)
+    torch.cuda.synchronize()
+    assert plan.read_errors() & binding.DEVERR_STALE_PLAN
+    assert torch.all(out[1] == 0)
+    ref = oracle_decode(w.to("cpu"))
+    assert max_diff(out[[0, 2]], ref[[0, 2]]) <= TOL["bf16"]
+
+
+def test_bad_page_is_reported_not_faulted(dev):
+    w = batch(dev, [3000, 800], H=(8, 2), D=128, seed=7)
+    w.block_tables[0, 3] = w.k_cache.shape[0] + 5
+    out, plan = run(w)
+    assert plan.read_errors() & binding.DEVERR_BAD_PAGE
+    ref = oracle_decode(wl.subset(w, [1]))
+    assert max_diff(out[[1]], ref) <= TOL["bf16"]
+
+
+def test_overflowing_query_rows_empty_the_plan(dev):
+    w = batch(dev, [500, 500], ql=[2, 2], H=(8, 2), D=64, seed=8)
+    plan = binding.Plan(2, 8, 2, 64, max_query_len=1, max_tokens=4, device=dev)
+    plan.refresh(w.context_lens, w.cu_query_lens)
+    out = binding.decode_workload(plan, w)
+    torch.cuda.synchronize()
+    assert plan.read_errors() & binding.DEVERR_PLAN_OVERFLOW
+    assert torch.all(out == 0)
+
+
+def test_validation_errors(dev):
+    w = wl.tiny(0, dev)
+    plan = binding.plan_for(w)
+    with pytest.raises(binding.PaError) as e:  # decode before any refresh
+        binding.decode_workload(plan, w)
+    assert e.value.status == binding.PA_ERR_PLAN_MISMATCH
+    plan.refresh(w.context_lens)
+    with pytest.raises(binding.PaError) as e:  # refreshed without cu, called with cu
+        plan.decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
+                    torch.arange(5, dtype=torch.int32, device=dev))
+    assert e.value.status == binding.PA_ERR_PLAN_MISMATCH
+    with pytest.raises(binding.PaError) as e:  # fp16 q with a bf16 cache
+        plan.decode(w.q.half(), w.k_cache, w.v_cache, w.block_tables, w.context_lens)
+    assert e.value.status == binding.PA_ERR_UNSUPPORTED
+    k32 = w.k_cache.view(64, 2, 32, 64)
+    with pytest.raises(binding.PaError) as e:  # block size 32 is outside the domain
+        plan.decode(w.q, k32, k32, w.block_tables, w.context_lens)
+    assert e.value.status == binding.PA_ERR_UNSUPPORTED
+    other = binding.Plan(5, 8, 2, 64, device=dev)
+    other.refresh(torch.ones(5, dtype=torch.int32, device=dev))
+    with pytest.raises(binding.PaError) as e:  # plan built for another batch size
+        binding.decode_workload(other, w)
+    assert e.value.status == binding.PA_ERR_PLAN_MISMATCH
+    lib = binding.load()
+    import ctypes
+    st = lib.pa_decode(plan._h, ctypes.c_void_p(w.q.data_ptr() + 2), 0, 4, 8, 64,
+                       ctypes.c_void_p(w.k_cache.data_ptr()), ctypes.c_void_p(w.v_cache.data_ptr()),
+                       0, 1.0, 1.0, 128, 2, 16, ctypes.c_void_p(w.block_tables.data_ptr()),
+                       w.block_tables.shape[1], ctypes.c_void_p(w.context_lens.data_ptr()), None,
+                       4, 0.125, ctypes.c_void_p(w.q.data_ptr()), None)
+    assert st == binding.PA_ERR_INVALID_ARG  # misaligned q
+
+
+def test_graph_capture_refresh_and_decode(dev):
+    """refresh + decode captured once, replayed after the lengths change in place."""
+    w = batch(dev, [3000, 800, 64, 2000], H=(8, 2), D=128, seed=10, spare_blocks=40)
+    plan = binding.plan_for(w)
+    out = torch.empty_like(w.q)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        plan.refresh(w.context_lens, stream=s)
+        binding.decode_workload(plan, w, out=out, stream=s)  # warm-up outside the graph
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        plan.refresh(w.context_lens)
+        binding.decode_workload(plan, w, out=out)
+    # extend the batch inside the allocated pages and replay
+    g2 = torch.Generator().manual_seed(0)
+    for step in range(3):
+        grow = torch.tensor([100, 257, 1, 300], dtype=torch.int32)
+        new = w.context_lens.cpu() + grow
+        bs = w.block_size
+        for r in range(w.num_seqs):  # give the grown requests pages
+            need = -(-int(new[r]) // bs)
+            have = int((w.block_tables[r] >= 0).sum())
+            if need > have:
+                free = torch.randperm(w.k_cache.shape[0], generator=g2)[: need - have]
+                w.block_tables[r, have:need] = free.to(torch.int32).to(dev)
+        w.context_lens.copy_(new.to(dev))
+        g.replay()
+        torch.cuda.synchronize()
+        ref = oracle_decode(w.to("cpu"))
+        assert max_diff(out, ref) <= TOL["bf16"]
+    assert plan.read_errors() == 0
+
+
+# ------------------------------------------------ full-size configurations
+
+def _sampled(w, out, requests):
+    sub = wl.subset(w, requests)
+    ref = oracle_decode(sub)
+    if w.cu_query_lens is None:
+        rows = torch.tensor(requests)
+    else:
+        cu = w.cu_query_lens.cpu()
+        rows = torch.cat([torch.arange(int(cu[r]), int(cu[r + 1])) for r in requests])
+    return max_diff(out[rows.to(out.device)], ref)
+
+
+def _pick(w, k=4):
+    lens = w.context_lens.cpu()
+    order = torch.argsort(lens)
+    picks = {int(order[-1]), int(order[0]), int(order[len(order) // 2])}
+    g = torch.Generator().manual_seed(1)
+    while len(picks) < min(k, w.num_seqs):
+        picks.add(int(torch.randint(w.num_seqs, (1,), generator=g)))
+    return sorted(picks)
+
+
+FULL = ["uniform", "skewed", "mtp_verify", "mixed_prompt", "large_bf16", "large_fp8"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(dev, name):
+    w = wl.CONFIGS[name](0, dev)
+    for kind in (binding.PROPORTIONAL, binding.UNIFORM):
+        out, plan = run(w, kind=kind)
+        assert plan.read_errors() == 0
+        d = _sampled(w, out, _pick(w))
+        assert d <= TOL[w.kv_dtype], (name, kind, d)
+        if w.cu_query_lens is not None:
+            assert torch.all(out[int(w.cu_query_lens[-1]):] == 0)
+    del w
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("seed", [1, 2])
+def test_skewed_seeds_sampled(dev, seed):
+    w = wl.skewed(seed, dev)
+    out, plan = run(w)
+    assert _sampled(w, out, _pick(w)) <= TOL["fp8"]
