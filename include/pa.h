@@ -162,6 +162,42 @@ int pa_decode(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int num
               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
               const int32_t* cu_query_lens, int num_seqs, float scale, void* out, void* stream);
 
+/* Size of the file-scope device array that pa_decode_static works in. */
+#define PA_STATIC_SCRATCH_BYTES (32u << 20)
+
+/* pa_decode_static: the work of pa_plan_refresh followed by pa_decode in one
+ * call that allocates no device memory.  The source pages have no counterpart:
+ * it exists for callers that cannot call cudaMalloc while decoding -- a serving
+ * engine that hands nearly all HBM to its own KV-cache pool and caching
+ * allocator, or code running inside a CUDA-graph capture -- and so cannot
+ * create a pa_plan.
+ *
+ * Arguments mean what they mean for pa_plan_build and pa_decode; the plan
+ * parameters (max_query_len, max_partitions, budget, kind) are passed per call
+ * and the plan is rebuilt from context_lens / cu_query_lens every call, on
+ * `stream`.  The plan arrays and fp32 partial results live in one static device
+ * array of PA_STATIC_SCRATCH_BYTES (32 MiB) that every GPU loading this code
+ * keeps until the process exits.  A batch whose plan and partial results need
+ * more than that is rejected with PA_ERR_UNSUPPORTED; the need is the
+ * pa_plan_build footprint: C x 20 + n x 16 bytes of plan plus
+ * min(C x max_query_len, max_partitions x num_tokens) x Hq x (D + 1) x 4 bytes
+ * of partials, with capacity C = min(n x P, max(n, ceil(W / Hkv))).
+ * device_errors: optional device pointer to a uint32 that receives the
+ * PA_DEVERR_* bits (the caller clears it); NULL uses a word inside the static
+ * array, cleared at the start of every call and not readable by the caller.
+ * The first call on a device looks up the array's device address there (with
+ * that device current), so make it before any stream capture.  Every call
+ * shares the array and it keeps the last call's contents: calls whose GPU work
+ * can overlap (several streams, threads or concurrently replayed graphs) race
+ * and must be serialised by the caller.  Never calls cudaMalloc or cudaFree. */
+int pa_decode_static(const void* q, int q_dtype, int num_tokens, int num_q_heads, int head_dim,
+                     const void* k_cache, const void* v_cache, int kv_dtype, float k_scale,
+                     float v_scale, int num_blocks, int num_kv_heads, int block_size,
+                     const int32_t* block_tables, int max_blocks_per_seq,
+                     const int32_t* context_lens, const int32_t* cu_query_lens, int num_seqs,
+                     int max_query_len, int max_partitions, int budget, int kind, float scale,
+                     void* out, uint32_t* device_errors, void* stream);
+
 /* Host-side facts about a plan (any pointer may be NULL): its capacity C, the
  * batch size, the budget W and ceiling P actually used, the plan kind, the
  * device, and the bytes of device memory it owns. */

@@ -1,0 +1,243 @@
+// pa_static.cu -- pa_decode_static: plan + split-KV decode + merge in one call
+// that allocates no device memory.
+//
+// Who needs it: callers that cannot call cudaMalloc at decode time.  A serving
+// engine typically hands (almost) all HBM to its own KV-cache pool and caching
+// allocator at start-up, so a library allocation either fails or fragments that
+// pool; code running while a CUDA graph is being captured may not allocate
+// either (cudaMalloc is not a stream operation and would not be replayed).  Such
+// callers cannot create a pa_plan, whose device buffers come from pa_plan_build.
+//
+// Instead, the plan arrays and the fp32 partial results live in one file-scope
+// __device__ array of PA_STATIC_SCRATCH_BYTES.  Every GPU on which this module is
+// loaded holds that memory until the process exits.  In host code the array's
+// name is only a host-side stand-in, never a device address: the address is
+// obtained once per device with cudaGetSymbolAddress, with that device current,
+// on the first call made on that device (so that first call should happen
+// before any stream capture), and then passed to the kernels as a pointer.
+//
+// All calls share the one array and it keeps the last call's contents.  Each
+// call rewrites the whole plan before using it and clears the error word it
+// uses, so nothing stale is read; but calls whose work overlaps on the GPU
+// (other streams, other threads, or a captured graph replaying concurrently)
+// race on the array and must be serialised by the caller.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/pa.h"
+#include "pa_internal.h"
+
+namespace {
+
+__device__ __align__(256) unsigned char g_pa_static_scratch[PA_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on `device` (which must be current).
+void* scratch_address(int device) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_addr[device]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_pa_static_scratch) != cudaSuccess || !p) return nullptr;
+    g_addr[device] = p;
+  }
+  return g_addr[device];
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn static_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// The same TMA view of a cache as pa_decode uses (rows x D, 128/64-byte
+// swizzled boxes), encoded on the host for this call.
+bool encode_cache(const void* ptr, int num_blocks, int Hkv, int bs, int D, int dtype,
+                  CUtensorMap* m) {
+  EncodeTiledFn fn = static_encode_fn();
+  if (!fn) return false;
+  const int esz = dtype == PA_FP8_E4M3 ? 1 : 2;
+  const int swb = pa::split_box_row_bytes(D, dtype);
+  CUtensorMapDataType dt = dtype == PA_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                           : dtype == PA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                              : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(num_blocks) * Hkv * bs};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * esz};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(swb / esz),
+                       static_cast<cuuint32_t>(pa::split_box_rows(D, dtype, bs))};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int num_q_heads,
+                                int head_dim, const void* k_cache, const void* v_cache,
+                                int kv_dtype, float k_scale, float v_scale, int num_blocks,
+                                int num_kv_heads, int block_size, const int32_t* block_tables,
+                                int max_blocks_per_seq, const int32_t* context_lens,
+                                const int32_t* cu_query_lens, int num_seqs, int max_query_len,
+                                int max_partitions, int budget, int kind, float scale, void* out,
+                                uint32_t* device_errors, void* stream) {
+  // ---- arguments (the same domain as pa_plan_build + pa_decode)
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return PA_ERR_INVALID_ARG;
+  if (num_seqs < 1 || num_tokens < 1 || num_blocks < 1 || max_blocks_per_seq < 1 ||
+      max_query_len < 1 || num_q_heads < 1 || num_kv_heads < 1)
+    return PA_ERR_INVALID_ARG;
+  if (kind != PA_PLAN_PROPORTIONAL && kind != PA_PLAN_UNIFORM) return PA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out) |
+       reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15u)
+    return PA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+  if (q_dtype != PA_BF16 && q_dtype != PA_FP16) return PA_ERR_UNSUPPORTED;
+  if (kv_dtype != PA_BF16 && kv_dtype != PA_FP16 && kv_dtype != PA_FP8_E4M3)
+    return PA_ERR_UNSUPPORTED;
+  if ((kv_dtype == PA_BF16 && q_dtype != PA_BF16) || (kv_dtype == PA_FP16 && q_dtype != PA_FP16))
+    return PA_ERR_UNSUPPORTED;
+  if (kv_dtype == PA_FP8_E4M3 && (!std::isfinite(k_scale) || !std::isfinite(v_scale)))
+    return PA_ERR_INVALID_ARG;
+  if (num_seqs > PA_MAX_SEQS || num_q_heads % num_kv_heads != 0) return PA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
+  if (block_size != 16 && block_size != 64 && block_size != 128) return PA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_blocks) * num_kv_heads * block_size >= (1ll << 31))
+    return PA_ERR_UNSUPPORTED;
+  if (!cu_query_lens && num_tokens != num_seqs) return PA_ERR_INVALID_ARG;
+  if (max_partitions <= 0) max_partitions = PA_DEFAULT_MAX_PARTITIONS;
+  if (max_partitions > 65536 || budget > (1 << 24)) return PA_ERR_UNSUPPORTED;
+
+  int device = -1;
+  if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices)
+    return PA_ERR_CUDA;
+  if (budget <= 0) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        sms <= 0)
+      return PA_ERR_CUDA;
+    budget = 2 * sms;
+  }
+
+  // ---- carve the static array: plan arrays, error word, partial results
+  const long long per_head = (static_cast<long long>(budget) + num_kv_heads - 1) / num_kv_heads;
+  const long long lo = per_head > num_seqs ? per_head : num_seqs;
+  const long long hi = static_cast<long long>(num_seqs) * max_partitions;
+  const long long C = hi < lo ? hi : lo;
+  long long rows_cap = C * max_query_len;
+  const long long rows_alt = static_cast<long long>(max_partitions) * num_tokens;
+  if (rows_alt < rows_cap) rows_cap = rows_alt;
+  const size_t n = static_cast<size_t>(num_seqs);
+  const size_t b_work = up256(static_cast<size_t>(C) * sizeof(int4));
+  const size_t b_prow = up256(static_cast<size_t>(C) * sizeof(int));
+  const size_t b_red = up256(n * sizeof(int2));
+  const size_t b_snap = up256(n * sizeof(int2));
+  const size_t b_err = 256;
+  const size_t b_po = up256(static_cast<size_t>(rows_cap) * num_q_heads * head_dim * 4);
+  const size_t b_pl = up256(static_cast<size_t>(rows_cap) * num_q_heads * 4);
+  if (b_work + b_prow + b_red + b_snap + b_err + b_po + b_pl > PA_STATIC_SCRATCH_BYTES)
+    return PA_ERR_UNSUPPORTED;  // this batch needs more scratch than the static array holds
+
+  char* base = static_cast<char*>(scratch_address(device));
+  if (!base) return PA_ERR_CUDA;
+  pa::PlanDev dev;
+  char* c = base;
+  dev.work = reinterpret_cast<int4*>(c);
+  c += b_work;
+  dev.part_row = reinterpret_cast<int*>(c);
+  c += b_prow;
+  dev.reduce = reinterpret_cast<int2*>(c);
+  c += b_red;
+  dev.snap = reinterpret_cast<int2*>(c);
+  c += b_snap;
+  unsigned* own_err = reinterpret_cast<unsigned*>(c);
+  c += b_err;
+  dev.part_o = reinterpret_cast<float*>(c);
+  c += b_po;
+  dev.part_lse = reinterpret_cast<float*>(c);
+  dev.err = device_errors ? reinterpret_cast<unsigned*>(device_errors) : own_err;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!device_errors && cudaMemsetAsync(own_err, 0, sizeof(unsigned), s) != cudaSuccess)
+    return PA_ERR_CUDA;
+
+  CUtensorMap tk, tv;
+  if (!encode_cache(k_cache, num_blocks, num_kv_heads, block_size, head_dim, kv_dtype, &tk) ||
+      !encode_cache(v_cache, num_blocks, num_kv_heads, block_size, head_dim, kv_dtype, &tv))
+    return PA_ERR_CUDA;
+
+  // ---- plan, split, merge
+  pa::PlanParams pp;
+  pp.context_lens = context_lens;
+  pp.cu = cu_query_lens;
+  pp.n = num_seqs;
+  pp.Hkv = num_kv_heads;
+  pp.P = max_partitions;
+  pp.C = static_cast<int>(C);
+  pp.kind = kind;
+  pp.max_qlen = max_query_len;
+  pp.max_tokens = num_tokens;
+  pp.rows_cap = rows_cap;
+  pp.dev = dev;
+  if (pa::launch_plan(pp, s) != cudaSuccess) return PA_ERR_CUDA;
+
+  const bool fp8 = kv_dtype == PA_FP8_E4M3;
+  pa::SplitParams sp;
+  sp.plan = dev;
+  sp.q = q;
+  sp.out = out;
+  sp.block_tables = block_tables;
+  sp.context_lens = context_lens;
+  sp.cu = cu_query_lens;
+  sp.num_tokens = num_tokens;
+  sp.num_blocks = num_blocks;
+  sp.Hq = num_q_heads;
+  sp.Hkv = num_kv_heads;
+  sp.G = num_q_heads / num_kv_heads;
+  sp.bs = block_size;
+  sp.max_blocks = max_blocks_per_seq;
+  sp.n = num_seqs;
+  sp.total_rows = num_blocks * num_kv_heads * block_size;
+  sp.out_f16 = q_dtype == PA_FP16 ? 1 : 0;
+  sp.scale_log2 = static_cast<float>(static_cast<double>(scale) * (fp8 ? k_scale : 1.0) *
+                                     1.4426950408889634);
+  sp.v_scale = fp8 ? v_scale : 1.0f;
+  const int wq = pa::split_row_groups(max_query_len, sp.G);
+  if (pa::launch_split(sp, static_cast<int>(C), head_dim, kv_dtype, wq, tk, tv, s) != cudaSuccess)
+    return PA_ERR_CUDA;
+
+  pa::MergeParams mp;
+  mp.plan = dev;
+  mp.out = out;
+  mp.context_lens = context_lens;
+  mp.cu = cu_query_lens;
+  mp.num_tokens = num_tokens;
+  mp.n = num_seqs;
+  mp.Hq = num_q_heads;
+  mp.D = head_dim;
+  mp.out_f16 = sp.out_f16;
+  if (pa::launch_merge(mp, s) != cudaSuccess) return PA_ERR_CUDA;
+  return PA_OK;
+}
