@@ -83,7 +83,7 @@ int split_box_row_bytes(int D, int kv_dtype) {
 }
 
 int split_box_rows(int D, int kv_dtype, int bs) {
-  const int ks = 16384 / (D * (kv_dtype == PA_FP8_E4M3 ? 1 : 2));  // keys per stage
+  const int ks = kStageTensorBytes / (D * (kv_dtype == PA_FP8_E4M3 ? 1 : 2));  // keys per stage
   return bs < ks ? bs : ks;
 }
 

@@ -10,6 +10,7 @@ namespace pa {
 
 constexpr int kTile = 256;       // partition tile, tokens
 constexpr int kMaxSeqs = 4096;   // planner domain
+constexpr int kStageTensorBytes = 16384;  // split kernel: K (or V) bytes per pipeline stage
 
 // Device buffers owned by one plan.
 struct PlanDev {

@@ -11,21 +11,32 @@
 // fp32 partial plus its log2-sum-exp for the merge kernel.
 //
 // GB300 mapping:
-//  * warp 0 is the producer: one lane walks the block table and issues TMA
-//    tile loads (cp.async.bulk.tensor.2d, 128-byte swizzle, L2 evict-first)
-//    of the K and V rows of each page into a 3-stage shared-memory ring,
-//    completion counted in bytes on a per-stage mbarrier;
-//  * the consumer warps form a (row group) x (key split) grid: warp (wq, wk)
-//    owns query rows [8wq, 8wq+8) of the pass and a 1/WK slice of every
-//    stage's keys, and keeps its own online-softmax state;
-//  * QK^T and PV run on the tensor cores as m16n8k16 MMAs in "swap-AB" form:
-//    16 keys (QK) or 16 head dims (PV) on M, the 8 query rows on N, so a GQA
-//    group of 8 fills N exactly.  P leaves the QK accumulator through
-//    movmatrix.trans straight into the PV B fragment (no shared memory);
+//  * warp 0 is the producer: it walks the block table (32-entry windows,
+//    coalesced) and issues the TMA tile loads (cp.async.bulk.tensor.2d,
+//    128-byte swizzle, L2 evict-first) of the K and V rows of a stage's pages
+//    from up to 32 lanes at once -- with pages of only 2-4 KB per head, one
+//    issuing lane caps the stream at roughly half the HBM bandwidth -- into a
+//    ring of NS 32 KB stages, completion counted in bytes on an mbarrier;
+//  * consumer warps form (row group wq) x (key warp wk); every consumer warp
+//    takes part in every stage (its key slice: T 16-key tiles handled
+//    together -- independent MMA chains, one softmax reduction), so each warp
+//    waits on the ring slots strictly in order;
+//  * every mbarrier wait is bounded: a wait that gives up raises
+//    PA_DEVERR_TIMEOUT and aborts the CTA's pipeline (no further copies are
+//    issued or consumed); the producer then drains the copies it issued before
+//    the CTA exits;
+//  * QK^T and PV are m16n8k16 tensor-core MMAs in "swap-AB" form: 16 keys
+//    (QK) or 16 head dims (PV) on M, the 8 query rows of the group on N, so a
+//    GQA group of 8 fills N exactly.  P moves from the QK accumulator to the
+//    PV B fragment with movmatrix.trans, never through shared memory;
+//  * the online softmax runs in the log2 domain and rescales lazily: the
+//    running reference only moves when the tile maximum exceeds it by more
+//    than 8 (probabilities stay below 2^8, exact in fp32 accumulators);
 //  * fp8 e4m3 caches are converted in registers (cvt.f16x2.e4m3x2, exact) and
 //    multiplied in fp16; k_scale is folded into the logit scale and v_scale
 //    into the epilogue;
-//  * the key-split warps are merged through shared memory at the end of a pass.
+//  * the key warps of a row group are merged through shared memory at the end
+//    of a pass.
 #pragma once
 
 #include "pa_device.cuh"
@@ -41,12 +52,15 @@ struct SplitCfg {
   static constexpr int ROW = D * ESZ;                 // bytes per key row
   static constexpr int SWB = ROW < 128 ? ROW : 128;   // swizzle span = box row bytes
   static constexpr int CB = ROW / SWB;                // column blocks per key row
-  static constexpr int KS = 16384 / ROW;              // keys per stage (16 KB per tensor)
-  static constexpr int NS = 3;                        // pipeline depth
-  static constexpr int WK0 = (WQ == 1) ? 4 : 2;
-  static constexpr int WK = (KS / 16 < WK0) ? KS / 16 : WK0;  // key-split warps
-  static constexpr int KW = KS / WK;                  // keys per warp per stage
-  static constexpr int MT = KW / 16;                  // 16-key tiles per warp per stage
+  static constexpr int KS = kStageTensorBytes / ROW;  // keys per stage
+  static constexpr int NS = 3;                        // ring depth
+  static constexpr int MTS = KS / 16;                 // 16-key tiles per stage
+  static constexpr int WK0 = (WQ == 1) ? 4 : (WQ == 4 ? 1 : 2);
+  static constexpr int WK = WK0 < MTS ? WK0 : MTS;   // key warps per row group
+  static constexpr int T = MTS / WK;                  // tiles one warp handles per stage
+  // Every key warp consumes every stage, in order, so a warp never waits on a
+  // ring slot's use u+1 before it consumed use u -- which keeps the
+  // parity-based mbarrier waits unambiguous.
   static constexpr int NCW = WQ * WK;                 // consumer warps
   static constexpr int THREADS = 32 * (1 + NCW);
   static constexpr int TILE_BYTES = KS * ROW;         // one tensor, one stage
@@ -57,14 +71,16 @@ struct SplitCfg {
   static constexpr int EX_BYTES = WQ * WK * 8 * (DP + 2) * 4;
   static constexpr int SMEM_BYTES = DATA_BYTES + 1024 + 2 * NS * 8;
   static constexpr int MIN_BLOCKS = (THREADS <= 224) ? 2 : 1;
-  static_assert(KW % 16 == 0, "a warp handles whole 16-key tiles");
+  static_assert(KS % 16 == 0 && MTS % WK == 0, "whole 16-key tiles per warp");
+  static_assert(MTS * CB * 2 <= 32, "a stage needs at most one copy per producer lane");
   static_assert(EX_BYTES <= DATA_BYTES, "epilogue exchange reuses the stage ring");
   static_assert(D % 32 == 0, "head_dim is a multiple of 32");
 };
 
 // Byte offset of 16-byte chunk `chunk` of row `row` inside a column block whose
 // base is aligned to the swizzle repeat: the TMA 128B (64B) swizzle XORs the
-// chunk index with address bits [9:7] ([8:7]).
+// chunk index with address bits [9:7] ([8:7]).  Adding a multiple of 8 rows to
+// `row` only adds 8*SWB per 8 rows, so callers add tile bases separately.
 template <int SWB>
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   const uint32_t o = static_cast<uint32_t>(row * SWB + chunk * 16);
@@ -78,6 +94,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
                  const SplitParams p) {
   using Cfg = SplitCfg<D, KVT, WQ>;
   constexpr int NQ = 8 * WQ;  // query rows per pass
+  constexpr int T = Cfg::T;
 
   const int slot = blockIdx.x;
   const int h = blockIdx.y;
@@ -111,7 +128,9 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  __shared__ int s_abort;  // set when a bounded wait gave up
   if (threadIdx.x == 0) {
+    s_abort = 0;
     for (int s = 0; s < Cfg::NS; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, Cfg::NCW);
@@ -119,6 +138,15 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
     fence_barrier_init();
   }
   __syncthreads();
+  // Warp-uniform view of the abort flag; raising it sets PA_DEVERR_TIMEOUT.
+  auto aborted = [&]() {
+    return __shfl_sync(0xffffffffu, *reinterpret_cast<volatile int*>(&s_abort), 0) != 0;
+  };
+  auto wait_all = [&](uint32_t bar, uint32_t parity) {
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, parity, p.plan.err));
+    if (!ok && lane == 0) *reinterpret_cast<volatile int*>(&s_abort) = 1;
+    return ok;
+  };
 
   // Last key any row of pass `pass` may see.
   auto pass_key_end = [&](int pass) {
@@ -141,55 +169,61 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
     const int npages = min((S + bs - 1) / bs, p.max_blocks);
     auto bt_at = [&](int idx) { return idx < npages ? __ldg(bt + idx) : -1; };
     int it = 0;
+    int issued = 0;  // stages [0, issued) were issued (a prefix: issuing stops at an abort)
     for (int pass = 0; pass < npass; ++pass) {
       const int ke = pass_key_end(pass);
       const int nst = ke > kb ? (ke - kb + Cfg::KS - 1) / Cfg::KS : 0;
-      int win = kb / bs;
+      int win = kb / bs;  // block-table entries [win, win + 64) live in cur / nxt
       int cur = bt_at(win + lane);
       int nxt = bt_at(win + 32 + lane);
       for (int s = 0; s < nst; ++s, ++it) {
         const int buf = it % Cfg::NS;
-        if (it >= Cfg::NS) mbar_wait(bar_empty + 8 * buf, ((it / Cfg::NS) & 1) ^ 1, p.plan.err);
+        if (aborted()) continue;
+        if (it >= Cfg::NS && !wait_all(bar_empty + 8 * buf, ((it / Cfg::NS) & 1) ^ 1)) continue;
+        issued = it + 1;
         const int key0 = kb + s * Cfg::KS;
         const int nkeys = min(Cfg::KS, ke - key0);
         const int nbox = (nkeys + box_rows - 1) / box_rows;
-        const uint32_t kdst = base + buf * Cfg::STAGE_BYTES;
-        const uint32_t vdst = kdst + Cfg::TILE_BYTES;
+        while (key0 / bs >= win + 32) {  // a stage spans at most 16 pages: [win, win + 48)
+          win += 32;
+          cur = nxt;
+          nxt = bt_at(win + 32 + lane);
+        }
+        // copy c of this stage (one per lane): K/V by c & 1, column block and
+        // row box from c >> 1
+        const int c = lane;
+        const int rb = (c >> 1) / Cfg::CB;
+        const int cb = (c >> 1) % Cfg::CB;
+        const int key = key0 + rb * box_rows;
+        const int pidx = key / bs;
+        const int widx = min(pidx - win, 63);
+        const int pc = __shfl_sync(0xffffffffu, cur, widx & 31);
+        const int pn = __shfl_sync(0xffffffffu, nxt, widx & 31);
+        const int page = widx < 32 ? pc : pn;
         if (lane == 0)
           mbar_arrive_expect_tx(bar_full + 8 * buf, nbox * box_bytes * Cfg::CB * 2);
-        for (int b = 0; b < nbox; ++b) {
-          const int key = key0 + b * box_rows;
-          const int pidx = key / bs;
-          while (pidx >= win + 32) {  // slide the 32-entry block-table window
-            win += 32;
-            cur = nxt;
-            nxt = bt_at(win + 32 + lane);
+        __syncwarp();
+        if (rb < nbox) {
+          int y;
+          if (page < 0 || page >= p.num_blocks || pidx >= p.max_blocks) {
+            atomicOr(p.plan.err, PA_DEVERR_BAD_PAGE);
+            y = p.total_rows;  // outside the tensor: the copy reads zeros
+          } else {
+            y = (page * p.Hkv + h) * bs + (key % bs);
           }
-          const int page = __shfl_sync(0xffffffffu, cur, pidx - win);
-          if (lane == 0) {
-            int y;
-            if (page < 0 || page >= p.num_blocks || pidx >= p.max_blocks) {
-              atomicOr(p.plan.err, PA_DEVERR_BAD_PAGE);
-              y = p.total_rows;  // outside the tensor: the copy reads zeros
-            } else {
-              y = (page * p.Hkv + h) * bs + (key % bs);
-            }
-            const uint32_t off = static_cast<uint32_t>(b * box_rows * Cfg::SWB);
-#pragma unroll
-            for (int cb = 0; cb < Cfg::CB; ++cb) {
-              const int x = cb * (Cfg::SWB / Cfg::ESZ);
-              tma_load_2d(kdst + cb * Cfg::BLOCK_BYTES + off, &tmk, x, y, bar_full + 8 * buf, policy);
-              tma_load_2d(vdst + cb * Cfg::BLOCK_BYTES + off, &tmv, x, y, bar_full + 8 * buf, policy);
-            }
-          }
+          const uint32_t dst = base + buf * Cfg::STAGE_BYTES + (c & 1) * Cfg::TILE_BYTES +
+                               cb * Cfg::BLOCK_BYTES + static_cast<uint32_t>(rb * box_rows * Cfg::SWB);
+          tma_load_2d(dst, (c & 1) ? &tmv : &tmk, cb * (Cfg::SWB / Cfg::ESZ), y, bar_full + 8 * buf,
+                      policy);
         }
       }
       __syncthreads();  // pairs with the consumers' end-of-pass barrier
     }
-    // Every issued stage was waited for by the consumers; re-check so that no
-    // copy can still be landing in shared memory when the CTA exits.
+    // Drain: wait (bounded) until the last copy issued into every ring slot
+    // has landed, so that none can still be writing shared memory when the
+    // CTA exits -- whether or not the pipeline was aborted.
     if (lane == 0) {
-      for (int k = (it > Cfg::NS ? it - Cfg::NS : 0); k < it; ++k)
+      for (int k = (issued > Cfg::NS ? issued - Cfg::NS : 0); k < issued; ++k)
         mbar_wait(bar_full + 8 * (k % Cfg::NS), (k / Cfg::NS) & 1, p.plan.err);
     }
     return;
@@ -203,7 +237,14 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
   const int t = lane & 3;   // MMA thread-in-group
   const float sl2 = p.scale_log2;
   const float NEG_INF = -__int_as_float(0x7f800000);
+  constexpr float kRescale = 8.f;  // lazy-rescale threshold, log2 units
   const int ct = threadIdx.x - 32;  // consumer thread index
+
+  // Per-thread swizzled offsets inside a 16-key tile (16-bit caches).
+  const int lrowK = (lane & 7) + ((lane >> 3) & 1) * 8;  // ldmatrix row, K (A operand)
+  const int lchkK = (lane >> 4) & 1;
+  const int lrowV = (lane & 7) + ((lane >> 4) & 1) * 8;  // ldmatrix.trans row, V^T (A operand)
+  const int lchkV = (lane >> 3) & 1;
 
   int it = 0;
   for (int pass = 0; pass < npass; ++pass) {
@@ -259,51 +300,62 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
       }
     }
 
-    float m[2] = {NEG_INF, NEG_INF};
-    float l[2] = {0.f, 0.f};
+    float m[2] = {NEG_INF, NEG_INF};  // reference (lazily updated running max)
+    float l[2] = {0.f, 0.f};          // this thread's share of the row sums
     float acc[D / 16][4];
 #pragma unroll
     for (int dt = 0; dt < D / 16; ++dt) acc[dt][0] = acc[dt][1] = acc[dt][2] = acc[dt][3] = 0.f;
 
     const bool warp_active = pass_base + 8 * wq < rows;
 
-    for (int s = 0; s < nst; ++s, ++it) {
-      const int buf = it % Cfg::NS;
-      mbar_wait(bar_full + 8 * buf, (it / Cfg::NS) & 1, p.plan.err);
+    for (int s = 0; s < nst; ++s) {
+      const int sit = it + s;
+      const int buf = sit % Cfg::NS;
+      if (aborted()) continue;
+      if (!wait_all(bar_full + 8 * buf, (sit / Cfg::NS) & 1)) continue;
       const uint32_t kt = base + buf * Cfg::STAGE_BYTES;
       const uint32_t vt = kt + Cfg::TILE_BYTES;
       const int key0 = kb + s * Cfg::KS;
+      const int rbase = wk * T * 16;  // row of this warp's first key in the stage
 
-      if (warp_active) {
-#pragma unroll 1
-        for (int mt = 0; mt < Cfg::MT; ++mt) {
-          const int rbase = wk * Cfg::KW + mt * 16;  // row of the tile's first key
-          const int kbase = key0 + rbase;
-          if (kbase >= ke) break;
+      if (warp_active && key0 + rbase < ke) {
 
-          // ---- S^T[16 keys x 8 rows] = K Q^T
-          float c[4] = {0.f, 0.f, 0.f, 0.f};
-          if constexpr (!Cfg::kFp8) {
-            const int lrow = rbase + (lane & 7) + ((lane >> 3) & 1) * 8;
-            const int lchk = (lane >> 4) & 1;
+        // ---- S^T[16 keys x 8 rows] = K Q^T for T tiles
+        float c[T][4];
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-              const int cb = ks / 4;                  // 64 elements per column block
-              const int chunk = (ks % 4) * 2 + lchk;
+        for (int tt = 0; tt < T; ++tt) c[tt][0] = c[tt][1] = c[tt][2] = c[tt][3] = 0.f;
+        if constexpr (!Cfg::kFp8) {
+          float c2[4] = {0.f, 0.f, 0.f, 0.f};  // second chain when T == 1
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t ko = kt + (ks / 4) * Cfg::BLOCK_BYTES + swz<Cfg::SWB>(lrowK, (ks % 4) * 2 + lchkK);
+#pragma unroll
+            for (int tt = 0; tt < T; ++tt) {
               uint32_t a0, a1, a2, a3;
-              ldsm_x4(kt + cb * Cfg::BLOCK_BYTES + swz<Cfg::SWB>(lrow, chunk), a0, a1, a2, a3);
-              mma16816<Cfg::kBf16Mma>(c, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+              ldsm_x4(ko + (rbase + 16 * tt) * Cfg::SWB, a0, a1, a2, a3);
+              if (T == 1 && (ks & 1))
+                mma16816<Cfg::kBf16Mma>(c2, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+              else
+                mma16816<Cfg::kBf16Mma>(c[tt], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
             }
-          } else {
-            constexpr int KPB = Cfg::SWB / 16;
-            constexpr int CPT = Cfg::SWB / 64;        // 16-byte chunks per thread per row
+          }
+          if (T == 1) {
+            c[0][0] += c2[0]; c[0][1] += c2[1]; c[0][2] += c2[2]; c[0][3] += c2[3];
+          }
+        } else {
+          constexpr int KPB = Cfg::SWB / 16;
+          constexpr int CPT = Cfg::SWB / 64;  // 16-byte chunks per thread per row
+#pragma unroll
+          for (int tt = 0; tt < T; ++tt) {
+            const int rt = rbase + 16 * tt;
 #pragma unroll
             for (int cb = 0; cb < Cfg::CB; ++cb) {
               uint32_t wg[4 * CPT], wg8[4 * CPT];
 #pragma unroll
               for (int k = 0; k < CPT; ++k) {
-                const uint4 x = lds128(kt + cb * Cfg::BLOCK_BYTES + swz<Cfg::SWB>(rbase + g, t * CPT + k));
-                const uint4 y = lds128(kt + cb * Cfg::BLOCK_BYTES + swz<Cfg::SWB>(rbase + g + 8, t * CPT + k));
+                const uint32_t o = kt + cb * Cfg::BLOCK_BYTES + rt * Cfg::SWB + swz<Cfg::SWB>(g, t * CPT + k);
+                const uint4 x = lds128(o);
+                const uint4 y = lds128(o + 8 * Cfg::SWB);
                 wg[4 * k] = x.x; wg[4 * k + 1] = x.y; wg[4 * k + 2] = x.z; wg[4 * k + 3] = x.w;
                 wg8[4 * k] = y.x; wg8[4 * k + 1] = y.y; wg8[4 * k + 2] = y.z; wg8[4 * k + 3] = y.w;
               }
@@ -312,39 +364,39 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
                 uint32_t a0, a1, a2, a3;
                 e4m3x4_to_f16x2x2(wg[j], a0, a2);
                 e4m3x4_to_f16x2x2(wg8[j], a1, a3);
-                mma16816<false>(c, a0, a1, a2, a3, qf[cb * KPB + j][0], qf[cb * KPB + j][1]);
+                mma16816<false>(c[tt], a0, a1, a2, a3, qf[cb * KPB + j][0], qf[cb * KPB + j][1]);
               }
             }
           }
+        }
 
-          // ---- online softmax (log2 domain); rows g and g+8 of the tile
-          const int k_lo = kbase + g;
-          float sv[4];
-          sv[0] = (k_lo < lim[0]) ? c[0] * sl2 : NEG_INF;
-          sv[1] = (k_lo < lim[1]) ? c[1] * sl2 : NEG_INF;
-          sv[2] = (k_lo + 8 < lim[0]) ? c[2] * sl2 : NEG_INF;
-          sv[3] = (k_lo + 8 < lim[1]) ? c[3] * sl2 : NEG_INF;
-          float mx0 = fmaxf(sv[0], sv[2]);
-          float mx1 = fmaxf(sv[1], sv[3]);
+        // ---- online softmax (log2 domain), lazily rescaled
+        float sv[T][4];
+        float mx0 = NEG_INF, mx1 = NEG_INF;
 #pragma unroll
-          for (int o = 4; o <= 16; o <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-          }
-          const float mn0 = fmaxf(m[0], mx0);
-          const float mn1 = fmaxf(m[1], mx1);
-          const float ref0 = (mn0 == NEG_INF) ? 0.f : mn0;
-          const float ref1 = (mn1 == NEG_INF) ? 0.f : mn1;
-          const float al0 = fast_exp2(m[0] - ref0);
-          const float al1 = fast_exp2(m[1] - ref1);
-          m[0] = mn0;
-          m[1] = mn1;
-          const float p0 = fast_exp2(sv[0] - ref0);
-          const float p1 = fast_exp2(sv[1] - ref1);
-          const float p2 = fast_exp2(sv[2] - ref0);
-          const float p3 = fast_exp2(sv[3] - ref1);
-          l[0] = l[0] * al0 + p0 + p2;
-          l[1] = l[1] * al1 + p1 + p3;
+        for (int tt = 0; tt < T; ++tt) {
+          const int k_lo = key0 + rbase + 16 * tt + g;
+          sv[tt][0] = (k_lo < lim[0]) ? c[tt][0] * sl2 : NEG_INF;
+          sv[tt][1] = (k_lo < lim[1]) ? c[tt][1] * sl2 : NEG_INF;
+          sv[tt][2] = (k_lo + 8 < lim[0]) ? c[tt][2] * sl2 : NEG_INF;
+          sv[tt][3] = (k_lo + 8 < lim[1]) ? c[tt][3] * sl2 : NEG_INF;
+          mx0 = fmaxf(mx0, fmaxf(sv[tt][0], sv[tt][2]));
+          mx1 = fmaxf(mx1, fmaxf(sv[tt][1], sv[tt][3]));
+        }
+#pragma unroll
+        for (int o = 4; o <= 16; o <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+        }
+        const bool up0 = mx0 > m[0] + kRescale;
+        const bool up1 = mx1 > m[1] + kRescale;
+        if (__any_sync(0xffffffffu, up0 || up1)) {
+          const float al0 = up0 ? fast_exp2(m[0] - mx0) : 1.f;  // 0 when m was -inf
+          const float al1 = up1 ? fast_exp2(m[1] - mx1) : 1.f;
+          if (up0) m[0] = mx0;
+          if (up1) m[1] = mx1;
+          l[0] *= al0;
+          l[1] *= al1;
 #pragma unroll
           for (int dt = 0; dt < D / 16; ++dt) {
             acc[dt][0] *= al0;
@@ -352,34 +404,52 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
             acc[dt][2] *= al0;
             acc[dt][3] *= al1;
           }
-          // P^T (keys x rows) -> B fragment of PV: transpose the two 8x8 halves.
-          const uint32_t pb0 = movmatrix_trans(pack2<Cfg::kBf16Mma>(p0, p1));
-          const uint32_t pb1 = movmatrix_trans(pack2<Cfg::kBf16Mma>(p2, p3));
-
-          // ---- O^T[D x 8] += V^T P^T.  Keys past `ke` may hold stale or
-          // uninitialised shared memory: zero them so 0 * NaN cannot occur.
-          const bool tail = kbase + 16 > ke;
-          const int kq = kbase + 2 * t;  // keys of this thread's B/A k-pairs
-          const uint32_t m01 = (kq < ke ? 0x0000ffffu : 0u) | (kq + 1 < ke ? 0xffff0000u : 0u);
-          const uint32_t m89 = (kq + 8 < ke ? 0x0000ffffu : 0u) | (kq + 9 < ke ? 0xffff0000u : 0u);
-          if constexpr (!Cfg::kFp8) {
-            const int lrow = rbase + (lane & 7) + ((lane >> 4) & 1) * 8;
-            const int lchk = (lane >> 3) & 1;
+        }
+        const float ref0 = (m[0] == NEG_INF) ? 0.f : m[0];
+        const float ref1 = (m[1] == NEG_INF) ? 0.f : m[1];
+        uint32_t pb[T][2];
 #pragma unroll
-            for (int dt = 0; dt < D / 16; ++dt) {
-              const int cb = dt / 4;
-              const int chunk = (dt % 4) * 2 + lchk;
+        for (int tt = 0; tt < T; ++tt) {
+          const float p0 = fast_exp2(sv[tt][0] - ref0);
+          const float p1 = fast_exp2(sv[tt][1] - ref1);
+          const float p2 = fast_exp2(sv[tt][2] - ref0);
+          const float p3 = fast_exp2(sv[tt][3] - ref1);
+          l[0] += p0 + p2;
+          l[1] += p1 + p3;
+          // P^T (keys x rows) -> B fragment of PV: transpose the two 8x8 halves.
+          pb[tt][0] = movmatrix_trans(pack2<Cfg::kBf16Mma>(p0, p1));
+          pb[tt][1] = movmatrix_trans(pack2<Cfg::kBf16Mma>(p2, p3));
+        }
+
+        // ---- O^T[D x 8] += V^T P^T.  Keys past `ke` may hold stale or
+        // uninitialised shared memory: zero them so 0 * NaN cannot occur.
+        if constexpr (!Cfg::kFp8) {
+#pragma unroll
+          for (int dt = 0; dt < D / 16; ++dt) {
+            const uint32_t vo = vt + (dt / 4) * Cfg::BLOCK_BYTES + swz<Cfg::SWB>(lrowV, (dt % 4) * 2 + lchkV);
+#pragma unroll
+            for (int tt = 0; tt < T; ++tt) {
+              const int kbt = key0 + rbase + 16 * tt;
               uint32_t a0, a1, a2, a3;
-              ldsm_x4_trans(vt + cb * Cfg::BLOCK_BYTES + swz<Cfg::SWB>(lrow, chunk), a0, a1, a2, a3);
-              if (tail) {
+              ldsm_x4_trans(vo + (rbase + 16 * tt) * Cfg::SWB, a0, a1, a2, a3);
+              if (kbt + 16 > ke) {
+                const int kq = kbt + 2 * t;
+                const uint32_t m01 = (kq < ke ? 0x0000ffffu : 0u) | (kq + 1 < ke ? 0xffff0000u : 0u);
+                const uint32_t m89 = (kq + 8 < ke ? 0x0000ffffu : 0u) | (kq + 9 < ke ? 0xffff0000u : 0u);
                 a0 &= m01; a1 &= m01; a2 &= m89; a3 &= m89;
               }
-              mma16816<Cfg::kBf16Mma>(acc[dt], a0, a1, a2, a3, pb0, pb1);
+              mma16816<Cfg::kBf16Mma>(acc[dt], a0, a1, a2, a3, pb[tt][0], pb[tt][1]);
             }
-          } else {
-            // d = 32u + 4g + e:  e = 0 / 1 -> tile 2u rows g / g+8,
-            //                    e = 2 / 3 -> tile 2u+1 rows g / g+8.
-            const int ra = rbase + 2 * t;
+          }
+        } else {
+          // d = 32u + 4g + e:  e = 0 / 1 -> tile 2u rows g / g+8,
+          //                    e = 2 / 3 -> tile 2u+1 rows g / g+8.
+#pragma unroll
+          for (int tt = 0; tt < T; ++tt) {
+            const int kbt = key0 + rbase + 16 * tt;
+            const int ra = rbase + 16 * tt + 2 * t;
+            const bool tail = kbt + 16 > ke;
+            const int kq = kbt + 2 * t;
             const uint32_t z0 = (kq < ke) ? 0xffffffffu : 0u, z1 = (kq + 1 < ke) ? 0xffffffffu : 0u;
             const uint32_t z8 = (kq + 8 < ke) ? 0xffffffffu : 0u, z9 = (kq + 9 < ke) ? 0xffffffffu : 0u;
 #pragma unroll
@@ -401,8 +471,8 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
               e4m3x4_to_f16x2x2(prmt(w0, w1, 0x7362u), y0, y1);  // d+2, d+3
               e4m3x4_to_f16x2x2(prmt(w8, w9, 0x5140u), u0, u1);  // keys 2t+8, 2t+9
               e4m3x4_to_f16x2x2(prmt(w8, w9, 0x7362u), v0, v1);
-              mma16816<false>(acc[2 * u], x0, x1, u0, u1, pb0, pb1);
-              mma16816<false>(acc[2 * u + 1], y0, y1, v0, v1, pb0, pb1);
+              mma16816<false>(acc[2 * u], x0, x1, u0, u1, pb[tt][0], pb[tt][1]);
+              mma16816<false>(acc[2 * u + 1], y0, y1, v0, v1, pb[tt][0], pb[tt][1]);
             }
           }
         }
@@ -410,6 +480,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty + 8 * buf);
     }
+    it += nst;
 
     // ------------------------------------------------------------ epilogue
 #pragma unroll
