@@ -179,9 +179,11 @@ int pa_decode(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int num
  * array of PA_STATIC_SCRATCH_BYTES (32 MiB) that every GPU loading this code
  * keeps until the process exits.  A batch whose plan and partial results need
  * more than that is rejected with PA_ERR_UNSUPPORTED; the need is the
- * pa_plan_build footprint: C x 20 + n x 16 bytes of plan plus
- * min(C x max_query_len, max_partitions x num_tokens) x Hq x (D + 1) x 4 bytes
- * of partials, with capacity C = min(n x P, max(n, ceil(W / Hkv))).
+ * pa_plan_build footprint, dominated by the fp32 partials:
+ * min(C x max_query_len, max_partitions x num_tokens) x Hq x (D + 1) x 4 bytes,
+ * with capacity C = min(n x P, max(n, ceil(W / Hkv))), plus about C x 24 +
+ * n x 16 bytes of plan (and a list of row chunks when max_query_len x Hq/Hkv
+ * exceeds 32).
  * device_errors: optional device pointer to a uint32 that receives the
  * PA_DEVERR_* bits (the caller clears it); NULL uses a word inside the static
  * array, cleared at the start of every call and not readable by the caller.

@@ -64,8 +64,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 }  // namespace
 
 struct pa_plan {
-  int device, n, Hq, Hkv, D, max_qlen, max_tokens, P, W, kind, C;
-  long long rows_cap;
+  int device, n, Hq, Hkv, D, max_qlen, max_tokens, P, W, kind, C, rpc;
+  long long rows_cap, max_extra;
   pa::PlanDev dev;
   void* mem;
   long long bytes;
@@ -90,7 +90,13 @@ int split_box_rows(int D, int kv_dtype, int bs) {
 int split_row_groups(int max_qlen, int G) {
   const long long rows = static_cast<long long>(max_qlen) * G;
   if (rows <= 32) return static_cast<int>((rows + 7) / 8);
-  return 1;  // long prompt rows take several passes over their (short) key range
+  return 1;  // long prompts: 8-row work items, spread over the CTAs by work stealing
+}
+
+long long split_max_extra(int G, int rpc, long long rows_cap, int max_tokens, int max_qlen) {
+  if (static_cast<long long>(max_qlen) * G <= rpc) return 0;
+  // sum_r p_r (ceil(L_r G / rpc) - 1) <= G / rpc * (sum_{p_r >= 2} p_r L_r + sum_{p_r = 1} L_r)
+  return (static_cast<long long>(G) * (rows_cap + max_tokens) + rpc - 1) / rpc;
 }
 
 cudaError_t launch_split(const SplitParams& p, int C, int D, int kv_dtype, int row_groups,
@@ -181,6 +187,9 @@ int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_q_heads, int
   if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
   if (max_partitions <= 0) max_partitions = PA_DEFAULT_MAX_PARTITIONS;
   if (max_partitions > 65536 || budget > (1 << 24)) return PA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(max_query_len) * (num_q_heads / num_kv_heads) > (1 << 24) ||
+      max_tokens > (1 << 28))
+    return PA_ERR_UNSUPPORTED;
 
   DeviceGuard guard(device);
   if (!guard.ok) return PA_ERR_CUDA;
@@ -199,6 +208,9 @@ int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_q_heads, int
   const long long rows_alt = static_cast<long long>(max_partitions) * max_tokens;
   if (rows_alt < rows_cap) rows_cap = rows_alt;
   if (rows_cap < 1) rows_cap = 1;
+  const int G = num_q_heads / num_kv_heads;
+  const int rpc = 8 * pa::split_row_groups(max_query_len, G);
+  const long long max_extra = pa::split_max_extra(G, rpc, rows_cap, max_tokens, max_query_len);
 
   const size_t n = static_cast<size_t>(num_seqs);
   const size_t b_work = align256(static_cast<size_t>(C) * sizeof(int4));
@@ -208,7 +220,9 @@ int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_q_heads, int
   const size_t b_err = 256;
   const size_t b_po = align256(static_cast<size_t>(rows_cap) * num_q_heads * head_dim * 4);
   const size_t b_pl = align256(static_cast<size_t>(rows_cap) * num_q_heads * 4);
-  const size_t total = b_work + b_prow + b_red + b_snap + b_err + b_po + b_pl;
+  const size_t b_ord = align256(static_cast<size_t>(C) * sizeof(int));
+  const size_t b_ext = align256(static_cast<size_t>(max_extra > 0 ? max_extra : 1) * sizeof(int2));
+  const size_t total = b_work + b_prow + b_red + b_snap + b_err + b_po + b_pl + b_ord + b_ext;
 
   pa_plan* pl = new (std::nothrow) pa_plan();
   if (!pl) return PA_ERR_OOM;
@@ -228,11 +242,16 @@ int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_q_heads, int
   pl->dev.snap = reinterpret_cast<int2*>(c);
   c += b_snap;
   pl->dev.err = reinterpret_cast<unsigned*>(c);
+  pl->dev.counters = reinterpret_cast<int*>(c + 16);  // shares the error word's 256-byte block
   c += b_err;
   pl->dev.part_o = reinterpret_cast<float*>(c);
   c += b_po;
   pl->dev.part_lse = reinterpret_cast<float*>(c);
-  if (cudaMemset(pl->dev.err, 0, sizeof(unsigned)) != cudaSuccess ||
+  c += b_pl;
+  pl->dev.order = reinterpret_cast<int*>(c);
+  c += b_ord;
+  pl->dev.extra = reinterpret_cast<int2*>(c);
+  if (cudaMemset(pl->dev.err, 0, 64) != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess) {
     cudaFree(mem);
     delete pl;
@@ -249,7 +268,9 @@ int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_q_heads, int
   pl->W = budget;
   pl->kind = kind;
   pl->C = static_cast<int>(C);
+  pl->rpc = rpc;
   pl->rows_cap = rows_cap;
+  pl->max_extra = max_extra;
   pl->mem = mem;
   pl->bytes = static_cast<long long>(total);
   pl->refreshed = 0;
@@ -274,7 +295,10 @@ int pa_plan_refresh(pa_plan* plan, const int32_t* context_lens, const int32_t* c
   p.kind = plan->kind;
   p.max_qlen = plan->max_qlen;
   p.max_tokens = plan->max_tokens;
+  p.G = plan->Hq / plan->Hkv;
+  p.rpc = plan->rpc;
   p.rows_cap = plan->rows_cap;
+  p.max_extra = plan->max_extra;
   p.dev = plan->dev;
   if (pa::launch_plan(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return PA_ERR_CUDA;
   plan->refreshed = cu_query_lens ? 2 : 1;
@@ -338,6 +362,7 @@ int pa_decode(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int num
   sp.n = num_seqs;
   sp.total_rows = num_blocks * num_kv_heads * block_size;
   sp.out_f16 = q_dtype == PA_FP16 ? 1 : 0;
+  sp.rpc = plan->rpc;
   sp.scale_log2 = static_cast<float>(static_cast<double>(scale) * (fp8 ? k_scale : 1.0) *
                                      1.4426950408889634);
   sp.v_scale = fp8 ? v_scale : 1.0f;

@@ -21,13 +21,19 @@ struct PlanDev {
   unsigned* err;    // sticky PA_DEVERR_* word
   float* part_o;    // [rows_cap][Hq][D] normalised partial outputs
   float* part_lse;  // [rows_cap][Hq] log2-sum-exp of each partial (log2 units)
+  int* order;       // [C] slots by task length, longest first (launch order)
+  int2* extra;      // [max_extra] (slot, row chunk >= 1) of requests with many query rows
+  int* counters;    // [0] number of extra items, [1] next extra item to take (x Hkv)
 };
 
 struct PlanParams {
   const int* context_lens;
   const int* cu;  // nullable
   int n, Hkv, P, C, kind, max_qlen, max_tokens;
+  int G;          // q heads per kv head
+  int rpc;        // query rows per split-kernel work item (row chunk)
   long long rows_cap;
+  long long max_extra;
   PlanDev dev;
 };
 
@@ -41,6 +47,7 @@ struct SplitParams {
   int num_tokens, num_blocks, Hq, Hkv, G, bs, max_blocks, n;
   int total_rows;   // num_blocks * Hkv * bs: first out-of-range row of the cache view
   int out_f16;      // q/out element type: 1 = fp16, 0 = bf16
+  int rpc;          // query rows per work item (row chunk); a multiple of 8 x row groups
   float scale_log2; // softmax scale * k_scale * log2(e)
   float v_scale;    // 1 for 16-bit caches
 };
@@ -59,6 +66,8 @@ int split_box_rows(int D, int kv_dtype, int bs);
 int split_box_row_bytes(int D, int kv_dtype);
 // Query-row groups of 8 handled per pass for a plan with this max query length.
 int split_row_groups(int max_qlen, int G);
+// Upper bound on the extra (slot, row chunk) items a plan with these limits can list.
+long long split_max_extra(int G, int rpc, long long rows_cap, int max_tokens, int max_qlen);
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);

@@ -6,8 +6,11 @@
 // (exp_sums / max_logits / temporary_output).  Here the partials are already
 // normalised: out = sum_j 2^(lse_j - M) o_j / sum_j 2^(lse_j - M), M = max lse.
 //
-// One CTA per output row t.  The row's request is found by binary search over
-// cu_query_lens (vllm-rdna pull 29, Change 1).  Rows past cu[n], rows of
+// One warp per (output row t, q head).  The row's request is found by binary
+// search over cu_query_lens (vllm-rdna pull 29, Change 1).  Lanes read 32
+// partitions' log-sum-exps at a time (max, then weights kept in registers);
+// the partial rows are then streamed with the weights broadcast by shuffle,
+// each lane owning D/32 consecutive outputs.  Rows past cu[n], rows of
 // requests without partitions and rows of a request whose lengths changed
 // since the last plan refresh are written as zeros (the latter also raise
 // PA_DEVERR_STALE_PLAN).  Requests with a single partition were written by the
@@ -20,10 +23,20 @@ namespace pa {
 
 namespace {
 
-constexpr int kMergeThreads = 128;
+constexpr int kMergeWarps = 8;
 
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
-  const int t = blockIdx.x;
+template <int D>
+__global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergeParams p) {
+  constexpr int EPL = D / 32;  // outputs per lane: 2, 4 or 8
+  const int lane = threadIdx.x & 31;
+  // The split kernel that ran before this one is done with its work-stealing
+  // counter: reset it for the next decode call on this plan.
+  if (blockIdx.x == 0 && threadIdx.x == 0) p.plan.counters[1] = 0;
+  const long long pair = static_cast<long long>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
+  if (pair >= static_cast<long long>(p.num_tokens) * p.Hq) return;
+  const int t = static_cast<int>(pair / p.Hq);
+  const int hq = static_cast<int>(pair % p.Hq);
+
   int r = -1, tok = 0;
   if (p.cu) {
     if (t < p.cu[p.n]) {
@@ -51,55 +64,75 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     const int2 red = p.plan.reduce[r];
     first = red.x;
     parts = red.y;
-    if (stale && threadIdx.x == 0) atomicOr(p.plan.err, PA_DEVERR_STALE_PLAN);
+    if (stale && lane == 0 && hq == 0) atomicOr(p.plan.err, PA_DEVERR_STALE_PLAN);
   }
   if (!stale && parts == 1) return;
 
-  const int D = p.D;
-  const int units = p.Hq * (D / 8);  // 8 output elements per unit
-  uint16_t* orow = static_cast<uint16_t*>(p.out) + static_cast<size_t>(t) * p.Hq * D;
-  if (stale || parts == 0) {
-    for (int u = threadIdx.x; u < units; u += kMergeThreads)
-      *reinterpret_cast<uint4*>(orow + u * 8) = make_uint4(0u, 0u, 0u, 0u);
-    return;
-  }
+  uint16_t* orow = static_cast<uint16_t*>(p.out) + (static_cast<size_t>(t) * p.Hq + hq) * D + lane * EPL;
+  float o[EPL];
+#pragma unroll
+  for (int k = 0; k < EPL; ++k) o[k] = 0.f;
 
   const float NEG_INF = -__int_as_float(0x7f800000);
-  for (int u = threadIdx.x; u < units; u += kMergeThreads) {
-    const int hq = u / (D / 8);
-    const int d0 = (u % (D / 8)) * 8;
+  if (!stale && parts > 1) {
+    // pass 1: the maximum log-sum-exp
     float M = NEG_INF;
-    for (int j = 0; j < parts; ++j) {
+    for (int j = lane; j < parts; j += 32) {
       const size_t prow = static_cast<size_t>(p.plan.part_row[first + j] + tok) * p.Hq + hq;
       M = fmaxf(M, p.plan.part_lse[prow]);
     }
-    float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     if (M != NEG_INF) {
+      // pass 2: 32 partitions at a time -- lane j holds weight and row of partition j
       float wsum = 0.f;
-      for (int j = 0; j < parts; ++j) {
-        const size_t prow = static_cast<size_t>(p.plan.part_row[first + j] + tok) * p.Hq + hq;
-        const float lse = p.plan.part_lse[prow];
-        if (lse == NEG_INF) continue;
-        const float w = fast_exp2(lse - M);
+      for (int j0 = 0; j0 < parts; j0 += 32) {
+        const int j = j0 + lane;
+        float w = 0.f;
+        size_t prow = 0;
+        if (j < parts) {
+          prow = static_cast<size_t>(p.plan.part_row[first + j] + tok) * p.Hq + hq;
+          const float lse = p.plan.part_lse[prow];
+          w = (lse == NEG_INF) ? 0.f : fast_exp2(lse - M);
+        }
         wsum += w;
-        const float4* src = reinterpret_cast<const float4*>(p.plan.part_o + prow * D + d0);
-        const float4 a = src[0], b = src[1];
-        o[0] += w * a.x; o[1] += w * a.y; o[2] += w * a.z; o[3] += w * a.w;
-        o[4] += w * b.x; o[5] += w * b.y; o[6] += w * b.z; o[7] += w * b.w;
+        const int cnt = min(32, parts - j0);
+#pragma unroll 4
+        for (int k = 0; k < cnt; ++k) {
+          const float wk = __shfl_sync(0xffffffffu, w, k);
+          const size_t rk = __shfl_sync(0xffffffffu, static_cast<unsigned long long>(prow), k);
+          const float* src = p.plan.part_o + rk * D + lane * EPL;
+          if constexpr (EPL == 2) {
+            const float2 v = *reinterpret_cast<const float2*>(src);
+            o[0] += wk * v.x; o[1] += wk * v.y;
+          } else {
+#pragma unroll
+            for (int q = 0; q < EPL / 4; ++q) {
+              const float4 v = *reinterpret_cast<const float4*>(src + 4 * q);
+              o[4 * q] += wk * v.x; o[4 * q + 1] += wk * v.y;
+              o[4 * q + 2] += wk * v.z; o[4 * q + 3] += wk * v.w;
+            }
+          }
+        }
       }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
       const float inv = 1.f / wsum;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) o[k] *= inv;
+      for (int k = 0; k < EPL; ++k) o[k] *= inv;
     }
-    uint4 pk;
-    if (p.out_f16) {
-      pk = make_uint4(pack2<false>(o[0], o[1]), pack2<false>(o[2], o[3]),
-                      pack2<false>(o[4], o[5]), pack2<false>(o[6], o[7]));
-    } else {
-      pk = make_uint4(pack2<true>(o[0], o[1]), pack2<true>(o[2], o[3]),
-                      pack2<true>(o[4], o[5]), pack2<true>(o[6], o[7]));
-    }
-    *reinterpret_cast<uint4*>(orow + hq * D + d0) = pk;
+  }
+
+  uint32_t pk[EPL / 2];
+#pragma unroll
+  for (int k = 0; k < EPL / 2; ++k)
+    pk[k] = p.out_f16 ? pack2<false>(o[2 * k], o[2 * k + 1]) : pack2<true>(o[2 * k], o[2 * k + 1]);
+  if constexpr (EPL == 2) {
+    *reinterpret_cast<uint32_t*>(orow) = pk[0];
+  } else if constexpr (EPL == 4) {
+    *reinterpret_cast<uint2*>(orow) = make_uint2(pk[0], pk[1]);
+  } else {
+    *reinterpret_cast<uint4*>(orow) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
   }
 }
 
@@ -107,7 +140,13 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s) {
   if (p.num_tokens <= 0) return cudaSuccess;
-  merge_kernel<<<p.num_tokens, kMergeThreads, 0, s>>>(p);
+  const long long pairs = static_cast<long long>(p.num_tokens) * p.Hq;
+  const unsigned grid = static_cast<unsigned>((pairs + kMergeWarps - 1) / kMergeWarps);
+  switch (p.D) {
+    case 64: merge_kernel<64><<<grid, 32 * kMergeWarps, 0, s>>>(p); break;
+    case 128: merge_kernel<128><<<grid, 32 * kMergeWarps, 0, s>>>(p); break;
+    default: merge_kernel<256><<<grid, 32 * kMergeWarps, 0, s>>>(p); break;
+  }
   return cudaGetLastError();
 }
 

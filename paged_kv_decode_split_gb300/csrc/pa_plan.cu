@@ -11,10 +11,13 @@
 // [floor(j*nt/p), floor((j+1)*nt/p)).
 //
 // One CTA of 1024 threads, each owning 4 consecutive requests (n <= 4096):
-// two block reductions (n_act, sum S), one block scan (slot and partial-row
-// offsets), then a slot-parallel fill that finds each slot's request by binary
-// search over the scanned offsets.  No allocation, no host synchronisation:
-// it can be captured in a CUDA graph.
+// two block reductions (n_act, sum S), one block scan (slot, partial-row and
+// extra-item offsets), then a slot-parallel fill that finds each slot's request
+// by binary search over the scanned offsets.  It also writes the split
+// kernel's launch order (slots by task length, longest first, by a counting
+// sort over 128 quarter-octave length classes) and the extra work items that
+// split the query rows of requests with more rows than one work item holds.
+// No allocation, no host synchronisation: it can be captured in a CUDA graph.
 #include "../../include/pa.h"
 #include "pa_internal.h"
 
@@ -32,50 +35,48 @@ __device__ __forceinline__ long long warp_sum64(long long v) {
   return v;
 }
 
-// Inclusive block scan of two 32-bit counters (one warp-level pass each plus
-// one pass over the warp totals); writes the block total to *total.
-__device__ void block_scan2(int& a, int& b, int* sa, int* sb, int* ta, int* tb) {
+// Inclusive block scan of three 32-bit counters (a warp-level pass, then one
+// pass over the warp totals); block totals land in tot[0..2].
+__device__ void block_scan3(int (&v)[3], int (*sw)[kWarps], int* tot) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int xa = __shfl_up_sync(0xffffffffu, a, o);
-    const int xb = __shfl_up_sync(0xffffffffu, b, o);
-    if (lane >= o) {
-      a += xa;
-      b += xb;
+#pragma unroll
+    for (int c = 0; c < 3; ++c) {
+      const int x = __shfl_up_sync(0xffffffffu, v[c], o);
+      if (lane >= o) v[c] += x;
     }
   }
   if (lane == 31) {
-    sa[warp] = a;
-    sb[warp] = b;
+#pragma unroll
+    for (int c = 0; c < 3; ++c) sw[c][warp] = v[c];
   }
   __syncthreads();
   if (warp == 0) {
-    int va = lane < kWarps ? sa[lane] : 0;
-    int vb = lane < kWarps ? sb[lane] : 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int xa = __shfl_up_sync(0xffffffffu, va, o);
-      const int xb = __shfl_up_sync(0xffffffffu, vb, o);
-      if (lane >= o) {
-        va += xa;
-        vb += xb;
+    for (int c = 0; c < 3; ++c) {
+      int w = lane < kWarps ? sw[c][lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += x;
       }
-    }
-    if (lane < kWarps) {
-      sa[lane] = va;
-      sb[lane] = vb;
-    }
-    if (lane == kWarps - 1) {
-      *ta = va;
-      *tb = vb;
+      if (lane < kWarps) sw[c][lane] = w;
+      if (lane == kWarps - 1) tot[c] = w;
     }
   }
   __syncthreads();
   if (warp > 0) {
-    a += sa[warp - 1];
-    b += sb[warp - 1];
+#pragma unroll
+    for (int c = 0; c < 3; ++c) v[c] += sw[c][warp - 1];
   }
+}
+
+// Length class of a task of `len` >= 1 keys: 4 classes per octave, 0..127.
+__device__ __forceinline__ int length_class(int len) {
+  const int msb = 31 - __clz(len);
+  const int frac = msb >= 2 ? (len >> (msb - 2)) & 3 : (len << (2 - msb)) & 3;
+  return msb * 4 + frac;
 }
 
 __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
@@ -88,8 +89,9 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
   __shared__ long long s_red[kWarps];
   __shared__ int s_cnt[kWarps];
   __shared__ int s_bad;
-  __shared__ int s_scan_a[kWarps], s_scan_b[kWarps];
-  __shared__ int s_total_slots, s_total_rows;
+  __shared__ int s_scan[3][kWarps];
+  __shared__ int s_tot[3];
+  __shared__ int s_bcnt[129];  // launch-order classes 127..0, then 128 = unused slots
   __shared__ long long s_sum, s_nact;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -141,9 +143,9 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
   const long long sum_s = s_sum, n_act = s_nact;
   const long long C = p.C;
 
-  // ---- 2. partition counts and partial rows per request
+  // ---- 2. partition counts, partial rows and extra row-chunk items per request
   int parts[kPer];
-  int my_slots = 0, my_rows = 0;
+  int my_slots = 0, my_rows = 0, my_extra = 0;
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
     parts[k] = 0;
@@ -160,14 +162,16 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
     }
     my_slots += parts[k];
     my_rows += parts[k] >= 2 ? parts[k] * L[k] : 0;
+    my_extra += parts[k] * ((L[k] * p.G + p.rpc - 1) / p.rpc - 1);
   }
 
-  // ---- 3. exclusive offsets (slots, partial rows)
-  int inc_slots = my_slots, inc_rows = my_rows;
-  block_scan2(inc_slots, inc_rows, s_scan_a, s_scan_b, &s_total_slots, &s_total_rows);
+  // ---- 3. exclusive offsets (slots, partial rows, extra items)
+  int inc[3] = {my_slots, my_rows, my_extra};
+  block_scan3(inc, s_scan, s_tot);
   __syncthreads();
-  int slot0 = inc_slots - my_slots, row0 = inc_rows - my_rows;
-  const bool rows_overflow = static_cast<long long>(s_total_rows) > p.rows_cap;
+  int slot0 = inc[0] - my_slots, row0 = inc[1] - my_rows, extra0 = inc[2] - my_extra;
+  const bool rows_overflow = static_cast<long long>(s_tot[1]) > p.rows_cap ||
+                             static_cast<long long>(s_tot[2]) > p.max_extra;
   if (rows_overflow) {
     // Cannot happen for a plan built with these limits; empty the plan rather
     // than write partial rows past the scratch.
@@ -175,8 +179,10 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
     for (int k = 0; k < kPer; ++k) parts[k] = 0;
     slot0 = 0;
     row0 = 0;
+    extra0 = 0;
   }
-  const int total_slots = rows_overflow ? 0 : s_total_slots;
+  const int total_slots = rows_overflow ? 0 : s_tot[0];
+  const int total_extra = rows_overflow ? 0 : s_tot[2];
   if (tid == 0 && (bad || rows_overflow)) atomicOr(p.dev.err, PA_DEVERR_PLAN_OVERFLOW);
 
 #pragma unroll
@@ -190,29 +196,55 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
       s_ctx[r] = S[k];
       s_qlen[r] = L[k];
       s_prow[r] = row0;
+      // extra work items: row chunks 1.. of every slot of this request
+      const int chunks = (L[k] * p.G + p.rpc - 1) / p.rpc;
+      for (int j = 0; j < parts[k]; ++j)
+        for (int c = 1; c < chunks; ++c)
+          p.dev.extra[extra0 + j * (chunks - 1) + (c - 1)] = make_int2(slot0 + j, c);
+      extra0 += parts[k] * (chunks - 1);
       slot0 += parts[k];
       row0 += parts[k] >= 2 ? parts[k] * L[k] : 0;
     }
   }
+  if (tid < 129) s_bcnt[tid] = 0;
+  if (tid == 0) {
+    p.dev.counters[0] = total_extra;
+    p.dev.counters[1] = 0;
+  }
   __syncthreads();
 
-  // ---- 4. slot fill
+  // ---- 4. slot fill (and launch-order class counts)
+  auto slot_task = [&](int slot, int& r, int& tb, int& te) {
+    int lo = 0, hi = n;  // last r with s_first[r] <= slot (it has parts > 0)
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_first[mid] <= slot)
+        lo = mid;
+      else
+        hi = mid;
+    }
+    r = lo;
+    const int pr = s_parts[r];
+    const int j = slot - s_first[r];
+    const long long nt = (static_cast<long long>(s_ctx[r]) + kTile - 1) / kTile;
+    tb = static_cast<int>((j * nt) / pr);
+    te = static_cast<int>(((j + 1) * nt) / pr);
+  };
+  auto slot_class = [&](int slot) {
+    if (slot >= total_slots) return 128;
+    int r, tb, te;
+    slot_task(slot, r, tb, te);
+    const long long keys = min(static_cast<long long>(te) * kTile, static_cast<long long>(s_ctx[r])) -
+                           static_cast<long long>(tb) * kTile;
+    return 127 - length_class(static_cast<int>(keys));  // 0 = longest class
+  };
   for (int slot = tid; slot < C; slot += kThreads) {
+    atomicAdd(&s_bcnt[slot_class(slot)], 1);
     if (slot < total_slots) {
-      int lo = 0, hi = n;  // last r with s_first[r] <= slot (it has parts > 0)
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (s_first[mid] <= slot)
-          lo = mid;
-        else
-          hi = mid;
-      }
-      const int r = lo;
+      int r, tb, te;
+      slot_task(slot, r, tb, te);
       const int pr = s_parts[r];
       const int j = slot - s_first[r];
-      const long long nt = (static_cast<long long>(s_ctx[r]) + kTile - 1) / kTile;
-      const int tb = static_cast<int>((j * nt) / pr);
-      const int te = static_cast<int>(((j + 1) * nt) / pr);
       p.dev.work[slot] = make_int4(r, tb, te, s_ctx[r]);
       p.dev.part_row[slot] = pr >= 2 ? s_prow[r] + j * s_qlen[r] : -1;
     } else {
@@ -220,6 +252,18 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
       p.dev.part_row[slot] = -1;
     }
   }
+  __syncthreads();
+  // ---- 5. launch order: counting sort of the slots by length class
+  if (tid == 0) {
+    int pos = 0;
+    for (int b = 0; b < 129; ++b) {
+      const int c = s_bcnt[b];
+      s_bcnt[b] = pos;
+      pos += c;
+    }
+  }
+  __syncthreads();
+  for (int slot = tid; slot < C; slot += kThreads) p.dev.order[atomicAdd(&s_bcnt[slot_class(slot)], 1)] = slot;
 }
 
 }  // namespace

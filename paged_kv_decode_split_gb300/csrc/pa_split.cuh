@@ -96,28 +96,6 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
   constexpr int NQ = 8 * WQ;  // query rows per pass
   constexpr int T = Cfg::T;
 
-  const int slot = blockIdx.x;
-  const int h = blockIdx.y;
-  const int4 task = p.plan.work[slot];
-  const int r = task.x;
-  if (r < 0) return;  // unused slot
-
-  // A plan refreshed from other lengths: the merge kernel zeroes these rows
-  // and reports it; this task does nothing.
-  const int S = task.w;
-  const int row0 = p.cu ? p.cu[r] : r;
-  const int L = p.cu ? p.cu[r + 1] - row0 : 1;
-  const int2 snap = p.plan.snap[r];
-  if (snap.x != p.context_lens[r] || snap.y != L) return;
-
-  const int parts = p.plan.reduce[r].y;
-  const int prow_base = p.plan.part_row[slot];
-  const int G = p.G;
-  const int rows = L * G;                 // query rows of this request
-  const int npass = (rows + NQ - 1) / NQ;
-  const int kb = task.y * kTile;          // first key of the task
-  const int ke_task = min(task.z * kTile, S);
-
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -148,19 +126,78 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
     return ok;
   };
 
-  // Last key any row of pass `pass` may see.
-  auto pass_key_end = [&](int pass) {
-    const int last_row = min(rows, (pass + 1) * NQ) - 1;
-    const int last_tok = last_row / G;
-    return min(ke_task, S - (L - 1 - last_tok));
-  };
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmk);
+    prefetch_tmap(&tmv);
+  }
+  const int G = p.G;
+  const int Hkv = p.Hkv;
+  int it = 0;      // stages so far (producer and consumers count alike)
+  int issued = 0;  // producer: stages [0, issued) were issued (a prefix: issuing stops at an abort)
+
+  // Work items: first this CTA's own (slot, kv head) in launch order -- the
+  // planner sorts slots longest first -- then, until none are left, extra row
+  // chunks of requests with many query rows, taken from a device counter.
+  __shared__ int s_item[4];
+  for (int round = 0;; ++round) {
+    __syncthreads();  // everyone has read the previous item
+    if (threadIdx.x == 0) {
+      int slot = -1, hh = 0, chunk = 0, valid = 1;
+      if (round == 0) {
+        slot = p.plan.order[blockIdx.x / Hkv];
+        hh = blockIdx.x % Hkv;
+      } else {
+        const int idx = atomicAdd(p.plan.counters + 1, 1);
+        if (idx < p.plan.counters[0] * Hkv) {
+          const int2 e = p.plan.extra[idx / Hkv];
+          slot = e.x;
+          chunk = e.y;
+          hh = idx % Hkv;
+        } else {
+          valid = 0;
+        }
+      }
+      s_item[0] = slot;
+      s_item[1] = hh;
+      s_item[2] = chunk;
+      s_item[3] = valid;
+    }
+    __syncthreads();
+    if (!s_item[3]) break;
+    const int slot = s_item[0];
+    const int h = s_item[1];
+    const int chunk = s_item[2];
+    const int4 task = p.plan.work[slot];
+    const int r = task.x;
+    if (r < 0) continue;  // unused slot
+
+    // A plan refreshed from other lengths: the merge kernel zeroes these rows
+    // and reports it; this task does nothing.
+    const int S = task.w;
+    const int row0 = p.cu ? p.cu[r] : r;
+    const int L = p.cu ? p.cu[r + 1] - row0 : 1;
+    const int2 snap = p.plan.snap[r];
+    if (snap.x != p.context_lens[r] || snap.y != L) continue;
+
+    const int parts = p.plan.reduce[r].y;
+    const int prow_base = p.plan.part_row[slot];
+    const int rows = L * G;                     // query rows of this request
+    const int row_lo = chunk * p.rpc;           // this item's rows [row_lo, row_hi)
+    const int row_hi = min(rows, row_lo + p.rpc);
+    if (row_lo >= row_hi) continue;
+    const int npass = (row_hi - row_lo + NQ - 1) / NQ;
+    const int kb = task.y * kTile;              // first key of the task
+    const int ke_task = min(task.z * kTile, S);
+
+    // Last key any row of pass `pass` may see.
+    auto pass_key_end = [&](int pass) {
+      const int last_row = min(row_hi, row_lo + (pass + 1) * NQ) - 1;
+      const int last_tok = last_row / G;
+      return min(ke_task, S - (L - 1 - last_tok));
+    };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      prefetch_tmap(&tmk);
-      prefetch_tmap(&tmv);
-    }
     const uint64_t policy = l2_evict_first_policy();
     const int bs = p.bs;
     const int box_rows = bs < Cfg::KS ? bs : Cfg::KS;
@@ -168,8 +205,6 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
     const int* bt = p.block_tables + static_cast<size_t>(r) * p.max_blocks;
     const int npages = min((S + bs - 1) / bs, p.max_blocks);
     auto bt_at = [&](int idx) { return idx < npages ? __ldg(bt + idx) : -1; };
-    int it = 0;
-    int issued = 0;  // stages [0, issued) were issued (a prefix: issuing stops at an abort)
     for (int pass = 0; pass < npass; ++pass) {
       const int ke = pass_key_end(pass);
       const int nst = ke > kb ? (ke - kb + Cfg::KS - 1) / Cfg::KS : 0;
@@ -219,16 +254,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
       }
       __syncthreads();  // pairs with the consumers' end-of-pass barrier
     }
-    // Drain: wait (bounded) until the last copy issued into every ring slot
-    // has landed, so that none can still be writing shared memory when the
-    // CTA exits -- whether or not the pipeline was aborted.
-    if (lane == 0) {
-      for (int k = (issued > Cfg::NS ? issued - Cfg::NS : 0); k < issued; ++k)
-        mbar_wait(bar_full + 8 * (k % Cfg::NS), (k / Cfg::NS) & 1, p.plan.err);
-    }
-    return;
-  }
-
+  } else {
   // -------------------------------------------------------------- consumers
   const int cw = warp - 1;
   const int wq = cw % WQ;
@@ -246,9 +272,8 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
   const int lrowV = (lane & 7) + ((lane >> 4) & 1) * 8;  // ldmatrix.trans row, V^T (A operand)
   const int lchkV = (lane >> 3) & 1;
 
-  int it = 0;
   for (int pass = 0; pass < npass; ++pass) {
-    const int pass_base = pass * NQ;
+    const int pass_base = row_lo + pass * NQ;
     const int ke = pass_key_end(pass);
     const int nst = ke > kb ? (ke - kb + Cfg::KS - 1) / Cfg::KS : 0;
 
@@ -257,7 +282,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int n = pass_base + 8 * wq + 2 * t + e;
-      lim[e] = (n < rows) ? min(ke_task, S - (L - 1 - n / G)) : kb;
+      lim[e] = (n < row_hi) ? min(ke_task, S - (L - 1 - n / G)) : kb;
     }
 
     // Q^T as the B operand of QK^T: row n = groupID of this warp's 8 rows.
@@ -265,7 +290,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
     {
       const int n = pass_base + 8 * wq + g;
       const int tok = n / G;
-      const bool ok = n < rows && row0 + tok < p.num_tokens;
+      const bool ok = n < row_hi && row0 + tok < p.num_tokens;
       const size_t qoff = ok ? (static_cast<size_t>(row0 + tok) * p.Hq + h * G + n % G) * D : 0;
       if constexpr (!Cfg::kFp8) {
         const uint16_t* qp = static_cast<const uint16_t*>(p.q) + qoff;
@@ -306,7 +331,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
 #pragma unroll
     for (int dt = 0; dt < D / 16; ++dt) acc[dt][0] = acc[dt][1] = acc[dt][2] = acc[dt][3] = 0.f;
 
-    const bool warp_active = pass_base + 8 * wq < rows;
+    const bool warp_active = pass_base + 8 * wq < row_hi;
 
     for (int s = 0; s < nst; ++s) {
       const int sit = it + s;
@@ -522,7 +547,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
       const int col = (u / D4) % 8;
       const int d4 = (u % D4) * 4;
       const int n = pass_base + 8 * gq + col;
-      if (n >= rows) continue;
+      if (n >= row_hi) continue;
       float M = NEG_INF;
 #pragma unroll
       for (int k = 0; k < Cfg::WK; ++k) M = fmaxf(M, ex_m[(gq * Cfg::WK + k) * 8 + col]);
@@ -566,6 +591,16 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
     fence_proxy_async_smem();  // exchange writes precede the next pass's TMA writes
     __syncthreads();           // pairs with the producer's end-of-pass barrier
   }
+  }  // consumers
+  }  // work items
+
+  // Drain: wait (bounded) until the last copy issued into every ring slot has
+  // landed, so that none can still be writing shared memory when the CTA
+  // exits -- whether or not the pipeline was aborted.
+  if (warp == 0 && lane == 0) {
+    for (int k = (issued > Cfg::NS ? issued - Cfg::NS : 0); k < issued; ++k)
+      mbar_wait(bar_full + 8 * (k % Cfg::NS), (k / Cfg::NS) & 1, p.plan.err);
+  }
 }
 
 template <int D, int KVT, int WQ>
@@ -580,8 +615,7 @@ cudaError_t launch_split_cfg(const SplitParams& p, int C, const CUtensorMap& tk,
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  dim3 grid(C, p.Hkv);
-  kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(tk, tv, p);
+  kern<<<static_cast<unsigned>(C) * p.Hkv, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(tk, tv, p);
   return cudaGetLastError();
 }
 

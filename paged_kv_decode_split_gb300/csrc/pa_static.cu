@@ -129,6 +129,8 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
   if (!cu_query_lens && num_tokens != num_seqs) return PA_ERR_INVALID_ARG;
   if (max_partitions <= 0) max_partitions = PA_DEFAULT_MAX_PARTITIONS;
   if (max_partitions > 65536 || budget > (1 << 24)) return PA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(max_query_len) * (num_q_heads / num_kv_heads) > (1 << 24))
+    return PA_ERR_UNSUPPORTED;
 
   int device = -1;
   if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices)
@@ -157,7 +159,14 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
   const size_t b_err = 256;
   const size_t b_po = up256(static_cast<size_t>(rows_cap) * num_q_heads * head_dim * 4);
   const size_t b_pl = up256(static_cast<size_t>(rows_cap) * num_q_heads * 4);
-  if (b_work + b_prow + b_red + b_snap + b_err + b_po + b_pl > PA_STATIC_SCRATCH_BYTES)
+  const int G = num_q_heads / num_kv_heads;
+  const int wq = pa::split_row_groups(max_query_len, G);
+  const int rpc = 8 * wq;
+  const long long max_extra = pa::split_max_extra(G, rpc, rows_cap, num_tokens, max_query_len);
+  const size_t b_ord = up256(static_cast<size_t>(C) * sizeof(int));
+  const size_t b_ext = up256(static_cast<size_t>(max_extra > 0 ? max_extra : 1) * sizeof(int2));
+  if (b_work + b_prow + b_red + b_snap + b_err + b_po + b_pl + b_ord + b_ext >
+      PA_STATIC_SCRATCH_BYTES)
     return PA_ERR_UNSUPPORTED;  // this batch needs more scratch than the static array holds
 
   char* base = static_cast<char*>(scratch_address(device));
@@ -173,10 +182,15 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
   dev.snap = reinterpret_cast<int2*>(c);
   c += b_snap;
   unsigned* own_err = reinterpret_cast<unsigned*>(c);
+  dev.counters = reinterpret_cast<int*>(c + 16);
   c += b_err;
   dev.part_o = reinterpret_cast<float*>(c);
   c += b_po;
   dev.part_lse = reinterpret_cast<float*>(c);
+  c += b_pl;
+  dev.order = reinterpret_cast<int*>(c);
+  c += b_ord;
+  dev.extra = reinterpret_cast<int2*>(c);
   dev.err = device_errors ? reinterpret_cast<unsigned*>(device_errors) : own_err;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -199,7 +213,10 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
   pp.kind = kind;
   pp.max_qlen = max_query_len;
   pp.max_tokens = num_tokens;
+  pp.G = G;
+  pp.rpc = rpc;
   pp.rows_cap = rows_cap;
+  pp.max_extra = max_extra;
   pp.dev = dev;
   if (pa::launch_plan(pp, s) != cudaSuccess) return PA_ERR_CUDA;
 
@@ -221,10 +238,10 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
   sp.n = num_seqs;
   sp.total_rows = num_blocks * num_kv_heads * block_size;
   sp.out_f16 = q_dtype == PA_FP16 ? 1 : 0;
+  sp.rpc = rpc;
   sp.scale_log2 = static_cast<float>(static_cast<double>(scale) * (fp8 ? k_scale : 1.0) *
                                      1.4426950408889634);
   sp.v_scale = fp8 ? v_scale : 1.0f;
-  const int wq = pa::split_row_groups(max_query_len, sp.G);
   if (pa::launch_split(sp, static_cast<int>(C), head_dim, kv_dtype, wq, tk, tv, s) != cudaSuccess)
     return PA_ERR_CUDA;
 
