@@ -64,7 +64,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 }  // namespace
 
 struct pa_plan {
-  int device, n, Hq, Hkv, D, max_qlen, max_tokens, P, W, kind, C, rpc;
+  int device, n, Hq, Hkv, D, max_qlen, max_tokens, P, W, kind, C, rpc, sms;
   long long rows_cap, max_extra;
   pa::PlanDev dev;
   void* mem;
@@ -193,13 +193,11 @@ int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_q_heads, int
 
   DeviceGuard guard(device);
   if (!guard.ok) return PA_ERR_CUDA;
-  if (budget <= 0) {
-    int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
-        sms <= 0)
-      return PA_ERR_CUDA;
-    budget = 2 * sms;
-  }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+      sms <= 0)
+    return PA_ERR_CUDA;
+  if (budget <= 0) budget = 2 * sms;
   const long long per_head = (static_cast<long long>(budget) + num_kv_heads - 1) / num_kv_heads;
   const long long lo = per_head > num_seqs ? per_head : num_seqs;
   const long long hi = static_cast<long long>(num_seqs) * max_partitions;
@@ -222,7 +220,9 @@ int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_q_heads, int
   const size_t b_pl = align256(static_cast<size_t>(rows_cap) * num_q_heads * 4);
   const size_t b_ord = align256(static_cast<size_t>(C) * sizeof(int));
   const size_t b_ext = align256(static_cast<size_t>(max_extra > 0 ? max_extra : 1) * sizeof(int2));
-  const size_t total = b_work + b_prow + b_red + b_snap + b_err + b_po + b_pl + b_ord + b_ext;
+  const size_t b_mrow = align256(static_cast<size_t>(max_tokens) * sizeof(int2));
+  const size_t total =
+      b_work + b_prow + b_red + b_snap + b_err + b_po + b_pl + b_ord + b_ext + b_mrow;
 
   pa_plan* pl = new (std::nothrow) pa_plan();
   if (!pl) return PA_ERR_OOM;
@@ -251,6 +251,8 @@ int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_q_heads, int
   pl->dev.order = reinterpret_cast<int*>(c);
   c += b_ord;
   pl->dev.extra = reinterpret_cast<int2*>(c);
+  c += b_ext;
+  pl->dev.mrows = reinterpret_cast<int2*>(c);
   if (cudaMemset(pl->dev.err, 0, 64) != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess) {
     cudaFree(mem);
@@ -269,6 +271,7 @@ int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_q_heads, int
   pl->kind = kind;
   pl->C = static_cast<int>(C);
   pl->rpc = rpc;
+  pl->sms = sms;
   pl->rows_cap = rows_cap;
   pl->max_extra = max_extra;
   pl->mem = mem;
@@ -360,6 +363,7 @@ int pa_decode(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int num
   sp.bs = block_size;
   sp.max_blocks = max_blocks_per_seq;
   sp.n = num_seqs;
+  sp.C = plan->C;
   sp.total_rows = num_blocks * num_kv_heads * block_size;
   sp.out_f16 = q_dtype == PA_FP16 ? 1 : 0;
   sp.rpc = plan->rpc;
@@ -369,10 +373,19 @@ int pa_decode(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int num
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int wq = pa::split_row_groups(plan->max_qlen, sp.G);
-  if (plan->ev_start && cudaEventRecord(plan->ev_start, s) != cudaSuccess) return PA_ERR_CUDA;
+  // Profiling events: inside a stream capture they must be external event
+  // records to fire on every replay of the graph.
+  auto record = [&](cudaEvent_t e) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return false;
+    return (cs == cudaStreamCaptureStatusActive
+                ? cudaEventRecordWithFlags(e, s, cudaEventRecordExternal)
+                : cudaEventRecord(e, s)) == cudaSuccess;
+  };
+  if (plan->ev_start && !record(plan->ev_start)) return PA_ERR_CUDA;
   if (pa::launch_split(sp, plan->C, head_dim, kv_dtype, wq, tk, tv, s) != cudaSuccess)
     return PA_ERR_CUDA;
-  if (plan->ev_stop && cudaEventRecord(plan->ev_stop, s) != cudaSuccess) return PA_ERR_CUDA;
+  if (plan->ev_stop && !record(plan->ev_stop)) return PA_ERR_CUDA;
 
   pa::MergeParams mp;
   mp.plan = plan->dev;
@@ -384,6 +397,8 @@ int pa_decode(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int num
   mp.Hq = num_q_heads;
   mp.D = head_dim;
   mp.out_f16 = sp.out_f16;
+  const long long pairs = static_cast<long long>(num_tokens) * num_q_heads;
+  mp.grid = static_cast<int>(pairs < 8ll * plan->sms ? pairs : 8ll * plan->sms);
   if (pa::launch_merge(mp, s) != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;
 }

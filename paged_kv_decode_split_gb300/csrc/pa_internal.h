@@ -23,7 +23,9 @@ struct PlanDev {
   float* part_lse;  // [rows_cap][Hq] log2-sum-exp of each partial (log2 units)
   int* order;       // [C] slots by task length, longest first (launch order)
   int2* extra;      // [max_extra] (slot, row chunk >= 1) of requests with many query rows
-  int* counters;    // [0] number of extra items, [1] next extra item to take (x Hkv)
+  int* counters;    // [0] extra items, [1] next extra item (x Hkv), [2] split CTAs done,
+                    // [3] rows to merge
+  int2* mrows;      // [max_tokens] (request, token) of every row of a multi-partition request
 };
 
 struct PlanParams {
@@ -45,19 +47,12 @@ struct SplitParams {
   const int* context_lens;
   const int* cu;  // nullable
   int num_tokens, num_blocks, Hq, Hkv, G, bs, max_blocks, n;
+  int C;            // plan capacity: CTAs [0, C*Hkv) run tasks, the rest write zero rows
   int total_rows;   // num_blocks * Hkv * bs: first out-of-range row of the cache view
   int out_f16;      // q/out element type: 1 = fp16, 0 = bf16
   int rpc;          // query rows per work item (row chunk); a multiple of 8 x row groups
   float scale_log2; // softmax scale * k_scale * log2(e)
   float v_scale;    // 1 for 16-bit caches
-};
-
-struct MergeParams {
-  PlanDev plan;
-  void* out;
-  const int* context_lens;
-  const int* cu;
-  int num_tokens, n, Hq, D, out_f16;
 };
 
 // Rows of one TMA box of a KV tile for head_dim D, cache dtype, block size.
@@ -68,6 +63,34 @@ int split_box_row_bytes(int D, int kv_dtype);
 int split_row_groups(int max_qlen, int G);
 // Upper bound on the extra (slot, row chunk) items a plan with these limits can list.
 long long split_max_extra(int G, int rpc, long long rows_cap, int max_tokens, int max_qlen);
+
+struct MergeParams {
+  PlanDev plan;
+  void* out;
+  const int* context_lens;
+  const int* cu;  // nullable
+  int num_tokens, n, Hq, D, out_f16;
+  int grid;       // persistent grid size
+};
+
+// Launches `kernel` with programmatic stream serialization: it may be
+// scheduled while the previous kernel on the stream is still running (every
+// kernel of this library waits for its predecessor before touching data).
+template <typename Kernel, typename... Args>
+cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, int smem, cudaStream_t s,
+                       const Args&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);

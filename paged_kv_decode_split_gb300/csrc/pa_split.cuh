@@ -36,11 +36,15 @@
 //    multiplied in fp16; k_scale is folded into the logit scale and v_scale
 //    into the epilogue;
 //  * the key warps of a row group are merged through shared memory at the end
-//    of a pass.
+//    of a pass;
+//  * a few extra CTAs at the end of the grid write the rows no task writes
+//    (graph padding, empty or stale requests); requests with several
+//    partitions are combined afterwards by the merge kernel.
 #pragma once
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
+#include "pa_merge.cuh"
 
 namespace pa {
 
@@ -96,15 +100,39 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
   constexpr int NQ = 8 * WQ;  // query rows per pass
   constexpr int T = Cfg::T;
 
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp == 0 && lane == 0) {  // descriptor fetch overlaps the planner's tail
+    prefetch_tmap(&tmk);
+    prefetch_tmap(&tmv);
+  }
+  pdl_wait();  // the plan (and everything before this kernel) is complete
+  // Every CTA counts itself out; the last one resets the work counters for the
+  // next decode on this plan.
+  auto cta_exit = [&]() {
+    __syncthreads();
+    pdl_trigger();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const unsigned gone = atomicAdd(reinterpret_cast<unsigned*>(p.plan.counters + 2), 1u);
+      if (gone == gridDim.x - 1) {
+        p.plan.counters[1] = 0;
+        p.plan.counters[2] = 0;
+      }
+    }
+  };
+  if (blockIdx.x >= static_cast<unsigned>(p.C * p.Hkv)) {  // zero-row CTA
+    zero_rows<D>(p, blockIdx.x - p.C * p.Hkv, warp, Cfg::THREADS / 32, lane);
+    cta_exit();
+    return;
+  }
+
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   float* ex = reinterpret_cast<float*>(smem_raw + (base - raw));
   const uint32_t bar_full = base + Cfg::DATA_BYTES;
   const uint32_t bar_empty = bar_full + 8 * Cfg::NS;
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
 
   __shared__ int s_abort;  // set when a bounded wait gave up
   if (threadIdx.x == 0) {
@@ -126,10 +154,6 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
     return ok;
   };
 
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tmk);
-    prefetch_tmap(&tmv);
-  }
   const int G = p.G;
   const int Hkv = p.Hkv;
   int it = 0;      // stages so far (producer and consumers count alike)
@@ -601,6 +625,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
     for (int k = (issued > Cfg::NS ? issued - Cfg::NS : 0); k < issued; ++k)
       mbar_wait(bar_full + 8 * (k % Cfg::NS), (k / Cfg::NS) & 1, p.plan.err);
   }
+  cta_exit();
 }
 
 template <int D, int KVT, int WQ>
@@ -615,8 +640,9 @@ cudaError_t launch_split_cfg(const SplitParams& p, int C, const CUtensorMap& tk,
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  kern<<<static_cast<unsigned>(C) * p.Hkv, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(tk, tv, p);
-  return cudaGetLastError();
+  const unsigned zero_ctas = static_cast<unsigned>((p.num_tokens + kZeroRows - 1) / kZeroRows);
+  return launch_pdl(kern, dim3(static_cast<unsigned>(C) * p.Hkv + zero_ctas), dim3(Cfg::THREADS),
+                    Cfg::SMEM_BYTES, s, tk, tv, p);
 }
 
 template <int D>

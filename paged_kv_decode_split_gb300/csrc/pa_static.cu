@@ -135,13 +135,11 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
   int device = -1;
   if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices)
     return PA_ERR_CUDA;
-  if (budget <= 0) {
-    int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
-        sms <= 0)
-      return PA_ERR_CUDA;
-    budget = 2 * sms;
-  }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+      sms <= 0)
+    return PA_ERR_CUDA;
+  if (budget <= 0) budget = 2 * sms;
 
   // ---- carve the static array: plan arrays, error word, partial results
   const long long per_head = (static_cast<long long>(budget) + num_kv_heads - 1) / num_kv_heads;
@@ -165,7 +163,8 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
   const long long max_extra = pa::split_max_extra(G, rpc, rows_cap, num_tokens, max_query_len);
   const size_t b_ord = up256(static_cast<size_t>(C) * sizeof(int));
   const size_t b_ext = up256(static_cast<size_t>(max_extra > 0 ? max_extra : 1) * sizeof(int2));
-  if (b_work + b_prow + b_red + b_snap + b_err + b_po + b_pl + b_ord + b_ext >
+  const size_t b_mrow = up256(static_cast<size_t>(num_tokens) * sizeof(int2));
+  if (b_work + b_prow + b_red + b_snap + b_err + b_po + b_pl + b_ord + b_ext + b_mrow >
       PA_STATIC_SCRATCH_BYTES)
     return PA_ERR_UNSUPPORTED;  // this batch needs more scratch than the static array holds
 
@@ -191,6 +190,8 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
   dev.order = reinterpret_cast<int*>(c);
   c += b_ord;
   dev.extra = reinterpret_cast<int2*>(c);
+  c += b_ext;
+  dev.mrows = reinterpret_cast<int2*>(c);
   dev.err = device_errors ? reinterpret_cast<unsigned*>(device_errors) : own_err;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -236,6 +237,7 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
   sp.bs = block_size;
   sp.max_blocks = max_blocks_per_seq;
   sp.n = num_seqs;
+  sp.C = static_cast<int>(C);
   sp.total_rows = num_blocks * num_kv_heads * block_size;
   sp.out_f16 = q_dtype == PA_FP16 ? 1 : 0;
   sp.rpc = rpc;
@@ -255,6 +257,8 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
   mp.Hq = num_q_heads;
   mp.D = head_dim;
   mp.out_f16 = sp.out_f16;
+  const long long pairs = static_cast<long long>(num_tokens) * num_q_heads;
+  mp.grid = static_cast<int>(pairs < 8ll * sms ? pairs : 8ll * sms);
   if (pa::launch_merge(mp, s) != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;
 }
