@@ -226,58 +226,76 @@ def _run_oracle(w):
 # ------------------------------------------------------------ GPU timings
 
 def time_native(w, steps: int, warmup: int, kind=binding.PROPORTIONAL, flush: bool = False,
-                sampler: ClockSampler | None = None, world: int = 1):
-    """Device-timed steps (refresh + decode).  Returns (ms/step, split-kernel ms
-    per launch, plan)."""
+                sampler: ClockSampler | None = None, world: int = 1, graph: bool = True):
+    """Device-timed steps (refresh + decode).  The K steps are captured once into
+    a CUDA graph (refresh and decode are capturable: no allocation, no host
+    synchronisation) and replayed, as a serving engine replays its decode
+    graphs; each step records its own event pair around the split kernel.
+    With flush=True every step is preceded by an L2-flushing write and timed
+    by its own event pair.  Returns (ms/step, split-kernel ms per launch, plan)."""
     dev = w.q.device
     plan = binding.plan_for(w, kind)
     out = torch.empty_like(w.q)
-    stream = torch.cuda.current_stream(dev)
     flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    pairs = [(ev(), ev()) for _ in range(steps)]
+    step_ev = [(ev(), ev()) for _ in range(steps)] if flush else None
 
     def step():
         plan.refresh(w.context_lens, w.cu_query_lens)
         binding.decode_workload(plan, w, out=out)
 
+    def body(stream):
+        for i, (a, b) in enumerate(pairs):
+            if flush:
+                flush_buf.zero_()
+                step_ev[i][0].record(stream)
+            plan.set_split_events(a, b)
+            step()
+            if flush:
+                step_ev[i][1].record(stream)
+
+    cur = torch.cuda.current_stream(dev)
     for _ in range(max(warmup, 3)):
         step()
-    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-             for _ in range(steps)]
     for a, b in pairs:  # materialise the CUDA events before handing them to the ABI
-        a.record(stream)
-        b.record(stream)
+        a.record(cur)
+        b.record(cur)
+    if step_ev:
+        for a, b in step_ev:
+            a.record(cur)
+            b.record(cur)
     torch.cuda.synchronize(dev)
-    if flush:
-        # per-step timing with an L2 flush between steps, outside the timed pairs
-        step_ms = []
-        for a, b in pairs:
-            flush_buf.zero_()
-            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            plan.set_split_events(a, b)
-            s0.record(stream)
-            step()
-            s1.record(stream)
-            step_ms.append((s0, s1))
+    g = None
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            body(torch.cuda.current_stream(dev))
+        plan.set_split_events(None, None)
+        g.replay()  # warm replay
         torch.cuda.synchronize(dev)
-        ms = statistics.median(x.elapsed_time(y) for x, y in step_ms)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0, t1 = ev(), ev()
+    if sampler:
+        sampler.start()
+    t0.record(cur)
+    if g is not None:
+        g.replay()
     else:
-        barrier(world)
-        torch.cuda.synchronize(dev)
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        if sampler:
-            sampler.start()
-        t0.record(stream)
-        for a, b in pairs:
-            plan.set_split_events(a, b)
-            step()
-        t1.record(stream)
-        torch.cuda.synchronize(dev)
-        if sampler:
-            sampler.stop()
-        barrier(world)
-        ms = t0.elapsed_time(t1) / steps
+        body(cur)
+    t1.record(cur)
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.stop()
+    barrier(world)
     plan.set_split_events(None, None)
+    if flush:
+        ms = statistics.median(a.elapsed_time(b) for a, b in step_ev)
+    else:
+        ms = t0.elapsed_time(t1) / steps
     split_ms = statistics.mean(a.elapsed_time(b) for a, b in pairs)
+    del g
     return ms, split_ms, plan
 
 
@@ -359,6 +377,7 @@ def run_native(args, world, rank, local):
                    "max_partitions": info["max_partitions"],
                    "l2": "inputs larger than L2 (no flush)" if kv_bytes > L2_BYTES
                    else "not flushed: inputs fit in L2",
+                   "timing": "K steps captured once in a CUDA graph and replayed",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -399,7 +418,8 @@ def sweep(args):
                                          max(1, min(w.context_lens.tolist())), 1)}
             for kind, tag in ((binding.PROPORTIONAL, "proportional"),
                               (binding.UNIFORM, "uniform")):
-                ms, split_ms, plan = time_native(w, args.steps, args.warmup, kind=kind, flush=True)
+                ms, split_ms, plan = time_native(w, args.steps, args.warmup, kind=kind, flush=True,
+                                                 graph=False)
                 _, red = plan.download()
                 res[tag] = {"us_per_call": round(ms * 1e3, 2),
                             "split_us": round(split_ms * 1e3, 2),
@@ -408,17 +428,22 @@ def sweep(args):
                             "frac_of_measured": round(kv / (split_ms * 1e-3) / 1e9 /
                                                       measured_peaks().get("hbm_gbs", 6800.0), 4),
                             "tasks": int(red[:, 1].sum()), "max_parts": int(red[:, 1].max())}
-            # refresh alone
+            # refresh alone: 100 refreshes captured in a graph, replayed
             plan = binding.plan_for(w)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            for _ in range(10):
-                plan.refresh(w.context_lens, w.cu_query_lens)
+            plan.refresh(w.context_lens, w.cu_query_lens)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for _ in range(100):
+                    plan.refresh(w.context_lens, w.cu_query_lens)
+            g.replay()
             a.record()
-            for _ in range(100):
-                plan.refresh(w.context_lens, w.cu_query_lens)
+            g.replay()
             b.record()
             torch.cuda.synchronize()
             res["refresh_us"] = round(a.elapsed_time(b) * 10, 2)
+            del g
             print(json.dumps(res), flush=True)
             del w
             torch.cuda.empty_cache()

@@ -220,7 +220,7 @@ int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_q_heads, int
   const size_t b_pl = align256(static_cast<size_t>(rows_cap) * num_q_heads * 4);
   const size_t b_ord = align256(static_cast<size_t>(C) * sizeof(int));
   const size_t b_ext = align256(static_cast<size_t>(max_extra > 0 ? max_extra : 1) * sizeof(int2));
-  const size_t b_mrow = align256(static_cast<size_t>(max_tokens) * sizeof(int2));
+  const size_t b_mrow = align256(static_cast<size_t>(max_tokens) * sizeof(int4));
   const size_t total =
       b_work + b_prow + b_red + b_snap + b_err + b_po + b_pl + b_ord + b_ext + b_mrow;
 
@@ -252,7 +252,7 @@ int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_q_heads, int
   c += b_ord;
   pl->dev.extra = reinterpret_cast<int2*>(c);
   c += b_ext;
-  pl->dev.mrows = reinterpret_cast<int2*>(c);
+  pl->dev.mrows = reinterpret_cast<int4*>(c);
   if (cudaMemset(pl->dev.err, 0, 64) != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess) {
     cudaFree(mem);

@@ -25,7 +25,9 @@ struct PlanDev {
   int2* extra;      // [max_extra] (slot, row chunk >= 1) of requests with many query rows
   int* counters;    // [0] extra items, [1] next extra item (x Hkv), [2] split CTAs done,
                     // [3] rows to merge
-  int2* mrows;      // [max_tokens] (request, token) of every row of a multi-partition request
+  int4* mrows;      // [max_tokens] one entry per row of a multi-partition request:
+                    // {r | (parts - 1) << 12, token, partial row of partition 0, L}
+                    // (partition j's partial row is that + j * L)
 };
 
 struct PlanParams {

@@ -234,7 +234,8 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
             p.dev.extra[extra0 + j * (chunks - 1) + (c - 1)] = make_int2(slot0 + j, c);
       extra0 += parts[k] * (chunks - 1);
       if (parts[k] >= 2)
-        for (int i = 0; i < L[k]; ++i) p.dev.mrows[mrow0 + i] = make_int2(r, i);
+        for (int i = 0; i < L[k]; ++i)
+          p.dev.mrows[mrow0 + i] = make_int4(r | ((parts[k] - 1) << 12), i, row0 + i, L[k]);
       mrow0 += parts[k] >= 2 ? L[k] : 0;
       slot0 += parts[k];
       row0 += parts[k] >= 2 ? parts[k] * L[k] : 0;

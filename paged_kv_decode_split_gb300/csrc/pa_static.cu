@@ -163,7 +163,7 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
   const long long max_extra = pa::split_max_extra(G, rpc, rows_cap, num_tokens, max_query_len);
   const size_t b_ord = up256(static_cast<size_t>(C) * sizeof(int));
   const size_t b_ext = up256(static_cast<size_t>(max_extra > 0 ? max_extra : 1) * sizeof(int2));
-  const size_t b_mrow = up256(static_cast<size_t>(num_tokens) * sizeof(int2));
+  const size_t b_mrow = up256(static_cast<size_t>(num_tokens) * sizeof(int4));
   if (b_work + b_prow + b_red + b_snap + b_err + b_po + b_pl + b_ord + b_ext + b_mrow >
       PA_STATIC_SCRATCH_BYTES)
     return PA_ERR_UNSUPPORTED;  // this batch needs more scratch than the static array holds
@@ -191,7 +191,7 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
   c += b_ord;
   dev.extra = reinterpret_cast<int2*>(c);
   c += b_ext;
-  dev.mrows = reinterpret_cast<int2*>(c);
+  dev.mrows = reinterpret_cast<int4*>(c);
   dev.err = device_errors ? reinterpret_cast<unsigned*>(device_errors) : own_err;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
