@@ -57,14 +57,12 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 
 struct pa_plan {
-  int device, n, Hq, Hkv, D, max_qlen, max_tokens, P, W, kind, C, rpc, sms;
+  int device, n, Hq, Hkv, D, max_qlen, max_tokens, P, W, kind, C, Q, rpc, sms;
   long long rows_cap, max_extra;
   pa::PlanDev dev;
   void* mem;
@@ -95,16 +93,77 @@ int split_row_groups(int max_qlen, int G) {
 
 long long split_max_extra(int G, int rpc, long long rows_cap, int max_tokens, int max_qlen) {
   if (static_cast<long long>(max_qlen) * G <= rpc) return 0;
-  // sum_r p_r (ceil(L_r G / rpc) - 1) <= G / rpc * (sum_{p_r >= 2} p_r L_r + sum_{p_r = 1} L_r)
+  // sum_r T_r (ceil(L_r G / rpc) - 1) <= G / rpc * (sum_{T_r >= 2} T_r L_r + sum_{T_r = 1} L_r)
+  // for T_r pieces of request r
   return (static_cast<long long>(G) * (rows_cap + max_tokens) + rpc - 1) / rpc;
 }
 
-cudaError_t launch_split(const SplitParams& p, int C, int D, int kv_dtype, int row_groups,
+namespace {
+size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+}  // namespace
+
+PlanLayout plan_layout(int num_seqs, int Hq, int Hkv, int D, int max_qlen, int max_tokens,
+                       int max_partitions, int budget, int sms, bool pieces) {
+  PlanLayout l;
+  const long long per_head = (static_cast<long long>(budget) + Hkv - 1) / Hkv;
+  const long long lo = per_head > num_seqs ? per_head : num_seqs;
+  const long long hi = static_cast<long long>(num_seqs) * max_partitions;
+  l.C = hi < lo ? hi : lo;
+  // Pieces: only decode-only plans whose grid is about one wave (2 CTAs per
+  // SM) gain from cutting long slots; elsewhere tasks run whole.
+  l.Q = (pieces && max_qlen == 1 && l.C * Hkv <= 4ll * sms) ? 4 : 1;
+  long long rows = l.C * max_qlen;
+  const long long rows_alt = static_cast<long long>(max_partitions) * max_tokens;
+  if (rows_alt < rows) rows = rows_alt;
+  if (rows < 1) rows = 1;
+  l.rows_cap = rows * l.Q;  // sum_r T_r L_r <= Q sum_r p_r L_r
+  const int G = Hq / Hkv;
+  l.rpc = 8 * split_row_groups(max_qlen, G);
+  l.max_extra = split_max_extra(G, l.rpc, l.rows_cap, max_tokens, max_qlen);
+  const size_t n = static_cast<size_t>(num_seqs);
+  l.b_work = up256(static_cast<size_t>(l.C) * sizeof(int4));
+  l.b_red = up256(n * sizeof(int2));
+  l.b_snap = up256(n * sizeof(int2));
+  l.b_err = 256;
+  l.b_po = up256(static_cast<size_t>(l.rows_cap) * Hq * D * 4);
+  l.b_pl = up256(static_cast<size_t>(l.rows_cap) * Hq * 4);
+  l.b_pieces = up256(static_cast<size_t>(l.C) * l.Q * sizeof(int4));
+  l.b_ext = up256(static_cast<size_t>(l.max_extra > 0 ? l.max_extra : 1) * sizeof(int2));
+  l.b_mrow = up256(static_cast<size_t>(max_tokens) * sizeof(int4));
+  l.total = l.b_work + l.b_red + l.b_snap + l.b_err + l.b_po + l.b_pl + l.b_pieces + l.b_ext +
+            l.b_mrow;
+  return l;
+}
+
+PlanDev carve_plan(char* c, const PlanLayout& l) {
+  PlanDev d;
+  d.work = reinterpret_cast<int4*>(c);
+  c += l.b_work;
+  d.reduce = reinterpret_cast<int2*>(c);
+  c += l.b_red;
+  d.snap = reinterpret_cast<int2*>(c);
+  c += l.b_snap;
+  d.err = reinterpret_cast<unsigned*>(c);
+  d.counters = reinterpret_cast<int*>(c + 16);
+  c += l.b_err;
+  d.part_o = reinterpret_cast<float*>(c);
+  c += l.b_po;
+  d.part_lse = reinterpret_cast<float*>(c);
+  c += l.b_pl;
+  d.pieces = reinterpret_cast<int4*>(c);
+  c += l.b_pieces;
+  d.extra = reinterpret_cast<int2*>(c);
+  c += l.b_ext;
+  d.mrows = reinterpret_cast<int4*>(c);
+  return d;
+}
+
+cudaError_t launch_split(const SplitParams& p, int D, int kv_dtype, int row_groups,
                          const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s) {
   switch (D) {
-    case 64: return launch_split_d64(p, C, kv_dtype, row_groups, tk, tv, s);
-    case 128: return launch_split_d128(p, C, kv_dtype, row_groups, tk, tv, s);
-    default: return launch_split_d256(p, C, kv_dtype, row_groups, tk, tv, s);
+    case 64: return launch_split_d64(p, kv_dtype, row_groups, tk, tv, s);
+    case 128: return launch_split_d128(p, kv_dtype, row_groups, tk, tv, s);
+    default: return launch_split_d256(p, kv_dtype, row_groups, tk, tv, s);
   }
 }
 
@@ -198,31 +257,10 @@ int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_q_heads, int
       sms <= 0)
     return PA_ERR_CUDA;
   if (budget <= 0) budget = 2 * sms;
-  const long long per_head = (static_cast<long long>(budget) + num_kv_heads - 1) / num_kv_heads;
-  const long long lo = per_head > num_seqs ? per_head : num_seqs;
-  const long long hi = static_cast<long long>(num_seqs) * max_partitions;
-  const long long C = hi < lo ? hi : lo;
-  long long rows_cap = C * max_query_len;
-  const long long rows_alt = static_cast<long long>(max_partitions) * max_tokens;
-  if (rows_alt < rows_cap) rows_cap = rows_alt;
-  if (rows_cap < 1) rows_cap = 1;
-  const int G = num_q_heads / num_kv_heads;
-  const int rpc = 8 * pa::split_row_groups(max_query_len, G);
-  const long long max_extra = pa::split_max_extra(G, rpc, rows_cap, max_tokens, max_query_len);
-
-  const size_t n = static_cast<size_t>(num_seqs);
-  const size_t b_work = align256(static_cast<size_t>(C) * sizeof(int4));
-  const size_t b_prow = align256(static_cast<size_t>(C) * sizeof(int));
-  const size_t b_red = align256(n * sizeof(int2));
-  const size_t b_snap = align256(n * sizeof(int2));
-  const size_t b_err = 256;
-  const size_t b_po = align256(static_cast<size_t>(rows_cap) * num_q_heads * head_dim * 4);
-  const size_t b_pl = align256(static_cast<size_t>(rows_cap) * num_q_heads * 4);
-  const size_t b_ord = align256(static_cast<size_t>(C) * sizeof(int));
-  const size_t b_ext = align256(static_cast<size_t>(max_extra > 0 ? max_extra : 1) * sizeof(int2));
-  const size_t b_mrow = align256(static_cast<size_t>(max_tokens) * sizeof(int4));
-  const size_t total =
-      b_work + b_prow + b_red + b_snap + b_err + b_po + b_pl + b_ord + b_ext + b_mrow;
+  const pa::PlanLayout lay = pa::plan_layout(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                             max_query_len, max_tokens, max_partitions, budget, sms,
+                                             true);
+  const size_t total = lay.total;
 
   pa_plan* pl = new (std::nothrow) pa_plan();
   if (!pl) return PA_ERR_OOM;
@@ -232,27 +270,7 @@ int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_q_heads, int
     delete pl;
     return PA_ERR_OOM;
   }
-  char* c = static_cast<char*>(mem);
-  pl->dev.work = reinterpret_cast<int4*>(c);
-  c += b_work;
-  pl->dev.part_row = reinterpret_cast<int*>(c);
-  c += b_prow;
-  pl->dev.reduce = reinterpret_cast<int2*>(c);
-  c += b_red;
-  pl->dev.snap = reinterpret_cast<int2*>(c);
-  c += b_snap;
-  pl->dev.err = reinterpret_cast<unsigned*>(c);
-  pl->dev.counters = reinterpret_cast<int*>(c + 16);  // shares the error word's 256-byte block
-  c += b_err;
-  pl->dev.part_o = reinterpret_cast<float*>(c);
-  c += b_po;
-  pl->dev.part_lse = reinterpret_cast<float*>(c);
-  c += b_pl;
-  pl->dev.order = reinterpret_cast<int*>(c);
-  c += b_ord;
-  pl->dev.extra = reinterpret_cast<int2*>(c);
-  c += b_ext;
-  pl->dev.mrows = reinterpret_cast<int4*>(c);
+  pl->dev = pa::carve_plan(static_cast<char*>(mem), lay);
   if (cudaMemset(pl->dev.err, 0, 64) != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess) {
     cudaFree(mem);
@@ -269,11 +287,12 @@ int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_q_heads, int
   pl->P = max_partitions;
   pl->W = budget;
   pl->kind = kind;
-  pl->C = static_cast<int>(C);
-  pl->rpc = rpc;
+  pl->C = static_cast<int>(lay.C);
+  pl->Q = lay.Q;
+  pl->rpc = lay.rpc;
   pl->sms = sms;
-  pl->rows_cap = rows_cap;
-  pl->max_extra = max_extra;
+  pl->rows_cap = lay.rows_cap;
+  pl->max_extra = lay.max_extra;
   pl->mem = mem;
   pl->bytes = static_cast<long long>(total);
   pl->refreshed = 0;
@@ -295,6 +314,7 @@ int pa_plan_refresh(pa_plan* plan, const int32_t* context_lens, const int32_t* c
   p.Hkv = plan->Hkv;
   p.P = plan->P;
   p.C = plan->C;
+  p.Q = plan->Q;
   p.kind = plan->kind;
   p.max_qlen = plan->max_qlen;
   p.max_tokens = plan->max_tokens;
@@ -383,7 +403,7 @@ int pa_decode(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int num
                 : cudaEventRecord(e, s)) == cudaSuccess;
   };
   if (plan->ev_start && !record(plan->ev_start)) return PA_ERR_CUDA;
-  if (pa::launch_split(sp, plan->C, head_dim, kv_dtype, wq, tk, tv, s) != cudaSuccess)
+  if (pa::launch_split(sp, head_dim, kv_dtype, wq, tk, tv, s) != cudaSuccess)
     return PA_ERR_CUDA;
   if (plan->ev_stop && !record(plan->ev_stop)) return PA_ERR_CUDA;
 

@@ -12,28 +12,55 @@ constexpr int kTile = 256;       // partition tile, tokens
 constexpr int kMaxSeqs = 4096;   // planner domain
 constexpr int kStageTensorBytes = 16384;  // split kernel: K (or V) bytes per pipeline stage
 
+constexpr int kMinPieceTiles = 2;  // a slot is cut into pieces of at least this many tiles
+
 // Device buffers owned by one plan.
+//
+// The plan's tasks (work_info: one per slot) are what the pages define.  The
+// split kernel runs *pieces*: a slot's tile range cut into q >= 1 consecutive
+// sub-ranges, q chosen by the planner so that, when the whole grid is one wave,
+// no CTA is left with a task much longer than the others (every piece writes
+// its own partial; the merge combines them with the request's other partials).
 struct PlanDev {
   int4* work;       // [C] (seq, tile_begin, tile_end, seq_ctx); seq = -1 unused
   int2* reduce;     // [n] (first_slot, num_parts)
-  int* part_row;    // [C] first partial row of the slot's request part; -1 if none
   int2* snap;       // [n] (context_len, query_len) seen by the last refresh
   unsigned* err;    // sticky PA_DEVERR_* word
   float* part_o;    // [rows_cap][Hq][D] normalised partial outputs
   float* part_lse;  // [rows_cap][Hq] log2-sum-exp of each partial (log2 units)
-  int* order;       // [C] slots by task length, longest first (launch order)
-  int2* extra;      // [max_extra] (slot, row chunk >= 1) of requests with many query rows
+  int4* pieces;     // [C * Q] in launch order (longest first): {r, first key, end key,
+                    // partial row of the piece's token 0, or -1 when the request has
+                    // one piece and its CTA writes the output row}
+  int2* extra;      // [max_extra] (piece position, row chunk >= 1) for requests whose
+                    // query rows exceed one work item
   int* counters;    // [0] extra items, [1] next extra item (x Hkv), [2] split CTAs done,
-                    // [3] rows to merge
-  int4* mrows;      // [max_tokens] one entry per row of a multi-partition request:
-                    // {r | (parts - 1) << 12, token, partial row of partition 0, L}
-                    // (partition j's partial row is that + j * L)
+                    // [3] rows to merge, [4] pieces
+  int4* mrows;      // [max_tokens] one entry per row of a request with several pieces:
+                    // {r | (pieces - 1) << 12, token, partial row of piece 0, L}
+                    // (piece k's partial row is that + k * L)
 };
+
+// Sizes and offsets of one plan's buffers (256-byte aligned, back to back).
+struct PlanLayout {
+  long long C;          // capacity: slots of work_info
+  int Q;                // at most Q pieces per slot
+  long long rows_cap;   // partial rows
+  int rpc;              // query rows per split-kernel work item
+  long long max_extra;  // extra (piece, row chunk) items
+  size_t b_work, b_red, b_snap, b_err, b_po, b_pl, b_pieces, b_ext, b_mrow, total;
+};
+// `pieces` = false keeps every task whole (Q = 1).
+PlanLayout plan_layout(int num_seqs, int Hq, int Hkv, int D, int max_qlen, int max_tokens,
+                       int max_partitions, int budget, int sms, bool pieces);
+// Points the buffers of `l` into [base, base + l.total); the error word and
+// the counters share one 256-byte block.
+PlanDev carve_plan(char* base, const PlanLayout& l);
 
 struct PlanParams {
   const int* context_lens;
   const int* cu;  // nullable
   int n, Hkv, P, C, kind, max_qlen, max_tokens;
+  int Q;          // at most Q pieces per slot
   int G;          // q heads per kv head
   int rpc;        // query rows per split-kernel work item (row chunk)
   long long rows_cap;
@@ -49,7 +76,8 @@ struct SplitParams {
   const int* context_lens;
   const int* cu;  // nullable
   int num_tokens, num_blocks, Hq, Hkv, G, bs, max_blocks, n;
-  int C;            // plan capacity: CTAs [0, C*Hkv) run tasks, the rest write zero rows
+  int C;            // plan capacity: CTAs [0, C*Hkv) start on pieces [0, C), the rest write
+                    // zero rows; pieces from C on are taken by CTAs that finished theirs
   int total_rows;   // num_blocks * Hkv * bs: first out-of-range row of the cache view
   int out_f16;      // q/out element type: 1 = fp16, 0 = bf16
   int rpc;          // query rows per work item (row chunk); a multiple of 8 x row groups
@@ -96,13 +124,13 @@ cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, int smem, cudaStrea
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
-cudaError_t launch_split(const SplitParams& p, int C, int D, int kv_dtype, int row_groups,
+cudaError_t launch_split(const SplitParams& p, int D, int kv_dtype, int row_groups,
                          const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s);
-cudaError_t launch_split_d64(const SplitParams& p, int C, int kv_dtype, int row_groups,
+cudaError_t launch_split_d64(const SplitParams& p, int kv_dtype, int row_groups,
                              const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s);
-cudaError_t launch_split_d128(const SplitParams& p, int C, int kv_dtype, int row_groups,
+cudaError_t launch_split_d128(const SplitParams& p, int kv_dtype, int row_groups,
                               const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s);
-cudaError_t launch_split_d256(const SplitParams& p, int C, int kv_dtype, int row_groups,
+cudaError_t launch_split_d256(const SplitParams& p, int kv_dtype, int row_groups,
                               const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s);
 
 }  // namespace pa

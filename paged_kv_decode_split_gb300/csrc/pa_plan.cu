@@ -10,13 +10,16 @@
 // Slots are request-major; part j of a request covers tiles
 // [floor(j*nt/p), floor((j+1)*nt/p)).
 //
-// One CTA of 1024 threads, each owning 4 consecutive requests (n <= 4096):
-// two block reductions (n_act, sum S), one block scan (slot, partial-row and
-// extra-item offsets), then a slot-parallel fill that finds each slot's request
-// by binary search over the scanned offsets.  It also writes the split
-// kernel's launch order (slots by task length, longest first, by a counting
-// sort over 128 quarter-octave length classes) and the extra work items that
-// split the query rows of requests with more rows than one work item holds.
+// One CTA of 1024 threads, each owning up to 4 consecutive requests (n <= 4096):
+// block reductions (n_act, sum S, sum of tiles), one block scan (slot, piece,
+// partial-row, extra-item and merge-row offsets), then a slot-parallel fill
+// that finds each slot's request by binary search over the scanned offsets.
+// Beyond the plan itself it writes what the split kernel runs: every slot cut
+// into pieces of about the mean slot length (at most Q; Q = 1 keeps tasks
+// whole), in launch order (longest first, by a counting sort over 128
+// quarter-octave length classes), the extra work items that split the query
+// rows of requests with more rows than one work item holds, and the list of
+// rows the merge combines.
 // No allocation, no host synchronisation: it can be captured in a CUDA graph.
 #include "../../include/pa.h"
 #include "pa_device.cuh"
@@ -101,6 +104,15 @@ __device__ __forceinline__ int length_class(int len) {
   return msb * 4 + frac;
 }
 
+// Pieces for a slot of `nts` tiles when no piece may exceed `x` tiles: as
+// few as that allows, but at most Q and each at least kMinPieceTiles long.
+__device__ __forceinline__ int piece_count(int nts, int x, int Q) {
+  if (Q <= 1) return 1;
+  int q = (nts + x - 1) / x;
+  q = min(q, nts / kMinPieceTiles);
+  return max(1, min(q, Q));
+}
+
 __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
   pdl_trigger();  // the split kernel may be scheduled now; it waits for this one
   pdl_wait();     // ... and this one for whatever ran before it
@@ -110,23 +122,26 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
   int* s_ctx = s_parts + p.n;      // [n] context length
   int* s_qlen = s_ctx + p.n;       // [n] query rows
   int* s_prow = s_qlen + p.n;      // [n] first partial row
-  __shared__ long long s_red[kWarps];
+  int* s_pfirst = s_prow + p.n;    // [n] first piece, in request order
+  int* s_xfirst = s_pfirst + p.n;  // [n] first extra item
+  __shared__ long long s_red[kWarps], s_red2[kWarps];
   __shared__ int s_cnt[kWarps];
   __shared__ int s_bad;
-  __shared__ int s_scan[4][kWarps];
-  __shared__ int s_tot[4];
-  __shared__ int s_bcnt[129];  // launch-order classes 127..0, then 128 = unused slots
-  __shared__ long long s_sum, s_nact;
+  __shared__ int s_scan[5][kWarps];
+  __shared__ int s_tot[5];
+  __shared__ int s_bcnt[128];  // launch-order classes, longest first
+  __shared__ long long s_sum, s_nact, s_tiles;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = p.n;
   const int per = (n + kThreads - 1) / kThreads;  // requests per thread, <= kPer
   if (tid == 0) s_bad = 0;
+  if (tid < 128) s_bcnt[tid] = 0;
   __syncthreads();
 
-  // ---- 1. lengths, activity, validity
+  // ---- 1. lengths, activity, validity; sum S and sum of tiles of active requests
   int S[kPer], L[kPer];
-  long long my_sum = 0;
+  long long my_sum = 0, my_tiles = 0;
   int my_act = 0, my_bad = 0;
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
@@ -140,27 +155,32 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
       if (S[k] > 0 && L[k] > 0) {
         my_act += 1;
         my_sum += S[k];
+        my_tiles += (S[k] + kTile - 1) / kTile;
       }
     }
   }
   if (tid == 0 && p.cu && (p.cu[0] != 0 || p.cu[n] > p.max_tokens)) my_bad = 1;
   if (my_bad) atomicOr(&s_bad, 1);
   my_sum = warp_sum64(my_sum);
+  my_tiles = warp_sum64(my_tiles);
   int act_w = my_act;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) act_w += __shfl_xor_sync(0xffffffffu, act_w, o);
   if (lane == 0) {
     s_red[warp] = my_sum;
+    s_red2[warp] = my_tiles;
     s_cnt[warp] = act_w;
   }
   __syncthreads();
   if (tid == 0) {
-    long long a = 0, c = 0;
+    long long a = 0, t = 0, c = 0;
     for (int w = 0; w < kWarps; ++w) {
       a += s_red[w];
+      t += s_red2[w];
       c += s_cnt[w];
     }
     s_sum = a;
+    s_tiles = t;
     s_nact = c;
   }
   __syncthreads();
@@ -168,12 +188,13 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
   const long long sum_s = s_sum, n_act = s_nact;
   const long long C = p.C;
 
-  // ---- 2. partition counts, partial rows and extra row-chunk items per request
-  int parts[kPer];
-  int my_slots = 0, my_rows = 0, my_extra = 0, my_mrows = 0;
+  // ---- 2. partitions per request (the plan rule)
+  int parts[kPer], pcs[kPer], nbase[kPer], nbig[kPer];
+  int my_maxslot = 0;
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
     parts[k] = 0;
+    nbase[k] = nbig[k] = 0;
     const int r = tid * per + k;
     if (k < per && r < n && !bad && S[k] > 0 && L[k] > 0) {
       const long long tiles = (static_cast<long long>(S[k]) + kTile - 1) / kTile;
@@ -184,36 +205,86 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
       if (tiles < v) v = tiles;
       if (share < v) v = share;
       parts[k] = static_cast<int>(v);
+      // slots of a request have base or base + 1 tiles; `big` of them the latter
+      const int nt = static_cast<int>(tiles);
+      nbase[k] = nt / parts[k];
+      nbig[k] = nt - nbase[k] * parts[k];
+      my_maxslot = max(my_maxslot, nbase[k] + (nbig[k] ? 1 : 0));
     }
-    my_slots += parts[k];
-    my_rows += parts[k] >= 2 ? parts[k] * L[k] : 0;
-    my_extra += parts[k] * ((L[k] * p.G + p.rpc - 1) / p.rpc - 1);
-    my_mrows += parts[k] >= 2 ? L[k] : 0;
+  }
+  // ---- 2b. pieces.  When the slots are uneven (the longest above 5/4 of the
+  // mean), no piece may exceed x = ceil(sum tiles / (1.5 C)) tiles, which
+  // leaves about 1.5 to 2 waves of pieces -- enough for the longest-first
+  // order to even out the CTAs' finishing times; otherwise slots run whole.
+  auto pieces_of = [&](int k, int x) {
+    return parts[k] ? (parts[k] - nbig[k]) * piece_count(nbase[k], x, p.Q) +
+                          (nbig[k] ? nbig[k] * piece_count(nbase[k] + 1, x, p.Q) : 0)
+                    : 0;
+  };
+  int xcut = 1;  // longest piece, in tiles
+  if (p.Q > 1) {
+    int my_nslots = 0;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) my_nslots += parts[k];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      my_maxslot = max(my_maxslot, __shfl_xor_sync(0xffffffffu, my_maxslot, o));
+      my_nslots += __shfl_xor_sync(0xffffffffu, my_nslots, o);
+    }
+    if (lane == 0) {
+      s_cnt[warp] = my_maxslot;
+      s_scan[0][warp] = my_nslots;
+    }
+    __syncthreads();
+    int mx = 1;
+    long long ns = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      mx = max(mx, s_cnt[w]);
+      ns += s_scan[0][w];
+    }
+    xcut = mx;
+    if (4ll * mx * ns > 5ll * s_tiles)
+      xcut = static_cast<int>(min(static_cast<long long>(mx),
+                                  max(static_cast<long long>(kMinPieceTiles),
+                                      (2 * s_tiles + 3 * C - 1) / (3 * C))));
+    __syncthreads();  // s_scan is reused by the block scan below
   }
 
-  // ---- 3. exclusive offsets (slots, partial rows, extra items)
-  int inc[4] = {my_slots, my_rows, my_extra, my_mrows};
-  block_scan<4>(inc, s_scan, s_tot);
-  __syncthreads();
-  int slot0 = inc[0] - my_slots, row0 = inc[1] - my_rows, extra0 = inc[2] - my_extra;
-  int mrow0 = inc[3] - my_mrows;
-  const bool rows_overflow = static_cast<long long>(s_tot[1]) > p.rows_cap ||
-                             static_cast<long long>(s_tot[2]) > p.max_extra ||
-                             s_tot[3] > p.max_tokens;
-  if (rows_overflow) {
-    // Cannot happen for a plan built with these limits; empty the plan rather
-    // than write partial rows past the scratch.
+  // ---- 2c. pieces, partial rows, extra row-chunk items, merge rows per request
+  int my_slots = 0, my_pieces = 0, my_rows = 0, my_extra = 0, my_mrows = 0;
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) parts[k] = 0;
-    slot0 = 0;
-    row0 = 0;
-    extra0 = 0;
-    mrow0 = 0;
+  for (int k = 0; k < kPer; ++k) {
+    pcs[k] = pieces_of(k, xcut);
+    const int chunks = (L[k] * p.G + p.rpc - 1) / p.rpc;
+    my_slots += parts[k];
+    my_pieces += pcs[k];
+    my_rows += pcs[k] >= 2 ? pcs[k] * L[k] : 0;
+    my_extra += pcs[k] * (chunks > 1 ? chunks - 1 : 0);
+    my_mrows += pcs[k] >= 2 ? L[k] : 0;
   }
-  const int total_slots = rows_overflow ? 0 : s_tot[0];
-  const int total_extra = rows_overflow ? 0 : s_tot[2];
-  const int total_mrows = rows_overflow ? 0 : s_tot[3];
-  if (tid == 0 && (bad || rows_overflow)) atomicOr(p.dev.err, PA_DEVERR_PLAN_OVERFLOW);
+
+  // ---- 3. exclusive offsets (slots, pieces, partial rows, extra items, merge rows)
+  int inc[5] = {my_slots, my_pieces, my_rows, my_extra, my_mrows};
+  block_scan<5>(inc, s_scan, s_tot);
+  __syncthreads();
+  int slot0 = inc[0] - my_slots, piece0 = inc[1] - my_pieces, row0 = inc[2] - my_rows;
+  int extra0 = inc[3] - my_extra, mrow0 = inc[4] - my_mrows;
+  const bool overflow = static_cast<long long>(s_tot[2]) > p.rows_cap ||
+                        static_cast<long long>(s_tot[3]) > p.max_extra ||
+                        s_tot[4] > p.max_tokens ||
+                        static_cast<long long>(s_tot[1]) > C * p.Q;
+  if (overflow) {
+    // Cannot happen for a plan built with these limits; empty the plan rather
+    // than write past the scratch.
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) parts[k] = pcs[k] = 0;
+    slot0 = piece0 = row0 = extra0 = mrow0 = 0;
+  }
+  const int total_slots = overflow ? 0 : s_tot[0];
+  const int total_pieces = overflow ? 0 : s_tot[1];
+  const int total_extra = overflow ? 0 : s_tot[3];
+  const int total_mrows = overflow ? 0 : s_tot[4];
+  if (tid == 0 && (bad || overflow)) atomicOr(p.dev.err, PA_DEVERR_PLAN_OVERFLOW);
 
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
@@ -226,47 +297,43 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
       s_ctx[r] = S[k];
       s_qlen[r] = L[k];
       s_prow[r] = row0;
-      // extra work items: row chunks 1.. of every slot of this request
-      const int chunks = (L[k] * p.G + p.rpc - 1) / p.rpc;
-      if (chunks > 1)
-        for (int j = 0; j < parts[k]; ++j)
-          for (int c = 1; c < chunks; ++c)
-            p.dev.extra[extra0 + j * (chunks - 1) + (c - 1)] = make_int2(slot0 + j, c);
-      extra0 += parts[k] * (chunks - 1);
-      if (parts[k] >= 2)
+      s_pfirst[r] = piece0;
+      s_xfirst[r] = extra0;
+      if (pcs[k] >= 2)
         for (int i = 0; i < L[k]; ++i)
-          p.dev.mrows[mrow0 + i] = make_int4(r | ((parts[k] - 1) << 12), i, row0 + i, L[k]);
-      mrow0 += parts[k] >= 2 ? L[k] : 0;
+          p.dev.mrows[mrow0 + i] = make_int4(r | ((pcs[k] - 1) << 12), i, row0 + i, L[k]);
+      const int chunks = (L[k] * p.G + p.rpc - 1) / p.rpc;
       slot0 += parts[k];
-      row0 += parts[k] >= 2 ? parts[k] * L[k] : 0;
+      piece0 += pcs[k];
+      row0 += pcs[k] >= 2 ? pcs[k] * L[k] : 0;
+      extra0 += pcs[k] * (chunks > 1 ? chunks - 1 : 0);
+      mrow0 += pcs[k] >= 2 ? L[k] : 0;
     }
   }
-  if (tid < 129) s_bcnt[tid] = 0;
   if (tid == 0) {
     p.dev.counters[0] = total_extra;
     p.dev.counters[1] = 0;
     p.dev.counters[2] = 0;
     p.dev.counters[3] = total_mrows;
+    p.dev.counters[4] = total_pieces;
   }
   __syncthreads();
 
-  // ---- 4. slot fill (and launch-order class counts)
-  // Lanes of a warp that share a class add their count with one atomic.
-  auto warp_claim = [&](int cls) {
-    const unsigned peers = __match_any_sync(__activemask(), cls);
+  // Lanes of a warp that share a class add their count with one atomic; every
+  // lane calls this (invalid ones with valid = false).
+  auto warp_claim = [&](int cls, bool valid) {
+    const unsigned peers = __match_any_sync(0xffffffffu, valid ? cls : -1);
     const int leader = __ffs(peers) - 1;
     int base = 0;
-    if (lane == leader) base = atomicAdd(&s_bcnt[cls], __popc(peers));
-    base = __shfl_sync(peers, base, leader);
+    if (valid && lane == leader) base = atomicAdd(&s_bcnt[cls], __popc(peers));
+    base = __shfl_sync(0xffffffffu, base, leader);
     return base + __popc(peers & ((1u << lane) - 1u));
   };
-  // Task of an active slot and its launch-order class (0 = longest tasks).
-  auto slot_fill = [&](int slot) {
-    if (slot >= total_slots) {
-      p.dev.work[slot] = make_int4(-1, 0, 0, 0);
-      p.dev.part_row[slot] = -1;
-      return 128;
-    }
+  // Slot `slot` (< total_slots): its request, tile range and the pieces of
+  // the request's earlier slots.
+  struct SlotInfo { int r, tb, te, q, before; };
+  auto slot_info = [&](int slot) {
+    SlotInfo o;
     int lo = 0, hi = n;  // last r with s_first[r] <= slot (it has parts > 0)
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -275,34 +342,53 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
       else
         hi = mid;
     }
-    const int r = lo;
-    const int pr = s_parts[r];
-    const int j = slot - s_first[r];
-    const int nt = (s_ctx[r] + kTile - 1) / kTile;
-    const int tb = tile_split(j, nt, pr);
-    const int te = tile_split(j + 1, nt, pr);
-    p.dev.work[slot] = make_int4(r, tb, te, s_ctx[r]);
-    p.dev.part_row[slot] = pr >= 2 ? s_prow[r] + j * s_qlen[r] : -1;
-    const int keys = min(te * kTile, s_ctx[r]) - tb * kTile;
-    return 127 - length_class(keys);
+    o.r = lo;
+    const int pr = s_parts[lo];
+    const int j = slot - s_first[lo];
+    const int nt = (s_ctx[lo] + kTile - 1) / kTile;
+    o.tb = tile_split(j, nt, pr);
+    o.te = tile_split(j + 1, nt, pr);
+    o.q = piece_count(o.te - o.tb, xcut, p.Q);
+    const int base = nt / pr;
+    const int qlo = piece_count(base, xcut, p.Q), qhi = piece_count(base + 1, xcut, p.Q);
+    o.before = j * qlo + (o.tb - j * base) * (qhi - qlo);
+    return o;
   };
-  constexpr int kCached = 4;  // classes kept in registers for the scatter (C <= 4096)
-  int cls[kCached];
-#pragma unroll
-  for (int k = 0; k < kCached; ++k) cls[k] = -1;
-  for (int slot = tid, k = 0; slot < C; slot += kThreads, ++k) {
-    const int c = slot_fill(slot);
-    if (k < kCached) cls[k] = c;
-    warp_claim(c);
+  // Keys [kb, ke) of piece `sub` of a slot, and its launch-order class.
+  auto piece_keys = [&](const SlotInfo& o, int sub, int& kb, int& ke) {
+    const int nts = o.te - o.tb;
+    const long long t0 = o.tb + tile_split(sub, nts, o.q);
+    const long long t1 = o.tb + tile_split(sub + 1, nts, o.q);
+    kb = static_cast<int>(t0 * kTile);
+    ke = static_cast<int>(min(t1 * kTile, static_cast<long long>(s_ctx[o.r])));
+    return 127 - length_class(ke - kb);
+  };
+
+  // ---- 4. work_info (the plan's task list) and the launch-order class counts
+  for (int s0 = 0; s0 < C; s0 += kThreads) {
+    const int slot = s0 + tid;
+    const bool act = slot < total_slots;
+    SlotInfo o = {0, 0, 0, 0, 0};
+    if (act) {
+      o = slot_info(slot);
+      p.dev.work[slot] = make_int4(o.r, o.tb, o.te, s_ctx[o.r]);
+    } else if (slot < C) {
+      p.dev.work[slot] = make_int4(-1, 0, 0, 0);
+    }
+    for (int sub = 0; sub < p.Q; ++sub) {
+      const bool valid = act && sub < o.q;
+      int kb = 0, ke = 1, cls = 0;
+      if (valid) cls = piece_keys(o, sub, kb, ke);
+      warp_claim(cls, valid);
+    }
   }
   __syncthreads();
-  // ---- 5. launch order: counting sort of the slots by length class
-  if (warp == 0) {  // exclusive prefix over the 129 classes: 5 per lane, then a warp scan
-    int v[5], sum = 0;
+  // ---- 5. launch order: counting sort of the pieces by length class
+  if (warp == 0) {  // exclusive prefix over the 128 classes: 4 per lane, then a warp scan
+    int v[4], sum = 0;
 #pragma unroll
-    for (int k = 0; k < 5; ++k) {
-      const int b = lane * 5 + k;
-      v[k] = b < 129 ? s_bcnt[b] : 0;
+    for (int k = 0; k < 4; ++k) {
+      v[k] = s_bcnt[lane * 4 + k];
       sum += v[k];
     }
     int inc = sum;
@@ -313,32 +399,31 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
     }
     int pos = inc - sum;
 #pragma unroll
-    for (int k = 0; k < 5; ++k) {
-      const int b = lane * 5 + k;
-      if (b < 129) s_bcnt[b] = pos;
+    for (int k = 0; k < 4; ++k) {
+      s_bcnt[lane * 4 + k] = pos;
       pos += v[k];
     }
   }
   __syncthreads();
-  for (int slot = tid, k = 0; slot < C; slot += kThreads, ++k) {
-    int c;
-    if (k < kCached) {
-      c = cls[k];
-    } else {  // beyond the cached slots: recompute the class (C > 4096 only)
-      int lo = 0, hi = n;
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (s_first[mid] <= slot) lo = mid; else hi = mid;
-      }
-      if (slot >= total_slots) {
-        c = 128;
-      } else {
-        const int nt = (s_ctx[lo] + kTile - 1) / kTile, j = slot - s_first[lo];
-        const int tb = tile_split(j, nt, s_parts[lo]), te = tile_split(j + 1, nt, s_parts[lo]);
-        c = 127 - length_class(min(te * kTile, s_ctx[lo]) - tb * kTile);
-      }
+  for (int s0 = 0; s0 < C; s0 += kThreads) {
+    const int slot = s0 + tid;
+    const bool act = slot < total_slots;
+    SlotInfo o = {0, 0, 0, 0, 0};
+    if (act) o = slot_info(slot);
+    for (int sub = 0; sub < p.Q; ++sub) {
+      const bool valid = act && sub < o.q;
+      int kb = 0, ke = 1, cls = 0;
+      if (valid) cls = piece_keys(o, sub, kb, ke);
+      const int pos = warp_claim(cls, valid);
+      if (!valid) continue;
+      const int r = o.r;
+      const int npieces = (r + 1 < n ? s_pfirst[r + 1] : total_pieces) - s_pfirst[r];
+      const int k = o.before + sub;  // piece index within the request
+      p.dev.pieces[pos] = make_int4(r, kb, ke, npieces >= 2 ? s_prow[r] + k * s_qlen[r] : -1);
+      const int chunks = (s_qlen[r] * p.G + p.rpc - 1) / p.rpc;
+      for (int c = 1; c < chunks; ++c)
+        p.dev.extra[s_xfirst[r] + k * (chunks - 1) + (c - 1)] = make_int2(pos, c);
     }
-    p.dev.order[warp_claim(c)] = slot;
   }
 }
 
@@ -346,14 +431,14 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
   static bool attr_done = false;
-  const int smem = 5 * kMaxSeqs * static_cast<int>(sizeof(int));
+  const int smem = 7 * kMaxSeqs * static_cast<int>(sizeof(int));
   if (!attr_done) {
     cudaError_t e =
         cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  return launch_pdl(plan_kernel, dim3(1), dim3(kThreads), 5 * p.n * static_cast<int>(sizeof(int)), s, p);
+  return launch_pdl(plan_kernel, dim3(1), dim3(kThreads), 7 * p.n * static_cast<int>(sizeof(int)), s, p);
 }
 
 }  // namespace pa

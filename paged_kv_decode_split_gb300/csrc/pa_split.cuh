@@ -126,6 +126,12 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
     cta_exit();
     return;
   }
+  // CTAs past this plan's pieces leave at once when nothing else is left to take.
+  const int npieces = p.plan.counters[4];
+  if (static_cast<int>(blockIdx.x / p.Hkv) >= npieces && p.plan.counters[0] == 0) {
+    cta_exit();
+    return;
+  }
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -159,59 +165,64 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
   int it = 0;      // stages so far (producer and consumers count alike)
   int issued = 0;  // producer: stages [0, issued) were issued (a prefix: issuing stops at an abort)
 
-  // Work items: first this CTA's own (slot, kv head) in launch order -- the
-  // planner sorts slots longest first -- then, until none are left, extra row
-  // chunks of requests with many query rows, taken from a device counter.
+  // Work items: first this CTA's own (piece, kv head) in launch order -- the
+  // planner sorts pieces longest first -- then, until none are left, from one
+  // device counter: the pieces past the first C (in launch order), then the
+  // extra row chunks of requests with many query rows.
   __shared__ int s_item[4];
   for (int round = 0;; ++round) {
     __syncthreads();  // everyone has read the previous item
     if (threadIdx.x == 0) {
-      int slot = -1, hh = 0, chunk = 0, valid = 1;
+      int pos = -1, hh = 0, chunk = 0, valid = 1;
       if (round == 0) {
-        slot = p.plan.order[blockIdx.x / Hkv];
-        hh = blockIdx.x % Hkv;
+        if (static_cast<int>(blockIdx.x / Hkv) < npieces) {
+          pos = blockIdx.x / Hkv;
+          hh = blockIdx.x % Hkv;
+        }
       } else {
-        const int idx = atomicAdd(p.plan.counters + 1, 1);
-        if (idx < p.plan.counters[0] * Hkv) {
+        int idx = atomicAdd(p.plan.counters + 1, 1);
+        const int late = (npieces > p.C ? npieces - p.C : 0) * Hkv;
+        if (idx < late) {
+          pos = p.C + idx / Hkv;
+          hh = idx % Hkv;
+        } else if ((idx -= late) < p.plan.counters[0] * Hkv) {
           const int2 e = p.plan.extra[idx / Hkv];
-          slot = e.x;
+          pos = e.x;
           chunk = e.y;
           hh = idx % Hkv;
         } else {
           valid = 0;
         }
       }
-      s_item[0] = slot;
+      s_item[0] = pos;
       s_item[1] = hh;
       s_item[2] = chunk;
       s_item[3] = valid;
     }
     __syncthreads();
     if (!s_item[3]) break;
-    const int slot = s_item[0];
+    if (s_item[0] < 0) continue;  // no piece for this CTA: look for extra items
     const int h = s_item[1];
     const int chunk = s_item[2];
-    const int4 task = p.plan.work[slot];
-    const int r = task.x;
-    if (r < 0) continue;  // unused slot
+    const int4 piece = p.plan.pieces[s_item[0]];
+    const int r = piece.x;
 
-    // A plan refreshed from other lengths: the merge kernel zeroes these rows
-    // and reports it; this task does nothing.
-    const int S = task.w;
+    // A plan refreshed from other lengths: the split kernel's zero CTAs zero
+    // these rows and report it; this piece does nothing.
+    const int S = p.context_lens[r];
     const int row0 = p.cu ? p.cu[r] : r;
     const int L = p.cu ? p.cu[r + 1] - row0 : 1;
     const int2 snap = p.plan.snap[r];
-    if (snap.x != p.context_lens[r] || snap.y != L) continue;
+    if (snap.x != S || snap.y != L) continue;
 
-    const int parts = p.plan.reduce[r].y;
-    const int prow_base = p.plan.part_row[slot];
+    const int prow_base = piece.w;              // -1: write the output rows directly
     const int rows = L * G;                     // query rows of this request
     const int row_lo = chunk * p.rpc;           // this item's rows [row_lo, row_hi)
     const int row_hi = min(rows, row_lo + p.rpc);
     if (row_lo >= row_hi) continue;
     const int npass = (row_hi - row_lo + NQ - 1) / NQ;
-    const int kb = task.y * kTile;              // first key of the task
-    const int ke_task = min(task.z * kTile, S);
+    const int kb = piece.y;                     // first key of the piece
+    const int ke_task = min(piece.z, S);
 
     // Last key any row of pass `pass` may see.
     auto pass_key_end = [&](int pass) {
@@ -590,7 +601,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
       o0 *= inv; o1 *= inv; o2 *= inv; o3 *= inv;
       const int tok = n / G;
       const int hq = h * G + n % G;
-      if (parts == 1) {
+      if (prow_base < 0) {
         const int trow = row0 + tok;
         if (trow >= p.num_tokens) {
           atomicOr(p.plan.err, PA_DEVERR_PLAN_OVERFLOW);
@@ -629,7 +640,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
 }
 
 template <int D, int KVT, int WQ>
-cudaError_t launch_split_cfg(const SplitParams& p, int C, const CUtensorMap& tk,
+cudaError_t launch_split_cfg(const SplitParams& p, const CUtensorMap& tk,
                              const CUtensorMap& tv, cudaStream_t s) {
   using Cfg = SplitCfg<D, KVT, WQ>;
   auto kern = split_kernel<D, KVT, WQ>;
@@ -641,19 +652,19 @@ cudaError_t launch_split_cfg(const SplitParams& p, int C, const CUtensorMap& tk,
     attr_done = true;
   }
   const unsigned zero_ctas = static_cast<unsigned>((p.num_tokens + kZeroRows - 1) / kZeroRows);
-  return launch_pdl(kern, dim3(static_cast<unsigned>(C) * p.Hkv + zero_ctas), dim3(Cfg::THREADS),
+  return launch_pdl(kern, dim3(static_cast<unsigned>(p.C) * p.Hkv + zero_ctas), dim3(Cfg::THREADS),
                     Cfg::SMEM_BYTES, s, tk, tv, p);
 }
 
 template <int D>
-cudaError_t launch_split_d(const SplitParams& p, int C, int kv_dtype, int wq,
+cudaError_t launch_split_d(const SplitParams& p, int kv_dtype, int wq,
                            const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s) {
 #define PA_SPLIT_CASE(KVT)                                                     \
   switch (wq) {                                                                \
-    case 1: return launch_split_cfg<D, KVT, 1>(p, C, tk, tv, s);               \
-    case 2: return launch_split_cfg<D, KVT, 2>(p, C, tk, tv, s);               \
-    case 3: return launch_split_cfg<D, KVT, 3>(p, C, tk, tv, s);               \
-    default: return launch_split_cfg<D, KVT, 4>(p, C, tk, tv, s);              \
+    case 1: return launch_split_cfg<D, KVT, 1>(p, tk, tv, s);               \
+    case 2: return launch_split_cfg<D, KVT, 2>(p, tk, tv, s);               \
+    case 3: return launch_split_cfg<D, KVT, 3>(p, tk, tv, s);               \
+    default: return launch_split_cfg<D, KVT, 4>(p, tk, tv, s);              \
   }
   switch (kv_dtype) {
     case PA_BF16: PA_SPLIT_CASE(PA_BF16)

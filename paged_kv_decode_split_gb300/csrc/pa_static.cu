@@ -91,8 +91,6 @@ bool encode_cache(const void* ptr, int num_blocks, int Hkv, int bs, int D, int d
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-
 }  // namespace
 
 extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int num_q_heads,
@@ -142,56 +140,21 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
   if (budget <= 0) budget = 2 * sms;
 
   // ---- carve the static array: plan arrays, error word, partial results
-  const long long per_head = (static_cast<long long>(budget) + num_kv_heads - 1) / num_kv_heads;
-  const long long lo = per_head > num_seqs ? per_head : num_seqs;
-  const long long hi = static_cast<long long>(num_seqs) * max_partitions;
-  const long long C = hi < lo ? hi : lo;
-  long long rows_cap = C * max_query_len;
-  const long long rows_alt = static_cast<long long>(max_partitions) * num_tokens;
-  if (rows_alt < rows_cap) rows_cap = rows_alt;
-  const size_t n = static_cast<size_t>(num_seqs);
-  const size_t b_work = up256(static_cast<size_t>(C) * sizeof(int4));
-  const size_t b_prow = up256(static_cast<size_t>(C) * sizeof(int));
-  const size_t b_red = up256(n * sizeof(int2));
-  const size_t b_snap = up256(n * sizeof(int2));
-  const size_t b_err = 256;
-  const size_t b_po = up256(static_cast<size_t>(rows_cap) * num_q_heads * head_dim * 4);
-  const size_t b_pl = up256(static_cast<size_t>(rows_cap) * num_q_heads * 4);
+  // (cutting long slots into pieces needs more partial rows: drop it first)
+  pa::PlanLayout lay = pa::plan_layout(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                       max_query_len, num_tokens, max_partitions, budget, sms, true);
+  if (lay.total > PA_STATIC_SCRATCH_BYTES)
+    lay = pa::plan_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_query_len,
+                          num_tokens, max_partitions, budget, sms, false);
+  if (lay.total > PA_STATIC_SCRATCH_BYTES)
+    return PA_ERR_UNSUPPORTED;  // this batch needs more scratch than the static array holds
   const int G = num_q_heads / num_kv_heads;
   const int wq = pa::split_row_groups(max_query_len, G);
-  const int rpc = 8 * wq;
-  const long long max_extra = pa::split_max_extra(G, rpc, rows_cap, num_tokens, max_query_len);
-  const size_t b_ord = up256(static_cast<size_t>(C) * sizeof(int));
-  const size_t b_ext = up256(static_cast<size_t>(max_extra > 0 ? max_extra : 1) * sizeof(int2));
-  const size_t b_mrow = up256(static_cast<size_t>(num_tokens) * sizeof(int4));
-  if (b_work + b_prow + b_red + b_snap + b_err + b_po + b_pl + b_ord + b_ext + b_mrow >
-      PA_STATIC_SCRATCH_BYTES)
-    return PA_ERR_UNSUPPORTED;  // this batch needs more scratch than the static array holds
 
   char* base = static_cast<char*>(scratch_address(device));
   if (!base) return PA_ERR_CUDA;
-  pa::PlanDev dev;
-  char* c = base;
-  dev.work = reinterpret_cast<int4*>(c);
-  c += b_work;
-  dev.part_row = reinterpret_cast<int*>(c);
-  c += b_prow;
-  dev.reduce = reinterpret_cast<int2*>(c);
-  c += b_red;
-  dev.snap = reinterpret_cast<int2*>(c);
-  c += b_snap;
-  unsigned* own_err = reinterpret_cast<unsigned*>(c);
-  dev.counters = reinterpret_cast<int*>(c + 16);
-  c += b_err;
-  dev.part_o = reinterpret_cast<float*>(c);
-  c += b_po;
-  dev.part_lse = reinterpret_cast<float*>(c);
-  c += b_pl;
-  dev.order = reinterpret_cast<int*>(c);
-  c += b_ord;
-  dev.extra = reinterpret_cast<int2*>(c);
-  c += b_ext;
-  dev.mrows = reinterpret_cast<int4*>(c);
+  pa::PlanDev dev = pa::carve_plan(base, lay);
+  unsigned* own_err = dev.err;
   dev.err = device_errors ? reinterpret_cast<unsigned*>(device_errors) : own_err;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -210,14 +173,15 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
   pp.n = num_seqs;
   pp.Hkv = num_kv_heads;
   pp.P = max_partitions;
-  pp.C = static_cast<int>(C);
+  pp.C = static_cast<int>(lay.C);
+  pp.Q = lay.Q;
   pp.kind = kind;
   pp.max_qlen = max_query_len;
   pp.max_tokens = num_tokens;
   pp.G = G;
-  pp.rpc = rpc;
-  pp.rows_cap = rows_cap;
-  pp.max_extra = max_extra;
+  pp.rpc = lay.rpc;
+  pp.rows_cap = lay.rows_cap;
+  pp.max_extra = lay.max_extra;
   pp.dev = dev;
   if (pa::launch_plan(pp, s) != cudaSuccess) return PA_ERR_CUDA;
 
@@ -237,14 +201,14 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
   sp.bs = block_size;
   sp.max_blocks = max_blocks_per_seq;
   sp.n = num_seqs;
-  sp.C = static_cast<int>(C);
+  sp.C = static_cast<int>(lay.C);
   sp.total_rows = num_blocks * num_kv_heads * block_size;
   sp.out_f16 = q_dtype == PA_FP16 ? 1 : 0;
-  sp.rpc = rpc;
+  sp.rpc = lay.rpc;
   sp.scale_log2 = static_cast<float>(static_cast<double>(scale) * (fp8 ? k_scale : 1.0) *
                                      1.4426950408889634);
   sp.v_scale = fp8 ? v_scale : 1.0f;
-  if (pa::launch_split(sp, static_cast<int>(C), head_dim, kv_dtype, wq, tk, tv, s) != cudaSuccess)
+  if (pa::launch_split(sp, head_dim, kv_dtype, wq, tk, tv, s) != cudaSuccess)
     return PA_ERR_CUDA;
 
   pa::MergeParams mp;
