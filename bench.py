@@ -2,12 +2,17 @@
 
 One step = one pass of the whole hot path over one synthetic batch: the plan
 refresh (planner kernel), the split-KV decode kernel and the merge kernel, all
-through the C ABI.  The headline workload is the uniform decode batch (32 seqs x
-8192 context, Hq/Hkv 32/4, D 128, page 16, bf16); its 537 MB of KV per step is
-larger than the 129 MB L2, so no flush is needed between steps.
+through the C ABI, captured in a CUDA graph and replayed.  The headline workload
+is the uniform decode batch (32 seqs x 8192 context, Hq/Hkv 32/4, D 128, page
+16, bf16); its 537 MB of KV per step is larger than the 129 MB L2, so no flush
+is needed between steps.
 
 Prints one JSON line (rank 0).  `value` is the algorithmic KV-read bandwidth,
-sum_r S_r * Hkv * D * 2 (K and V) * elem_bytes per step, over the measured time.
+sum_r S_r * Hkv * D * 2 (K and V) * elem_bytes per step, over the measured step
+time; `us_per_decode_call` is the pa_decode call (split + merge, the refresh
+excluded; a graph of K calls) and `us_per_refresh` the refresh alone.  `--sweep all` adds
+one line per configuration (L2 flushed before every step) and a summary over the
+skewed batch's seeds.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
                   [--workload NAME] [--sweep]
@@ -225,78 +230,114 @@ def _run_oracle(w):
 
 # ------------------------------------------------------------ GPU timings
 
+def _graph(fn):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def _replay_ms(g, dev) -> float:
+    """Device time of one replay of g (events on the replaying stream)."""
+    cur = torch.cuda.current_stream(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(cur)
+    g.replay()
+    t1.record(cur)
+    torch.cuda.synchronize(dev)
+    return t0.elapsed_time(t1)
+
+
 def time_native(w, steps: int, warmup: int, kind=binding.PROPORTIONAL, flush: bool = False,
-                sampler: ClockSampler | None = None, world: int = 1, graph: bool = True):
-    """Device-timed steps (refresh + decode).  The K steps are captured once into
-    a CUDA graph (refresh and decode are capturable: no allocation, no host
-    synchronisation) and replayed, as a serving engine replays its decode
-    graphs; each step records its own event pair around the split kernel.
-    With flush=True every step is preceded by an L2-flushing write and timed
-    by its own event pair.  Returns (ms/step, split-kernel ms per launch, plan)."""
+                sampler: ClockSampler | None = None, world: int = 1):
+    """Graph-replayed timing of K steps, as a serving engine replays its decode
+    graphs.  A step is refresh + decode (planner, split, merge kernels).
+
+    Pass 1 (the number): the K steps captured in one CUDA graph with nothing
+    else inside, timed by an event pair around its replay.  With flush=True
+    every step is preceded by an L2 flush (write a 2xL2 buffer, then read
+    another, so that no dirty line is written back inside the timed kernels),
+    and the replay time of a graph of the K flushes alone is subtracted.
+    Pass 2: the same with K pa_decode calls alone (the plan refreshed once
+    before): the decode call time.  Pass 3 (the breakdown): the steps with
+    per-step events that the library records around the split kernel; their
+    median (an event pair between kernels costs the launch overlap, so this
+    errs long).
+
+    Returns dict(step_ms, call_ms, split_ms, split_all) and the plan."""
     dev = w.q.device
     plan = binding.plan_for(w, kind)
     out = torch.empty_like(w.q)
-    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    fa = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    fb = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    sink = torch.empty(steps, dtype=torch.float32, device=dev) if flush else None
     ev = lambda: torch.cuda.Event(enable_timing=True)
-    pairs = [(ev(), ev()) for _ in range(steps)]
-    step_ev = [(ev(), ev()) for _ in range(steps)] if flush else None
+    splits = [(ev(), ev()) for _ in range(steps)]
 
-    def step():
-        plan.refresh(w.context_lens, w.cu_query_lens)
-        binding.decode_workload(plan, w, out=out)
+    def flush_l2(i):
+        fa.zero_()
+        torch.sum(fb, dim=0, out=sink[i])
 
-    def body(stream):
-        for i, (a, b) in enumerate(pairs):
+    def body(events: bool, work: bool = True, refresh: bool = True):
+        for i in range(steps):
             if flush:
-                flush_buf.zero_()
-                step_ev[i][0].record(stream)
-            plan.set_split_events(a, b)
-            step()
-            if flush:
-                step_ev[i][1].record(stream)
+                flush_l2(i)
+            if not work:
+                continue
+            if events:
+                plan.set_split_events(*splits[i])
+            if refresh:
+                plan.refresh(w.context_lens, w.cu_query_lens)
+            binding.decode_workload(plan, w, out=out)
+        plan.set_split_events(None, None)
 
     cur = torch.cuda.current_stream(dev)
     for _ in range(max(warmup, 3)):
-        step()
-    for a, b in pairs:  # materialise the CUDA events before handing them to the ABI
+        plan.refresh(w.context_lens, w.cu_query_lens)
+        binding.decode_workload(plan, w, out=out)
+    for a, b in splits:  # materialise the CUDA events before handing them to the ABI
         a.record(cur)
         b.record(cur)
-    if step_ev:
-        for a, b in step_ev:
-            a.record(cur)
-            b.record(cur)
     torch.cuda.synchronize(dev)
-    g = None
-    if graph:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            body(torch.cuda.current_stream(dev))
-        plan.set_split_events(None, None)
-        g.replay()  # warm replay
-        torch.cuda.synchronize(dev)
+    g_plain = _graph(lambda: body(False))
+    g_call = _graph(lambda: body(False, refresh=False))
+    g_flush = _graph(lambda: body(False, work=False)) if flush else None
+    g_events = _graph(lambda: body(True))
+    g_plain.replay()
+    torch.cuda.synchronize(dev)
     barrier(world)
     torch.cuda.synchronize(dev)
-    t0, t1 = ev(), ev()
     if sampler:
         sampler.start()
-    t0.record(cur)
-    if g is not None:
-        g.replay()
-    else:
-        body(cur)
-    t1.record(cur)
-    torch.cuda.synchronize(dev)
+    total = _replay_ms(g_plain, dev)
     if sampler:
         sampler.stop()
     barrier(world)
-    plan.set_split_events(None, None)
-    if flush:
-        ms = statistics.median(a.elapsed_time(b) for a, b in step_ev)
-    else:
-        ms = t0.elapsed_time(t1) / steps
-    split_ms = statistics.mean(a.elapsed_time(b) for a, b in pairs)
+    g_call.replay()
+    torch.cuda.synchronize(dev)
+    calls = _replay_ms(g_call, dev)
+    if g_flush is not None:
+        fl = _replay_ms(g_flush, dev)
+        total -= fl
+        calls -= fl
+    g_events.replay()
+    torch.cuda.synchronize(dev)
+    split_all = [a.elapsed_time(b) for a, b in splits]
+    del g_plain, g_call, g_flush, g_events
+    return {"step_ms": total / steps, "call_ms": calls / steps,
+            "split_ms": statistics.median(split_all), "split_all": split_all}, plan
+
+
+def time_refresh(w, reps: int = 100) -> float:
+    """µs per plan refresh: a graph of `reps` refreshes, replayed."""
+    plan = binding.plan_for(w)
+    plan.refresh(w.context_lens, w.cu_query_lens)
+    torch.cuda.synchronize()
+    g = _graph(lambda: [plan.refresh(w.context_lens, w.cu_query_lens) for _ in range(reps)])
+    g.replay()
+    ms = _replay_ms(g, w.q.device)
     del g
-    return ms, split_ms, plan
+    return ms * 1e3 / reps
 
 
 def time_e2e(w, steps: int, warmup: int):
@@ -352,32 +393,40 @@ def run_native(args, world, rank, local):
     w = wl.CONFIGS[args.workload](0, dev)
     kv_bytes = w.kv_bytes()
     sampler = ClockSampler(dev) if rank == 0 else None
-    ms, split_ms, plan = time_native(w, args.steps, args.warmup, sampler=sampler, world=world)
-    ms = max_over_ranks(ms, world)
+    t, plan = time_native(w, args.steps, args.warmup, sampler=sampler, world=world)
+    ms = max_over_ranks(t["step_ms"], world)
     info = plan.info()
     clocks = sampler.close() if sampler else None
-    ms_u, split_u, plan_u = time_native(w, args.steps, args.warmup, kind=binding.UNIFORM)
+    tu, _ = time_native(w, args.steps, args.warmup, kind=binding.UNIFORM)
+    refresh_us = time_refresh(w)
     e2e_ms, h2d, d2h = time_e2e(w, args.steps, args.warmup)
     e2e_ms = max_over_ranks(e2e_ms, world)
     peaks = measured_peaks()
     peak = peaks.get("hbm_gbs")
     peak_kind = "measured" if peak else "fallback"
     peak = peak or 6800.0
+    split_ms = t["split_ms"]
     achieved = kv_bytes / (split_ms * 1e-3) / 1e9
     traffic = ncu_traffic(args.workload)
     line = {
         "metric": METRIC, "value": round(world * kv_bytes / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(ms, 5), "us_per_decode_call": round(ms * 1e3, 2),
+        "ms_per_step": round(ms, 5),
+        "us_per_decode_call": round(t["call_ms"] * 1e3, 2),
+        "decode_call_gbs": round(kv_bytes / (t["call_ms"] * 1e-3) / 1e9, 1),
+        "us_per_refresh": round(refresh_us, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": workload_dtype(w), "data": "synthetic (seeded N(0,1) q/K/V, random page order)",
         "config": {"workload": DESCRIBE[args.workload], "name": args.workload,
                    "kv_bytes_per_step": kv_bytes, "plan": "proportional",
                    "budget": info["budget"], "capacity": info["capacity"],
                    "max_partitions": info["max_partitions"],
+                   "step": "plan refresh + pa_decode (split-KV kernel + merge kernel)",
                    "l2": "inputs larger than L2 (no flush)" if kv_bytes > L2_BYTES
                    else "not flushed: inputs fit in L2",
-                   "timing": "K steps captured once in a CUDA graph and replayed",
+                   "timing": "K steps captured once in a CUDA graph and replayed; decode "
+                             "calls alone likewise; split time: median of per-step events "
+                             "in a third replay",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -385,7 +434,10 @@ def run_native(args, world, rank, local):
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "kernel_sha": split_kernel_sha()},
-        "plan_ab": {"proportional_us": round(ms * 1e3, 2), "uniform_us": round(ms_u * 1e3, 2)},
+        "plan_ab": {"proportional_us_per_step": round(ms * 1e3, 2),
+                    "uniform_us_per_step": round(tu["step_ms"] * 1e3, 2),
+                    "proportional_split_us": round(split_ms * 1e3, 2),
+                    "uniform_split_us": round(tu["split_ms"] * 1e3, 2)},
         "e2e": {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4)},
@@ -402,12 +454,19 @@ def run_native(args, world, rank, local):
         sweep(args)
 
 
+def _pct(xs, q):
+    xs = sorted(xs)
+    return xs[min(len(xs) - 1, int(round(q * (len(xs) - 1))))]
+
+
 def sweep(args):
-    """One line per configuration: proportional vs uniform plan on the same kernel,
-    L2 flushed between steps, median step time."""
+    """One line per configuration (and skewed seed): proportional vs uniform
+    plan on the same kernel, L2 flushed before every step, graph-replayed;
+    then a summary line over the skewed seeds (median, p90)."""
     dev = torch.device("cuda", torch.cuda.current_device())
-    names = [n for n in wl.CONFIGS if n != "tiny"] if args.sweep == "all" else \
-        args.sweep.split(",")
+    names = list(wl.CONFIGS) if args.sweep == "all" else args.sweep.split(",")
+    peak = measured_peaks().get("hbm_gbs", 6800.0)
+    skew = []
     for name in names:
         seeds = range(args.seeds) if name == "skewed" else [0]
         for seed in seeds:
@@ -418,35 +477,37 @@ def sweep(args):
                                          max(1, min(w.context_lens.tolist())), 1)}
             for kind, tag in ((binding.PROPORTIONAL, "proportional"),
                               (binding.UNIFORM, "uniform")):
-                ms, split_ms, plan = time_native(w, args.steps, args.warmup, kind=kind, flush=True,
-                                                 graph=False)
+                t, plan = time_native(w, args.steps, args.warmup, kind=kind, flush=True)
                 _, red = plan.download()
-                res[tag] = {"us_per_call": round(ms * 1e3, 2),
-                            "split_us": round(split_ms * 1e3, 2),
-                            "kv_gbs": round(kv / (ms * 1e-3) / 1e9, 1),
-                            "split_gbs": round(kv / (split_ms * 1e-3) / 1e9, 1),
-                            "frac_of_measured": round(kv / (split_ms * 1e-3) / 1e9 /
-                                                      measured_peaks().get("hbm_gbs", 6800.0), 4),
+                res[tag] = {"us_per_step": round(t["step_ms"] * 1e3, 2),
+                            "us_per_decode_call": round(t["call_ms"] * 1e3, 2),
+                            "split_us": round(t["split_ms"] * 1e3, 2),
+                            "call_gbs": round(kv / (t["call_ms"] * 1e-3) / 1e9, 1),
+                            "split_gbs": round(kv / (t["split_ms"] * 1e-3) / 1e9, 1),
+                            "split_frac_of_measured": round(kv / (t["split_ms"] * 1e-3) / 1e9 / peak, 4),
+                            "split_frac_of_8tbs": round(kv / (t["split_ms"] * 1e-3) / 8e12, 4),
                             "tasks": int(red[:, 1].sum()), "max_parts": int(red[:, 1].max())}
-            # refresh alone: 100 refreshes captured in a graph, replayed
-            plan = binding.plan_for(w)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            plan.refresh(w.context_lens, w.cu_query_lens)
-            torch.cuda.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                for _ in range(100):
-                    plan.refresh(w.context_lens, w.cu_query_lens)
-            g.replay()
-            a.record()
-            g.replay()
-            b.record()
-            torch.cuda.synchronize()
-            res["refresh_us"] = round(a.elapsed_time(b) * 10, 2)
-            del g
+            res["refresh_us"] = round(time_refresh(w), 2)
             print(json.dumps(res), flush=True)
+            if name == "skewed":
+                skew.append(res)
             del w
             torch.cuda.empty_cache()
+    if skew:
+        sp = [r["proportional"]["split_us"] for r in skew]
+        cp = [r["proportional"]["us_per_decode_call"] for r in skew]
+        fr = [r["proportional"]["split_frac_of_measured"] for r in skew]
+        su = [r["uniform"]["split_us"] / r["proportional"]["split_us"] for r in skew]
+        mm = [r["max_over_min"] for r in skew]
+        print(json.dumps({"sweep": "skewed_summary", "seeds": len(skew),
+                          "max_over_min": {"min": min(mm), "median": _pct(mm, 0.5), "max": max(mm)},
+                          "split_us": {"median": _pct(sp, 0.5), "p90": _pct(sp, 0.9)},
+                          "decode_call_us": {"median": _pct(cp, 0.5), "p90": _pct(cp, 0.9)},
+                          "split_frac_of_measured": {"median": _pct(fr, 0.5), "p10": _pct(fr, 0.1),
+                                                     "min": min(fr)},
+                          "uniform_over_proportional_split": {"median": round(_pct(su, 0.5), 2),
+                                                              "min": round(min(su), 2)}}),
+              flush=True)
 
 
 def run_reference(args, world, rank, local):
@@ -484,12 +545,12 @@ def run_reference(args, world, rank, local):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", choices=list(wl.CONFIGS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--sweep", default="", help="'all' or comma list: extra per-config lines")
-    ap.add_argument("--seeds", type=int, default=3, help="skewed seeds in the sweep")
+    ap.add_argument("--seeds", type=int, default=20, help="skewed seeds in the sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     world, rank, local = dist_setup()

@@ -223,6 +223,11 @@ int pa_plan_read_errors(pa_plan* plan, uint32_t* errors, int clear, void* stream
  * caller owns them).  NULL, NULL turns it off. */
 int pa_plan_set_split_events(pa_plan* plan, void* start_event, void* stop_event);
 
+/* Profiling hook: as pa_plan_set_split_events, but the events bracket the
+ * whole pa_decode call (split-KV kernel and merge kernel).  Inside a stream
+ * capture both hooks record external events, which fire on every replay. */
+int pa_plan_set_call_events(pa_plan* plan, void* start_event, void* stop_event);
+
 /* Releases the plan's device buffers and the plan (NULL is a no-op).  The
  * caller must ensure no enqueued work still uses the plan. */
 int pa_plan_destroy(pa_plan* plan);

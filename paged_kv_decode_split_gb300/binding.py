@@ -66,11 +66,13 @@ def load() -> ctypes.CDLL:
     lib.pa_plan_download.argtypes = [P, P, P, P]
     lib.pa_plan_read_errors.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), i32, P]
     lib.pa_plan_set_split_events.argtypes = [P, P, P]
+    lib.pa_plan_set_call_events.argtypes = [P, P, P]
     lib.pa_plan_destroy.argtypes = [P]
     lib.pa_status_string.argtypes = [i32]
     lib.pa_status_string.restype = ctypes.c_char_p
     for name in ("pa_plan_build", "pa_plan_refresh", "pa_decode", "pa_plan_info",
                  "pa_plan_download", "pa_plan_read_errors", "pa_plan_set_split_events",
+                 "pa_plan_set_call_events",
                  "pa_plan_destroy"):
         getattr(lib, name).restype = i32
     _lib = lib
@@ -186,6 +188,11 @@ class Plan:
         a = None if start is None else ctypes.c_void_p(start.cuda_event)
         b = None if stop is None else ctypes.c_void_p(stop.cuda_event)
         _check(load().pa_plan_set_split_events(self._h, a, b), "pa_plan_set_split_events")
+
+    def set_call_events(self, start=None, stop=None):
+        a = None if start is None else ctypes.c_void_p(start.cuda_event)
+        b = None if stop is None else ctypes.c_void_p(stop.cuda_event)
+        _check(load().pa_plan_set_call_events(self._h, a, b), "pa_plan_set_call_events")
 
     # -- decode
     def decode(self, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,

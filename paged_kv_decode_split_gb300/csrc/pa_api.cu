@@ -68,7 +68,8 @@ struct pa_plan {
   void* mem;
   long long bytes;
   int refreshed;  // 0: never; 1: without cu_query_lens; 2: with cu_query_lens
-  cudaEvent_t ev_start, ev_stop;
+  cudaEvent_t ev_start, ev_stop;      // around the split kernel
+  cudaEvent_t ev_call0, ev_call1;     // around the whole decode call
   TmapSlot tmaps[8];
   int tmap_next;
 };
@@ -297,6 +298,7 @@ int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_q_heads, int
   pl->bytes = static_cast<long long>(total);
   pl->refreshed = 0;
   pl->ev_start = pl->ev_stop = nullptr;
+  pl->ev_call0 = pl->ev_call1 = nullptr;
   pl->tmap_next = 0;
   *plan = pl;
   return PA_OK;
@@ -402,6 +404,7 @@ int pa_decode(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int num
                 ? cudaEventRecordWithFlags(e, s, cudaEventRecordExternal)
                 : cudaEventRecord(e, s)) == cudaSuccess;
   };
+  if (plan->ev_call0 && !record(plan->ev_call0)) return PA_ERR_CUDA;
   if (plan->ev_start && !record(plan->ev_start)) return PA_ERR_CUDA;
   if (pa::launch_split(sp, head_dim, kv_dtype, wq, tk, tv, s) != cudaSuccess)
     return PA_ERR_CUDA;
@@ -420,6 +423,7 @@ int pa_decode(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int num
   const long long pairs = static_cast<long long>(num_tokens) * num_q_heads;
   mp.grid = static_cast<int>(pairs < 8ll * plan->sms ? pairs : 8ll * plan->sms);
   if (pa::launch_merge(mp, s) != cudaSuccess) return PA_ERR_CUDA;
+  if (plan->ev_call1 && !record(plan->ev_call1)) return PA_ERR_CUDA;
   return PA_OK;
 }
 
@@ -472,6 +476,14 @@ int pa_plan_set_split_events(pa_plan* plan, void* start_event, void* stop_event)
   if ((start_event == nullptr) != (stop_event == nullptr)) return PA_ERR_INVALID_ARG;
   plan->ev_start = static_cast<cudaEvent_t>(start_event);
   plan->ev_stop = static_cast<cudaEvent_t>(stop_event);
+  return PA_OK;
+}
+
+int pa_plan_set_call_events(pa_plan* plan, void* start_event, void* stop_event) {
+  if (!plan) return PA_ERR_INVALID_ARG;
+  if ((start_event == nullptr) != (stop_event == nullptr)) return PA_ERR_INVALID_ARG;
+  plan->ev_call0 = static_cast<cudaEvent_t>(start_event);
+  plan->ev_call1 = static_cast<cudaEvent_t>(stop_event);
   return PA_OK;
 }
 

@@ -68,5 +68,6 @@ def test_null_handles(lib):
         binding.PA_ERR_INVALID_ARG
     assert lib.pa_plan_download(None, None, None, None) == binding.PA_ERR_INVALID_ARG
     assert lib.pa_plan_set_split_events(None, None, None) == binding.PA_ERR_INVALID_ARG
+    assert lib.pa_plan_set_call_events(None, None, None) == binding.PA_ERR_INVALID_ARG
     assert lib.pa_decode(None, None, 0, 1, 8, 64, None, None, 0, 1.0, 1.0, 1, 2, 16, None, 1,
                          None, None, 1, 1.0, None, None) == binding.PA_ERR_INVALID_ARG

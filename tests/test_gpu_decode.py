@@ -262,6 +262,33 @@ def test_graph_capture_refresh_and_decode(dev):
     assert plan.read_errors() == 0
 
 
+def test_profiling_events_bracket_the_call_and_the_split(dev):
+    """The call events enclose the split events, eagerly and in a replayed graph."""
+    w = batch(dev, [3000, 800, 64, 2000], H=(8, 2), D=128, seed=11)
+    plan = binding.plan_for(w)
+    out = torch.empty_like(w.q)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    for e in ev:
+        e.record()
+    plan.refresh(w.context_lens)
+    plan.set_call_events(ev[1], ev[4])
+    plan.set_split_events(ev[2], ev[3])
+    ev[0].record()
+    binding.decode_workload(plan, w, out=out)
+    torch.cuda.synchronize()
+    call, split = ev[1].elapsed_time(ev[4]), ev[2].elapsed_time(ev[3])
+    assert 0 < split <= call and ev[0].elapsed_time(ev[1]) >= 0
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        binding.decode_workload(plan, w, out=out)
+    plan.set_call_events(None, None)
+    plan.set_split_events(None, None)
+    g.replay()
+    torch.cuda.synchronize()
+    assert 0 < ev[2].elapsed_time(ev[3]) <= ev[1].elapsed_time(ev[4])
+    assert max_diff(out, oracle_decode(w.to("cpu"))) <= TOL["bf16"]
+
+
 # ------------------------------------------------ full-size configurations
 
 def _sampled(w, out, requests):
