@@ -10,7 +10,8 @@
 // Slots are request-major; part j of a request covers tiles
 // [floor(j*nt/p), floor((j+1)*nt/p)).
 //
-// One CTA of 1024 threads, each owning up to 4 consecutive requests (n <= 4096):
+// One CTA (128 threads up to 128 requests, else 1024), each thread owning up
+// to 4 consecutive requests (n <= 4096):
 // block reductions (n_act, sum S, sum of tiles), one block scan (slot, piece,
 // partial-row, extra-item and merge-row offsets), then a slot-parallel fill
 // that finds each slot's request by binary search over the scanned offsets.
@@ -29,9 +30,7 @@ namespace pa {
 
 namespace {
 
-constexpr int kThreads = 1024;
-constexpr int kPer = kMaxSeqs / kThreads;  // requests per thread
-constexpr int kWarps = kThreads / 32;
+constexpr int kPer = 4;  // requests per thread at most: n <= 4 * kThreads
 
 __device__ __forceinline__ long long warp_sum64(long long v) {
 #pragma unroll
@@ -41,8 +40,9 @@ __device__ __forceinline__ long long warp_sum64(long long v) {
 
 // Inclusive block scan of K 32-bit counters (a warp-level pass, then one pass
 // over the warp totals); block totals land in tot[0..K-1].
-template <int K>
-__device__ void block_scan(int (&v)[K], int (*sw)[kWarps], int* tot) {
+template <int kThreads, int K>
+__device__ void block_scan(int (&v)[K], int (*sw)[kThreads / 32], int* tot) {
+  constexpr int kWarps = kThreads / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -113,7 +113,12 @@ __device__ __forceinline__ int piece_count(int nts, int x, int Q) {
   return max(1, min(q, Q));
 }
 
+// kThreads: 128 for batches of up to 128 requests (fewer idle warps on the
+// one SM the planner runs on), 1024 up to 4096.
+template <int kThreads>
 __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
+  constexpr int kWarps = kThreads / 32;
+  static_assert(kWarps <= 32, "warp totals are reduced by one warp, one per lane");
   pdl_trigger();  // the split kernel may be scheduled now; it waits for this one
   pdl_wait();     // ... and this one for whatever ran before it
   extern __shared__ int s_dyn[];
@@ -130,7 +135,6 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
   __shared__ int s_scan[5][kWarps];
   __shared__ int s_tot[5];
   __shared__ int s_bcnt[128];  // launch-order classes, longest first
-  __shared__ long long s_sum, s_nact, s_tiles;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = p.n;
@@ -172,20 +176,12 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
     s_cnt[warp] = act_w;
   }
   __syncthreads();
-  if (tid == 0) {
-    long long a = 0, t = 0, c = 0;
-    for (int w = 0; w < kWarps; ++w) {
-      a += s_red[w];
-      t += s_red2[w];
-      c += s_cnt[w];
-    }
-    s_sum = a;
-    s_tiles = t;
-    s_nact = c;
-  }
-  __syncthreads();
+  // every warp reduces the warp totals itself: no second barrier
+  const long long sum_s = warp_sum64(lane < kWarps ? s_red[lane] : 0);
+  const long long sum_tiles = warp_sum64(lane < kWarps ? s_red2[lane] : 0);
+  long long n_act = lane < kWarps ? s_cnt[lane] : 0;
+  n_act = warp_sum64(n_act);
   const bool bad = s_bad != 0;
-  const long long sum_s = s_sum, n_act = s_nact;
   const long long C = p.C;
 
   // ---- 2. partitions per request (the plan rule)
@@ -222,6 +218,7 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
                     : 0;
   };
   int xcut = 1;  // longest piece, in tiles
+  int qmax = 1;  // most pieces of one slot
   if (p.Q > 1) {
     int my_nslots = 0;
 #pragma unroll
@@ -231,22 +228,23 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
       my_maxslot = max(my_maxslot, __shfl_xor_sync(0xffffffffu, my_maxslot, o));
       my_nslots += __shfl_xor_sync(0xffffffffu, my_nslots, o);
     }
+    __syncthreads();  // s_cnt of phase 1 has been read by every warp
     if (lane == 0) {
       s_cnt[warp] = my_maxslot;
       s_scan[0][warp] = my_nslots;
     }
     __syncthreads();
-    int mx = 1;
-    long long ns = 0;
-    for (int w = 0; w < kWarps; ++w) {
-      mx = max(mx, s_cnt[w]);
-      ns += s_scan[0][w];
-    }
+    int mx = max(1, lane < kWarps ? s_cnt[lane] : 0);
+    long long ns = lane < kWarps ? s_scan[0][lane] : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    ns = warp_sum64(ns);
     xcut = mx;
-    if (4ll * mx * ns > 5ll * s_tiles)
+    if (4ll * mx * ns > 5ll * sum_tiles)
       xcut = static_cast<int>(min(static_cast<long long>(mx),
                                   max(static_cast<long long>(kMinPieceTiles),
-                                      (2 * s_tiles + 3 * C - 1) / (3 * C))));
+                                      (2 * sum_tiles + 3 * C - 1) / (3 * C))));
+    qmax = piece_count(mx, xcut, p.Q);
     __syncthreads();  // s_scan is reused by the block scan below
   }
 
@@ -265,7 +263,7 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
 
   // ---- 3. exclusive offsets (slots, pieces, partial rows, extra items, merge rows)
   int inc[5] = {my_slots, my_pieces, my_rows, my_extra, my_mrows};
-  block_scan<5>(inc, s_scan, s_tot);
+  block_scan<kThreads, 5>(inc, s_scan, s_tot);
   __syncthreads();
   int slot0 = inc[0] - my_slots, piece0 = inc[1] - my_pieces, row0 = inc[2] - my_rows;
   int extra0 = inc[3] - my_extra, mrow0 = inc[4] - my_mrows;
@@ -365,7 +363,9 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
   };
 
   // ---- 4. work_info (the plan's task list) and the launch-order class counts
-  for (int s0 = 0; s0 < C; s0 += kThreads) {
+  constexpr int kCached = 4;  // slots per thread kept for phase 5 (C <= 4096)
+  SlotInfo cache[kCached];
+  for (int s0 = 0, it = 0; s0 < C; s0 += kThreads, ++it) {
     const int slot = s0 + tid;
     const bool act = slot < total_slots;
     SlotInfo o = {0, 0, 0, 0, 0};
@@ -375,7 +375,10 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
     } else if (slot < C) {
       p.dev.work[slot] = make_int4(-1, 0, 0, 0);
     }
-    for (int sub = 0; sub < p.Q; ++sub) {
+#pragma unroll
+    for (int c = 0; c < kCached; ++c)
+      if (c == it) cache[c] = o;
+    for (int sub = 0; sub < qmax; ++sub) {
       const bool valid = act && sub < o.q;
       int kb = 0, ke = 1, cls = 0;
       if (valid) cls = piece_keys(o, sub, kb, ke);
@@ -405,12 +408,18 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
     }
   }
   __syncthreads();
-  for (int s0 = 0; s0 < C; s0 += kThreads) {
+  for (int s0 = 0, it = 0; s0 < C; s0 += kThreads, ++it) {
     const int slot = s0 + tid;
     const bool act = slot < total_slots;
     SlotInfo o = {0, 0, 0, 0, 0};
-    if (act) o = slot_info(slot);
-    for (int sub = 0; sub < p.Q; ++sub) {
+    if (it < kCached) {
+#pragma unroll
+      for (int c = 0; c < kCached; ++c)
+        if (c == it) o = cache[c];
+    } else if (act) {
+      o = slot_info(slot);
+    }
+    for (int sub = 0; sub < qmax; ++sub) {
       const bool valid = act && sub < o.q;
       int kb = 0, ke = 1, cls = 0;
       if (valid) cls = piece_keys(o, sub, kb, ke);
@@ -434,11 +443,15 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
   const int smem = 7 * kMaxSeqs * static_cast<int>(sizeof(int));
   if (!attr_done) {
     cudaError_t e =
-        cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaFuncSetAttribute(plan_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(plan_kernel<1024>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  return launch_pdl(plan_kernel, dim3(1), dim3(kThreads), 7 * p.n * static_cast<int>(sizeof(int)), s, p);
+  const int dyn = 7 * p.n * static_cast<int>(sizeof(int));
+  if (p.n <= 128) return launch_pdl(plan_kernel<128>, dim3(1), dim3(128), dyn, s, p);
+  return launch_pdl(plan_kernel<1024>, dim3(1), dim3(1024), dyn, s, p);
 }
 
 }  // namespace pa
