@@ -33,8 +33,9 @@ struct PlanDev {
                     // one piece and its CTA writes the output row}
   int2* extra;      // [max_extra] (piece position, row chunk >= 1) for requests whose
                     // query rows exceed one work item
-  int* counters;    // [0] extra items, [1] next extra item (x Hkv), [2] split CTAs done,
-                    // [3] rows to merge, [4] pieces
+  int* counters;    // [0] extra items, [1] next late piece or extra item (x Hkv; reset by
+                    // the planner and by the merge kernel), [2] unused, [3] rows to
+                    // merge, [4] pieces
   int4* mrows;      // [max_tokens] one entry per row of a request with several pieces:
                     // {r | (pieces - 1) << 12, token, partial row of piece 0, L}
                     // (piece k's partial row is that + k * L)

@@ -40,6 +40,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
   const float NEG_INF = -__int_as_float(0x7f800000);
   pdl_trigger();
   pdl_wait();  // the split kernel's partials are complete
+  // The split kernel is done with its work counter: reset it for the next decode.
+  if (blockIdx.x == 0 && threadIdx.x == 0) p.plan.counters[1] = 0;
   const int tid = threadIdx.x, u = tid / UL, ul = tid % UL;
   const int Hq = p.Hq;
   const int total = p.plan.counters[3] * Hq;

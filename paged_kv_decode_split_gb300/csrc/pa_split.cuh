@@ -107,30 +107,28 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
     prefetch_tmap(&tmv);
   }
   pdl_wait();  // the plan (and everything before this kernel) is complete
-  // Every CTA counts itself out; the last one resets the work counters for the
-  // next decode on this plan.
+  // (The work counter this kernel takes items from is reset by the merge
+  // kernel, which runs after it.)
   auto cta_exit = [&]() {
     __syncthreads();
     pdl_trigger();
-    if (threadIdx.x == 0) {
-      __threadfence();
-      const unsigned gone = atomicAdd(reinterpret_cast<unsigned*>(p.plan.counters + 2), 1u);
-      if (gone == gridDim.x - 1) {
-        p.plan.counters[1] = 0;
-        p.plan.counters[2] = 0;
-      }
-    }
   };
   if (blockIdx.x >= static_cast<unsigned>(p.C * p.Hkv)) {  // zero-row CTA
     zero_rows<D>(p, blockIdx.x - p.C * p.Hkv, warp, Cfg::THREADS / 32, lane);
     cta_exit();
     return;
   }
-  // CTAs past this plan's pieces leave at once when nothing else is left to take.
-  const int npieces = p.plan.counters[4];
-  if (static_cast<int>(blockIdx.x / p.Hkv) >= npieces && p.plan.counters[0] == 0) {
-    cta_exit();
-    return;
+  // This CTA's first piece, read together with the counts it depends on.
+  __shared__ int s_item[4];
+  __shared__ int4 s_rec;
+  __shared__ int s_npieces, s_nextra;
+  if (threadIdx.x == 0) {
+    const int npieces = p.plan.counters[4];
+    const int nextra = p.plan.counters[0];
+    const int4 rec = p.plan.pieces[blockIdx.x / p.Hkv];  // < C: inside the array
+    s_npieces = npieces;
+    s_nextra = nextra;
+    s_rec = rec;
   }
 
   extern __shared__ uint8_t smem_raw[];
@@ -169,23 +167,27 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
   // planner sorts pieces longest first -- then, until none are left, from one
   // device counter: the pieces past the first C (in launch order), then the
   // extra row chunks of requests with many query rows.
-  __shared__ int s_item[4];
   for (int round = 0;; ++round) {
     __syncthreads();  // everyone has read the previous item
     if (threadIdx.x == 0) {
+      const int npieces = s_npieces, nextra = s_nextra;
+      const int late = (npieces > p.C ? npieces - p.C : 0) * Hkv;
       int pos = -1, hh = 0, chunk = 0, valid = 1;
       if (round == 0) {
         if (static_cast<int>(blockIdx.x / Hkv) < npieces) {
           pos = blockIdx.x / Hkv;
           hh = blockIdx.x % Hkv;
+        } else if (late == 0 && nextra == 0) {
+          valid = 0;  // nothing for this CTA, now or later
         }
+      } else if (late == 0 && nextra == 0) {
+        valid = 0;
       } else {
         int idx = atomicAdd(p.plan.counters + 1, 1);
-        const int late = (npieces > p.C ? npieces - p.C : 0) * Hkv;
         if (idx < late) {
           pos = p.C + idx / Hkv;
           hh = idx % Hkv;
-        } else if ((idx -= late) < p.plan.counters[0] * Hkv) {
+        } else if ((idx -= late) < nextra * Hkv) {
           const int2 e = p.plan.extra[idx / Hkv];
           pos = e.x;
           chunk = e.y;
@@ -193,6 +195,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
         } else {
           valid = 0;
         }
+        if (pos >= 0) s_rec = p.plan.pieces[pos];
       }
       s_item[0] = pos;
       s_item[1] = hh;
@@ -204,8 +207,19 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
     if (s_item[0] < 0) continue;  // no piece for this CTA: look for extra items
     const int h = s_item[1];
     const int chunk = s_item[2];
-    const int4 piece = p.plan.pieces[s_item[0]];
+    const int4 piece = s_rec;
     const int r = piece.x;
+
+    // Block-table window of the piece's first pages, loaded by the producer
+    // alongside the length checks (entries past the piece's end are not used).
+    int bt_cur = -1, bt_nxt = -1;
+    if (warp == 0) {
+      const int* bt = p.block_tables + static_cast<size_t>(r) * p.max_blocks;
+      const int np = min((piece.z + p.bs - 1) / p.bs, p.max_blocks);
+      const int w0 = piece.y / p.bs;
+      bt_cur = (w0 + lane < np) ? __ldg(bt + w0 + lane) : -1;
+      bt_nxt = (w0 + 32 + lane < np) ? __ldg(bt + w0 + 32 + lane) : -1;
+    }
 
     // A plan refreshed from other lengths: the split kernel's zero CTAs zero
     // these rows and report it; this piece does nothing.
@@ -244,8 +258,8 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
       const int ke = pass_key_end(pass);
       const int nst = ke > kb ? (ke - kb + Cfg::KS - 1) / Cfg::KS : 0;
       int win = kb / bs;  // block-table entries [win, win + 64) live in cur / nxt
-      int cur = bt_at(win + lane);
-      int nxt = bt_at(win + 32 + lane);
+      int cur = bt_cur;
+      int nxt = bt_nxt;
       for (int s = 0; s < nst; ++s, ++it) {
         const int buf = it % Cfg::NS;
         if (aborted()) continue;
