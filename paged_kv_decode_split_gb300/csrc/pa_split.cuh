@@ -119,8 +119,10 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
     return;
   }
   // This CTA's first piece, read together with the counts it depends on.
-  __shared__ int s_item[4];
-  __shared__ int4 s_rec;
+  // Item slots, double-buffered: round k reads slot k & 1 while the producer
+  // may already claim round k + 1's item into the other slot.
+  __shared__ int s_item[2][4];
+  __shared__ int4 s_rec[2];
   __shared__ int s_npieces, s_nextra;
   if (threadIdx.x == 0) {
     const int npieces = p.plan.counters[4];
@@ -128,7 +130,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
     const int4 rec = p.plan.pieces[blockIdx.x / p.Hkv];  // < C: inside the array
     s_npieces = npieces;
     s_nextra = nextra;
-    s_rec = rec;
+    s_rec[0] = rec;
   }
 
   extern __shared__ uint8_t smem_raw[];
@@ -167,47 +169,68 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
   // planner sorts pieces longest first -- then, until none are left, from one
   // device counter: the pieces past the first C (in launch order), then the
   // extra row chunks of requests with many query rows.
+  // Takes the next item from the device counter into slot `sl` (one thread).
+  // The producer calls it as soon as it has issued the last stage of an item,
+  // so that the claim and the record load overlap the consumers' last stages;
+  // the loop head calls it when that did not happen.
+  __shared__ int s_pre;  // 1: the next round's slot already holds its item
+  auto claim_next = [&](int sl) {
+    const int npieces = s_npieces, nextra = s_nextra;
+    const int late = (npieces > p.C ? npieces - p.C : 0) * Hkv;
+    int pos = -1, hh = 0, chunk = 0, valid = 1;
+    if (late == 0 && nextra == 0) {
+      valid = 0;
+    } else {
+      int idx = atomicAdd(p.plan.counters + 1, 1);
+      if (idx < late) {
+        pos = p.C + idx / Hkv;
+        hh = idx % Hkv;
+      } else if ((idx -= late) < nextra * Hkv) {
+        const int2 e = p.plan.extra[idx / Hkv];
+        pos = e.x;
+        chunk = e.y;
+        hh = idx % Hkv;
+      } else {
+        valid = 0;
+      }
+      if (pos >= 0) s_rec[sl] = p.plan.pieces[pos];
+    }
+    s_item[sl][0] = pos;
+    s_item[sl][1] = hh;
+    s_item[sl][2] = chunk;
+    s_item[sl][3] = valid;
+  };
+  if (threadIdx.x == 0) s_pre = 0;
   for (int round = 0;; ++round) {
     __syncthreads();  // everyone has read the previous item
     if (threadIdx.x == 0) {
-      const int npieces = s_npieces, nextra = s_nextra;
-      const int late = (npieces > p.C ? npieces - p.C : 0) * Hkv;
-      int pos = -1, hh = 0, chunk = 0, valid = 1;
       if (round == 0) {
+        const int npieces = s_npieces;
+        const int late = (npieces > p.C ? npieces - p.C : 0) * Hkv;
+        int pos = -1, hh = 0, valid = 1;
         if (static_cast<int>(blockIdx.x / Hkv) < npieces) {
           pos = blockIdx.x / Hkv;
           hh = blockIdx.x % Hkv;
-        } else if (late == 0 && nextra == 0) {
+        } else if (late == 0 && s_nextra == 0) {
           valid = 0;  // nothing for this CTA, now or later
         }
-      } else if (late == 0 && nextra == 0) {
-        valid = 0;
+        s_item[0][0] = pos;
+        s_item[0][1] = hh;
+        s_item[0][2] = 0;
+        s_item[0][3] = valid;
+      } else if (s_pre) {
+        s_pre = 0;  // claimed ahead by the producer
       } else {
-        int idx = atomicAdd(p.plan.counters + 1, 1);
-        if (idx < late) {
-          pos = p.C + idx / Hkv;
-          hh = idx % Hkv;
-        } else if ((idx -= late) < nextra * Hkv) {
-          const int2 e = p.plan.extra[idx / Hkv];
-          pos = e.x;
-          chunk = e.y;
-          hh = idx % Hkv;
-        } else {
-          valid = 0;
-        }
-        if (pos >= 0) s_rec = p.plan.pieces[pos];
+        claim_next(round & 1);
       }
-      s_item[0] = pos;
-      s_item[1] = hh;
-      s_item[2] = chunk;
-      s_item[3] = valid;
     }
     __syncthreads();
-    if (!s_item[3]) break;
-    if (s_item[0] < 0) continue;  // no piece for this CTA: look for extra items
-    const int h = s_item[1];
-    const int chunk = s_item[2];
-    const int4 piece = s_rec;
+    const int sl = round & 1;
+    if (!s_item[sl][3]) break;
+    if (s_item[sl][0] < 0) continue;  // no piece for this CTA: look for extra items
+    const int h = s_item[sl][1];
+    const int chunk = s_item[sl][2];
+    const int4 piece = s_rec[sl];
     const int r = piece.x;
 
     // Block-table window of the piece's first pages, loaded by the producer
@@ -300,6 +323,12 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
           tma_load_2d(dst, (c & 1) ? &tmv : &tmk, cb * (Cfg::SWB / Cfg::ESZ), y, bar_full + 8 * buf,
                       policy);
         }
+      }
+      // Last stage of the item issued: claim the next one (into the other
+      // slot) while the consumers finish this one.
+      if (pass == npass - 1 && lane == 0 && *reinterpret_cast<volatile int*>(&s_abort) == 0) {
+        claim_next(sl ^ 1);
+        s_pre = 1;
       }
       __syncthreads();  // pairs with the consumers' end-of-pass barrier
     }
