@@ -485,6 +485,7 @@ def sweep(args):
                             "call_gbs": round(kv / (t["call_ms"] * 1e-3) / 1e9, 1),
                             "split_gbs": round(kv / (t["split_ms"] * 1e-3) / 1e9, 1),
                             "split_frac_of_measured": round(kv / (t["split_ms"] * 1e-3) / 1e9 / peak, 4),
+                            "call_frac_of_measured": round(kv / (t["call_ms"] * 1e-3) / 1e9 / peak, 4),
                             "split_frac_of_8tbs": round(kv / (t["split_ms"] * 1e-3) / 8e12, 4),
                             "tasks": int(red[:, 1].sum()), "max_parts": int(red[:, 1].max())}
             res["refresh_us"] = round(time_refresh(w), 2)
@@ -497,6 +498,7 @@ def sweep(args):
         sp = [r["proportional"]["split_us"] for r in skew]
         cp = [r["proportional"]["us_per_decode_call"] for r in skew]
         fr = [r["proportional"]["split_frac_of_measured"] for r in skew]
+        fc = [r["proportional"]["call_frac_of_measured"] for r in skew]
         su = [r["uniform"]["split_us"] / r["proportional"]["split_us"] for r in skew]
         mm = [r["max_over_min"] for r in skew]
         print(json.dumps({"sweep": "skewed_summary", "seeds": len(skew),
@@ -505,6 +507,8 @@ def sweep(args):
                           "decode_call_us": {"median": _pct(cp, 0.5), "p90": _pct(cp, 0.9)},
                           "split_frac_of_measured": {"median": _pct(fr, 0.5), "p10": _pct(fr, 0.1),
                                                      "min": min(fr)},
+                          "decode_call_frac_of_measured": {"median": _pct(fc, 0.5),
+                                                           "p10": _pct(fc, 0.1), "min": min(fc)},
                           "uniform_over_proportional_split": {"median": round(_pct(su, 0.5), 2),
                                                               "min": round(min(su), 2)}}),
               flush=True)
