@@ -13,6 +13,7 @@ constexpr int kMaxSeqs = 4096;   // planner domain
 constexpr int kStageTensorBytes = 16384;  // split kernel: K (or V) bytes per pipeline stage
 
 constexpr int kMinPieceTiles = 2;  // a slot is cut into pieces of at least this many tiles
+constexpr int kWarpMergePieces = 8;  // rows with at most this many pieces are merged by one warp
 
 // Device buffers owned by one plan.
 //
@@ -34,11 +35,13 @@ struct PlanDev {
   int2* extra;      // [max_extra] (piece position, row chunk >= 1) for requests whose
                     // query rows exceed one work item
   int* counters;    // [0] extra items, [1] next late piece or extra item (x Hkv; reset by
-                    // the planner and by the merge kernel), [2] unused, [3] rows to
-                    // merge, [4] pieces
+                    // the planner and by the merge kernel), [2] merge rows with more than
+                    // kWarpMergePieces pieces, [3] merge rows with 2..kWarpMergePieces
+                    // pieces, [4] pieces
   int4* mrows;      // [max_tokens] one entry per row of a request with several pieces:
                     // {r | (pieces - 1) << 12, token, partial row of piece 0, L}
-                    // (piece k's partial row is that + k * L)
+                    // (piece k's partial row is that + k * L); rows with few pieces
+                    // first ([0, counters[3])), then rows with many
 };
 
 // Sizes and offsets of one plan's buffers (256-byte aligned, back to back).

@@ -7,11 +7,13 @@
 // The split kernel's partials are already normalised, so
 //     out = sum_j 2^(lse_j - M) o_j / sum_j 2^(lse_j - M),   M = max_j lse_j.
 //
-// The planner lists the rows of multi-partition requests, each entry carrying
+// The planner lists the rows of requests with several pieces, each entry carrying
 // what the merge needs (request, token, the first partial row and the row
 // stride between partitions), so that the partial rows and log-sum-exps are
-// addressed straight from the entry.  A persistent grid walks (row, q head)
-// pairs, one CTA per pair at a time.  The CTA is cut into units of D/4 lanes
+// addressed straight from the entry.  Rows with at most 8 pieces (listed
+// first) are merged one warp per (row, q head) pair: every piece's log-sum-exp
+// and partial slice are loaded at once and combined with shuffles.  Rows with
+// more pieces take a whole CTA per pair: the CTA is cut into units of D/4 lanes
 // (at most a warp), each unit holding one partial row with 4 outputs per lane;
 // unit u merges partitions u, u + NU, ... online (running maximum, rescaled
 // sum), with kMergeUnroll partitions' loads in flight, and the units are
@@ -44,10 +46,12 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
   if (blockIdx.x == 0 && threadIdx.x == 0) p.plan.counters[1] = 0;
   const int tid = threadIdx.x, u = tid / UL, ul = tid % UL;
   const int Hq = p.Hq;
-  const int total = p.plan.counters[3] * Hq;
+  const int nfew = p.plan.counters[3];  // rows listed first: at most kWarpMergePieces pieces
+  const int total = p.plan.counters[2] * Hq;
 
+  // Rows with many pieces: one CTA per (row, q head) pair.
   for (int pair = blockIdx.x; pair < total; pair += gridDim.x) {
-    const int4 e = p.plan.mrows[pair / Hq];
+    const int4 e = p.plan.mrows[nfew + pair / Hq];
     const int r = e.x & 4095, parts = (e.x >> 12) + 1, tok = e.y, L = e.w;
     const int hq = pair % Hq;
     // staleness inputs; only the final store depends on them
@@ -142,6 +146,75 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
       }
     }
     __syncthreads();  // shared memory is reused by the next pair
+  }
+
+  // Rows with few pieces: one warp per (row, q head) pair, every piece's
+  // partial loaded at once, combined with shuffles.
+  constexpr int VL = D / 32;  // outputs per lane
+  const int warp = tid >> 5, lane = tid & 31;
+  constexpr int kWarps = kMergeThreads / 32;
+  for (int wp = blockIdx.x * kWarps + warp; wp < nfew * Hq; wp += gridDim.x * kWarps) {
+    const int4 e = p.plan.mrows[wp / Hq];
+    const int r = e.x & 4095, parts = (e.x >> 12) + 1, tok = e.y, L = e.w;
+    const int hq = wp % Hq;
+    const int2 snap = p.plan.snap[r];
+    const int ctx = p.context_lens[r];
+    const int c0 = p.cu ? p.cu[r] : r;
+    const int Lnow = p.cu ? p.cu[r + 1] - c0 : 1;
+    float lse = NEG_INF;
+    if (lane < parts) lse = __ldcg(p.plan.part_lse + static_cast<long long>(e.z + lane * L) * Hq + hq);
+    float o[kWarpMergePieces][VL];
+#pragma unroll
+    for (int j = 0; j < kWarpMergePieces; ++j) {
+      if (j < parts) {
+        const float* src = p.plan.part_o + (static_cast<long long>(e.z + j * L) * Hq + hq) * D + lane * VL;
+#pragma unroll
+        for (int v = 0; v < VL; v += 2) {
+          const float2 x = __ldcg(reinterpret_cast<const float2*>(src + v));
+          o[j][v] = x.x;
+          o[j][v + 1] = x.y;
+        }
+      } else {
+#pragma unroll
+        for (int v = 0; v < VL; ++v) o[j][v] = 0.f;
+      }
+    }
+    float M = lse;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float w = (lse == NEG_INF) ? 0.f : fast_exp2(lse - M);
+    float W = w;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
+    float acc[VL];
+#pragma unroll
+    for (int v = 0; v < VL; ++v) acc[v] = 0.f;
+#pragma unroll
+    for (int j = 0; j < kWarpMergePieces; ++j) {
+      const float wj = __shfl_sync(0xffffffffu, w, j);
+#pragma unroll
+      for (int v = 0; v < VL; ++v) acc[v] += wj * o[j][v];
+    }
+    if (snap.x != ctx || snap.y != Lnow) continue;  // stale: zeroed by the split kernel
+    const int t = c0 + tok;
+    if (t >= p.num_tokens) {
+      if (lane == 0) atomicOr(p.plan.err, PA_DEVERR_PLAN_OVERFLOW);
+      continue;
+    }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    uint32_t pk[VL / 2];
+#pragma unroll
+    for (int v = 0; v < VL; v += 2)
+      pk[v / 2] = p.out_f16 ? pack2<false>(acc[v] * inv, acc[v + 1] * inv)
+                            : pack2<true>(acc[v] * inv, acc[v + 1] * inv);
+    uint16_t* dst = static_cast<uint16_t*>(p.out) + (static_cast<size_t>(t) * Hq + hq) * D + lane * VL;
+    if constexpr (VL == 2) {
+      *reinterpret_cast<uint32_t*>(dst) = pk[0];
+    } else if constexpr (VL == 4) {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(pk[0], pk[1]);
+    } else {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
   }
 }
 

@@ -132,8 +132,8 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
   __shared__ long long s_red[kWarps], s_red2[kWarps];
   __shared__ int s_cnt[kWarps];
   __shared__ int s_bad;
-  __shared__ int s_scan[5][kWarps];
-  __shared__ int s_tot[5];
+  __shared__ int s_scan[6][kWarps];
+  __shared__ int s_tot[6];
   __shared__ int s_bcnt[128];  // launch-order classes, longest first
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -249,7 +249,10 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
   }
 
   // ---- 2c. pieces, partial rows, extra row-chunk items, merge rows per request
-  int my_slots = 0, my_pieces = 0, my_rows = 0, my_extra = 0, my_mrows = 0;
+  // Merge rows are listed in two runs: rows of requests with at most
+  // kWarpMergePieces pieces first (the merge gives each (row, head) a warp),
+  // then rows with more (a whole CTA each).
+  int my_slots = 0, my_pieces = 0, my_rows = 0, my_extra = 0, my_mfew = 0, my_mmany = 0;
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
     pcs[k] = pieces_of(k, xcut);
@@ -258,30 +261,32 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
     my_pieces += pcs[k];
     my_rows += pcs[k] >= 2 ? pcs[k] * L[k] : 0;
     my_extra += pcs[k] * (chunks > 1 ? chunks - 1 : 0);
-    my_mrows += pcs[k] >= 2 ? L[k] : 0;
+    my_mfew += (pcs[k] >= 2 && pcs[k] <= kWarpMergePieces) ? L[k] : 0;
+    my_mmany += pcs[k] > kWarpMergePieces ? L[k] : 0;
   }
 
   // ---- 3. exclusive offsets (slots, pieces, partial rows, extra items, merge rows)
-  int inc[5] = {my_slots, my_pieces, my_rows, my_extra, my_mrows};
-  block_scan<kThreads, 5>(inc, s_scan, s_tot);
+  int inc[6] = {my_slots, my_pieces, my_rows, my_extra, my_mfew, my_mmany};
+  block_scan<kThreads, 6>(inc, s_scan, s_tot);
   __syncthreads();
   int slot0 = inc[0] - my_slots, piece0 = inc[1] - my_pieces, row0 = inc[2] - my_rows;
-  int extra0 = inc[3] - my_extra, mrow0 = inc[4] - my_mrows;
+  int extra0 = inc[3] - my_extra, mfew0 = inc[4] - my_mfew, mmany0 = s_tot[4] + inc[5] - my_mmany;
   const bool overflow = static_cast<long long>(s_tot[2]) > p.rows_cap ||
                         static_cast<long long>(s_tot[3]) > p.max_extra ||
-                        s_tot[4] > p.max_tokens ||
+                        static_cast<long long>(s_tot[4]) + s_tot[5] > p.max_tokens ||
                         static_cast<long long>(s_tot[1]) > C * p.Q;
   if (overflow) {
     // Cannot happen for a plan built with these limits; empty the plan rather
     // than write past the scratch.
 #pragma unroll
     for (int k = 0; k < kPer; ++k) parts[k] = pcs[k] = 0;
-    slot0 = piece0 = row0 = extra0 = mrow0 = 0;
+    slot0 = piece0 = row0 = extra0 = mfew0 = mmany0 = 0;
   }
   const int total_slots = overflow ? 0 : s_tot[0];
   const int total_pieces = overflow ? 0 : s_tot[1];
   const int total_extra = overflow ? 0 : s_tot[3];
-  const int total_mrows = overflow ? 0 : s_tot[4];
+  const int total_mfew = overflow ? 0 : s_tot[4];
+  const int total_mmany = overflow ? 0 : s_tot[5];
   if (tid == 0 && (bad || overflow)) atomicOr(p.dev.err, PA_DEVERR_PLAN_OVERFLOW);
 
 #pragma unroll
@@ -297,22 +302,24 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
       s_prow[r] = row0;
       s_pfirst[r] = piece0;
       s_xfirst[r] = extra0;
-      if (pcs[k] >= 2)
+      if (pcs[k] >= 2) {
+        int& m0 = pcs[k] <= kWarpMergePieces ? mfew0 : mmany0;
         for (int i = 0; i < L[k]; ++i)
-          p.dev.mrows[mrow0 + i] = make_int4(r | ((pcs[k] - 1) << 12), i, row0 + i, L[k]);
+          p.dev.mrows[m0 + i] = make_int4(r | ((pcs[k] - 1) << 12), i, row0 + i, L[k]);
+        m0 += L[k];
+      }
       const int chunks = (L[k] * p.G + p.rpc - 1) / p.rpc;
       slot0 += parts[k];
       piece0 += pcs[k];
       row0 += pcs[k] >= 2 ? pcs[k] * L[k] : 0;
       extra0 += pcs[k] * (chunks > 1 ? chunks - 1 : 0);
-      mrow0 += pcs[k] >= 2 ? L[k] : 0;
     }
   }
   if (tid == 0) {
     p.dev.counters[0] = total_extra;
     p.dev.counters[1] = 0;
-    p.dev.counters[2] = 0;
-    p.dev.counters[3] = total_mrows;
+    p.dev.counters[2] = total_mmany;
+    p.dev.counters[3] = total_mfew;
     p.dev.counters[4] = total_pieces;
   }
   __syncthreads();
