@@ -89,6 +89,21 @@ def test_split_count_sweep(dev, P, W, kv):
     assert d <= TOL[kv]
 
 
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_uneven_slots_run_as_pieces(dev, kv):
+    """A small budget leaves one slot per request, one of them 150x longer than
+    the rest: the split kernel runs that slot as several pieces, and the merge
+    combines them (the plan itself is unchanged)."""
+    w = batch(dev, [40000] + [300 + 37 * i for i in range(15)], H=(8, 2), D=128, kv=kv, seed=12,
+              budget=32)
+    out, plan = run(w)
+    work, red = plan.download()
+    assert bool((red[:, 1] == 1).all())  # one partition per request: pieces are not partitions
+    ref = oracle_decode(w.to("cpu"))
+    assert max_diff(out, ref) <= TOL[kv]
+    assert plan.read_errors() == 0
+
+
 # ---------------------------------------------------- multi-token rows (cu)
 
 def test_verify_rows_and_padding(dev):
