@@ -64,12 +64,21 @@ def _load():
         lib.oracle_plan_capacity.restype = i64
         lib.oracle_plan.argtypes = [i32, P, P, i32, i32, i32, i32, i32, P, i64, P]
         lib.oracle_plan.restype = i64
+        lib.oracle_plan_window.argtypes = [i32, P, P, i32, i32, i32, i32, i32, i32, P, i64, P]
+        lib.oracle_plan_window.restype = i64
         lib.oracle_decode.argtypes = [P, i32, i32, i32, i32, P, P, i32, dbl, dbl, i32, i32,
                                       P, i32, P, P, i32, dbl, P]
         lib.oracle_decode.restype = None
+        lib.oracle_decode_ext.argtypes = [P, i32, i32, i32, i32, P, P, i32, dbl, dbl, i32, i32,
+                                          P, i32, P, P, i32, dbl, i32, P, P]
+        lib.oracle_decode_ext.restype = None
         lib.oracle_decode_planned.argtypes = [P, i32, i32, i32, i32, P, P, i32, dbl, dbl, i32,
                                               i32, P, i32, P, P, i32, dbl, P, P, i32, P]
         lib.oracle_decode_planned.restype = None
+        lib.oracle_decode_planned_ext.argtypes = [P, i32, i32, i32, i32, P, P, i32, dbl, dbl,
+                                                  i32, i32, P, i32, P, P, i32, dbl, P, P, i32,
+                                                  i32, P, P]
+        lib.oracle_decode_planned_ext.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = i32
         _lib = lib
@@ -105,16 +114,21 @@ def plan_capacity(n: int, num_kv_heads: int, max_partitions: int, budget: int) -
 
 
 def plan(context_lens, cu_query_lens, num_kv_heads: int, max_partitions: int, budget: int,
-         kind: int = PLAN_PROPORTIONAL, tile: int = TILE):
-    """Work plan for the given lengths.  Returns (work_info [C,4], reduce_info [n,2])."""
+         kind: int = PLAN_PROPORTIONAL, tile: int = TILE, window: int = 0):
+    """Work plan for the given lengths (and sliding window; 0 = none).  Returns
+    (work_info [C,4], reduce_info [n,2])."""
     lens = _c(context_lens, np.int32)
     cu = _c(cu_query_lens, np.int32)
     n = lens.shape[0]
     C = plan_capacity(n, num_kv_heads, max_partitions, budget)
     work = np.zeros((C, 4), dtype=np.int32)
     red = np.zeros((n, 2), dtype=np.int32)
-    got = _load().oracle_plan(n, _ptr(lens), _ptr(cu), num_kv_heads, max_partitions, budget,
-                              tile, kind, _ptr(work), C, _ptr(red))
+    if window:
+        got = _load().oracle_plan_window(n, _ptr(lens), _ptr(cu), num_kv_heads, max_partitions,
+                                         budget, tile, kind, window, _ptr(work), C, _ptr(red))
+    else:
+        got = _load().oracle_plan(n, _ptr(lens), _ptr(cu), num_kv_heads, max_partitions, budget,
+                                  tile, kind, _ptr(work), C, _ptr(red))
     assert got == C
     return work, red
 
@@ -140,21 +154,32 @@ def _decode_args(q_bits, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale, 
 
 
 def decode(q_bits, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale, block_tables,
-           context_lens, cu_query_lens, scale):
-    """Exact paged decode in fp64.  Returns out [num_tokens, Hq, D] float64."""
+           context_lens, cu_query_lens, scale, window: int = 0, sinks=None):
+    """Exact paged decode in fp64 (sliding window: 0 = none; sinks: [Hq] logits or
+    None).  Returns out [num_tokens, Hq, D] float64."""
     args, out, _keep = _decode_args(q_bits, q_dtype, k_cache, v_cache, kv_dtype, k_scale,
                                     v_scale, block_tables, context_lens, cu_query_lens, scale)
-    _load().oracle_decode(*args, _ptr(out))
+    if window or sinks is not None:
+        sk = _c(sinks, np.float64)
+        _load().oracle_decode_ext(*args, int(window), _ptr(sk), _ptr(out))
+    else:
+        _load().oracle_decode(*args, _ptr(out))
     return out
 
 
 def decode_planned(q_bits, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale, block_tables,
-                   context_lens, cu_query_lens, scale, work_info, reduce_info, tile: int = TILE):
+                   context_lens, cu_query_lens, scale, work_info, reduce_info, tile: int = TILE,
+                   window: int = 0, sinks=None):
     """The same result computed by partial softmaxes over the plan's tasks plus an
     LSE-weighted merge, in fp64."""
     args, out, _keep = _decode_args(q_bits, q_dtype, k_cache, v_cache, kv_dtype, k_scale,
                                     v_scale, block_tables, context_lens, cu_query_lens, scale)
     w = _c(work_info, np.int32)
     r = _c(reduce_info, np.int32)
-    _load().oracle_decode_planned(*args, _ptr(w), _ptr(r), tile, _ptr(out))
+    if window or sinks is not None:
+        sk = _c(sinks, np.float64)
+        _load().oracle_decode_planned_ext(*args, _ptr(w), _ptr(r), tile, int(window), _ptr(sk),
+                                          _ptr(out))
+    else:
+        _load().oracle_decode_planned(*args, _ptr(w), _ptr(r), tile, _ptr(out))
     return out

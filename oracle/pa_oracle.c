@@ -35,7 +35,16 @@
  *     first_slot the exclusive running sum of num_parts;
  *   - fp8 is OCP e4m3fn (bias 7, no infinities, S.1111.111 = NaN); a stored
  *     byte b means e4m3fn(b) * scale;
- *   - the kv head of q head hq is hq / (Hq / Hkv).
+ *   - the kv head of q head hq is hq / (Hq / Hkv);
+ *   - sliding window W > 0 ([RDNA-29] Change 1: "the sliding window applies
+ *     per token"): token i, which may see keys [0, K_i), sees only the W most
+ *     recent of them, [max(0, K_i - W), K_i); W = 0 means no window;
+ *   - with a window the plan sizes a request by the keys its tokens read: it
+ *     starts at the tile holding the first token's first visible key and runs
+ *     the rule on that range's length (tile indices stay absolute);
+ *   - attention sinks (named in the pa_decode signature the pages quote): a
+ *     logit per q head, in the units of scale * q.k, that joins the softmax
+ *     denominator only: out = sum_j e^(s_j) v_j / (sum_j e^(s_j) + e^(sink)).
  */
 #include <math.h>
 #include <stdint.h>
@@ -111,41 +120,57 @@ static long long rows_of(const int32_t* cu, int r) {
   return cu ? (long long)cu[r + 1] - (long long)cu[r] : 1;
 }
 
+/* First tile a request's plan covers: 0 without a window; with one, the tile
+ * holding the first visible key of its first query token. */
+static long long first_tile(long long S, long long L, int window, int tile) {
+  if (window <= 0) return 0;
+  long long first_key = S - (L - 1) - window;
+  if (first_key < 0) first_key = 0;
+  return first_key / tile;
+}
+
 /* Builds the plan.  Returns the capacity C, or -1 if work_info has fewer than
- * C slots.  work_info is C x 4 int32, reduce_info is n x 2 int32. */
-long long oracle_plan(int n, const int32_t* context_lens, const int32_t* cu, int num_kv_heads,
-                      int max_partitions, int budget, int tile, int kind, int32_t* work_info,
-                      long long work_slots, int32_t* reduce_info) {
+ * C slots.  work_info is C x 4 int32, reduce_info is n x 2 int32.  With a
+ * sliding window the rule runs on each request's planned range (see
+ * first_tile); window = 0 is the plain rule. */
+long long oracle_plan_window(int n, const int32_t* context_lens, const int32_t* cu,
+                             int num_kv_heads, int max_partitions, int budget, int tile, int kind,
+                             int window, int32_t* work_info, long long work_slots,
+                             int32_t* reduce_info) {
   long long C = oracle_plan_capacity(n, num_kv_heads, max_partitions, budget);
   if (C > work_slots) return -1;
 
+  /* the length the rule sees: from the first planned tile to S */
   long long n_act = 0, sum_s = 0;
   for (int r = 0; r < n; ++r) {
-    if (context_lens[r] > 0 && rows_of(cu, r) > 0) {
+    long long S = context_lens[r], L = rows_of(cu, r);
+    if (S > 0 && L > 0) {
       n_act += 1;
-      sum_s += context_lens[r];
+      sum_s += S - first_tile(S, L, window, tile) * tile;
     }
   }
 
   long long slot = 0;
   for (int r = 0; r < n; ++r) {
-    long long S = context_lens[r];
+    long long S = context_lens[r], L = rows_of(cu, r);
     long long p = 0;
-    if (S > 0 && rows_of(cu, r) > 0) {
-      long long tiles = (S + tile - 1) / tile;
+    if (S > 0 && L > 0) {
+      long long t0 = first_tile(S, L, window, tile);
+      long long len = S - t0 * tile;
+      long long tiles = (len + tile - 1) / tile;
       long long share;
       if (kind == OR_PLAN_UNIFORM)
-        share = C / n_act;                       /* same count for everyone */
+        share = C / n_act;                        /* same count for everyone */
       else
-        share = 1 + ((C - n_act) * S) / sum_s;   /* proportional to S */
+        share = 1 + ((C - n_act) * len) / sum_s;  /* proportional to the length */
       p = max_partitions;
       if (tiles < p) p = tiles;
       if (share < p) p = share;
       for (long long j = 0; j < p; ++j) {
         int32_t* w = work_info + 4 * (slot + j);
         w[0] = r;
-        w[1] = (int32_t)((j * tiles) / p);
-        w[2] = (int32_t)(((j + 1) * tiles) / p);
+        w[1] = (int32_t)(t0 + (j * tiles) / p);
+        w[2] = (int32_t)(t0 + ((j + 1) * tiles) / p);
         w[3] = (int32_t)S;
       }
     }
@@ -159,6 +184,14 @@ long long oracle_plan(int n, const int32_t* context_lens, const int32_t* cu, int
     w[1] = w[2] = w[3] = 0;
   }
   return C;
+}
+
+/* The pages' rule: no window. */
+long long oracle_plan(int n, const int32_t* context_lens, const int32_t* cu, int num_kv_heads,
+                      int max_partitions, int budget, int tile, int kind, int32_t* work_info,
+                      long long work_slots, int32_t* reduce_info) {
+  return oracle_plan_window(n, context_lens, cu, num_kv_heads, max_partitions, budget, tile,
+                            kind, 0, work_info, work_slots, reduce_info);
 }
 
 /* ------------------------------------------------------------- attention */
@@ -204,14 +237,23 @@ static long long keys_of_row(const int32_t* context_lens, const int32_t* cu, int
   return (long long)context_lens[r] - (L - 1 - i);
 }
 
+/* First visible key of a row that sees keys below K: 0, or K - W with a window. */
+static long long window_lo(long long K, int window) {
+  if (window <= 0 || K <= window) return 0;
+  return K - window;
+}
+
 /* Dense decode: the exact result, softmax(scale * q K^T) V per row and q head,
- * accumulated in fp64.  out is num_tokens x Hq x D doubles.  Rows past cu[n],
- * rows of a request with S <= 0 and rows with no visible key are 0. */
-void oracle_decode(const void* q, int q_dtype, int num_tokens, int num_q_heads, int head_dim,
-                   const void* k_cache, const void* v_cache, int kv_dtype, double k_scale,
-                   double v_scale, int num_kv_heads, int block_size,
-                   const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
-                   const int32_t* cu, int n, double scale, double* out) {
+ * accumulated in fp64, over each row's visible keys [window_lo(K), K); a sink
+ * (if given) adds e^(sink) to the denominator.  out is num_tokens x Hq x D
+ * doubles.  Rows past cu[n], rows of a request with S <= 0 and rows with no
+ * visible key are 0. */
+void oracle_decode_ext(const void* q, int q_dtype, int num_tokens, int num_q_heads, int head_dim,
+                       const void* k_cache, const void* v_cache, int kv_dtype, double k_scale,
+                       double v_scale, int num_kv_heads, int block_size,
+                       const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
+                       const int32_t* cu, int n, double scale, int window, const double* sinks,
+                       double* out) {
   struct kv_view kv = {k_cache, v_cache, kv_dtype,
                        kv_dtype == OR_FP8_E4M3 ? k_scale : 1.0,
                        kv_dtype == OR_FP8_E4M3 ? v_scale : 1.0,
@@ -228,23 +270,37 @@ void oracle_decode(const void* q, int q_dtype, int num_tokens, int num_q_heads, 
     if (r < 0 || context_lens[r] <= 0) continue;
     long long K = keys_of_row(context_lens, cu, r, t);
     if (K <= 0) continue;
+    long long lo = window_lo(K, window);
 
-    double* s = (double*)malloc(sizeof(double) * (size_t)K);
+    double* s = (double*)malloc(sizeof(double) * (size_t)(K - lo));
     double m = -INFINITY, l = 0.0;
-    for (long long j = 0; j < K; ++j) {
-      s[j] = logit(&kv, q, q_dtype, th * head_dim, r, h, j, scale);
-      if (s[j] > m) m = s[j];
+    for (long long j = lo; j < K; ++j) {
+      s[j - lo] = logit(&kv, q, q_dtype, th * head_dim, r, h, j, scale);
+      if (s[j - lo] > m) m = s[j - lo];
     }
-    for (long long j = 0; j < K; ++j) {
-      double w = exp(s[j] - m);
+    if (sinks && sinks[hq] > m) m = sinks[hq];
+    for (long long j = lo; j < K; ++j) {
+      double w = exp(s[j - lo] - m);
       int64_t vrow = key_row(&kv, r, h, j);
       l += w;
       for (int d = 0; d < head_dim; ++d)
         o[d] += w * load_kv(kv.v, kv.dtype, vrow + d, kv.v_scale);
     }
+    if (sinks) l += exp(sinks[hq] - m);
     for (int d = 0; d < head_dim; ++d) o[d] /= l;
     free(s);
   }
+}
+
+/* No window, no sink. */
+void oracle_decode(const void* q, int q_dtype, int num_tokens, int num_q_heads, int head_dim,
+                   const void* k_cache, const void* v_cache, int kv_dtype, double k_scale,
+                   double v_scale, int num_kv_heads, int block_size,
+                   const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
+                   const int32_t* cu, int n, double scale, double* out) {
+  oracle_decode_ext(q, q_dtype, num_tokens, num_q_heads, head_dim, k_cache, v_cache, kv_dtype,
+                    k_scale, v_scale, num_kv_heads, block_size, block_tables, max_blocks,
+                    context_lens, cu, n, scale, 0, NULL, out);
 }
 
 /* Planned decode, computed the way the method computes it: each task of the
@@ -252,13 +308,14 @@ void oracle_decode(const void* q, int q_dtype, int num_tokens, int num_q_heads, 
  * are then combined with weights exp(lse_j - max lse) ([ATOM-2366] sections 3
  * and 6.5: split attention tile, then the "PS reduce").  Equal to
  * oracle_decode up to rounding for every valid plan. */
-void oracle_decode_planned(const void* q, int q_dtype, int num_tokens, int num_q_heads,
-                           int head_dim, const void* k_cache, const void* v_cache, int kv_dtype,
-                           double k_scale, double v_scale, int num_kv_heads, int block_size,
-                           const int32_t* block_tables, int max_blocks,
-                           const int32_t* context_lens, const int32_t* cu, int n, double scale,
-                           const int32_t* work_info, const int32_t* reduce_info, int tile,
-                           double* out) {
+void oracle_decode_planned_ext(const void* q, int q_dtype, int num_tokens, int num_q_heads,
+                               int head_dim, const void* k_cache, const void* v_cache,
+                               int kv_dtype, double k_scale, double v_scale, int num_kv_heads,
+                               int block_size, const int32_t* block_tables, int max_blocks,
+                               const int32_t* context_lens, const int32_t* cu, int n,
+                               double scale, const int32_t* work_info,
+                               const int32_t* reduce_info, int tile, int window,
+                               const double* sinks, double* out) {
   struct kv_view kv = {k_cache, v_cache, kv_dtype,
                        kv_dtype == OR_FP8_E4M3 ? k_scale : 1.0,
                        kv_dtype == OR_FP8_E4M3 ? v_scale : 1.0,
@@ -276,6 +333,7 @@ void oracle_decode_planned(const void* q, int q_dtype, int num_tokens, int num_q
     int first = reduce_info[2 * r], parts = reduce_info[2 * r + 1];
     if (parts <= 0) continue;
     long long K = keys_of_row(context_lens, cu, r, t);
+    long long row_lo = window_lo(K, window);
 
     double* po = (double*)calloc((size_t)parts * head_dim, sizeof(double));
     double* lse = (double*)malloc(sizeof(double) * (size_t)parts);
@@ -284,6 +342,7 @@ void oracle_decode_planned(const void* q, int q_dtype, int num_tokens, int num_q
       long long lo = (long long)w[1] * tile, hi = (long long)w[2] * tile;
       if (hi > w[3]) hi = w[3];
       if (hi > K) hi = K;
+      if (lo < row_lo) lo = row_lo;
       lse[j] = -INFINITY;
       if (lo >= hi) continue;
       double m = -INFINITY, l = 0.0;
@@ -305,6 +364,7 @@ void oracle_decode_planned(const void* q, int q_dtype, int num_tokens, int num_q
     for (int j = 0; j < parts; ++j)
       if (lse[j] > M) M = lse[j];
     if (M > -INFINITY) {
+      if (sinks && sinks[hq] > M) M = sinks[hq];
       double wsum = 0.0;
       for (int j = 0; j < parts; ++j) {
         if (lse[j] == -INFINITY) continue;
@@ -312,11 +372,26 @@ void oracle_decode_planned(const void* q, int q_dtype, int num_tokens, int num_q
         wsum += w;
         for (int d = 0; d < head_dim; ++d) o[d] += w * po[(size_t)j * head_dim + d];
       }
+      if (sinks) wsum += exp(sinks[hq] - M);  /* the sink joins the merge once */
       for (int d = 0; d < head_dim; ++d) o[d] /= wsum;
     }
     free(po);
     free(lse);
   }
+}
+
+/* No window, no sink. */
+void oracle_decode_planned(const void* q, int q_dtype, int num_tokens, int num_q_heads,
+                           int head_dim, const void* k_cache, const void* v_cache, int kv_dtype,
+                           double k_scale, double v_scale, int num_kv_heads, int block_size,
+                           const int32_t* block_tables, int max_blocks,
+                           const int32_t* context_lens, const int32_t* cu, int n, double scale,
+                           const int32_t* work_info, const int32_t* reduce_info, int tile,
+                           double* out) {
+  oracle_decode_planned_ext(q, q_dtype, num_tokens, num_q_heads, head_dim, k_cache, v_cache,
+                            kv_dtype, k_scale, v_scale, num_kv_heads, block_size, block_tables,
+                            max_blocks, context_lens, cu, n, scale, work_info, reduce_info, tile,
+                            0, NULL, out);
 }
 
 /* Threads an OpenMP region of this library uses (1 without OpenMP). */

@@ -30,16 +30,17 @@ def oracle_args(w):
             w.context_lens.cpu().numpy(), cu, w.scale)
 
 
-def oracle_decode(w) -> np.ndarray:
-    return oracle.decode(*oracle_args(w))
+def oracle_decode(w, window: int = 0, sinks=None) -> np.ndarray:
+    return oracle.decode(*oracle_args(w), window=window, sinks=sinks)
 
 
-def oracle_decode_planned(w, work, red) -> np.ndarray:
-    return oracle.decode_planned(*oracle_args(w), work, red)
+def oracle_decode_planned(w, work, red, window: int = 0, sinks=None) -> np.ndarray:
+    return oracle.decode_planned(*oracle_args(w), work, red, window=window, sinks=sinks)
 
 
-def oracle_plan(w, budget: int, kind: int = oracle.PLAN_PROPORTIONAL, max_partitions=None):
+def oracle_plan(w, budget: int, kind: int = oracle.PLAN_PROPORTIONAL, max_partitions=None,
+                window: int = 0):
     cu = None if w.cu_query_lens is None else w.cu_query_lens.cpu().numpy()
     return oracle.plan(w.context_lens.cpu().numpy(), cu, w.num_kv_heads,
                        w.max_partitions if max_partitions is None else max_partitions,
-                       budget, kind)
+                       budget, kind, window=window)

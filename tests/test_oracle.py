@@ -384,3 +384,145 @@ def test_plan_skips_zero_length_and_rowless_requests():
     # n_act = 2, sum S = 800, C = 16: 1 + floor(14*500/800) = 9 -> 2 tiles; 1 + floor(14*300/800) = 6 -> 2
     assert red[:, 1].tolist() == [2, 0, 0, 2]
     assert red[:, 0].tolist() == [0, 2, 2, 2]
+
+
+# ------------------------------------------------- sliding window and attention sinks
+
+def sdpa_window_reference(w, window: int, sinks=None) -> torch.Tensor:
+    """torch SDPA in float64 with a banded mask: token i (end-aligned causal range
+    [0, K_i)) sees only keys [K_i - window, K_i).  A sink is an extra key whose
+    logit is the sink and whose value row is zero, appended to every row."""
+    n, G = w.num_seqs, w.num_q_heads // w.num_kv_heads
+    out = torch.zeros(w.num_tokens, w.num_q_heads, w.head_dim, dtype=torch.float64)
+    cu = w.cu_query_lens
+    for r in range(n):
+        S = int(w.context_lens[r])
+        rows = list(range(int(cu[r]), int(cu[r + 1]))) if cu is not None else [r]
+        L = len(rows)
+        if S <= 0 or L == 0:
+            continue
+        pages = w.block_tables[r, : -(-S // w.block_size)].long()
+        K = _dequant(w.k_cache[pages], w.kv_dtype, w.k_scale)
+        V = _dequant(w.v_cache[pages], w.kv_dtype, w.v_scale)
+        K = K.permute(1, 0, 2, 3).reshape(w.num_kv_heads, -1, w.head_dim)[:, :S]
+        V = V.permute(1, 0, 2, 3).reshape(w.num_kv_heads, -1, w.head_dim)[:, :S]
+        K = K.repeat_interleave(G, dim=0)
+        V = V.repeat_interleave(G, dim=0)
+        q = w.q[rows].to(torch.float64).permute(1, 0, 2)  # [Hq, L, D]
+        mask = torch.ones(L, S, dtype=torch.bool).tril(diagonal=S - L)
+        if window > 0:
+            mask &= ~torch.ones(L, S, dtype=torch.bool).tril(diagonal=S - L - window)
+        visible = mask.any(dim=1)
+        if sinks is None:
+            o = F.scaled_dot_product_attention(q, K, V, attn_mask=mask, scale=w.scale)
+        else:
+            # the sink as one more key: a key vector along q with logit = sink (per
+            # head and row), and a zero value row
+            sk = torch.as_tensor(sinks, dtype=torch.float64)  # [Hq]
+            qn = (q * q).sum(-1, keepdim=True)  # [Hq, L, 1]
+            ksink = q * (sk[:, None, None] / (w.scale * qn))  # scale * q . ksink = sink
+            Kx = torch.cat([K[:, None].expand(-1, L, -1, -1), ksink[:, :, None]], dim=2)
+            Vx = torch.cat([V[:, None].expand(-1, L, -1, -1),
+                            torch.zeros(w.num_q_heads, L, 1, w.head_dim, dtype=torch.float64)], dim=2)
+            mx = torch.cat([mask, torch.ones(L, 1, dtype=torch.bool)], dim=1)
+            o = F.scaled_dot_product_attention(q[:, :, None], Kx, Vx, attn_mask=mx[:, None],
+                                               scale=w.scale)[:, :, 0]
+        o[:, ~visible] = 0.0
+        out[rows] = o.permute(1, 0, 2)
+    return out
+
+
+WINDOW_CASES = [c for c in CASES if c["name"] in ("decode_bf16", "decode_fp8", "verify", "mixed")]
+
+
+@pytest.mark.parametrize("window", [1, 3, 50, 500])
+@pytest.mark.parametrize("c", WINDOW_CASES, ids=[c["name"] for c in WINDOW_CASES])
+def test_window_matches_torch_sdpa_banded(c, window):
+    w = _case(c)
+    got = oracle_decode(w, window=window)
+    ref = sdpa_window_reference(w, window).numpy()
+    assert np.abs(got - ref).max() < 1e-12
+
+
+def test_window_wider_than_every_row_is_no_window():
+    w = _case(CASES[0])  # longest request: 1000 keys
+    assert np.array_equal(oracle_decode(w, window=1000), oracle_decode(w))
+    assert np.array_equal(oracle_decode(w, window=5000), oracle_decode(w))
+
+
+def test_window_one_returns_the_last_visible_value_row():
+    w = _single(300, H=(4, 2))
+    out = oracle_decode(w, window=1)
+    G = 2
+    page = int(w.block_tables[0, 299 // w.block_size])
+    for hq in range(4):
+        v = w.v_cache[page, hq // G, 299 % w.block_size].to(torch.float64).numpy()
+        assert np.abs(out[0, hq] - v).max() < 1e-15
+
+
+@pytest.mark.parametrize("c", WINDOW_CASES, ids=[c["name"] for c in WINDOW_CASES])
+def test_sinks_match_torch_sdpa_with_an_extra_key(c):
+    w = _case(c)
+    rng = np.random.default_rng(4)
+    sinks = rng.normal(0.0, 2.0, w.num_q_heads)
+    for window in (0, 50):
+        got = oracle_decode(w, window=window, sinks=sinks)
+        ref = sdpa_window_reference(w, window, sinks).numpy()
+        assert np.abs(got - ref).max() < 1e-12, window
+
+
+def test_sink_at_minus_infinity_is_no_sink_and_a_huge_sink_silences_the_row():
+    w = _case(CASES[0])
+    none = oracle_decode(w)
+    assert np.array_equal(oracle_decode(w, sinks=np.full(w.num_q_heads, -np.inf)), none)
+    quiet = oracle_decode(w, sinks=np.full(w.num_q_heads, 800.0))
+    assert np.abs(quiet).max() < 1e-300
+
+
+@pytest.mark.parametrize("window", [1, 37, 300, 5000])
+@pytest.mark.parametrize("c", WINDOW_CASES, ids=[c["name"] for c in WINDOW_CASES])
+def test_windowed_plan_covers_the_read_range_and_merges_to_dense(c, window):
+    """The windowed plan covers, for each request, the tiles from the one holding
+    its first token's first visible key up to ceil(S/T), once each; its partials
+    merge to the dense windowed result, with and without sinks."""
+    w = _case(c)
+    lens = w.context_lens.numpy()
+    cu = None if w.cu_query_lens is None else w.cu_query_lens.numpy()
+    sinks = np.linspace(-1.0, 1.0, w.num_q_heads)
+    for P, W in ((1, 8), (7, 100), (256, 4096)):
+        work, red = oracle_plan(w, W, max_partitions=P, window=window)
+        for r in range(w.num_seqs):
+            f, p = red[r]
+            if p == 0:
+                continue
+            L = 1 if cu is None else int(cu[r + 1] - cu[r])
+            first = max(0, int(lens[r]) - (L - 1) - window)
+            seg = work[f:f + p]
+            assert seg[0, 1] == first // oracle.TILE
+            assert seg[-1, 2] == -(-int(lens[r]) // oracle.TILE)
+            assert np.all(seg[1:, 1] == seg[:-1, 2])
+        for sk in (None, sinks):
+            got = oracle_decode_planned(w, work, red, window=window, sinks=sk)
+            dense = oracle_decode(w, window=window, sinks=sk)
+            assert np.abs(got - dense).max() < 1e-12, (P, W)
+
+
+def test_windowed_plan_with_no_window_is_the_plain_plan():
+    lens = np.array([100000, 5000, 300, 0, 70000], np.int32)
+    for kind in (oracle.PLAN_PROPORTIONAL, oracle.PLAN_UNIFORM):
+        a = oracle.plan(lens, None, 4, 256, 304, kind)
+        b = oracle.plan(lens, None, 4, 256, 304, kind, window=200000)  # wider than every S
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_windowed_plan_sizes_requests_by_their_window():
+    # A window of 1000 keys makes every request read at most 1000 (+ alignment)
+    # keys: the proportional shares follow the read ranges, not S.
+    lens = np.array([100000, 5000, 300], np.int32)
+    work, red = oracle.plan(lens, None, 4, 256, 304, window=1000)
+    # read ranges from the first visible key's tile: 100000-1000=99000 -> tile 386
+    # (98816): 1184 keys, 5 tiles; 5000-1000=4000 -> tile 15 (3840): 1160, 5
+    # tiles; 300: 300 keys, 2 tiles.  sum = 2644; C - n_act = 73:
+    # 1 + floor(73*1184/2644) = 33 -> 5; 1 + floor(73*1160/2644) = 33 -> 5; 1 + 8 -> 2
+    assert red[:, 1].tolist() == [5, 5, 2]
+    assert work[0, 1] == 386 and work[4, 2] == 391
