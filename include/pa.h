@@ -162,6 +162,30 @@ int pa_decode(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int num
               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
               const int32_t* cu_query_lens, int num_seqs, float scale, void* out, void* stream);
 
+/* Sliding window ("vllm-rdna pull 29", Change 1: the window applies per
+ * token; the aiter pa_decode signature the pages quote carries
+ * sliding_window): with sliding_window = W > 0, query token i, whose causal
+ * range is keys [0, K_i), attends only to [max(0, K_i - W), K_i); 0 (the
+ * default) turns the window off.  A plan property: it takes effect at the
+ * next pa_plan_refresh, which then sizes each request by the keys its tokens
+ * read (from the tile holding the first token's first visible key; tile
+ * indices in work_info stay absolute), and every pa_decode uses the window of
+ * the plan's last refresh.  PA_ERR_INVALID_ARG for W < 0. */
+int pa_plan_set_window(pa_plan* plan, int sliding_window);
+
+/* pa_decode with attention sinks (named in the same aiter signature): sinks
+ * is NULL or a device array of num_q_heads fp32 logits, in the units of
+ * scale * q.k, each joining its head's softmax denominator only:
+ * out = sum_j e^(s_j) v_j / (sum_j e^(s_j) + e^(sink)).  A row with no
+ * visible key is still 0.  Everything else is as pa_decode (which is this
+ * call with sinks = NULL). */
+int pa_decode_ex(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int num_q_heads,
+                 int head_dim, const void* k_cache, const void* v_cache, int kv_dtype,
+                 float k_scale, float v_scale, int num_blocks, int num_kv_heads, int block_size,
+                 const int32_t* block_tables, int max_blocks_per_seq,
+                 const int32_t* context_lens, const int32_t* cu_query_lens, int num_seqs,
+                 float scale, const float* sinks, void* out, void* stream);
+
 /* Size of the file-scope device array that pa_decode_static works in. */
 #define PA_STATIC_SCRATCH_BYTES (32u << 20)
 
@@ -170,7 +194,7 @@ int pa_decode(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int num
  * it exists for callers that cannot call cudaMalloc while decoding -- a serving
  * engine that hands nearly all HBM to its own KV-cache pool and caching
  * allocator, or code running inside a CUDA-graph capture -- and so cannot
- * create a pa_plan.
+ * create a pa_plan.  It has no sliding window and no sinks.
  *
  * Arguments mean what they mean for pa_plan_build and pa_decode; the plan
  * parameters (max_query_len, max_partitions, budget, kind) are passed per call
@@ -180,7 +204,10 @@ int pa_decode(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int num
  * keeps until the process exits.  A batch whose plan and partial results need
  * more than that is rejected with PA_ERR_UNSUPPORTED; the need is the
  * pa_plan_build footprint, dominated by the fp32 partials:
- * min(C x max_query_len, max_partitions x num_tokens) x Hq x (D + 1) x 4 bytes,
+ * Q x min(C x max_query_len, max_partitions x num_tokens) x Hq x (D + 1) x 4
+ * bytes, with Q = 4 when the split kernel may cut slots into pieces (single
+ * query row per request and C x Hkv <= 4 x SMs; dropped to 1 when that does
+ * not fit) and 1 otherwise,
  * with capacity C = min(n x P, max(n, ceil(W / Hkv))), plus about C x 24 +
  * n x 16 bytes of plan (and a list of row chunks when max_query_len x Hq/Hkv
  * exceeds 32).

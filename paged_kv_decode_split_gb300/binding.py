@@ -60,6 +60,9 @@ def load() -> ctypes.CDLL:
     lib.pa_plan_refresh.argtypes = [P, P, P, P]
     lib.pa_decode.argtypes = [P, P, i32, i32, i32, i32, P, P, i32, f32, f32, i32, i32, i32, P,
                               i32, P, P, i32, f32, P, P]
+    lib.pa_decode_ex.argtypes = [P, P, i32, i32, i32, i32, P, P, i32, f32, f32, i32, i32, i32, P,
+                                 i32, P, P, i32, f32, P, P, P]
+    lib.pa_plan_set_window.argtypes = [P, i32]
     lib.pa_plan_info.argtypes = [P, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                  ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32),
                                  ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_longlong)]
@@ -70,7 +73,8 @@ def load() -> ctypes.CDLL:
     lib.pa_plan_destroy.argtypes = [P]
     lib.pa_status_string.argtypes = [i32]
     lib.pa_status_string.restype = ctypes.c_char_p
-    for name in ("pa_plan_build", "pa_plan_refresh", "pa_decode", "pa_plan_info",
+    for name in ("pa_plan_build", "pa_plan_refresh", "pa_decode", "pa_decode_ex",
+                 "pa_plan_set_window", "pa_plan_info",
                  "pa_plan_download", "pa_plan_read_errors", "pa_plan_set_split_events",
                  "pa_plan_set_call_events",
                  "pa_plan_destroy"):
@@ -199,8 +203,12 @@ class Plan:
                block_tables: torch.Tensor, context_lens: torch.Tensor,
                cu_query_lens: Optional[torch.Tensor] = None, scale: Optional[float] = None,
                k_scale: float = 1.0, v_scale: float = 1.0, out: Optional[torch.Tensor] = None,
-               stream=None) -> torch.Tensor:
+               stream=None, sinks: Optional[torch.Tensor] = None) -> torch.Tensor:
         dev = self.device
+        if sinks is not None:
+            _need(sinks, "sinks", dev, (torch.float32,))
+            if sinks.shape != (q.shape[1],):
+                raise ValueError("sinks must be [num_q_heads] float32")
         _need(q, "q", dev, (torch.bfloat16, torch.float16))
         _need(k_cache, "k_cache", dev)
         _need(v_cache, "v_cache", dev, (k_cache.dtype,))
@@ -225,12 +233,17 @@ class Plan:
         if scale is None:
             scale = 1.0 / math.sqrt(D)
         qcode = FP16 if q.dtype == torch.float16 else BF16
-        _check(load().pa_decode(self._h, _ptr(q), qcode, T, Hq, D, _ptr(k_cache), _ptr(v_cache),
-                                kv_code(k_cache), float(k_scale), float(v_scale), nb, Hkv, bs,
-                                _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
-                                _ptr(cu_query_lens), context_lens.shape[0], float(scale),
-                                _ptr(out), _stream(dev, stream)), "pa_decode")
+        _check(load().pa_decode_ex(self._h, _ptr(q), qcode, T, Hq, D, _ptr(k_cache),
+                                   _ptr(v_cache), kv_code(k_cache), float(k_scale),
+                                   float(v_scale), nb, Hkv, bs, _ptr(block_tables),
+                                   block_tables.shape[1], _ptr(context_lens), _ptr(cu_query_lens),
+                                   context_lens.shape[0], float(scale), _ptr(sinks), _ptr(out),
+                                   _stream(dev, stream)), "pa_decode_ex")
         return out
+
+    def set_window(self, sliding_window: int):
+        """Sliding window for the next refresh on (0: none)."""
+        _check(load().pa_plan_set_window(self._h, int(sliding_window)), "pa_plan_set_window")
 
     def close(self):
         h, self._h = getattr(self, "_h", None), None
@@ -257,6 +270,7 @@ def plan_for(w, kind: int = PROPORTIONAL, budget: Optional[int] = None,
                 budget=(w.budget or 0) if budget is None else budget, kind=kind, device=device)
 
 
-def decode_workload(plan: Plan, w, out=None, stream=None) -> torch.Tensor:
+def decode_workload(plan: Plan, w, out=None, stream=None, sinks=None) -> torch.Tensor:
     return plan.decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
-                       w.cu_query_lens, w.scale, w.k_scale, w.v_scale, out=out, stream=stream)
+                       w.cu_query_lens, w.scale, w.k_scale, w.v_scale, out=out, stream=stream,
+                       sinks=sinks)

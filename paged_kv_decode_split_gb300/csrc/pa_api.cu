@@ -63,6 +63,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 struct pa_plan {
   int device, n, Hq, Hkv, D, max_qlen, max_tokens, P, W, kind, C, Q, rpc, sms;
+  int window;          // sliding window for the next refresh (0: none)
+  int window_planned;  // the window the last refresh planned with
   long long rows_cap, max_extra;
   pa::PlanDev dev;
   void* mem;
@@ -298,6 +300,7 @@ int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_q_heads, int
   pl->bytes = static_cast<long long>(total);
   pl->refreshed = 0;
   pl->ev_start = pl->ev_stop = nullptr;
+  pl->window = pl->window_planned = 0;
   pl->ev_call0 = pl->ev_call1 = nullptr;
   pl->tmap_next = 0;
   *plan = pl;
@@ -317,6 +320,7 @@ int pa_plan_refresh(pa_plan* plan, const int32_t* context_lens, const int32_t* c
   p.P = plan->P;
   p.C = plan->C;
   p.Q = plan->Q;
+  p.window = plan->window;
   p.kind = plan->kind;
   p.max_qlen = plan->max_qlen;
   p.max_tokens = plan->max_tokens;
@@ -327,6 +331,13 @@ int pa_plan_refresh(pa_plan* plan, const int32_t* context_lens, const int32_t* c
   p.dev = plan->dev;
   if (pa::launch_plan(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return PA_ERR_CUDA;
   plan->refreshed = cu_query_lens ? 2 : 1;
+  plan->window_planned = plan->window;
+  return PA_OK;
+}
+
+int pa_plan_set_window(pa_plan* plan, int sliding_window) {
+  if (!plan || sliding_window < 0) return PA_ERR_INVALID_ARG;
+  plan->window = sliding_window;
   return PA_OK;
 }
 
@@ -335,6 +346,18 @@ int pa_decode(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int num
               float v_scale, int num_blocks, int num_kv_heads, int block_size,
               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
               const int32_t* cu_query_lens, int num_seqs, float scale, void* out, void* stream) {
+  return pa_decode_ex(plan, q, q_dtype, num_tokens, num_q_heads, head_dim, k_cache, v_cache,
+                      kv_dtype, k_scale, v_scale, num_blocks, num_kv_heads, block_size,
+                      block_tables, max_blocks_per_seq, context_lens, cu_query_lens, num_seqs,
+                      scale, nullptr, out, stream);
+}
+
+int pa_decode_ex(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int num_q_heads,
+                 int head_dim, const void* k_cache, const void* v_cache, int kv_dtype,
+                 float k_scale, float v_scale, int num_blocks, int num_kv_heads, int block_size,
+                 const int32_t* block_tables, int max_blocks_per_seq,
+                 const int32_t* context_lens, const int32_t* cu_query_lens, int num_seqs,
+                 float scale, const float* sinks, void* out, void* stream) {
   if (!plan) return PA_ERR_INVALID_ARG;
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
     return PA_ERR_INVALID_ARG;
@@ -392,6 +415,8 @@ int pa_decode(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int num
   sp.scale_log2 = static_cast<float>(static_cast<double>(scale) * (fp8 ? k_scale : 1.0) *
                                      1.4426950408889634);
   sp.v_scale = fp8 ? v_scale : 1.0f;
+  sp.window = plan->window_planned;
+  sp.sinks = sinks;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int wq = pa::split_row_groups(plan->max_qlen, sp.G);
@@ -420,6 +445,7 @@ int pa_decode(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int num
   mp.Hq = num_q_heads;
   mp.D = head_dim;
   mp.out_f16 = sp.out_f16;
+  mp.sinks = sinks;
   const long long pairs = static_cast<long long>(num_tokens) * num_q_heads;
   mp.grid = static_cast<int>(pairs < 8ll * plan->sms ? pairs : 8ll * plan->sms);
   if (pa::launch_merge(mp, s) != cudaSuccess) return PA_ERR_CUDA;

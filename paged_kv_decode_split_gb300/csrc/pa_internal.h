@@ -65,6 +65,7 @@ struct PlanParams {
   const int* cu;  // nullable
   int n, Hkv, P, C, kind, max_qlen, max_tokens;
   int Q;          // at most Q pieces per slot
+  int window;     // sliding window (0: none): a request's plan starts at its first visible tile
   int G;          // q heads per kv head
   int rpc;        // query rows per split-kernel work item (row chunk)
   long long rows_cap;
@@ -87,6 +88,8 @@ struct SplitParams {
   int rpc;          // query rows per work item (row chunk); a multiple of 8 x row groups
   float scale_log2; // softmax scale * k_scale * log2(e)
   float v_scale;    // 1 for 16-bit caches
+  int window;       // sliding window: a row that may see keys [0, K) sees [K - window, K); 0: none
+  const float* sinks;  // [Hq] sink logits (scale * q.k units) or null
 };
 
 // Rows of one TMA box of a KV tile for head_dim D, cache dtype, block size.
@@ -105,7 +108,23 @@ struct MergeParams {
   const int* cu;  // nullable
   int num_tokens, n, Hq, D, out_f16;
   int grid;       // persistent grid size
+  const float* sinks;  // [Hq] sink logits (scale * q.k units) or null
 };
+
+// A softmax whose numerator and denominator W are relative to 2^M (log2 units)
+// gains a sink logit s2 (log2 units) in its denominator: W becomes the new
+// denominator relative to 2^max(M, s2), and the numerator must be multiplied
+// by the returned factor.  No-op for s2 = -inf.
+__device__ __forceinline__ float add_sink(float M, float s2, float& W) {
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  if (s2 == NEG_INF) return 1.f;
+  const float M2 = fmaxf(M, s2);
+  float y, f = 0.f;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(s2 - M2));
+  if (M != NEG_INF) asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(f) : "f"(M - M2));
+  W = W * f + y;
+  return f;
+}
 
 // Launches `kernel` with programmatic stream serialization: it may be
 // scheduled while the previous kernel on the stream is still running (every

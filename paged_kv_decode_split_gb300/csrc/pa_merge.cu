@@ -128,6 +128,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
           W += f * s_ws[k];
         }
       }
+      if (p.sinks) {  // the head's sink joins the denominator once, here
+        const float f = add_sink(M, __ldg(p.sinks + hq) * 1.4426950408889634f, W);
+        out.x *= f; out.y *= f; out.z *= f; out.w *= f;
+      }
       const float inv = W > 0.f ? 1.f / W : 0.f;
       const int t = c0 + tok;
       if (t >= p.num_tokens) {
@@ -200,6 +204,11 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     if (t >= p.num_tokens) {
       if (lane == 0) atomicOr(p.plan.err, PA_DEVERR_PLAN_OVERFLOW);
       continue;
+    }
+    if (p.sinks) {
+      const float f = add_sink(M, __ldg(p.sinks + hq) * 1.4426950408889634f, W);
+#pragma unroll
+      for (int v = 0; v < VL; ++v) acc[v] *= f;
     }
     const float inv = W > 0.f ? 1.f / W : 0.f;
     uint32_t pk[VL / 2];

@@ -129,6 +129,7 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
   int* s_prow = s_qlen + p.n;      // [n] first partial row
   int* s_pfirst = s_prow + p.n;    // [n] first piece, in request order
   int* s_xfirst = s_pfirst + p.n;  // [n] first extra item
+  int* s_t0 = s_xfirst + p.n;      // [n] first planned tile (sliding window; else 0)
   __shared__ long long s_red[kWarps], s_red2[kWarps];
   __shared__ int s_cnt[kWarps];
   __shared__ int s_bad;
@@ -143,8 +144,10 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
   if (tid < 128) s_bcnt[tid] = 0;
   __syncthreads();
 
-  // ---- 1. lengths, activity, validity; sum S and sum of tiles of active requests
-  int S[kPer], L[kPer];
+  // ---- 1. lengths, activity, validity; the planned range of each request
+  // (with a sliding window: from the tile holding its first token's first
+  // visible key; else from key 0), the sum of its lengths and of its tiles
+  int S[kPer], L[kPer], T0[kPer];
   long long my_sum = 0, my_tiles = 0;
   int my_act = 0, my_bad = 0;
 #pragma unroll
@@ -152,14 +155,20 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
     const int r = tid * per + k;
     S[k] = 0;
     L[k] = 0;
+    T0[k] = 0;
     if (k < per && r < n) {
       S[k] = p.context_lens[r];
       L[k] = p.cu ? p.cu[r + 1] - p.cu[r] : 1;
       if (L[k] < 0 || L[k] > p.max_qlen) my_bad = 1;
       if (S[k] > 0 && L[k] > 0) {
+        if (p.window > 0) {
+          const long long first = static_cast<long long>(S[k]) - (L[k] - 1) - p.window;
+          T0[k] = first > 0 ? static_cast<int>(first / kTile) : 0;
+        }
+        const int len = S[k] - T0[k] * kTile;
         my_act += 1;
-        my_sum += S[k];
-        my_tiles += (S[k] + kTile - 1) / kTile;
+        my_sum += len;
+        my_tiles += (len + kTile - 1) / kTile;
       }
     }
   }
@@ -193,10 +202,11 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
     nbase[k] = nbig[k] = 0;
     const int r = tid * per + k;
     if (k < per && r < n && !bad && S[k] > 0 && L[k] > 0) {
-      const long long tiles = (static_cast<long long>(S[k]) + kTile - 1) / kTile;
+      const int len = S[k] - T0[k] * kTile;  // the planned range
+      const long long tiles = (static_cast<long long>(len) + kTile - 1) / kTile;
       const long long share = (p.kind == PA_PLAN_UNIFORM)
                                   ? C / n_act
-                                  : 1 + floor_mul_div(C - n_act, S[k], sum_s);
+                                  : 1 + floor_mul_div(C - n_act, len, sum_s);
       long long v = p.P;
       if (tiles < v) v = tiles;
       if (share < v) v = share;
@@ -302,6 +312,7 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
       s_prow[r] = row0;
       s_pfirst[r] = piece0;
       s_xfirst[r] = extra0;
+      s_t0[r] = T0[k];
       if (pcs[k] >= 2) {
         int& m0 = pcs[k] <= kWarpMergePieces ? mfew0 : mmany0;
         for (int i = 0; i < L[k]; ++i)
@@ -350,13 +361,15 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
     o.r = lo;
     const int pr = s_parts[lo];
     const int j = slot - s_first[lo];
-    const int nt = (s_ctx[lo] + kTile - 1) / kTile;
-    o.tb = tile_split(j, nt, pr);
-    o.te = tile_split(j + 1, nt, pr);
+    const int t0 = s_t0[lo];
+    const int nt = (s_ctx[lo] - t0 * kTile + kTile - 1) / kTile;
+    const int rb = tile_split(j, nt, pr);  // relative to the planned range
+    o.tb = t0 + rb;
+    o.te = t0 + tile_split(j + 1, nt, pr);
     o.q = piece_count(o.te - o.tb, xcut, p.Q);
     const int base = nt / pr;
     const int qlo = piece_count(base, xcut, p.Q), qhi = piece_count(base + 1, xcut, p.Q);
-    o.before = j * qlo + (o.tb - j * base) * (qhi - qlo);
+    o.before = j * qlo + (rb - j * base) * (qhi - qlo);
     return o;
   };
   // Keys [kb, ke) of piece `sub` of a slot, and its launch-order class.
@@ -447,7 +460,7 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
   static bool attr_done = false;
-  const int smem = 7 * kMaxSeqs * static_cast<int>(sizeof(int));
+  const int smem = 8 * kMaxSeqs * static_cast<int>(sizeof(int));
   if (!attr_done) {
     cudaError_t e =
         cudaFuncSetAttribute(plan_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -456,7 +469,7 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  const int dyn = 7 * p.n * static_cast<int>(sizeof(int));
+  const int dyn = 8 * p.n * static_cast<int>(sizeof(int));
   if (p.n <= 128) return launch_pdl(plan_kernel<128>, dim3(1), dim3(128), dyn, s, p);
   return launch_pdl(plan_kernel<1024>, dim3(1), dim3(1024), dyn, s, p);
 }

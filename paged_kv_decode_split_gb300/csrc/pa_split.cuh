@@ -355,12 +355,15 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
     const int ke = pass_key_end(pass);
     const int nst = ke > kb ? (ke - kb + Cfg::KS - 1) / Cfg::KS : 0;
 
-    // Key limit of this thread's two accumulator columns (query rows).
-    int lim[2];
+    // Key limits of this thread's two accumulator columns (query rows): keys
+    // [llo, lim) are visible (llo > 0 only under a sliding window).
+    int lim[2], llo[2];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int n = pass_base + 8 * wq + 2 * t + e;
-      lim[e] = (n < row_hi) ? min(ke_task, S - (L - 1 - n / G)) : kb;
+      const int K = S - (L - 1 - n / G);  // causal range [0, K) of this row's token
+      lim[e] = (n < row_hi) ? min(ke_task, K) : kb;
+      llo[e] = p.window > 0 ? max(0, K - p.window) : 0;
     }
 
     // Q^T as the B operand of QK^T: row n = groupID of this warp's 8 rows.
@@ -479,10 +482,10 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
 #pragma unroll
         for (int tt = 0; tt < T; ++tt) {
           const int k_lo = key0 + rbase + 16 * tt + g;
-          sv[tt][0] = (k_lo < lim[0]) ? c[tt][0] * sl2 : NEG_INF;
-          sv[tt][1] = (k_lo < lim[1]) ? c[tt][1] * sl2 : NEG_INF;
-          sv[tt][2] = (k_lo + 8 < lim[0]) ? c[tt][2] * sl2 : NEG_INF;
-          sv[tt][3] = (k_lo + 8 < lim[1]) ? c[tt][3] * sl2 : NEG_INF;
+          sv[tt][0] = (k_lo < lim[0] && k_lo >= llo[0]) ? c[tt][0] * sl2 : NEG_INF;
+          sv[tt][1] = (k_lo < lim[1] && k_lo >= llo[1]) ? c[tt][1] * sl2 : NEG_INF;
+          sv[tt][2] = (k_lo + 8 < lim[0] && k_lo + 8 >= llo[0]) ? c[tt][2] * sl2 : NEG_INF;
+          sv[tt][3] = (k_lo + 8 < lim[1] && k_lo + 8 >= llo[1]) ? c[tt][3] * sl2 : NEG_INF;
           mx0 = fmaxf(mx0, fmaxf(sv[tt][0], sv[tt][2]));
           mx1 = fmaxf(mx1, fmaxf(sv[tt][1], sv[tt][3]));
         }
@@ -640,10 +643,16 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
           o0 += w * v.x; o1 += w * v.y; o2 += w * v.z; o3 += w * v.w;
         }
       }
-      const float inv = lsum > 0.f ? p.v_scale / lsum : 0.f;
-      o0 *= inv; o1 *= inv; o2 *= inv; o3 *= inv;
       const int tok = n / G;
       const int hq = h * G + n % G;
+      // A single piece writes the output row: its head's sink joins here (a
+      // request with several pieces gets it in the merge).
+      if (prow_base < 0 && p.sinks) {
+        const float f = add_sink(M, __ldg(p.sinks + hq) * 1.4426950408889634f, lsum);
+        o0 *= f; o1 *= f; o2 *= f; o3 *= f;
+      }
+      const float inv = lsum > 0.f ? p.v_scale / lsum : 0.f;
+      o0 *= inv; o1 *= inv; o2 *= inv; o3 *= inv;
       if (prow_base < 0) {
         const int trow = row0 + tok;
         if (trow >= p.num_tokens) {

@@ -175,6 +175,7 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
   pp.P = max_partitions;
   pp.C = static_cast<int>(lay.C);
   pp.Q = lay.Q;
+  pp.window = 0;
   pp.kind = kind;
   pp.max_qlen = max_query_len;
   pp.max_tokens = num_tokens;
@@ -205,6 +206,8 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
   sp.total_rows = num_blocks * num_kv_heads * block_size;
   sp.out_f16 = q_dtype == PA_FP16 ? 1 : 0;
   sp.rpc = lay.rpc;
+  sp.window = 0;
+  sp.sinks = nullptr;
   sp.scale_log2 = static_cast<float>(static_cast<double>(scale) * (fp8 ? k_scale : 1.0) *
                                      1.4426950408889634);
   sp.v_scale = fp8 ? v_scale : 1.0f;
@@ -221,6 +224,7 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
   mp.Hq = num_q_heads;
   mp.D = head_dim;
   mp.out_f16 = sp.out_f16;
+  mp.sinks = nullptr;
   const long long pairs = static_cast<long long>(num_tokens) * num_q_heads;
   mp.grid = static_cast<int>(pairs < 8ll * sms ? pairs : 8ll * sms);
   if (pa::launch_merge(mp, s) != cudaSuccess) return PA_ERR_CUDA;

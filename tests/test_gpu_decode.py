@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import oracle_decode
+from helpers import oracle_plan, oracle_decode
 from paged_kv_decode_split_gb300 import binding, workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -102,6 +102,77 @@ def test_uneven_slots_run_as_pieces(dev, kv):
     ref = oracle_decode(w.to("cpu"))
     assert max_diff(out, ref) <= TOL[kv]
     assert plan.read_errors() == 0
+
+
+# ------------------------------------------------- sliding window and sinks
+
+def run_ext(w, window=0, sinks=None, budget=None, max_partitions=None):
+    plan = binding.plan_for(w, binding.PROPORTIONAL, budget, max_partitions)
+    plan.set_window(window)
+    plan.refresh(w.context_lens, w.cu_query_lens)
+    sk = None if sinks is None else torch.tensor(sinks, dtype=torch.float32, device=w.q.device)
+    o = binding.decode_workload(plan, w, sinks=sk)
+    torch.cuda.synchronize()
+    return o, plan
+
+
+@pytest.mark.parametrize("window", [1, 3, 50, 500])
+@pytest.mark.parametrize("kv,D,bs", [("bf16", 128, 16), ("fp8", 128, 16), ("bf16", 64, 64),
+                                     ("fp16", 256, 128)])
+def test_sliding_window_decode(dev, window, kv, D, bs):
+    q = "fp16" if kv == "fp16" else "bf16"
+    w = batch(dev, RAGGED + [6000], H=(8, 2), D=D, bs=bs, kv=kv, q=q, seed=window + D)
+    out, plan = run_ext(w, window=window)
+    ref = oracle_decode(w.to("cpu"), window=window)
+    assert max_diff(out, ref) <= TOL[kv]
+    assert plan.read_errors() == 0
+
+
+@pytest.mark.parametrize("window", [1, 50])
+def test_sliding_window_verify_rows(dev, window):
+    w = batch(dev, [600, 40, 3000, 2], ql=[3, 3, 3, 3], H=(6, 1), D=256, bs=64, pad=5, seed=21)
+    out, plan = run_ext(w, window=window)
+    ref = oracle_decode(w.to("cpu"), window=window)
+    assert max_diff(out, ref) <= TOL["bf16"]
+    assert torch.all(out[12:] == 0)
+
+
+@pytest.mark.parametrize("window", [37, 700])
+def test_windowed_plan_is_bit_exact(dev, window):
+    for w in (wl.skewed(0, dev), batch(dev, [600, 40, 3000, 2], ql=[3, 3, 3, 3], H=(6, 1), D=256,
+                                       bs=64, seed=22)):
+        plan = binding.plan_for(w)
+        plan.set_window(window)
+        plan.refresh(w.context_lens, w.cu_query_lens)
+        work, red = plan.download()
+        ow, orr = oracle_plan(w, plan.info()["budget"], window=window)
+        assert np.array_equal(work.numpy(), ow) and np.array_equal(red.numpy(), orr)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("P,W", [(1, 8), (8, 64), (256, 4096)])
+def test_sinks_direct_few_and_many_pieces(dev, kv, P, W):
+    """Sinks on rows written by one CTA (P = 1), merged by a warp (a few
+    partitions) and merged by a CTA (hundreds of partitions), with and without
+    a window; one head's sink at -inf is no sink."""
+    w = batch(dev, [9000, 40, 2600, 0, 700], H=(8, 2), D=128, kv=kv, seed=23)
+    rng = np.random.default_rng(5)
+    sinks = rng.normal(0.0, 3.0, 8)
+    sinks[3] = -np.inf
+    for window in (0, 300):
+        out, plan = run_ext(w, window=window, sinks=sinks, budget=W, max_partitions=P)
+        ref = oracle_decode(w.to("cpu"), window=window, sinks=sinks)
+        assert max_diff(out, ref) <= TOL[kv], window
+        assert plan.read_errors() == 0
+
+
+def test_window_with_pieces(dev):
+    w = batch(dev, [40000] + [300 + 37 * i for i in range(15)], H=(8, 2), D=128, seed=24,
+              budget=32)
+    for window in (5000, 20000):
+        out, _ = run_ext(w, window=window, sinks=np.linspace(-2, 2, 8))
+        ref = oracle_decode(w.to("cpu"), window=window, sinks=np.linspace(-2, 2, 8))
+        assert max_diff(out, ref) <= TOL["bf16"], window
 
 
 # ---------------------------------------------------- multi-token rows (cu)
