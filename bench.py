@@ -53,6 +53,8 @@ DESCRIBE = {
                   "D 128, page 128, bf16",
     "large_fp8": "large skewed: 512 seqs, ctx lognormal(2048, 1.2) in [16,65536], Hq/Hkv 64/8, "
                  "D 128, page 128, fp8-e4m3 KV",
+    "uniform_w1024": "uniform decode under a 1024-key sliding window",
+    "skewed_w4096": "skewed agentic decode under a 4096-key sliding window",
 }
 SPLIT_SOURCES = ["pa_split.cuh", "pa_device.cuh"]
 L2_BYTES = 129 * 1024 * 1024
@@ -225,7 +227,7 @@ def _run_oracle(w):
     qc = oracle.FP16 if w.q.dtype == torch.float16 else oracle.BF16
     cu = None if w.cu_query_lens is None else w.cu_query_lens.cpu().numpy()
     return oracle.decode(q, qc, k, v, code, w.k_scale, w.v_scale, w.block_tables.cpu().numpy(),
-                         w.context_lens.cpu().numpy(), cu, w.scale)
+                         w.context_lens.cpu().numpy(), cu, w.scale, window=w.window)
 
 
 # ------------------------------------------------------------ GPU timings

@@ -264,10 +264,13 @@ def plan_for(w, kind: int = PROPORTIONAL, budget: Optional[int] = None,
     if w.cu_query_lens is not None:
         cu = w.cu_query_lens.cpu()
         ql = max(1, int((cu[1:] - cu[:-1]).max()))
-    return Plan(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, max_query_len=ql,
+    plan = Plan(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, max_query_len=ql,
                 max_tokens=w.num_tokens,
                 max_partitions=w.max_partitions if max_partitions is None else max_partitions,
                 budget=(w.budget or 0) if budget is None else budget, kind=kind, device=device)
+    if getattr(w, "window", 0):
+        plan.set_window(w.window)
+    return plan
 
 
 def decode_workload(plan: Plan, w, out=None, stream=None, sinks=None) -> torch.Tensor:

@@ -51,6 +51,7 @@ class Workload:
     budget: Optional[int] = None        # None: 2 x SM count of the device
     max_partitions: int = 256
     meta: dict = field(default_factory=dict)
+    window: int = 0                     # sliding window (0: none)
 
     @property
     def num_seqs(self) -> int:
@@ -65,9 +66,19 @@ class Workload:
         return 1 if self.kv_dtype == "fp8" else 2
 
     def kv_bytes(self) -> int:
-        """Algorithmic KV bytes of one decode call: every key and value row of
-        every (request, kv head) read once."""
-        s = int(self.context_lens.clamp(min=0).sum().item())
+        """Algorithmic KV bytes of one decode call: every key and value row a
+        request's tokens can see, per (request, kv head), read once (under a
+        sliding window W: the last W + L - 1 keys of a request with L tokens)."""
+        lens = self.context_lens.clamp(min=0).to(torch.int64).cpu()
+        if self.window > 0:
+            if self.cu_query_lens is None:
+                L = torch.ones_like(lens)
+            else:
+                cu = self.cu_query_lens.to(torch.int64).cpu()
+                L = cu[1:] - cu[:-1]
+            lens = torch.minimum(lens, self.window + L - 1)
+            lens[L == 0] = 0
+        s = int(lens.sum().item())
         return s * self.num_kv_heads * self.head_dim * 2 * self.kv_elem_bytes
 
     def to(self, device) -> "Workload":
@@ -76,7 +87,7 @@ class Workload:
                         self.k_scale, self.v_scale, mv(self.block_tables), mv(self.context_lens),
                         mv(self.cu_query_lens), self.scale, self.num_q_heads, self.num_kv_heads,
                         self.head_dim, self.block_size, self.budget, self.max_partitions,
-                        dict(self.meta))
+                        dict(self.meta), self.window)
 
 
 def _gen(seed: int, device) -> torch.Generator:
@@ -208,6 +219,21 @@ def large(kv_dtype: str = "bf16", seed: int = 0, device="cpu") -> Workload:
                       kv_scale=0.05, device=device)
 
 
+def uniform_window(seed: int = 0, device="cpu") -> Workload:
+    """The uniform batch under a 1024-key sliding window (each request reads its
+    last 1024 keys)."""
+    w = uniform(seed, device)
+    w.name, w.window = "uniform_w1024", 1024
+    return w
+
+
+def skewed_window(seed: int = 0, device="cpu") -> Workload:
+    """The skewed batch under a 4096-key sliding window."""
+    w = skewed(seed, device)
+    w.name, w.window = "skewed_w4096", 4096
+    return w
+
+
 CONFIGS = {
     "tiny": tiny,
     "uniform": uniform,
@@ -216,6 +242,8 @@ CONFIGS = {
     "mixed_prompt": mixed_prompt,
     "large_bf16": lambda seed=0, device="cpu": large("bf16", seed, device),
     "large_fp8": lambda seed=0, device="cpu": large("fp8", seed, device),
+    "uniform_w1024": uniform_window,
+    "skewed_w4096": skewed_window,
 }
 
 
@@ -255,4 +283,4 @@ def subset(w: Workload, requests: Sequence[int]) -> Workload:
         ncu[1:] = torch.cumsum(torch.tensor(qlens), 0).to(torch.int32)
     return Workload(w.name + "_subset", q, k, v, w.kv_dtype, w.k_scale, w.v_scale, nbt,
                     lens[requests].clone(), ncu, w.scale, w.num_q_heads, w.num_kv_heads,
-                    w.head_dim, w.block_size, w.budget, w.max_partitions, dict(w.meta))
+                    w.head_dim, w.block_size, w.budget, w.max_partitions, dict(w.meta), w.window)

@@ -379,7 +379,7 @@ def test_profiling_events_bracket_the_call_and_the_split(dev):
 
 def _sampled(w, out, requests):
     sub = wl.subset(w, requests)
-    ref = oracle_decode(sub)
+    ref = oracle_decode(sub, window=w.window)
     if w.cu_query_lens is None:
         rows = torch.tensor(requests)
     else:
@@ -398,7 +398,8 @@ def _pick(w, k=4):
     return sorted(picks)
 
 
-FULL = ["uniform", "skewed", "mtp_verify", "mixed_prompt", "large_bf16", "large_fp8"]
+FULL = ["uniform", "skewed", "mtp_verify", "mixed_prompt", "large_bf16", "large_fp8",
+        "uniform_w1024", "skewed_w4096"]
 
 
 @pytest.mark.parametrize("name", FULL)

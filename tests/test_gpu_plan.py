@@ -21,7 +21,7 @@ def dev():
 
 
 def _gpu_plan(dev, lens, cu, Hq, Hkv, D=128, P=0, W=0, kind=binding.PROPORTIONAL, max_qlen=None,
-              max_tokens=None):
+              max_tokens=None, window=0):
     n = len(lens)
     if max_qlen is None:
         max_qlen = 1 if cu is None else max(1, int(np.max(np.diff(cu))))
@@ -29,6 +29,7 @@ def _gpu_plan(dev, lens, cu, Hq, Hkv, D=128, P=0, W=0, kind=binding.PROPORTIONAL
         max_tokens = n if cu is None else max(1, int(cu[-1]))
     plan = binding.Plan(n, Hq, Hkv, D, max_query_len=max_qlen, max_tokens=max_tokens,
                         max_partitions=P, budget=W, kind=kind, device=dev)
+    plan.set_window(window)
     lt = torch.tensor(np.asarray(lens, np.int32), device=dev)
     ct = None if cu is None else torch.tensor(np.asarray(cu, np.int32), device=dev)
     plan.refresh(lt, ct)
@@ -36,10 +37,10 @@ def _gpu_plan(dev, lens, cu, Hq, Hkv, D=128, P=0, W=0, kind=binding.PROPORTIONAL
     return plan, work.numpy(), red.numpy()
 
 
-def _oracle_plan(plan, lens, cu, Hkv, kind):
+def _oracle_plan(plan, lens, cu, Hkv, kind, window=0):
     info = plan.info()
     return oracle.plan(np.asarray(lens, np.int32), None if cu is None else np.asarray(cu, np.int32),
-                       Hkv, info["max_partitions"], info["budget"], kind)
+                       Hkv, info["max_partitions"], info["budget"], kind, window=window)
 
 
 @pytest.mark.parametrize("name", list(wl.CONFIGS))
@@ -48,13 +49,13 @@ def test_config_plans_bit_exact(dev, name, kind):
     w = wl.CONFIGS[name](0, "cpu") if name not in ("large_bf16", "large_fp8") else None
     if w is None:  # only the lengths matter: skip drawing 8 GB of cache values
         lens = wl.lognormal_lengths(512, 2048, 1.2, 16, 65536, 0)
-        cu, Hq, Hkv, W = None, 64, 8, 0
+        cu, Hq, Hkv, W, win = None, 64, 8, 0, 0
     else:
         lens = w.context_lens.tolist()
         cu = None if w.cu_query_lens is None else w.cu_query_lens.tolist()
-        Hq, Hkv, W = w.num_q_heads, w.num_kv_heads, w.budget or 0
-    plan, work, red = _gpu_plan(dev, lens, cu, Hq, Hkv, W=W, kind=kind)
-    ow, orr = _oracle_plan(plan, lens, cu, Hkv, kind)
+        Hq, Hkv, W, win = w.num_q_heads, w.num_kv_heads, w.budget or 0, w.window
+    plan, work, red = _gpu_plan(dev, lens, cu, Hq, Hkv, W=W, kind=kind, window=win)
+    ow, orr = _oracle_plan(plan, lens, cu, Hkv, kind, window=win)
     assert np.array_equal(work, ow)
     assert np.array_equal(red, orr)
     assert plan.read_errors() == 0
