@@ -102,9 +102,23 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  if (warp == 0 && lane == 0) {  // descriptor fetch overlaps the planner's tail
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  float* ex = reinterpret_cast<float*>(smem_raw + (base - raw));
+  const uint32_t bar_full = base + Cfg::DATA_BYTES;
+  const uint32_t bar_empty = bar_full + 8 * Cfg::NS;
+  __shared__ int s_abort;  // set when a bounded wait gave up
+  if (warp == 0 && lane == 0) {  // all of this overlaps the planner's tail
     prefetch_tmap(&tmk);
     prefetch_tmap(&tmv);
+    s_abort = 0;
+    for (int s = 0; s < Cfg::NS; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, Cfg::NCW);
+    }
+    fence_barrier_init();
   }
   pdl_wait();  // the plan (and everything before this kernel) is complete
   // (The work counter this kernel takes items from is reset by the merge
@@ -118,12 +132,14 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
     cta_exit();
     return;
   }
-  // This CTA's first piece, read together with the counts it depends on.
-  // Item slots, double-buffered: round k reads slot k & 1 while the producer
-  // may already claim round k + 1's item into the other slot.
+  // This CTA's first item -- piece blockIdx / Hkv, head blockIdx % Hkv --
+  // read together with the counts it depends on.  Item slots are
+  // double-buffered: round k reads slot k & 1 while the producer may already
+  // claim round k + 1's item into the other slot.
   __shared__ int s_item[2][4];
   __shared__ int4 s_rec[2];
   __shared__ int s_npieces, s_nextra;
+  __shared__ int s_pre;  // 1: the next round's slot already holds its item
   if (threadIdx.x == 0) {
     const int npieces = p.plan.counters[4];
     const int nextra = p.plan.counters[0];
@@ -131,23 +147,13 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
     s_npieces = npieces;
     s_nextra = nextra;
     s_rec[0] = rec;
-  }
-
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  float* ex = reinterpret_cast<float*>(smem_raw + (base - raw));
-  const uint32_t bar_full = base + Cfg::DATA_BYTES;
-  const uint32_t bar_empty = bar_full + 8 * Cfg::NS;
-
-  __shared__ int s_abort;  // set when a bounded wait gave up
-  if (threadIdx.x == 0) {
-    s_abort = 0;
-    for (int s = 0; s < Cfg::NS; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, Cfg::NCW);
-    }
-    fence_barrier_init();
+    s_pre = 0;
+    const int late = (npieces > p.C ? npieces - p.C : 0) * p.Hkv;
+    const bool mine = static_cast<int>(blockIdx.x / p.Hkv) < npieces;
+    s_item[0][0] = mine ? static_cast<int>(blockIdx.x / p.Hkv) : -1;
+    s_item[0][1] = mine ? static_cast<int>(blockIdx.x % p.Hkv) : 0;
+    s_item[0][2] = 0;
+    s_item[0][3] = (mine || late > 0 || nextra > 0) ? 1 : 0;  // 0: nothing now or later
   }
   __syncthreads();
   // Warp-uniform view of the abort flag; raising it sets PA_DEVERR_TIMEOUT.
@@ -173,7 +179,6 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
   // The producer calls it as soon as it has issued the last stage of an item,
   // so that the claim and the record load overlap the consumers' last stages;
   // the loop head calls it when that did not happen.
-  __shared__ int s_pre;  // 1: the next round's slot already holds its item
   auto claim_next = [&](int sl) {
     const int npieces = s_npieces, nextra = s_nextra;
     const int late = (npieces > p.C ? npieces - p.C : 0) * Hkv;
@@ -200,31 +205,17 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
     s_item[sl][2] = chunk;
     s_item[sl][3] = valid;
   };
-  if (threadIdx.x == 0) s_pre = 0;
   for (int round = 0;; ++round) {
-    __syncthreads();  // everyone has read the previous item
-    if (threadIdx.x == 0) {
-      if (round == 0) {
-        const int npieces = s_npieces;
-        const int late = (npieces > p.C ? npieces - p.C : 0) * Hkv;
-        int pos = -1, hh = 0, valid = 1;
-        if (static_cast<int>(blockIdx.x / Hkv) < npieces) {
-          pos = blockIdx.x / Hkv;
-          hh = blockIdx.x % Hkv;
-        } else if (late == 0 && s_nextra == 0) {
-          valid = 0;  // nothing for this CTA, now or later
-        }
-        s_item[0][0] = pos;
-        s_item[0][1] = hh;
-        s_item[0][2] = 0;
-        s_item[0][3] = valid;
-      } else if (s_pre) {
-        s_pre = 0;  // claimed ahead by the producer
-      } else {
-        claim_next(round & 1);
+    if (round > 0) {  // round 0's item was set up with the prologue
+      __syncthreads();  // everyone has read the previous item
+      if (threadIdx.x == 0) {
+        if (s_pre)
+          s_pre = 0;  // claimed ahead by the producer
+        else
+          claim_next(round & 1);
       }
+      __syncthreads();
     }
-    __syncthreads();
     const int sl = round & 1;
     if (!s_item[sl][3]) break;
     if (s_item[sl][0] < 0) continue;  // no piece for this CTA: look for extra items
