@@ -70,14 +70,14 @@ def _load():
                                       P, i32, P, P, i32, dbl, P]
         lib.oracle_decode.restype = None
         lib.oracle_decode_ext.argtypes = [P, i32, i32, i32, i32, P, P, i32, dbl, dbl, i32, i32,
-                                          P, i32, P, P, i32, dbl, i32, P, P]
+                                          P, i32, P, P, i32, dbl, i32, P, i32, P]
         lib.oracle_decode_ext.restype = None
         lib.oracle_decode_planned.argtypes = [P, i32, i32, i32, i32, P, P, i32, dbl, dbl, i32,
                                               i32, P, i32, P, P, i32, dbl, P, P, i32, P]
         lib.oracle_decode_planned.restype = None
         lib.oracle_decode_planned_ext.argtypes = [P, i32, i32, i32, i32, P, P, i32, dbl, dbl,
                                                   i32, i32, P, i32, P, P, i32, dbl, P, P, i32,
-                                                  i32, P, P]
+                                                  i32, P, i32, P]
         lib.oracle_decode_planned_ext.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = i32
@@ -143,8 +143,10 @@ def _decode_args(q_bits, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale, 
     lens = _c(context_lens, np.int32)
     cu = _c(cu_query_lens, np.int32)
     T, Hq, D = q.shape
-    _, Hkv, bs, Dk = k.shape
-    assert Dk == D and v.shape == k.shape and Hq % Hkv == 0
+    _, Hkv, bs, Dv = v.shape
+    # K: [nb, Hkv, bs, D], or the 5-D [nb, Hkv, D/16, bs, 16]
+    assert k.shape == v.shape or k.shape == (v.shape[0], Hkv, D // 16, bs, 16)
+    assert Dv == D and Hq % Hkv == 0
     out = np.zeros((T, Hq, D), dtype=np.float64)
     args = [_ptr(q), q_dtype, T, Hq, D, _ptr(k), _ptr(v), kv_dtype, float(k_scale),
             float(v_scale), Hkv, bs, _ptr(bt), bt.shape[1], _ptr(lens), _ptr(cu),
@@ -156,12 +158,14 @@ def _decode_args(q_bits, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale, 
 def decode(q_bits, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale, block_tables,
            context_lens, cu_query_lens, scale, window: int = 0, sinks=None):
     """Exact paged decode in fp64 (sliding window: 0 = none; sinks: [Hq] logits or
-    None).  Returns out [num_tokens, Hq, D] float64."""
+    None; K in either layout, told apart by its rank).  Returns out
+    [num_tokens, Hq, D] float64."""
     args, out, _keep = _decode_args(q_bits, q_dtype, k_cache, v_cache, kv_dtype, k_scale,
                                     v_scale, block_tables, context_lens, cu_query_lens, scale)
-    if window or sinks is not None:
+    k_layout = 1 if np.ndim(k_cache) == 5 else 0
+    if window or sinks is not None or k_layout:
         sk = _c(sinks, np.float64)
-        _load().oracle_decode_ext(*args, int(window), _ptr(sk), _ptr(out))
+        _load().oracle_decode_ext(*args, int(window), _ptr(sk), k_layout, _ptr(out))
     else:
         _load().oracle_decode(*args, _ptr(out))
     return out
@@ -176,10 +180,11 @@ def decode_planned(q_bits, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale
                                     v_scale, block_tables, context_lens, cu_query_lens, scale)
     w = _c(work_info, np.int32)
     r = _c(reduce_info, np.int32)
-    if window or sinks is not None:
+    k_layout = 1 if np.ndim(k_cache) == 5 else 0
+    if window or sinks is not None or k_layout:
         sk = _c(sinks, np.float64)
         _load().oracle_decode_planned_ext(*args, _ptr(w), _ptr(r), tile, int(window), _ptr(sk),
-                                          _ptr(out))
+                                          k_layout, _ptr(out))
     else:
         _load().oracle_decode_planned(*args, _ptr(w), _ptr(r), tile, _ptr(out))
     return out

@@ -44,7 +44,10 @@
  *     the rule on that range's length (tile indices stay absolute);
  *   - attention sinks (named in the pa_decode signature the pages quote): a
  *     logit per q head, in the units of scale * q.k, that joins the softmax
- *     denominator only: out = sum_j e^(s_j) v_j / (sum_j e^(s_j) + e^(sink)).
+ *     denominator only: out = sum_j e^(s_j) v_j / (sum_j e^(s_j) + e^(sink));
+ *   - K may also come in the 5-D layout [num_blocks, Hkv, D/16, block_size, 16]
+ *     the pages' gate checks (the head dim in 16-element groups, each group's
+ *     rows contiguous per page); V keeps [num_blocks, Hkv, block_size, D].
  */
 #include <math.h>
 #include <stdint.h>
@@ -210,6 +213,7 @@ struct kv_view {
   double k_scale, v_scale;
   int num_kv_heads, block_size, head_dim, max_blocks;
   const int32_t* block_tables;
+  int k_layout;  /* 0: [nb, Hkv, bs, D]; 1: [nb, Hkv, D/16, bs, 16] */
 };
 
 /* Flat element index of key j's row of request r, kv head h, in a cache laid
@@ -220,12 +224,21 @@ static int64_t key_row(const struct kv_view* kv, int r, int h, long long j) {
          kv->head_dim;
 }
 
+/* Flat element index of element d of key j's K row of request r, kv head h. */
+static int64_t key_elem(const struct kv_view* kv, int r, int h, long long j, int d) {
+  if (kv->k_layout == 0) return key_row(kv, r, h, j) + d;
+  int32_t page = kv->block_tables[(int64_t)r * kv->max_blocks + j / kv->block_size];
+  int64_t slab = (int64_t)page * kv->num_kv_heads + h;  /* one (page, head): D/16 x bs x 16 */
+  return ((slab * (kv->head_dim / 16) + d / 16) * kv->block_size + j % kv->block_size) * 16 +
+         d % 16;
+}
+
 static double logit(const struct kv_view* kv, const void* q, int q_dtype, int64_t qoff, int r,
                     int h, long long j, double scale) {
-  int64_t krow = key_row(kv, r, h, j);
   double dot = 0.0;
   for (int d = 0; d < kv->head_dim; ++d)
-    dot += load_q(q, q_dtype, qoff + d) * load_kv(kv->k, kv->dtype, krow + d, kv->k_scale);
+    dot += load_q(q, q_dtype, qoff + d) *
+           load_kv(kv->k, kv->dtype, key_elem(kv, r, h, j, d), kv->k_scale);
   return scale * dot;
 }
 
@@ -253,11 +266,11 @@ void oracle_decode_ext(const void* q, int q_dtype, int num_tokens, int num_q_hea
                        double v_scale, int num_kv_heads, int block_size,
                        const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
                        const int32_t* cu, int n, double scale, int window, const double* sinks,
-                       double* out) {
+                       int k_layout, double* out) {
   struct kv_view kv = {k_cache, v_cache, kv_dtype,
                        kv_dtype == OR_FP8_E4M3 ? k_scale : 1.0,
                        kv_dtype == OR_FP8_E4M3 ? v_scale : 1.0,
-                       num_kv_heads, block_size, head_dim, max_blocks, block_tables};
+                       num_kv_heads, block_size, head_dim, max_blocks, block_tables, k_layout};
   int group = num_q_heads / num_kv_heads;
   long long total = (long long)num_tokens * num_q_heads;
 
@@ -300,7 +313,7 @@ void oracle_decode(const void* q, int q_dtype, int num_tokens, int num_q_heads, 
                    const int32_t* cu, int n, double scale, double* out) {
   oracle_decode_ext(q, q_dtype, num_tokens, num_q_heads, head_dim, k_cache, v_cache, kv_dtype,
                     k_scale, v_scale, num_kv_heads, block_size, block_tables, max_blocks,
-                    context_lens, cu, n, scale, 0, NULL, out);
+                    context_lens, cu, n, scale, 0, NULL, 0, out);
 }
 
 /* Planned decode, computed the way the method computes it: each task of the
@@ -315,11 +328,11 @@ void oracle_decode_planned_ext(const void* q, int q_dtype, int num_tokens, int n
                                const int32_t* context_lens, const int32_t* cu, int n,
                                double scale, const int32_t* work_info,
                                const int32_t* reduce_info, int tile, int window,
-                               const double* sinks, double* out) {
+                               const double* sinks, int k_layout, double* out) {
   struct kv_view kv = {k_cache, v_cache, kv_dtype,
                        kv_dtype == OR_FP8_E4M3 ? k_scale : 1.0,
                        kv_dtype == OR_FP8_E4M3 ? v_scale : 1.0,
-                       num_kv_heads, block_size, head_dim, max_blocks, block_tables};
+                       num_kv_heads, block_size, head_dim, max_blocks, block_tables, k_layout};
   int group = num_q_heads / num_kv_heads;
   long long total = (long long)num_tokens * num_q_heads;
 
@@ -391,7 +404,7 @@ void oracle_decode_planned(const void* q, int q_dtype, int num_tokens, int num_q
   oracle_decode_planned_ext(q, q_dtype, num_tokens, num_q_heads, head_dim, k_cache, v_cache,
                             kv_dtype, k_scale, v_scale, num_kv_heads, block_size, block_tables,
                             max_blocks, context_lens, cu, n, scale, work_info, reduce_info, tile,
-                            0, NULL, out);
+                            0, NULL, 0, out);
 }
 
 /* Threads an OpenMP region of this library uses (1 without OpenMP). */

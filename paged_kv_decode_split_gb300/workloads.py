@@ -247,6 +247,17 @@ CONFIGS = {
 }
 
 
+def with_k_groups(w: Workload) -> Workload:
+    """The same batch with K stored in the 5-D layout [num_blocks, Hkv, D/16,
+    block_size, 16] (the head dim in 16-element groups; V unchanged)."""
+    nb, hkv, bs, d = w.k_cache.shape
+    k5 = w.k_cache.view(nb, hkv, bs, d // 16, 16).permute(0, 1, 3, 2, 4).contiguous()
+    return Workload(w.name + "_k5", w.q, k5, w.v_cache, w.kv_dtype, w.k_scale, w.v_scale,
+                    w.block_tables, w.context_lens, w.cu_query_lens, w.scale, w.num_q_heads,
+                    w.num_kv_heads, w.head_dim, w.block_size, w.budget, w.max_partitions,
+                    dict(w.meta), w.window)
+
+
 def subset(w: Workload, requests: Sequence[int]) -> Workload:
     """The sub-batch of the given requests, with their pages copied into a compact
     pool (same bytes, same page order inside each request).  Every output row of a

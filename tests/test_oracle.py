@@ -526,3 +526,36 @@ def test_windowed_plan_sizes_requests_by_their_window():
     # 1 + floor(73*1184/2644) = 33 -> 5; 1 + floor(73*1160/2644) = 33 -> 5; 1 + 8 -> 2
     assert red[:, 1].tolist() == [5, 5, 2]
     assert work[0, 1] == 386 and work[4, 2] == 391
+
+
+# ------------------------------------------------------ K in 16-element groups
+
+@pytest.mark.parametrize("c", WINDOW_CASES, ids=[c["name"] for c in WINDOW_CASES])
+def test_grouped_k_layout_gives_the_same_result(c):
+    """K rearranged into [num_blocks, Hkv, D/16, block_size, 16] (torch permute)
+    must give exactly the same outputs, dense and planned, with a window and
+    sinks."""
+    w = _case(c)
+    w5 = wl.with_k_groups(w)
+    assert w5.k_cache.dim() == 5
+    sinks = np.linspace(-1.0, 1.0, w.num_q_heads)
+    assert np.array_equal(oracle_decode(w5), oracle_decode(w))
+    assert np.array_equal(oracle_decode(w5, window=30, sinks=sinks),
+                          oracle_decode(w, window=30, sinks=sinks))
+    work, red = oracle_plan(w, 100, max_partitions=7)
+    assert np.array_equal(oracle_decode_planned(w5, work, red), oracle_decode_planned(w, work, red))
+
+
+def test_grouped_k_layout_element_positions():
+    # element (page p, head h, key slot j, dim d) of the 5-D K sits at
+    # [p, h, d // 16, j, d % 16]: a cache whose every element encodes its own
+    # (j, d) checks the permutation, independent of the oracle
+    w = _single(40, H=(2, 2), D=64, bs=16)
+    nb, hkv, bs, d = w.k_cache.shape
+    jj = torch.arange(bs).view(1, 1, bs, 1).expand(nb, hkv, bs, d)
+    dd = torch.arange(d).view(1, 1, 1, d).expand(nb, hkv, bs, d)
+    code = ((jj << 8) | dd).to(torch.int16)  # distinct bit patterns
+    w.k_cache.view(torch.int16).copy_(code)
+    k5 = wl.with_k_groups(w).k_cache.view(torch.int16)
+    for j, dim in ((0, 0), (3, 17), (15, 63), (7, 48)):
+        assert int(k5[1, 1, dim // 16, j, dim % 16]) == (j << 8) | dim
