@@ -37,6 +37,8 @@
  * Data layouts (all row-major, contiguous, device memory unless stated):
  *   q, out          [num_tokens, Hq, D]          bf16 or fp16; out has q's dtype
  *   k_cache,v_cache [num_blocks, Hkv, block_size, D]  bf16, fp16 or e4m3fn bytes
+ *                   (pa_decode_ex also takes k_cache as PA_K_GROUPED:
+ *                   [num_blocks, Hkv, D/16, block_size, 16])
  *   block_tables    int32 [num_seqs, max_blocks_per_seq]; entry b of row r is
  *                   the physical block holding keys [b*bs, (b+1)*bs) of r
  *   context_lens    int32 [num_seqs]  KV length of each request (query tokens
@@ -101,6 +103,13 @@ enum pa_status {
 
 /* Element types. */
 enum pa_dtype { PA_BF16 = 0, PA_FP16 = 1, PA_FP8_E4M3 = 2 };
+
+/* K cache layouts (pa_decode_ex).  PA_K_ROWS: [num_blocks, Hkv, block_size, D].
+ * PA_K_GROUPED: the 5-D [num_blocks, Hkv, D/16, block_size, 16] that the
+ * capability gate of [ATOM-2366] (review items 5 and 12) checks the key cache
+ * against -- the head dim cut into 16-element groups, each group's block_size
+ * rows contiguous.  V is [num_blocks, Hkv, block_size, D] in both. */
+enum pa_k_layout { PA_K_ROWS = 0, PA_K_GROUPED = 1 };
 
 /* Plan kinds: the context-proportional plan, and the uniform comparator. */
 enum pa_plan_kind { PA_PLAN_PROPORTIONAL = 0, PA_PLAN_UNIFORM = 1 };
@@ -173,18 +182,20 @@ int pa_decode(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int num
  * the plan's last refresh.  PA_ERR_INVALID_ARG for W < 0. */
 int pa_plan_set_window(pa_plan* plan, int sliding_window);
 
-/* pa_decode with attention sinks (named in the same aiter signature): sinks
- * is NULL or a device array of num_q_heads fp32 logits, in the units of
- * scale * q.k, each joining its head's softmax denominator only:
- * out = sum_j e^(s_j) v_j / (sum_j e^(s_j) + e^(sink)).  A row with no
- * visible key is still 0.  Everything else is as pa_decode (which is this
- * call with sinks = NULL). */
+/* pa_decode with attention sinks and a choice of K layout.  sinks (named in
+ * the same aiter signature) is NULL or a device array of num_q_heads fp32
+ * logits, in the units of scale * q.k, each joining its head's softmax
+ * denominator only: out = sum_j e^(s_j) v_j / (sum_j e^(s_j) + e^(sink)).  A
+ * row with no visible key is still 0.  k_layout is a pa_k_layout (the same
+ * bytes of keys either way; results are identical up to summation order);
+ * PA_ERR_UNSUPPORTED for another value.  Everything else is as pa_decode
+ * (which is this call with sinks = NULL and k_layout = PA_K_ROWS). */
 int pa_decode_ex(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int num_q_heads,
                  int head_dim, const void* k_cache, const void* v_cache, int kv_dtype,
                  float k_scale, float v_scale, int num_blocks, int num_kv_heads, int block_size,
                  const int32_t* block_tables, int max_blocks_per_seq,
                  const int32_t* context_lens, const int32_t* cu_query_lens, int num_seqs,
-                 float scale, const float* sinks, void* out, void* stream);
+                 float scale, const float* sinks, int k_layout, void* out, void* stream);
 
 /* Size of the file-scope device array that pa_decode_static works in. */
 #define PA_STATIC_SCRATCH_BYTES (32u << 20)
@@ -194,7 +205,8 @@ int pa_decode_ex(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int 
  * it exists for callers that cannot call cudaMalloc while decoding -- a serving
  * engine that hands nearly all HBM to its own KV-cache pool and caching
  * allocator, or code running inside a CUDA-graph capture -- and so cannot
- * create a pa_plan.  It has no sliding window and no sinks.
+ * create a pa_plan.  It has no sliding window and no sinks, and takes K in
+ * the PA_K_ROWS layout.
  *
  * Arguments mean what they mean for pa_plan_build and pa_decode; the plan
  * parameters (max_query_len, max_partitions, budget, kind) are passed per call

@@ -29,6 +29,7 @@ PA_ERR_OOM = -5
 
 BF16, FP16, FP8_E4M3 = 0, 1, 2
 PROPORTIONAL, UNIFORM = 0, 1
+K_ROWS, K_GROUPED = 0, 1  # K cache layouts: [nb, Hkv, bs, D] / [nb, Hkv, D/16, bs, 16]
 
 DEVERR_STALE_PLAN = 0x1
 DEVERR_BAD_PAGE = 0x2
@@ -61,7 +62,7 @@ def load() -> ctypes.CDLL:
     lib.pa_decode.argtypes = [P, P, i32, i32, i32, i32, P, P, i32, f32, f32, i32, i32, i32, P,
                               i32, P, P, i32, f32, P, P]
     lib.pa_decode_ex.argtypes = [P, P, i32, i32, i32, i32, P, P, i32, f32, f32, i32, i32, i32, P,
-                                 i32, P, P, i32, f32, P, P, P]
+                                 i32, P, P, i32, f32, P, i32, P, P]
     lib.pa_plan_set_window.argtypes = [P, i32]
     lib.pa_plan_info.argtypes = [P, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                  ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32),
@@ -212,11 +213,18 @@ class Plan:
         _need(q, "q", dev, (torch.bfloat16, torch.float16))
         _need(k_cache, "k_cache", dev)
         _need(v_cache, "v_cache", dev, (k_cache.dtype,))
+        # K as [nb, Hkv, bs, D], or grouped as [nb, Hkv, D/16, bs, 16] (5-D)
+        grouped = k_cache.dim() == 5
         _need(block_tables, "block_tables", dev, (torch.int32,))
         _need(context_lens, "context_lens", dev, (torch.int32,))
         if cu_query_lens is not None:
             _need(cu_query_lens, "cu_query_lens", dev, (torch.int32,))
-        if q.dim() != 3 or k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        if grouped:
+            nb_, hk_, g_, bs_, x_ = k_cache.shape
+            if x_ != 16 or v_cache.dim() != 4 or tuple(v_cache.shape) != (nb_, hk_, bs_, 16 * g_):
+                raise ValueError("grouped K must be [num_blocks, Hkv, D/16, bs, 16] with V "
+                                 "[num_blocks, Hkv, bs, D]")
+        if q.dim() != 3 or v_cache.dim() != 4 or (not grouped and v_cache.shape != k_cache.shape):
             raise ValueError("q must be [T, Hq, D]; k/v caches [num_blocks, Hkv, bs, D]")
         if block_tables.dim() != 2:
             raise ValueError("block_tables must be [num_seqs, max_blocks]")
@@ -227,7 +235,7 @@ class Plan:
             if out.shape != q.shape:
                 raise ValueError("out must have q's shape")
         T, Hq, D = q.shape
-        nb, Hkv, bs, Dk = k_cache.shape
+        nb, Hkv, bs, Dk = v_cache.shape
         if Dk != D:
             raise ValueError("cache head_dim differs from q's")
         if scale is None:
@@ -237,7 +245,8 @@ class Plan:
                                    _ptr(v_cache), kv_code(k_cache), float(k_scale),
                                    float(v_scale), nb, Hkv, bs, _ptr(block_tables),
                                    block_tables.shape[1], _ptr(context_lens), _ptr(cu_query_lens),
-                                   context_lens.shape[0], float(scale), _ptr(sinks), _ptr(out),
+                                   context_lens.shape[0], float(scale), _ptr(sinks),
+                                   K_GROUPED if grouped else K_ROWS, _ptr(out),
                                    _stream(dev, stream)), "pa_decode_ex")
         return out
 

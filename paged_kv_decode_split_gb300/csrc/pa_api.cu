@@ -20,7 +20,7 @@ namespace {
 struct TmapSlot {
   bool valid = false;
   const void* ptr = nullptr;
-  int num_blocks = 0, Hkv = 0, bs = 0, D = 0, dtype = 0;
+  int num_blocks = 0, Hkv = 0, bs = 0, D = 0, dtype = 0, grouped = 0;
   CUtensorMap map;
 };
 
@@ -161,12 +161,16 @@ PlanDev carve_plan(char* c, const PlanLayout& l) {
   return d;
 }
 
-cudaError_t launch_split(const SplitParams& p, int D, int kv_dtype, int row_groups,
+cudaError_t launch_split(const SplitParams& p, int D, int kv_dtype, int row_groups, int k_layout,
                          const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s) {
+  const bool gk = k_layout == PA_K_GROUPED;
   switch (D) {
-    case 64: return launch_split_d64(p, kv_dtype, row_groups, tk, tv, s);
-    case 128: return launch_split_d128(p, kv_dtype, row_groups, tk, tv, s);
-    default: return launch_split_d256(p, kv_dtype, row_groups, tk, tv, s);
+    case 64:
+      return (gk ? launch_split_d64_gk : launch_split_d64)(p, kv_dtype, row_groups, tk, tv, s);
+    case 128:
+      return (gk ? launch_split_d128_gk : launch_split_d128)(p, kv_dtype, row_groups, tk, tv, s);
+    default:
+      return (gk ? launch_split_d256_gk : launch_split_d256)(p, kv_dtype, row_groups, tk, tv, s);
   }
 }
 
@@ -177,11 +181,15 @@ namespace {
 // TMA view of a cache [num_blocks, Hkv, bs, D] as a 2-D tensor of
 // num_blocks*Hkv*bs rows x D elements; boxes of box_rows rows x one swizzle
 // span (128 bytes, or 64 for a 64-byte row), swizzled to match the kernel.
+// grouped: a K cache [num_blocks, Hkv, D/16, bs, 16] as the 3-D tensor
+// {128 bytes, bs * 16 * elem / 128, num_blocks * Hkv * D/16} (innermost first):
+// rows of 128 bytes, each 4 (fp8: 8) consecutive keys of one 16-dim group; one
+// box is 16 keys of every group of one page and head, 128-byte swizzled.
 int make_tmap(pa_plan* plan, const void* ptr, int num_blocks, int Hkv, int bs, int D, int dtype,
-              CUtensorMap* out) {
+              int grouped, CUtensorMap* out) {
   for (auto& s : plan->tmaps) {
     if (s.valid && s.ptr == ptr && s.num_blocks == num_blocks && s.Hkv == Hkv && s.bs == bs &&
-        s.D == D && s.dtype == dtype) {
+        s.D == D && s.dtype == dtype && s.grouped == grouped) {
       *out = s.map;
       return PA_OK;
     }
@@ -190,20 +198,34 @@ int make_tmap(pa_plan* plan, const void* ptr, int num_blocks, int Hkv, int bs, i
   if (!fn) return PA_ERR_CUDA;
   const int esz = dtype == PA_FP8_E4M3 ? 1 : 2;
   const int swb = pa::split_box_row_bytes(D, dtype);
+  const cuuint32_t rows = static_cast<cuuint32_t>(pa::split_box_rows(D, dtype, bs));
   CUtensorMapDataType dt = dtype == PA_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                            : dtype == PA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                               : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(D),
-                        static_cast<cuuint64_t>(num_blocks) * Hkv * bs};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * esz};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(swb / esz),
-                       static_cast<cuuint32_t>(pa::split_box_rows(D, dtype, bs))};
-  cuuint32_t estr[2] = {1, 1};
   CUtensorMap m;
-  CUresult r = fn(&m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  swb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r;
+  if (grouped) {
+    const cuuint64_t kpr = 128 / (16 * esz);  // keys per 128-byte row
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(128 / esz), bs / kpr,
+                          static_cast<cuuint64_t>(num_blocks) * Hkv * (D / 16)};
+    cuuint64_t strides[2] = {128, 128 * (bs / kpr)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(16 / kpr),
+                         static_cast<cuuint32_t>(D / 16)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    r = fn(&m, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(D),
+                          static_cast<cuuint64_t>(num_blocks) * Hkv * bs};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * esz};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(swb / esz), rows};
+    cuuint32_t estr[2] = {1, 1};
+    r = fn(&m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE,
+           swb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   if (r != CUDA_SUCCESS) return PA_ERR_CUDA;
   TmapSlot& s = plan->tmaps[plan->tmap_next];
   plan->tmap_next = (plan->tmap_next + 1) % 8;
@@ -214,6 +236,7 @@ int make_tmap(pa_plan* plan, const void* ptr, int num_blocks, int Hkv, int bs, i
   s.bs = bs;
   s.D = D;
   s.dtype = dtype;
+  s.grouped = grouped;
   s.map = m;
   *out = m;
   return PA_OK;
@@ -349,7 +372,7 @@ int pa_decode(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int num
   return pa_decode_ex(plan, q, q_dtype, num_tokens, num_q_heads, head_dim, k_cache, v_cache,
                       kv_dtype, k_scale, v_scale, num_blocks, num_kv_heads, block_size,
                       block_tables, max_blocks_per_seq, context_lens, cu_query_lens, num_seqs,
-                      scale, nullptr, out, stream);
+                      scale, nullptr, PA_K_ROWS, out, stream);
 }
 
 int pa_decode_ex(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int num_q_heads,
@@ -357,8 +380,9 @@ int pa_decode_ex(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int 
                  float k_scale, float v_scale, int num_blocks, int num_kv_heads, int block_size,
                  const int32_t* block_tables, int max_blocks_per_seq,
                  const int32_t* context_lens, const int32_t* cu_query_lens, int num_seqs,
-                 float scale, const float* sinks, void* out, void* stream) {
+                 float scale, const float* sinks, int k_layout, void* out, void* stream) {
   if (!plan) return PA_ERR_INVALID_ARG;
+  if (k_layout != PA_K_ROWS && k_layout != PA_K_GROUPED) return PA_ERR_UNSUPPORTED;
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
     return PA_ERR_INVALID_ARG;
   if (num_tokens < 1 || num_blocks < 1 || max_blocks_per_seq < 1) return PA_ERR_INVALID_ARG;
@@ -387,9 +411,10 @@ int pa_decode_ex(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int 
   DeviceGuard guard(plan->device);
   if (!guard.ok) return PA_ERR_CUDA;
   CUtensorMap tk, tv;
-  int st = make_tmap(plan, k_cache, num_blocks, num_kv_heads, block_size, head_dim, kv_dtype, &tk);
+  int st = make_tmap(plan, k_cache, num_blocks, num_kv_heads, block_size, head_dim, kv_dtype,
+                     k_layout == PA_K_GROUPED ? 1 : 0, &tk);
   if (st != PA_OK) return st;
-  st = make_tmap(plan, v_cache, num_blocks, num_kv_heads, block_size, head_dim, kv_dtype, &tv);
+  st = make_tmap(plan, v_cache, num_blocks, num_kv_heads, block_size, head_dim, kv_dtype, 0, &tv);
   if (st != PA_OK) return st;
 
   const bool fp8 = kv_dtype == PA_FP8_E4M3;
@@ -431,7 +456,7 @@ int pa_decode_ex(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int 
   };
   if (plan->ev_call0 && !record(plan->ev_call0)) return PA_ERR_CUDA;
   if (plan->ev_start && !record(plan->ev_start)) return PA_ERR_CUDA;
-  if (pa::launch_split(sp, head_dim, kv_dtype, wq, tk, tv, s) != cudaSuccess)
+  if (pa::launch_split(sp, head_dim, kv_dtype, wq, k_layout, tk, tv, s) != cudaSuccess)
     return PA_ERR_CUDA;
   if (plan->ev_stop && !record(plan->ev_stop)) return PA_ERR_CUDA;
 

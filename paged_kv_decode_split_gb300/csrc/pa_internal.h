@@ -147,13 +147,19 @@ cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, int smem, cudaStrea
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
-cudaError_t launch_split(const SplitParams& p, int D, int kv_dtype, int row_groups,
+// k_layout: PA_K_ROWS or PA_K_GROUPED (the K cache's layout; V is always rows).
+cudaError_t launch_split(const SplitParams& p, int D, int kv_dtype, int row_groups, int k_layout,
                          const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s);
-cudaError_t launch_split_d64(const SplitParams& p, int kv_dtype, int row_groups,
-                             const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s);
-cudaError_t launch_split_d128(const SplitParams& p, int kv_dtype, int row_groups,
-                              const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s);
-cudaError_t launch_split_d256(const SplitParams& p, int kv_dtype, int row_groups,
-                              const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s);
+// One translation unit per head_dim and K layout (the _gk ones: grouped K).
+#define PA_DECLARE_SPLIT(NAME)                                                        \
+  cudaError_t NAME(const SplitParams& p, int kv_dtype, int row_groups, const CUtensorMap& tk, \
+                   const CUtensorMap& tv, cudaStream_t s);
+PA_DECLARE_SPLIT(launch_split_d64)
+PA_DECLARE_SPLIT(launch_split_d128)
+PA_DECLARE_SPLIT(launch_split_d256)
+PA_DECLARE_SPLIT(launch_split_d64_gk)
+PA_DECLARE_SPLIT(launch_split_d128_gk)
+PA_DECLARE_SPLIT(launch_split_d256_gk)
+#undef PA_DECLARE_SPLIT
 
 }  // namespace pa

@@ -13,7 +13,10 @@
 // GB300 mapping:
 //  * warp 0 is the producer: it walks the block table (32-entry windows,
 //    coalesced) and issues the TMA tile loads (cp.async.bulk.tensor.2d,
-//    128-byte swizzle, L2 evict-first) of the K and V rows of a stage's pages
+//    128-byte swizzle, L2 evict-first; a K cache in the grouped layout
+//    [num_blocks, Hkv, D/16, bs, 16] is read as 128-byte rows -- 4 (8 for
+//    fp8) keys of one 16-dim group -- in 3-D boxes of every group of a page's
+//    keys, also 128-byte swizzled) of the K and V rows of a stage's pages
 //    from up to 32 lanes at once -- with pages of only 2-4 KB per head, one
 //    issuing lane caps the stream at roughly half the HBM bandwidth -- into a
 //    ring of NS 32 KB stages, completion counted in bytes on an mbarrier;
@@ -48,9 +51,14 @@
 
 namespace pa {
 
-template <int D, int KVT, int WQ>
+// KL: K cache layout -- 0: [num_blocks, Hkv, bs, D]; 1: the grouped
+// [num_blocks, Hkv, D/16, bs, 16] (V is always [num_blocks, Hkv, bs, D]).
+template <int D, int KVT, int WQ, int KL>
 struct SplitCfg {
   static constexpr bool kFp8 = (KVT == PA_FP8_E4M3);
+  static constexpr bool kGroupedK = (KL == 1);
+  static constexpr int GRP = 16 * (kFp8 ? 1 : 2);     // grouped K: one key's 16-dim group, bytes
+
   static constexpr bool kBf16Mma = (KVT == PA_BF16);
   static constexpr int ESZ = kFp8 ? 1 : 2;            // bytes per cached element
   static constexpr int ROW = D * ESZ;                 // bytes per key row
@@ -77,6 +85,9 @@ struct SplitCfg {
   static constexpr int MIN_BLOCKS = (THREADS <= 224) ? 2 : 1;
   static_assert(KS % 16 == 0 && MTS % WK == 0, "whole 16-key tiles per warp");
   static_assert(MTS * CB * 2 <= 32, "a stage needs at most one copy per producer lane");
+  static_assert(!kGroupedK || MTS * (1 + CB) <= 32, "grouped K: one copy per producer lane");
+  static_assert(!kGroupedK || (16 * ROW) % 1024 == 0,
+                "grouped K: every 16-key box starts on a 1024-byte swizzle repeat");
   static_assert(EX_BYTES <= DATA_BYTES, "epilogue exchange reuses the stage ring");
   static_assert(D % 32 == 0, "head_dim is a multiple of 32");
 };
@@ -92,11 +103,12 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return o ^ (((o >> 7) & mask) << 4);
 }
 
-template <int D, int KVT, int WQ>
-__global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT, WQ>::MIN_BLOCKS)
+template <int D, int KVT, int WQ, int KL>
+__global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
+                                  SplitCfg<D, KVT, WQ, KL>::MIN_BLOCKS)
     split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                  const SplitParams p) {
-  using Cfg = SplitCfg<D, KVT, WQ>;
+  using Cfg = SplitCfg<D, KVT, WQ, KL>;
   constexpr int NQ = 8 * WQ;  // query rows per pass
   constexpr int T = Cfg::T;
 
@@ -288,31 +300,50 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
           nxt = bt_at(win + 32 + lane);
         }
         // copy c of this stage (one per lane): K/V by c & 1, column block and
-        // row box from c >> 1
+        // row box from c >> 1; with grouped K, lanes [0, MTS) copy K -- one box
+        // of 16 keys by every 16-dim group each -- and the others V
         const int c = lane;
-        const int rb = (c >> 1) / Cfg::CB;
-        const int cb = (c >> 1) % Cfg::CB;
-        const int key = key0 + rb * box_rows;
+        bool is_v;
+        int rb, cb;
+        if constexpr (Cfg::kGroupedK) {
+          is_v = c >= Cfg::MTS;
+          rb = is_v ? (c - Cfg::MTS) / Cfg::CB : c;
+          cb = is_v ? (c - Cfg::MTS) % Cfg::CB : 0;
+        } else {
+          is_v = (c & 1) != 0;
+          rb = (c >> 1) / Cfg::CB;
+          cb = (c >> 1) % Cfg::CB;
+        }
+        const int key = key0 + rb * ((Cfg::kGroupedK && !is_v) ? 16 : box_rows);
         const int pidx = key / bs;
         const int widx = min(pidx - win, 63);
         const int pc = __shfl_sync(0xffffffffu, cur, widx & 31);
         const int pn = __shfl_sync(0xffffffffu, nxt, widx & 31);
         const int page = widx < 32 ? pc : pn;
+        const int nbox_k = Cfg::kGroupedK ? (nkeys + 15) / 16 : nbox;  // grouped K: 16-key boxes
         if (lane == 0)
-          mbar_arrive_expect_tx(bar_full + 8 * buf, nbox * box_bytes * Cfg::CB * 2);
+          mbar_arrive_expect_tx(bar_full + 8 * buf,
+                                Cfg::kGroupedK ? (nbox_k * 16 + nbox * box_rows) * Cfg::ROW
+                                               : nbox * box_bytes * Cfg::CB * 2);
         __syncwarp();
-        if (rb < nbox) {
-          int y;
-          if (page < 0 || page >= p.num_blocks || pidx >= p.max_blocks) {
-            atomicOr(p.plan.err, PA_DEVERR_BAD_PAGE);
-            y = p.total_rows;  // outside the tensor: the copy reads zeros
+        if (rb < ((Cfg::kGroupedK && !is_v) ? nbox_k : nbox)) {
+          const bool bad = page < 0 || page >= p.num_blocks || pidx >= p.max_blocks;
+          if (bad) atomicOr(p.plan.err, PA_DEVERR_BAD_PAGE);  // the copy reads zeros
+          if (Cfg::kGroupedK && !is_v) {
+            // coordinates {byte in 128-byte row, 128-byte row of the group in
+            // the page, (page * Hkv + head) * D/16 + group}
+            const int slab = bad ? p.num_blocks * p.Hkv : page * p.Hkv + h;
+            const uint32_t dst = base + buf * Cfg::STAGE_BYTES +
+                                 static_cast<uint32_t>(rb * 16 * Cfg::ROW);
+            tma_load_3d(dst, &tmk, 0, (key % bs) * Cfg::GRP / 128, slab * (D / 16),
+                        bar_full + 8 * buf, policy);
           } else {
-            y = (page * p.Hkv + h) * bs + (key % bs);
+            const int y = bad ? p.total_rows : (page * p.Hkv + h) * bs + (key % bs);
+            const uint32_t dst = base + buf * Cfg::STAGE_BYTES + (is_v ? Cfg::TILE_BYTES : 0) +
+                                 cb * Cfg::BLOCK_BYTES + static_cast<uint32_t>(rb * box_rows * Cfg::SWB);
+            tma_load_2d(dst, is_v ? &tmv : &tmk, cb * (Cfg::SWB / Cfg::ESZ), y, bar_full + 8 * buf,
+                        policy);
           }
-          const uint32_t dst = base + buf * Cfg::STAGE_BYTES + (c & 1) * Cfg::TILE_BYTES +
-                               cb * Cfg::BLOCK_BYTES + static_cast<uint32_t>(rb * box_rows * Cfg::SWB);
-          tma_load_2d(dst, (c & 1) ? &tmv : &tmk, cb * (Cfg::SWB / Cfg::ESZ), y, bar_full + 8 * buf,
-                      policy);
         }
       }
       // Last stage of the item issued: claim the next one (into the other
@@ -340,6 +371,18 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
   const int lchkK = (lane >> 4) & 1;
   const int lrowV = (lane & 7) + ((lane >> 4) & 1) * 8;  // ldmatrix.trans row, V^T (A operand)
   const int lchkV = (lane >> 3) & 1;
+  // Grouped K: a stage holds one box per 16-key tile, [D/16 groups][16 keys][16
+  // dims] (16 * ROW bytes, 1024-byte aligned), 128-byte swizzled as a run of
+  // 128-byte rows: linear offset o = group * 16 * GRP + key * GRP + byte lands
+  // at o ^ (((o >> 7) & 7) << 4).  16-bit: group j's ldmatrix row of this lane
+  // sits at j * 512 + kswz[j & 1]; fp8: key g + 8h of group j at j * 256 + h * 128
+  // + ((g ^ ((2j + h) & 7)) * 16) + 4t.
+  uint32_t kswz[2] = {0u, 0u};
+  if constexpr (Cfg::kGroupedK && !Cfg::kFp8) {
+    const uint32_t lin = static_cast<uint32_t>(lrowK * 32 + lchkK * 16);  // < 512
+    kswz[0] = lin ^ (((lin >> 7) & 3u) << 4);
+    kswz[1] = lin ^ ((((lin >> 7) & 3u) | 4u) << 4);
+  }
 
   for (int pass = 0; pass < npass; ++pass) {
     const int pass_base = row_lo + pass * NQ;
@@ -373,11 +416,13 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
         }
       } else {
         // fp16 operands; head-dim order permuted to match the fp8 K fragment:
-        // k-step ks uses d = cb*SWB + t*(SWB/4) + 4j + {0,1 | 2,3}.
+        // k-step ks uses d = cb*SWB + t*(SWB/4) + 4j + {0,1 | 2,3} (row-major
+        // K), or d = 16ks + 4t + {0,1 | 2,3} (grouped K).
         constexpr int KPB = Cfg::SWB / 16;  // k-steps per column block
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const int d = (ks / KPB) * Cfg::SWB + t * (Cfg::SWB / 4) + 4 * (ks % KPB);
+          const int d = Cfg::kGroupedK ? 16 * ks + 4 * t
+                                       : (ks / KPB) * Cfg::SWB + t * (Cfg::SWB / 4) + 4 * (ks % KPB);
           float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
           if (ok) {
             const uint2 raw4 = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.q) + qoff + d);
@@ -429,7 +474,10 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
 #pragma unroll
             for (int tt = 0; tt < T; ++tt) {
               uint32_t a0, a1, a2, a3;
-              ldsm_x4(ko + (rbase + 16 * tt) * Cfg::SWB, a0, a1, a2, a3);
+              if constexpr (Cfg::kGroupedK)
+                ldsm_x4(kt + (rbase + 16 * tt) * Cfg::ROW + ks * 512 + kswz[ks & 1], a0, a1, a2, a3);
+              else
+                ldsm_x4(ko + (rbase + 16 * tt) * Cfg::SWB, a0, a1, a2, a3);
               if (T == 1 && (ks & 1))
                 mma16816<Cfg::kBf16Mma>(c2, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
               else
@@ -438,6 +486,23 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
           }
           if (T == 1) {
             c[0][0] += c2[0]; c[0][1] += c2[1]; c[0][2] += c2[2]; c[0][3] += c2[3];
+          }
+        } else if constexpr (Cfg::kGroupedK) {
+          // grouped fp8 K: a 16-dim group of a key is 16 bytes; thread t takes
+          // dims 4t..4t+3 of keys g and g + 8 (two conflict-free 32-bit loads
+          // per k-step), matched by the Q fragment's head-dim order
+#pragma unroll
+          for (int tt = 0; tt < T; ++tt) {
+            const uint32_t kg = kt + (rbase + 16 * tt) * Cfg::ROW + 4 * t;
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const uint32_t w0 = lds32(kg + ks * 256 + ((g ^ ((2 * ks) & 7)) << 4));
+              const uint32_t w1 = lds32(kg + ks * 256 + 128 + ((g ^ ((2 * ks + 1) & 7)) << 4));
+              uint32_t a0, a1, a2, a3;
+              e4m3x4_to_f16x2x2(w0, a0, a2);
+              e4m3x4_to_f16x2x2(w1, a1, a3);
+              mma16816<false>(c[tt], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+            }
           }
         } else {
           constexpr int KPB = Cfg::SWB / 16;
@@ -682,11 +747,11 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ>::THREADS, SplitCfg<D, KVT
   cta_exit();
 }
 
-template <int D, int KVT, int WQ>
+template <int D, int KVT, int WQ, int KL>
 cudaError_t launch_split_cfg(const SplitParams& p, const CUtensorMap& tk,
                              const CUtensorMap& tv, cudaStream_t s) {
-  using Cfg = SplitCfg<D, KVT, WQ>;
-  auto kern = split_kernel<D, KVT, WQ>;
+  using Cfg = SplitCfg<D, KVT, WQ, KL>;
+  auto kern = split_kernel<D, KVT, WQ, KL>;
   static bool attr_done = false;  // benign race: the attribute call is idempotent
   if (!attr_done) {
     cudaError_t e =
@@ -699,15 +764,15 @@ cudaError_t launch_split_cfg(const SplitParams& p, const CUtensorMap& tk,
                     Cfg::SMEM_BYTES, s, tk, tv, p);
 }
 
-template <int D>
+template <int D, int KL>
 cudaError_t launch_split_d(const SplitParams& p, int kv_dtype, int wq,
                            const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s) {
 #define PA_SPLIT_CASE(KVT)                                                     \
   switch (wq) {                                                                \
-    case 1: return launch_split_cfg<D, KVT, 1>(p, tk, tv, s);               \
-    case 2: return launch_split_cfg<D, KVT, 2>(p, tk, tv, s);               \
-    case 3: return launch_split_cfg<D, KVT, 3>(p, tk, tv, s);               \
-    default: return launch_split_cfg<D, KVT, 4>(p, tk, tv, s);              \
+    case 1: return launch_split_cfg<D, KVT, 1, KL>(p, tk, tv, s);           \
+    case 2: return launch_split_cfg<D, KVT, 2, KL>(p, tk, tv, s);           \
+    case 3: return launch_split_cfg<D, KVT, 3, KL>(p, tk, tv, s);           \
+    default: return launch_split_cfg<D, KVT, 4, KL>(p, tk, tv, s);          \
   }
   switch (kv_dtype) {
     case PA_BF16: PA_SPLIT_CASE(PA_BF16)

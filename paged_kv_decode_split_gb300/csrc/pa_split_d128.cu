@@ -6,7 +6,7 @@ namespace pa {
 
 cudaError_t launch_split_d128(const SplitParams& p, int kv_dtype, int row_groups,
                              const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s) {
-  return launch_split_d<128>(p, kv_dtype, row_groups, tk, tv, s);
+  return launch_split_d<128, 0>(p, kv_dtype, row_groups, tk, tv, s);
 }
 
 }  // namespace pa

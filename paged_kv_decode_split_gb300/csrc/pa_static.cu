@@ -211,7 +211,7 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
   sp.scale_log2 = static_cast<float>(static_cast<double>(scale) * (fp8 ? k_scale : 1.0) *
                                      1.4426950408889634);
   sp.v_scale = fp8 ? v_scale : 1.0f;
-  if (pa::launch_split(sp, head_dim, kv_dtype, wq, tk, tv, s) != cudaSuccess)
+  if (pa::launch_split(sp, head_dim, kv_dtype, wq, PA_K_ROWS, tk, tv, s) != cudaSuccess)
     return PA_ERR_CUDA;
 
   pa::MergeParams mp;

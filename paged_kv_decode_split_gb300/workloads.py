@@ -258,6 +258,11 @@ def with_k_groups(w: Workload) -> Workload:
                     dict(w.meta), w.window)
 
 
+# The uniform and skewed batches with K in the grouped 5-D layout (same bytes).
+CONFIGS["uniform_k5"] = lambda seed=0, device="cpu": with_k_groups(uniform(seed, device))
+CONFIGS["skewed_k5"] = lambda seed=0, device="cpu": with_k_groups(skewed(seed, device))
+
+
 def subset(w: Workload, requests: Sequence[int]) -> Workload:
     """The sub-batch of the given requests, with their pages copied into a compact
     pool (same bytes, same page order inside each request).  Every output row of a

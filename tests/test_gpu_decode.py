@@ -175,6 +175,63 @@ def test_window_with_pieces(dev):
         assert max_diff(out, ref) <= TOL["bf16"], window
 
 
+# ------------------------------------------ K in the grouped 5-D layout
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("kv,q", [("bf16", "bf16"), ("fp16", "fp16"), ("fp8", "bf16")])
+@pytest.mark.parametrize("bs", [16, 64, 128])
+def test_grouped_k_sweep(dev, D, kv, q, bs):
+    """K as [num_blocks, Hkv, D/16, bs, 16]: the oracle reads that layout by its
+    own indexing; with 16-bit caches the result also equals the row-major run
+    bit for bit (the same MMA k-steps in the same order)."""
+    w = batch(dev, RAGGED + [5000], H=(8, 2), D=D, bs=bs, kv=kv, q=q, seed=3 * D + bs)
+    w5 = wl.with_k_groups(w)
+    out5, plan = run(w5)
+    ref = oracle_decode(w5.to("cpu"))
+    assert max_diff(out5, ref) <= TOL[kv]
+    assert plan.read_errors() == 0
+    if kv != "fp8":
+        out4, _ = run(w)
+        assert torch.equal(out4, out5)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_grouped_k_rows_window_sinks_pieces(dev, kv):
+    """Grouped K through every other path: multi-token rows with padding, a
+    sliding window with sinks, and a slot run as pieces with a CTA merge."""
+    w = wl.with_k_groups(batch(dev, [600, 40, 3000, 2, 0], ql=[3, 3, 3, 3, 1], H=(6, 1), D=256,
+                               bs=64, kv=kv, pad=5, seed=31))
+    check(w)
+    w = wl.with_k_groups(batch(dev, [40000] + [300 + 37 * i for i in range(15)], H=(8, 2), D=128,
+                               kv=kv, seed=32, budget=32))
+    sinks = np.linspace(-2, 2, 8)
+    for window in (0, 7000):
+        out, plan = run_ext(w, window=window, sinks=sinks)
+        ref = oracle_decode(w.to("cpu"), window=window, sinks=sinks)
+        assert max_diff(out, ref) <= TOL[kv], window
+        assert plan.read_errors() == 0
+
+
+def test_grouped_k_layout_checks(dev):
+    w = batch(dev, [300, 20], H=(8, 2), D=128, seed=33)
+    w5 = wl.with_k_groups(w)
+    plan = binding.plan_for(w5)
+    plan.refresh(w5.context_lens)
+    bad_v = w5.v_cache[:, :, :8]  # V must be [nb, Hkv, bs, D] with K's nb, Hkv and bs
+    with pytest.raises(ValueError):
+        plan.decode(w5.q, w5.k_cache, bad_v, w5.block_tables, w5.context_lens)
+    bad_k = w5.k_cache.reshape(*w5.k_cache.shape[:3], 8, 32)
+    with pytest.raises(ValueError):
+        plan.decode(w5.q, bad_k, w5.v_cache, w5.block_tables, w5.context_lens)
+    lib = binding.load()
+    st = lib.pa_decode_ex(plan._h, binding._ptr(w5.q), binding.BF16, 2, 8, 128,
+                          binding._ptr(w5.k_cache), binding._ptr(w5.v_cache), binding.BF16,
+                          1.0, 1.0, w5.v_cache.shape[0], 2, 16, binding._ptr(w5.block_tables),
+                          w5.block_tables.shape[1], binding._ptr(w5.context_lens), None, 2,
+                          0.1, None, 2, binding._ptr(torch.empty_like(w5.q)), None)
+    assert st == binding.PA_ERR_UNSUPPORTED  # no third K layout
+
+
 # ---------------------------------------------------- multi-token rows (cu)
 
 def test_verify_rows_and_padding(dev):
@@ -260,10 +317,11 @@ def test_stale_plan_is_reported_and_zeroed(dev):
     assert max_diff(out[[0, 2]], ref[[0, 2]]) <= TOL["bf16"]
 
 
-def test_bad_page_is_reported_not_faulted(dev):
+@pytest.mark.parametrize("grouped", [False, True])
+def test_bad_page_is_reported_not_faulted(dev, grouped):
     w = batch(dev, [3000, 800], H=(8, 2), D=128, seed=7)
     w.block_tables[0, 3] = w.k_cache.shape[0] + 5
-    out, plan = run(w)
+    out, plan = run(wl.with_k_groups(w) if grouped else w)
     assert plan.read_errors() & binding.DEVERR_BAD_PAGE
     ref = oracle_decode(wl.subset(w, [1]))
     assert max_diff(out[[1]], ref) <= TOL["bf16"]
@@ -375,6 +433,26 @@ def test_profiling_events_bracket_the_call_and_the_split(dev):
     assert max_diff(out, oracle_decode(w.to("cpu"))) <= TOL["bf16"]
 
 
+def test_largest_batch_4096_requests(dev):
+    """The planner's domain limit: 4096 requests (lengths 0..3000, a few empty),
+    with and without multi-token rows; sampled rows against the oracle."""
+    rng = np.random.default_rng(31)
+    lens = rng.integers(0, 3000, 4096).tolist()
+    lens[:3] = [0, 1, 2999]
+    w = batch(dev, lens, H=(8, 1), D=64, bs=16, seed=31)
+    out, plan = run(w)
+    assert plan.read_errors() == 0
+    pick = [0, 1, 2, 5, 100, 2047, 4095]
+    assert _sampled(w, out, pick) <= TOL["bf16"]
+    assert torch.all(out[0] == 0)  # the empty request
+    ql = rng.integers(0, 3, 4096).tolist()
+    w = batch(dev, lens, ql=ql, H=(4, 1), D=64, bs=16, pad=7, seed=32)
+    out, plan = run(w)
+    assert plan.read_errors() == 0
+    assert _sampled(w, out, [r for r in pick if ql[r] > 0]) <= TOL["bf16"]
+    assert torch.all(out[int(w.cu_query_lens[-1]):] == 0)
+
+
 # ------------------------------------------------ full-size configurations
 
 def _sampled(w, out, requests):
@@ -399,7 +477,7 @@ def _pick(w, k=4):
 
 
 FULL = ["uniform", "skewed", "mtp_verify", "mixed_prompt", "large_bf16", "large_fp8",
-        "uniform_w1024", "skewed_w4096"]
+        "uniform_w1024", "skewed_w4096", "uniform_k5", "skewed_k5"]
 
 
 @pytest.mark.parametrize("name", FULL)
