@@ -18,7 +18,9 @@ HEADER = os.path.join(ROOT, "include", "pa.h")
 
 SOURCES = ["pa_api.cu", "pa_plan.cu", "pa_merge.cu", "pa_static.cu",
            "pa_split_d64.cu", "pa_split_d128.cu", "pa_split_d256.cu",
-           "pa_split_d64_gk.cu", "pa_split_d128_gk.cu", "pa_split_d256_gk.cu"]
+           "pa_split_d64_gk.cu", "pa_split_d128_gk.cu", "pa_split_d256_gk.cu",
+           "pa_split_d384.cu", "pa_split_d512.cu", "pa_split_d640.cu", "pa_split_d768.cu",
+           "pa_split_d896.cu", "pa_split_d1024.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                 "-Xcompiler", "-Wall", "-I", os.path.join(ROOT, "include")]

@@ -84,14 +84,16 @@ int split_box_row_bytes(int D, int kv_dtype) {
 }
 
 int split_box_rows(int D, int kv_dtype, int bs) {
-  const int ks = kStageTensorBytes / (D * (kv_dtype == PA_FP8_E4M3 ? 1 : 2));  // keys per stage
+  // keys per stage: one 16-key tile above head_dim 256
+  const int ks = D > 256 ? 16 : kStageTensorBytes / (D * (kv_dtype == PA_FP8_E4M3 ? 1 : 2));
   return bs < ks ? bs : ks;
 }
 
-int split_row_groups(int max_qlen, int G) {
+int split_row_groups(int max_qlen, int G, int D) {
   const long long rows = static_cast<long long>(max_qlen) * G;
-  if (rows <= 32) return static_cast<int>((rows + 7) / 8);
-  return 1;  // long prompts: 8-row work items, spread over the CTAs by work stealing
+  int wq = 1;  // long prompts: 8-row work items, spread over the CTAs by work stealing
+  if (rows <= 32) wq = static_cast<int>((rows + 7) / 8);
+  return wq < split_max_row_groups(D) ? wq : split_max_row_groups(D);
 }
 
 long long split_max_extra(int G, int rpc, long long rows_cap, int max_tokens, int max_qlen) {
@@ -121,7 +123,7 @@ PlanLayout plan_layout(int num_seqs, int Hq, int Hkv, int D, int max_qlen, int m
   if (rows < 1) rows = 1;
   l.rows_cap = rows * l.Q;  // sum_r T_r L_r <= Q sum_r p_r L_r
   const int G = Hq / Hkv;
-  l.rpc = 8 * split_row_groups(max_qlen, G);
+  l.rpc = 8 * split_row_groups(max_qlen, G, D);
   l.max_extra = split_max_extra(G, l.rpc, l.rows_cap, max_tokens, max_qlen);
   const size_t n = static_cast<size_t>(num_seqs);
   l.b_work = up256(static_cast<size_t>(l.C) * sizeof(int4));
@@ -165,6 +167,12 @@ cudaError_t launch_split(const SplitParams& p, int D, int kv_dtype, int row_grou
                          const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s) {
   const bool gk = k_layout == PA_K_GROUPED;
   switch (D) {
+    case 384: return launch_split_d384(p, kv_dtype, row_groups, k_layout, tk, tv, s);
+    case 512: return launch_split_d512(p, kv_dtype, row_groups, k_layout, tk, tv, s);
+    case 640: return launch_split_d640(p, kv_dtype, row_groups, k_layout, tk, tv, s);
+    case 768: return launch_split_d768(p, kv_dtype, row_groups, k_layout, tk, tv, s);
+    case 896: return launch_split_d896(p, kv_dtype, row_groups, k_layout, tk, tv, s);
+    case 1024: return launch_split_d1024(p, kv_dtype, row_groups, k_layout, tk, tv, s);
     case 64:
       return (gk ? launch_split_d64_gk : launch_split_d64)(p, kv_dtype, row_groups, tk, tv, s);
     case 128:
@@ -269,7 +277,7 @@ int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_q_heads, int
   if (kind != PA_PLAN_PROPORTIONAL && kind != PA_PLAN_UNIFORM) return PA_ERR_INVALID_ARG;
   if (num_seqs > PA_MAX_SEQS) return PA_ERR_UNSUPPORTED;
   if (num_q_heads % num_kv_heads != 0) return PA_ERR_UNSUPPORTED;
-  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
+  if (!pa::head_dim_supported(head_dim)) return PA_ERR_UNSUPPORTED;
   if (max_partitions <= 0) max_partitions = PA_DEFAULT_MAX_PARTITIONS;
   if (max_partitions > 65536 || budget > (1 << 24)) return PA_ERR_UNSUPPORTED;
   if (static_cast<long long>(max_query_len) * (num_q_heads / num_kv_heads) > (1 << 24) ||
@@ -397,7 +405,7 @@ int pa_decode_ex(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int 
   if (kv_dtype == PA_FP8_E4M3 && (!std::isfinite(k_scale) || !std::isfinite(v_scale)))
     return PA_ERR_INVALID_ARG;
   if (block_size != 16 && block_size != 64 && block_size != 128) return PA_ERR_UNSUPPORTED;
-  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
+  if (!pa::head_dim_supported(head_dim)) return PA_ERR_UNSUPPORTED;
   if (num_kv_heads < 1 || num_q_heads % num_kv_heads != 0) return PA_ERR_UNSUPPORTED;
   if (static_cast<long long>(num_blocks) * num_kv_heads * block_size >= (1ll << 31))
     return PA_ERR_UNSUPPORTED;
@@ -444,7 +452,7 @@ int pa_decode_ex(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int 
   sp.sinks = sinks;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int wq = pa::split_row_groups(plan->max_qlen, sp.G);
+  const int wq = pa::split_row_groups(plan->max_qlen, sp.G, head_dim);
   // Profiling events: inside a stream capture they must be external event
   // records to fire on every replay of the graph.
   auto record = [&](cudaEvent_t e) {

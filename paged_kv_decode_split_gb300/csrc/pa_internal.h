@@ -92,12 +92,17 @@ struct SplitParams {
   const float* sinks;  // [Hq] sink logits (scale * q.k units) or null
 };
 
+// Head dims the kernels take: 64, and 128 to 1024 in steps of 128.
+constexpr bool head_dim_supported(int D) { return D == 64 || (D % 128 == 0 && D >= 128 && D <= 1024); }
+// Query-row groups of 8 per pass the split kernel is built with for head_dim D:
+// head dims above 256 run one warp per 128-dim slice, so fewer row groups fit.
+constexpr int split_max_row_groups(int D) { return D <= 256 ? 4 : (D <= 512 ? 2 : 1); }
 // Rows of one TMA box of a KV tile for head_dim D, cache dtype, block size.
 int split_box_rows(int D, int kv_dtype, int bs);
 // Bytes of one box row (the swizzle span): min(128, D * elem_bytes).
 int split_box_row_bytes(int D, int kv_dtype);
 // Query-row groups of 8 handled per pass for a plan with this max query length.
-int split_row_groups(int max_qlen, int G);
+int split_row_groups(int max_qlen, int G, int D);
 // Upper bound on the extra (slot, row chunk) items a plan with these limits can list.
 long long split_max_extra(int G, int rpc, long long rows_cap, int max_tokens, int max_qlen);
 
@@ -150,7 +155,8 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
 // k_layout: PA_K_ROWS or PA_K_GROUPED (the K cache's layout; V is always rows).
 cudaError_t launch_split(const SplitParams& p, int D, int kv_dtype, int row_groups, int k_layout,
                          const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s);
-// One translation unit per head_dim and K layout (the _gk ones: grouped K).
+// One translation unit per head_dim and K layout (the _gk ones: grouped K); head
+// dims above 256 share one per head_dim for both layouts (k_layout argument).
 #define PA_DECLARE_SPLIT(NAME)                                                        \
   cudaError_t NAME(const SplitParams& p, int kv_dtype, int row_groups, const CUtensorMap& tk, \
                    const CUtensorMap& tv, cudaStream_t s);
@@ -160,6 +166,16 @@ PA_DECLARE_SPLIT(launch_split_d256)
 PA_DECLARE_SPLIT(launch_split_d64_gk)
 PA_DECLARE_SPLIT(launch_split_d128_gk)
 PA_DECLARE_SPLIT(launch_split_d256_gk)
+#define PA_DECLARE_SPLIT_WIDE(NAME)                                                   \
+  cudaError_t NAME(const SplitParams& p, int kv_dtype, int row_groups, int k_layout,  \
+                   const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s);
+PA_DECLARE_SPLIT_WIDE(launch_split_d384)
+PA_DECLARE_SPLIT_WIDE(launch_split_d512)
+PA_DECLARE_SPLIT_WIDE(launch_split_d640)
+PA_DECLARE_SPLIT_WIDE(launch_split_d768)
+PA_DECLARE_SPLIT_WIDE(launch_split_d896)
+PA_DECLARE_SPLIT_WIDE(launch_split_d1024)
+#undef PA_DECLARE_SPLIT_WIDE
 #undef PA_DECLARE_SPLIT
 
 }  // namespace pa

@@ -29,13 +29,14 @@ namespace pa {
 namespace {
 
 constexpr int kMergeThreads = 256;
-constexpr int kMergeUnroll = 4;  // partitions in flight per unit
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
   constexpr int UL = D / 4 < 32 ? D / 4 : 32;  // lanes per unit
   constexpr int VPL = D / 4 / UL;               // float4 outputs per lane
   constexpr int NU = kMergeThreads / UL;        // units per CTA
+  // partitions in flight per unit: 4, fewer for wide rows (registers)
+  constexpr int kMergeUnroll = VPL <= 2 ? 4 : (VPL <= 4 ? 2 : 1);
   __shared__ float4 s_acc[NU][D / 4];
   __shared__ float s_m[NU];
   __shared__ float s_ws[NU];
@@ -152,9 +153,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     __syncthreads();  // shared memory is reused by the next pair
   }
 
-  // Rows with few pieces: one warp per (row, q head) pair, every piece's
-  // partial loaded at once, combined with shuffles.
+  // Rows with few pieces: one warp per (row, q head) pair, the pieces' partials
+  // loaded PB at a time (all at once up to head_dim 256), weights from shuffles.
   constexpr int VL = D / 32;  // outputs per lane
+  constexpr int PB = VL <= 8 ? kWarpMergePieces : 2;
   const int warp = tid >> 5, lane = tid & 31;
   constexpr int kWarps = kMergeThreads / 32;
   for (int wp = blockIdx.x * kWarps + warp; wp < nfew * Hq; wp += gridDim.x * kWarps) {
@@ -167,22 +169,6 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     const int Lnow = p.cu ? p.cu[r + 1] - c0 : 1;
     float lse = NEG_INF;
     if (lane < parts) lse = __ldcg(p.plan.part_lse + static_cast<long long>(e.z + lane * L) * Hq + hq);
-    float o[kWarpMergePieces][VL];
-#pragma unroll
-    for (int j = 0; j < kWarpMergePieces; ++j) {
-      if (j < parts) {
-        const float* src = p.plan.part_o + (static_cast<long long>(e.z + j * L) * Hq + hq) * D + lane * VL;
-#pragma unroll
-        for (int v = 0; v < VL; v += 2) {
-          const float2 x = __ldcg(reinterpret_cast<const float2*>(src + v));
-          o[j][v] = x.x;
-          o[j][v + 1] = x.y;
-        }
-      } else {
-#pragma unroll
-        for (int v = 0; v < VL; ++v) o[j][v] = 0.f;
-      }
-    }
     float M = lse;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
@@ -193,11 +179,38 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     float acc[VL];
 #pragma unroll
     for (int v = 0; v < VL; ++v) acc[v] = 0.f;
+    for (int j0 = 0; j0 < parts; j0 += PB) {
+      float o[PB][VL];
 #pragma unroll
-    for (int j = 0; j < kWarpMergePieces; ++j) {
-      const float wj = __shfl_sync(0xffffffffu, w, j);
+      for (int k = 0; k < PB; ++k) {
+        const int j = j0 + k;
+        if (j < parts) {
+          const float* src = p.plan.part_o + (static_cast<long long>(e.z + j * L) * Hq + hq) * D + lane * VL;
+          if constexpr (VL % 4 == 0) {
 #pragma unroll
-      for (int v = 0; v < VL; ++v) acc[v] += wj * o[j][v];
+            for (int v = 0; v < VL; v += 4) {
+              const float4 x = __ldcg(reinterpret_cast<const float4*>(src + v));
+              o[k][v] = x.x; o[k][v + 1] = x.y; o[k][v + 2] = x.z; o[k][v + 3] = x.w;
+            }
+          } else {
+#pragma unroll
+            for (int v = 0; v < VL; v += 2) {
+              const float2 x = __ldcg(reinterpret_cast<const float2*>(src + v));
+              o[k][v] = x.x;
+              o[k][v + 1] = x.y;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int v = 0; v < VL; ++v) o[k][v] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < PB; ++k) {
+        const float wj = __shfl_sync(0xffffffffu, w, (j0 + k) & 31);  // w = 0 past `parts`
+#pragma unroll
+        for (int v = 0; v < VL; ++v) acc[v] += wj * o[k][v];
+      }
     }
     if (snap.x != ctx || snap.y != Lnow) continue;  // stale: zeroed by the split kernel
     const int t = c0 + tok;
@@ -219,10 +232,14 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     uint16_t* dst = static_cast<uint16_t*>(p.out) + (static_cast<size_t>(t) * Hq + hq) * D + lane * VL;
     if constexpr (VL == 2) {
       *reinterpret_cast<uint32_t*>(dst) = pk[0];
-    } else if constexpr (VL == 4) {
-      *reinterpret_cast<uint2*>(dst) = make_uint2(pk[0], pk[1]);
-    } else {
-      *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    } else if constexpr (VL % 8 == 0) {  // 16-byte aligned: lane * VL * 2 bytes
+#pragma unroll
+      for (int v = 0; v < VL / 2; v += 4)
+        *reinterpret_cast<uint4*>(dst + 2 * v) = make_uint4(pk[v], pk[v + 1], pk[v + 2], pk[v + 3]);
+    } else {  // VL % 4 == 0: 8-byte aligned
+#pragma unroll
+      for (int v = 0; v < VL / 2; v += 2)
+        *reinterpret_cast<uint2*>(dst + 2 * v) = make_uint2(pk[v], pk[v + 1]);
     }
   }
 }
@@ -231,11 +248,21 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s) {
   if (p.grid <= 0) return cudaSuccess;
+#define PA_MERGE_CASE(DD) \
+  case DD: return launch_pdl(merge_kernel<DD>, dim3(p.grid), dim3(kMergeThreads), 0, s, p);
   switch (p.D) {
-    case 64: return launch_pdl(merge_kernel<64>, dim3(p.grid), dim3(kMergeThreads), 0, s, p);
-    case 128: return launch_pdl(merge_kernel<128>, dim3(p.grid), dim3(kMergeThreads), 0, s, p);
-    default: return launch_pdl(merge_kernel<256>, dim3(p.grid), dim3(kMergeThreads), 0, s, p);
+    PA_MERGE_CASE(64)
+    PA_MERGE_CASE(128)
+    PA_MERGE_CASE(256)
+    PA_MERGE_CASE(384)
+    PA_MERGE_CASE(512)
+    PA_MERGE_CASE(640)
+    PA_MERGE_CASE(768)
+    PA_MERGE_CASE(896)
+    PA_MERGE_CASE(1024)
+    default: return cudaErrorInvalidValue;
   }
+#undef PA_MERGE_CASE
 }
 
 }  // namespace pa

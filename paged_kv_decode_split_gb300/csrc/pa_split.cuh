@@ -58,13 +58,21 @@ struct SplitCfg {
   static constexpr bool kFp8 = (KVT == PA_FP8_E4M3);
   static constexpr bool kGroupedK = (KL == 1);
   static constexpr int GRP = 16 * (kFp8 ? 1 : 2);     // grouped K: one key's 16-dim group, bytes
-
   static constexpr bool kBf16Mma = (KVT == PA_BF16);
   static constexpr int ESZ = kFp8 ? 1 : 2;            // bytes per cached element
   static constexpr int ROW = D * ESZ;                 // bytes per key row
   static constexpr int SWB = ROW < 128 ? ROW : 128;   // swizzle span = box row bytes
   static constexpr int CB = ROW / SWB;                // column blocks per key row
-  static constexpr int KS = kStageTensorBytes / ROW;  // keys per stage
+  // Head dims above 256 are cut into 128-dim slices, one consumer warp each:
+  // a warp forms the partial logits of its slice, the slices' partials are
+  // summed through shared memory (every warp of the row group adds them in
+  // the same order, so all hold the same logits and softmax state), and each
+  // warp accumulates P V for its own slice.  Stages are one 16-key tile.
+  static constexpr bool kWide = D > 256;
+  static constexpr int DS = kWide ? 128 : D;          // head dims per consumer warp
+  static constexpr int ND = D / DS;                   // dim slices
+  static constexpr int CBS = DS * ESZ / SWB;          // column blocks per slice
+  static constexpr int KS = kWide ? 16 : kStageTensorBytes / ROW;  // keys per stage
   static constexpr int NS = 3;                        // ring depth
   static constexpr int MTS = KS / 16;                 // 16-key tiles per stage
   static constexpr int WK0 = (WQ == 1) ? 4 : (WQ == 4 ? 1 : 2);
@@ -73,7 +81,7 @@ struct SplitCfg {
   // Every key warp consumes every stage, in order, so a warp never waits on a
   // ring slot's use u+1 before it consumed use u -- which keeps the
   // parity-based mbarrier waits unambiguous.
-  static constexpr int NCW = WQ * WK;                 // consumer warps
+  static constexpr int NCW = WQ * WK * ND;            // consumer warps
   static constexpr int THREADS = 32 * (1 + NCW);
   static constexpr int TILE_BYTES = KS * ROW;         // one tensor, one stage
   static constexpr int BLOCK_BYTES = KS * SWB;        // one column block of a tile
@@ -81,8 +89,15 @@ struct SplitCfg {
   static constexpr int DATA_BYTES = NS * STAGE_BYTES;
   static constexpr int DP = D + 4;                    // padded exchange row, floats
   static constexpr int EX_BYTES = WQ * WK * 8 * (DP + 2) * 4;
-  static constexpr int SMEM_BYTES = DATA_BYTES + 1024 + 2 * NS * 8;
-  static constexpr int MIN_BLOCKS = (THREADS <= 224) ? 2 : 1;
+  // partial-logit exchange of the dim slices: [stage parity][WQ][ND][32 lanes] float4
+  static constexpr int SX_BYTES = kWide ? 2 * WQ * ND * 32 * 16 : 0;
+  static constexpr int SMEM_BYTES = DATA_BYTES + 1024 + 64 + SX_BYTES;
+  // two CTAs per SM where the threads' registers and both rings fit (228 KB per SM)
+  static constexpr int MIN_BLOCKS = (THREADS <= 224 && 2 * (SMEM_BYTES + 1024) <= 228 * 1024) ? 2 : 1;
+  static_assert(!kWide || (WK == 1 && T == 1 && CBS * SWB == DS * ESZ && WQ <= 2),
+                "sliced head dims: one key warp, one tile per stage, whole column blocks");
+  static_assert(2 * NS * 8 <= 64, "mbarriers fit before the exchange area");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
   static_assert(KS % 16 == 0 && MTS % WK == 0, "whole 16-key tiles per warp");
   static_assert(MTS * CB * 2 <= 32, "a stage needs at most one copy per producer lane");
   static_assert(!kGroupedK || MTS * (1 + CB) <= 32, "grouped K: one copy per producer lane");
@@ -121,6 +136,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
   float* ex = reinterpret_cast<float*>(smem_raw + (base - raw));
   const uint32_t bar_full = base + Cfg::DATA_BYTES;
   const uint32_t bar_empty = bar_full + 8 * Cfg::NS;
+  float4* sx = reinterpret_cast<float4*>(smem_raw + (base - raw) + Cfg::DATA_BYTES + 64);
   __shared__ int s_abort;  // set when a bounded wait gave up
   if (warp == 0 && lane == 0) {  // all of this overlaps the planner's tail
     prefetch_tmap(&tmk);
@@ -358,7 +374,10 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
   // -------------------------------------------------------------- consumers
   const int cw = warp - 1;
   const int wq = cw % WQ;
-  const int wk = cw / WQ;
+  const int wk = (cw / WQ) % Cfg::WK;
+  const int wd = cw / (WQ * Cfg::WK);  // head-dim slice: dims [wd * DS, (wd + 1) * DS)
+  constexpr int DS = Cfg::DS;
+  const int ks0 = wd * (DS / 16);      // first k-step (16 dims) of the slice
   const int g = lane >> 2;  // MMA groupID
   const int t = lane & 3;   // MMA thread-in-group
   const float sl2 = p.scale_log2;
@@ -400,8 +419,9 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
       llo[e] = p.window > 0 ? max(0, K - p.window) : 0;
     }
 
-    // Q^T as the B operand of QK^T: row n = groupID of this warp's 8 rows.
-    uint32_t qf[D / 16][2];
+    // Q^T as the B operand of QK^T: row n = groupID of this warp's 8 rows;
+    // k-step ks of the slice is global k-step ks0 + ks.
+    uint32_t qf[DS / 16][2];
     {
       const int n = pass_base + 8 * wq + g;
       const int tok = n / G;
@@ -410,9 +430,10 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
       if constexpr (!Cfg::kFp8) {
         const uint16_t* qp = static_cast<const uint16_t*>(p.q) + qoff;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          qf[ks][0] = ok ? *reinterpret_cast<const uint32_t*>(qp + 16 * ks + 2 * t) : 0u;
-          qf[ks][1] = ok ? *reinterpret_cast<const uint32_t*>(qp + 16 * ks + 2 * t + 8) : 0u;
+        for (int ks = 0; ks < DS / 16; ++ks) {
+          const int kg = ks0 + ks;
+          qf[ks][0] = ok ? *reinterpret_cast<const uint32_t*>(qp + 16 * kg + 2 * t) : 0u;
+          qf[ks][1] = ok ? *reinterpret_cast<const uint32_t*>(qp + 16 * kg + 2 * t + 8) : 0u;
         }
       } else {
         // fp16 operands; head-dim order permuted to match the fp8 K fragment:
@@ -420,9 +441,10 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
         // K), or d = 16ks + 4t + {0,1 | 2,3} (grouped K).
         constexpr int KPB = Cfg::SWB / 16;  // k-steps per column block
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const int d = Cfg::kGroupedK ? 16 * ks + 4 * t
-                                       : (ks / KPB) * Cfg::SWB + t * (Cfg::SWB / 4) + 4 * (ks % KPB);
+        for (int ks = 0; ks < DS / 16; ++ks) {
+          const int kg = ks0 + ks;
+          const int d = Cfg::kGroupedK ? 16 * kg + 4 * t
+                                       : (kg / KPB) * Cfg::SWB + t * (Cfg::SWB / 4) + 4 * (kg % KPB);
           float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
           if (ok) {
             const uint2 raw4 = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.q) + qoff + d);
@@ -444,23 +466,31 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
 
     float m[2] = {NEG_INF, NEG_INF};  // reference (lazily updated running max)
     float l[2] = {0.f, 0.f};          // this thread's share of the row sums
-    float acc[D / 16][4];
+    float acc[DS / 16][4];
 #pragma unroll
-    for (int dt = 0; dt < D / 16; ++dt) acc[dt][0] = acc[dt][1] = acc[dt][2] = acc[dt][3] = 0.f;
+    for (int dt = 0; dt < DS / 16; ++dt) acc[dt][0] = acc[dt][1] = acc[dt][2] = acc[dt][3] = 0.f;
 
     const bool warp_active = pass_base + 8 * wq < row_hi;
 
     for (int s = 0; s < nst; ++s) {
       const int sit = it + s;
       const int buf = sit % Cfg::NS;
-      if (aborted()) continue;
-      if (!wait_all(bar_full + 8 * buf, (sit / Cfg::NS) & 1)) continue;
-      const uint32_t kt = base + buf * Cfg::STAGE_BYTES;
-      const uint32_t vt = kt + Cfg::TILE_BYTES;
       const int key0 = kb + s * Cfg::KS;
       const int rbase = wk * T * 16;  // row of this warp's first key in the stage
+      // Whether this warp computes on the stage; the same for every slice warp
+      // of a row group, which therefore all meet at the logit exchange.
+      const bool busy = warp_active && key0 + rbase < ke;
+      if (aborted() || !wait_all(bar_full + 8 * buf, (sit / Cfg::NS) & 1)) {
+        // A gave-up wait aborts the pipeline; slice warps still take part in
+        // the exchange barrier so that none of their row group waits on them.
+        if constexpr (Cfg::ND > 1)
+          if (busy) named_barrier_sync(2 + wq, Cfg::ND * 32);
+        continue;
+      }
+      const uint32_t kt = base + buf * Cfg::STAGE_BYTES;
+      const uint32_t vt = kt + Cfg::TILE_BYTES;
 
-      if (warp_active && key0 + rbase < ke) {
+      if (busy) {
 
         // ---- S^T[16 keys x 8 rows] = K Q^T for T tiles
         float c[T][4];
@@ -469,13 +499,14 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
         if constexpr (!Cfg::kFp8) {
           float c2[4] = {0.f, 0.f, 0.f, 0.f};  // second chain when T == 1
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t ko = kt + (ks / 4) * Cfg::BLOCK_BYTES + swz<Cfg::SWB>(lrowK, (ks % 4) * 2 + lchkK);
+          for (int ks = 0; ks < DS / 16; ++ks) {
+            const int kg = ks0 + ks;  // (kg & 3) == (ks & 3): DS / 16 is a multiple of 4
+            const uint32_t ko = kt + (kg / 4) * Cfg::BLOCK_BYTES + swz<Cfg::SWB>(lrowK, (ks % 4) * 2 + lchkK);
 #pragma unroll
             for (int tt = 0; tt < T; ++tt) {
               uint32_t a0, a1, a2, a3;
               if constexpr (Cfg::kGroupedK)
-                ldsm_x4(kt + (rbase + 16 * tt) * Cfg::ROW + ks * 512 + kswz[ks & 1], a0, a1, a2, a3);
+                ldsm_x4(kt + (rbase + 16 * tt) * Cfg::ROW + kg * 512 + kswz[ks & 1], a0, a1, a2, a3);
               else
                 ldsm_x4(ko + (rbase + 16 * tt) * Cfg::SWB, a0, a1, a2, a3);
               if (T == 1 && (ks & 1))
@@ -495,9 +526,10 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
           for (int tt = 0; tt < T; ++tt) {
             const uint32_t kg = kt + (rbase + 16 * tt) * Cfg::ROW + 4 * t;
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-              const uint32_t w0 = lds32(kg + ks * 256 + ((g ^ ((2 * ks) & 7)) << 4));
-              const uint32_t w1 = lds32(kg + ks * 256 + 128 + ((g ^ ((2 * ks + 1) & 7)) << 4));
+            for (int ks = 0; ks < DS / 16; ++ks) {
+              // ((2 * (ks0 + ks)) & 7) == ((2 * ks) & 7): DS / 16 is a multiple of 4
+              const uint32_t w0 = lds32(kg + (ks0 + ks) * 256 + ((g ^ ((2 * ks) & 7)) << 4));
+              const uint32_t w1 = lds32(kg + (ks0 + ks) * 256 + 128 + ((g ^ ((2 * ks + 1) & 7)) << 4));
               uint32_t a0, a1, a2, a3;
               e4m3x4_to_f16x2x2(w0, a0, a2);
               e4m3x4_to_f16x2x2(w1, a1, a3);
@@ -511,11 +543,12 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
           for (int tt = 0; tt < T; ++tt) {
             const int rt = rbase + 16 * tt;
 #pragma unroll
-            for (int cb = 0; cb < Cfg::CB; ++cb) {
+            for (int cb = 0; cb < Cfg::CBS; ++cb) {  // the slice's column blocks
               uint32_t wg[4 * CPT], wg8[4 * CPT];
 #pragma unroll
               for (int k = 0; k < CPT; ++k) {
-                const uint32_t o = kt + cb * Cfg::BLOCK_BYTES + rt * Cfg::SWB + swz<Cfg::SWB>(g, t * CPT + k);
+                const uint32_t o = kt + (wd * Cfg::CBS + cb) * Cfg::BLOCK_BYTES + rt * Cfg::SWB +
+                                   swz<Cfg::SWB>(g, t * CPT + k);
                 const uint4 x = lds128(o);
                 const uint4 y = lds128(o + 8 * Cfg::SWB);
                 wg[4 * k] = x.x; wg[4 * k + 1] = x.y; wg[4 * k + 2] = x.z; wg[4 * k + 3] = x.w;
@@ -530,6 +563,21 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
               }
             }
           }
+        }
+
+        // ---- sliced head dims: sum the slices' partial logits (same order in
+        // every warp of the row group)
+        if constexpr (Cfg::ND > 1) {
+          float4* xs = sx + ((s & 1) * WQ + wq) * Cfg::ND * 32;
+          xs[wd * 32 + lane] = make_float4(c[0][0], c[0][1], c[0][2], c[0][3]);
+          named_barrier_sync(2 + wq, Cfg::ND * 32);
+          float4 a = xs[lane];
+#pragma unroll
+          for (int k = 1; k < Cfg::ND; ++k) {
+            const float4 b = xs[k * 32 + lane];
+            a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+          }
+          c[0][0] = a.x; c[0][1] = a.y; c[0][2] = a.z; c[0][3] = a.w;
         }
 
         // ---- online softmax (log2 domain), lazily rescaled
@@ -560,7 +608,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
           l[0] *= al0;
           l[1] *= al1;
 #pragma unroll
-          for (int dt = 0; dt < D / 16; ++dt) {
+          for (int dt = 0; dt < DS / 16; ++dt) {
             acc[dt][0] *= al0;
             acc[dt][1] *= al1;
             acc[dt][2] *= al0;
@@ -587,8 +635,9 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
         // uninitialised shared memory: zero them so 0 * NaN cannot occur.
         if constexpr (!Cfg::kFp8) {
 #pragma unroll
-          for (int dt = 0; dt < D / 16; ++dt) {
-            const uint32_t vo = vt + (dt / 4) * Cfg::BLOCK_BYTES + swz<Cfg::SWB>(lrowV, (dt % 4) * 2 + lchkV);
+          for (int dt = 0; dt < DS / 16; ++dt) {
+            const int dg = ks0 + dt;  // global 16-dim tile; (dg & 3) == (dt & 3)
+            const uint32_t vo = vt + (dg / 4) * Cfg::BLOCK_BYTES + swz<Cfg::SWB>(lrowV, (dt % 4) * 2 + lchkV);
 #pragma unroll
             for (int tt = 0; tt < T; ++tt) {
               const int kbt = key0 + rbase + 16 * tt;
@@ -615,8 +664,8 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
             const uint32_t z0 = (kq < ke) ? 0xffffffffu : 0u, z1 = (kq + 1 < ke) ? 0xffffffffu : 0u;
             const uint32_t z8 = (kq + 8 < ke) ? 0xffffffffu : 0u, z9 = (kq + 9 < ke) ? 0xffffffffu : 0u;
 #pragma unroll
-            for (int u = 0; u < D / 32; ++u) {
-              const int byte = 32 * u + 4 * g;
+            for (int u = 0; u < DS / 32; ++u) {
+              const int byte = 32 * (wd * (DS / 32) + u) + 4 * g;
               const int cb = byte / Cfg::SWB;
               const int inb = byte % Cfg::SWB;
               const uint32_t blk = vt + cb * Cfg::BLOCK_BYTES;
@@ -658,19 +707,19 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     float* ex_l = ex_m + WQ * Cfg::WK * 8;
     const int wslot = (wq * Cfg::WK + wk) * 8;
 #pragma unroll
-    for (int dt = 0; dt < D / 16; ++dt) {
+    for (int dt = 0; dt < DS / 16; ++dt) {
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        int d;
+        int d = wd * DS;  // the slice's dims
         if constexpr (!Cfg::kFp8)
-          d = 16 * dt + g + 8 * hh;
+          d += 16 * dt + g + 8 * hh;
         else
-          d = 32 * (dt / 2) + 4 * g + 2 * (dt % 2) + hh;
+          d += 32 * (dt / 2) + 4 * g + 2 * (dt % 2) + hh;
         ex_o[(wslot + 2 * t) * Cfg::DP + d] = acc[dt][2 * hh];
         ex_o[(wslot + 2 * t + 1) * Cfg::DP + d] = acc[dt][2 * hh + 1];
       }
     }
-    if (g == 0) {
+    if (g == 0 && wd == 0) {  // every slice warp holds the same m and l
       ex_m[wslot + 2 * t] = m[0];
       ex_m[wslot + 2 * t + 1] = m[1];
       ex_l[wslot + 2 * t] = l[0];
@@ -767,12 +816,19 @@ cudaError_t launch_split_cfg(const SplitParams& p, const CUtensorMap& tk,
 template <int D, int KL>
 cudaError_t launch_split_d(const SplitParams& p, int kv_dtype, int wq,
                            const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s) {
-#define PA_SPLIT_CASE(KVT)                                                     \
-  switch (wq) {                                                                \
-    case 1: return launch_split_cfg<D, KVT, 1, KL>(p, tk, tv, s);           \
-    case 2: return launch_split_cfg<D, KVT, 2, KL>(p, tk, tv, s);           \
-    case 3: return launch_split_cfg<D, KVT, 3, KL>(p, tk, tv, s);           \
-    default: return launch_split_cfg<D, KVT, 4, KL>(p, tk, tv, s);          \
+  constexpr int kMaxWq = split_max_row_groups(D);
+#define PA_SPLIT_CASE(KVT)                                                               \
+  switch (wq) {                                                                          \
+    case 1: return launch_split_cfg<D, KVT, 1, KL>(p, tk, tv, s);                     \
+    case 2:                                                                              \
+      if constexpr (kMaxWq >= 2) return launch_split_cfg<D, KVT, 2, KL>(p, tk, tv, s); \
+      return cudaErrorInvalidValue;                                                      \
+    case 3:                                                                              \
+      if constexpr (kMaxWq >= 3) return launch_split_cfg<D, KVT, 3, KL>(p, tk, tv, s); \
+      return cudaErrorInvalidValue;                                                      \
+    default:                                                                             \
+      if constexpr (kMaxWq >= 4) return launch_split_cfg<D, KVT, 4, KL>(p, tk, tv, s); \
+      return cudaErrorInvalidValue;                                                      \
   }
   switch (kv_dtype) {
     case PA_BF16: PA_SPLIT_CASE(PA_BF16)

@@ -1,0 +1,13 @@
+// pa_split_d384.cu -- split-KV decode kernels for head_dim 384 (bf16, fp16 and
+// fp8-e4m3 caches; K row-major or grouped; 1 or 2 query-row groups per pass).
+#include "pa_split.cuh"
+
+namespace pa {
+
+cudaError_t launch_split_d384(const SplitParams& p, int kv_dtype, int row_groups, int k_layout,
+                                const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s) {
+  return k_layout == PA_K_GROUPED ? launch_split_d<384, 1>(p, kv_dtype, row_groups, tk, tv, s)
+                                  : launch_split_d<384, 0>(p, kv_dtype, row_groups, tk, tv, s);
+}
+
+}  // namespace pa

@@ -120,7 +120,7 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
   if (kv_dtype == PA_FP8_E4M3 && (!std::isfinite(k_scale) || !std::isfinite(v_scale)))
     return PA_ERR_INVALID_ARG;
   if (num_seqs > PA_MAX_SEQS || num_q_heads % num_kv_heads != 0) return PA_ERR_UNSUPPORTED;
-  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
+  if (!pa::head_dim_supported(head_dim)) return PA_ERR_UNSUPPORTED;
   if (block_size != 16 && block_size != 64 && block_size != 128) return PA_ERR_UNSUPPORTED;
   if (static_cast<long long>(num_blocks) * num_kv_heads * block_size >= (1ll << 31))
     return PA_ERR_UNSUPPORTED;
@@ -149,7 +149,7 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
   if (lay.total > PA_STATIC_SCRATCH_BYTES)
     return PA_ERR_UNSUPPORTED;  // this batch needs more scratch than the static array holds
   const int G = num_q_heads / num_kv_heads;
-  const int wq = pa::split_row_groups(max_query_len, G);
+  const int wq = pa::split_row_groups(max_query_len, G, head_dim);
 
   char* base = static_cast<char*>(scratch_address(device));
   if (!base) return PA_ERR_CUDA;

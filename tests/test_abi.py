@@ -53,7 +53,8 @@ def _build_status(lib, **kw):
     (dict(n=4097), binding.PA_ERR_UNSUPPORTED),
     (dict(hq=6, hkv=4), binding.PA_ERR_UNSUPPORTED),
     (dict(d=96), binding.PA_ERR_UNSUPPORTED),
-    (dict(d=512), binding.PA_ERR_UNSUPPORTED),
+    (dict(d=192), binding.PA_ERR_UNSUPPORTED),   # above 128: multiples of 128 only
+    (dict(d=1152), binding.PA_ERR_UNSUPPORTED),  # above 1024
     (dict(parts=1 << 20), binding.PA_ERR_UNSUPPORTED),
 ])
 def test_plan_build_rejects_bad_parameters_before_cuda(lib, kw, want):

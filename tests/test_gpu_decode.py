@@ -232,6 +232,48 @@ def test_grouped_k_layout_checks(dev):
     assert st == binding.PA_ERR_UNSUPPORTED  # no third K layout
 
 
+# -------------------------------------------- head dims 384 to 1024
+
+WIDE = [384, 512, 640, 768, 896, 1024]
+
+
+@pytest.mark.parametrize("D", WIDE)
+@pytest.mark.parametrize("kv,q", [("bf16", "bf16"), ("fp16", "fp16"), ("fp8", "bf16")])
+def test_wide_head_dims(dev, D, kv, q):
+    """Head dims above 256 run one warp per 128-dim slice with the partial
+    logits summed through shared memory; K row-major and grouped."""
+    bs = 16 if D % 256 else 128
+    w = batch(dev, [1, 15, 17, 255, 257, 700, 2100], H=(8, 1), D=D, bs=bs, kv=kv, q=q, seed=D)
+    check(w)
+    w5 = wl.with_k_groups(w)
+    out5, plan = run(w5)
+    assert max_diff(out5, oracle_decode(w5.to("cpu"))) <= TOL[kv]
+    assert plan.read_errors() == 0
+
+
+@pytest.mark.parametrize("D", [512, 1024])
+def test_wide_head_dims_rows_groups_and_merges(dev, D):
+    """Wide heads with GQA groups of 16 (two row groups, or two row chunks),
+    multi-token rows with padding, and partitions merged by warps (few pieces)
+    and by CTAs (many pieces)."""
+    check(batch(dev, [300, 5000, 40], H=(32, 2), D=D, kv="bf16", seed=D + 1))
+    check(batch(dev, [600, 40, 3000, 2, 0], ql=[3, 3, 3, 3, 1], H=(8, 1), D=D, bs=64, kv="fp8",
+                pad=5, seed=D + 2))
+    for P, W in ((4, 16), (64, 512)):
+        check(batch(dev, [20000, 900, 40], H=(8, 1), D=D, kv="bf16", seed=D + 3, budget=W,
+                    max_partitions=P))
+
+
+def test_wide_head_dims_window_sinks_pieces(dev):
+    w = batch(dev, [40000] + [300 + 37 * i for i in range(15)], H=(8, 1), D=640, kv="fp8",
+              seed=41, budget=32)
+    sinks = np.linspace(-2, 2, 8)
+    for window in (0, 9000):
+        out, plan = run_ext(w, window=window, sinks=sinks)
+        assert max_diff(out, oracle_decode(w.to("cpu"), window=window, sinks=sinks)) <= TOL["fp8"]
+        assert plan.read_errors() == 0
+
+
 # ---------------------------------------------------- multi-token rows (cu)
 
 def test_verify_rows_and_padding(dev):
