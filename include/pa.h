@@ -137,7 +137,8 @@ typedef struct pa_plan pa_plan; /* opaque */
  * 2 x multiProcessorCount of the device ([ATOM-2514] Design, "default
  * budget").  kind is a pa_plan_kind.  The plan is unusable by pa_decode until
  * the first pa_plan_refresh.  Supported: 1 <= num_seqs <= 4096, Hq % Hkv == 0,
- * head_dim in {64, 128, 256}.  Returns PA_ERR_OOM / PA_ERR_CUDA on device
+ * head_dim 64 or a multiple of 128 up to 1024 (the [ATOM-2366] capability
+ * gate, review item 5).  Returns PA_ERR_OOM / PA_ERR_CUDA on device
  * failures (nothing is leaked), PA_ERR_INVALID_ARG / PA_ERR_UNSUPPORTED on bad
  * parameters.  On success *plan owns the buffers until pa_plan_destroy. */
 int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_q_heads, int num_kv_heads,

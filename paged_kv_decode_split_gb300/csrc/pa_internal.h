@@ -95,7 +95,8 @@ struct SplitParams {
 // Head dims the kernels take: 64, and 128 to 1024 in steps of 128.
 constexpr bool head_dim_supported(int D) { return D == 64 || (D % 128 == 0 && D >= 128 && D <= 1024); }
 // Query-row groups of 8 per pass the split kernel is built with for head_dim D:
-// head dims above 256 run one warp per 128-dim slice, so fewer row groups fit.
+// head dims above 256 run one warp per 128- or 256-dim slice, so fewer row
+// groups fit.
 constexpr int split_max_row_groups(int D) { return D <= 256 ? 4 : (D <= 512 ? 2 : 1); }
 // Rows of one TMA box of a KV tile for head_dim D, cache dtype, block size.
 int split_box_rows(int D, int kv_dtype, int bs);

@@ -63,13 +63,14 @@ struct SplitCfg {
   static constexpr int ROW = D * ESZ;                 // bytes per key row
   static constexpr int SWB = ROW < 128 ? ROW : 128;   // swizzle span = box row bytes
   static constexpr int CB = ROW / SWB;                // column blocks per key row
-  // Head dims above 256 are cut into 128-dim slices, one consumer warp each:
-  // a warp forms the partial logits of its slice, the slices' partials are
-  // summed through shared memory (every warp of the row group adds them in
-  // the same order, so all hold the same logits and softmax state), and each
-  // warp accumulates P V for its own slice.  Stages are one 16-key tile.
+  // Head dims above 256 are cut into slices of 256 dims (128 when 256 does
+  // not divide D), one consumer warp each: a warp forms the partial logits of
+  // its slice, the slices' partials are summed through shared memory (every
+  // warp of the row group adds them in the same order, so all hold the same
+  // logits and softmax state), and each warp accumulates P V for its own
+  // slice.  Stages are one 16-key tile.
   static constexpr bool kWide = D > 256;
-  static constexpr int DS = kWide ? 128 : D;          // head dims per consumer warp
+  static constexpr int DS = kWide ? (D % 256 == 0 ? 256 : 128) : D;  // head dims per consumer warp
   static constexpr int ND = D / DS;                   // dim slices
   static constexpr int CBS = DS * ESZ / SWB;          // column blocks per slice
   static constexpr int KS = kWide ? 16 : kStageTensorBytes / ROW;  // keys per stage

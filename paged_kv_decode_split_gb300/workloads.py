@@ -263,6 +263,29 @@ CONFIGS["uniform_k5"] = lambda seed=0, device="cpu": with_k_groups(uniform(seed,
 CONFIGS["skewed_k5"] = lambda seed=0, device="cpu": with_k_groups(skewed(seed, device))
 
 
+def uniform_d512(seed: int = 0, device="cpu") -> Workload:
+    """16 decodes x 8192 context, Hq/Hkv 32/4, D 512, page 16, bf16."""
+    return make_batch("uniform_d512", [8192] * 16, None, 32, 4, 512, 16, "bf16", seed=seed,
+                      device=device)
+
+
+def skewed_d1024(seed: int = 0, device="cpu") -> Workload:
+    """The skewed length mix (32 decodes, lognormal median 4096, sigma 1.5) with
+    Hq/Hkv 16/2, D 1024, page 16, fp8 e4m3fn KV (scale 0.05), K in the grouped
+    5-D layout, budget 2 x 148, partition cap 256."""
+    lens = lognormal_lengths(32, 4096, 1.5, 64, 131072, seed)
+    w = make_batch("skewed_d1024", lens, None, 16, 2, 1024, 16, "fp8", seed=seed,
+                   kv_scale=0.05, device=device, budget=296, max_partitions=256)
+    w.meta["max_over_min"] = max(lens) / min(lens)
+    w = with_k_groups(w)
+    w.name = "skewed_d1024"
+    return w
+
+
+CONFIGS["uniform_d512"] = uniform_d512
+CONFIGS["skewed_d1024"] = skewed_d1024
+
+
 def subset(w: Workload, requests: Sequence[int]) -> Workload:
     """The sub-batch of the given requests, with their pages copied into a compact
     pool (same bytes, same page order inside each request).  Every output row of a

@@ -240,7 +240,7 @@ WIDE = [384, 512, 640, 768, 896, 1024]
 @pytest.mark.parametrize("D", WIDE)
 @pytest.mark.parametrize("kv,q", [("bf16", "bf16"), ("fp16", "fp16"), ("fp8", "bf16")])
 def test_wide_head_dims(dev, D, kv, q):
-    """Head dims above 256 run one warp per 128-dim slice with the partial
+    """Head dims above 256 run one warp per 128- or 256-dim slice with the partial
     logits summed through shared memory; K row-major and grouped."""
     bs = 16 if D % 256 else 128
     w = batch(dev, [1, 15, 17, 255, 257, 700, 2100], H=(8, 1), D=D, bs=bs, kv=kv, q=q, seed=D)
@@ -519,7 +519,8 @@ def _pick(w, k=4):
 
 
 FULL = ["uniform", "skewed", "mtp_verify", "mixed_prompt", "large_bf16", "large_fp8",
-        "uniform_w1024", "skewed_w4096", "uniform_k5", "skewed_k5"]
+        "uniform_w1024", "skewed_w4096", "uniform_k5", "skewed_k5", "uniform_d512",
+        "skewed_d1024"]
 
 
 @pytest.mark.parametrize("name", FULL)

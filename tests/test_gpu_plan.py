@@ -46,7 +46,7 @@ def _oracle_plan(plan, lens, cu, Hkv, kind, window=0):
 @pytest.mark.parametrize("name", list(wl.CONFIGS))
 @pytest.mark.parametrize("kind", [binding.PROPORTIONAL, binding.UNIFORM])
 def test_config_plans_bit_exact(dev, name, kind):
-    w = wl.CONFIGS[name](0, "cpu") if name not in ("large_bf16", "large_fp8") else None
+    w = wl.CONFIGS[name](0, dev) if name not in ("large_bf16", "large_fp8") else None
     if w is None:  # only the lengths matter: skip drawing 8 GB of cache values
         lens = wl.lognormal_lengths(512, 2048, 1.2, 16, 65536, 0)
         cu, Hq, Hkv, W, win = None, 64, 8, 0, 0
