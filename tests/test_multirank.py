@@ -54,3 +54,10 @@ def test_single_rank_needs_no_process_group():
     import bench
     assert bench.max_over_ranks(2.5, 1) == 2.5
     bench.barrier(1)
+
+
+def test_every_workload_is_described():
+    sys.path.insert(0, ROOT)
+    import bench
+    from paged_kv_decode_split_gb300 import workloads as wl
+    assert set(wl.CONFIGS) <= set(bench.DESCRIBE)
