@@ -58,6 +58,7 @@ DESCRIBE = {
     "uniform_k5": "uniform decode with K in the grouped layout [nb, Hkv, D/16, 16, 16]",
     "skewed_k5": "skewed agentic decode with K in the grouped layout [nb, Hkv, D/16, 16, 16]",
     "uniform_d512": "uniform decode: 16 seqs x 8192 ctx, Hq/Hkv 32/4, D 512, page 16, bf16",
+    "uniform_d1024": "uniform decode: 16 seqs x 8192 ctx, Hq/Hkv 32/4, D 1024, page 16, bf16",
     "skewed_d1024": "skewed agentic decode: 32 seqs, ctx lognormal(4096, 1.5) in [64,131072], "
                     "Hq/Hkv 16/2, D 1024, page 16, fp8-e4m3 KV (scale 0.05), K grouped, "
                     "budget 296, cap 256",

@@ -269,6 +269,12 @@ def uniform_d512(seed: int = 0, device="cpu") -> Workload:
                       device=device)
 
 
+def uniform_d1024(seed: int = 0, device="cpu") -> Workload:
+    """16 decodes x 8192 context, Hq/Hkv 32/4, D 1024, page 16, bf16."""
+    return make_batch("uniform_d1024", [8192] * 16, None, 32, 4, 1024, 16, "bf16", seed=seed,
+                      device=device)
+
+
 def skewed_d1024(seed: int = 0, device="cpu") -> Workload:
     """The skewed length mix (32 decodes, lognormal median 4096, sigma 1.5) with
     Hq/Hkv 16/2, D 1024, page 16, fp8 e4m3fn KV (scale 0.05), K in the grouped
@@ -283,6 +289,7 @@ def skewed_d1024(seed: int = 0, device="cpu") -> Workload:
 
 
 CONFIGS["uniform_d512"] = uniform_d512
+CONFIGS["uniform_d1024"] = uniform_d1024
 CONFIGS["skewed_d1024"] = skewed_d1024
 
 
