@@ -66,6 +66,9 @@ def _load():
         lib.oracle_plan.restype = i64
         lib.oracle_plan_window.argtypes = [i32, P, P, i32, i32, i32, i32, i32, i32, P, i64, P]
         lib.oracle_plan_window.restype = i64
+        lib.oracle_sparse_select.argtypes = [P, i32, P, P, i32, i32, i32, i32, i32, i32, P,
+                                             i32, P]
+        lib.oracle_sparse_select.restype = i32
         lib.oracle_decode.argtypes = [P, i32, i32, i32, i32, P, P, i32, dbl, dbl, i32, i32,
                                       P, i32, P, P, i32, dbl, P]
         lib.oracle_decode.restype = None
@@ -169,6 +172,41 @@ def decode(q_bits, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale, block_
     else:
         _load().oracle_decode(*args, _ptr(out))
     return out
+
+
+def sparse_select(scores, context_lens, block_tables, block_size: int, top_k: int,
+                  init_blocks: int, local_blocks: int, sel_stride: int | None = None):
+    """Sparse top-k block selection (the readings in pa_oracle.c).  scores
+    [n, >= max_blocks] float32 (None when top_k == 0).  Returns (sel_tables
+    [n, sel_stride] int32 -- physical blocks of the selected logical blocks in
+    ascending order, then -1 -- and sel_lens [n] int32, the tokens they hold)."""
+    bt = _c(block_tables, np.int32)
+    lens = _c(context_lens, np.int32)
+    n, max_blocks = bt.shape
+    if sel_stride is None:
+        sel_stride = init_blocks + top_k + local_blocks
+    sc = None if scores is None else _c(scores, np.float32)
+    stride = 0 if sc is None else sc.shape[1]
+    if sc is None and top_k > 0:
+        raise ValueError("scores are needed when top_k > 0")
+    sel = np.empty((n, sel_stride), dtype=np.int32)
+    sl = np.empty(n, dtype=np.int32)
+    _load().oracle_sparse_select(_ptr(sc), stride, _ptr(lens), _ptr(bt), max_blocks, n,
+                                 block_size, top_k, init_blocks, local_blocks, _ptr(sel),
+                                 sel_stride, _ptr(sl))
+    return sel, sl
+
+
+def sparse_decode(q_bits, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale, block_tables,
+                  context_lens, scale, scores, block_size: int, top_k: int, init_blocks: int,
+                  local_blocks: int):
+    """Sparse top-k decode: one query token per request attends to the keys of
+    its selected blocks (sparse_select), i.e. the exact decode over the sparse
+    block table and the selected lengths."""
+    sel, sl = sparse_select(scores, context_lens, block_tables, block_size, top_k, init_blocks,
+                            local_blocks)
+    return decode(q_bits, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale, sel, sl, None,
+                  scale)
 
 
 def decode_planned(q_bits, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale, block_tables,

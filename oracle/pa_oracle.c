@@ -36,8 +36,8 @@
  *   - fp8 is OCP e4m3fn (bias 7, no infinities, S.1111.111 = NaN); a stored
  *     byte b means e4m3fn(b) * scale;
  *   - the kv head of q head hq is hq / (Hq / Hkv);
- *   - sliding window W > 0 ([RDNA-29] Change 1: "the sliding window applies
- *     per token"): token i, which may see keys [0, K_i), sees only the W most
+ *   - sliding window W > 0 ([RDNA-29] Change 1 applies the window to each
+ *     token on its own): token i, which may see keys [0, K_i), sees only the W most
  *     recent of them, [max(0, K_i - W), K_i); W = 0 means no window;
  *   - with a window the plan sizes a request by the keys its tokens read: it
  *     starts at the tile holding the first token's first visible key and runs
@@ -47,7 +47,20 @@
  *     denominator only: out = sum_j e^(s_j) v_j / (sum_j e^(s_j) + e^(sink));
  *   - K may also come in the 5-D layout [num_blocks, Hkv, D/16, block_size, 16]
  *     the pages' gate checks (the head dim in 16-element groups, each group's
- *     rows contiguous per page); V keeps [num_blocks, Hkv, block_size, D].
+ *     rows contiguous per page); V keeps [num_blocks, Hkv, block_size, D];
+ *   - sparse top-k decode ([ATOM-2366] section 3, the sparse call sites read a
+ *     fixed top-k window; [ATOM-2514] Design, "Once-per-step sparse refresh":
+ *     the local tail block is always selected, so a row's length depends on
+ *     seq_len only; Known Limitations item 2: top-k, init-block and
+ *     local-block settings): the indexer that scores a request's blocks is not
+ *     described, so its per-block fp32 scores are an input.  Of request r's
+ *     nb = ceil(S / block_size) logical blocks, the first init_blocks and the
+ *     last local_blocks are always selected, and of the others the top_k with
+ *     the highest score, scores compared in the total order of their fp32 bit
+ *     patterns (-NaN < -inf < ... < -0 < +0 < ... < +inf < +NaN) and equal
+ *     scores by the lower block index.  The selected blocks in ascending
+ *     logical order make the request's sparse block-table row and its length
+ *     is the tokens they hold (the tail block holds S - (nb - 1) * block_size).
  */
 #include <math.h>
 #include <stdint.h>
@@ -405,6 +418,77 @@ void oracle_decode_planned(const void* q, int q_dtype, int num_tokens, int num_q
                             kv_dtype, k_scale, v_scale, num_kv_heads, block_size, block_tables,
                             max_blocks, context_lens, cu, n, scale, work_info, reduce_info, tile,
                             0, NULL, 0, out);
+}
+
+/* ------------------------------------------------------ sparse top-k select */
+
+/* The fp32 total order as an unsigned key: flip every bit of a negative
+ * pattern, set the sign bit of a non-negative one. */
+static uint32_t order_key(float x) {
+  uint32_t u;
+  memcpy(&u, &x, sizeof u);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+typedef struct {
+  uint32_t key;
+  int block;
+} scored_block;
+
+/* Higher key first, then lower block index. */
+static int by_score_then_index(const void* a, const void* b) {
+  const scored_block* x = (const scored_block*)a;
+  const scored_block* y = (const scored_block*)b;
+  if (x->key != y->key) return x->key > y->key ? -1 : 1;
+  return (x->block > y->block) - (x->block < y->block);
+}
+
+/* Selection for every request (see the reading above).  scores: row r holds
+ * the scores of r's logical blocks at [r * score_stride, ...); may be NULL when
+ * top_k == 0.  Blocks at or past max_blocks do not exist for the selection.
+ * sel_tables [num_seqs][sel_stride] receives the physical blocks (block_tables
+ * entries) of the selected logical blocks in ascending order, -1 after them;
+ * sel_lens[r] the tokens they hold.  Returns the largest selection size. */
+int oracle_sparse_select(const float* scores, int score_stride, const int32_t* context_lens,
+                         const int32_t* block_tables, int max_blocks, int num_seqs,
+                         int block_size, int top_k, int init_blocks, int local_blocks,
+                         int32_t* sel_tables, int sel_stride, int32_t* sel_lens) {
+  int most = 0;
+  unsigned char* take = (unsigned char*)malloc(max_blocks > 0 ? (size_t)max_blocks : 1);
+  scored_block* cand = (scored_block*)malloc(sizeof(scored_block) * (max_blocks > 0 ? max_blocks : 1));
+  for (int r = 0; r < num_seqs; ++r) {
+    const long long S = context_lens[r] > 0 ? context_lens[r] : 0;
+    long long nb_all = (S + block_size - 1) / block_size;
+    const int nb = (int)(nb_all < max_blocks ? nb_all : max_blocks);
+    int ncand = 0;
+    for (int b = 0; b < nb; ++b) {
+      const int fixed = b < init_blocks || b >= nb - local_blocks;
+      take[b] = (unsigned char)fixed;
+      if (!fixed) {
+        cand[ncand].key = order_key(scores[(size_t)r * score_stride + b]);
+        cand[ncand].block = b;
+        ++ncand;
+      }
+    }
+    qsort(cand, (size_t)ncand, sizeof(scored_block), by_score_then_index);
+    for (int i = 0; i < ncand && i < top_k; ++i) take[cand[i].block] = 1;
+    int count = 0;
+    long long tokens = 0;
+    for (int b = 0; b < nb; ++b) {
+      if (!take[b]) continue;
+      if (count < sel_stride)
+        sel_tables[(size_t)r * sel_stride + count] = block_tables[(size_t)r * max_blocks + b];
+      ++count;
+      const long long end = (long long)(b + 1) * block_size < S ? (long long)(b + 1) * block_size : S;
+      tokens += end - (long long)b * block_size;
+    }
+    for (int i = count; i < sel_stride; ++i) sel_tables[(size_t)r * sel_stride + i] = -1;
+    sel_lens[r] = (int32_t)tokens;
+    if (count > most) most = count;
+  }
+  free(take);
+  free(cand);
+  return most;
 }
 
 /* Threads an OpenMP region of this library uses (1 without OpenMP). */

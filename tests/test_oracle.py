@@ -559,3 +559,102 @@ def test_grouped_k_layout_element_positions():
     k5 = wl.with_k_groups(w).k_cache.view(torch.int16)
     for j, dim in ((0, 0), (3, 17), (15, 63), (7, 48)):
         assert int(k5[1, 1, dim // 16, j, dim % 16]) == (j << 8) | dim
+
+
+# ------------------------------------------------------- sparse top-k decode
+
+def test_sparse_select_order_by_hand():
+    """Seven blocks, no fixed blocks: the scores rank NaN > 2.0 (block 3) = 2.0
+    (block 4, the higher index loses the tie) > 1.0 > +0 > -0 > -inf, so the
+    top k for k = 0..7 adds blocks 1, 3, 4, 0, 6, 5, 2 in that order."""
+    sc = np.array([[1.0, np.nan, -np.inf, 2.0, 2.0, -0.0, 0.0]], dtype=np.float32)
+    bt = np.arange(10, 17, dtype=np.int32)[None]
+    rank = [1, 3, 4, 0, 6, 5, 2]
+    for k in range(8):
+        sel, sl = oracle.sparse_select(sc, np.array([7 * 16], np.int32), bt, 16, k, 0, 0)
+        want = sorted(10 + b for b in rank[:k])
+        assert sel[0].tolist() == want, k
+        assert sl[0] == 16 * k
+
+
+def _order_key(x: np.float32) -> int:
+    u = int(np.array([x], dtype=np.float32).view(np.uint32)[0])
+    return (~u & 0xFFFFFFFF) if u & 0x80000000 else (u | 0x80000000)
+
+
+def _select_by_repeated_argmax(scores, S, bs, top_k, init, local, max_blocks):
+    """The same selection found another way: fixed blocks, then top_k times the
+    remaining candidate with the largest (key, -index)."""
+    nb = min(-(-S // bs) if S > 0 else 0, max_blocks)
+    chosen = {b for b in range(nb) if b < init or b >= nb - local}
+    rest = [b for b in range(nb) if b not in chosen]
+    for _ in range(top_k):
+        if not rest:
+            break
+        best = max(rest, key=lambda b: (_order_key(scores[b]), -b))
+        chosen.add(best)
+        rest.remove(best)
+    blocks = sorted(chosen)
+    tokens = sum(min((b + 1) * bs, S) - b * bs for b in blocks)
+    return blocks, tokens
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_sparse_select_matches_repeated_argmax(seed):
+    rng = np.random.default_rng(seed)
+    n, bs, max_blocks = 12, 16, 20
+    palette = np.array([0.5, -1.0, 3.0, 0.0, -0.0, np.inf, -np.inf, np.nan, 3.0], np.float32)
+    scores = palette[rng.integers(0, len(palette), (n, max_blocks))]  # many ties
+    lens = rng.integers(0, max_blocks * bs + 1, n).astype(np.int32)
+    lens[0], lens[1], lens[2] = 0, 5, bs  # empty, one partial block, one full block
+    bt = rng.permutation(1000)[: n * max_blocks].reshape(n, max_blocks).astype(np.int32)
+    for top_k, init, local in [(0, 1, 1), (3, 0, 1), (4, 1, 2), (5, 2, 0), (25, 1, 1), (2, 9, 9)]:
+        sel, sl = oracle.sparse_select(scores, lens, bt, bs, top_k, init, local)
+        for r in range(n):
+            blocks, tokens = _select_by_repeated_argmax(scores[r], int(lens[r]), bs, top_k, init,
+                                                        local, max_blocks)
+            want = [int(bt[r, b]) for b in blocks]
+            assert sel[r, : len(want)].tolist() == want, (r, top_k, init, local)
+            assert (sel[r, len(want):] == -1).all()
+            assert sl[r] == tokens
+
+
+def _sparse_case(kv="bf16", seed=0):
+    return wl.make_batch("sparse", [1, 40, 300, 777, 1500], None, 8, 2, 64, 16, kv, seed=seed,
+                         kv_scale=0.05)
+
+
+def test_sparse_decode_with_every_block_selected_is_dense():
+    w = _sparse_case()
+    a = oracle_args(w)
+    nbmax = w.block_tables.shape[1]
+    scores = np.random.default_rng(1).normal(size=(w.num_seqs, nbmax)).astype(np.float32)
+    sparse = oracle.sparse_decode(*a[:9], a[10], scores, w.block_size, nbmax, 1, 1)
+    assert np.array_equal(sparse, oracle_decode(w))
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_sparse_decode_matches_sdpa_over_the_selected_keys(kv):
+    """torch SDPA in float64 over the explicit token positions of the selected
+    blocks (gathered from the request's own block table)."""
+    w = _sparse_case(kv, seed=2)
+    a = oracle_args(w)
+    nbmax = w.block_tables.shape[1]
+    scores = np.random.default_rng(3).normal(size=(w.num_seqs, nbmax)).astype(np.float32)
+    top_k, init, local = 5, 1, 2
+    got = oracle.sparse_decode(*a[:9], a[10], scores, w.block_size, top_k, init, local)
+    G = w.num_q_heads // w.num_kv_heads
+    for r in range(w.num_seqs):
+        S = int(w.context_lens[r])
+        blocks, _ = _select_by_repeated_argmax(scores[r], S, w.block_size, top_k, init, local,
+                                               nbmax)
+        pos = [j for b in blocks for j in range(b * w.block_size, min((b + 1) * w.block_size, S))]
+        pages = w.block_tables[r, torch.tensor(pos) // w.block_size].long()
+        slot = torch.tensor(pos) % w.block_size
+        K = _dequant(w.k_cache[pages, :, slot], w.kv_dtype, w.k_scale)  # [keys, Hkv, D]
+        V = _dequant(w.v_cache[pages, :, slot], w.kv_dtype, w.v_scale)
+        K = K.permute(1, 0, 2).repeat_interleave(G, dim=0)
+        V = V.permute(1, 0, 2).repeat_interleave(G, dim=0)
+        q = w.q[r].to(torch.float64)[:, None, :]
+        o = F.scaled_dot_product_attention(q, K, V, scale=w.scale)[:, 0]
+        assert np.abs(got[r] - o.numpy()).max() < 1e-12, r
