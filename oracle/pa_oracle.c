@@ -464,8 +464,8 @@ int oracle_sparse_select(const float* scores, int score_stride, const int32_t* c
     for (int b = 0; b < nb; ++b) {
       const int fixed = b < init_blocks || b >= nb - local_blocks;
       take[b] = (unsigned char)fixed;
-      if (!fixed) {
-        cand[ncand].key = order_key(scores[(size_t)r * score_stride + b]);
+      if (!fixed) {  /* scores are read only when some are chosen by them */
+        cand[ncand].key = top_k > 0 ? order_key(scores[(size_t)r * score_stride + b]) : 0u;
         cand[ncand].block = b;
         ++ncand;
       }

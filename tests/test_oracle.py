@@ -619,6 +619,14 @@ def test_sparse_select_matches_repeated_argmax(seed):
             assert sl[r] == tokens
 
 
+def test_sparse_select_without_scores_keeps_only_fixed_blocks():
+    lens = np.array([0, 10, 100, 1000], np.int32)
+    bt = np.arange(4 * 70, dtype=np.int32).reshape(4, 70)
+    sel, sl = oracle.sparse_select(None, lens, bt, 16, 0, 2, 1)
+    assert sel.tolist() == [[-1, -1, -1], [70, -1, -1], [140, 141, 146], [210, 211, 272]]
+    assert sl.tolist() == [0, 10, 16 + 16 + 4, 16 + 16 + 8]
+
+
 def _sparse_case(kv="bf16", seed=0):
     return wl.make_batch("sparse", [1, 40, 300, 777, 1500], None, 8, 2, 64, 16, kv, seed=seed,
                          kv_scale=0.05)
