@@ -257,6 +257,32 @@ def _replay_ms(g, dev) -> float:
     return t0.elapsed_time(t1)
 
 
+def _step_fns(w, kind, out):
+    """(plan, refresh, decode) for a Workload, or for a SparseWorkload: there the
+    refresh is the block selection followed by the plan refresh from the
+    selected lengths, and the decode runs over the sparse block table."""
+    if isinstance(w, wl.SparseWorkload):
+        sw, b = w, w.base
+        plan = binding.Plan(b.num_seqs, b.num_q_heads, b.num_kv_heads, b.head_dim,
+                            max_partitions=sw.max_partitions, budget=b.budget or 0, kind=kind,
+                            device=b.q.device)
+        sel = torch.empty((b.num_seqs, sw.sel_stride), dtype=torch.int32, device=b.q.device)
+        sl = torch.empty(b.num_seqs, dtype=torch.int32, device=b.q.device)
+
+        def refresh():
+            binding.sparse_select(sw.scores, b.context_lens, b.block_tables, b.block_size,
+                                  sw.top_k, sw.init_blocks, sw.local_blocks, sel, sl)
+            plan.refresh(sl)
+
+        def decode():
+            plan.decode(b.q, b.k_cache, b.v_cache, sel, sl, None, b.scale, b.k_scale, b.v_scale,
+                        out=out)
+        return plan, refresh, decode
+    plan = binding.plan_for(w, kind)
+    return (plan, lambda: plan.refresh(w.context_lens, w.cu_query_lens),
+            lambda: binding.decode_workload(plan, w, out=out))
+
+
 def time_native(w, steps: int, warmup: int, kind=binding.PROPORTIONAL, flush: bool = False,
                 sampler: ClockSampler | None = None, world: int = 1):
     """Graph-replayed timing of K steps, as a serving engine replays its decode
@@ -273,10 +299,13 @@ def time_native(w, steps: int, warmup: int, kind=binding.PROPORTIONAL, flush: bo
     median (an event pair between kernels costs the launch overlap, so this
     errs long).
 
+    A SparseWorkload's step is selection + refresh + decode over the selection.
+
     Returns dict(step_ms, call_ms, split_ms, split_all) and the plan."""
-    dev = w.q.device
-    plan = binding.plan_for(w, kind)
-    out = torch.empty_like(w.q)
+    q = w.base.q if isinstance(w, wl.SparseWorkload) else w.q
+    dev = q.device
+    out = torch.empty_like(q)
+    plan, refresh_fn, decode_fn = _step_fns(w, kind, out)
     fa = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
     fb = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
     sink = torch.empty(steps, dtype=torch.float32, device=dev) if flush else None
@@ -296,14 +325,14 @@ def time_native(w, steps: int, warmup: int, kind=binding.PROPORTIONAL, flush: bo
             if events:
                 plan.set_split_events(*splits[i])
             if refresh:
-                plan.refresh(w.context_lens, w.cu_query_lens)
-            binding.decode_workload(plan, w, out=out)
+                refresh_fn()
+            decode_fn()
         plan.set_split_events(None, None)
 
     cur = torch.cuda.current_stream(dev)
     for _ in range(max(warmup, 3)):
-        plan.refresh(w.context_lens, w.cu_query_lens)
-        binding.decode_workload(plan, w, out=out)
+        refresh_fn()
+        decode_fn()
     for a, b in splits:  # materialise the CUDA events before handing them to the ABI
         a.record(cur)
         b.record(cur)
@@ -338,13 +367,15 @@ def time_native(w, steps: int, warmup: int, kind=binding.PROPORTIONAL, flush: bo
 
 
 def time_refresh(w, reps: int = 100) -> float:
-    """µs per plan refresh: a graph of `reps` refreshes, replayed."""
-    plan = binding.plan_for(w)
-    plan.refresh(w.context_lens, w.cu_query_lens)
+    """µs per plan refresh (for a SparseWorkload: selection + refresh): a graph
+    of `reps` of them, replayed."""
+    q = w.base.q if isinstance(w, wl.SparseWorkload) else w.q
+    plan, refresh_fn, _ = _step_fns(w, binding.PROPORTIONAL, None)
+    refresh_fn()
     torch.cuda.synchronize()
-    g = _graph(lambda: [plan.refresh(w.context_lens, w.cu_query_lens) for _ in range(reps)])
+    g = _graph(lambda: [refresh_fn() for _ in range(reps)])
     g.replay()
-    ms = _replay_ms(g, w.q.device)
+    ms = _replay_ms(g, q.device)
     del g
     return ms * 1e3 / reps
 
@@ -473,17 +504,20 @@ def sweep(args):
     plan on the same kernel, L2 flushed before every step, graph-replayed;
     then a summary line over the skewed seeds (median, p90)."""
     dev = torch.device("cuda", torch.cuda.current_device())
-    names = list(wl.CONFIGS) if args.sweep == "all" else args.sweep.split(",")
+    names = (list(wl.CONFIGS) + list(wl.SPARSE_CONFIGS) if args.sweep == "all"
+             else args.sweep.split(","))
     peak = measured_peaks().get("hbm_gbs", 6800.0)
     skew = []
     for name in names:
         seeds = range(args.seeds) if name == "skewed" else [0]
         for seed in seeds:
-            w = wl.CONFIGS[name](seed, dev)
+            w = (wl.SPARSE_CONFIGS[name] if name in wl.SPARSE_CONFIGS else wl.CONFIGS[name])(
+                seed, dev)
             kv = w.kv_bytes()
+            lens = (w.selected_tokens() if isinstance(w, wl.SparseWorkload)
+                    else w.context_lens).tolist()
             res = {"sweep": name, "seed": seed, "kv_bytes": kv,
-                   "max_over_min": round(max(w.context_lens.tolist()) /
-                                         max(1, min(w.context_lens.tolist())), 1)}
+                   "max_over_min": round(max(lens) / max(1, min(lens)), 1)}
             for kind, tag in ((binding.PROPORTIONAL, "proportional"),
                               (binding.UNIFORM, "uniform")):
                 t, plan = time_native(w, args.steps, args.warmup, kind=kind, flush=True)

@@ -198,6 +198,41 @@ int pa_decode_ex(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int 
                  const int32_t* context_lens, const int32_t* cu_query_lens, int num_seqs,
                  float scale, const float* sinks, int k_layout, void* out, void* stream);
 
+/* Sparse top-k block selection, for the sparse decode of [ATOM-2366] section 3
+ * (the sparse call sites read a fixed top-k window) and [ATOM-2514] Design
+ * ("Once-per-step sparse refresh": the local tail block is always selected, so
+ * a request's selected length depends on its context length only; "Partition
+ * ceiling": sparse plans keep a ceiling of 8) and Known Limitations item 2
+ * (top-k, init-block and local-block settings).  The indexer that scores blocks
+ * is not described; its scores are an input.
+ *
+ * For request r with S = context_lens[r] tokens and nb = ceil(S / block_size)
+ * logical blocks (at most max_blocks_per_seq; a longer request raises
+ * PA_DEVERR_BAD_PAGE in *device_errors and only its first max_blocks_per_seq
+ * blocks exist): the first init_blocks and the last local_blocks blocks are
+ * always selected; of the blocks between them, the top_k with the highest
+ * block_scores[r * score_stride + b], scores ordered as their fp32 bit
+ * patterns (-NaN < -inf < ... < -0 < +0 < ... < +inf < +NaN) and equal scores
+ * by the lower block index.  Row r of sel_block_tables [num_seqs][sel_stride]
+ * receives block_tables[r][b] of the selected blocks b in ascending order, then
+ * -1; sel_context_lens[r] the tokens they hold (the tail block counts
+ * S - (nb - 1) * block_size).  A pa_decode with sel_block_tables
+ * (max_blocks_per_seq = sel_stride) and sel_context_lens is then the sparse
+ * decode: each request's token attends to the keys of its selected blocks.
+ *
+ * block_scores: device fp32, rows of score_stride >= max_blocks_per_seq
+ * entries; may be NULL when top_k == 0.  Requires sel_stride >= init_blocks +
+ * top_k + local_blocks, all counts >= 0, 1 <= num_seqs <= 4096.
+ * device_errors: optional device uint32 (NULL: none).  One kernel on `stream`
+ * on the current device; no allocation, no host synchronisation, so it may be
+ * captured in a CUDA graph.  PA_ERR_INVALID_ARG / PA_ERR_UNSUPPORTED on bad
+ * arguments, PA_ERR_CUDA if the launch fails. */
+int pa_sparse_select(const float* block_scores, int score_stride, const int32_t* context_lens,
+                     const int32_t* block_tables, int max_blocks_per_seq, int num_seqs,
+                     int block_size, int top_k, int init_blocks, int local_blocks,
+                     int32_t* sel_block_tables, int sel_stride, int32_t* sel_context_lens,
+                     uint32_t* device_errors, void* stream);
+
 /* Size of the file-scope device array that pa_decode_static works in. */
 #define PA_STATIC_SCRATCH_BYTES (32u << 20)
 

@@ -16,7 +16,7 @@ OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libpa.so")
 HEADER = os.path.join(ROOT, "include", "pa.h")
 
-SOURCES = ["pa_api.cu", "pa_plan.cu", "pa_merge.cu", "pa_static.cu",
+SOURCES = ["pa_api.cu", "pa_plan.cu", "pa_merge.cu", "pa_static.cu", "pa_sparse.cu",
            "pa_split_d64.cu", "pa_split_d128.cu", "pa_split_d256.cu",
            "pa_split_d64_gk.cu", "pa_split_d128_gk.cu", "pa_split_d256_gk.cu",
            "pa_split_d384.cu", "pa_split_d512.cu", "pa_split_d640.cu", "pa_split_d768.cu",

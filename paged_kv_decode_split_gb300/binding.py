@@ -72,12 +72,13 @@ def load() -> ctypes.CDLL:
     lib.pa_plan_set_split_events.argtypes = [P, P, P]
     lib.pa_plan_set_call_events.argtypes = [P, P, P]
     lib.pa_plan_destroy.argtypes = [P]
+    lib.pa_sparse_select.argtypes = [P, i32, P, P, i32, i32, i32, i32, i32, i32, P, i32, P, P, P]
     lib.pa_status_string.argtypes = [i32]
     lib.pa_status_string.restype = ctypes.c_char_p
     for name in ("pa_plan_build", "pa_plan_refresh", "pa_decode", "pa_decode_ex",
                  "pa_plan_set_window", "pa_plan_info",
                  "pa_plan_download", "pa_plan_read_errors", "pa_plan_set_split_events",
-                 "pa_plan_set_call_events",
+                 "pa_plan_set_call_events", "pa_sparse_select",
                  "pa_plan_destroy"):
         getattr(lib, name).restype = i32
     _lib = lib
@@ -286,3 +287,42 @@ def decode_workload(plan: Plan, w, out=None, stream=None, sinks=None) -> torch.T
     return plan.decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
                        w.cu_query_lens, w.scale, w.k_scale, w.v_scale, out=out, stream=stream,
                        sinks=sinks)
+
+
+def sparse_select(block_scores: Optional[torch.Tensor], context_lens: torch.Tensor,
+                  block_tables: torch.Tensor, block_size: int, top_k: int, init_blocks: int,
+                  local_blocks: int, sel_block_tables: Optional[torch.Tensor] = None,
+                  sel_context_lens: Optional[torch.Tensor] = None,
+                  device_errors: Optional[torch.Tensor] = None, stream=None):
+    """pa_sparse_select: the sparse block table [n, init + top_k + local] (or the
+    width of sel_block_tables when given) and the selected lengths [n], both
+    int32 on the device of context_lens."""
+    dev = context_lens.device
+    _need(context_lens, "context_lens", dev, (torch.int32,))
+    _need(block_tables, "block_tables", dev, (torch.int32,))
+    if block_tables.dim() != 2 or block_tables.shape[0] != context_lens.shape[0]:
+        raise ValueError("block_tables must be [num_seqs, max_blocks]")
+    n, max_blocks = block_tables.shape
+    stride = 0
+    if block_scores is not None:
+        _need(block_scores, "block_scores", dev, (torch.float32,))
+        if block_scores.dim() != 2 or block_scores.shape[0] != n:
+            raise ValueError("block_scores must be [num_seqs, >= max_blocks]")
+        stride = block_scores.shape[1]
+    if sel_block_tables is None:
+        sel_block_tables = torch.empty((n, init_blocks + top_k + local_blocks), dtype=torch.int32,
+                                       device=dev)
+    _need(sel_block_tables, "sel_block_tables", dev, (torch.int32,))
+    if sel_context_lens is None:
+        sel_context_lens = torch.empty(n, dtype=torch.int32, device=dev)
+    _need(sel_context_lens, "sel_context_lens", dev, (torch.int32,))
+    if device_errors is not None:
+        _need(device_errors, "device_errors", dev, (torch.int32,))
+    with torch.cuda.device(dev):
+        _check(load().pa_sparse_select(_ptr(block_scores), stride, _ptr(context_lens),
+                                       _ptr(block_tables), max_blocks, n, int(block_size),
+                                       int(top_k), int(init_blocks), int(local_blocks),
+                                       _ptr(sel_block_tables), sel_block_tables.shape[1],
+                                       _ptr(sel_context_lens), _ptr(device_errors),
+                                       _stream(dev, stream)), "pa_sparse_select")
+    return sel_block_tables, sel_context_lens

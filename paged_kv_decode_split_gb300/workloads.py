@@ -293,6 +293,66 @@ CONFIGS["uniform_d1024"] = uniform_d1024
 CONFIGS["skewed_d1024"] = skewed_d1024
 
 
+@dataclass
+class SparseWorkload:
+    """A decode batch whose requests attend to a top-k selection of their KV
+    blocks: `base` is the batch (caches, block tables, context lengths, one
+    query token per request), `scores` the per-block indexer scores [n,
+    max_blocks] fp32; the selection keeps the first `init_blocks`, the last
+    `local_blocks` and the `top_k` best-scored blocks between them."""
+    name: str
+    base: Workload
+    scores: torch.Tensor
+    top_k: int
+    init_blocks: int
+    local_blocks: int
+    max_partitions: int = 8             # the sparse partition ceiling
+
+    @property
+    def sel_stride(self) -> int:
+        return self.init_blocks + self.top_k + self.local_blocks
+
+    def selected_tokens(self) -> torch.Tensor:
+        """Tokens each request's selection holds, from the lengths alone (the
+        count of selected blocks is fixed; with local_blocks >= 1 the tail
+        block is one of them)."""
+        assert self.local_blocks >= 1
+        bs = self.base.block_size
+        S = self.base.context_lens.clamp(min=0).to(torch.int64).cpu()
+        nb = (S + bs - 1) // bs
+        lo = torch.clamp(nb, max=self.init_blocks)
+        hi = torch.maximum(lo, nb - self.local_blocks)
+        count = lo + (nb - hi) + torch.clamp(hi - lo, max=self.top_k)
+        return torch.where(nb > 0, count * bs - (nb * bs - S), torch.zeros_like(S))
+
+    def kv_bytes(self) -> int:
+        w = self.base
+        return int(self.selected_tokens().sum()) * w.num_kv_heads * w.head_dim * 2 * \
+            w.kv_elem_bytes
+
+    def to(self, device) -> "SparseWorkload":
+        return SparseWorkload(self.name, self.base.to(device), self.scores.to(device), self.top_k,
+                              self.init_blocks, self.local_blocks, self.max_partitions)
+
+
+def sparse(seed: int = 0, device="cpu") -> SparseWorkload:
+    """Sparse top-k decode: 32 decodes, context lognormal(median 4096, sigma 1.5)
+    clipped to [64, 131072], Hq/Hkv 32/4, D 128, page 64, fp8 e4m3fn KV (scale
+    0.05), bf16 q; per-block scores N(0, 1); the first block, the last block and
+    the top 32 blocks between them (at most 34 blocks = 2176 tokens per
+    request); partition ceiling 8, budget 2 x 148."""
+    lens = lognormal_lengths(32, 4096, 1.5, 64, 131072, seed)
+    w = make_batch("sparse", lens, None, 32, 4, 128, 64, "fp8", seed=seed, kv_scale=0.05,
+                   device=device, budget=296, max_partitions=8)
+    g = _gen(seed + 104729, device)
+    scores = torch.randn(tuple(w.block_tables.shape), generator=g, device=device,
+                         dtype=torch.float32)
+    return SparseWorkload("sparse", w, scores, 32, 1, 1)
+
+
+SPARSE_CONFIGS = {"sparse": sparse}
+
+
 def subset(w: Workload, requests: Sequence[int]) -> Workload:
     """The sub-batch of the given requests, with their pages copied into a compact
     pool (same bytes, same page order inside each request).  Every output row of a

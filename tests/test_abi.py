@@ -61,6 +61,28 @@ def test_plan_build_rejects_bad_parameters_before_cuda(lib, kw, want):
     assert _build_status(lib, **kw) == want
 
 
+def test_sparse_select_rejects_bad_arguments_before_cuda(lib):
+    """Validation returns before any launch, so these need no GPU."""
+    assert lib.pa_sparse_select(None, 0, None, None, 4, 2, 16, 0, 1, 1, None, 2, None, None,
+                                None) == binding.PA_ERR_INVALID_ARG
+    p = ctypes.c_void_p(16)  # never dereferenced: every call below fails validation
+    # top_k > 0 without scores
+    assert lib.pa_sparse_select(None, 4, p, p, 4, 2, 16, 2, 1, 1, p, 4, p, None,
+                                None) == binding.PA_ERR_INVALID_ARG
+    # rows narrower than init + top_k + local
+    assert lib.pa_sparse_select(p, 4, p, p, 4, 2, 16, 2, 1, 1, p, 3, p, None,
+                                None) == binding.PA_ERR_INVALID_ARG
+    # score rows shorter than the block table
+    assert lib.pa_sparse_select(p, 3, p, p, 4, 2, 16, 2, 1, 1, p, 4, p, None,
+                                None) == binding.PA_ERR_INVALID_ARG
+    # negative counts
+    assert lib.pa_sparse_select(p, 4, p, p, 4, 2, 16, -1, 1, 1, p, 4, p, None,
+                                None) == binding.PA_ERR_INVALID_ARG
+    # more requests than the planner's domain
+    assert lib.pa_sparse_select(p, 4, p, p, 4, 4097, 16, 2, 1, 1, p, 4, p, None,
+                                None) == binding.PA_ERR_UNSUPPORTED
+
+
 def test_null_handles(lib):
     assert lib.pa_plan_build(None, 0, 4, 8, 2, 64, 1, 4, 0, 0, 0) == binding.PA_ERR_INVALID_ARG
     assert lib.pa_plan_refresh(None, None, None, None) == binding.PA_ERR_INVALID_ARG
