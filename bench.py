@@ -430,6 +430,10 @@ def run_native(args, world, rank, local):
     torch.cuda.set_device(dev)
     import __graft_entry__
     __graft_entry__.build()
+    if args.sweep_only:
+        if rank == 0:
+            sweep(args)
+        return
     w = wl.CONFIGS[args.workload](0, dev)
     kv_bytes = w.kv_bytes()
     sampler = ClockSampler(dev) if rank == 0 else None
@@ -598,6 +602,8 @@ def main(argv=None):
     ap.add_argument("--workload", choices=list(wl.CONFIGS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--sweep", default="", help="'all' or comma list: extra per-config lines")
     ap.add_argument("--seeds", type=int, default=20, help="skewed seeds in the sweep")
+    ap.add_argument("--sweep-only", action="store_true",
+                    help="print the --sweep lines only (no headline line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     world, rank, local = dist_setup()

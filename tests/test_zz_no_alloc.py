@@ -106,3 +106,15 @@ def test_too_large_a_batch_is_rejected(lib):
     out = torch.zeros_like(w.q)
     assert static_decode(lib, w, out, max_query_len=100) == binding.PA_ERR_UNSUPPORTED
     assert torch.all(out == 0)
+
+
+@pytest.mark.parametrize("D,kv", [(512, "bf16"), (1024, "fp8")])
+def test_wide_heads_match_the_planned_path(lib, D, kv):
+    dev = torch.device("cuda", 0)
+    w = wl.make_batch("no_alloc_wide", [3000, 17, 900, 5000], None, 16, 2, D, 16, kv, seed=6,
+                      kv_scale=0.05, device=dev)
+    ref = planned_decode(w)
+    out = torch.full_like(w.q, float("nan"))
+    assert static_decode(lib, w, out) == binding.PA_OK
+    torch.cuda.synchronize()
+    assert _max_diff(out, ref) <= TOL[kv]
