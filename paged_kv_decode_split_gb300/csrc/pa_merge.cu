@@ -42,13 +42,31 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
   __shared__ float s_ws[NU];
   const float NEG_INF = -__int_as_float(0x7f800000);
   pdl_trigger();
-  pdl_wait();  // the split kernel's partials are complete
-  // The split kernel is done with its work counter: reset it for the next decode.
-  if (blockIdx.x == 0 && threadIdx.x == 0) p.plan.counters[1] = 0;
+  // What the planner wrote (the row lists and their counts) and the lengths
+  // were complete before the split kernel started, so they are read before
+  // waiting for the split kernel's partials.
   const int tid = threadIdx.x, u = tid / UL, ul = tid % UL;
   const int Hq = p.Hq;
   const int nfew = p.plan.counters[3];  // rows listed first: at most kWarpMergePieces pieces
   const int total = p.plan.counters[2] * Hq;
+  const int warp = tid >> 5, lane = tid & 31;
+  constexpr int kWarps = kMergeThreads / 32;
+  // the first (row, head) pair of this warp's few-piece loop, fetched ahead
+  const int wp0 = blockIdx.x * kWarps + warp;
+  int4 e0 = make_int4(0, 0, 0, 0);
+  int2 snap0 = make_int2(0, 0);
+  int ctx0 = 0, c00 = 0, L0 = 0;
+  if (wp0 < nfew * Hq) {
+    e0 = p.plan.mrows[wp0 / Hq];
+    const int r0 = e0.x & 4095;
+    snap0 = p.plan.snap[r0];
+    ctx0 = p.context_lens[r0];
+    c00 = p.cu ? p.cu[r0] : r0;
+    L0 = p.cu ? p.cu[r0 + 1] - c00 : 1;
+  }
+  pdl_wait();  // the split kernel's partials are complete
+  // The split kernel is done with its work counter: reset it for the next decode.
+  if (blockIdx.x == 0 && threadIdx.x == 0) p.plan.counters[1] = 0;
 
   // Rows with many pieces: one CTA per (row, q head) pair.
   for (int pair = blockIdx.x; pair < total; pair += gridDim.x) {
@@ -157,16 +175,15 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
   // loaded PB at a time (all at once up to head_dim 256), weights from shuffles.
   constexpr int VL = D / 32;  // outputs per lane
   constexpr int PB = VL <= 8 ? kWarpMergePieces : 2;
-  const int warp = tid >> 5, lane = tid & 31;
-  constexpr int kWarps = kMergeThreads / 32;
-  for (int wp = blockIdx.x * kWarps + warp; wp < nfew * Hq; wp += gridDim.x * kWarps) {
-    const int4 e = p.plan.mrows[wp / Hq];
+  for (int wp = wp0; wp < nfew * Hq; wp += gridDim.x * kWarps) {
+    const bool first = wp == wp0;
+    const int4 e = first ? e0 : p.plan.mrows[wp / Hq];
     const int r = e.x & 4095, parts = (e.x >> 12) + 1, tok = e.y, L = e.w;
     const int hq = wp % Hq;
-    const int2 snap = p.plan.snap[r];
-    const int ctx = p.context_lens[r];
-    const int c0 = p.cu ? p.cu[r] : r;
-    const int Lnow = p.cu ? p.cu[r + 1] - c0 : 1;
+    const int2 snap = first ? snap0 : p.plan.snap[r];
+    const int ctx = first ? ctx0 : p.context_lens[r];
+    const int c0 = first ? c00 : (p.cu ? p.cu[r] : r);
+    const int Lnow = first ? L0 : (p.cu ? p.cu[r + 1] - c0 : 1);
     float lse = NEG_INF;
     if (lane < parts) lse = __ldcg(p.plan.part_lse + static_cast<long long>(e.z + lane * L) * Hq + hq);
     float M = lse;
