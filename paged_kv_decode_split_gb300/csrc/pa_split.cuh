@@ -74,7 +74,15 @@ struct SplitCfg {
   static constexpr int ND = D / DS;                   // dim slices
   static constexpr int CBS = DS * ESZ / SWB;          // column blocks per slice
   static constexpr int KS = kWide ? 16 : kStageTensorBytes / ROW;  // keys per stage
-  static constexpr int NS = 3;                        // ring depth
+  // partial-logit exchange of the dim slices: [stage parity][WQ][ND][32 lanes] float4
+  static constexpr int SX_BYTES = kWide ? 2 * WQ * ND * 32 * 16 : 0;
+  // Ring depth: 3 stages, or 2 where that lets two CTAs share an SM (wide
+  // heads of 640 and 768 dims: 3 stages of 40-48 KB need more than half of
+  // the SM's 228 KB of shared memory).
+  static constexpr int kFixedBytes = 1024 + 64 + SX_BYTES;
+  static constexpr bool kTwoPerSm3 = 2 * (3 * 2 * KS * ROW + kFixedBytes + 1024) <= 228 * 1024;
+  static constexpr bool kTwoPerSm2 = 2 * (2 * 2 * KS * ROW + kFixedBytes + 1024) <= 228 * 1024;
+  static constexpr int NS = (kWide && !kTwoPerSm3 && kTwoPerSm2) ? 2 : 3;  // ring depth
   static constexpr int MTS = KS / 16;                 // 16-key tiles per stage
   static constexpr int WK0 = (WQ == 1) ? 4 : (WQ == 4 ? 1 : 2);
   static constexpr int WK = WK0 < MTS ? WK0 : MTS;   // key warps per row group
@@ -90,9 +98,7 @@ struct SplitCfg {
   static constexpr int DATA_BYTES = NS * STAGE_BYTES;
   static constexpr int DP = D + 4;                    // padded exchange row, floats
   static constexpr int EX_BYTES = WQ * WK * 8 * (DP + 2) * 4;
-  // partial-logit exchange of the dim slices: [stage parity][WQ][ND][32 lanes] float4
-  static constexpr int SX_BYTES = kWide ? 2 * WQ * ND * 32 * 16 : 0;
-  static constexpr int SMEM_BYTES = DATA_BYTES + 1024 + 64 + SX_BYTES;
+  static constexpr int SMEM_BYTES = DATA_BYTES + kFixedBytes;
   // two CTAs per SM where the threads' registers and both rings fit (228 KB per SM)
   static constexpr int MIN_BLOCKS = (THREADS <= 224 && 2 * (SMEM_BYTES + 1024) <= 228 * 1024) ? 2 : 1;
   static_assert(!kWide || (WK == 1 && T == 1 && CBS * SWB == DS * ESZ && WQ <= 2),
