@@ -1,14 +1,17 @@
-// pa_split.cuh -- the split-KV paged decode kernel (one CTA per plan task and
-// kv head).
+// pa_split.cuh -- the split-KV paged decode kernel (one CTA per piece -- a plan
+// task, or a cut of one -- and kv head; further pieces and row chunks are
+// taken from a device counter by CTAs that finish early).
 //
 // What it computes ("[MiniMax-M3] Route the paged decode to aiter's FlyDSL
 // kernel with work planner", sections 1 and 3; vllm-rdna pull 29, Change 1):
 // task (r, tile_begin, tile_end, S) of the plan covers keys
 // [tile_begin*256, min(tile_end*256, S)) of request r.  For every query row of
 // r (token i of L, q head of kv head h) the CTA forms the partial softmax over
-// the task's keys that the row may see (key < S - (L-1-i)), and writes either
-// the finished output row (when r has a single partition) or a normalised
-// fp32 partial plus its log2-sum-exp for the merge kernel.
+// the task's keys that the row may see (key < S - (L-1-i), and within the
+// row's sliding window if there is one), and writes either the finished
+// output row (when r has a single piece; an attention sink joins its
+// denominator there) or a normalised fp32 partial plus its log2-sum-exp for
+// the merge kernel.
 //
 // GB300 mapping:
 //  * warp 0 is the producer: it walks the block table (32-entry windows,
@@ -19,7 +22,8 @@
 //    keys, also 128-byte swizzled) of the K and V rows of a stage's pages
 //    from up to 32 lanes at once -- with pages of only 2-4 KB per head, one
 //    issuing lane caps the stream at roughly half the HBM bandwidth -- into a
-//    ring of NS 32 KB stages, completion counted in bytes on an mbarrier;
+//    ring of NS stages (32 KB up to head_dim 256; one 16-key tile of K and V
+//    for wider heads), completion counted in bytes on an mbarrier;
 //  * consumer warps form (row group wq) x (key warp wk); every consumer warp
 //    takes part in every stage (its key slice: T 16-key tiles handled
 //    together -- independent MMA chains, one softmax reduction), so each warp
@@ -40,6 +44,9 @@
 //    into the epilogue;
 //  * the key warps of a row group are merged through shared memory at the end
 //    of a pass;
+//  * head dims above 256 are cut into 128- or 256-dim slices, one consumer
+//    warp each, whose partial logits are summed through shared memory per
+//    stage (see SplitCfg);
 //  * a few extra CTAs at the end of the grid write the rows no task writes
 //    (graph padding, empty or stale requests); requests with several
 //    partitions are combined afterwards by the merge kernel.
