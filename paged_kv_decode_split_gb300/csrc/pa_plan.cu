@@ -57,17 +57,22 @@ __device__ void block_scan(int (&v)[K], int (*sw)[kThreads / 32], int* tot) {
     for (int c = 0; c < K; ++c) sw[c][warp] = v[c];
   }
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 0) {  // the K counters' warp totals, scanned together
+    int w[K];
+#pragma unroll
+    for (int c = 0; c < K; ++c) w[c] = lane < kWarps ? sw[c][lane] : 0;
+#pragma unroll
+    for (int o = 1; o < kWarps; o <<= 1) {
+#pragma unroll
+      for (int c = 0; c < K; ++c) {
+        const int x = __shfl_up_sync(0xffffffffu, w[c], o);
+        if (lane >= o) w[c] += x;
+      }
+    }
 #pragma unroll
     for (int c = 0; c < K; ++c) {
-      int w = lane < kWarps ? sw[c][lane] : 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int x = __shfl_up_sync(0xffffffffu, w, o);
-        if (lane >= o) w += x;
-      }
-      if (lane < kWarps) sw[c][lane] = w;
-      if (lane == kWarps - 1) tot[c] = w;
+      if (lane < kWarps) sw[c][lane] = w[c];
+      if (lane == kWarps - 1) tot[c] = w[c];
     }
   }
   __syncthreads();
