@@ -340,8 +340,13 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
   }
   __syncthreads();
 
-  // Lanes of a warp that share a class add their count with one atomic; every
-  // lane calls this (invalid ones with valid = false).
+  // Phase 4 only counts the pieces of each class (plain atomics).  Phase 5
+  // places them: lanes of a warp that share a class add their count with one
+  // atomic and take consecutive places in lane order, so the launch order is
+  // the same on every refresh (within a class: slot order, warp by warp).
+  auto count_class = [&](int cls, bool valid) {
+    if (valid) atomicAdd(&s_bcnt[cls], 1);
+  };
   auto warp_claim = [&](int cls, bool valid) {
     const unsigned peers = __match_any_sync(0xffffffffu, valid ? cls : -1);
     const int leader = __ffs(peers) - 1;
@@ -407,7 +412,7 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
       const bool valid = act && sub < o.q;
       int kb = 0, ke = 1, cls = 0;
       if (valid) cls = piece_keys(o, sub, kb, ke);
-      warp_claim(cls, valid);
+      count_class(cls, valid);
     }
   }
   __syncthreads();
