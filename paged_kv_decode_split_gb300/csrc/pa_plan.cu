@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
   const int n = p.n;
   const int per = (n + kThreads - 1) / kThreads;  // requests per thread, <= kPer
   if (tid == 0) s_bad = 0;
-  if (tid < 128) s_bcnt[tid] = 0;
+  for (int i = tid; i < 128; i += kThreads) s_bcnt[i] = 0;
   __syncthreads();
 
   // ---- 1. lengths, activity, validity; the planned range of each request
