@@ -24,9 +24,10 @@
 // (four 8-bit digits, shared-memory histograms).  A final pass in block order
 // takes every fixed block, every candidate above T and the first `need`
 // candidates equal to T; a block's place in the row is (fixed and larger
-// blocks before it) + min(equal blocks before it, need), so one block-wide
-// prefix sum of a packed pair of counts per 256 blocks places them all and the
-// row comes out sorted.  No sort, no global scratch, no host synchronisation.
+// blocks before it) + min(equal blocks before it, need), counted with warp
+// ballots over each warp's run of blocks and one barrier for the warp totals,
+// so the row comes out sorted.  No sort, no global scratch, no host
+// synchronisation.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -65,37 +66,9 @@ __device__ __forceinline__ uint32_t order_key(uint32_t u) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Exclusive prefix sum of v over the CTA's threads (in thread order); the sum
-// of all of them goes to `total`.  Every thread must call it.
-__device__ int block_exclusive_sum(int v, int* sh, int& total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) sh[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int t = lane < kSelWarps ? sh[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < kSelWarps; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, t, o);
-      if (lane >= o) t += y;
-    }
-    if (lane < kSelWarps) sh[lane] = t;
-  }
-  __syncthreads();
-  const int before = (warp > 0 ? sh[warp - 1] : 0) + x - v;
-  total = sh[kSelWarps - 1];
-  __syncthreads();  // sh is reused by the next call
-  return before;
-}
-
 __global__ void __launch_bounds__(kSelThreads) sparse_select_kernel(const SelectParams p) {
   __shared__ int s_hist[256];
-  __shared__ int s_scan[kSelWarps];
+  __shared__ int s_wbig[kSelWarps], s_weq[kSelWarps];
   __shared__ uint32_t s_prefix;
   __shared__ int s_remaining;
   __shared__ int s_tail;
@@ -182,35 +155,68 @@ __global__ void __launch_bounds__(kSelThreads) sparse_select_kernel(const Select
   }
 
   // ---- take and compact, in block order.  Per block: big = fixed, or a
-  // candidate taken whole or above T; eq = a candidate equal to T.  Packed as
-  // big << 16 | eq, one prefix sum per 256 blocks gives both counts before it.
+  // candidate taken whole or above T; eq = a candidate equal to T.  A block is
+  // taken if big, or eq and fewer than `need` eq blocks precede it; its place
+  // in the row is (big blocks before it) + min(eq blocks before it, need).
+  // Warp w owns a contiguous run of 32-block chunks: a first pass counts its
+  // big and eq blocks (ballots), one barrier publishes the warp totals, and a
+  // second pass places the blocks from the totals of the warps before it.
   int32_t* row = p.sel_tables + static_cast<long long>(r) * p.sel_stride;
   const int32_t* bt = p.block_tables + static_cast<long long>(r) * p.max_blocks;
-  if (threadIdx.x == 0) s_tail = 0;
-  int big_seen = 0, eq_seen = 0;
-  for (int c0 = 0; c0 < nb; c0 += kSelThreads) {
-    const int b = c0 + threadIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned lt = (1u << lane) - 1u;  // lanes below this one
+  const int chunks = (nb + 31) / 32;
+  const int cpw = (chunks + kSelWarps - 1) / kSelWarps;  // chunks per warp
+  const int c_lo = min(chunks, warp * cpw), c_hi = min(chunks, c_lo + cpw);
+  auto flags = [&](int b, bool& big, bool& eq) {
     const bool in = b < nb;
     const bool cand = in && b >= lo && b < hi;
-    int big = (in && (!cand || k == ncand)) ? 1 : 0;
-    int eq = 0;
+    big = in && (!cand || k == ncand);
+    eq = false;
     if (partial && cand) {
       const uint32_t key = key_at(b);
-      big = key > T ? 1 : 0;
-      eq = key == T ? 1 : 0;
+      big = key > T;
+      eq = key == T;
     }
-    int both;
-    const int before = block_exclusive_sum((big << 16) | eq, s_scan, both);
-    const int eq_before = eq_seen + (before & 0xFFFF);
-    const int big_before = big_seen + (before >> 16);
+  };
+  int my_big = 0, my_eq = 0;
+  for (int c = c_lo; c < c_hi; ++c) {
+    bool big, eq;
+    flags(c * 32 + lane, big, eq);
+    my_big += __popc(__ballot_sync(0xffffffffu, big));
+    my_eq += __popc(__ballot_sync(0xffffffffu, eq));
+  }
+  if (lane == 0) {
+    s_wbig[warp] = my_big;
+    s_weq[warp] = my_eq;
+  }
+  if (threadIdx.x == 0) s_tail = 0;
+  __syncthreads();
+  int big_base = 0, eq_base = 0, big_all = 0, eq_all = 0;
+#pragma unroll
+  for (int v = 0; v < kSelWarps; ++v) {
+    const int wb = s_wbig[v], we = s_weq[v];
+    if (v < warp) {
+      big_base += wb;
+      eq_base += we;
+    }
+    big_all += wb;
+    eq_all += we;
+  }
+  for (int c = c_lo; c < c_hi; ++c) {
+    const int b = c * 32 + lane;
+    bool big, eq;
+    flags(b, big, eq);
+    const unsigned bb = __ballot_sync(0xffffffffu, big), be = __ballot_sync(0xffffffffu, eq);
+    const int eq_before = eq_base + __popc(be & lt);
     if (big || (eq && eq_before < need)) {
-      row[big_before + min(eq_before, need)] = __ldg(bt + b);
+      row[big_base + __popc(bb & lt) + min(eq_before, need)] = __ldg(bt + b);
       if (b == nb_all - 1) s_tail = 1;  // the request's last, possibly partial, block
     }
-    big_seen += both >> 16;
-    eq_seen += both & 0xFFFF;
+    big_base += __popc(bb);
+    eq_base += __popc(be);
   }
-  const int taken = big_seen + min(eq_seen, need);
+  const int taken = big_all + min(eq_all, need);
   for (int i = taken + threadIdx.x; i < p.sel_stride; i += kSelThreads) row[i] = -1;
   __syncthreads();
   if (threadIdx.x == 0) {
