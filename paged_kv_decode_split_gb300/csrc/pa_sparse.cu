@@ -67,10 +67,10 @@ __device__ __forceinline__ uint32_t order_key(uint32_t u) {
 }
 
 __global__ void __launch_bounds__(kSelThreads) sparse_select_kernel(const SelectParams p) {
-  __shared__ int s_hist[256];
+  __shared__ int s_hist[2][256];  // digit histograms, alternating by pass
   __shared__ int s_wbig[kSelWarps], s_weq[kSelWarps];
-  __shared__ uint32_t s_prefix;
-  __shared__ int s_remaining;
+  __shared__ uint32_t s_prefix[2];  // alternating by pass
+  __shared__ int s_remaining[2];
   __shared__ int s_tail;
   extern __shared__ uint32_t s_keys[];  // min(max_blocks, kSelSmemKeys) entries
   pdl_trigger();  // the planner may be scheduled; it waits for these lengths
@@ -91,10 +91,10 @@ __global__ void __launch_bounds__(kSelThreads) sparse_select_kernel(const Select
                        static_cast<long long>(r) * p.score_stride;
   const bool cached = ncand <= kSelSmemKeys;
   auto key_at = [&](int b) { return cached ? s_keys[b - lo] : order_key(__ldg(sc + b)); };
-  if (partial && cached) {
+  if (partial && cached)
     for (int b = lo + threadIdx.x; b < hi; b += kSelThreads) s_keys[b - lo] = order_key(__ldg(sc + b));
-    // (the first histogram pass begins with a barrier)
-  }
+  for (int i = threadIdx.x; i < 256; i += kSelThreads) s_hist[0][i] = 0;
+  __syncthreads();  // the keys and the first histogram are ready
 
   // ---- radix select: T = the k-th largest candidate key, need = how many
   // candidates equal to T are taken (the k - need larger ones all are)
@@ -103,12 +103,14 @@ __global__ void __launch_bounds__(kSelThreads) sparse_select_kernel(const Select
   if (partial) {
     uint32_t prefix = 0u, mask = 0u;
     int remaining = k;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = threadIdx.x; i < 256; i += kSelThreads) s_hist[i] = 0;
-      __syncthreads();
+    for (int pass = 0, shift = 24; shift >= 0; ++pass, shift -= 8) {
+      // Histogram pass `pass` fills s_hist[pass & 1] (zeroed one pass ahead)
+      // and zeroes the other one, whose last readers finished a barrier ago.
+      int* hist = s_hist[pass & 1];
+      for (int i = threadIdx.x; i < 256; i += kSelThreads) s_hist[(pass + 1) & 1][i] = 0;
       for (int b = lo + threadIdx.x; b < hi; b += kSelThreads) {
         const uint32_t key = key_at(b);
-        if ((key & mask) == prefix) atomicAdd(&s_hist[(key >> shift) & 255u], 1);
+        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
       }
       __syncthreads();
       if (threadIdx.x < 32) {
@@ -118,7 +120,7 @@ __global__ void __launch_bounds__(kSelThreads) sparse_select_kernel(const Select
         int c[8], sum = 0;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          c[j] = s_hist[255 - 8 * lane - j];
+          c[j] = hist[255 - 8 * lane - j];
           sum += c[j];
         }
         int incl = sum;
@@ -140,15 +142,14 @@ __global__ void __launch_bounds__(kSelThreads) sparse_select_kernel(const Select
             }
             acc += c[j];
           }
-          s_prefix = prefix | (static_cast<uint32_t>(d) << shift);
-          s_remaining = remaining - acc;
+          s_prefix[pass & 1] = prefix | (static_cast<uint32_t>(d) << shift);
+          s_remaining[pass & 1] = remaining - acc;
         }
       }
-      __syncthreads();
-      prefix = s_prefix;
-      remaining = s_remaining;
+      __syncthreads();  // (the next pass writes the other s_prefix / s_remaining)
+      prefix = s_prefix[pass & 1];
+      remaining = s_remaining[pass & 1];
       mask |= 0xFFu << shift;
-      __syncthreads();  // s_prefix / s_remaining read before the next digit writes them
     }
     T = prefix;
     need = remaining;
