@@ -163,15 +163,14 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     fence_barrier_init();
   }
   pdl_wait();  // the plan (and everything before this kernel) is complete
-  // (The work counter this kernel takes items from is reset by the merge
-  // kernel, which runs after it.)
-  auto cta_exit = [&]() {
-    __syncthreads();
-    pdl_trigger();
-  };
+  // The merge kernel may be scheduled once every CTA of this grid has got
+  // here, i.e. once all of them are resident: its CTAs take what is left of
+  // the SMs, read the planner's row lists and then wait for this whole grid to
+  // complete before they read a partial or reset the work counter that this
+  // kernel takes items from.
+  pdl_trigger();
   if (blockIdx.x >= static_cast<unsigned>(p.C * p.Hkv)) {  // zero-row CTA
     zero_rows<D>(p, blockIdx.x - p.C * p.Hkv, warp, Cfg::THREADS / 32, lane);
-    cta_exit();
     return;
   }
   // This CTA's first item -- piece blockIdx / Hkv, head blockIdx % Hkv --
@@ -807,7 +806,6 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     for (int k = (issued > Cfg::NS ? issued - Cfg::NS : 0); k < issued; ++k)
       mbar_wait(bar_full + 8 * (k % Cfg::NS), (k / Cfg::NS) & 1, p.plan.err);
   }
-  cta_exit();
 }
 
 template <int D, int KVT, int WQ, int KL>
