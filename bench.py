@@ -59,11 +59,12 @@ DESCRIBE = {
     "skewed_k5": "skewed agentic decode with K in the grouped layout [nb, Hkv, D/16, 16, 16]",
     "uniform_d512": "uniform decode: 16 seqs x 8192 ctx, Hq/Hkv 32/4, D 512, page 16, bf16",
     "uniform_d1024": "uniform decode: 16 seqs x 8192 ctx, Hq/Hkv 32/4, D 1024, page 16, bf16",
+    "uniform_n64_h8": "uniform decode: 64 seqs x 4096 ctx, Hq/Hkv 64/8, D 128, page 16, bf16",
     "skewed_d1024": "skewed agentic decode: 32 seqs, ctx lognormal(4096, 1.5) in [64,131072], "
                     "Hq/Hkv 16/2, D 1024, page 16, fp8-e4m3 KV (scale 0.05), K grouped, "
                     "budget 296, cap 256",
 }
-SPLIT_SOURCES = ["pa_split.cuh", "pa_device.cuh"]
+SPLIT_SOURCES = ["pa_split.cuh", "pa_split_cfg.h", "pa_device.cuh"]
 L2_BYTES = 129 * 1024 * 1024
 
 

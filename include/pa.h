@@ -183,6 +183,18 @@ int pa_decode(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int num
  * the plan's last refresh.  PA_ERR_INVALID_ARG for W < 0. */
 int pa_plan_set_window(pa_plan* plan, int sliding_window);
 
+/* The element type of the caches the plan's pa_decode calls will read (a
+ * pa_dtype: PA_BF16 by default, PA_FP16 or PA_FP8_E4M3).  No counterpart in
+ * the pages: it tells the planner how many CTAs of the decode kernel one SM
+ * holds (an fp8 stage is half the size of a 16-bit one), so that when the
+ * plan's CTAs (capacity x num_kv_heads) are more than the GPU runs at once,
+ * the refresh cuts the tasks into pieces (at least two 256-key tiles, at most
+ * four per task) that the CTAs of the first wave share, instead of leaving a
+ * second, partly empty wave of whole tasks.  work_info and reduce_info do not
+ * change; a pa_decode over another cache type stays correct.  Takes effect at
+ * the next pa_plan_refresh.  PA_ERR_INVALID_ARG for another value. */
+int pa_plan_set_kv_dtype(pa_plan* plan, int kv_dtype);
+
 /* pa_decode with attention sinks and a choice of K layout.  sinks (named in
  * the same aiter signature) is NULL or a device array of num_q_heads fp32
  * logits, in the units of scale * q.k, each joining its head's softmax

@@ -28,6 +28,7 @@ PA_ERR_CUDA = -4
 PA_ERR_OOM = -5
 
 BF16, FP16, FP8_E4M3 = 0, 1, 2
+_DTYPES = {"bf16": BF16, "fp16": FP16, "fp8": FP8_E4M3}
 PROPORTIONAL, UNIFORM = 0, 1
 K_ROWS, K_GROUPED = 0, 1  # K cache layouts: [nb, Hkv, bs, D] / [nb, Hkv, D/16, bs, 16]
 
@@ -64,6 +65,7 @@ def load() -> ctypes.CDLL:
     lib.pa_decode_ex.argtypes = [P, P, i32, i32, i32, i32, P, P, i32, f32, f32, i32, i32, i32, P,
                                  i32, P, P, i32, f32, P, i32, P, P]
     lib.pa_plan_set_window.argtypes = [P, i32]
+    lib.pa_plan_set_kv_dtype.argtypes = [P, i32]
     lib.pa_plan_info.argtypes = [P, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                  ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32),
                                  ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_longlong)]
@@ -76,7 +78,7 @@ def load() -> ctypes.CDLL:
     lib.pa_status_string.argtypes = [i32]
     lib.pa_status_string.restype = ctypes.c_char_p
     for name in ("pa_plan_build", "pa_plan_refresh", "pa_decode", "pa_decode_ex",
-                 "pa_plan_set_window", "pa_plan_info",
+                 "pa_plan_set_window", "pa_plan_set_kv_dtype", "pa_plan_info",
                  "pa_plan_download", "pa_plan_read_errors", "pa_plan_set_split_events",
                  "pa_plan_set_call_events", "pa_sparse_select",
                  "pa_plan_destroy"):
@@ -255,6 +257,12 @@ class Plan:
         """Sliding window for the next refresh on (0: none)."""
         _check(load().pa_plan_set_window(self._h, int(sliding_window)), "pa_plan_set_window")
 
+    def set_kv_dtype(self, kv_dtype):
+        """Cache element type the decode calls will read ("bf16", "fp16",
+        "fp8" or a PA_* code), for the next refresh on."""
+        code = _DTYPES[kv_dtype] if isinstance(kv_dtype, str) else int(kv_dtype)
+        _check(load().pa_plan_set_kv_dtype(self._h, code), "pa_plan_set_kv_dtype")
+
     def close(self):
         h, self._h = getattr(self, "_h", None), None
         if h:
@@ -280,6 +288,7 @@ def plan_for(w, kind: int = PROPORTIONAL, budget: Optional[int] = None,
                 budget=(w.budget or 0) if budget is None else budget, kind=kind, device=device)
     if getattr(w, "window", 0):
         plan.set_window(w.window)
+    plan.set_kv_dtype(w.kv_dtype)
     return plan
 
 

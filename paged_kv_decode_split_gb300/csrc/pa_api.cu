@@ -14,6 +14,7 @@
 
 #include "../../include/pa.h"
 #include "pa_internal.h"
+#include "pa_split_cfg.h"
 
 namespace {
 
@@ -63,6 +64,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 struct pa_plan {
   int device, n, Hq, Hkv, D, max_qlen, max_tokens, P, W, kind, C, Q, rpc, sms;
+  int kv_dtype;  // the cache type the decode calls are expected to read
+  int wave;      // CTAs of that decode grid that run at once
   int window;          // sliding window for the next refresh (0: none)
   int window_planned;  // the window the last refresh planned with
   long long rows_cap, max_extra;
@@ -325,6 +328,8 @@ int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_q_heads, int
   pl->Q = lay.Q;
   pl->rpc = lay.rpc;
   pl->sms = sms;
+  pl->kv_dtype = PA_BF16;
+  pl->wave = pa::split_ctas_per_sm(head_dim, PA_BF16, lay.rpc / 8) * sms;
   pl->rows_cap = lay.rows_cap;
   pl->max_extra = lay.max_extra;
   pl->mem = mem;
@@ -357,6 +362,7 @@ int pa_plan_refresh(pa_plan* plan, const int32_t* context_lens, const int32_t* c
   p.max_tokens = plan->max_tokens;
   p.G = plan->Hq / plan->Hkv;
   p.rpc = plan->rpc;
+  p.wave = plan->wave;
   p.rows_cap = plan->rows_cap;
   p.max_extra = plan->max_extra;
   p.dev = plan->dev;
@@ -369,6 +375,14 @@ int pa_plan_refresh(pa_plan* plan, const int32_t* context_lens, const int32_t* c
 int pa_plan_set_window(pa_plan* plan, int sliding_window) {
   if (!plan || sliding_window < 0) return PA_ERR_INVALID_ARG;
   plan->window = sliding_window;
+  return PA_OK;
+}
+
+int pa_plan_set_kv_dtype(pa_plan* plan, int kv_dtype) {
+  if (!plan || (kv_dtype != PA_BF16 && kv_dtype != PA_FP16 && kv_dtype != PA_FP8_E4M3))
+    return PA_ERR_INVALID_ARG;
+  plan->kv_dtype = kv_dtype;
+  plan->wave = pa::split_ctas_per_sm(plan->D, kv_dtype, plan->rpc / 8) * plan->sms;
   return PA_OK;
 }
 
@@ -442,6 +456,8 @@ int pa_decode_ex(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int 
   sp.max_blocks = max_blocks_per_seq;
   sp.n = num_seqs;
   sp.C = plan->C;
+  sp.sms = plan->sms;
+  sp.resident = 0;
   sp.total_rows = num_blocks * num_kv_heads * block_size;
   sp.out_f16 = q_dtype == PA_FP16 ? 1 : 0;
   sp.rpc = plan->rpc;

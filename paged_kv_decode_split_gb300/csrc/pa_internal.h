@@ -68,6 +68,8 @@ struct PlanParams {
   int window;     // sliding window (0: none): a request's plan starts at its first visible tile
   int G;          // q heads per kv head
   int rpc;        // query rows per split-kernel work item (row chunk)
+  int wave;       // CTAs of the decode grid that run at once (0: unknown); a plan of
+                  // more (C * Hkv > wave) has its slots cut into pieces
   long long rows_cap;
   long long max_extra;
   PlanDev dev;
@@ -81,8 +83,13 @@ struct SplitParams {
   const int* context_lens;
   const int* cu;  // nullable
   int num_tokens, num_blocks, Hq, Hkv, G, bs, max_blocks, n;
-  int C;            // plan capacity: CTAs [0, C*Hkv) start on pieces [0, C), the rest write
-                    // zero rows; pieces from C on are taken by CTAs that finished theirs
+  int C;            // plan capacity: CTAs [C*Hkv, grid) write zero rows
+  int sms;          // multiprocessors of the device
+  int resident;     // set by the launcher: CTAs of this grid that run at once (0: all).
+                    // CTA b starts on item b (piece b / Hkv, kv head b % Hkv) for b < C*Hkv,
+                    // or, when the plan holds more pieces than C, for b < min(resident,
+                    // C*Hkv); every later item is taken from the work counter by
+                    // whichever CTA is free
   int total_rows;   // num_blocks * Hkv * bs: first out-of-range row of the cache view
   int out_f16;      // q/out element type: 1 = fp16, 0 = bf16
   int rpc;          // query rows per work item (row chunk); a multiple of 8 x row groups

@@ -16,8 +16,9 @@
 // partial-row, extra-item and merge-row offsets), then a slot-parallel fill
 // that finds each slot's request by binary search over the scanned offsets.
 // Beyond the plan itself it writes what the split kernel runs: every slot cut
-// into pieces of about the mean slot length (at most Q; Q = 1 keeps tasks
-// whole), in launch order (longest first, by a counting sort over 128
+// into pieces of about the mean slot length, or as short as allowed when the
+// decode grid is more than one wave (at most Q; Q = 1 keeps tasks whole), in
+// launch order (longest first, by a counting sort over 128
 // quarter-octave length classes), the extra work items that split the query
 // rows of requests with more rows than one work item holds, and the list of
 // rows the merge combines.
@@ -223,10 +224,14 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
       my_maxslot = max(my_maxslot, nbase[k] + (nbig[k] ? 1 : 0));
     }
   }
-  // ---- 2b. pieces.  When the slots are uneven (the longest above 5/4 of the
-  // mean), no piece may exceed x = ceil(sum tiles / (1.5 C)) tiles, which
-  // leaves about 1.5 to 2 waves of pieces -- enough for the longest-first
-  // order to even out the CTAs' finishing times; otherwise slots run whole.
+  // ---- 2b. pieces.  When the decode grid has more CTAs than run at once
+  // (C * Hkv > wave), a second wave of whole slots would leave SMs idle, so
+  // every slot is cut as finely as allowed (pieces of kMinPieceTiles, at most
+  // Q per slot) and the first wave's CTAs share them.  Else, when the slots
+  // are uneven (the longest above 5/4 of the mean), no piece may exceed
+  // x = ceil(sum tiles / (1.5 C)) tiles, which leaves about 1.5 to 2 waves of
+  // pieces -- enough for the longest-first order to even out the CTAs'
+  // finishing times; otherwise slots run whole.
   auto pieces_of = [&](int k, int x) {
     return parts[k] ? (parts[k] - nbig[k]) * piece_count(nbase[k], x, p.Q) +
                           (nbig[k] ? nbig[k] * piece_count(nbase[k] + 1, x, p.Q) : 0)
@@ -255,7 +260,9 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
     for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     ns = warp_sum64(ns);
     xcut = mx;
-    if (4ll * mx * ns > 5ll * sum_tiles)
+    if (p.wave > 0 && C * p.Hkv > p.wave)
+      xcut = min(mx, kMinPieceTiles);
+    else if (4ll * mx * ns > 5ll * sum_tiles)
       xcut = static_cast<int>(min(static_cast<long long>(mx),
                                   max(static_cast<long long>(kMinPieceTiles),
                                       (2 * sum_tiles + 3 * C - 1) / (3 * C))));

@@ -55,71 +55,9 @@
 #include "pa_device.cuh"
 #include "pa_internal.h"
 #include "pa_merge.cuh"
+#include "pa_split_cfg.h"
 
 namespace pa {
-
-// KL: K cache layout -- 0: [num_blocks, Hkv, bs, D]; 1: the grouped
-// [num_blocks, Hkv, D/16, bs, 16] (V is always [num_blocks, Hkv, bs, D]).
-template <int D, int KVT, int WQ, int KL>
-struct SplitCfg {
-  static constexpr bool kFp8 = (KVT == PA_FP8_E4M3);
-  static constexpr bool kGroupedK = (KL == 1);
-  static constexpr int GRP = 16 * (kFp8 ? 1 : 2);     // grouped K: one key's 16-dim group, bytes
-  static constexpr bool kBf16Mma = (KVT == PA_BF16);
-  static constexpr int ESZ = kFp8 ? 1 : 2;            // bytes per cached element
-  static constexpr int ROW = D * ESZ;                 // bytes per key row
-  static constexpr int SWB = ROW < 128 ? ROW : 128;   // swizzle span = box row bytes
-  static constexpr int CB = ROW / SWB;                // column blocks per key row
-  // Head dims above 256 are cut into slices of 256 dims (128 when 256 does
-  // not divide D), one consumer warp each: a warp forms the partial logits of
-  // its slice, the slices' partials are summed through shared memory (every
-  // warp of the row group adds them in the same order, so all hold the same
-  // logits and softmax state), and each warp accumulates P V for its own
-  // slice.  Stages are one 16-key tile.
-  static constexpr bool kWide = D > 256;
-  static constexpr int DS = kWide ? (D % 256 == 0 ? 256 : 128) : D;  // head dims per consumer warp
-  static constexpr int ND = D / DS;                   // dim slices
-  static constexpr int CBS = DS * ESZ / SWB;          // column blocks per slice
-  static constexpr int KS = kWide ? 16 : kStageTensorBytes / ROW;  // keys per stage
-  // partial-logit exchange of the dim slices: [stage parity][WQ][ND][32 lanes] float4
-  static constexpr int SX_BYTES = kWide ? 2 * WQ * ND * 32 * 16 : 0;
-  // Ring depth: 3 stages, or 2 where that lets two CTAs share an SM (wide
-  // heads of 640 and 768 dims: 3 stages of 40-48 KB need more than half of
-  // the SM's 228 KB of shared memory).
-  static constexpr int kFixedBytes = 1024 + 64 + SX_BYTES;
-  static constexpr bool kTwoPerSm3 = 2 * (3 * 2 * KS * ROW + kFixedBytes + 1024) <= 228 * 1024;
-  static constexpr bool kTwoPerSm2 = 2 * (2 * 2 * KS * ROW + kFixedBytes + 1024) <= 228 * 1024;
-  static constexpr int NS = (kWide && !kTwoPerSm3 && kTwoPerSm2) ? 2 : 3;  // ring depth
-  static constexpr int MTS = KS / 16;                 // 16-key tiles per stage
-  static constexpr int WK0 = (WQ == 1) ? 4 : (WQ == 4 ? 1 : 2);
-  static constexpr int WK = WK0 < MTS ? WK0 : MTS;   // key warps per row group
-  static constexpr int T = MTS / WK;                  // tiles one warp handles per stage
-  // Every key warp consumes every stage, in order, so a warp never waits on a
-  // ring slot's use u+1 before it consumed use u -- which keeps the
-  // parity-based mbarrier waits unambiguous.
-  static constexpr int NCW = WQ * WK * ND;            // consumer warps
-  static constexpr int THREADS = 32 * (1 + NCW);
-  static constexpr int TILE_BYTES = KS * ROW;         // one tensor, one stage
-  static constexpr int BLOCK_BYTES = KS * SWB;        // one column block of a tile
-  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K then V
-  static constexpr int DATA_BYTES = NS * STAGE_BYTES;
-  static constexpr int DP = D + 4;                    // padded exchange row, floats
-  static constexpr int EX_BYTES = WQ * WK * 8 * (DP + 2) * 4;
-  static constexpr int SMEM_BYTES = DATA_BYTES + kFixedBytes;
-  // two CTAs per SM where the threads' registers and both rings fit (228 KB per SM)
-  static constexpr int MIN_BLOCKS = (THREADS <= 224 && 2 * (SMEM_BYTES + 1024) <= 228 * 1024) ? 2 : 1;
-  static_assert(!kWide || (WK == 1 && T == 1 && CBS * SWB == DS * ESZ && WQ <= 2),
-                "sliced head dims: one key warp, one tile per stage, whole column blocks");
-  static_assert(2 * NS * 8 <= 64, "mbarriers fit before the exchange area");
-  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
-  static_assert(KS % 16 == 0 && MTS % WK == 0, "whole 16-key tiles per warp");
-  static_assert(MTS * CB * 2 <= 32, "a stage needs at most one copy per producer lane");
-  static_assert(!kGroupedK || MTS * (1 + CB) <= 32, "grouped K: one copy per producer lane");
-  static_assert(!kGroupedK || (16 * ROW) % 1024 == 0,
-                "grouped K: every 16-key box starts on a 1024-byte swizzle repeat");
-  static_assert(EX_BYTES <= DATA_BYTES, "epilogue exchange reuses the stage ring");
-  static_assert(D % 32 == 0, "head_dim is a multiple of 32");
-};
 
 // Byte offset of 16-byte chunk `chunk` of row `row` inside a column block whose
 // base is aligned to the swizzle repeat: the TMA 128B (64B) swizzle XORs the
@@ -173,10 +111,18 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     zero_rows<D>(p, blockIdx.x - p.C * p.Hkv, warp, Cfg::THREADS / 32, lane);
     return;
   }
-  // This CTA's first item -- piece blockIdx / Hkv, head blockIdx % Hkv --
-  // read together with the counts it depends on.  Item slots are
-  // double-buffered: round k reads slot k & 1 while the producer may already
-  // claim round k + 1's item into the other slot.
+  // Items (piece, kv head) are numbered piece-major: item i is piece i / Hkv,
+  // head i % Hkv.  The first `nst` of them belong to CTAs 0..nst-1, one each,
+  // and the rest come from the work counter.  nst = C * Hkv (every CTA starts
+  // on an item of its own) unless the planner cut the slots into more pieces
+  // than C and the grid is more than one wave: then only the CTAs of the
+  // first wave own one (a later CTA would run its own after everyone else).
+  // Only thread 0 (prologue and claims) uses it.
+  int nst = p.C * p.Hkv;
+  // This CTA's first item -- item blockIdx, when it is below nst -- read
+  // together with the counts it depends on.  Item slots are double-buffered:
+  // round k reads slot k & 1 while the producer may already claim round
+  // k + 1's item into the other slot.
   __shared__ int s_item[2][4];
   __shared__ int4 s_rec[2];
   __shared__ int s_npieces, s_nextra;
@@ -185,12 +131,14 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     const int npieces = p.plan.counters[4];
     const int nextra = p.plan.counters[0];
     const int4 rec = p.plan.pieces[blockIdx.x / p.Hkv];  // < C: inside the array
+    if (npieces > p.C && p.resident > 0 && p.resident < nst) nst = p.resident;
     s_npieces = npieces;
     s_nextra = nextra;
     s_rec[0] = rec;
     s_pre = 0;
-    const int late = (npieces > p.C ? npieces - p.C : 0) * p.Hkv;
-    const bool mine = static_cast<int>(blockIdx.x / p.Hkv) < npieces;
+    const int late = npieces * p.Hkv > nst ? npieces * p.Hkv - nst : 0;
+    const bool mine = static_cast<int>(blockIdx.x) < nst &&
+                      static_cast<int>(blockIdx.x / p.Hkv) < npieces;
     s_item[0][0] = mine ? static_cast<int>(blockIdx.x / p.Hkv) : -1;
     s_item[0][1] = mine ? static_cast<int>(blockIdx.x % p.Hkv) : 0;
     s_item[0][2] = 0;
@@ -214,23 +162,23 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
 
   // Work items: first this CTA's own (piece, kv head) in launch order -- the
   // planner sorts pieces longest first -- then, until none are left, from one
-  // device counter: the pieces past the first C (in launch order), then the
-  // extra row chunks of requests with many query rows.
+  // device counter: the items from nst on (in launch order), then the extra
+  // row chunks of requests with many query rows.
   // Takes the next item from the device counter into slot `sl` (one thread).
   // The producer calls it as soon as it has issued the last stage of an item,
   // so that the claim and the record load overlap the consumers' last stages;
   // the loop head calls it when that did not happen.
   auto claim_next = [&](int sl) {
     const int npieces = s_npieces, nextra = s_nextra;
-    const int late = (npieces > p.C ? npieces - p.C : 0) * Hkv;
+    const int late = npieces * Hkv > nst ? npieces * Hkv - nst : 0;
     int pos = -1, hh = 0, chunk = 0, valid = 1;
     if (late == 0 && nextra == 0) {
       valid = 0;
     } else {
       int idx = atomicAdd(p.plan.counters + 1, 1);
       if (idx < late) {
-        pos = p.C + idx / Hkv;
-        hh = idx % Hkv;
+        pos = (nst + idx) / Hkv;
+        hh = (nst + idx) % Hkv;
       } else if ((idx -= late) < nextra * Hkv) {
         const int2 e = p.plan.extra[idx / Hkv];
         pos = e.x;
@@ -246,6 +194,119 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     s_item[sl][2] = chunk;
     s_item[sl][3] = valid;
   };
+  // What an item covers: request r, kv head h, its rows [row_lo, row_hi) in
+  // passes of NQ, keys [kb, ke_task); ok = false when the plan was refreshed
+  // from other lengths (the zero CTAs handle the request) or the row chunk is
+  // empty.
+  struct ItemGeo {
+    int r, h, S, row0, L, prow_base, row_lo, row_hi, npass, kb, kz, ke_task;
+    bool ok;
+  };
+  auto item_geo = [&](int sl) {
+    ItemGeo q;
+    const int4 pc = s_rec[sl];
+    q.r = pc.x;
+    q.h = s_item[sl][1];
+    q.S = p.context_lens[q.r];
+    q.row0 = p.cu ? p.cu[q.r] : q.r;
+    q.L = p.cu ? p.cu[q.r + 1] - q.row0 : 1;
+    const int2 snap = p.plan.snap[q.r];
+    q.prow_base = pc.w;
+    q.row_lo = s_item[sl][2] * p.rpc;
+    q.row_hi = min(q.L * G, q.row_lo + p.rpc);
+    q.npass = (q.row_hi - q.row_lo + NQ - 1) / NQ;
+    q.kb = pc.y;
+    q.kz = pc.z;
+    q.ke_task = min(pc.z, q.S);
+    q.ok = snap.x == q.S && snap.y == q.L && q.row_lo < q.row_hi;
+    return q;
+  };
+  // Last key any row of pass `pass` of item q may see.
+  auto geo_key_end = [&](const ItemGeo& q, int pass) {
+    const int last_row = min(q.row_hi, q.row_lo + (pass + 1) * NQ) - 1;
+    const int last_tok = last_row / G;
+    return min(q.ke_task, q.S - (q.L - 1 - last_tok));
+  };
+  // Producer: block-table entries [kb / bs, + 64) of item q, 32 per register.
+  auto bt_window = [&](const ItemGeo& q, int& cur, int& nxt) {
+    const int* bt = p.block_tables + static_cast<size_t>(q.r) * p.max_blocks;
+    const int np = min((q.kz + p.bs - 1) / p.bs, p.max_blocks);
+    const int w0 = q.kb / p.bs;
+    cur = (w0 + lane < np) ? __ldg(bt + w0 + lane) : -1;
+    nxt = (w0 + 32 + lane < np) ? __ldg(bt + w0 + 32 + lane) : -1;
+  };
+  // Producer: issues stage s of a pass over keys [q.kb, ke) into ring stage
+  // `it` (the caller advances it); win / cur / nxt: the block-table window.
+  const uint64_t policy = l2_evict_first_policy();
+  const int box_rows = p.bs < Cfg::KS ? p.bs : Cfg::KS;
+  const uint32_t box_bytes = static_cast<uint32_t>(box_rows * Cfg::SWB);
+  auto issue_stage = [&](const ItemGeo& q, int s, int ke, int& win, int& cur, int& nxt) {
+    const int bs = p.bs;
+    const int buf = it % Cfg::NS;
+    if (aborted()) return;
+    if (it >= Cfg::NS && !wait_all(bar_empty + 8 * buf, ((it / Cfg::NS) & 1) ^ 1)) return;
+    issued = it + 1;
+    const int* bt = p.block_tables + static_cast<size_t>(q.r) * p.max_blocks;
+    const int npages = min((q.S + bs - 1) / bs, p.max_blocks);
+    const int key0 = q.kb + s * Cfg::KS;
+    const int nkeys = min(Cfg::KS, ke - key0);
+    const int nbox = (nkeys + box_rows - 1) / box_rows;
+    while (key0 / bs >= win + 32) {  // a stage spans at most 16 pages: [win, win + 48)
+      win += 32;
+      cur = nxt;
+      nxt = (win + 32 + lane < npages) ? __ldg(bt + win + 32 + lane) : -1;
+    }
+    // copy c of this stage (one per lane): K/V by c & 1, column block and
+    // row box from c >> 1; with grouped K, lanes [0, MTS) copy K -- one box
+    // of 16 keys by every 16-dim group each -- and the others V
+    const int c = lane;
+    bool is_v;
+    int rb, cb;
+    if constexpr (Cfg::kGroupedK) {
+      is_v = c >= Cfg::MTS;
+      rb = is_v ? (c - Cfg::MTS) / Cfg::CB : c;
+      cb = is_v ? (c - Cfg::MTS) % Cfg::CB : 0;
+    } else {
+      is_v = (c & 1) != 0;
+      rb = (c >> 1) / Cfg::CB;
+      cb = (c >> 1) % Cfg::CB;
+    }
+    const int key = key0 + rb * ((Cfg::kGroupedK && !is_v) ? 16 : box_rows);
+    const int pidx = key / bs;
+    const int widx = min(pidx - win, 63);
+    const int pc = __shfl_sync(0xffffffffu, cur, widx & 31);
+    const int pn = __shfl_sync(0xffffffffu, nxt, widx & 31);
+    const int page = widx < 32 ? pc : pn;
+    const int nbox_k = Cfg::kGroupedK ? (nkeys + 15) / 16 : nbox;  // grouped K: 16-key boxes
+    if (lane == 0)
+      mbar_arrive_expect_tx(bar_full + 8 * buf,
+                            Cfg::kGroupedK ? (nbox_k * 16 + nbox * box_rows) * Cfg::ROW
+                                           : nbox * box_bytes * Cfg::CB * 2);
+    __syncwarp();
+    if (rb < ((Cfg::kGroupedK && !is_v) ? nbox_k : nbox)) {
+      const bool bad = page < 0 || page >= p.num_blocks || pidx >= p.max_blocks;
+      if (bad) atomicOr(p.plan.err, PA_DEVERR_BAD_PAGE);  // the copy reads zeros
+      if (Cfg::kGroupedK && !is_v) {
+        // coordinates {byte in 128-byte row, 128-byte row of the group in
+        // the page, (page * Hkv + head) * D/16 + group}
+        const int slab = bad ? p.num_blocks * p.Hkv : page * p.Hkv + q.h;
+        const uint32_t dst = base + buf * Cfg::STAGE_BYTES +
+                             static_cast<uint32_t>(rb * 16 * Cfg::ROW);
+        tma_load_3d(dst, &tmk, 0, (key % bs) * Cfg::GRP / 128, slab * (D / 16),
+                    bar_full + 8 * buf, policy);
+      } else {
+        const int y = bad ? p.total_rows : (page * p.Hkv + q.h) * bs + (key % bs);
+        const uint32_t dst = base + buf * Cfg::STAGE_BYTES + (is_v ? Cfg::TILE_BYTES : 0) +
+                             cb * Cfg::BLOCK_BYTES + static_cast<uint32_t>(rb * box_rows * Cfg::SWB);
+        tma_load_2d(dst, is_v ? &tmv : &tmk, cb * (Cfg::SWB / Cfg::ESZ), y, bar_full + 8 * buf,
+                    policy);
+      }
+    }
+  };
+  // Producer: stages of the coming pass issued ahead, and the block-table
+  // window after them.
+  int pre_n = 0, pre_win = 0, pre_cur = -1, pre_nxt = -1;
+
   for (int round = 0;; ++round) {
     if (round > 0) {  // round 0's item was set up with the prologue
       __syncthreads();  // everyone has read the previous item
@@ -260,126 +321,81 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     const int sl = round & 1;
     if (!s_item[sl][3]) break;
     if (s_item[sl][0] < 0) continue;  // no piece for this CTA: look for extra items
-    const int h = s_item[sl][1];
-    const int chunk = s_item[sl][2];
-    const int4 piece = s_rec[sl];
-    const int r = piece.x;
+    const ItemGeo cg = item_geo(sl);
+    const int h = cg.h;
+    const int r = cg.r;
 
     // Block-table window of the piece's first pages, loaded by the producer
     // alongside the length checks (entries past the piece's end are not used).
     int bt_cur = -1, bt_nxt = -1;
-    if (warp == 0) {
-      const int* bt = p.block_tables + static_cast<size_t>(r) * p.max_blocks;
-      const int np = min((piece.z + p.bs - 1) / p.bs, p.max_blocks);
-      const int w0 = piece.y / p.bs;
-      bt_cur = (w0 + lane < np) ? __ldg(bt + w0 + lane) : -1;
-      bt_nxt = (w0 + 32 + lane < np) ? __ldg(bt + w0 + 32 + lane) : -1;
-    }
+    if (warp == 0) bt_window(cg, bt_cur, bt_nxt);
 
     // A plan refreshed from other lengths: the split kernel's zero CTAs zero
-    // these rows and report it; this piece does nothing.
-    const int S = p.context_lens[r];
-    const int row0 = p.cu ? p.cu[r] : r;
-    const int L = p.cu ? p.cu[r + 1] - row0 : 1;
-    const int2 snap = p.plan.snap[r];
-    if (snap.x != S || snap.y != L) continue;
-
-    const int prow_base = piece.w;              // -1: write the output rows directly
-    const int rows = L * G;                     // query rows of this request
-    const int row_lo = chunk * p.rpc;           // this item's rows [row_lo, row_hi)
-    const int row_hi = min(rows, row_lo + p.rpc);
-    if (row_lo >= row_hi) continue;
-    const int npass = (row_hi - row_lo + NQ - 1) / NQ;
-    const int kb = piece.y;                     // first key of the piece
-    const int ke_task = min(piece.z, S);
-
-    // Last key any row of pass `pass` may see.
-    auto pass_key_end = [&](int pass) {
-      const int last_row = min(row_hi, row_lo + (pass + 1) * NQ) - 1;
-      const int last_tok = last_row / G;
-      return min(ke_task, S - (L - 1 - last_tok));
-    };
+    // these rows and report it; this piece does nothing.  Likewise a row chunk
+    // past the request's rows.
+    if (!cg.ok) continue;
+    const int S = cg.S;
+    const int row0 = cg.row0;
+    const int L = cg.L;
+    const int prow_base = cg.prow_base;  // -1: write the output rows directly
+    const int row_lo = cg.row_lo;        // this item's rows [row_lo, row_hi)
+    const int row_hi = cg.row_hi;
+    const int npass = cg.npass;
+    const int kb = cg.kb;                // first key of the piece
+    const int ke_task = cg.ke_task;
+    auto pass_key_end = [&](int pass) { return geo_key_end(cg, pass); };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    const uint64_t policy = l2_evict_first_policy();
-    const int bs = p.bs;
-    const int box_rows = bs < Cfg::KS ? bs : Cfg::KS;
-    const uint32_t box_bytes = static_cast<uint32_t>(box_rows * Cfg::SWB);
-    const int* bt = p.block_tables + static_cast<size_t>(r) * p.max_blocks;
-    const int npages = min((S + bs - 1) / bs, p.max_blocks);
-    auto bt_at = [&](int idx) { return idx < npages ? __ldg(bt + idx) : -1; };
     for (int pass = 0; pass < npass; ++pass) {
       const int ke = pass_key_end(pass);
       const int nst = ke > kb ? (ke - kb + Cfg::KS - 1) / Cfg::KS : 0;
-      int win = kb / bs;  // block-table entries [win, win + 64) live in cur / nxt
-      int cur = bt_cur;
-      int nxt = bt_nxt;
-      for (int s = 0; s < nst; ++s, ++it) {
-        const int buf = it % Cfg::NS;
-        if (aborted()) continue;
-        if (it >= Cfg::NS && !wait_all(bar_empty + 8 * buf, ((it / Cfg::NS) & 1) ^ 1)) continue;
-        issued = it + 1;
-        const int key0 = kb + s * Cfg::KS;
-        const int nkeys = min(Cfg::KS, ke - key0);
-        const int nbox = (nkeys + box_rows - 1) / box_rows;
-        while (key0 / bs >= win + 32) {  // a stage spans at most 16 pages: [win, win + 48)
-          win += 32;
-          cur = nxt;
-          nxt = bt_at(win + 32 + lane);
-        }
-        // copy c of this stage (one per lane): K/V by c & 1, column block and
-        // row box from c >> 1; with grouped K, lanes [0, MTS) copy K -- one box
-        // of 16 keys by every 16-dim group each -- and the others V
-        const int c = lane;
-        bool is_v;
-        int rb, cb;
-        if constexpr (Cfg::kGroupedK) {
-          is_v = c >= Cfg::MTS;
-          rb = is_v ? (c - Cfg::MTS) / Cfg::CB : c;
-          cb = is_v ? (c - Cfg::MTS) % Cfg::CB : 0;
-        } else {
-          is_v = (c & 1) != 0;
-          rb = (c >> 1) / Cfg::CB;
-          cb = (c >> 1) % Cfg::CB;
-        }
-        const int key = key0 + rb * ((Cfg::kGroupedK && !is_v) ? 16 : box_rows);
-        const int pidx = key / bs;
-        const int widx = min(pidx - win, 63);
-        const int pc = __shfl_sync(0xffffffffu, cur, widx & 31);
-        const int pn = __shfl_sync(0xffffffffu, nxt, widx & 31);
-        const int page = widx < 32 ? pc : pn;
-        const int nbox_k = Cfg::kGroupedK ? (nkeys + 15) / 16 : nbox;  // grouped K: 16-key boxes
-        if (lane == 0)
-          mbar_arrive_expect_tx(bar_full + 8 * buf,
-                                Cfg::kGroupedK ? (nbox_k * 16 + nbox * box_rows) * Cfg::ROW
-                                               : nbox * box_bytes * Cfg::CB * 2);
-        __syncwarp();
-        if (rb < ((Cfg::kGroupedK && !is_v) ? nbox_k : nbox)) {
-          const bool bad = page < 0 || page >= p.num_blocks || pidx >= p.max_blocks;
-          if (bad) atomicOr(p.plan.err, PA_DEVERR_BAD_PAGE);  // the copy reads zeros
-          if (Cfg::kGroupedK && !is_v) {
-            // coordinates {byte in 128-byte row, 128-byte row of the group in
-            // the page, (page * Hkv + head) * D/16 + group}
-            const int slab = bad ? p.num_blocks * p.Hkv : page * p.Hkv + h;
-            const uint32_t dst = base + buf * Cfg::STAGE_BYTES +
-                                 static_cast<uint32_t>(rb * 16 * Cfg::ROW);
-            tma_load_3d(dst, &tmk, 0, (key % bs) * Cfg::GRP / 128, slab * (D / 16),
-                        bar_full + 8 * buf, policy);
-          } else {
-            const int y = bad ? p.total_rows : (page * p.Hkv + h) * bs + (key % bs);
-            const uint32_t dst = base + buf * Cfg::STAGE_BYTES + (is_v ? Cfg::TILE_BYTES : 0) +
-                                 cb * Cfg::BLOCK_BYTES + static_cast<uint32_t>(rb * box_rows * Cfg::SWB);
-            tma_load_2d(dst, is_v ? &tmv : &tmk, cb * (Cfg::SWB / Cfg::ESZ), y, bar_full + 8 * buf,
-                        policy);
-          }
-        }
+      // block-table entries [win, win + 64) live in cur / nxt
+      int win = kb / p.bs, cur = bt_cur, nxt = bt_nxt, s0 = 0;
+      if (pre_n > 0) {  // the first stages were issued at the end of the last pass
+        s0 = pre_n;
+        win = pre_win;
+        cur = pre_cur;
+        nxt = pre_nxt;
+        pre_n = 0;
       }
+      for (int s = s0; s < nst; ++s, ++it) issue_stage(cg, s, ke, win, cur, nxt);
       // Last stage of the item issued: claim the next one (into the other
       // slot) while the consumers finish this one.
       if (pass == npass - 1 && lane == 0 && *reinterpret_cast<volatile int*>(&s_abort) == 0) {
         claim_next(sl ^ 1);
         s_pre = 1;
+      }
+      if constexpr (Cfg::kPreIssue) {
+        // While the consumers finish this pass, issue the first stages (at
+        // most NS - 1) of the next one -- this item's next row pass, or the
+        // next item's first -- into the ring slots they have released.  The
+        // slot of this pass's last stage holds their exchange and is
+        // released after it.
+        __syncwarp();  // lane 0's claim is visible to the warp
+        if (nst > 0 && !aborted()) {
+          ItemGeo nq = cg;
+          bool have = pass + 1 < npass;
+          int npass_idx = pass + 1;
+          int ncur = bt_cur, nnxt = bt_nxt;
+          if (!have && s_item[sl ^ 1][3] && s_item[sl ^ 1][0] >= 0) {
+            nq = item_geo(sl ^ 1);
+            have = nq.ok;
+            npass_idx = 0;
+            if (have) bt_window(nq, ncur, nnxt);
+          }
+          if (have) {
+            const int nke = geo_key_end(nq, npass_idx);
+            const int nn = nke > nq.kb ? (nke - nq.kb + Cfg::KS - 1) / Cfg::KS : 0;
+            const int np = nn < Cfg::NS - 1 ? nn : Cfg::NS - 1;
+            int nwin = nq.kb / p.bs;
+            for (int s = 0; s < np; ++s, ++it) issue_stage(nq, s, nke, nwin, ncur, nnxt);
+            pre_n = np;
+            pre_win = nwin;
+            pre_cur = ncur;
+            pre_nxt = nnxt;
+          }
+        }
       }
       __syncthreads();  // pairs with the consumers' end-of-pass barrier
     }
@@ -702,8 +718,14 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_empty + 8 * buf);
+      // The slot of a pass's last stage is released after the exchange that
+      // reuses it (below) when the producer issues ahead.
+      if (lane == 0 && !(Cfg::kPreIssue && s == nst - 1)) mbar_arrive(bar_empty + 8 * buf);
     }
+    // ring slot of the epilogue exchange: the last stage's (the producer may
+    // already be filling the others with the next pass), or any when the pass
+    // had no stage (nothing is then in flight)
+    const int xbuf = (nst > 0 ? it + nst - 1 : it) % Cfg::NS;
     it += nst;
 
     // ------------------------------------------------------------ epilogue
@@ -715,8 +737,8 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     named_barrier_sync(1, Cfg::NCW * 32);  // all stage reads of this pass done
 
     // exchange area: O [WQ][WK][8][DP], then m and l [WQ][WK][8]
-    float* ex_o = ex;
-    float* ex_m = ex + WQ * Cfg::WK * 8 * Cfg::DP;
+    float* ex_o = Cfg::kPreIssue ? ex + xbuf * (Cfg::STAGE_BYTES / 4) : ex;
+    float* ex_m = ex_o + WQ * Cfg::WK * 8 * Cfg::DP;
     float* ex_l = ex_m + WQ * Cfg::WK * 8;
     const int wslot = (wq * Cfg::WK + wk) * 8;
 #pragma unroll
@@ -794,7 +816,11 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
       }
     }
     fence_proxy_async_smem();  // exchange writes precede the next pass's TMA writes
-    __syncthreads();           // pairs with the producer's end-of-pass barrier
+    if constexpr (Cfg::kPreIssue) {
+      __syncwarp();
+      if (nst > 0 && lane == 0) mbar_arrive(bar_empty + 8 * xbuf);  // this warp is done with it
+    }
+    __syncthreads();  // pairs with the producer's end-of-pass barrier
   }
   }  // consumers
   }  // work items
@@ -813,16 +839,24 @@ cudaError_t launch_split_cfg(const SplitParams& p, const CUtensorMap& tk,
                              const CUtensorMap& tv, cudaStream_t s) {
   using Cfg = SplitCfg<D, KVT, WQ, KL>;
   auto kern = split_kernel<D, KVT, WQ, KL>;
-  static bool attr_done = false;  // benign race: the attribute call is idempotent
+  // benign races: both calls are idempotent
+  static bool attr_done = false;
+  static int per_sm = 0;  // CTAs per SM, as the occupancy calculator sees the kernel
   if (!attr_done) {
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    int b = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, Cfg::THREADS, Cfg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    per_sm = b;
     attr_done = true;
   }
+  SplitParams q = p;
+  q.resident = per_sm > 0 && p.sms > 0 ? per_sm * p.sms : 0;
   const unsigned zero_ctas = static_cast<unsigned>((p.num_tokens + kZeroRows - 1) / kZeroRows);
   return launch_pdl(kern, dim3(static_cast<unsigned>(p.C) * p.Hkv + zero_ctas), dim3(Cfg::THREADS),
-                    Cfg::SMEM_BYTES, s, tk, tv, p);
+                    Cfg::SMEM_BYTES, s, tk, tv, q);
 }
 
 template <int D, int KL>

@@ -30,6 +30,7 @@
 
 #include "../../include/pa.h"
 #include "pa_internal.h"
+#include "pa_split_cfg.h"
 
 namespace {
 
@@ -181,6 +182,7 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
   pp.max_tokens = num_tokens;
   pp.G = G;
   pp.rpc = lay.rpc;
+  pp.wave = pa::split_ctas_per_sm(head_dim, kv_dtype, wq) * sms;
   pp.rows_cap = lay.rows_cap;
   pp.max_extra = lay.max_extra;
   pp.dev = dev;
@@ -203,6 +205,8 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
   sp.max_blocks = max_blocks_per_seq;
   sp.n = num_seqs;
   sp.C = static_cast<int>(lay.C);
+  sp.sms = sms;
+  sp.resident = 0;
   sp.total_rows = num_blocks * num_kv_heads * block_size;
   sp.out_f16 = q_dtype == PA_FP16 ? 1 : 0;
   sp.rpc = lay.rpc;

@@ -288,9 +288,18 @@ def skewed_d1024(seed: int = 0, device="cpu") -> Workload:
     return w
 
 
+def uniform_n64_h8(seed: int = 0, device="cpu") -> Workload:
+    """64 decodes x 4096 context, Hq/Hkv 64/8, D 128, page 16, bf16: the plan
+    keeps one partition per request (C = n = 64), so its 512 CTAs are more
+    than the 2 x SM count that run at once."""
+    return make_batch("uniform_n64_h8", [4096] * 64, None, 64, 8, 128, 16, "bf16", seed=seed,
+                      device=device)
+
+
 CONFIGS["uniform_d512"] = uniform_d512
 CONFIGS["uniform_d1024"] = uniform_d1024
 CONFIGS["skewed_d1024"] = skewed_d1024
+CONFIGS["uniform_n64_h8"] = uniform_n64_h8
 
 
 @dataclass

@@ -104,6 +104,49 @@ def test_uneven_slots_run_as_pieces(dev, kv):
     assert plan.read_errors() == 0
 
 
+@pytest.mark.parametrize("case", ["d128_48x8", "d1024_bf16", "d896_fp16", "d1024_fp8_plan_bf16",
+                                  "d1024_bf16_plan_fp8"])
+def test_more_ctas_than_one_wave(dev, case):
+    """Plans whose CTAs (capacity x kv heads) outnumber those the GPU runs at
+    once: the refresh cuts even slots into short pieces that the first wave
+    shares, and CTAs past the resident count start by taking items from the
+    work counter.  The plan (work_info, reduce_info) is the oracle's; the
+    output matches the oracle.  A plan told another cache type than the decode
+    reads is still correct (only the piece sizes differ)."""
+    if case == "d128_48x8":  # C = n = 48, 384 CTAs; slots of 8 tiles
+        w = batch(dev, [2048] * 40 + [1900, 2100, 1, 0, 700, 2048, 300, 2040], H=(64, 8), D=128,
+                  seed=41)
+    else:
+        D = 896 if case.startswith("d896") else 1024
+        kv = {"d1024_bf16": "bf16", "d896_fp16": "fp16", "d1024_fp8_plan_bf16": "fp8",
+              "d1024_bf16_plan_fp8": "bf16"}[case]
+        q = "fp16" if kv == "fp16" else "bf16"
+        # C = min(4 x 16, 76) = 64: 256 CTAs, one per SM for 16-bit caches
+        w = batch(dev, [12000, 9000, 15000, 20000], H=(32, 4), D=D, kv=kv, q=q, seed=D,
+                  max_partitions=16)
+    plan = binding.plan_for(w)
+    if case.endswith("_plan_bf16"):
+        plan.set_kv_dtype("bf16")
+    elif case.endswith("_plan_fp8"):
+        plan.set_kv_dtype(binding.FP8_E4M3)
+    plan.refresh(w.context_lens, w.cu_query_lens)
+    out = binding.decode_workload(plan, w)
+    torch.cuda.synchronize()
+    work, red = plan.download()
+    ow, orr = oracle_plan(w, plan.info()["budget"])
+    assert np.array_equal(work, ow) and np.array_equal(red, orr)
+    assert plan.capacity * w.num_kv_heads > 152
+    ref = oracle_decode(w.to("cpu"))
+    assert max_diff(out, ref) <= TOL[w.kv_dtype]
+    assert plan.read_errors() == 0
+
+
+def test_set_kv_dtype_rejects_other_values(dev):
+    plan = binding.Plan(4, 8, 2, 128, device=dev)
+    with pytest.raises(binding.PaError):
+        plan.set_kv_dtype(7)
+
+
 # ------------------------------------------------- sliding window and sinks
 
 def run_ext(w, window=0, sinks=None, budget=None, max_partitions=None):
@@ -520,7 +563,7 @@ def _pick(w, k=4):
 
 FULL = ["uniform", "skewed", "mtp_verify", "mixed_prompt", "large_bf16", "large_fp8",
         "uniform_w1024", "skewed_w4096", "uniform_k5", "skewed_k5", "uniform_d512",
-        "skewed_d1024"]
+        "skewed_d1024", "uniform_d1024", "uniform_n64_h8"]
 
 
 @pytest.mark.parametrize("name", FULL)
