@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
   // from other lengths (the zero CTAs handle the request) or the row chunk is
   // empty.
   struct ItemGeo {
-    int r, h, S, row0, L, prow_base, row_lo, row_hi, npass, kb, kz, ke_task;
+    int r, h, S, row0, L, prow_base, row_lo, row_hi, npass, kb, ke_task;
     bool ok;
   };
   auto item_geo = [&](int sl) {
@@ -216,7 +216,6 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     q.row_hi = min(q.L * G, q.row_lo + p.rpc);
     q.npass = (q.row_hi - q.row_lo + NQ - 1) / NQ;
     q.kb = pc.y;
-    q.kz = pc.z;
     q.ke_task = min(pc.z, q.S);
     q.ok = snap.x == q.S && snap.y == q.L && q.row_lo < q.row_hi;
     return q;
@@ -227,11 +226,14 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     const int last_tok = last_row / G;
     return min(q.ke_task, q.S - (q.L - 1 - last_tok));
   };
-  // Producer: block-table entries [kb / bs, + 64) of item q, 32 per register.
-  auto bt_window = [&](const ItemGeo& q, int& cur, int& nxt) {
-    const int* bt = p.block_tables + static_cast<size_t>(q.r) * p.max_blocks;
-    const int np = min((q.kz + p.bs - 1) / p.bs, p.max_blocks);
-    const int w0 = q.kb / p.bs;
+  // Producer: block-table entries [kb / bs, + 64) of the piece in item slot
+  // sl, 32 per register -- read from the piece record alone, so that these
+  // loads are in flight together with the length checks of item_geo.
+  auto bt_window = [&](int sl, int& cur, int& nxt) {
+    const int4 pc = s_rec[sl];
+    const int* bt = p.block_tables + static_cast<size_t>(pc.x) * p.max_blocks;
+    const int np = min((pc.z + p.bs - 1) / p.bs, p.max_blocks);
+    const int w0 = pc.y / p.bs;
     cur = (w0 + lane < np) ? __ldg(bt + w0 + lane) : -1;
     nxt = (w0 + 32 + lane < np) ? __ldg(bt + w0 + 32 + lane) : -1;
   };
@@ -321,14 +323,13 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     const int sl = round & 1;
     if (!s_item[sl][3]) break;
     if (s_item[sl][0] < 0) continue;  // no piece for this CTA: look for extra items
-    const ItemGeo cg = item_geo(sl);
-    const int h = cg.h;
-    const int r = cg.r;
-
     // Block-table window of the piece's first pages, loaded by the producer
     // alongside the length checks (entries past the piece's end are not used).
     int bt_cur = -1, bt_nxt = -1;
-    if (warp == 0) bt_window(cg, bt_cur, bt_nxt);
+    if (warp == 0) bt_window(sl, bt_cur, bt_nxt);
+    const ItemGeo cg = item_geo(sl);
+    const int h = cg.h;
+    const int r = cg.r;
 
     // A plan refreshed from other lengths: the split kernel's zero CTAs zero
     // these rows and report it; this piece does nothing.  Likewise a row chunk
@@ -379,10 +380,10 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
           int npass_idx = pass + 1;
           int ncur = bt_cur, nnxt = bt_nxt;
           if (!have && s_item[sl ^ 1][3] && s_item[sl ^ 1][0] >= 0) {
+            bt_window(sl ^ 1, ncur, nnxt);
             nq = item_geo(sl ^ 1);
             have = nq.ok;
             npass_idx = 0;
-            if (have) bt_window(nq, ncur, nnxt);
           }
           if (have) {
             const int nke = geo_key_end(nq, npass_idx);
@@ -720,7 +721,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
       __syncwarp();
       // The slot of a pass's last stage is released after the exchange that
       // reuses it (below) when the producer issues ahead.
-      if (lane == 0 && !(Cfg::kPreIssue && s == nst - 1)) mbar_arrive(bar_empty + 8 * buf);
+      if (lane == 0 && !(Cfg::kHoldSlot && s == nst - 1)) mbar_arrive(bar_empty + 8 * buf);
     }
     // ring slot of the epilogue exchange: the last stage's (the producer may
     // already be filling the others with the next pass), or any when the pass
@@ -734,10 +735,71 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
       l[0] += __shfl_xor_sync(0xffffffffu, l[0], o);
       l[1] += __shfl_xor_sync(0xffffffffu, l[1], o);
     }
+    if constexpr (Cfg::kDirectEpi) {
+      // One key warp per row group: its m, l and accumulators are the pass's
+      // final ones (the slice warps of a row group hold the same m and l), so
+      // each thread scales its own elements and stores them -- rows 2t and
+      // 2t+1 of its group, the head dims its accumulator tiles cover.
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int n = pass_base + 8 * wq + 2 * t + e;
+        if (!warp_active || n >= row_hi) continue;
+        const int tok = n / G;
+        const int hq = h * G + n % G;
+        const float M = m[e];
+        float lsum = M != NEG_INF ? l[e] : 0.f;
+        // A single piece writes the output row: its head's sink joins here.
+        const bool sink = prow_base < 0 && p.sinks != nullptr;
+        const float f = sink ? add_sink(M, __ldg(p.sinks + hq) * 1.4426950408889634f, lsum) : 1.f;
+        const float inv = lsum > 0.f ? p.v_scale / lsum : 0.f;
+        auto fin = [&](float v) {
+          if (M == NEG_INF) v = 0.f;
+          if (sink) v *= f;
+          return v * inv;
+        };
+        if (prow_base < 0) {
+          const int trow = row0 + tok;
+          if (trow >= p.num_tokens) {
+            atomicOr(p.plan.err, PA_DEVERR_PLAN_OVERFLOW);
+            continue;
+          }
+          uint16_t* orow = static_cast<uint16_t*>(p.out) + (static_cast<size_t>(trow) * p.Hq + hq) * D;
+#pragma unroll
+          for (int dt = 0; dt < DS / 16; ++dt) {
+            if constexpr (!Cfg::kFp8) {
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const float v = fin(acc[dt][2 * hh + e]);
+                const uint32_t pk = p.out_f16 ? pack2<false>(v, 0.f) : pack2<true>(v, 0.f);
+                orow[wd * DS + 16 * dt + g + 8 * hh] = static_cast<uint16_t>(pk & 0xffffu);
+              }
+            } else {  // dims d, d + 1 of the pair hh = 0, 1
+              const int d = wd * DS + 32 * (dt / 2) + 4 * g + 2 * (dt % 2);
+              const float v0 = fin(acc[dt][e]), v1 = fin(acc[dt][2 + e]);
+              *reinterpret_cast<uint32_t*>(orow + d) = p.out_f16 ? pack2<false>(v0, v1) : pack2<true>(v0, v1);
+            }
+          }
+        } else {
+          const size_t prow = static_cast<size_t>(prow_base + tok) * p.Hq + hq;
+          float* po = p.plan.part_o + prow * D;
+#pragma unroll
+          for (int dt = 0; dt < DS / 16; ++dt) {
+            if constexpr (!Cfg::kFp8) {
+              po[wd * DS + 16 * dt + g] = fin(acc[dt][e]);
+              po[wd * DS + 16 * dt + g + 8] = fin(acc[dt][2 + e]);
+            } else {
+              const int d = wd * DS + 32 * (dt / 2) + 4 * g + 2 * (dt % 2);
+              *reinterpret_cast<float2*>(po + d) = make_float2(fin(acc[dt][e]), fin(acc[dt][2 + e]));
+            }
+          }
+          if (g == 0 && wd == 0) p.plan.part_lse[prow] = lsum > 0.f ? M + __log2f(lsum) : NEG_INF;
+        }
+      }
+    } else {
     named_barrier_sync(1, Cfg::NCW * 32);  // all stage reads of this pass done
 
     // exchange area: O [WQ][WK][8][DP], then m and l [WQ][WK][8]
-    float* ex_o = Cfg::kPreIssue ? ex + xbuf * (Cfg::STAGE_BYTES / 4) : ex;
+    float* ex_o = Cfg::kHoldSlot ? ex + xbuf * (Cfg::STAGE_BYTES / 4) : ex;
     float* ex_m = ex_o + WQ * Cfg::WK * 8 * Cfg::DP;
     float* ex_l = ex_m + WQ * Cfg::WK * 8;
     const int wslot = (wq * Cfg::WK + wk) * 8;
@@ -816,10 +878,11 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
       }
     }
     fence_proxy_async_smem();  // exchange writes precede the next pass's TMA writes
-    if constexpr (Cfg::kPreIssue) {
+    if constexpr (Cfg::kHoldSlot) {
       __syncwarp();
       if (nst > 0 && lane == 0) mbar_arrive(bar_empty + 8 * xbuf);  // this warp is done with it
     }
+    }  // exchange epilogue
     __syncthreads();  // pairs with the producer's end-of-pass barrier
   }
   }  // consumers

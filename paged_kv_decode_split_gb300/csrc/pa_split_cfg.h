@@ -57,9 +57,15 @@ struct SplitCfg {
   static constexpr int DP = D + 4;                    // padded exchange row, floats
   static constexpr int EX_BYTES = WQ * WK * 8 * (DP + 2) * 4;
   static constexpr int SMEM_BYTES = DATA_BYTES + kFixedBytes;
-  // The epilogue exchange fits in one ring slot: the producer may then issue
-  // the next pass's first stages while the consumers finish this one.
-  static constexpr bool kPreIssue = EX_BYTES <= STAGE_BYTES;
+  // One key warp per row group (every wide head dim): the epilogue needs no
+  // exchange, each warp stores its own accumulators.
+  static constexpr bool kDirectEpi = WK == 1;
+  // The producer issues the next pass's first stages while the consumers
+  // finish this one: with no exchange, or with one that fits in a ring slot
+  // -- the slot of the pass's last stage, which the consumers then hold
+  // until the exchange is done (kHoldSlot).
+  static constexpr bool kHoldSlot = !kDirectEpi && EX_BYTES <= STAGE_BYTES;
+  static constexpr bool kPreIssue = kDirectEpi || kHoldSlot;
   // two CTAs per SM where the threads' registers and both rings fit (228 KB per SM)
   static constexpr int MIN_BLOCKS = (THREADS <= 224 && 2 * (SMEM_BYTES + 1024) <= 228 * 1024) ? 2 : 1;
   static_assert(!kWide || (WK == 1 && T == 1 && CBS * SWB == DS * ESZ && WQ <= 2),
