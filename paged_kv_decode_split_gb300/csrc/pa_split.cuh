@@ -24,6 +24,11 @@
 //    issuing lane caps the stream at roughly half the HBM bandwidth -- into a
 //    ring of NS stages (32 KB up to head_dim 256; one 16-key tile of K and V
 //    for wider heads), completion counted in bytes on an mbarrier;
+//  * up to head_dim 128 a second producer warp splits that work (warp 0 the
+//    K copies, warp 1 the V copies, each walking the block table itself): a
+//    warp issues its lanes' copies one after the other, about 100 cycles per
+//    2 KB box, which alone held a CTA near 30 GB/s -- what a CTA left alone
+//    at the end of a skewed batch streams at;
 //  * consumer warps form (row group wq) x (key warp wk); every consumer warp
 //    takes part in every stage (its key slice: T 16-key tiles handled
 //    together -- independent MMA chains, one softmax reduction), so each warp
@@ -90,12 +95,16 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
   const uint32_t bar_empty = bar_full + 8 * Cfg::NS;
   float4* sx = reinterpret_cast<float4*>(smem_raw + (base - raw) + Cfg::DATA_BYTES + 64);
   __shared__ int s_abort;  // set when a bounded wait gave up
+  // Both producer warps issue (K copies and V copies) when a stage takes more
+  // than one box per tensor; with pages that hold a whole stage (one box
+  // each) warp 0 issues both and warp 1 idles.
+  const bool dual = Cfg::NPW == 2 && (Cfg::kGroupedK || Cfg::CB > 1 || p.bs < Cfg::KS);
   if (warp == 0 && lane == 0) {  // all of this overlaps the planner's tail
     prefetch_tmap(&tmk);
     prefetch_tmap(&tmv);
     s_abort = 0;
     for (int s = 0; s < Cfg::NS; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_full + 8 * s, dual ? 2 : 1);  // one expect-tx arrival per issuing warp
       mbar_init(bar_empty + 8 * s, Cfg::NCW);
     }
     fence_barrier_init();
@@ -245,6 +254,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
   auto issue_stage = [&](const ItemGeo& q, int s, int ke, int& win, int& cur, int& nxt) {
     const int bs = p.bs;
     const int buf = it % Cfg::NS;
+    if (warp == 1 && !dual) return;
     if (aborted()) return;
     if (it >= Cfg::NS && !wait_all(bar_empty + 8 * buf, ((it / Cfg::NS) & 1) ^ 1)) return;
     issued = it + 1;
@@ -260,11 +270,16 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     }
     // copy c of this stage (one per lane): K/V by c & 1, column block and
     // row box from c >> 1; with grouped K, lanes [0, MTS) copy K -- one box
-    // of 16 keys by every 16-dim group each -- and the others V
+    // of 16 keys by every 16-dim group each -- and the others V.  With two
+    // producer warps, warp 0 copies K and warp 1 V, one box per lane.
     const int c = lane;
     bool is_v;
     int rb, cb;
-    if constexpr (Cfg::kGroupedK) {
+    if (dual) {
+      is_v = warp == 1;
+      rb = (Cfg::kGroupedK && !is_v) ? c : c / Cfg::CB;
+      cb = (Cfg::kGroupedK && !is_v) ? 0 : c % Cfg::CB;
+    } else if constexpr (Cfg::kGroupedK) {
       is_v = c >= Cfg::MTS;
       rb = is_v ? (c - Cfg::MTS) / Cfg::CB : c;
       cb = is_v ? (c - Cfg::MTS) % Cfg::CB : 0;
@@ -280,10 +295,13 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     const int pn = __shfl_sync(0xffffffffu, nxt, widx & 31);
     const int page = widx < 32 ? pc : pn;
     const int nbox_k = Cfg::kGroupedK ? (nkeys + 15) / 16 : nbox;  // grouped K: 16-key boxes
-    if (lane == 0)
+    if (lane == 0) {
+      // bytes this warp's copies bring: K's and V's, or its own tensor's
+      const uint32_t kbytes = Cfg::kGroupedK ? nbox_k * 16 * Cfg::ROW : nbox * box_bytes * Cfg::CB;
+      const uint32_t vbytes = nbox * box_bytes * Cfg::CB;
       mbar_arrive_expect_tx(bar_full + 8 * buf,
-                            Cfg::kGroupedK ? (nbox_k * 16 + nbox * box_rows) * Cfg::ROW
-                                           : nbox * box_bytes * Cfg::CB * 2);
+                            !dual ? kbytes + vbytes : (warp == 0 ? kbytes : vbytes));
+    }
     __syncwarp();
     if (rb < ((Cfg::kGroupedK && !is_v) ? nbox_k : nbox)) {
       const bool bad = page < 0 || page >= p.num_blocks || pidx >= p.max_blocks;
@@ -326,7 +344,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     // Block-table window of the piece's first pages, loaded by the producer
     // alongside the length checks (entries past the piece's end are not used).
     int bt_cur = -1, bt_nxt = -1;
-    if (warp == 0) bt_window(sl, bt_cur, bt_nxt);
+    if (warp < Cfg::NPW) bt_window(sl, bt_cur, bt_nxt);
     const ItemGeo cg = item_geo(sl);
     const int h = cg.h;
     const int r = cg.r;
@@ -346,7 +364,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     const int ke_task = cg.ke_task;
     auto pass_key_end = [&](int pass) { return geo_key_end(cg, pass); };
 
-  if (warp == 0) {
+  if (warp < Cfg::NPW) {
     // ------------------------------------------------------------ producer
     for (int pass = 0; pass < npass; ++pass) {
       const int ke = pass_key_end(pass);
@@ -363,10 +381,13 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
       for (int s = s0; s < nst; ++s, ++it) issue_stage(cg, s, ke, win, cur, nxt);
       // Last stage of the item issued: claim the next one (into the other
       // slot) while the consumers finish this one.
-      if (pass == npass - 1 && lane == 0 && *reinterpret_cast<volatile int*>(&s_abort) == 0) {
+      if (pass == npass - 1 && warp == 0 && lane == 0 &&
+          *reinterpret_cast<volatile int*>(&s_abort) == 0) {
         claim_next(sl ^ 1);
         s_pre = 1;
       }
+      // the other producer warp reads the claimed item below
+      if constexpr (Cfg::NPW > 1) named_barrier_sync(6, 32 * Cfg::NPW);
       if constexpr (Cfg::kPreIssue) {
         // While the consumers finish this pass, issue the first stages (at
         // most NS - 1) of the next one -- this item's next row pass, or the
@@ -402,7 +423,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     }
   } else {
   // -------------------------------------------------------------- consumers
-  const int cw = warp - 1;
+  const int cw = warp - Cfg::NPW;
   const int wq = cw % WQ;
   const int wk = (cw / WQ) % Cfg::WK;
   const int wd = cw / (WQ * Cfg::WK);  // head-dim slice: dims [wd * DS, (wd + 1) * DS)
@@ -413,7 +434,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
   const float sl2 = p.scale_log2;
   const float NEG_INF = -__int_as_float(0x7f800000);
   constexpr float kRescale = 8.f;  // lazy-rescale threshold, log2 units
-  const int ct = threadIdx.x - 32;  // consumer thread index
+  const int ct = threadIdx.x - 32 * Cfg::NPW;  // consumer thread index
 
   // Per-thread swizzled offsets inside a 16-key tile (16-bit caches).
   const int lrowK = (lane & 7) + ((lane >> 3) & 1) * 8;  // ldmatrix row, K (A operand)
@@ -891,7 +912,8 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
   // Drain: wait (bounded) until the last copy issued into every ring slot has
   // landed, so that none can still be writing shared memory when the CTA
   // exits -- whether or not the pipeline was aborted.
-  if (warp == 0 && lane == 0) {
+  // Each producer warp drains the stages it issued.
+  if (warp < Cfg::NPW && lane == 0) {
     for (int k = (issued > Cfg::NS ? issued - Cfg::NS : 0); k < issued; ++k)
       mbar_wait(bar_full + 8 * (k % Cfg::NS), (k / Cfg::NS) & 1, p.plan.err);
   }

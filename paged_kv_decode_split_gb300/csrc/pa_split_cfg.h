@@ -49,7 +49,14 @@ struct SplitCfg {
   // ring slot's use u+1 before it consumed use u -- which keeps the
   // parity-based mbarrier waits unambiguous.
   static constexpr int NCW = WQ * WK * ND;            // consumer warps
-  static constexpr int THREADS = 32 * (1 + NCW);
+  // Producer warps.  A warp issues the copies of a stage one lane after the
+  // other, and each 2 KB box holds it for about 100 cycles, so one producer
+  // caps a CTA near 30 GB/s with 16-key pages -- below what its consumers
+  // take.  Two producers (K copies from one, V copies from the other) issue
+  // in parallel, for head dims up to 128 where the extra warp still leaves
+  // two CTAs per SM.
+  static constexpr int NPW = (D <= 128 && 32 * (2 + NCW) <= 224) ? 2 : 1;
+  static constexpr int THREADS = 32 * (NPW + NCW);
   static constexpr int TILE_BYTES = KS * ROW;         // one tensor, one stage
   static constexpr int BLOCK_BYTES = KS * SWB;        // one column block of a tile
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K then V
