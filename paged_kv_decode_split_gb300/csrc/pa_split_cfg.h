@@ -42,7 +42,11 @@ struct SplitCfg {
   static constexpr bool kTwoPerSm2 = 2 * (2 * 2 * KS * ROW + kFixedBytes + 1024) <= 228 * 1024;
   static constexpr int NS = (kWide && !kTwoPerSm3 && kTwoPerSm2) ? 2 : 3;  // ring depth
   static constexpr int MTS = KS / 16;                 // 16-key tiles per stage
-  static constexpr int WK0 = (WQ == 1) ? 4 : (WQ == 4 ? 1 : 2);
+  // Key warps per row group: 4 for one row group, 2 for two or three, 1 for
+  // four -- and 1 for three row groups of 256-dim heads (MTP verify: 18-24
+  // query rows), whose epilogue then needs no exchange between key warps
+  // (measured 7-10% faster there; 2-19% slower for two row groups or 128 dims).
+  static constexpr int WK0 = (WQ == 1) ? 4 : ((WQ == 4 || (D == 256 && WQ == 3)) ? 1 : 2);
   static constexpr int WK = WK0 < MTS ? WK0 : MTS;   // key warps per row group
   static constexpr int T = MTS / WK;                  // tiles one warp handles per stage
   // Every key warp consumes every stage, in order, so a warp never waits on a
