@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace pa {
 
 constexpr int kTile = 256;       // partition tile, tokens
@@ -14,6 +16,29 @@ constexpr int kStageTensorBytes = 16384;  // split kernel: K (or V) bytes per pi
 
 constexpr int kMinPieceTiles = 2;  // a slot is cut into pieces of at least this many tiles
 constexpr int kWarpMergePieces = 8;  // rows with at most this many pieces are merged by one warp
+
+// Launch set-up that every device needs once: a kernel's function attributes
+// (cudaFuncSetAttribute) and its occupancy belong to the device, so launchers
+// keep one entry per device ordinal -- 0 until set up, else the value + 1 --
+// for the current device.  Concurrent first calls both set up: idempotent.
+constexpr int kMaxDevices = 64;
+template <typename SetUp>
+inline cudaError_t per_device_once(std::atomic<int>* state, int& value, SetUp&& set_up) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  int v = state[dev].load(std::memory_order_acquire);
+  if (v == 0) {
+    int x = 0;
+    e = set_up(x);
+    if (e != cudaSuccess) return e;
+    v = x + 1;
+    state[dev].store(v, std::memory_order_release);
+  }
+  value = v - 1;
+  return cudaSuccess;
+}
 
 // Device buffers owned by one plan.
 //

@@ -475,16 +475,18 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
 }  // namespace
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
-  static bool attr_done = false;
+  // per device: the dynamic shared-memory limit of both planner shapes
+  static std::atomic<int> state[kMaxDevices];
   const int smem = 8 * kMaxSeqs * static_cast<int>(sizeof(int));
-  if (!attr_done) {
-    cudaError_t e =
+  int unused = 0;
+  const cudaError_t e = per_device_once(state, unused, [&](int&) {
+    cudaError_t r =
         cudaFuncSetAttribute(plan_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(plan_kernel<1024>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(plan_kernel<1024>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    return r;
+  });
+  if (e != cudaSuccess) return e;
   const int dyn = 8 * p.n * static_cast<int>(sizeof(int));
   if (p.n <= 128) return launch_pdl(plan_kernel<128>, dim3(1), dim3(128), dyn, s, p);
   return launch_pdl(plan_kernel<1024>, dim3(1), dim3(1024), dyn, s, p);

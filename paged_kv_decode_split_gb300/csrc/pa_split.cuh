@@ -924,19 +924,18 @@ cudaError_t launch_split_cfg(const SplitParams& p, const CUtensorMap& tk,
                              const CUtensorMap& tv, cudaStream_t s) {
   using Cfg = SplitCfg<D, KVT, WQ, KL>;
   auto kern = split_kernel<D, KVT, WQ, KL>;
-  // benign races: both calls are idempotent
-  static bool attr_done = false;
-  static int per_sm = 0;  // CTAs per SM, as the occupancy calculator sees the kernel
-  if (!attr_done) {
-    cudaError_t e =
+  // per device: the shared-memory attribute, then CTAs per SM as the
+  // occupancy calculator sees the kernel
+  static std::atomic<int> state[kMaxDevices];
+  int per_sm = 0;
+  const cudaError_t e = per_device_once(state, per_sm, [&](int& b) {
+    cudaError_t r =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    int b = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, Cfg::THREADS, Cfg::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    per_sm = b;
-    attr_done = true;
-  }
+    if (r == cudaSuccess)
+      r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, Cfg::THREADS, Cfg::SMEM_BYTES);
+    return r;
+  });
+  if (e != cudaSuccess) return e;
   SplitParams q = p;
   q.resident = per_sm > 0 && p.sms > 0 ? per_sm * p.sms : 0;
   const unsigned zero_ctas = static_cast<unsigned>((p.num_tokens + kZeroRows - 1) / kZeroRows);

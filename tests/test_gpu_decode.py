@@ -382,6 +382,36 @@ def test_nan_poisoned_unread_slots(dev, kv):
     check(w)
 
 
+GUARD = 0x7FC1  # a NaN in both bf16 and fp16
+
+
+@pytest.mark.parametrize("case", ["decode_bf16", "decode_fp8", "verify_d256", "wide_d1024",
+                                  "fp16_pieces"])
+def test_output_guard_regions(dev, case):
+    """The output sits inside a larger buffer whose every element holds a NaN
+    sentinel: after the call the elements before and after it are untouched
+    (no write out of bounds) and none inside it still holds the sentinel
+    (every row written: outputs, merged rows, zero rows of padding and empty
+    requests)."""
+    mk = {
+        "decode_bf16": lambda: batch(dev, [17, 300, 1000, 5000, 0], H=(8, 2), D=128),
+        "decode_fp8": lambda: batch(dev, [17, 300, 1000, 5000, 0], H=(32, 4), D=128, kv="fp8"),
+        "verify_d256": lambda: batch(dev, [600, 40, 3000, 2, 0], ql=[3, 3, 3, 3, 1], H=(6, 1),
+                                     D=256, bs=64, pad=5),
+        "wide_d1024": lambda: batch(dev, [700, 3000, 0], ql=[2, 1, 1], H=(16, 2), D=1024, pad=3),
+        "fp16_pieces": lambda: batch(dev, [9000, 64, 300], H=(8, 1), D=64, bs=64, kv="fp16",
+                                     q="fp16"),
+    }
+    w = mk[case]()
+    n, g = w.q.numel(), 4096
+    buf = torch.full((n + 2 * g,), GUARD, dtype=torch.int16, device=dev)
+    out = buf[g:g + n].view(w.q.dtype).view(w.q.shape)
+    kw = {"budget": 64} if case == "fp16_pieces" else {}
+    check(w, out=out, **kw)
+    assert torch.all(buf[:g] == GUARD) and torch.all(buf[g + n:] == GUARD), "write out of bounds"
+    assert not torch.any(buf[g:g + n] == GUARD), "output element never written"
+
+
 def test_deterministic(dev):
     w = wl.tiny(0, dev)
     a, _ = run(w)
