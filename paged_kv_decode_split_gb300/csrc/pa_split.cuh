@@ -469,6 +469,8 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
       lim[e] = (n < row_hi) ? min(ke_task, K) : kb;
       llo[e] = p.window > 0 ? max(0, K - p.window) : 0;
     }
+    const int vis_lo = max(llo[0], llo[1]);  // keys [vis_lo, vis_hi) are visible to both rows
+    const int vis_hi = min(lim[0], lim[1]);
 
     // Q^T as the B operand of QK^T: row n = groupID of this warp's 8 rows;
     // k-step ks of the slice is global k-step ks0 + ks.
@@ -634,15 +636,28 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
         // ---- online softmax (log2 domain), lazily rescaled
         float sv[T][4];
         float mx0 = NEG_INF, mx1 = NEG_INF;
+        // Both of this thread's rows see every key of the warp's T tiles on
+        // all but the boundary stages (range end, window start): no masks.
+        const int kw0 = key0 + rbase;
+        if (kw0 >= vis_lo && kw0 + 16 * T <= vis_hi) {
 #pragma unroll
-        for (int tt = 0; tt < T; ++tt) {
-          const int k_lo = key0 + rbase + 16 * tt + g;
-          sv[tt][0] = (k_lo < lim[0] && k_lo >= llo[0]) ? c[tt][0] * sl2 : NEG_INF;
-          sv[tt][1] = (k_lo < lim[1] && k_lo >= llo[1]) ? c[tt][1] * sl2 : NEG_INF;
-          sv[tt][2] = (k_lo + 8 < lim[0] && k_lo + 8 >= llo[0]) ? c[tt][2] * sl2 : NEG_INF;
-          sv[tt][3] = (k_lo + 8 < lim[1] && k_lo + 8 >= llo[1]) ? c[tt][3] * sl2 : NEG_INF;
-          mx0 = fmaxf(mx0, fmaxf(sv[tt][0], sv[tt][2]));
-          mx1 = fmaxf(mx1, fmaxf(sv[tt][1], sv[tt][3]));
+          for (int tt = 0; tt < T; ++tt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sv[tt][e] = c[tt][e] * sl2;
+            mx0 = fmaxf(mx0, fmaxf(sv[tt][0], sv[tt][2]));
+            mx1 = fmaxf(mx1, fmaxf(sv[tt][1], sv[tt][3]));
+          }
+        } else {
+#pragma unroll
+          for (int tt = 0; tt < T; ++tt) {
+            const int k_lo = kw0 + 16 * tt + g;
+            sv[tt][0] = (k_lo < lim[0] && k_lo >= llo[0]) ? c[tt][0] * sl2 : NEG_INF;
+            sv[tt][1] = (k_lo < lim[1] && k_lo >= llo[1]) ? c[tt][1] * sl2 : NEG_INF;
+            sv[tt][2] = (k_lo + 8 < lim[0] && k_lo + 8 >= llo[0]) ? c[tt][2] * sl2 : NEG_INF;
+            sv[tt][3] = (k_lo + 8 < lim[1] && k_lo + 8 >= llo[1]) ? c[tt][3] * sl2 : NEG_INF;
+            mx0 = fmaxf(mx0, fmaxf(sv[tt][0], sv[tt][2]));
+            mx1 = fmaxf(mx1, fmaxf(sv[tt][1], sv[tt][3]));
+          }
         }
 #pragma unroll
         for (int o = 4; o <= 16; o <<= 1) {
