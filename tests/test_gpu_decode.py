@@ -89,13 +89,17 @@ def test_split_count_sweep(dev, P, W, kv):
     assert d <= TOL[kv]
 
 
-@pytest.mark.parametrize("kv", ["bf16", "fp8"])
-def test_uneven_slots_run_as_pieces(dev, kv):
+@pytest.mark.parametrize("kv,bs,D", [("bf16", 16, 128), ("fp8", 16, 128), ("fp8", 128, 128),
+                                     ("bf16", 128, 64), ("fp16", 64, 64)])
+def test_uneven_slots_run_as_pieces(dev, kv, bs, D):
     """A small budget leaves one slot per request, one of them 150x longer than
     the rest: the split kernel runs that slot as several pieces, and the merge
-    combines them (the plan itself is unchanged)."""
-    w = batch(dev, [40000] + [300 + 37 * i for i in range(15)], H=(8, 2), D=128, kv=kv, seed=12,
-              budget=32)
+    combines them (the plan itself is unchanged).  CTAs take several pieces
+    each, so the next piece's first stages are issued during the epilogue; with
+    16-key pages both producer warps issue, with pages that hold a whole stage
+    (fp8 at 128 keys, 64-dim bf16 at 128 keys) warp 0 issues K and V alone."""
+    w = batch(dev, [40000] + [300 + 37 * i for i in range(15)], H=(8, 2), D=D, bs=bs, kv=kv,
+              q="fp16" if kv == "fp16" else "bf16", seed=12, budget=32)
     out, plan = run(w)
     work, red = plan.download()
     assert bool((red[:, 1] == 1).all())  # one partition per request: pieces are not partitions
