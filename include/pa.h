@@ -69,7 +69,10 @@
  * every tensor.  A plan owns its device buffers, allocated only by
  * pa_plan_build and released by pa_plan_destroy; pa_plan_refresh and
  * pa_decode never allocate and never wait on the host, so both may be
- * captured in a CUDA graph.  One plan may be in flight on one stream at a time
+ * captured in a CUDA graph.  The first launch of each kernel shape on a device
+ * sets that kernel's shared-memory limit and reads its occupancy there (host
+ * calls, no stream work; kept per device ordinal, safe from several threads).
+ * One plan may be in flight on one stream at a time
  * (its partial-result scratch is per plan).  pa_plan_refresh must run after
  * every change of context_lens or cu_query_lens and before the pa_decode
  * calls that use it; pa_decode detects a plan refreshed from other lengths and
