@@ -25,10 +25,10 @@
 //    ring of NS stages (32 KB up to head_dim 256; one 16-key tile of K and V
 //    for wider heads), completion counted in bytes on an mbarrier;
 //  * up to head_dim 128 a second producer warp splits that work (warp 0 the
-//    K copies, warp 1 the V copies, each walking the block table itself): a
-//    warp issues its lanes' copies one after the other, about 100 cycles per
-//    2 KB box, which alone held a CTA near 30 GB/s -- what a CTA left alone
-//    at the end of a skewed batch streams at;
+//    K copies, warp 1 the V copies, each walking the block table itself):
+//    issuing holds a warp for about 100-140 cycles per 2 KB box, which kept
+//    a CTA left alone at the end of a skewed batch near 25 GB/s; the two
+//    warps share a per-CTA limit but overlap enough for about 20% more;
 //  * consumer warps form (row group wq) x (key warp wk); every consumer warp
 //    takes part in every stage (its key slice: T 16-key tiles handled
 //    together -- independent MMA chains, one softmax reduction), so each warp

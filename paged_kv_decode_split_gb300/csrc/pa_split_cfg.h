@@ -53,12 +53,13 @@ struct SplitCfg {
   // ring slot's use u+1 before it consumed use u -- which keeps the
   // parity-based mbarrier waits unambiguous.
   static constexpr int NCW = WQ * WK * ND;            // consumer warps
-  // Producer warps.  A warp issues the copies of a stage one lane after the
-  // other, and each 2 KB box holds it for about 100 cycles, so one producer
-  // caps a CTA near 30 GB/s with 16-key pages -- below what its consumers
-  // take.  Two producers (K copies from one, V copies from the other) issue
-  // in parallel, for head dims up to 128 where the extra warp still leaves
-  // two CTAs per SM.
+  // Producer warps.  Issuing a stage's copies (one per lane) holds a warp
+  // for about 100-140 cycles per 2 KB box, which capped a lone CTA near
+  // 25 GB/s with 16-key pages.  Two producers (K copies from one, V copies
+  // from the other) overlap that work -- they still share a per-CTA limit
+  // of about 110-120 cycles per box, so a lone CTA gains about 20%, not 2x --
+  // for head dims up to 128, where the extra warp still leaves two CTAs per
+  // SM.
   static constexpr int NPW = (D <= 128 && 32 * (2 + NCW) <= 224) ? 2 : 1;
   static constexpr int THREADS = 32 * (NPW + NCW);
   static constexpr int TILE_BYTES = KS * ROW;         // one tensor, one stage
