@@ -3,19 +3,24 @@
 One step = one pass of the whole hot path over one synthetic batch: the plan
 refresh (planner kernel), the split-KV decode kernel and the merge kernel, all
 through the C ABI, captured in a CUDA graph and replayed.  The headline workload
-is the uniform decode batch (32 seqs x 8192 context, Hq/Hkv 32/4, D 128, page
-16, bf16); its 537 MB of KV per step is larger than the 129 MB L2, so no flush
+is the largest single-GPU batch, the Large skewed batch (512 seqs, context
+lognormal(median 2048, sigma 1.2) in [16, 65536], Hq/Hkv 64/8, D 128, page 128,
+bf16); its ~8.6 GB of KV per step is far larger than the 129 MB L2, so no flush
 is needed between steps.
 
 Prints one JSON line (rank 0).  `value` is the algorithmic KV-read bandwidth,
 sum_r S_r * Hkv * D * 2 (K and V) * elem_bytes per step, over the measured step
 time; `us_per_decode_call` is the pa_decode call (split + merge, the refresh
-excluded; a graph of K calls) and `us_per_refresh` the refresh alone.  `--sweep all` adds
-one line per configuration (L2 flushed before every step) and a summary over the
-skewed batch's seeds.
+excluded; a graph of K calls) and `us_per_refresh` the refresh alone.  With the
+default workload the same line also carries the Large batch with an fp8 cache
+(`large_fp8`) and the skewed agentic batch over --seeds seeds (`skewed_seeds`:
+median / p10 fraction of the measured HBM copy peak, and the uniform-split
+plan's time over the proportional plan's on the same kernel, L2 flushed before
+every step).  `--sweep all` adds one line per configuration (L2 flushed before
+every step) and a summary over the skewed batch's seeds.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
-                  [--workload NAME] [--sweep]
+                  [--workload NAME] [--seeds S] [--sweep]
 """
 from __future__ import annotations
 
@@ -39,7 +44,7 @@ from paged_kv_decode_split_gb300 import binding, workloads as wl  # noqa: E402
 
 METRIC = "paged-decode KV-read GB/s vs ~8 TB/s HBM roofline; µs per decode call"
 UNIT = "GB/s"
-DEFAULT_WORKLOAD = "uniform"
+DEFAULT_WORKLOAD = "large_bf16"
 DESCRIBE = {
     "tiny": "tiny decode: 4 seqs, ctx {17,64,200,1000}, Hq/Hkv 8/2, D 64, page 16, bf16",
     "uniform": "uniform decode: 32 seqs x 8192 ctx, Hq/Hkv 32/4, D 128, page 16, bf16",
@@ -192,31 +197,30 @@ def max_over_ranks(x: float, world: int) -> float:
 # -------------------------------------------------------------- CPU oracle
 
 def oracle_sample(w, max_seconds: float = 20.0):
-    """Times the fp64 oracle on a bounded sample of the workload's requests.
+    """Times the fp64 oracle on a bounded sample of the workload's requests: a
+    first request calibrates its speed, then requests are taken in order while
+    the estimated cost stays under half the budget.
     Returns (KV GB/s, seconds, cores, description)."""
-    import numpy as np
     import oracle
 
-    lens = w.context_lens.cpu().tolist()
-    # grow the sample one request at a time until its estimated cost reaches
-    # ~1/4 of the budget (first call calibrates the per-byte speed)
-    order = list(range(len(lens)))
-    picks = [order[0]]
+    per_req = w.kv_bytes_per_request().tolist()
+    n = len(per_req)
+    sub = wl.subset(w, [0])
+    t0 = time.perf_counter()
+    _run_oracle(sub)
+    dt = time.perf_counter() - t0
+    per_byte = dt / max(1, per_req[0])
+    picks, total = [0], per_req[0]
+    for r in range(1, n):
+        if per_byte * (total + per_req[r]) >= max_seconds / 2:
+            break
+        picks.append(r)
+        total += per_req[r]
     sub = wl.subset(w, picks)
     t0 = time.perf_counter()
     _run_oracle(sub)
     dt = time.perf_counter() - t0
-    per_byte = dt / max(1, sub.kv_bytes())
-    target = max_seconds / 2
-    i = 1
-    while i < len(order) and per_byte * wl.subset(w, picks + [order[i]]).kv_bytes() < target:
-        picks.append(order[i])
-        i += 1
-    sub = wl.subset(w, picks)
-    t0 = time.perf_counter()
-    _run_oracle(sub)
-    dt = time.perf_counter() - t0
-    desc = (f"{len(picks)} of {len(lens)} requests ({sub.kv_bytes() / 1e6:.1f} MB of "
+    desc = (f"{len(picks)} of {n} requests ({sub.kv_bytes() / 1e6:.1f} MB of "
             f"{w.kv_bytes() / 1e6:.1f} MB KV), all query rows and heads, fp64")
     return sub.kv_bytes() / dt / 1e9, dt, oracle.num_threads(), desc
 
@@ -381,16 +385,21 @@ def time_refresh(w, reps: int = 100) -> float:
     return ms * 1e3 / reps
 
 
-def time_e2e(w, steps: int, warmup: int):
+def time_e2e(w, steps: int, warmup: int, kv_resident: bool = False):
     """Same metric through the public API with host-resident inputs: every step
-    copies q, K, V, block tables, lengths (and cu) from pinned host memory, runs
-    refresh + decode, and reads the output back.  As a serving engine overlaps
-    the next batch's upload with the current batch's attention, the copies of
-    step i+1 run on a copy stream into the other of two device buffer sets
-    while step i decodes; the timed region spans the first upload to the last
-    read-back."""
+    copies the step's inputs from pinned host memory, runs refresh + decode, and
+    reads the output back.  kv_resident=False copies everything -- q, K, V,
+    block tables, lengths (and cu); kv_resident=True copies what changes from
+    one decode step to the next in a serving engine -- q, block tables, lengths
+    (and cu) -- while the paged KV cache stays in HBM.  As a serving engine
+    overlaps the next batch's upload with the current batch's attention, the
+    copies of step i+1 run on a copy stream into the other of two device buffer
+    sets while step i decodes; the timed region spans the first upload to the
+    last read-back."""
     dev = w.q.device
-    names = ["q", "k_cache", "v_cache", "block_tables", "context_lens"]
+    names = ["q", "block_tables", "context_lens"]
+    if not kv_resident:
+        names[1:1] = ["k_cache", "v_cache"]
     if w.cu_query_lens is not None:
         names.append("cu_query_lens")
     host = {n: getattr(w, n).cpu().pin_memory() for n in names}
@@ -441,6 +450,7 @@ def time_e2e(w, steps: int, warmup: int):
     ms = t0.elapsed_time(t1) / steps
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_h.numel() * out_h.element_size()
+    del host, sets, wds, outs
     return ms, h2d, d2h
 
 
@@ -451,6 +461,55 @@ def workload_dtype(w) -> str:
 
 # ------------------------------------------------------------------ arms
 
+def plan_ab(w, steps: int, warmup: int, flush: bool, peak: float) -> dict:
+    """The proportional and the uniform-split plan on the same kernel and batch:
+    decode call and split kernel times, and their fractions of the copy peak."""
+    kv = w.kv_bytes()
+    tp, _ = time_native(w, steps, warmup, flush=flush)
+    tu, _ = time_native(w, steps, warmup, kind=binding.UNIFORM, flush=flush)
+    gbs = lambda ms: kv / (ms * 1e-3) / 1e9
+    return {"kv_bytes": kv,
+            "us_per_decode_call": round(tp["call_ms"] * 1e3, 2),
+            "split_us": round(tp["split_ms"] * 1e3, 2),
+            "call_gbs": round(gbs(tp["call_ms"]), 1),
+            "call_frac_of_measured": round(gbs(tp["call_ms"]) / peak, 4),
+            "split_frac_of_measured": round(gbs(tp["split_ms"]) / peak, 4),
+            "uniform_us_per_decode_call": round(tu["call_ms"] * 1e3, 2),
+            "uniform_split_us": round(tu["split_ms"] * 1e3, 2),
+            "uniform_over_proportional_call": round(tu["call_ms"] / tp["call_ms"], 3),
+            "uniform_over_proportional_split": round(tu["split_ms"] / tp["split_ms"], 3)}
+
+
+def skewed_seeds(dev, seeds: int, steps: int, warmup: int, peak: float) -> dict:
+    """The skewed agentic batch over seeds 0..seeds-1 (each a fresh length draw,
+    cache and page order), both plans on the same kernel, L2 flushed before
+    every step: medians and tails of the fractions of the copy peak and of the
+    uniform plan's time over the proportional plan's."""
+    rows = []
+    for seed in range(seeds):
+        w = wl.skewed(seed, dev)
+        r = plan_ab(w, steps, warmup, True, peak)
+        r["seed"] = seed
+        r["max_over_min"] = round(w.meta["max_over_min"], 1)
+        rows.append(r)
+        del w
+        torch.cuda.empty_cache()
+    col = lambda k: [r[k] for r in rows]
+    stat = lambda xs: {"median": _pct(xs, 0.5), "p10": _pct(xs, 0.1), "min": min(xs),
+                       "max": max(xs)}
+    return {"workload": DESCRIBE["skewed"], "seeds": seeds,
+            "l2": "flushed before every step (write a 2xL2 buffer, read another)",
+            "max_over_min": stat(col("max_over_min")),
+            "call_frac_of_measured": stat(col("call_frac_of_measured")),
+            "split_frac_of_measured": stat(col("split_frac_of_measured")),
+            "us_per_decode_call": stat(col("us_per_decode_call")),
+            "uniform_over_proportional_call": stat(col("uniform_over_proportional_call")),
+            "uniform_over_proportional_split": stat(col("uniform_over_proportional_split")),
+            "per_seed": [{k: r[k] for k in ("seed", "max_over_min", "us_per_decode_call",
+                                            "uniform_us_per_decode_call",
+                                            "call_frac_of_measured")} for r in rows]}
+
+
 def run_native(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -460,6 +519,7 @@ def run_native(args, world, rank, local):
         if rank == 0:
             sweep(args)
         return
+    t_start = time.perf_counter()
     w = wl.CONFIGS[args.workload](0, dev)
     kv_bytes = w.kv_bytes()
     sampler = ClockSampler(dev) if rank == 0 else None
@@ -471,6 +531,8 @@ def run_native(args, world, rank, local):
     refresh_us = time_refresh(w)
     e2e_ms, h2d, d2h = time_e2e(w, args.steps, args.warmup)
     e2e_ms = max_over_ranks(e2e_ms, world)
+    res_ms, res_h2d, res_d2h = time_e2e(w, args.steps, args.warmup, kv_resident=True)
+    res_ms = max_over_ranks(res_ms, world)
     peaks = measured_peaks()
     peak = peaks.get("hbm_gbs")
     peak_kind = "measured" if peak else "fallback"
@@ -510,14 +572,34 @@ def run_native(args, world, rank, local):
                     "uniform_split_us": round(tu["split_ms"] * 1e3, 2)},
         "e2e": {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_ms, 4)},
+                "ms_per_step": round(e2e_ms, 4),
+                "inputs": "q, K and V caches, block tables, lengths uploaded every step"},
+        "e2e_kv_resident": {"value": round(world * kv_bytes / (res_ms * 1e-3) / 1e9, 1),
+                            "unit": UNIT, "h2d_bytes_per_step": res_h2d,
+                            "d2h_bytes_per_step": res_d2h, "ms_per_step": round(res_ms, 4),
+                            "inputs": "q, block tables, lengths uploaded every step; the paged "
+                                      "KV cache stays in HBM"},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
     }
+    del w, plan
+    torch.cuda.empty_cache()
+    if args.workload == DEFAULT_WORKLOAD and rank == 0 and not args.no_extra:
+        wf = wl.CONFIGS["large_fp8"](0, dev)
+        line["large_fp8"] = {"workload": DESCRIBE["large_fp8"],
+                             **plan_ab(wf, args.steps, args.warmup, False, peak)}
+        del wf
+        torch.cuda.empty_cache()
+        if args.seeds > 0:
+            line["skewed_seeds"] = skewed_seeds(dev, args.seeds, min(args.steps, 50),
+                                                args.warmup, peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        gbs, secs, cores, desc = oracle_sample(w)
+        w = wl.CONFIGS[args.workload](0, dev)
+        gbs, secs, cores, desc = oracle_sample(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(gbs, 4), "unit": UNIT, "cores": cores,
                                 "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
+        del w
+    line["wall_s"] = round(time.perf_counter() - t_start, 1)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if args.sweep and rank == 0:
@@ -594,7 +676,10 @@ def run_reference(args, world, rank, local):
         return
     import oracle
     oracle.build()
-    w = wl.CONFIGS[args.workload](0, "cpu")
+    # the inputs are drawn where they are drawn for the native arm (the same
+    # seeded batch); only the sampled request is copied to the host and timed
+    gen = torch.device("cuda", local) if torch.cuda.is_available() else "cpu"
+    w = wl.CONFIGS[args.workload](0, gen)
     lens = w.context_lens.tolist()
     # one request per step (the first), all its query rows and heads
     sub = wl.subset(w, [0])
@@ -631,6 +716,10 @@ def main(argv=None):
     ap.add_argument("--sweep-only", action="store_true",
                     help="print the --sweep lines only (no headline line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0,
+                    help="bound on the oracle's timed sample (cpu_baseline)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="headline workload only (no large_fp8 / skewed_seeds keys)")
     args = ap.parse_args(argv)
     world, rank, local = dist_setup()
     if args.impl == "reference":

@@ -132,8 +132,9 @@ enum pa_plan_kind { PA_PLAN_PROPORTIONAL = 0, PA_PLAN_UNIFORM = 1 };
 
 typedef struct pa_plan pa_plan; /* opaque */
 
-/* Creates a plan for batches of exactly num_seqs requests on device `device`
- * and allocates its device buffers: work_info, reduce_info, the per-request
+/* Creates a plan for batches of exactly num_seqs requests, num_kv_heads kv
+ * heads and num_q_heads query heads (in that order) on device `device` and
+ * allocates its device buffers: work_info, reduce_info, the per-request
  * snapshot of query lengths, the error word, and fp32 partial-result scratch
  * sized for at most max_query_len query rows per request and max_tokens rows
  * per call.  max_partitions <= 0 selects 256; budget <= 0 selects
@@ -144,7 +145,7 @@ typedef struct pa_plan pa_plan; /* opaque */
  * gate, review item 5).  Returns PA_ERR_OOM / PA_ERR_CUDA on device
  * failures (nothing is leaked), PA_ERR_INVALID_ARG / PA_ERR_UNSUPPORTED on bad
  * parameters.  On success *plan owns the buffers until pa_plan_destroy. */
-int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_q_heads, int num_kv_heads,
+int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_kv_heads, int num_q_heads,
                   int head_dim, int max_query_len, int max_tokens, int max_partitions, int budget,
                   int kind);
 
@@ -255,9 +256,9 @@ int pa_sparse_select(const float* block_scores, int score_stride, const int32_t*
  * call that allocates no device memory.  The source pages have no counterpart:
  * it exists for callers that cannot call cudaMalloc while decoding -- a serving
  * engine that hands nearly all HBM to its own KV-cache pool and caching
- * allocator, or code running inside a CUDA-graph capture -- and so cannot
- * create a pa_plan.  It has no sliding window and no sinks, and takes K in
- * the PA_K_ROWS layout.
+ * allocator at start-up, or a runtime that may not allocate device memory once
+ * it serves -- and so cannot create a pa_plan.  It has no sliding window and no
+ * sinks, and takes K in the PA_K_ROWS layout.
  *
  * Arguments mean what they mean for pa_plan_build and pa_decode; the plan
  * parameters (max_query_len, max_partitions, budget, kind) are passed per call
@@ -280,8 +281,8 @@ int pa_sparse_select(const float* block_scores, int score_stride, const int32_t*
  * The first call on a device looks up the array's device address there (with
  * that device current), so make it before any stream capture.  Every call
  * shares the array and it keeps the last call's contents: calls whose GPU work
- * can overlap (several streams, threads or concurrently replayed graphs) race
- * and must be serialised by the caller.  Never calls cudaMalloc or cudaFree. */
+ * can overlap (several streams or threads) race and must be serialised by the
+ * caller.  Never calls cudaMalloc or cudaFree. */
 int pa_decode_static(const void* q, int q_dtype, int num_tokens, int num_q_heads, int head_dim,
                      const void* k_cache, const void* v_cache, int kv_dtype, float k_scale,
                      float v_scale, int num_blocks, int num_kv_heads, int block_size,
@@ -298,9 +299,11 @@ int pa_plan_info(const pa_plan* plan, int* capacity, int* num_seqs, int* budget,
 
 /* Copies the current work_info (capacity x 4 int32) and reduce_info
  * (num_seqs x 2 int32) to host memory, ordered after prior work on `stream`,
- * and waits for the copy (synchronises `stream`; not capturable).  Either
- * destination may be NULL.  For tests and diagnostics. */
-int pa_plan_download(const pa_plan* plan, int32_t* work_info, int32_t* reduce_info, void* stream);
+ * and waits for the copy (synchronises `stream`; not capturable); *capacity
+ * receives C, the rows of work_info.  Any of the three destinations may be
+ * NULL.  For tests and diagnostics. */
+int pa_plan_download(const pa_plan* plan, int32_t* work_info, int32_t* reduce_info, int* capacity,
+                     void* stream);
 
 /* Reads the plan's sticky device error word (PA_DEVERR_* bits) into *errors,
  * ordered after prior work on `stream`; waits for it (synchronises `stream`;

@@ -69,7 +69,7 @@ def load() -> ctypes.CDLL:
     lib.pa_plan_info.argtypes = [P, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                  ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32),
                                  ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_longlong)]
-    lib.pa_plan_download.argtypes = [P, P, P, P]
+    lib.pa_plan_download.argtypes = [P, P, P, ctypes.POINTER(i32), P]
     lib.pa_plan_read_errors.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), i32, P]
     lib.pa_plan_set_split_events.argtypes = [P, P, P]
     lib.pa_plan_set_call_events.argtypes = [P, P, P]
@@ -147,8 +147,8 @@ class Plan:
         self.head_dim, self.max_query_len = head_dim, max_query_len
         self.max_tokens = max_tokens if max_tokens is not None else num_seqs * max_query_len
         h = ctypes.c_void_p()
-        _check(lib.pa_plan_build(ctypes.byref(h), self.device.index, num_seqs, num_q_heads,
-                                 num_kv_heads, head_dim, max_query_len, self.max_tokens,
+        _check(lib.pa_plan_build(ctypes.byref(h), self.device.index, num_seqs, num_kv_heads,
+                                 num_q_heads, head_dim, max_query_len, self.max_tokens,
                                  max_partitions, budget, kind), "pa_plan_build")
         self._h = h
         self.with_cu = None
@@ -182,8 +182,10 @@ class Plan:
         C = self.capacity
         work = torch.empty((C, 4), dtype=torch.int32)
         red = torch.empty((self.num_seqs, 2), dtype=torch.int32)
-        _check(load().pa_plan_download(self._h, _ptr(work), _ptr(red),
+        cap = ctypes.c_int(-1)
+        _check(load().pa_plan_download(self._h, _ptr(work), _ptr(red), ctypes.byref(cap),
                                        _stream(self.device, stream)), "pa_plan_download")
+        assert cap.value == C
         return work, red
 
     def read_errors(self, clear: bool = True, stream=None) -> int:

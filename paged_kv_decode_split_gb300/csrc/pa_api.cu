@@ -166,6 +166,51 @@ PlanDev carve_plan(char* c, const PlanLayout& l) {
   return d;
 }
 
+// TMA view of a cache [num_blocks, Hkv, bs, D] as a 2-D tensor of
+// num_blocks*Hkv*bs rows x D elements; boxes of split_box_rows() rows x one
+// swizzle span (128 bytes, or 64 for a 64-byte row), swizzled to match the
+// split kernel's shared-memory layout.  grouped: a K cache
+// [num_blocks, Hkv, D/16, bs, 16] as the 3-D tensor
+// {128 bytes, bs * 16 * elem / 128, num_blocks * Hkv * D/16} (innermost first):
+// rows of 128 bytes, each 4 (fp8: 8) consecutive keys of one 16-dim group; one
+// box is 16 keys of every group of one page and head, 128-byte swizzled.
+// Every path that launches the split kernel encodes its maps here.
+bool encode_cache_tmap(const void* ptr, int num_blocks, int Hkv, int bs, int D, int dtype,
+                       bool grouped, CUtensorMap* out) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const int esz = dtype == PA_FP8_E4M3 ? 1 : 2;
+  const int swb = split_box_row_bytes(D, dtype);
+  const cuuint32_t rows = static_cast<cuuint32_t>(split_box_rows(D, dtype, bs));
+  CUtensorMapDataType dt = dtype == PA_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                           : dtype == PA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                              : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  CUresult r;
+  if (grouped) {
+    const cuuint64_t kpr = 128 / (16 * esz);  // keys per 128-byte row
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(128 / esz), bs / kpr,
+                          static_cast<cuuint64_t>(num_blocks) * Hkv * (D / 16)};
+    cuuint64_t strides[2] = {128, 128 * (bs / kpr)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(16 / kpr),
+                         static_cast<cuuint32_t>(D / 16)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    r = fn(out, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(D),
+                          static_cast<cuuint64_t>(num_blocks) * Hkv * bs};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * esz};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(swb / esz), rows};
+    cuuint32_t estr[2] = {1, 1};
+    r = fn(out, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE,
+           swb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  return r == CUDA_SUCCESS;
+}
+
 cudaError_t launch_split(const SplitParams& p, int D, int kv_dtype, int row_groups, int k_layout,
                          const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s) {
   const bool gk = k_layout == PA_K_GROUPED;
@@ -189,13 +234,8 @@ cudaError_t launch_split(const SplitParams& p, int D, int kv_dtype, int row_grou
 
 namespace {
 
-// TMA view of a cache [num_blocks, Hkv, bs, D] as a 2-D tensor of
-// num_blocks*Hkv*bs rows x D elements; boxes of box_rows rows x one swizzle
-// span (128 bytes, or 64 for a 64-byte row), swizzled to match the kernel.
-// grouped: a K cache [num_blocks, Hkv, D/16, bs, 16] as the 3-D tensor
-// {128 bytes, bs * 16 * elem / 128, num_blocks * Hkv * D/16} (innermost first):
-// rows of 128 bytes, each 4 (fp8: 8) consecutive keys of one 16-dim group; one
-// box is 16 keys of every group of one page and head, 128-byte swizzled.
+// Returns the cached tensor map of this cache view, or encodes one
+// (pa::encode_cache_tmap) and keeps it in the plan's small cache.
 int make_tmap(pa_plan* plan, const void* ptr, int num_blocks, int Hkv, int bs, int D, int dtype,
               int grouped, CUtensorMap* out) {
   for (auto& s : plan->tmaps) {
@@ -205,39 +245,9 @@ int make_tmap(pa_plan* plan, const void* ptr, int num_blocks, int Hkv, int bs, i
       return PA_OK;
     }
   }
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return PA_ERR_CUDA;
-  const int esz = dtype == PA_FP8_E4M3 ? 1 : 2;
-  const int swb = pa::split_box_row_bytes(D, dtype);
-  const cuuint32_t rows = static_cast<cuuint32_t>(pa::split_box_rows(D, dtype, bs));
-  CUtensorMapDataType dt = dtype == PA_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                           : dtype == PA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                              : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   CUtensorMap m;
-  CUresult r;
-  if (grouped) {
-    const cuuint64_t kpr = 128 / (16 * esz);  // keys per 128-byte row
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(128 / esz), bs / kpr,
-                          static_cast<cuuint64_t>(num_blocks) * Hkv * (D / 16)};
-    cuuint64_t strides[2] = {128, 128 * (bs / kpr)};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(16 / kpr),
-                         static_cast<cuuint32_t>(D / 16)};
-    cuuint32_t estr[3] = {1, 1, 1};
-    r = fn(&m, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  } else {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(D),
-                          static_cast<cuuint64_t>(num_blocks) * Hkv * bs};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * esz};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(swb / esz), rows};
-    cuuint32_t estr[2] = {1, 1};
-    r = fn(&m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE,
-           swb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  }
-  if (r != CUDA_SUCCESS) return PA_ERR_CUDA;
+  if (!pa::encode_cache_tmap(ptr, num_blocks, Hkv, bs, D, dtype, grouped != 0, &m))
+    return PA_ERR_CUDA;
   TmapSlot& s = plan->tmaps[plan->tmap_next];
   plan->tmap_next = (plan->tmap_next + 1) % 8;
   s.valid = true;
@@ -269,7 +279,7 @@ const char* pa_status_string(int status) {
   }
 }
 
-int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_q_heads, int num_kv_heads,
+int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_kv_heads, int num_q_heads,
                   int head_dim, int max_query_len, int max_tokens, int max_partitions, int budget,
                   int kind) {
   if (!plan) return PA_ERR_INVALID_ARG;
@@ -515,8 +525,10 @@ int pa_plan_info(const pa_plan* plan, int* capacity, int* num_seqs, int* budget,
   return PA_OK;
 }
 
-int pa_plan_download(const pa_plan* plan, int32_t* work_info, int32_t* reduce_info, void* stream) {
+int pa_plan_download(const pa_plan* plan, int32_t* work_info, int32_t* reduce_info, int* capacity,
+                     void* stream) {
   if (!plan) return PA_ERR_INVALID_ARG;
+  if (capacity) *capacity = plan->C;
   DeviceGuard guard(plan->device);
   if (!guard.ok) return PA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -134,6 +134,12 @@ constexpr int split_max_row_groups(int D) { return D <= 256 ? 4 : (D <= 512 ? 2 
 int split_box_rows(int D, int kv_dtype, int bs);
 // Bytes of one box row (the swizzle span): min(128, D * elem_bytes).
 int split_box_row_bytes(int D, int kv_dtype);
+// TMA descriptor of a K or V cache view for the split kernel (grouped: K in
+// [num_blocks, Hkv, D/16, bs, 16]); false if the driver rejects it.  The one
+// encoder every launch path uses, so the boxes and swizzle always match the
+// kernel's shared-memory layout.
+bool encode_cache_tmap(const void* ptr, int num_blocks, int Hkv, int bs, int D, int dtype,
+                       bool grouped, CUtensorMap* out);
 // Query-row groups of 8 handled per pass for a plan with this max query length.
 int split_row_groups(int max_qlen, int G, int D);
 // Upper bound on the extra (slot, row chunk) items a plan with these limits can list.

@@ -3,10 +3,11 @@
 //
 // Who needs it: callers that cannot call cudaMalloc at decode time.  A serving
 // engine typically hands (almost) all HBM to its own KV-cache pool and caching
-// allocator at start-up, so a library allocation either fails or fragments that
-// pool; code running while a CUDA graph is being captured may not allocate
-// either (cudaMalloc is not a stream operation and would not be replayed).  Such
-// callers cannot create a pa_plan, whose device buffers come from pa_plan_build.
+// allocator at start-up, so a library allocation either fails outright or
+// carves into memory the engine has already promised to its KV pages; an
+// embedded runtime may not be allowed to allocate device memory at all once it
+// is serving.  Such callers cannot create a pa_plan, whose device buffers come
+// from pa_plan_build.
 //
 // Instead, the plan arrays and the fp32 partial results live in one file-scope
 // __device__ array of PA_STATIC_SCRATCH_BYTES.  Every GPU on which this module is
@@ -19,8 +20,8 @@
 // All calls share the one array and it keeps the last call's contents.  Each
 // call rewrites the whole plan before using it and clears the error word it
 // uses, so nothing stale is read; but calls whose work overlaps on the GPU
-// (other streams, other threads, or a captured graph replaying concurrently)
-// race on the array and must be serialised by the caller.
+// (other streams or other threads) race on the array and must be serialised by the caller.  The tensor maps of
+// the caches come from pa::encode_cache_tmap, the encoder pa_decode uses.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -49,47 +50,6 @@ void* scratch_address(int device) {
     g_addr[device] = p;
   }
   return g_addr[device];
-}
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn static_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  });
-  return fn;
-}
-
-// The same TMA view of a cache as pa_decode uses (rows x D, 128/64-byte
-// swizzled boxes), encoded on the host for this call.
-bool encode_cache(const void* ptr, int num_blocks, int Hkv, int bs, int D, int dtype,
-                  CUtensorMap* m) {
-  EncodeTiledFn fn = static_encode_fn();
-  if (!fn) return false;
-  const int esz = dtype == PA_FP8_E4M3 ? 1 : 2;
-  const int swb = pa::split_box_row_bytes(D, dtype);
-  CUtensorMapDataType dt = dtype == PA_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                           : dtype == PA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                              : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(num_blocks) * Hkv * bs};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * esz};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(swb / esz),
-                       static_cast<cuuint32_t>(pa::split_box_rows(D, dtype, bs))};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE,
-            swb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -163,8 +123,10 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
     return PA_ERR_CUDA;
 
   CUtensorMap tk, tv;
-  if (!encode_cache(k_cache, num_blocks, num_kv_heads, block_size, head_dim, kv_dtype, &tk) ||
-      !encode_cache(v_cache, num_blocks, num_kv_heads, block_size, head_dim, kv_dtype, &tv))
+  if (!pa::encode_cache_tmap(k_cache, num_blocks, num_kv_heads, block_size, head_dim, kv_dtype,
+                             false, &tk) ||
+      !pa::encode_cache_tmap(v_cache, num_blocks, num_kv_heads, block_size, head_dim, kv_dtype,
+                             false, &tv))
     return PA_ERR_CUDA;
 
   // ---- plan, split, merge

@@ -65,10 +65,10 @@ class Workload:
     def kv_elem_bytes(self) -> int:
         return 1 if self.kv_dtype == "fp8" else 2
 
-    def kv_bytes(self) -> int:
-        """Algorithmic KV bytes of one decode call: every key and value row a
-        request's tokens can see, per (request, kv head), read once (under a
-        sliding window W: the last W + L - 1 keys of a request with L tokens)."""
+    def kv_bytes_per_request(self) -> torch.Tensor:
+        """Algorithmic KV bytes of each request (int64, CPU): every key and
+        value row its tokens can see, per kv head, read once (under a sliding
+        window W: the last W + L - 1 keys of a request with L tokens)."""
         lens = self.context_lens.clamp(min=0).to(torch.int64).cpu()
         if self.window > 0:
             if self.cu_query_lens is None:
@@ -78,8 +78,11 @@ class Workload:
                 L = cu[1:] - cu[:-1]
             lens = torch.minimum(lens, self.window + L - 1)
             lens[L == 0] = 0
-        s = int(lens.sum().item())
-        return s * self.num_kv_heads * self.head_dim * 2 * self.kv_elem_bytes
+        return lens * self.num_kv_heads * self.head_dim * 2 * self.kv_elem_bytes
+
+    def kv_bytes(self) -> int:
+        """Algorithmic KV bytes of one decode call (kv_bytes_per_request summed)."""
+        return int(self.kv_bytes_per_request().sum().item())
 
     def to(self, device) -> "Workload":
         mv = lambda t: None if t is None else t.to(device)
@@ -124,10 +127,14 @@ def make_batch(name: str, context_lens: Sequence[int], query_lens: Optional[Sequ
                pool_pages: Optional[int] = None, pad_tokens: int = 0,
                kv_scale: float = 0.05, scale: Optional[float] = None, device="cpu",
                budget: Optional[int] = None, max_partitions: int = 256,
-               spare_blocks: int = 0) -> Workload:
+               spare_blocks: int = 0, q_std: float = 1.0) -> Workload:
     """A paged batch.  query_lens=None means one query token per request and no
     cu_query_lens; otherwise cu_query_lens is the running sum of query_lens and
-    pad_tokens graph-padding rows follow the last request's rows."""
+    pad_tokens graph-padding rows follow the last request's rows.  q is drawn
+    N(0, q_std^2): q_std = 1 gives logits of about unit spread (a nearly flat
+    softmax over a long context); a larger q_std (e.g. 6) gives sharp
+    attention, dominated by a few keys, whose outputs stay of order 1 however
+    long the context."""
     n = len(context_lens)
     g = _gen(seed, device)
     gc = _gen(seed + 7919, "cpu")
@@ -154,8 +161,8 @@ def make_batch(name: str, context_lens: Sequence[int], query_lens: Optional[Sequ
         num_tokens = int(cu[-1]) + pad_tokens
 
     qdt = {"bf16": torch.bfloat16, "fp16": torch.float16}[q_dtype]
-    q = torch.randn((num_tokens, num_q_heads, head_dim), generator=g, device=device,
-                    dtype=torch.float32).to(qdt)
+    q = (torch.randn((num_tokens, num_q_heads, head_dim), generator=g, device=device,
+                     dtype=torch.float32) * q_std).to(qdt)
     shape = (nb, num_kv_heads, block_size, head_dim)
     k = _kv_values(shape, kv_dtype, kv_scale, g, device)
     v = _kv_values(shape, kv_dtype, kv_scale, g, device)

@@ -38,7 +38,7 @@ def _build_status(lib, **kw):
     args = dict(device=0, n=4, hq=8, hkv=2, d=64, qlen=1, tokens=4, parts=0, budget=0, kind=0)
     args.update(kw)
     h = ctypes.c_void_p()
-    st = lib.pa_plan_build(ctypes.byref(h), args["device"], args["n"], args["hq"], args["hkv"],
+    st = lib.pa_plan_build(ctypes.byref(h), args["device"], args["n"], args["hkv"], args["hq"],
                            args["d"], args["qlen"], args["tokens"], args["parts"],
                            args["budget"], args["kind"])
     assert h.value is None  # nothing allocated on any rejected call
@@ -52,6 +52,7 @@ def _build_status(lib, **kw):
     (dict(kind=7), binding.PA_ERR_INVALID_ARG),
     (dict(n=4097), binding.PA_ERR_UNSUPPORTED),
     (dict(hq=6, hkv=4), binding.PA_ERR_UNSUPPORTED),
+    (dict(hq=2, hkv=8), binding.PA_ERR_UNSUPPORTED),  # num_kv_heads comes before num_q_heads
     (dict(d=96), binding.PA_ERR_UNSUPPORTED),
     (dict(d=192), binding.PA_ERR_UNSUPPORTED),   # above 128: multiples of 128 only
     (dict(d=1152), binding.PA_ERR_UNSUPPORTED),  # above 1024
@@ -84,12 +85,12 @@ def test_sparse_select_rejects_bad_arguments_before_cuda(lib):
 
 
 def test_null_handles(lib):
-    assert lib.pa_plan_build(None, 0, 4, 8, 2, 64, 1, 4, 0, 0, 0) == binding.PA_ERR_INVALID_ARG
+    assert lib.pa_plan_build(None, 0, 4, 2, 8, 64, 1, 4, 0, 0, 0) == binding.PA_ERR_INVALID_ARG
     assert lib.pa_plan_refresh(None, None, None, None) == binding.PA_ERR_INVALID_ARG
     assert lib.pa_plan_destroy(None) == binding.PA_OK
     assert lib.pa_plan_info(None, None, None, None, None, None, None, None) == \
         binding.PA_ERR_INVALID_ARG
-    assert lib.pa_plan_download(None, None, None, None) == binding.PA_ERR_INVALID_ARG
+    assert lib.pa_plan_download(None, None, None, None, None) == binding.PA_ERR_INVALID_ARG
     assert lib.pa_plan_set_split_events(None, None, None) == binding.PA_ERR_INVALID_ARG
     assert lib.pa_plan_set_call_events(None, None, None) == binding.PA_ERR_INVALID_ARG
     assert lib.pa_plan_set_window(None, 5) == binding.PA_ERR_INVALID_ARG

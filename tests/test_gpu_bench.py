@@ -24,7 +24,7 @@ def _run(*args) -> dict:
 
 
 def test_native_line_has_the_contract_keys():
-    d = _run("--steps", "5", "--warmup", "3")
+    d = _run("--steps", "5", "--warmup", "3", "--seeds", "2", "--cpu-seconds", "2")
     for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
               "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "roofline",
               "cpu_baseline", "e2e", "gpu_launches", "clocks"):
@@ -32,6 +32,16 @@ def test_native_line_has_the_contract_keys():
     assert d["n_gpus"] == 1 and d["steps"] == 5 and d["warmup"] == 3
     assert d["value"] > 0 and d["ms_per_step"] > 0 and d["higher_is_better"] is True
     assert "workload" in d["config"]
+    assert d["config"]["name"] == "large_bf16"  # the largest single-GPU configuration
+    for key in ("large_fp8", "skewed_seeds"):  # the target's evidence, in the same line
+        assert key in d, key
+    sk = d["skewed_seeds"]
+    assert sk["seeds"] == 2 and len(sk["per_seed"]) == 2
+    for k in ("call_frac_of_measured", "split_frac_of_measured",
+              "uniform_over_proportional_call"):
+        assert sk[k]["median"] > 0 and sk[k]["p10"] > 0
+    assert d["large_fp8"]["us_per_decode_call"] > 0
+    assert d["e2e_kv_resident"]["h2d_bytes_per_step"] < d["e2e"]["h2d_bytes_per_step"]
     rf = d["roofline"]
     assert rf["bound"] == "hbm" and rf["unit"] == "GB/s"
     assert 0 < rf["achieved"] and 0 < rf["peak"]

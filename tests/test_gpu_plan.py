@@ -2,6 +2,9 @@
 reduce_info for every configuration, random batches and the edge cases."""
 from __future__ import annotations
 
+import ctypes
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -114,3 +117,39 @@ def test_query_rows_beyond_plan_limits_empty_the_plan(dev):
     plan2, _, red2 = _gpu_plan(dev, [500, 500, 500], cu, 8, 1, max_qlen=8, max_tokens=9)
     assert np.all(red2[:, 1] == 0)
     assert plan2.read_errors() & binding.DEVERR_PLAN_OVERFLOW
+
+
+@pytest.mark.parametrize("hkv,hq", [(2, 8), (4, 4), (1, 6)])
+def test_plan_build_in_the_contract_order(dev, hkv, hq):
+    """pa_plan_build(plan, device, num_seqs, num_kv_heads, num_q_heads, head_dim,
+    ...) called through ctypes in that order: the capacity C = min(n P,
+    max(n, ceil(W / Hkv))) that pa_plan_info and pa_plan_download report
+    depends on which argument is the kv head count (with Hq != Hkv a swap gives
+    another C), and the plan decodes a batch of those head counts."""
+    lib = binding.load()
+    n, W = 8, 64
+    h = ctypes.c_void_p()
+    st = lib.pa_plan_build(ctypes.byref(h), dev.index, n, hkv, hq, 128, 1, n, 0, W,
+                           binding.PROPORTIONAL)
+    assert st == binding.PA_OK, binding.status_string(st)
+    try:
+        cap = ctypes.c_int()
+        seqs = ctypes.c_int()
+        assert lib.pa_plan_info(h, ctypes.byref(cap), ctypes.byref(seqs), None, None, None, None,
+                                None) == binding.PA_OK
+        want = min(n * 256, max(n, math.ceil(W / hkv)))
+        assert cap.value == want and seqs.value == n
+        lens = torch.tensor([300, 17, 4000, 1, 900, 2600, 64, 5], dtype=torch.int32, device=dev)
+        s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        assert lib.pa_plan_refresh(h, ctypes.c_void_p(lens.data_ptr()), None, s) == binding.PA_OK
+        work = torch.empty((want, 4), dtype=torch.int32)
+        red = torch.empty((n, 2), dtype=torch.int32)
+        cap2 = ctypes.c_int(-1)
+        assert lib.pa_plan_download(h, ctypes.c_void_p(work.data_ptr()),
+                                    ctypes.c_void_p(red.data_ptr()), ctypes.byref(cap2),
+                                    s) == binding.PA_OK
+        assert cap2.value == want
+        ow, orr = oracle.plan(lens.cpu().numpy(), None, hkv, 256, W)
+        assert np.array_equal(work.numpy(), ow) and np.array_equal(red.numpy(), orr)
+    finally:
+        assert lib.pa_plan_destroy(h) == binding.PA_OK

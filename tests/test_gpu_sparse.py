@@ -8,12 +8,10 @@ import pytest
 import torch
 
 import oracle
-from helpers import kv_bits, bits16, q_code, DT_CODE
+from helpers import kv_bits, bits16, q_code, DT_CODE, parity
 from paged_kv_decode_split_gb300 import binding, workloads as wl
 
 pytestmark = pytest.mark.gpu
-
-TOL = {"bf16": 1e-2, "fp16": 1e-2, "fp8": 3e-2}
 
 
 @pytest.fixture(scope="module")
@@ -136,7 +134,7 @@ def test_sparse_decode_parity(dev, kv, bs, D, top_k, init, local):
     sw = _small(dev, kv, bs, seed=bs + top_k, top_k=top_k, init=init, local=local, D=D)
     out, plan, _, sl = _run_sparse(sw)
     ref = _oracle_sparse(sw)
-    assert float(np.abs(out.float().cpu().numpy() - ref).max()) <= TOL[kv]
+    parity(out, ref, kv)
     assert plan.read_errors() == 0
     assert torch.all(out[sw.base.context_lens == 0] == 0)
 
@@ -146,7 +144,7 @@ def test_sparse_decode_grouped_k_and_uniform_plan(dev):
     ref = _oracle_sparse(sw)
     for kind, grouped in ((binding.UNIFORM, False), (binding.PROPORTIONAL, True)):
         out, plan, _, _ = _run_sparse(sw, kind=kind, grouped=grouped)
-        assert float(np.abs(out.float().cpu().numpy() - ref).max()) <= TOL["fp8"]
+        parity(out, ref, "fp8", what=f"kind {kind} grouped {grouped}")
 
 
 def test_sparse_full_size(dev):
@@ -155,7 +153,7 @@ def test_sparse_full_size(dev):
     out, plan, sel, sl = _run_sparse(sw)
     assert np.array_equal(sl.cpu().numpy(), sw.selected_tokens().numpy().astype(np.int32))
     ref = _oracle_sparse(sw)
-    assert float(np.abs(out.float().cpu().numpy() - ref).max()) <= TOL["fp8"]
+    parity(out, ref, "fp8")
     assert plan.read_errors() == 0
     work, red = plan.download()
     assert int(red[:, 1].max()) <= 8  # the sparse partition ceiling
@@ -193,5 +191,5 @@ def test_sparse_step_in_a_cuda_graph(dev):
         g.replay()
         torch.cuda.synchronize()
         ref = _oracle_sparse(sw)
-        assert float(np.abs(out.float().cpu().numpy() - ref).max()) <= TOL["bf16"], trial
+        parity(out, ref, "bf16", what=f"trial {trial}")
     assert plan.read_errors() == 0
