@@ -58,6 +58,8 @@ DESCRIBE = {
                   "D 128, page 128, bf16",
     "large_fp8": "large skewed: 512 seqs, ctx lognormal(2048, 1.2) in [16,65536], Hq/Hkv 64/8, "
                  "D 128, page 128, fp8-e4m3 KV",
+    "large_bf16_quarter": "the first 128 requests of the large skewed batch (Hq/Hkv 64/8, D 128, "
+                          "page 128, bf16): a profiling-sized case",
     "uniform_w1024": "uniform decode under a 1024-key sliding window",
     "skewed_w4096": "skewed agentic decode under a 4096-key sliding window",
     "uniform_k5": "uniform decode with K in the grouped layout [nb, Hkv, D/16, 16, 16]",
@@ -519,6 +521,9 @@ def run_native(args, world, rank, local):
         if rank == 0:
             sweep(args)
         return
+    if args.profile_run:
+        profile_run(args, dev)
+        return
     t_start = time.perf_counter()
     w = wl.CONFIGS[args.workload](0, dev)
     kv_bytes = w.kv_bytes()
@@ -604,6 +609,22 @@ def run_native(args, world, rank, local):
         print(json.dumps(line), flush=True)
     if args.sweep and rank == 0:
         sweep(args)
+
+
+def profile_run(args, dev):
+    """For profilers: W + K plain (eager) steps of the workload -- refresh and
+    decode, three kernel launches each -- with nothing else on the GPU; the
+    first W are the warm-up to skip (ncu -s 3W for every kernel, -s W for one)."""
+    w = wl.CONFIGS[args.workload](0, dev)
+    plan = binding.plan_for(w)
+    out = torch.empty_like(w.q)
+    for _ in range(args.warmup + args.steps):
+        plan.refresh(w.context_lens, w.cu_query_lens)
+        binding.decode_workload(plan, w, out=out)
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"profile_run": args.workload, "steps": args.steps, "warmup": args.warmup,
+                      "kv_bytes_per_step": w.kv_bytes(), "errors": plan.read_errors()}),
+          flush=True)
 
 
 def _pct(xs, q):
@@ -718,6 +739,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0,
                     help="bound on the oracle's timed sample (cpu_baseline)")
+    ap.add_argument("--profile-run", action="store_true",
+                    help="W + K plain steps of the workload for a profiler (no timing)")
     ap.add_argument("--no-extra", action="store_true",
                     help="headline workload only (no large_fp8 / skewed_seeds keys)")
     args = ap.parse_args(argv)

@@ -226,6 +226,15 @@ def large(kv_dtype: str = "bf16", seed: int = 0, device="cpu") -> Workload:
                       kv_scale=0.05, device=device)
 
 
+def large_quarter(kv_dtype: str = "bf16", seed: int = 0, device="cpu") -> Workload:
+    """The first 128 requests of the Large batch's length draw (same shapes:
+    Hq/Hkv 64/8, D 128, page 128): about 2 GB of bf16 KV, a profiling-sized
+    case of the same kernel (larger than L2, a few GB on the device)."""
+    lens = lognormal_lengths(512, 2048, 1.2, 16, 65536, seed)[:128]
+    return make_batch(f"large_{kv_dtype}_quarter", lens, None, 64, 8, 128, 128, kv_dtype,
+                      seed=seed, kv_scale=0.05, device=device)
+
+
 def uniform_window(seed: int = 0, device="cpu") -> Workload:
     """The uniform batch under a 1024-key sliding window (each request reads its
     last 1024 keys)."""
@@ -249,6 +258,7 @@ CONFIGS = {
     "mixed_prompt": mixed_prompt,
     "large_bf16": lambda seed=0, device="cpu": large("bf16", seed, device),
     "large_fp8": lambda seed=0, device="cpu": large("fp8", seed, device),
+    "large_bf16_quarter": lambda seed=0, device="cpu": large_quarter("bf16", seed, device),
     "uniform_w1024": uniform_window,
     "skewed_w4096": skewed_window,
 }
