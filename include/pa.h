@@ -199,6 +199,23 @@ int pa_plan_set_window(pa_plan* plan, int sliding_window);
  * the next pa_plan_refresh.  PA_ERR_INVALID_ARG for another value. */
 int pa_plan_set_kv_dtype(pa_plan* plan, int kv_dtype);
 
+/* Limit of the decode kernel's bounded waits, for the plan's later pa_decode
+ * calls: a wait on a pipeline stage that has not completed after wait_limit_ns
+ * nanoseconds gives up, raises PA_DEVERR_TIMEOUT in the plan's error word and
+ * abandons that CTA's remaining work (its output rows are then meaningless);
+ * the kernel still returns and the context stays usable.  0 restores the
+ * default of 4 s; otherwise at least 10 us (PA_ERR_INVALID_ARG below that or
+ * for a negative value).  No counterpart in the pages. */
+int pa_plan_set_wait_limit(pa_plan* plan, long long wait_limit_ns);
+
+/* Test hook for the timeout path: with stage >= 0, the producer of every CTA
+ * of the plan's later pa_decode calls leaves its pipeline stage number `stage`
+ * (counted from 0 across the CTA's work items) neither copied nor armed, so
+ * every wait on it runs out after the wait limit and PA_DEVERR_TIMEOUT is
+ * raised; -1 (the default) turns it off.  The results of such a call are
+ * meaningless.  PA_ERR_INVALID_ARG below -1.  No counterpart in the pages. */
+int pa_plan_skip_stage_for_test(pa_plan* plan, int stage);
+
 /* pa_decode with attention sinks and a choice of K layout.  sinks (named in
  * the same aiter signature) is NULL or a device array of num_q_heads fp32
  * logits, in the units of scale * q.k, each joining its head's softmax

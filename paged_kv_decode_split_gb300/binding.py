@@ -66,6 +66,8 @@ def load() -> ctypes.CDLL:
                                  i32, P, P, i32, f32, P, i32, P, P]
     lib.pa_plan_set_window.argtypes = [P, i32]
     lib.pa_plan_set_kv_dtype.argtypes = [P, i32]
+    lib.pa_plan_set_wait_limit.argtypes = [P, ctypes.c_longlong]
+    lib.pa_plan_skip_stage_for_test.argtypes = [P, i32]
     lib.pa_plan_info.argtypes = [P, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                  ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32),
                                  ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_longlong)]
@@ -79,6 +81,7 @@ def load() -> ctypes.CDLL:
     lib.pa_status_string.restype = ctypes.c_char_p
     for name in ("pa_plan_build", "pa_plan_refresh", "pa_decode", "pa_decode_ex",
                  "pa_plan_set_window", "pa_plan_set_kv_dtype", "pa_plan_info",
+                 "pa_plan_set_wait_limit", "pa_plan_skip_stage_for_test",
                  "pa_plan_download", "pa_plan_read_errors", "pa_plan_set_split_events",
                  "pa_plan_set_call_events", "pa_sparse_select",
                  "pa_plan_destroy"):
@@ -264,6 +267,17 @@ class Plan:
         "fp8" or a PA_* code), for the next refresh on."""
         code = _DTYPES[kv_dtype] if isinstance(kv_dtype, str) else int(kv_dtype)
         _check(load().pa_plan_set_kv_dtype(self._h, code), "pa_plan_set_kv_dtype")
+
+    def set_wait_limit(self, wait_limit_ns: int):
+        """Limit of the decode kernel's bounded waits (0: the default 4 s)."""
+        _check(load().pa_plan_set_wait_limit(self._h, int(wait_limit_ns)),
+               "pa_plan_set_wait_limit")
+
+    def skip_stage_for_test(self, stage: int):
+        """Test hook: every CTA leaves its pipeline stage `stage` un-issued, so
+        its waits run out (-1: off)."""
+        _check(load().pa_plan_skip_stage_for_test(self._h, int(stage)),
+               "pa_plan_skip_stage_for_test")
 
     def close(self):
         h, self._h = getattr(self, "_h", None), None

@@ -67,6 +67,8 @@ struct pa_plan {
   int kv_dtype;  // the cache type the decode calls are expected to read
   int wave;      // CTAs of that decode grid that run at once
   int window;          // sliding window for the next refresh (0: none)
+  unsigned long long wait_ns;  // limit of the kernels' bounded waits
+  int skip_stage;              // test hook (pa_plan_skip_stage_for_test); -1: off
   int window_planned;  // the window the last refresh planned with
   long long rows_cap, max_extra;
   pa::PlanDev dev;
@@ -349,6 +351,8 @@ int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_kv_heads, in
   pl->window = pl->window_planned = 0;
   pl->ev_call0 = pl->ev_call1 = nullptr;
   pl->tmap_next = 0;
+  pl->wait_ns = pa::kWaitLimitNs;
+  pl->skip_stage = -1;
   *plan = pl;
   return PA_OK;
 }
@@ -385,6 +389,20 @@ int pa_plan_refresh(pa_plan* plan, const int32_t* context_lens, const int32_t* c
 int pa_plan_set_window(pa_plan* plan, int sliding_window) {
   if (!plan || sliding_window < 0) return PA_ERR_INVALID_ARG;
   plan->window = sliding_window;
+  return PA_OK;
+}
+
+int pa_plan_set_wait_limit(pa_plan* plan, long long wait_limit_ns) {
+  if (!plan || wait_limit_ns < 0) return PA_ERR_INVALID_ARG;
+  if (wait_limit_ns > 0 && wait_limit_ns < 10000) return PA_ERR_INVALID_ARG;
+  plan->wait_ns = wait_limit_ns == 0 ? pa::kWaitLimitNs
+                                     : static_cast<unsigned long long>(wait_limit_ns);
+  return PA_OK;
+}
+
+int pa_plan_skip_stage_for_test(pa_plan* plan, int stage) {
+  if (!plan || stage < -1) return PA_ERR_INVALID_ARG;
+  plan->skip_stage = stage;
   return PA_OK;
 }
 
@@ -476,6 +494,8 @@ int pa_decode_ex(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int 
   sp.v_scale = fp8 ? v_scale : 1.0f;
   sp.window = plan->window_planned;
   sp.sinks = sinks;
+  sp.wait_ns = plan->wait_ns;
+  sp.skip_stage = plan->skip_stage;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int wq = pa::split_row_groups(plan->max_qlen, sp.G, head_dim);

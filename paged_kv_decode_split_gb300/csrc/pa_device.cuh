@@ -12,9 +12,6 @@
 
 namespace pa {
 
-// Bounded waits give up after this long and raise PA_DEVERR_TIMEOUT.
-constexpr unsigned long long kWaitLimitNs = 4000000000ull;
-
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -61,13 +58,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Gives up after
-// kWaitLimitNs, setting PA_DEVERR_TIMEOUT; the caller then carries on so that
-// every thread still reaches the kernel's later barriers.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err) {
+// limit_ns nanoseconds, setting PA_DEVERR_TIMEOUT; the caller then carries on
+// so that every thread still reaches the kernel's later barriers.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err,
+                                          unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (global_ns() - t0 > limit_ns) {
       atomicOr(err, PA_DEVERR_TIMEOUT);
       return false;
     }

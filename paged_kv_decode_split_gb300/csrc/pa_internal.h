@@ -14,6 +14,10 @@ constexpr int kTile = 256;       // partition tile, tokens
 constexpr int kMaxSeqs = 4096;   // planner domain
 constexpr int kStageTensorBytes = 16384;  // split kernel: K (or V) bytes per pipeline stage
 
+// Bounded waits inside the kernels give up after this long by default (a plan
+// may set another limit) and raise PA_DEVERR_TIMEOUT.
+constexpr unsigned long long kWaitLimitNs = 4000000000ull;
+
 constexpr int kMinPieceTiles = 2;  // a slot is cut into pieces of at least this many tiles
 constexpr int kWarpMergePieces = 8;  // rows with at most this many pieces are merged by one warp
 
@@ -122,6 +126,9 @@ struct SplitParams {
   float v_scale;    // 1 for 16-bit caches
   int window;       // sliding window: a row that may see keys [0, K) sees [K - window, K); 0: none
   const float* sinks;  // [Hq] sink logits (scale * q.k units) or null
+  unsigned long long wait_ns;  // limit of every bounded wait (PA_DEVERR_TIMEOUT after it)
+  int skip_stage;   // test hook: when >= 0, every CTA's producer leaves ring stage number
+                    // skip_stage un-issued (no copy, no arrival), so the waits on it run out
 };
 
 // Head dims the kernels take: 64, and 128 to 1024 in steps of 128.

@@ -33,10 +33,12 @@
 //    takes part in every stage (its key slice: T 16-key tiles handled
 //    together -- independent MMA chains, one softmax reduction), so each warp
 //    waits on the ring slots strictly in order;
-//  * every mbarrier wait is bounded: a wait that gives up raises
-//    PA_DEVERR_TIMEOUT and aborts the CTA's pipeline (no further copies are
-//    issued or consumed); the producer then drains the copies it issued before
-//    the CTA exits;
+//  * every mbarrier wait is bounded (4 s unless the plan sets another limit):
+//    a wait that gives up raises PA_DEVERR_TIMEOUT and aborts the CTA's
+//    pipeline (no further copies are issued or consumed); the producer then
+//    drains the copies it issued before the CTA exits.  Every named barrier
+//    and __syncthreads is still met on that path, so an aborted CTA returns;
+//    a test hook (skip_stage) leaves one stage un-issued to exercise it;
 //  * QK^T and PV are m16n8k16 tensor-core MMAs in "swap-AB" form: 16 keys
 //    (QK) or 16 head dims (PV) on M, the 8 query rows of the group on N, so a
 //    GQA group of 8 fills N exactly.  P moves from the QK accumulator to the
@@ -159,7 +161,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     return __shfl_sync(0xffffffffu, *reinterpret_cast<volatile int*>(&s_abort), 0) != 0;
   };
   auto wait_all = [&](uint32_t bar, uint32_t parity) {
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, parity, p.plan.err));
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, parity, p.plan.err, p.wait_ns));
     if (!ok && lane == 0) *reinterpret_cast<volatile int*>(&s_abort) = 1;
     return ok;
   };
@@ -258,6 +260,9 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     if (aborted()) return;
     if (it >= Cfg::NS && !wait_all(bar_empty + 8 * buf, ((it / Cfg::NS) & 1) ^ 1)) return;
     issued = it + 1;
+    // Test hook: this stage is counted as issued (the drain waits on it) but
+    // neither copied nor armed, so every wait on it gives up after wait_ns.
+    if (it == p.skip_stage) return;
     const int* bt = p.block_tables + static_cast<size_t>(q.r) * p.max_blocks;
     const int npages = min((q.S + bs - 1) / bs, p.max_blocks);
     const int key0 = q.kb + s * Cfg::KS;
@@ -930,7 +935,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
   // Each producer warp drains the stages it issued.
   if (warp < Cfg::NPW && lane == 0) {
     for (int k = (issued > Cfg::NS ? issued - Cfg::NS : 0); k < issued; ++k)
-      mbar_wait(bar_full + 8 * (k % Cfg::NS), (k / Cfg::NS) & 1, p.plan.err);
+      mbar_wait(bar_full + 8 * (k % Cfg::NS), (k / Cfg::NS) & 1, p.plan.err, p.wait_ns);
   }
 }
 

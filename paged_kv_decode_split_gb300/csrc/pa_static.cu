@@ -174,6 +174,8 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
   sp.rpc = lay.rpc;
   sp.window = 0;
   sp.sinks = nullptr;
+  sp.wait_ns = pa::kWaitLimitNs;
+  sp.skip_stage = -1;
   sp.scale_log2 = static_cast<float>(static_cast<double>(scale) * (fp8 ? k_scale : 1.0) *
                                      1.4426950408889634);
   sp.v_scale = fp8 ? v_scale : 1.0f;

@@ -445,6 +445,47 @@ def test_bad_page_is_reported_not_faulted(dev, grouped):
     assert max_diff(out[[1]], ref) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("case", ["d128", "d128_two_rows", "d512_slices"])
+def test_a_wait_that_runs_out_sets_the_timeout_bit(dev, case):
+    """The timeout path, made to run on purpose: with a 100 us wait limit and
+    the test hook that leaves every CTA's second pipeline stage un-issued, the
+    consumers' bounded waits give up, PA_DEVERR_TIMEOUT is raised, the call
+    returns (every barrier is still met on the abort path: the single-slice
+    kernel, the two-row-group exchange epilogue, and a 512-dim head whose
+    slice warps meet a named barrier per stage), and the next call on the same
+    plan, with the hook off and the default limit, is correct."""
+    if case == "d128":
+        w = batch(dev, [3000, 800, 1200, 17], H=(8, 2), D=128, seed=71)
+    elif case == "d128_two_rows":
+        w = batch(dev, [3000, 800, 1200], ql=[2, 2, 2], H=(8, 1), D=128, pad=2, seed=72)
+    else:
+        w = batch(dev, [3000, 800, 1200], H=(8, 1), D=512, seed=73)
+    plan = binding.plan_for(w)
+    plan.refresh(w.context_lens, w.cu_query_lens)
+    plan.set_wait_limit(100_000)
+    plan.skip_stage_for_test(1)
+    binding.decode_workload(plan, w)
+    torch.cuda.synchronize()
+    assert plan.read_errors() & binding.DEVERR_TIMEOUT
+    plan.skip_stage_for_test(-1)
+    plan.set_wait_limit(0)
+    out = binding.decode_workload(plan, w)
+    torch.cuda.synchronize()
+    assert plan.read_errors() == 0
+    assert max_diff(out, oracle_decode(w.to("cpu"))) <= TOL[w.kv_dtype]
+
+
+def test_wait_limit_arguments(dev):
+    plan = binding.Plan(4, 8, 2, 128, device=dev)
+    for bad in (-1, 5):
+        with pytest.raises(binding.PaError):
+            plan.set_wait_limit(bad)
+    with pytest.raises(binding.PaError):
+        plan.skip_stage_for_test(-2)
+    plan.set_wait_limit(10_000)
+    plan.set_wait_limit(0)
+
+
 def test_overflowing_query_rows_empty_the_plan(dev):
     w = batch(dev, [500, 500], ql=[2, 2], H=(8, 2), D=64, seed=8)
     plan = binding.Plan(2, 8, 2, 64, max_query_len=1, max_tokens=4, device=dev)
