@@ -264,7 +264,7 @@ def _replay_ms(g, dev) -> float:
     return t0.elapsed_time(t1)
 
 
-def _step_fns(w, kind, out):
+def _step_fns(w, kind, out, fused=None):
     """(plan, refresh, decode) for a Workload, or for a SparseWorkload: there the
     refresh is the block selection followed by the plan refresh from the
     selected lengths, and the decode runs over the sparse block table."""
@@ -273,6 +273,8 @@ def _step_fns(w, kind, out):
         plan = binding.Plan(b.num_seqs, b.num_q_heads, b.num_kv_heads, b.head_dim,
                             max_partitions=sw.max_partitions, budget=b.budget or 0, kind=kind,
                             device=b.q.device)
+        if fused is not None:
+            plan.set_fused_merge(fused)
         sel = torch.empty((b.num_seqs, sw.sel_stride), dtype=torch.int32, device=b.q.device)
         sl = torch.empty(b.num_seqs, dtype=torch.int32, device=b.q.device)
 
@@ -286,12 +288,14 @@ def _step_fns(w, kind, out):
                         out=out)
         return plan, refresh, decode
     plan = binding.plan_for(w, kind)
+    if fused is not None:
+        plan.set_fused_merge(fused)
     return (plan, lambda: plan.refresh(w.context_lens, w.cu_query_lens),
             lambda: binding.decode_workload(plan, w, out=out))
 
 
 def time_native(w, steps: int, warmup: int, kind=binding.PROPORTIONAL, flush: bool = False,
-                sampler: ClockSampler | None = None, world: int = 1):
+                sampler: ClockSampler | None = None, world: int = 1, fused=None):
     """Graph-replayed timing of K steps, as a serving engine replays its decode
     graphs.  A step is refresh + decode (planner, split, merge kernels).
 
@@ -307,12 +311,14 @@ def time_native(w, steps: int, warmup: int, kind=binding.PROPORTIONAL, flush: bo
     errs long).
 
     A SparseWorkload's step is selection + refresh + decode over the selection.
+    fused: None keeps the plan's default merge; True / False force the merge
+    inside the split kernel / the separate merge kernel.
 
     Returns dict(step_ms, call_ms, split_ms, split_all) and the plan."""
     q = w.base.q if isinstance(w, wl.SparseWorkload) else w.q
     dev = q.device
     out = torch.empty_like(q)
-    plan, refresh_fn, decode_fn = _step_fns(w, kind, out)
+    plan, refresh_fn, decode_fn = _step_fns(w, kind, out, fused)
     fa = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
     fb = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
     sink = torch.empty(steps, dtype=torch.float32, device=dev) if flush else None
@@ -558,7 +564,8 @@ def run_native(args, world, rank, local):
                    "kv_bytes_per_step": kv_bytes, "plan": "proportional",
                    "budget": info["budget"], "capacity": info["capacity"],
                    "max_partitions": info["max_partitions"],
-                   "step": "plan refresh + pa_decode (split-KV kernel + merge kernel)",
+                   "step": "plan refresh + pa_decode (split-KV kernel; merge fused into it, "
+                           "or a merge kernel for multi-token plans)",
                    "l2": "inputs larger than L2 (no flush)" if kv_bytes > L2_BYTES
                    else "not flushed: inputs fit in L2",
                    "timing": "K steps captured once in a CUDA graph and replayed; decode "
@@ -584,7 +591,8 @@ def run_native(args, world, rank, local):
                             "d2h_bytes_per_step": res_d2h, "ms_per_step": round(res_ms, 4),
                             "inputs": "q, block tables, lengths uploaded every step; the paged "
                                       "KV cache stays in HBM"},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (1 + plan.kernels_per_decode()) * args.steps,
+        "merge": "fused into the split kernel" if plan.fused_merge else "separate merge kernel",
         "clocks": clocks,
     }
     del w, plan
@@ -627,6 +635,15 @@ def profile_run(args, dev):
           flush=True)
 
 
+def _fusable(w) -> bool:
+    """Whether a workload's plan takes the fused merge (one query row per request)."""
+    b = w.base if isinstance(w, wl.SparseWorkload) else w
+    if b.cu_query_lens is None:
+        return True
+    cu = b.cu_query_lens.cpu()
+    return int((cu[1:] - cu[:-1]).max()) <= 1
+
+
 def _pct(xs, q):
     xs = sorted(xs)
     return xs[min(len(xs) - 1, int(round(q * (len(xs) - 1))))]
@@ -665,6 +682,10 @@ def sweep(args):
                             "split_frac_of_8tbs": round(kv / (t["split_ms"] * 1e-3) / 8e12, 4),
                             "tasks": int(red[:, 1].sum()), "max_parts": int(red[:, 1].max())}
             res["refresh_us"] = round(time_refresh(w), 2)
+            if plan.fused_merge or _fusable(w):  # A/B: the same plan with the merge kernel
+                t, _ = time_native(w, args.steps, args.warmup, flush=True, fused=False)
+                res["merge_kernel_us_per_decode_call"] = round(t["call_ms"] * 1e3, 2)
+                res["fused_merge_us_per_decode_call"] = res["proportional"]["us_per_decode_call"]
             print(json.dumps(res), flush=True)
             if name == "skewed":
                 skew.append(res)

@@ -159,7 +159,8 @@ int pa_plan_refresh(pa_plan* plan, const int32_t* context_lens, const int32_t* c
 
 /* Paged decode over the plan's tasks, then an LSE-weighted merge of each
  * request's partial results ([ATOM-2366] sections 3 and 6 item 5: split
- * attention tile, then the partial-softmax reduce).  Arguments follow the
+ * attention tile, then the partial-softmax reduce) -- inside the split kernel
+ * or by a second kernel, see pa_plan_set_fused_merge.  Arguments follow the
  * layouts above; num_q_heads, head_dim, num_kv_heads and num_seqs must equal
  * the plan's.  q_dtype is PA_BF16 or PA_FP16; kv_dtype is PA_BF16 (q bf16),
  * PA_FP16 (q fp16) or PA_FP8_E4M3 (q bf16 or fp16; the dot products then run
@@ -169,7 +170,7 @@ int pa_plan_refresh(pa_plan* plan, const int32_t* context_lens, const int32_t* c
  * num_tokens == num_seqs; with it, num_tokens >= 1 and rows past
  * cu[num_seqs] are graph padding (written as zeros).  q, out, k_cache and
  * v_cache must be 16-byte aligned.  Every output row is written.  Enqueues
- * two kernels on `stream`; returns without waiting. */
+ * one kernel (fused merge) or two on `stream`; returns without waiting. */
 int pa_decode(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int num_q_heads,
               int head_dim, const void* k_cache, const void* v_cache, int kv_dtype, float k_scale,
               float v_scale, int num_blocks, int num_kv_heads, int block_size,
@@ -198,6 +199,27 @@ int pa_plan_set_window(pa_plan* plan, int sliding_window);
  * change; a pa_decode over another cache type stays correct.  Takes effect at
  * the next pa_plan_refresh.  PA_ERR_INVALID_ARG for another value. */
 int pa_plan_set_kv_dtype(pa_plan* plan, int kv_dtype);
+
+/* Where pa_decode merges the partial results of requests split into several
+ * pieces ([ATOM-2366] section 6 item 5 and review item 7: the partial-softmax
+ * reduce after the split attention tiles, which the pages measured ~14%
+ * dearer as a separate pass).  enable = 1: the split kernel merges them itself
+ * -- the CTA that finishes the last piece of a group of up to 8 takes the
+ * group's last ticket (an atomic count, no waiting) and merges the group, up a
+ * tree until the request's output rows are written -- and pa_decode launches
+ * one kernel; enable = 0: a separate merge kernel runs after the split kernel.
+ * The fused merge is possible for plans with one query row per request
+ * (max_query_len 1) whose GQA group fits one work item of the split kernel,
+ * and is the default there; every other plan keeps the merge kernel, where a
+ * request's many query rows are better spread over many CTAs.
+ * PA_ERR_UNSUPPORTED for enable = 1 on such a plan, PA_ERR_INVALID_ARG for
+ * another value.  Takes effect at the next pa_decode.  No counterpart in the
+ * pages beyond the cost they measured. */
+int pa_plan_set_fused_merge(pa_plan* plan, int enable);
+
+/* Whether the plan's pa_decode calls merge in the split kernel (1) or in a
+ * separate merge kernel (0). */
+int pa_plan_get_fused_merge(const pa_plan* plan, int* enabled);
 
 /* Limit of the decode kernel's bounded waits, for the plan's later pa_decode
  * calls: a wait on a pipeline stage that has not completed after wait_limit_ns

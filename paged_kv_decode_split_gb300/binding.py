@@ -67,6 +67,8 @@ def load() -> ctypes.CDLL:
     lib.pa_plan_set_window.argtypes = [P, i32]
     lib.pa_plan_set_kv_dtype.argtypes = [P, i32]
     lib.pa_plan_set_wait_limit.argtypes = [P, ctypes.c_longlong]
+    lib.pa_plan_set_fused_merge.argtypes = [P, i32]
+    lib.pa_plan_get_fused_merge.argtypes = [P, ctypes.POINTER(i32)]
     lib.pa_plan_skip_stage_for_test.argtypes = [P, i32]
     lib.pa_plan_info.argtypes = [P, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                  ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32),
@@ -82,6 +84,7 @@ def load() -> ctypes.CDLL:
     for name in ("pa_plan_build", "pa_plan_refresh", "pa_decode", "pa_decode_ex",
                  "pa_plan_set_window", "pa_plan_set_kv_dtype", "pa_plan_info",
                  "pa_plan_set_wait_limit", "pa_plan_skip_stage_for_test",
+                 "pa_plan_set_fused_merge", "pa_plan_get_fused_merge",
                  "pa_plan_download", "pa_plan_read_errors", "pa_plan_set_split_events",
                  "pa_plan_set_call_events", "pa_sparse_select",
                  "pa_plan_destroy"):
@@ -267,6 +270,22 @@ class Plan:
         "fp8" or a PA_* code), for the next refresh on."""
         code = _DTYPES[kv_dtype] if isinstance(kv_dtype, str) else int(kv_dtype)
         _check(load().pa_plan_set_kv_dtype(self._h, code), "pa_plan_set_kv_dtype")
+
+    @property
+    def fused_merge(self) -> bool:
+        """True when pa_decode merges the partials inside the split kernel."""
+        v = ctypes.c_int()
+        _check(load().pa_plan_get_fused_merge(self._h, ctypes.byref(v)), "pa_plan_get_fused_merge")
+        return bool(v.value)
+
+    def set_fused_merge(self, enable: bool):
+        """Merge in the split kernel (where the plan allows it) or in a separate
+        merge kernel."""
+        _check(load().pa_plan_set_fused_merge(self._h, int(bool(enable))),
+               "pa_plan_set_fused_merge")
+
+    def kernels_per_decode(self) -> int:
+        return 1 if self.fused_merge else 2
 
     def set_wait_limit(self, wait_limit_ns: int):
         """Limit of the decode kernel's bounded waits (0: the default 4 s)."""

@@ -67,6 +67,8 @@ struct pa_plan {
   int kv_dtype;  // the cache type the decode calls are expected to read
   int wave;      // CTAs of that decode grid that run at once
   int window;          // sliding window for the next refresh (0: none)
+  int fused_ok;   // the layout allows the fused merge (decode-only plan; tickets allocated)
+  int fused;      // decode calls merge in the split kernel (no merge kernel launch)
   unsigned long long wait_ns;  // limit of the kernels' bounded waits
   int skip_stage;              // test hook (pa_plan_skip_stage_for_test); -1: off
   int window_planned;  // the window the last refresh planned with
@@ -113,7 +115,7 @@ size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 }  // namespace
 
 PlanLayout plan_layout(int num_seqs, int Hq, int Hkv, int D, int max_qlen, int max_tokens,
-                       int max_partitions, int budget, int sms, bool pieces) {
+                       int max_partitions, int budget, int sms, bool pieces, bool fused) {
   PlanLayout l;
   const long long per_head = (static_cast<long long>(budget) + Hkv - 1) / Hkv;
   const long long lo = per_head > num_seqs ? per_head : num_seqs;
@@ -130,6 +132,19 @@ PlanLayout plan_layout(int num_seqs, int Hq, int Hkv, int D, int max_qlen, int m
   const int G = Hq / Hkv;
   l.rpc = 8 * split_row_groups(max_qlen, G, D);
   l.max_extra = split_max_extra(G, l.rpc, l.rows_cap, max_tokens, max_qlen);
+  // The split kernel merges a request's partials itself when every query row
+  // of a request is in one work item and there is one row per request.
+  l.fused = (fused && max_qlen == 1 && G <= l.rpc) ? 1 : 0;
+  l.levels = 0;
+  if (l.fused) {
+    const long long kmax = static_cast<long long>(l.Q) * max_partitions;
+    long long cover = 1;
+    while (cover < kmax && l.levels < kFusedLevels) {
+      cover *= kFusedFanIn;
+      ++l.levels;
+    }
+    if (l.levels < 1) l.levels = 1;
+  }
   const size_t n = static_cast<size_t>(num_seqs);
   l.b_work = up256(static_cast<size_t>(l.C) * sizeof(int4));
   l.b_red = up256(n * sizeof(int2));
@@ -140,8 +155,11 @@ PlanLayout plan_layout(int num_seqs, int Hq, int Hkv, int D, int max_qlen, int m
   l.b_pieces = up256(static_cast<size_t>(l.C) * l.Q * sizeof(int4));
   l.b_ext = up256(static_cast<size_t>(l.max_extra > 0 ? l.max_extra : 1) * sizeof(int2));
   l.b_mrow = up256(static_cast<size_t>(max_tokens) * sizeof(int4));
+  l.b_preq = up256(n * sizeof(int2));
+  l.b_tick = up256(static_cast<size_t>(l.levels > 0 ? l.levels : 1) * l.rows_cap * Hkv *
+                   sizeof(int));
   l.total = l.b_work + l.b_red + l.b_snap + l.b_err + l.b_po + l.b_pl + l.b_pieces + l.b_ext +
-            l.b_mrow;
+            l.b_mrow + l.b_preq + l.b_tick;
   return l;
 }
 
@@ -165,6 +183,10 @@ PlanDev carve_plan(char* c, const PlanLayout& l) {
   d.extra = reinterpret_cast<int2*>(c);
   c += l.b_ext;
   d.mrows = reinterpret_cast<int4*>(c);
+  c += l.b_mrow;
+  d.preq = reinterpret_cast<int2*>(c);
+  c += l.b_preq;
+  d.tickets = reinterpret_cast<int*>(c);
   return d;
 }
 
@@ -308,7 +330,7 @@ int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_kv_heads, in
   if (budget <= 0) budget = 2 * sms;
   const pa::PlanLayout lay = pa::plan_layout(num_seqs, num_q_heads, num_kv_heads, head_dim,
                                              max_query_len, max_tokens, max_partitions, budget, sms,
-                                             true);
+                                             true, true);
   const size_t total = lay.total;
 
   pa_plan* pl = new (std::nothrow) pa_plan();
@@ -321,6 +343,7 @@ int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_kv_heads, in
   }
   pl->dev = pa::carve_plan(static_cast<char*>(mem), lay);
   if (cudaMemset(pl->dev.err, 0, 64) != cudaSuccess ||
+      cudaMemset(pl->dev.tickets, 0, lay.b_tick) != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess) {
     cudaFree(mem);
     delete pl;
@@ -353,6 +376,8 @@ int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_kv_heads, in
   pl->tmap_next = 0;
   pl->wait_ns = pa::kWaitLimitNs;
   pl->skip_stage = -1;
+  pl->fused_ok = lay.fused;
+  pl->fused = lay.fused;
   *plan = pl;
   return PA_OK;
 }
@@ -397,6 +422,19 @@ int pa_plan_set_wait_limit(pa_plan* plan, long long wait_limit_ns) {
   if (wait_limit_ns > 0 && wait_limit_ns < 10000) return PA_ERR_INVALID_ARG;
   plan->wait_ns = wait_limit_ns == 0 ? pa::kWaitLimitNs
                                      : static_cast<unsigned long long>(wait_limit_ns);
+  return PA_OK;
+}
+
+int pa_plan_set_fused_merge(pa_plan* plan, int enable) {
+  if (!plan || (enable != 0 && enable != 1)) return PA_ERR_INVALID_ARG;
+  if (enable && !plan->fused_ok) return PA_ERR_UNSUPPORTED;
+  plan->fused = enable;
+  return PA_OK;
+}
+
+int pa_plan_get_fused_merge(const pa_plan* plan, int* enabled) {
+  if (!plan || !enabled) return PA_ERR_INVALID_ARG;
+  *enabled = plan->fused;
   return PA_OK;
 }
 
@@ -496,6 +534,8 @@ int pa_decode_ex(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int 
   sp.sinks = sinks;
   sp.wait_ns = plan->wait_ns;
   sp.skip_stage = plan->skip_stage;
+  sp.fused = plan->fused;
+  sp.rows_cap = plan->rows_cap;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int wq = pa::split_row_groups(plan->max_qlen, sp.G, head_dim);
@@ -514,6 +554,7 @@ int pa_decode_ex(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int 
     return PA_ERR_CUDA;
   if (plan->ev_stop && !record(plan->ev_stop)) return PA_ERR_CUDA;
 
+  if (!plan->fused) {
   pa::MergeParams mp;
   mp.plan = plan->dev;
   mp.out = out;
@@ -528,6 +569,7 @@ int pa_decode_ex(pa_plan* plan, const void* q, int q_dtype, int num_tokens, int 
   const long long pairs = static_cast<long long>(num_tokens) * num_q_heads;
   mp.grid = static_cast<int>(pairs < 8ll * plan->sms ? pairs : 8ll * plan->sms);
   if (pa::launch_merge(mp, s) != cudaSuccess) return PA_ERR_CUDA;
+  }
   if (plan->ev_call1 && !record(plan->ev_call1)) return PA_ERR_CUDA;
   return PA_OK;
 }

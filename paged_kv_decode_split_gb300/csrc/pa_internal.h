@@ -64,14 +64,28 @@ struct PlanDev {
   int2* extra;      // [max_extra] (piece position, row chunk >= 1) for requests whose
                     // query rows exceed one work item
   int* counters;    // [0] extra items, [1] next late piece or extra item (x Hkv; reset by
-                    // the planner and by the merge kernel), [2] merge rows with more than
-                    // kWarpMergePieces pieces, [3] merge rows with 2..kWarpMergePieces
-                    // pieces, [4] pieces
+                    // the planner, and after each decode by the merge kernel or, with the
+                    // merge fused, by the split kernel's last CTA), [2] merge rows with more
+                    // than kWarpMergePieces pieces, [3] merge rows with 2..kWarpMergePieces
+                    // pieces, [4] pieces, [5] split CTAs finished (fused merge only)
   int4* mrows;      // [max_tokens] one entry per row of a request with several pieces:
                     // {r | (pieces - 1) << 12, token, partial row of piece 0, L}
                     // (piece k's partial row is that + k * L); rows with few pieces
                     // first ([0, counters[3])), then rows with many
+  int2* preq;       // [n] (first partial row, pieces) of each request (fused merge)
+  int* tickets;     // [levels][rows_cap][Hkv] arrival counts of the fused merge's
+                    // groups, zero between decode calls (each is reset by the CTA that
+                    // takes its last ticket)
 };
+
+// Fused merge (decode-only plans): the pieces of a (request, kv head) are
+// merged in a tree of fan-in kFusedFanIn -- the CTA that finishes the last
+// piece of a group merges the group's partials into one, in place of its first
+// -- with one ticket per group and level; kFusedLevels levels cover
+// kFusedFanIn^kFusedLevels >= Q * P pieces.
+constexpr int kFusedFanIn = 8;
+constexpr int kFusedLog2FanIn = 3;
+constexpr int kFusedLevels = 7;  // at most: 8^7 > 4 * 65536
 
 // Sizes and offsets of one plan's buffers (256-byte aligned, back to back).
 struct PlanLayout {
@@ -80,11 +94,15 @@ struct PlanLayout {
   long long rows_cap;   // partial rows
   int rpc;              // query rows per split-kernel work item
   long long max_extra;  // extra (piece, row chunk) items
-  size_t b_work, b_red, b_snap, b_err, b_po, b_pl, b_pieces, b_ext, b_mrow, total;
+  int fused;            // 1: the split kernel merges the partials (decode-only plans whose
+                        // query rows fit one work item); 0: the merge kernel does
+  int levels;           // fused merge: tree levels needed for Q * P pieces
+  size_t b_work, b_red, b_snap, b_err, b_po, b_pl, b_pieces, b_ext, b_mrow, b_preq, b_tick, total;
 };
-// `pieces` = false keeps every task whole (Q = 1).
+// `pieces` = false keeps every task whole (Q = 1); `fused` = false keeps the
+// separate merge kernel for every plan.
 PlanLayout plan_layout(int num_seqs, int Hq, int Hkv, int D, int max_qlen, int max_tokens,
-                       int max_partitions, int budget, int sms, bool pieces);
+                       int max_partitions, int budget, int sms, bool pieces, bool fused);
 // Points the buffers of `l` into [base, base + l.total); the error word and
 // the counters share one 256-byte block.
 PlanDev carve_plan(char* base, const PlanLayout& l);
@@ -126,6 +144,8 @@ struct SplitParams {
   float v_scale;    // 1 for 16-bit caches
   int window;       // sliding window: a row that may see keys [0, K) sees [K - window, K); 0: none
   const float* sinks;  // [Hq] sink logits (scale * q.k units) or null
+  int fused;        // 1: merge each request's partials in this kernel (no merge kernel)
+  long long rows_cap;  // partial rows of the plan (ticket indexing)
   unsigned long long wait_ns;  // limit of every bounded wait (PA_DEVERR_TIMEOUT after it)
   int skip_stage;   // test hook: when >= 0, every CTA's producer leaves ring stage number
                     // skip_stage un-issued (no copy, no arrival), so the waits on it run out

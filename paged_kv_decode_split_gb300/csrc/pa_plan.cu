@@ -317,6 +317,7 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
     if (k < per && r < n) {
       p.dev.reduce[r] = make_int2(slot0, parts[k]);
       p.dev.snap[r] = make_int2(S[k], L[k]);
+      p.dev.preq[r] = make_int2(row0, pcs[k]);
       s_first[r] = slot0;
       s_parts[r] = parts[k];
       s_ctx[r] = S[k];
@@ -344,6 +345,7 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const PlanParams p) {
     p.dev.counters[2] = total_mmany;
     p.dev.counters[3] = total_mfew;
     p.dev.counters[4] = total_pieces;
+    p.dev.counters[5] = 0;
   }
   __syncthreads();
 

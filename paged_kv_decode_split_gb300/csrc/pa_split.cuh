@@ -61,6 +61,7 @@
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
+#include "pa_fused.cuh"
 #include "pa_merge.cuh"
 #include "pa_split_cfg.h"
 
@@ -75,6 +76,15 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   const uint32_t o = static_cast<uint32_t>(row * SWB + chunk * 16);
   constexpr uint32_t mask = (SWB == 128) ? 7u : 3u;
   return o ^ (((o >> 7) & mask) << 4);
+}
+
+// Counts a finished CTA (thread 0, after its last claim); the last CTA of the
+// grid resets the work counter and this count for the next decode call.
+__device__ __forceinline__ void cta_finished(const SplitParams& p) {
+  if (atomicAdd(p.plan.counters + 5, 1) == static_cast<int>(gridDim.x) - 1) {
+    p.plan.counters[1] = 0;
+    p.plan.counters[5] = 0;
+  }
 }
 
 template <int D, int KVT, int WQ, int KL>
@@ -120,6 +130,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
   pdl_trigger();
   if (blockIdx.x >= static_cast<unsigned>(p.C * p.Hkv)) {  // zero-row CTA
     zero_rows<D>(p, blockIdx.x - p.C * p.Hkv, warp, Cfg::THREADS / 32, lane);
+    if (p.fused && threadIdx.x == 0) cta_finished(p);
     return;
   }
   // Items (piece, kv head) are numbered piece-major: item i is piece i / Hkv,
@@ -924,6 +935,11 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
       if (nst > 0 && lane == 0) mbar_arrive(bar_empty + 8 * xbuf);  // this warp is done with it
     }
     }  // exchange epilogue
+    // Fused merge: the consumers of the CTA that finished a request's last
+    // piece (of a group) combine the pieces' partials while the producer
+    // issues the next item's first stages.
+    if (p.fused && prow_base >= 0 && pass == npass - 1)
+      fused_merge<D>(p, r, h, prow_base, row0, ct, cw, Cfg::NCW, lane);
     __syncthreads();  // pairs with the producer's end-of-pass barrier
   }
   }  // consumers
@@ -937,6 +953,9 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     for (int k = (issued > Cfg::NS ? issued - Cfg::NS : 0); k < issued; ++k)
       mbar_wait(bar_full + 8 * (k % Cfg::NS), (k / Cfg::NS) & 1, p.plan.err, p.wait_ns);
   }
+  // With the merge fused there is no merge kernel to reset the work counter
+  // after this grid: the last CTA to finish does (thread 0 made every claim).
+  if (p.fused && threadIdx.x == 0) cta_finished(p);
 }
 
 template <int D, int KVT, int WQ, int KL>

@@ -103,10 +103,11 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
   // ---- carve the static array: plan arrays, error word, partial results
   // (cutting long slots into pieces needs more partial rows: drop it first)
   pa::PlanLayout lay = pa::plan_layout(num_seqs, num_q_heads, num_kv_heads, head_dim,
-                                       max_query_len, num_tokens, max_partitions, budget, sms, true);
+                                       max_query_len, num_tokens, max_partitions, budget, sms, true,
+                                       false);
   if (lay.total > PA_STATIC_SCRATCH_BYTES)
     lay = pa::plan_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_query_len,
-                          num_tokens, max_partitions, budget, sms, false);
+                          num_tokens, max_partitions, budget, sms, false, false);
   if (lay.total > PA_STATIC_SCRATCH_BYTES)
     return PA_ERR_UNSUPPORTED;  // this batch needs more scratch than the static array holds
   const int G = num_q_heads / num_kv_heads;
@@ -176,6 +177,8 @@ extern "C" int pa_decode_static(const void* q, int q_dtype, int num_tokens, int 
   sp.sinks = nullptr;
   sp.wait_ns = pa::kWaitLimitNs;
   sp.skip_stage = -1;
+  sp.fused = 0;
+  sp.rows_cap = lay.rows_cap;
   sp.scale_log2 = static_cast<float>(static_cast<double>(scale) * (fp8 ? k_scale : 1.0) *
                                      1.4426950408889634);
   sp.v_scale = fp8 ? v_scale : 1.0f;

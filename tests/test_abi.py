@@ -96,6 +96,8 @@ def test_null_handles(lib):
     assert lib.pa_plan_set_window(None, 5) == binding.PA_ERR_INVALID_ARG
     assert lib.pa_plan_set_kv_dtype(None, binding.BF16) == binding.PA_ERR_INVALID_ARG
     assert lib.pa_plan_set_wait_limit(None, 0) == binding.PA_ERR_INVALID_ARG
+    assert lib.pa_plan_set_fused_merge(None, 1) == binding.PA_ERR_INVALID_ARG
+    assert lib.pa_plan_get_fused_merge(None, None) == binding.PA_ERR_INVALID_ARG
     assert lib.pa_plan_skip_stage_for_test(None, -1) == binding.PA_ERR_INVALID_ARG
     assert lib.pa_decode_ex(None, None, 0, 1, 8, 64, None, None, 0, 1.0, 1.0, 1, 2, 16, None, 1,
                             None, None, 1, 1.0, None, binding.K_ROWS, None,

@@ -50,7 +50,8 @@ def test_native_line_has_the_contract_keys():
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0 and cb["sample"]
     e2e = d["e2e"]
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
-    assert d["gpu_launches"] == 3 * 5  # planner, split and merge per step
+    # planner and split kernel per step, and the merge kernel unless it is fused
+    assert d["gpu_launches"] in (2 * 5, 3 * 5)
     assert d["clocks"]["sm_max_mhz"] > 0
 
 

@@ -55,6 +55,7 @@ def batch(dev, lens, ql=None, H=(8, 2), D=128, bs=16, kv="bf16", q="bf16", pad=0
                          kv_scale=0.05, device=dev, **kw)
 
 
+
 # ---------------------------------------------------------------- small sweeps
 
 def test_tiny(dev):
@@ -142,6 +143,72 @@ def test_more_ctas_than_one_wave(dev, case):
     ref = oracle_decode(w.to("cpu"))
     assert max_diff(out, ref) <= TOL[w.kv_dtype]
     assert plan.read_errors() == 0
+
+
+FUSED_CASES = {
+    # every request within one 256-key tile: one piece each, rows written directly
+    "direct": dict(lens=[17, 200, 256, 1, 0], H=(8, 2)),
+    # up to 8 pieces per request: one level of the ticket tree
+    "few": dict(lens=[3000, 900, 40, 0], H=(8, 2), budget=64, max_partitions=8),
+    # 36 pieces: two levels
+    "two_levels": dict(lens=[9000, 40, 2600], H=(8, 1), budget=4096),
+    # 157 and 36 pieces: three levels
+    "three_levels": dict(lens=[40000, 9000, 300, 1], H=(8, 1), budget=4096),
+    # one slot cut into pieces by the split kernel (budget 32: one partition each)
+    "pieces": dict(lens=[40000] + [300 + 37 * i for i in range(15)], H=(8, 2), budget=32),
+}
+
+
+@pytest.mark.parametrize("case", list(FUSED_CASES))
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_fused_merge(dev, case, kv):
+    """Decode-only plans merge the pieces' partials inside the split kernel
+    (ticket tree of fan-in 8) and launch no merge kernel: the result matches
+    the oracle, matches the separate merge kernel's within the bounds, and a
+    second call on the same plan gives the same bits (every ticket was reset).
+    Sharp queries (q std 6) so that a wrong weight or a lost piece shows."""
+    c = dict(FUSED_CASES[case])
+    lens, H = c.pop("lens"), c.pop("H")
+    w = batch(dev, lens, H=H, kv=kv, seed=81 + len(lens), q_std=6.0, **c)
+    ref = oracle_decode(w.to("cpu"))
+    plan = binding.plan_for(w)
+    assert plan.fused_merge and plan.kernels_per_decode() == 1
+    plan.refresh(w.context_lens)
+    a = binding.decode_workload(plan, w)
+    b = binding.decode_workload(plan, w)
+    torch.cuda.synchronize()
+    assert plan.read_errors() == 0
+    parity(a, ref, None, what=f"fused {case}")
+    assert torch.equal(a, b), "a second fused call differs: tickets not reset"
+    plan.set_fused_merge(False)
+    assert plan.kernels_per_decode() == 2
+    m = binding.decode_workload(plan, w)
+    torch.cuda.synchronize()
+    assert plan.read_errors() == 0
+    parity(m, ref, None, what=f"merge kernel {case}")
+    parity(a, m.float().cpu().numpy(), None, what=f"fused vs merge kernel {case}")
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_fused_merge_with_window_and_sinks(dev, kv):
+    w = batch(dev, [40000, 9000, 300, 1], H=(8, 1), kv=kv, seed=91, budget=4096, q_std=6.0)
+    sinks = np.linspace(-2, 2, 8)
+    for window in (0, 9000):
+        out, plan = run_ext(w, window=window, sinks=sinks)
+        assert plan.fused_merge
+        parity(out, oracle_decode(w.to("cpu"), window=window, sinks=sinks), None, what=window)
+        assert plan.read_errors() == 0
+
+
+def test_multi_token_plans_keep_the_merge_kernel(dev):
+    plan = binding.Plan(3, 6, 1, 256, max_query_len=3, max_tokens=12, device=dev)
+    assert not plan.fused_merge and plan.kernels_per_decode() == 2
+    with pytest.raises(binding.PaError) as e:
+        plan.set_fused_merge(True)
+    assert e.value.status == binding.PA_ERR_UNSUPPORTED
+    # a GQA group of 64 rows is more than one work item holds: no fused merge either
+    plan = binding.Plan(3, 64, 1, 128, device=dev)
+    assert not plan.fused_merge
 
 
 def test_set_kv_dtype_rejects_other_values(dev):
