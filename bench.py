@@ -564,8 +564,7 @@ def run_native(args, world, rank, local):
                    "kv_bytes_per_step": kv_bytes, "plan": "proportional",
                    "budget": info["budget"], "capacity": info["capacity"],
                    "max_partitions": info["max_partitions"],
-                   "step": "plan refresh + pa_decode (split-KV kernel; merge fused into it, "
-                           "or a merge kernel for multi-token plans)",
+                   "step": "plan refresh + pa_decode (split-KV kernel + merge kernel)",
                    "l2": "inputs larger than L2 (no flush)" if kv_bytes > L2_BYTES
                    else "not flushed: inputs fit in L2",
                    "timing": "K steps captured once in a CUDA graph and replayed; decode "
@@ -682,10 +681,10 @@ def sweep(args):
                             "split_frac_of_8tbs": round(kv / (t["split_ms"] * 1e-3) / 8e12, 4),
                             "tasks": int(red[:, 1].sum()), "max_parts": int(red[:, 1].max())}
             res["refresh_us"] = round(time_refresh(w), 2)
-            if plan.fused_merge or _fusable(w):  # A/B: the same plan with the merge kernel
-                t, _ = time_native(w, args.steps, args.warmup, flush=True, fused=False)
-                res["merge_kernel_us_per_decode_call"] = round(t["call_ms"] * 1e3, 2)
-                res["fused_merge_us_per_decode_call"] = res["proportional"]["us_per_decode_call"]
+            if _fusable(w):  # A/B: the same plan with the merge fused into the split kernel
+                t, _ = time_native(w, args.steps, args.warmup, flush=True, fused=True)
+                res["fused_merge_us_per_decode_call"] = round(t["call_ms"] * 1e3, 2)
+                res["merge_kernel_us_per_decode_call"] = res["proportional"]["us_per_decode_call"]
             print(json.dumps(res), flush=True)
             if name == "skewed":
                 skew.append(res)

@@ -377,7 +377,8 @@ int pa_plan_build(pa_plan** plan, int device, int num_seqs, int num_kv_heads, in
   pl->wait_ns = pa::kWaitLimitNs;
   pl->skip_stage = -1;
   pl->fused_ok = lay.fused;
-  pl->fused = lay.fused;
+  pl->fused = 0;  // measured slower than the merge kernel on every batch tried
+
   *plan = pl;
   return PA_OK;
 }

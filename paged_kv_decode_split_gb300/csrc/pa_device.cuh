@@ -203,6 +203,12 @@ __device__ __forceinline__ float fast_exp2(float x) {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
+// GPU-scope acquire-release fence: with a CTA barrier before it, it publishes
+// every write of the CTA's threads that precede the barrier (release), and
+// after an atomic that observed another CTA's release it makes that CTA's
+// writes visible (acquire).
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }

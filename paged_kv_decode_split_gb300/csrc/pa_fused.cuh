@@ -21,10 +21,10 @@
 // at the last level a sink logit joins W once (add_sink), and o is rounded to
 // the output type.
 //
-// Ordering: every consumer thread fences its partial stores before a named
-// barrier of the consumer warps; one thread then fences (release) and takes the
-// ticket; the taker of the last ticket fences again (acquire) before the
-// barrier after which the consumer warps read the partials through L2 (ld.cg).
+// Ordering: a named barrier of the consumer warps orders their partial stores
+// before one thread's GPU-scope release fence and its relaxed ticket atomic;
+// the taker of a group's last ticket fences again (acquire) before the barrier
+// after which the consumer warps read the partials through L2 (ld.cg).
 #pragma once
 
 #include "pa_device.cuh"
@@ -146,7 +146,6 @@ __device__ void fused_merge(const SplitParams& p, int r, int h, int prow, int or
   const int base = pq.x;
   int k = prow - base;             // this piece's index, then its group's at each level
   int K = pq.y;                    // items at this level
-  __threadfence();                 // this thread's partial stores, GPU-wide
   for (int level = 0;; ++level) {
     const int first = (k >> kFusedLog2FanIn) << kFusedLog2FanIn;
     const int count = min(kFusedFanIn, K - first);
@@ -155,12 +154,12 @@ __device__ void fused_merge(const SplitParams& p, int r, int h, int prow, int or
       int* t = p.plan.tickets +
                (static_cast<long long>(level) * p.rows_cap +
                 (base + (first << (kFusedLog2FanIn * level)))) * p.Hkv + h;
-      __threadfence();  // release: the partials above precede the ticket
+      fence_acq_rel_gpu();  // release: the CTA's partials above precede the ticket
       const int prev = atomicAdd(t, 1);
       const int last = prev == count - 1;
       if (last) {
-        *t = 0;          // the group is complete: ready for the next decode call
-        __threadfence(); // acquire: the other pieces' partials are visible
+        *t = 0;               // the group is complete: ready for the next decode call
+        fence_acq_rel_gpu();  // acquire: the other pieces' partials are visible
       }
       s_last = last;
     }
@@ -169,7 +168,6 @@ __device__ void fused_merge(const SplitParams& p, int r, int h, int prow, int or
     const bool final = K <= kFusedFanIn;
     fused_merge_group<D>(p, h, base, first, count, level, final, orow, cw, ncw, lane);
     if (final) return;
-    __threadfence();
     k >>= kFusedLog2FanIn;
     K = (K + kFusedFanIn - 1) >> kFusedLog2FanIn;
   }

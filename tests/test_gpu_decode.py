@@ -162,7 +162,7 @@ FUSED_CASES = {
 @pytest.mark.parametrize("case", list(FUSED_CASES))
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
 def test_fused_merge(dev, case, kv):
-    """Decode-only plans merge the pieces' partials inside the split kernel
+    """Decode-only plans can merge the pieces' partials inside the split kernel
     (ticket tree of fan-in 8) and launch no merge kernel: the result matches
     the oracle, matches the separate merge kernel's within the bounds, and a
     second call on the same plan gives the same bits (every ticket was reset).
@@ -172,6 +172,8 @@ def test_fused_merge(dev, case, kv):
     w = batch(dev, lens, H=H, kv=kv, seed=81 + len(lens), q_std=6.0, **c)
     ref = oracle_decode(w.to("cpu"))
     plan = binding.plan_for(w)
+    assert not plan.fused_merge  # the merge kernel is the default
+    plan.set_fused_merge(True)
     assert plan.fused_merge and plan.kernels_per_decode() == 1
     plan.refresh(w.context_lens)
     a = binding.decode_workload(plan, w)
@@ -194,7 +196,7 @@ def test_fused_merge_with_window_and_sinks(dev, kv):
     w = batch(dev, [40000, 9000, 300, 1], H=(8, 1), kv=kv, seed=91, budget=4096, q_std=6.0)
     sinks = np.linspace(-2, 2, 8)
     for window in (0, 9000):
-        out, plan = run_ext(w, window=window, sinks=sinks)
+        out, plan = run_ext(w, window=window, sinks=sinks, fused=True)
         assert plan.fused_merge
         parity(out, oracle_decode(w.to("cpu"), window=window, sinks=sinks), None, what=window)
         assert plan.read_errors() == 0
@@ -219,8 +221,10 @@ def test_set_kv_dtype_rejects_other_values(dev):
 
 # ------------------------------------------------- sliding window and sinks
 
-def run_ext(w, window=0, sinks=None, budget=None, max_partitions=None):
+def run_ext(w, window=0, sinks=None, budget=None, max_partitions=None, fused=False):
     plan = binding.plan_for(w, binding.PROPORTIONAL, budget, max_partitions)
+    if fused:
+        plan.set_fused_merge(True)
     plan.set_window(window)
     plan.refresh(w.context_lens, w.cu_query_lens)
     sk = None if sinks is None else torch.tensor(sinks, dtype=torch.float32, device=w.q.device)
