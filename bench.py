@@ -67,6 +67,9 @@ DESCRIBE = {
     "uniform_d512": "uniform decode: 16 seqs x 8192 ctx, Hq/Hkv 32/4, D 512, page 16, bf16",
     "uniform_d1024": "uniform decode: 16 seqs x 8192 ctx, Hq/Hkv 32/4, D 1024, page 16, bf16",
     "uniform_n64_h8": "uniform decode: 64 seqs x 4096 ctx, Hq/Hkv 64/8, D 128, page 16, bf16",
+    "skewed_mtp3": "MTP verify on the skewed agentic batch: 32 seqs x 3 query tokens, ctx "
+                   "lognormal(4096, 1.5) in [64,131072], Hq/Hkv 32/4, D 128, page 16, fp8-e4m3 KV "
+                   "(scale 0.05), budget 296, cap 256",
     "skewed_d1024": "skewed agentic decode: 32 seqs, ctx lognormal(4096, 1.5) in [64,131072], "
                     "Hq/Hkv 16/2, D 1024, page 16, fp8-e4m3 KV (scale 0.05), K grouped, "
                     "budget 296, cap 256",

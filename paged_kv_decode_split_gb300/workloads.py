@@ -204,6 +204,19 @@ def skewed(seed: int = 0, device="cpu") -> Workload:
     return w
 
 
+def skewed_mtp3(seed: int = 0, device="cpu") -> Workload:
+    """MTP verify on the skewed agentic batch: the skewed lengths (32 requests,
+    lognormal median 4096, sigma 1.5, clipped to [64, 131072]), 3 query tokens
+    per request (the target token and two drafts), Hq/Hkv 32/4, D 128, page 16,
+    fp8 e4m3fn KV (scale 0.05), bf16 q, budget 2 x 148, cap 256 -- the pages'
+    production shape, fp8 page-16 KV with speculative-decoding verify rows."""
+    lens = lognormal_lengths(32, 4096, 1.5, 64, 131072, seed)
+    w = make_batch("skewed_mtp3", lens, [3] * 32, 32, 4, 128, 16, "fp8", seed=seed,
+                   kv_scale=0.05, device=device, budget=296, max_partitions=256)
+    w.meta["max_over_min"] = max(lens) / min(lens)
+    return w
+
+
 def mtp_verify(seed: int = 0, device="cpu", pad_tokens: int = 8) -> Workload:
     """MTP verify: 8 requests x 3 query tokens at 16384 context, Hq/Hkv 6/1, D 256,
     page 64, bf16, per-token causal ranges, graph padding rows after cu[-1]."""
@@ -317,6 +330,7 @@ CONFIGS["uniform_d512"] = uniform_d512
 CONFIGS["uniform_d1024"] = uniform_d1024
 CONFIGS["skewed_d1024"] = skewed_d1024
 CONFIGS["uniform_n64_h8"] = uniform_n64_h8
+CONFIGS["skewed_mtp3"] = skewed_mtp3
 
 
 @dataclass

@@ -419,6 +419,37 @@ def test_verify_row_groups(dev, ql):
     check(batch(dev, [5000, 900, 64], ql=[ql] * 3, H=(8, 1), D=128, kv="fp8", seed=ql))
 
 
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("ql,H", [(2, (8, 1)), (3, (8, 1)), (3, (6, 1)), (2, (12, 2))])
+@pytest.mark.parametrize("bs", [16, 64])
+def test_fp8_verify_rows_convert_once(dev, D, ql, H, bs):
+    """fp8 caches with two or three query-row groups per pass: each consumer
+    warp takes every row group for a 64-dim slice of its keys and converts
+    each e4m3 element once; the slices' logits are summed per 16-key tile.
+    Ragged lengths (one-key requests, rows with no visible key, a zero-length
+    request), graph padding, fp16 and bf16 q, against the oracle."""
+    lens = [5000, 900, 64, 1, 2, 257, 3000]
+    q = "fp16" if (D + ql) % 2 else "bf16"
+    w = batch(dev, lens, ql=[ql] * len(lens), H=H, D=D, bs=bs, kv="fp8", q=q, pad=3,
+              seed=D + 10 * ql + bs)
+    out, _, _ = check(w)
+    assert torch.all(out[int(w.cu_query_lens[-1]):] == 0)
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_fp8_verify_rows_convert_once_window_sinks_sharp(dev, D):
+    """The same path with a sliding window, sinks, partitions merged by the
+    merge kernel (a few and many), and sharp queries."""
+    w = batch(dev, [20000, 700, 3000, 0], ql=[3, 3, 3, 1], H=(8, 1), D=D, kv="fp8", pad=2,
+              seed=D + 7, q_std=6.0)
+    sinks = np.linspace(-2, 2, 8)
+    for window, P, W in ((0, 256, 2048), (500, 8, 64), (9000, 256, 2048)):
+        out, plan = run_ext(w, window=window, sinks=sinks, budget=W, max_partitions=P)
+        parity(out, oracle_decode(w.to("cpu"), window=window, sinks=sinks), None,
+               what=(window, P))
+        assert plan.read_errors() == 0
+
+
 def test_cu_arange_matches_no_cu(dev):
     w = batch(dev, RAGGED, H=(8, 2), D=128, seed=9)
     a, _ = run(w)
@@ -708,7 +739,7 @@ def _pick(w, k=4):
 
 FULL = ["uniform", "skewed", "mtp_verify", "mixed_prompt", "large_bf16", "large_fp8",
         "uniform_w1024", "skewed_w4096", "uniform_k5", "skewed_k5", "uniform_d512",
-        "skewed_d1024", "uniform_d1024", "uniform_n64_h8"]
+        "skewed_d1024", "uniform_d1024", "uniform_n64_h8", "skewed_mtp3"]
 
 
 @pytest.mark.parametrize("name", FULL)
