@@ -379,66 +379,6 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     const int kb = cg.kb;                // first key of the piece
     const int ke_task = cg.ke_task;
     auto pass_key_end = [&](int pass) { return geo_key_end(cg, pass); };
-    // Exchange epilogue, last step: combine the key warps' (m, l, O) of every
-    // row of the pass from shared memory and write the output row (a single
-    // piece: with its head's sink) or the normalised partial and its log2-sum-exp.
-    auto combine_exchange = [&](int pass_base, const float* ex_o, const float* ex_m,
-                                const float* ex_l, int ct) {
-      const float NEG_INF = -__int_as_float(0x7f800000);
-      constexpr int D4 = D / 4;
-      for (int u = ct; u < WQ * 8 * D4; u += Cfg::NCW * 32) {
-        const int gq = u / (8 * D4);
-        const int col = (u / D4) % 8;
-        const int d4 = (u % D4) * 4;
-        const int n = pass_base + 8 * gq + col;
-        if (n >= row_hi) continue;
-        float M = NEG_INF;
-#pragma unroll
-        for (int k = 0; k < Cfg::WK; ++k) M = fmaxf(M, ex_m[(gq * Cfg::WK + k) * 8 + col]);
-        float lsum = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-        if (M != NEG_INF) {
-#pragma unroll
-          for (int k = 0; k < Cfg::WK; ++k) {
-            const int ws = (gq * Cfg::WK + k) * 8 + col;
-            const float w = fast_exp2(ex_m[ws] - M);
-            const float4 v = *reinterpret_cast<const float4*>(ex_o + ws * Cfg::DP + d4);
-            lsum += w * ex_l[ws];
-            o0 += w * v.x; o1 += w * v.y; o2 += w * v.z; o3 += w * v.w;
-          }
-        }
-        const int tok = n / G;
-        const int hq = h * G + n % G;
-        // A single piece writes the output row: its head's sink joins here (a
-        // request with several pieces gets it in the merge).
-        if (prow_base < 0 && p.sinks) {
-          const float f = add_sink(M, __ldg(p.sinks + hq) * 1.4426950408889634f, lsum);
-          o0 *= f; o1 *= f; o2 *= f; o3 *= f;
-        }
-        const float inv = lsum > 0.f ? p.v_scale / lsum : 0.f;
-        o0 *= inv; o1 *= inv; o2 *= inv; o3 *= inv;
-        if (prow_base < 0) {
-          const int trow = row0 + tok;
-          if (trow >= p.num_tokens) {
-            atomicOr(p.plan.err, PA_DEVERR_PLAN_OVERFLOW);
-            continue;
-          }
-          uint2 pk;
-          if (p.out_f16) {
-            pk.x = pack2<false>(o0, o1);
-            pk.y = pack2<false>(o2, o3);
-          } else {
-            pk.x = pack2<true>(o0, o1);
-            pk.y = pack2<true>(o2, o3);
-          }
-          *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) +
-                                    (static_cast<size_t>(trow) * p.Hq + hq) * D + d4) = pk;
-        } else {
-          const size_t prow = static_cast<size_t>(prow_base + tok) * p.Hq + hq;
-          *reinterpret_cast<float4*>(p.plan.part_o + prow * D + d4) = make_float4(o0, o1, o2, o3);
-          if (d4 == 0) p.plan.part_lse[prow] = lsum > 0.f ? M + __log2f(lsum) : NEG_INF;
-        }
-      }
-    };
 
   if (warp < Cfg::NPW) {
     // ------------------------------------------------------------ producer
@@ -497,323 +437,6 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
       }
       __syncthreads();  // pairs with the consumers' end-of-pass barrier
     }
-  } else if constexpr (Cfg::kShareCvt) {
-  // ---------------------------------------- consumers, fp8 converted once
-  // Consumer warp (wk, wd): tiles wk*T .. wk*T + T-1 of every stage, head dims
-  // [64 wd, 64 wd + 64), every query-row group of the pass (R of them).  Each
-  // e4m3 K / V element of a tile is converted to fp16 by one warp only, and
-  // the converted fragment feeds one MMA per row group.  The ND slice warps of
-  // a key warp sum their partial logits through shared memory (slice order,
-  // so all hold identical logits and softmax state) once per 16-key tile.
-  constexpr int R = Cfg::RW;
-  const int cw = warp - Cfg::NPW;
-  const int wk = cw % Cfg::WK;
-  const int wd = cw / Cfg::WK;
-  const int g = lane >> 2;  // MMA groupID
-  const int t = lane & 3;   // MMA thread-in-group
-  const float sl2 = p.scale_log2;
-  const float NEG_INF = -__int_as_float(0x7f800000);
-  constexpr float kRescale = 8.f;  // lazy-rescale threshold, log2 units
-  const int ct = threadIdx.x - 32 * Cfg::NPW;
-  constexpr int SPB = Cfg::SWB / 64;  // 64-dim slices per column block
-  // K: this thread reads 16-byte chunk (wd % SPB) * 4 + t of its key rows --
-  // dims 64 wd + 16 t .. + 15 -- so word j of it is k-step j of the slice.
-  const uint32_t kcol = static_cast<uint32_t>((wd / SPB) * Cfg::BLOCK_BYTES);
-  const int kchunk = (wd % SPB) * 4 + t;
-  int xpar = 0;  // parity of the logit-exchange buffer (one flip per exchanged tile)
-
-  for (int pass = 0; pass < npass; ++pass) {
-    const int pass_base = row_lo + pass * NQ;
-    const int ke = pass_key_end(pass);
-    const int nst = ke > kb ? (ke - kb + Cfg::KS - 1) / Cfg::KS : 0;
-
-    // Key limits of this thread's rows 2t, 2t+1 of each row group.
-    int lim[R][2], llo[R][2];
-    int vis_lo = 0, vis_hi = 0x7fffffff;
-#pragma unroll
-    for (int rg = 0; rg < R; ++rg) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int n = pass_base + 8 * rg + 2 * t + e;
-        const int K = S - (L - 1 - n / G);
-        lim[rg][e] = (n < row_hi) ? min(ke_task, K) : kb;
-        llo[rg][e] = p.window > 0 ? max(0, K - p.window) : 0;
-        if (n < row_hi) {  // padding rows are masked only where some real row is
-          vis_lo = max(vis_lo, llo[rg][e]);
-          vis_hi = min(vis_hi, lim[rg][e]);
-        }
-      }
-    }
-
-    // Q^T fragments (fp16): row pass_base + 8 rg + g, k-step j = dims
-    // 64 wd + 16 t + 4 j + {0, 1 | 2, 3}.
-    uint32_t qf[R][4][2];
-#pragma unroll
-    for (int rg = 0; rg < R; ++rg) {
-      const int n = pass_base + 8 * rg + g;
-      const int tok = n / G;
-      const bool ok = n < row_hi && row0 + tok < p.num_tokens;
-      const size_t qoff = ok ? (static_cast<size_t>(row0 + tok) * p.Hq + h * G + n % G) * D : 0;
-      const uint4* qp = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + qoff +
-                                                       64 * wd + 16 * t);
-      const uint4 qa = ok ? qp[0] : make_uint4(0u, 0u, 0u, 0u);
-      const uint4 qb = ok ? qp[1] : make_uint4(0u, 0u, 0u, 0u);
-      const uint32_t w[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (p.out_f16) {  // fp16 q: the fragment words are q's own
-          qf[rg][i / 2][i % 2] = w[i];
-        } else {
-          const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
-          qf[rg][i / 2][i % 2] = pack2<false>(__low2float(b), __high2float(b));
-        }
-      }
-    }
-
-    float m[R][2], l[R][2], acc[R][4][4];
-#pragma unroll
-    for (int rg = 0; rg < R; ++rg) {
-      m[rg][0] = m[rg][1] = NEG_INF;
-      l[rg][0] = l[rg][1] = 0.f;
-#pragma unroll
-      for (int dt = 0; dt < 4; ++dt) acc[rg][dt][0] = acc[rg][dt][1] = acc[rg][dt][2] = acc[rg][dt][3] = 0.f;
-    }
-    const bool warp_active = pass_base < row_hi;
-
-    for (int s = 0; s < nst; ++s) {
-      const int sit = it + s;
-      const int buf = sit % Cfg::NS;
-      const int key0 = kb + s * Cfg::KS;
-      const int rbase = wk * T * 16;  // row of this warp's first key in the stage
-      const bool live = !aborted() && wait_all(bar_full + 8 * buf, (sit / Cfg::NS) & 1);
-      const uint32_t kt = base + buf * Cfg::STAGE_BYTES;
-      const uint32_t vt = kt + Cfg::TILE_BYTES;
-#pragma unroll 1
-      for (int tt = 0; tt < T; ++tt) {
-        const int k0 = key0 + rbase + 16 * tt;  // the tile's first key
-        // the same for every slice warp of this key warp: they meet at the exchange
-        if (!warp_active || k0 >= ke) continue;
-        float c[R][4];
-#pragma unroll
-        for (int rg = 0; rg < R; ++rg) c[rg][0] = c[rg][1] = c[rg][2] = c[rg][3] = 0.f;
-        if (live) {
-          // ---- S^T[16 keys x 8 rows] per row group, this slice's dims
-          const uint32_t ko = kt + kcol + static_cast<uint32_t>((rbase + 16 * tt) * Cfg::SWB);
-          const uint4 x = lds128(ko + swz<Cfg::SWB>(g, kchunk));
-          const uint4 y = lds128(ko + 8 * Cfg::SWB + swz<Cfg::SWB>(g, kchunk));
-          const uint32_t wx[4] = {x.x, x.y, x.z, x.w};
-          const uint32_t wy[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint32_t a0, a1, a2, a3;
-            e4m3x4_to_f16x2x2(wx[j], a0, a2);
-            e4m3x4_to_f16x2x2(wy[j], a1, a3);
-#pragma unroll
-            for (int rg = 0; rg < R; ++rg) mma16816<false>(c[rg], a0, a1, a2, a3, qf[rg][j][0], qf[rg][j][1]);
-          }
-        }
-        if constexpr (Cfg::ND > 1) {
-          float4* xs = sx + (xpar * Cfg::WK + wk) * Cfg::ND * R * 32;
-          xpar ^= 1;
-#pragma unroll
-          for (int rg = 0; rg < R; ++rg)
-            xs[(wd * R + rg) * 32 + lane] = make_float4(c[rg][0], c[rg][1], c[rg][2], c[rg][3]);
-          named_barrier_sync(2 + wk, Cfg::ND * 32);
-#pragma unroll
-          for (int rg = 0; rg < R; ++rg) {
-            float4 a = xs[rg * 32 + lane];
-#pragma unroll
-            for (int k = 1; k < Cfg::ND; ++k) {
-              const float4 b = xs[(k * R + rg) * 32 + lane];
-              a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
-            }
-            c[rg][0] = a.x; c[rg][1] = a.y; c[rg][2] = a.z; c[rg][3] = a.w;
-          }
-        }
-        if (!live) continue;  // an abandoned stage: the exchange above was still met
-
-        // ---- online softmax per row group (log2 domain, lazily rescaled)
-        const bool full = k0 >= vis_lo && k0 + 16 <= vis_hi;  // no key masked for any row
-        uint32_t pb[R][2];
-#pragma unroll
-        for (int rg = 0; rg < R; ++rg) {
-          float sv[4];
-          if (full) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sv[e] = c[rg][e] * sl2;
-          } else {
-            const int k_lo = k0 + g;
-            sv[0] = (k_lo < lim[rg][0] && k_lo >= llo[rg][0]) ? c[rg][0] * sl2 : NEG_INF;
-            sv[1] = (k_lo < lim[rg][1] && k_lo >= llo[rg][1]) ? c[rg][1] * sl2 : NEG_INF;
-            sv[2] = (k_lo + 8 < lim[rg][0] && k_lo + 8 >= llo[rg][0]) ? c[rg][2] * sl2 : NEG_INF;
-            sv[3] = (k_lo + 8 < lim[rg][1] && k_lo + 8 >= llo[rg][1]) ? c[rg][3] * sl2 : NEG_INF;
-          }
-          float mx0 = fmaxf(sv[0], sv[2]), mx1 = fmaxf(sv[1], sv[3]);
-#pragma unroll
-          for (int o = 4; o <= 16; o <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-          }
-          const bool up0 = mx0 > m[rg][0] + kRescale;
-          const bool up1 = mx1 > m[rg][1] + kRescale;
-          if (__any_sync(0xffffffffu, up0 || up1)) {
-            const float al0 = up0 ? fast_exp2(m[rg][0] - mx0) : 1.f;  // 0 when m was -inf
-            const float al1 = up1 ? fast_exp2(m[rg][1] - mx1) : 1.f;
-            if (up0) m[rg][0] = mx0;
-            if (up1) m[rg][1] = mx1;
-            l[rg][0] *= al0;
-            l[rg][1] *= al1;
-#pragma unroll
-            for (int dt = 0; dt < 4; ++dt) {
-              acc[rg][dt][0] *= al0;
-              acc[rg][dt][1] *= al1;
-              acc[rg][dt][2] *= al0;
-              acc[rg][dt][3] *= al1;
-            }
-          }
-          const float ref0 = (m[rg][0] == NEG_INF) ? 0.f : m[rg][0];
-          const float ref1 = (m[rg][1] == NEG_INF) ? 0.f : m[rg][1];
-          const float p0 = fast_exp2(sv[0] - ref0);
-          const float p1 = fast_exp2(sv[1] - ref1);
-          const float p2 = fast_exp2(sv[2] - ref0);
-          const float p3 = fast_exp2(sv[3] - ref1);
-          l[rg][0] += p0 + p2;
-          l[rg][1] += p1 + p3;
-          pb[rg][0] = movmatrix_trans(pack2<false>(p0, p1));
-          pb[rg][1] = movmatrix_trans(pack2<false>(p2, p3));
-        }
-
-        // ---- O^T[this slice's 64 dims x 8 rows] += V^T P^T per row group.
-        // d = 64 wd + 32 u + 4 g + e: e = 0 / 1 -> tile 2u rows g / g+8,
-        // e = 2 / 3 -> tile 2u+1 rows g / g+8.  Keys past `ke` are zeroed.
-        const int ra = rbase + 16 * tt + 2 * t;
-        const bool tail = k0 + 16 > ke;
-        const int kq = k0 + 2 * t;
-        const uint32_t z0 = (kq < ke) ? 0xffffffffu : 0u, z1 = (kq + 1 < ke) ? 0xffffffffu : 0u;
-        const uint32_t z8 = (kq + 8 < ke) ? 0xffffffffu : 0u, z9 = (kq + 9 < ke) ? 0xffffffffu : 0u;
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int byte = 64 * wd + 32 * u + 4 * g;
-          const uint32_t blk = vt + static_cast<uint32_t>((byte / Cfg::SWB) * Cfg::BLOCK_BYTES);
-          const int inb = byte % Cfg::SWB;
-          const uint32_t wsub = static_cast<uint32_t>(inb & 15);
-          uint32_t w0 = lds32(blk + swz<Cfg::SWB>(ra, inb >> 4) + wsub);
-          uint32_t w1 = lds32(blk + swz<Cfg::SWB>(ra + 1, inb >> 4) + wsub);
-          uint32_t w8 = lds32(blk + swz<Cfg::SWB>(ra + 8, inb >> 4) + wsub);
-          uint32_t w9 = lds32(blk + swz<Cfg::SWB>(ra + 9, inb >> 4) + wsub);
-          if (tail) {
-            w0 &= z0; w1 &= z1; w8 &= z8; w9 &= z9;
-          }
-          uint32_t x0, x1, y0, y1, u0, u1, v0, v1;
-          e4m3x4_to_f16x2x2(prmt(w0, w1, 0x5140u), x0, x1);  // d+0, d+1; keys 2t,2t+1
-          e4m3x4_to_f16x2x2(prmt(w0, w1, 0x7362u), y0, y1);  // d+2, d+3
-          e4m3x4_to_f16x2x2(prmt(w8, w9, 0x5140u), u0, u1);  // keys 2t+8, 2t+9
-          e4m3x4_to_f16x2x2(prmt(w8, w9, 0x7362u), v0, v1);
-#pragma unroll
-          for (int rg = 0; rg < R; ++rg) {
-            mma16816<false>(acc[rg][2 * u], x0, x1, u0, u1, pb[rg][0], pb[rg][1]);
-            mma16816<false>(acc[rg][2 * u + 1], y0, y1, v0, v1, pb[rg][0], pb[rg][1]);
-          }
-        }
-      }  // tiles
-      __syncwarp();
-      if (live && lane == 0 && !(Cfg::kHoldSlot && s == nst - 1)) mbar_arrive(bar_empty + 8 * buf);
-    }
-    const int xbuf = (nst > 0 ? it + nst - 1 : it) % Cfg::NS;
-    it += nst;
-
-    // ------------------------------------------------------------ epilogue
-#pragma unroll
-    for (int rg = 0; rg < R; ++rg) {
-#pragma unroll
-      for (int o = 4; o <= 16; o <<= 1) {
-        l[rg][0] += __shfl_xor_sync(0xffffffffu, l[rg][0], o);
-        l[rg][1] += __shfl_xor_sync(0xffffffffu, l[rg][1], o);
-      }
-    }
-    if constexpr (Cfg::kDirectEpi) {
-      // One key warp: each slice warp scales and stores its own dims of every
-      // row (the slice warps hold the same m and l).
-#pragma unroll
-      for (int rg = 0; rg < R; ++rg) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int n = pass_base + 8 * rg + 2 * t + e;
-          if (n >= row_hi) continue;
-          const int tok = n / G;
-          const int hq = h * G + n % G;
-          const float M = m[rg][e];
-          float lsum = M != NEG_INF ? l[rg][e] : 0.f;
-          const bool sink = prow_base < 0 && p.sinks != nullptr;
-          const float f = sink ? add_sink(M, __ldg(p.sinks + hq) * 1.4426950408889634f, lsum) : 1.f;
-          const float inv = lsum > 0.f ? p.v_scale / lsum : 0.f;
-          auto fin = [&](float v) {
-            if (M == NEG_INF) v = 0.f;
-            if (sink) v *= f;
-            return v * inv;
-          };
-          if (prow_base < 0) {
-            const int trow = row0 + tok;
-            if (trow >= p.num_tokens) {
-              atomicOr(p.plan.err, PA_DEVERR_PLAN_OVERFLOW);
-              continue;
-            }
-            uint16_t* orow = static_cast<uint16_t*>(p.out) + (static_cast<size_t>(trow) * p.Hq + hq) * D;
-#pragma unroll
-            for (int dt = 0; dt < 4; ++dt) {
-              const int d = 64 * wd + 32 * (dt / 2) + 4 * g + 2 * (dt % 2);
-              const float v0 = fin(acc[rg][dt][e]), v1 = fin(acc[rg][dt][2 + e]);
-              *reinterpret_cast<uint32_t*>(orow + d) = p.out_f16 ? pack2<false>(v0, v1) : pack2<true>(v0, v1);
-            }
-          } else {
-            const size_t prow = static_cast<size_t>(prow_base + tok) * p.Hq + hq;
-            float* po = p.plan.part_o + prow * D;
-#pragma unroll
-            for (int dt = 0; dt < 4; ++dt) {
-              const int d = 64 * wd + 32 * (dt / 2) + 4 * g + 2 * (dt % 2);
-              *reinterpret_cast<float2*>(po + d) = make_float2(fin(acc[rg][dt][e]), fin(acc[rg][dt][2 + e]));
-            }
-            if (g == 0 && wd == 0) p.plan.part_lse[prow] = lsum > 0.f ? M + __log2f(lsum) : NEG_INF;
-          }
-        }
-      }
-    } else {
-      named_barrier_sync(1, Cfg::NCW * 32);  // all stage reads of this pass done
-      // exchange area: O [WQ][WK][8][DP], then m and l [WQ][WK][8]
-      float* ex_o = Cfg::kHoldSlot ? ex + xbuf * (Cfg::STAGE_BYTES / 4) : ex;
-      float* ex_m = ex_o + WQ * Cfg::WK * 8 * Cfg::DP;
-      float* ex_l = ex_m + WQ * Cfg::WK * 8;
-#pragma unroll
-      for (int rg = 0; rg < R; ++rg) {
-        const int wslot = (rg * Cfg::WK + wk) * 8;
-#pragma unroll
-        for (int dt = 0; dt < 4; ++dt) {
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int d = 64 * wd + 32 * (dt / 2) + 4 * g + 2 * (dt % 2) + hh;
-            ex_o[(wslot + 2 * t) * Cfg::DP + d] = acc[rg][dt][2 * hh];
-            ex_o[(wslot + 2 * t + 1) * Cfg::DP + d] = acc[rg][dt][2 * hh + 1];
-          }
-        }
-        if (g == 0 && wd == 0) {  // every slice warp holds the same m and l
-          ex_m[wslot + 2 * t] = m[rg][0];
-          ex_m[wslot + 2 * t + 1] = m[rg][1];
-          ex_l[wslot + 2 * t] = l[rg][0];
-          ex_l[wslot + 2 * t + 1] = l[rg][1];
-        }
-      }
-      named_barrier_sync(1, Cfg::NCW * 32);
-      combine_exchange(pass_base, ex_o, ex_m, ex_l, ct);
-      fence_proxy_async_smem();  // exchange writes precede the next pass's TMA writes
-      if constexpr (Cfg::kHoldSlot) {
-        __syncwarp();
-        if (nst > 0 && lane == 0) mbar_arrive(bar_empty + 8 * xbuf);  // this warp is done with it
-      }
-    }
-    if (p.fused && prow_base >= 0 && pass == npass - 1)
-      fused_merge<D>(p, r, h, prow_base, row0, ct, cw, Cfg::NCW, lane);
-    __syncthreads();  // pairs with the producer's end-of-pass barrier
-  }
   } else {
   // -------------------------------------------------------------- consumers
   const int cw = warp - Cfg::NPW;
@@ -1253,7 +876,59 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     }
     named_barrier_sync(1, Cfg::NCW * 32);
 
-    combine_exchange(pass_base, ex_o, ex_m, ex_l, ct);
+    constexpr int D4 = D / 4;
+    for (int u = ct; u < WQ * 8 * D4; u += Cfg::NCW * 32) {
+      const int gq = u / (8 * D4);
+      const int col = (u / D4) % 8;
+      const int d4 = (u % D4) * 4;
+      const int n = pass_base + 8 * gq + col;
+      if (n >= row_hi) continue;
+      float M = NEG_INF;
+#pragma unroll
+      for (int k = 0; k < Cfg::WK; ++k) M = fmaxf(M, ex_m[(gq * Cfg::WK + k) * 8 + col]);
+      float lsum = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+      if (M != NEG_INF) {
+#pragma unroll
+        for (int k = 0; k < Cfg::WK; ++k) {
+          const int ws = (gq * Cfg::WK + k) * 8 + col;
+          const float w = fast_exp2(ex_m[ws] - M);
+          const float4 v = *reinterpret_cast<const float4*>(ex_o + ws * Cfg::DP + d4);
+          lsum += w * ex_l[ws];
+          o0 += w * v.x; o1 += w * v.y; o2 += w * v.z; o3 += w * v.w;
+        }
+      }
+      const int tok = n / G;
+      const int hq = h * G + n % G;
+      // A single piece writes the output row: its head's sink joins here (a
+      // request with several pieces gets it in the merge).
+      if (prow_base < 0 && p.sinks) {
+        const float f = add_sink(M, __ldg(p.sinks + hq) * 1.4426950408889634f, lsum);
+        o0 *= f; o1 *= f; o2 *= f; o3 *= f;
+      }
+      const float inv = lsum > 0.f ? p.v_scale / lsum : 0.f;
+      o0 *= inv; o1 *= inv; o2 *= inv; o3 *= inv;
+      if (prow_base < 0) {
+        const int trow = row0 + tok;
+        if (trow >= p.num_tokens) {
+          atomicOr(p.plan.err, PA_DEVERR_PLAN_OVERFLOW);
+          continue;
+        }
+        uint2 pk;
+        if (p.out_f16) {
+          pk.x = pack2<false>(o0, o1);
+          pk.y = pack2<false>(o2, o3);
+        } else {
+          pk.x = pack2<true>(o0, o1);
+          pk.y = pack2<true>(o2, o3);
+        }
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) +
+                                  (static_cast<size_t>(trow) * p.Hq + hq) * D + d4) = pk;
+      } else {
+        const size_t prow = static_cast<size_t>(prow_base + tok) * p.Hq + hq;
+        *reinterpret_cast<float4*>(p.plan.part_o + prow * D + d4) = make_float4(o0, o1, o2, o3);
+        if (d4 == 0) p.plan.part_lse[prow] = lsum > 0.f ? M + __log2f(lsum) : NEG_INF;
+      }
+    }
     fence_proxy_async_smem();  // exchange writes precede the next pass's TMA writes
     if constexpr (Cfg::kHoldSlot) {
       __syncwarp();

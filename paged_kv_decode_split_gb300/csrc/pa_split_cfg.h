@@ -28,23 +28,12 @@ struct SplitCfg {
   // logits and softmax state), and each warp accumulates P V for its own
   // slice.  Stages are one 16-key tile.
   static constexpr bool kWide = D > 256;
-  // fp8 caches with two or three query-row groups (multi-token rows): each
-  // consumer warp takes every row group for one 64-dim slice of its keys, so
-  // each e4m3 element is converted to fp16 once per CTA and the converted
-  // fragment feeds one MMA per row group (with a warp per row group, every
-  // warp converted the same tile again and the conversions bound the kernel).
-  // The slices' partial logits are summed through shared memory per tile.
-  static constexpr bool kShareCvt = kFp8 && KL == 0 && (WQ == 2 || WQ == 3) && D <= 256;
-  static constexpr int RW = kShareCvt ? WQ : 1;       // query-row groups per consumer warp
-  static constexpr int DS = kShareCvt ? 64 : (kWide ? (D % 256 == 0 ? 256 : 128) : D);  // head dims per consumer warp
+  static constexpr int DS = kWide ? (D % 256 == 0 ? 256 : 128) : D;  // head dims per consumer warp
   static constexpr int ND = D / DS;                   // dim slices
-  static constexpr int CBS = DS * ESZ / SWB < 1 ? 1 : DS * ESZ / SWB;  // column blocks per slice
+  static constexpr int CBS = DS * ESZ / SWB;          // column blocks per slice
   static constexpr int KS = kWide ? 16 : kStageTensorBytes / ROW;  // keys per stage
-  // partial-logit exchange of the dim slices: [parity][WQ][ND][32 lanes] float4
-  // (wide heads: parity of the stage), or [parity][WK][ND][RW][32 lanes] float4
-  // (shared conversion: parity of the tile)
-  static constexpr int SX_BYTES = kWide ? 2 * WQ * ND * 32 * 16
-                                        : (kShareCvt && ND > 1 ? 2 * (256 / D) * ND * RW * 32 * 16 : 0);
+  // partial-logit exchange of the dim slices: [stage parity][WQ][ND][32 lanes] float4
+  static constexpr int SX_BYTES = kWide ? 2 * WQ * ND * 32 * 16 : 0;
   // Ring depth: 3 stages, or 2 where that lets two CTAs share an SM (wide
   // heads of 640 and 768 dims: 3 stages of 40-48 KB need more than half of
   // the SM's 228 KB of shared memory).
@@ -57,14 +46,13 @@ struct SplitCfg {
   // four -- and 1 for three row groups of 256-dim heads (MTP verify: 18-24
   // query rows), whose epilogue then needs no exchange between key warps
   // (measured 7-10% faster there; 2-19% slower for two row groups or 128 dims).
-  static constexpr int WK0 = kShareCvt ? 256 / D
-                            : ((WQ == 1) ? 4 : ((WQ == 4 || (D == 256 && WQ == 3)) ? 1 : 2));
+  static constexpr int WK0 = (WQ == 1) ? 4 : ((WQ == 4 || (D == 256 && WQ == 3)) ? 1 : 2);
   static constexpr int WK = WK0 < MTS ? WK0 : MTS;   // key warps per row group
   static constexpr int T = MTS / WK;                  // tiles one warp handles per stage
   // Every key warp consumes every stage, in order, so a warp never waits on a
   // ring slot's use u+1 before it consumed use u -- which keeps the
   // parity-based mbarrier waits unambiguous.
-  static constexpr int NCW = (WQ / RW) * WK * ND;     // consumer warps
+  static constexpr int NCW = WQ * WK * ND;            // consumer warps
   // Producer warps.  Issuing a stage's copies (one per lane) holds a warp
   // for about 100-140 cycles per 2 KB box, which capped a lone CTA near
   // 25 GB/s with 16-key pages.  Two producers (K copies from one, V copies
@@ -94,8 +82,6 @@ struct SplitCfg {
   static constexpr int MIN_BLOCKS = (THREADS <= 224 && 2 * (SMEM_BYTES + 1024) <= 228 * 1024) ? 2 : 1;
   static_assert(!kWide || (WK == 1 && T == 1 && CBS * SWB == DS * ESZ && WQ <= 2),
                 "sliced head dims: one key warp, one tile per stage, whole column blocks");
-  static_assert(!kShareCvt || (SWB == 128 || D == 64), "shared conversion: 128-byte rows or one slice");
-  static_assert(!kShareCvt || WK <= 4, "shared conversion: slice barriers 2..5");
   static_assert(2 * NS * 8 <= 64, "mbarriers fit before the exchange area");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
   static_assert(KS % 16 == 0 && MTS % WK == 0, "whole 16-key tiles per warp");

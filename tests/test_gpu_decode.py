@@ -422,12 +422,11 @@ def test_verify_row_groups(dev, ql):
 @pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("ql,H", [(2, (8, 1)), (3, (8, 1)), (3, (6, 1)), (2, (12, 2))])
 @pytest.mark.parametrize("bs", [16, 64])
-def test_fp8_verify_rows_convert_once(dev, D, ql, H, bs):
-    """fp8 caches with two or three query-row groups per pass: each consumer
-    warp takes every row group for a 64-dim slice of its keys and converts
-    each e4m3 element once; the slices' logits are summed per 16-key tile.
-    Ragged lengths (one-key requests, rows with no visible key, a zero-length
-    request), graph padding, fp16 and bf16 q, against the oracle."""
+def test_fp8_verify_rows(dev, D, ql, H, bs):
+    """fp8 caches with two or three query-row groups per pass (speculative
+    verify rows on an fp8 cache).  Ragged lengths (one-key requests, rows with
+    no visible key, a zero-length request), graph padding, fp16 and bf16 q,
+    against the oracle."""
     lens = [5000, 900, 64, 1, 2, 257, 3000]
     q = "fp16" if (D + ql) % 2 else "bf16"
     w = batch(dev, lens, ql=[ql] * len(lens), H=H, D=D, bs=bs, kv="fp8", q=q, pad=3,
@@ -437,8 +436,8 @@ def test_fp8_verify_rows_convert_once(dev, D, ql, H, bs):
 
 
 @pytest.mark.parametrize("D", [128, 256])
-def test_fp8_verify_rows_convert_once_window_sinks_sharp(dev, D):
-    """The same path with a sliding window, sinks, partitions merged by the
+def test_fp8_verify_rows_window_sinks_sharp(dev, D):
+    """fp8 verify rows with a sliding window, sinks, partitions merged by the
     merge kernel (a few and many), and sharp queries."""
     w = batch(dev, [20000, 700, 3000, 0], ql=[3, 3, 3, 1], H=(8, 1), D=D, kv="fp8", pad=2,
               seed=D + 7, q_std=6.0)
