@@ -209,7 +209,8 @@ int pa_plan_set_kv_dtype(pa_plan* plan, int kv_dtype);
  * tree until the request's output rows are written -- and pa_decode launches
  * one kernel; enable = 0: a separate merge kernel runs after the split kernel.
  * The fused merge is possible for plans with one query row per request
- * (max_query_len 1) whose GQA group fits one work item of the split kernel;
+ * (max_query_len 1), head_dim at most 256, whose GQA group fits one work item
+ * of the split kernel;
  * every other plan keeps the merge kernel, where a request's many query rows
  * are better spread over many CTAs.  The default is 0 for every plan: on
  * GB300 the merge kernel, chained to the split kernel by programmatic

@@ -139,7 +139,7 @@ __device__ __forceinline__ void fused_merge_group(const SplitParams& p, int h, i
 // written.  Takes this piece's tickets up the tree and merges where it took a
 // group's last one; orow is the request's output row.
 template <int D>
-__device__ void fused_merge(const SplitParams& p, int r, int h, int prow, int orow, int ct, int cw,
+__device__ __noinline__ void fused_merge(const SplitParams& p, int r, int h, int prow, int orow, int ct, int cw,
                             int ncw, int lane) {
   __shared__ int s_last;
   const int2 pq = p.plan.preq[r];  // (first partial row, pieces)

@@ -130,7 +130,8 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
   pdl_trigger();
   if (blockIdx.x >= static_cast<unsigned>(p.C * p.Hkv)) {  // zero-row CTA
     zero_rows<D>(p, blockIdx.x - p.C * p.Hkv, warp, Cfg::THREADS / 32, lane);
-    if (p.fused && threadIdx.x == 0) cta_finished(p);
+    if constexpr (D <= 256)
+      if (p.fused && threadIdx.x == 0) cta_finished(p);
     return;
   }
   // Items (piece, kv head) are numbered piece-major: item i is piece i / Hkv,
@@ -938,8 +939,10 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     // Fused merge: the consumers of the CTA that finished a request's last
     // piece (of a group) combine the pieces' partials while the producer
     // issues the next item's first stages.
-    if (p.fused && prow_base >= 0 && pass == npass - 1)
-      fused_merge<D>(p, r, h, prow_base, row0, ct, cw, Cfg::NCW, lane);
+    if constexpr (D <= 256) {  // wide heads keep the merge kernel (registers)
+      if (p.fused && prow_base >= 0 && pass == npass - 1)
+        fused_merge<D>(p, r, h, prow_base, row0, ct, cw, Cfg::NCW, lane);
+    }
     __syncthreads();  // pairs with the producer's end-of-pass barrier
   }
   }  // consumers
@@ -955,7 +958,8 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
   }
   // With the merge fused there is no merge kernel to reset the work counter
   // after this grid: the last CTA to finish does (thread 0 made every claim).
-  if (p.fused && threadIdx.x == 0) cta_finished(p);
+  if constexpr (D <= 256)
+    if (p.fused && threadIdx.x == 0) cta_finished(p);
 }
 
 template <int D, int KVT, int WQ, int KL>
