@@ -638,8 +638,11 @@ def profile_run(args, dev):
 
 
 def _fusable(w) -> bool:
-    """Whether a workload's plan takes the fused merge (one query row per request)."""
+    """Whether a workload's plan can take the fused merge: one query row per
+    request, head dim at most 256, a GQA group of at most 32 rows."""
     b = w.base if isinstance(w, wl.SparseWorkload) else w
+    if b.head_dim > 256 or b.num_q_heads // b.num_kv_heads > 32:
+        return False
     if b.cu_query_lens is None:
         return True
     cu = b.cu_query_lens.cpu()
