@@ -117,7 +117,14 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     s_abort = 0;
     for (int s = 0; s < Cfg::NS; ++s) {
       mbar_init(bar_full + 8 * s, dual ? 2 : 1);  // one expect-tx arrival per issuing warp
-      mbar_init(bar_empty + 8 * s, Cfg::NCW);
+      // released by every consumer warp, or (tensor-memory path) by the commit
+      // of the stage's P V
+      mbar_init(bar_empty + 8 * s, Cfg::kTc ? 1 : Cfg::NCW);
+    }
+    if constexpr (Cfg::kTc) {
+      mbar_init(bar_full + 16 * Cfg::NS, 1);      // S^T buffer 0 computed
+      mbar_init(bar_full + 16 * Cfg::NS + 8, 1);  // S^T buffer 1 computed
+      mbar_init(base + Cfg::DATA_BYTES + Cfg::TC_ARR_OFF + 1024, 1);  // a P V completed
     }
     fence_barrier_init();
   }
@@ -133,6 +140,12 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     if constexpr (D <= 256)
       if (p.fused && threadIdx.x == 0) cta_finished(p);
     return;
+  }
+  if constexpr (Cfg::kTc) {
+    // 128 columns of tensor memory: S^T buffers [0, 2 TN), O^T [2 TN, 3 TN);
+    // two CTAs per SM take 256 of the SM's 512
+    if (warp == Cfg::NPW) tc_alloc(base + Cfg::DATA_BYTES + Cfg::TC_ARR_OFF + 1032, 128);
+    tc_fence_before();
   }
   // Items (piece, kv head) are numbered piece-major: item i is piece i / Hkv,
   // head i % Hkv.  The first `nst` of them belong to CTAs 0..nst-1, one each,
@@ -343,6 +356,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
   // Producer: stages of the coming pass issued ahead, and the block-table
   // window after them.
   int pre_n = 0, pre_win = 0, pre_cur = -1, pre_nxt = -1;
+  int n_o = 0;  // tensor-memory path: P V commits so far (every consumer thread counts)
 
   for (int round = 0;; ++round) {
     if (round > 0) {  // round 0's item was set up with the prologue
@@ -438,6 +452,317 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
       }
       __syncthreads();  // pairs with the consumers' end-of-pass barrier
     }
+  } else if constexpr (Cfg::kTc) {
+  // ------------------------------- consumers on tensor memory (tcgen05), fp8
+  // One warpgroup.  Per 128-key stage: one thread issues S^T[128 keys x TN
+  // rows] = K Q^T (A = the K tile, K-major; B = q as e4m3 hi and lo) into one
+  // of two TMEM buffers; every thread takes the key of its TMEM lane, masks
+  // its rows, forms the probabilities against a per-row reference (moved,
+  // with the accumulators rescaled, only when a logit exceeds it by more than
+  // 0.8 in log2 units, so that 128 * p stays inside e4m3's range), writes
+  // them as e4m3 hi and lo into the stage's K tile (dead once S is computed);
+  // then the thread issues O^T[128 dims x TN] += V^T P^T (A = the V tile read
+  // as MN-major) and commits it to the ring slot's empty barrier.
+  constexpr int TN = Cfg::TN;
+  const int ct = threadIdx.x - 32 * Cfg::NPW;
+  const int cw = warp - Cfg::NPW;
+  const int quad = warp & 3;               // the TMEM lane quadrant this warp may access
+  const int kk = quad * 32 + lane;         // its key in a stage / its head dim in the epilogue
+  const bool issuer = ct == 0;
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  uint8_t* smb = smem_raw + (base - raw);
+  const uint32_t q_hi = base + Cfg::DATA_BYTES + Cfg::TC_Q_OFF;
+  const uint32_t q_lo = q_hi + TN * 128;
+  int* s_lim = reinterpret_cast<int*>(smb + Cfg::DATA_BYTES + Cfg::TC_ARR_OFF);
+  int* s_llo = s_lim + 32;
+  float* s_mref = reinterpret_cast<float*>(s_llo + 32);
+  float* s_fac = s_mref + 32;              // rescale factors, then row sums
+  float* s_red = s_fac + 32;               // [4 warps][32]
+  const uint32_t bar_s = bar_full + 16 * Cfg::NS;  // [2], one per S buffer
+  const uint32_t bar_o = base + Cfg::DATA_BYTES + Cfg::TC_ARR_OFF + 1024;
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smb + Cfg::DATA_BYTES + Cfg::TC_ARR_OFF + 1032);
+  const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);  // this warp's lanes
+  constexpr uint32_t kIdQK = tc_idesc(0, 0, TN, 128);  // K (K-major) x q (K-major)
+  constexpr uint32_t kIdPV = tc_idesc(1, 0, TN, 128);  // V^T (MN-major) x P (K-major)
+  tc_fence_after();  // the tensor-memory address written at allocation
+
+  for (int pass = 0; pass < npass; ++pass) {
+    const int pass_base = row_lo + pass * NQ;
+    const int ke = pass_key_end(pass);
+    const int nst = ke > kb ? (ke - kb + Cfg::KS - 1) / Cfg::KS : 0;
+
+    // ---- rows of the pass: key limits; q * 2^e as e4m3 hi + lo (exact for
+    // bf16 / fp16 q up to the last bits of elements 2^10 below the largest)
+    if (ct < TN) {
+      const int n = pass_base + ct;
+      const int K = S - (L - 1 - n / G);
+      s_lim[ct] = (ct < NQ && n < row_hi) ? min(ke_task, K) : kb;  // rows past the pass: padding
+      s_llo[ct] = p.window > 0 ? max(0, K - p.window) : 0;
+      s_mref[ct] = NEG_INF;
+    }
+    float qv[32];
+    const int qrow = ct >> 2, qpart = ct & 3;  // 32 head dims [32 qpart, +32) of row qrow
+    float amax = 0.f;
+    {
+      const int n = pass_base + qrow;
+      const int tok = n / G;
+      const bool ok = qrow < NQ && n < row_hi && row0 + tok < p.num_tokens;
+      const size_t qoff = ok ? (static_cast<size_t>(row0 + tok) * p.Hq + h * G + n % G) * D + 32 * qpart : 0;
+      const uint4* qp = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + qoff);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 w = ok ? qp[i] : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float2 f;
+          if (p.out_f16) {
+            f = __half22float2(*reinterpret_cast<const __half2*>(&ws[j]));
+          } else {
+            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&ws[j]);
+            f = make_float2(__low2float(b), __high2float(b));
+          }
+          qv[8 * i + 2 * j] = f.x;
+          qv[8 * i + 2 * j + 1] = f.y;
+          amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0) s_red[cw * 32] = amax;
+    named_barrier_sync(1, 128);
+    amax = fmaxf(fmaxf(s_red[0], s_red[32]), fmaxf(s_red[64], s_red[96]));
+    int qexp = 0;  // q is scaled by 2^qexp: its largest element lands in [128, 256)
+    if (amax > 0.f) {
+      int x;
+      frexpf(amax, &x);
+      qexp = min(100, max(-100, 8 - x));
+    }
+    const float qs = exp2f(static_cast<float>(qexp));
+    if (qrow < TN) {
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {  // two 16-byte chunks (16 dims each) of the row
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const int i = 16 * c + 4 * w;
+          const float a0 = qv[i] * qs, a1 = qv[i + 1] * qs, a2 = qv[i + 2] * qs, a3 = qv[i + 3] * qs;
+          const uint32_t h01 = f32x2_to_e4m3x2(a0, a1), h23 = f32x2_to_e4m3x2(a2, a3);
+          const float2 r01 = e4m3x2_to_f32x2(h01), r23 = e4m3x2_to_f32x2(h23);
+          const uint32_t l01 = f32x2_to_e4m3x2(a0 - r01.x, a1 - r01.y);
+          const uint32_t l23 = f32x2_to_e4m3x2(a2 - r23.x, a3 - r23.y);
+          hw[w] = h01 | (h23 << 16);
+          lw[w] = l01 | (l23 << 16);
+        }
+        const uint32_t off = static_cast<uint32_t>(qrow * 128 + (((2 * qpart + c) ^ (qrow & 7)) << 4));
+        *reinterpret_cast<uint4*>(smb + (q_hi - base) + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(smb + (q_lo - base) + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
+    }
+    fence_proxy_async_smem();  // q is read by the tensor cores
+    named_barrier_sync(1, 128);
+    const float c2 = p.scale_log2 / qs;  // logit (log2 units) = S^T * c2
+    int vis_lo = 0, vis_hi = 0x7fffffff;  // keys every real row of the pass sees
+    for (int j = 0; j < TN; ++j) {
+      if (j < NQ && pass_base + j < row_hi) {
+        vis_lo = max(vis_lo, s_llo[j]);
+        vis_hi = min(vis_hi, s_lim[j]);
+      }
+    }
+
+    float lp[TN];  // this thread's key lane's share of each row's sum of p
+#pragma unroll
+    for (int j = 0; j < TN; ++j) lp[j] = 0.f;
+    bool o_started = false;
+    for (int s = 0; s < nst; ++s) {
+      const int sit = it + s;
+      const int slot = sit % Cfg::NS;
+      const int sb = sit & 1;
+      const uint32_t kt = base + slot * Cfg::STAGE_BYTES;
+      const uint32_t vt = kt + Cfg::TILE_BYTES;
+      const int key0 = kb + s * Cfg::KS;
+      const int nkeys = min(Cfg::KS, ke - key0);
+      // ---- S^T = K q^T (hi, then lo)
+      if (issuer) {
+        if (!aborted()) {
+          if (mbar_wait(bar_full + 8 * slot, (sit / Cfg::NS) & 1, p.plan.err, p.wait_ns)) {
+            tc_fence_after();
+            const uint32_t sd = tmem + static_cast<uint32_t>(sb * TN);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              tc_mma_e4m3(sd, tc_desc(kt + 32 * ks, 16, 1024), tc_desc(q_hi + 32 * ks, 16, 1024), kIdQK,
+                          ks > 0);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              tc_mma_e4m3(sd, tc_desc(kt + 32 * ks, 16, 1024), tc_desc(q_lo + 32 * ks, 16, 1024), kIdQK,
+                          true);
+            tc_commit(bar_s + 8 * sb);
+          } else {
+            *reinterpret_cast<volatile int*>(&s_abort) = 1;
+          }
+        }
+      }
+      const bool live_w = !aborted() && wait_all(bar_s + 8 * sb, (sit >> 1) & 1);
+      // ---- probabilities of this thread's key for every row
+      float t[TN];
+      bool over = false;
+      if (live_w) {
+        tc_fence_after();
+        uint32_t sv[TN];
+        tc_ld<TN>(tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(sb * TN), sv);
+        const int kabs = key0 + kk;
+        const bool full = kk < nkeys && kabs >= vis_lo && kabs < vis_hi;
+#pragma unroll
+        for (int j = 0; j < TN; ++j) {
+          const bool vis = full || (kk < nkeys && kabs < s_lim[j] && kabs >= s_llo[j]);
+          t[j] = vis ? __uint_as_float(sv[j]) * c2 : NEG_INF;
+          over = over || t[j] > s_mref[j] + 0.8f;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < TN; ++j) t[j] = NEG_INF;
+      }
+      // a stage some warp could not read is dropped by all (the pipeline aborts)
+      const bool dead = named_barrier_or(1, 128, !live_w);
+      if (dead && ct == 0) *reinterpret_cast<volatile int*>(&s_abort) = 1;
+      if (named_barrier_or(1, 128, over && !dead)) {
+        // a new reference per row: the running maximum; p, l and O rescaled
+#pragma unroll
+        for (int j = 0; j < TN; ++j) {
+          float m = t[j];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+          if (lane == 0) s_red[cw * 32 + j] = m;
+        }
+        named_barrier_sync(1, 128);
+        if (ct < TN) {
+          const float ms = fmaxf(fmaxf(s_red[ct], s_red[32 + ct]), fmaxf(s_red[64 + ct], s_red[96 + ct]));
+          const float mo = s_mref[ct];
+          const float mn = fmaxf(mo, ms);
+          s_fac[ct] = (mo == NEG_INF) ? 0.f : fast_exp2(mo - mn);
+          s_mref[ct] = mn;
+        }
+        named_barrier_sync(1, 128);
+#pragma unroll
+        for (int j = 0; j < TN; ++j) lp[j] *= s_fac[j];
+        if (o_started) {
+          if (wait_all(bar_o, (n_o - 1) & 1)) {  // the previous stage's P V is complete
+            tc_fence_after();
+            uint32_t ov[TN];
+            tc_ld<TN>(tl + static_cast<uint32_t>(2 * TN), ov);
+#pragma unroll
+            for (int j = 0; j < TN; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * s_fac[j]);
+            tc_st<TN>(tl + static_cast<uint32_t>(2 * TN), ov);
+          }
+        }
+      }
+      // p' = 128 p (at most 2^7.8) as e4m3 hi + lo, rows [j][key] into the K tile
+      if (!dead) {
+        uint8_t* ph = smb + (kt - base);
+        uint8_t* pl = ph + TN * 128;
+        const uint32_t cbyte = static_cast<uint32_t>(kk & 15);
+        const int chunk = kk >> 4;
+#pragma unroll
+        for (int j = 0; j < TN; j += 2) {
+          const float m0 = s_mref[j], m1 = s_mref[j + 1];
+          const float p0 = (t[j] == NEG_INF) ? 0.f : fast_exp2(t[j] - m0);
+          const float p1 = (t[j + 1] == NEG_INF) ? 0.f : fast_exp2(t[j + 1] - m1);
+          lp[j] += p0;
+          lp[j + 1] += p1;
+          const float a0 = 128.f * p0, a1 = 128.f * p1;
+          const uint32_t hi = f32x2_to_e4m3x2(a0, a1);
+          const float2 hr = e4m3x2_to_f32x2(hi);
+          const uint32_t lo = f32x2_to_e4m3x2(a0 - hr.x, a1 - hr.y);
+          const uint32_t o0 = static_cast<uint32_t>(j * 128 + ((chunk ^ (j & 7)) << 4)) + cbyte;
+          const uint32_t o1 = static_cast<uint32_t>((j + 1) * 128 + ((chunk ^ ((j + 1) & 7)) << 4)) + cbyte;
+          ph[o0] = static_cast<uint8_t>(hi & 0xffu);
+          ph[o1] = static_cast<uint8_t>(hi >> 8);
+          pl[o0] = static_cast<uint8_t>(lo & 0xffu);
+          pl[o1] = static_cast<uint8_t>(lo >> 8);
+        }
+        if (kk >= nkeys) {  // keys past the piece: their V rows may hold anything (0 * NaN)
+          uint4* vr = reinterpret_cast<uint4*>(smb + (vt - base) + kk * 128);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) vr[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      fence_proxy_async_smem();  // P and the zeroed rows are read by the tensor cores
+      tc_fence_before();
+      named_barrier_sync(1, 128);
+      // ---- O^T += V^T P^T (hi, then lo); the commit frees the ring slot
+      if (issuer && !dead) {
+        tc_fence_after();
+        const uint32_t od = tmem + static_cast<uint32_t>(2 * TN);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          tc_mma_e4m3(od, tc_desc(vt + 4096 * ks, 16, 1024), tc_desc(kt + 32 * ks, 16, 1024), kIdPV,
+                      o_started || ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          tc_mma_e4m3(od, tc_desc(vt + 4096 * ks, 16, 1024), tc_desc(kt + TN * 128 + 32 * ks, 16, 1024),
+                      kIdPV, true);
+        tc_commit(bar_empty + 8 * slot);
+        tc_commit(bar_o);
+      }
+      if (!dead) ++n_o;  // every consumer thread counts the P V commits (uniform)
+      o_started = o_started || !dead;
+    }
+    it += nst;
+
+    // ------------------------------------------------------------ epilogue
+    // the last P V is complete (or, after an abort, O is not read)
+    const bool ok_o = o_started && !aborted() && wait_all(bar_o, (n_o - 1) & 1);
+    const bool have_o = o_started && !named_barrier_or(1, 128, o_started && !ok_o);
+    tc_fence_after();
+#pragma unroll
+    for (int j = 0; j < TN; ++j) {
+      float x = lp[j];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+      if (lane == 0) s_red[cw * 32 + j] = x;
+    }
+    named_barrier_sync(1, 128);
+    if (ct < TN) s_fac[ct] = s_red[ct] + s_red[32 + ct] + s_red[64 + ct] + s_red[96 + ct];
+    named_barrier_sync(1, 128);
+    uint32_t ov[TN];
+    if (have_o) {
+      tc_ld<TN>(tl + static_cast<uint32_t>(2 * TN), ov);
+    } else {
+#pragma unroll
+      for (int j = 0; j < TN; ++j) ov[j] = 0u;
+    }
+    const int d = kk;  // this thread's head dim
+#pragma unroll
+    for (int j = 0; j < TN; ++j) {
+      const int n = pass_base + j;
+      if (j >= NQ || n >= row_hi) continue;
+      const int tok = n / G;
+      const int hq = h * G + n % G;
+      const float M = s_mref[j];
+      float lsum = M != NEG_INF ? s_fac[j] : 0.f;
+      float v = M != NEG_INF ? __uint_as_float(ov[j]) : 0.f;
+      if (prow_base < 0) {
+        if (p.sinks) v *= add_sink(M, __ldg(p.sinks + hq) * 1.4426950408889634f, lsum);
+        const float inv = lsum > 0.f ? p.v_scale / (128.f * lsum) : 0.f;
+        const int trow = row0 + tok;
+        if (trow >= p.num_tokens) {
+          if (d == 0) atomicOr(p.plan.err, PA_DEVERR_PLAN_OVERFLOW);
+          continue;
+        }
+        const uint32_t pk = p.out_f16 ? pack2<false>(v * inv, 0.f) : pack2<true>(v * inv, 0.f);
+        static_cast<uint16_t*>(p.out)[(static_cast<size_t>(trow) * p.Hq + hq) * D + d] =
+            static_cast<uint16_t>(pk & 0xffffu);
+      } else {
+        const float inv = lsum > 0.f ? p.v_scale / (128.f * lsum) : 0.f;
+        const size_t prow = static_cast<size_t>(prow_base + tok) * p.Hq + hq;
+        p.plan.part_o[prow * D + d] = v * inv;
+        if (d == 0) p.plan.part_lse[prow] = lsum > 0.f ? M + __log2f(lsum) : NEG_INF;
+      }
+    }
+    tc_fence_before();
+    __syncthreads();  // pairs with the producer's end-of-pass barrier
+  }
   } else {
   // -------------------------------------------------------------- consumers
   const int cw = warp - Cfg::NPW;
@@ -955,6 +1280,22 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
   if (warp < Cfg::NPW && lane == 0) {
     for (int k = (issued > Cfg::NS ? issued - Cfg::NS : 0); k < issued; ++k)
       mbar_wait(bar_full + 8 * (k % Cfg::NS), (k / Cfg::NS) & 1, p.plan.err, p.wait_ns);
+  }
+  if constexpr (Cfg::kTc) {
+    // Every MMA the issuing thread started has completed (a last, bounded
+    // commit) before the tensor memory is released.
+    if (warp == Cfg::NPW) {
+      const uint32_t bar_o = base + Cfg::DATA_BYTES + Cfg::TC_ARR_OFF + 1024;
+      if (lane == 0) {
+        tc_commit(bar_o);
+        mbar_wait(bar_o, n_o & 1, p.plan.err, p.wait_ns);
+      }
+      __syncwarp();
+      tc_fence_after();
+      tc_dealloc(*reinterpret_cast<volatile uint32_t*>(smem_raw + (base - raw) + Cfg::DATA_BYTES +
+                                                       Cfg::TC_ARR_OFF + 1032),
+                 128);
+    }
   }
   // With the merge fused there is no merge kernel to reset the work counter
   // after this grid: the last CTA to finish does (thread 0 made every claim).

@@ -28,6 +28,14 @@ struct SplitCfg {
   // logits and softmax state), and each warp accumulates P V for its own
   // slice.  Stages are one 16-key tile.
   static constexpr bool kWide = D > 256;
+  // Tensor-memory path (tcgen05): fp8 caches, head dim 128, K in rows, two to
+  // four query-row groups (multi-token rows).  S^T = K Q^T and O^T += V^T P^T
+  // run on tcgen05.mma (kind::f8f6f4) with the accumulators in TMEM, K and V^T
+  // read straight from the TMA tiles, q and P as exact e4m3 hi + lo pairs; one
+  // warpgroup does the softmax, one thread per key.  TN: the MMA's N (the
+  // pass's query rows, padded to 16 or 32).
+  static constexpr bool kTc = kFp8 && D == 128 && KL == 0 && WQ >= 2;
+  static constexpr int TN = WQ <= 2 ? 16 : 32;
   static constexpr int DS = kWide ? (D % 256 == 0 ? 256 : 128) : D;  // head dims per consumer warp
   static constexpr int ND = D / DS;                   // dim slices
   static constexpr int CBS = DS * ESZ / SWB;          // column blocks per slice
@@ -37,7 +45,12 @@ struct SplitCfg {
   // Ring depth: 3 stages, or 2 where that lets two CTAs share an SM (wide
   // heads of 640 and 768 dims: 3 stages of 40-48 KB need more than half of
   // the SM's 228 KB of shared memory).
-  static constexpr int kFixedBytes = 1024 + 64 + SX_BYTES;
+  // kTc: barriers, then (1024-aligned) q as e4m3 hi and lo [32 rows][128 B]
+  // each, then per-row limits, reference maxima, factors, a reduction area and
+  // the tensor-memory address
+  static constexpr int TC_Q_OFF = 1024;                 // from DATA_BYTES
+  static constexpr int TC_ARR_OFF = TC_Q_OFF + 8192;
+  static constexpr int kFixedBytes = kTc ? 1024 + TC_ARR_OFF + 2048 : 1024 + 64 + SX_BYTES;
   static constexpr bool kTwoPerSm3 = 2 * (3 * 2 * KS * ROW + kFixedBytes + 1024) <= 228 * 1024;
   static constexpr bool kTwoPerSm2 = 2 * (2 * 2 * KS * ROW + kFixedBytes + 1024) <= 228 * 1024;
   static constexpr int NS = (kWide && !kTwoPerSm3 && kTwoPerSm2) ? 2 : 3;  // ring depth
@@ -52,7 +65,7 @@ struct SplitCfg {
   // Every key warp consumes every stage, in order, so a warp never waits on a
   // ring slot's use u+1 before it consumed use u -- which keeps the
   // parity-based mbarrier waits unambiguous.
-  static constexpr int NCW = WQ * WK * ND;            // consumer warps
+  static constexpr int NCW = kTc ? 4 : WQ * WK * ND;  // consumer warps (kTc: one warpgroup)
   // Producer warps.  Issuing a stage's copies (one per lane) holds a warp
   // for about 100-140 cycles per 2 KB box, which capped a lone CTA near
   // 25 GB/s with 16-key pages.  Two producers (K copies from one, V copies
@@ -76,8 +89,8 @@ struct SplitCfg {
   // finish this one: with no exchange, or with one that fits in a ring slot
   // -- the slot of the pass's last stage, which the consumers then hold
   // until the exchange is done (kHoldSlot).
-  static constexpr bool kHoldSlot = !kDirectEpi && EX_BYTES <= STAGE_BYTES;
-  static constexpr bool kPreIssue = kDirectEpi || kHoldSlot;
+  static constexpr bool kHoldSlot = !kTc && !kDirectEpi && EX_BYTES <= STAGE_BYTES;
+  static constexpr bool kPreIssue = kTc || kDirectEpi || kHoldSlot;
   // two CTAs per SM where the threads' registers and both rings fit (228 KB per SM)
   static constexpr int MIN_BLOCKS = (THREADS <= 224 && 2 * (SMEM_BYTES + 1024) <= 228 * 1024) ? 2 : 1;
   static_assert(!kWide || (WK == 1 && T == 1 && CBS * SWB == DS * ESZ && WQ <= 2),
@@ -89,7 +102,9 @@ struct SplitCfg {
   static_assert(!kGroupedK || MTS * (1 + CB) <= 32, "grouped K: one copy per producer lane");
   static_assert(!kGroupedK || (16 * ROW) % 1024 == 0,
                 "grouped K: every 16-key box starts on a 1024-byte swizzle repeat");
-  static_assert(EX_BYTES <= DATA_BYTES, "epilogue exchange reuses the stage ring");
+  static_assert(kTc || EX_BYTES <= DATA_BYTES, "epilogue exchange reuses the stage ring");
+  static_assert(!kTc || (KS == 128 && SWB == 128 && CB == 1 && NS * 16 + 16 <= 64),
+                "tcgen05 path: 128-key stages of 128-byte rows; barriers fit before the q area");
   static_assert(D % 32 == 0, "head_dim is a multiple of 32");
 };
 
