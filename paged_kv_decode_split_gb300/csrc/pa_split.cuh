@@ -584,8 +584,8 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
       const int key0 = kb + s * Cfg::KS;
       const int nkeys = min(Cfg::KS, ke - key0);
       // ---- S^T = K q^T (hi, then lo)
-      if (issuer) {
-        if (!aborted()) {
+      if (issuer) {  // one lane: no warp-collective calls in here
+        if (*reinterpret_cast<volatile int*>(&s_abort) == 0) {
           if (mbar_wait(bar_full + 8 * slot, (sit / Cfg::NS) & 1, p.plan.err, p.wait_ns)) {
             tc_fence_after();
             const uint32_t sd = tmem + static_cast<uint32_t>(sb * TN);
@@ -603,6 +603,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
           }
         }
       }
+      __syncwarp();  // the issuing lane rejoins its warp before the warp-wide calls below
       const bool live_w = !aborted() && wait_all(bar_s + 8 * sb, (sit >> 1) & 1);
       // ---- probabilities of this thread's key for every row
       float t[TN];
@@ -705,6 +706,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
         tc_commit(bar_empty + 8 * slot);
         tc_commit(bar_o);
       }
+      __syncwarp();
       if (!dead) ++n_o;  // every consumer thread counts the P V commits (uniform)
       o_started = o_started || !dead;
     }
