@@ -57,6 +57,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking: has the phase with the given parity completed?
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Gives up after
 // limit_ns nanoseconds, setting PA_DEVERR_TIMEOUT; the caller then carries on
 // so that every thread still reaches the kernel's later barriers.
@@ -65,6 +78,23 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > limit_ns) {
+      atomicOr(err, PA_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// mbar_wait that also gives up (without an error of its own) once *abort is
+// set -- for waits on work that an aborted pipeline will never produce.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, unsigned* err,
+                                                   unsigned long long limit_ns,
+                                                   const volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort) return false;
     if (global_ns() - t0 > limit_ns) {
       atomicOr(err, PA_DEVERR_TIMEOUT);
       return false;
@@ -224,11 +254,18 @@ __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
 // 32 bytes per MMA along K inside the 128-byte row; MN-major ones take SBO =
 // 1024 between 8-row groups along K and LBO between 128-byte column blocks
 // along M.
-__device__ __forceinline__ uint64_t tc_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+//
+// Layout type 0 (no swizzle) is built of 8-row x 16-byte core matrices (128
+// contiguous bytes).  For an MN-major operand in that layout LBO is the
+// stride between core matrices along K (8-row groups) and SBO the stride
+// between 16-byte column chunks along M / N (checked against a host product
+// on small exact e4m3 operands).
+__device__ __forceinline__ uint64_t tc_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
+                                            uint32_t layout = 2u) {
   return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) |
          (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1u) << 46) |
-         (static_cast<uint64_t>(2u) << 61);
+         (static_cast<uint64_t>(layout & 7u) << 61);
 }
 
 // Instruction descriptor of tcgen05.mma: fp32 accumulator (bits 4-5 = 1),
@@ -276,8 +313,16 @@ __device__ __forceinline__ void tc_dealloc(uint32_t taddr, uint32_t cols) {
 // (quadrant * 32 + i), N consecutive 32-bit columns.
 template <int N>
 __device__ __forceinline__ void tc_ld(uint32_t taddr, uint32_t (&r)[N]) {
-  static_assert(N == 16 || N == 32, "16 or 32 columns");
-  if constexpr (N == 16) {
+  static_assert(N == 16 || N == 32 || N == 64, "16, 32 or 64 columns");
+  if constexpr (N == 64) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr)
+        : "memory");
+    return;
+  } else if constexpr (N == 16) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
@@ -338,6 +383,47 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// Two fp32 -> one f16x2 word (round to nearest; first in the low half).
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// 2^x for both halves of an f16x2 word (the approximate f16 exponential).
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
+  uint32_t r;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t max_f16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t sub_f16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// f16x2 -> two e4m3fn codes (low byte = low half), round to nearest even,
+// saturating to +-448.
+__device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t x) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(x));
+  return r;
+}
+
+// Two e4m3fn codes (low byte = first) -> f16x2 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 l;\n\tcvt.u16.u32 l, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\t}" : "=r"(h2) : "r"(v));
+  return h2;
 }
 
 // Two e4m3fn codes (low byte = first) -> two fp32 (exact).

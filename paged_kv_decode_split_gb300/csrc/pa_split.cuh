@@ -122,9 +122,13 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
       mbar_init(bar_empty + 8 * s, Cfg::kTc ? 1 : Cfg::NCW);
     }
     if constexpr (Cfg::kTc) {
-      mbar_init(bar_full + 16 * Cfg::NS, 1);      // S^T buffer 0 computed
-      mbar_init(bar_full + 16 * Cfg::NS + 8, 1);  // S^T buffer 1 computed
-      mbar_init(base + Cfg::DATA_BYTES + Cfg::TC_ARR_OFF + 1024, 1);  // a P V completed
+      const uint32_t b = bar_full + 16 * Cfg::NS;
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(b + 8 * i, 1);       // S^T buffer i computed (a commit)
+        mbar_init(b + 16 + 8 * i, 4);  // P' of a stage of parity i written (each softmax warp)
+        mbar_init(b + 32 + 8 * i, 1);  // P V of a stage of parity i completed (a commit)
+      }
+      mbar_init(b + 48, 1);            // the last commit before the tensor memory is released
     }
     fence_barrier_init();
   }
@@ -142,9 +146,10 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     return;
   }
   if constexpr (Cfg::kTc) {
-    // 128 columns of tensor memory: S^T buffers [0, 2 TN), O^T [2 TN, 3 TN);
-    // two CTAs per SM take 256 of the SM's 512
-    if (warp == Cfg::NPW) tc_alloc(base + Cfg::DATA_BYTES + Cfg::TC_ARR_OFF + 1032, 128);
+    // 8 TN columns of tensor memory: S^T buffers [0, 2 TN) and [2 TN, 4 TN),
+    // O^T [4 TN, 6 TN), L^T [6 TN, 8 TN) (each hi then lo); two CTAs per SM
+    // take at most the SM's 512
+    if (warp == Cfg::NPW) tc_alloc(base + Cfg::DATA_BYTES + Cfg::TC_TMEM_SLOT, Cfg::TC_COLS);
     tc_fence_before();
   }
   // Items (piece, kv head) are numbered piece-major: item i is piece i / Hkv,
@@ -356,7 +361,6 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
   // Producer: stages of the coming pass issued ahead, and the block-table
   // window after them.
   int pre_n = 0, pre_win = 0, pre_cur = -1, pre_nxt = -1;
-  int n_o = 0;  // tensor-memory path: P V commits so far (every consumer thread counts)
 
   for (int round = 0;; ++round) {
     if (round > 0) {  // round 0's item was set up with the prologue
@@ -454,36 +458,70 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     }
   } else if constexpr (Cfg::kTc) {
   // ------------------------------- consumers on tensor memory (tcgen05), fp8
-  // One warpgroup.  Per 128-key stage: one thread issues S^T[128 keys x TN
-  // rows] = K Q^T (A = the K tile, K-major; B = q as e4m3 hi and lo) into one
-  // of two TMEM buffers; every thread takes the key of its TMEM lane, masks
-  // its rows, forms the probabilities against a per-row reference (moved,
-  // with the accumulators rescaled, only when a logit exceeds it by more than
-  // 0.8 in log2 units, so that 128 * p stays inside e4m3's range), writes
-  // them as e4m3 hi and lo into the stage's K tile (dead once S is computed);
-  // then the thread issues O^T[128 dims x TN] += V^T P^T (A = the V tile read
-  // as MN-major) and commits it to the ring slot's empty barrier.
+  // Warp NPW issues the MMAs (one thread); the next four warps -- one per
+  // tensor-memory lane quadrant -- do the softmax, one thread per key of a
+  // 128-key stage (per head dim in the epilogue).  q and P' are held as
+  // e4m3 hi + lo pairs stacked along the MMA's N (2 TN columns: hi rows,
+  // then lo rows), so every product is one MMA per 32-key (or 32-dim) step,
+  // and the two halves of a result are added where they are read.
+  // Stage g of the pass:
+  //   S^T[128 keys x 2TN] = K [q_hi; q_lo]^T into S buffer g & 1 (A = the K
+  //     tile, K-major; B = q * 2^qexp, K-major);
+  //   P' = 64 * 2^(logit - m_ref) for every key and row (f16 exponential),
+  //     as e4m3 hi and lo, written over the stage's K tile (dead once S is
+  //     computed): planes of 16 rows, key k's 16 bytes at k * 16 (MN-major,
+  //     no swizzle), hi planes then lo planes, so each softmax thread stores
+  //     whole 16-byte rows;
+  //   O^T[128 dims x 2TN] += V^T P'^T (A = the V tile read MN-major) and
+  //   L^T[128 x 2TN] += 1 P'^T (A = a block of ones read for all 128 rows):
+  //     L is every row's sum of the very weights O was accumulated with; the
+  //     commit frees the ring slot.
+  // The issuing thread runs S(g + 2) as soon as P'(g) is written (S buffer
+  // g & 1 is then free), so the softmax of stage g + 1 works on an S computed
+  // while stage g's softmax ran.  A row's reference m_ref moves (O and L
+  // rescaled) only when a logit exceeds it by more than 2.8 (log2 units):
+  // P' stays below 2^8.8, inside e4m3's range (448).
+  // Barriers (by stage parity where two operations of a kind can be
+  // outstanding): S computed [2], P' written [2], P V done [2], and one for
+  // the last commit before the tensor memory is released.
   constexpr int TN = Cfg::TN;
-  const int ct = threadIdx.x - 32 * Cfg::NPW;
-  const int cw = warp - Cfg::NPW;
-  const int quad = warp & 3;               // the TMEM lane quadrant this warp may access
-  const int kk = quad * 32 + lane;         // its key in a stage / its head dim in the epilogue
-  const bool issuer = ct == 0;
+  constexpr int TN2 = 2 * TN;
+  const int ct = threadIdx.x - 32 * Cfg::NPW;  // consumer thread
+  const int cw = warp - Cfg::NPW;              // 0: the MMA warp
+  const int st = ct - 32;                      // softmax thread
+  const int sw = cw - 1;                       // softmax warp
+  const int quad = warp & 3;                   // the TMEM lane quadrant this warp may access
+  const int kk = quad * 32 + lane;             // its key in a stage / its head dim in the epilogue
   const float NEG_INF = -__int_as_float(0x7f800000);
+  const float POS_INF = __int_as_float(0x7f800000);
   uint8_t* smb = smem_raw + (base - raw);
   const uint32_t q_hi = base + Cfg::DATA_BYTES + Cfg::TC_Q_OFF;
   const uint32_t q_lo = q_hi + TN * 128;
+  const uint32_t ones = base + Cfg::DATA_BYTES + Cfg::TC_ONES_OFF;
   int* s_lim = reinterpret_cast<int*>(smb + Cfg::DATA_BYTES + Cfg::TC_ARR_OFF);
   int* s_llo = s_lim + 32;
-  float* s_mref = reinterpret_cast<float*>(s_llo + 32);
-  float* s_fac = s_mref + 32;              // rescale factors, then row sums
-  float* s_red = s_fac + 32;               // [4 warps][32]
-  const uint32_t bar_s = bar_full + 16 * Cfg::NS;  // [2], one per S buffer
-  const uint32_t bar_o = base + Cfg::DATA_BYTES + Cfg::TC_ARR_OFF + 1024;
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smb + Cfg::DATA_BYTES + Cfg::TC_ARR_OFF + 1032);
+  float* s_mref = reinterpret_cast<float*>(s_llo + 32);  // the row's reference m_ref
+  float* s_nm = s_mref + 32;                             // 6 - m_ref (log2 of 64, less m_ref)
+  float* s_fac = s_nm + 32;                              // rescale factors, then row sums
+  float* s_red = reinterpret_cast<float*>(smb + Cfg::DATA_BYTES + Cfg::TC_RED_OFF);  // [4 warps][32]
+  const uint32_t bar_s = bar_full + 16 * Cfg::NS;
+  const uint32_t bar_p = bar_s + 16;
+  const uint32_t bar_o = bar_p + 16;
+  const volatile int* abort_flag = reinterpret_cast<volatile int*>(&s_abort);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smb + Cfg::DATA_BYTES + Cfg::TC_TMEM_SLOT);
   const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);  // this warp's lanes
-  constexpr uint32_t kIdQK = tc_idesc(0, 0, TN, 128);  // K (K-major) x q (K-major)
-  constexpr uint32_t kIdPV = tc_idesc(1, 0, TN, 128);  // V^T (MN-major) x P (K-major)
+  constexpr uint32_t kColO = 2 * TN2, kColL = 3 * TN2;  // S buffers at 0 and TN2
+  constexpr uint32_t kIdQK = tc_idesc(0, 0, TN2, 128);  // K (K-major) x q (K-major)
+  constexpr uint32_t kIdPV = tc_idesc(1, 1, TN2, 128);  // V^T (MN-major) x P' (MN-major)
+  constexpr uint32_t kIdL = tc_idesc(0, 1, TN2, 128);   // ones (K-major) x P' (MN-major)
+  constexpr uint32_t kPlo = TN * 128;                   // P' lo planes, from the K tile
+  // Softmax warps: a bounded wait that also ends once the pipeline aborted
+  // (warp-uniform result; a failure raises the abort).
+  auto wait_sm = [&](uint32_t bar, uint32_t parity) {
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_or_abort(bar, parity, p.plan.err, p.wait_ns, abort_flag));
+    if (!ok && lane == 0) *reinterpret_cast<volatile int*>(&s_abort) = 1;
+    return ok;
+  };
   tc_fence_after();  // the tensor-memory address written at allocation
 
   for (int pass = 0; pass < npass; ++pass) {
@@ -491,279 +529,363 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     const int ke = pass_key_end(pass);
     const int nst = ke > kb ? (ke - kb + Cfg::KS - 1) / Cfg::KS : 0;
 
-    // ---- rows of the pass: key limits; q * 2^e as e4m3 hi + lo (exact for
-    // bf16 / fp16 q up to the last bits of elements 2^10 below the largest)
-    if (ct < TN) {
-      const int n = pass_base + ct;
-      const int K = S - (L - 1 - n / G);
-      s_lim[ct] = (ct < NQ && n < row_hi) ? min(ke_task, K) : kb;  // rows past the pass: padding
-      s_llo[ct] = p.window > 0 ? max(0, K - p.window) : 0;
-      s_mref[ct] = NEG_INF;
-    }
-    float qv[32];
-    const int qrow = ct >> 2, qpart = ct & 3;  // 32 head dims [32 qpart, +32) of row qrow
-    float amax = 0.f;
-    {
-      const int n = pass_base + qrow;
-      const int tok = n / G;
-      const bool ok = qrow < NQ && n < row_hi && row0 + tok < p.num_tokens;
-      const size_t qoff = ok ? (static_cast<size_t>(row0 + tok) * p.Hq + h * G + n % G) * D + 32 * qpart : 0;
-      const uint4* qp = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + qoff);
+    float qs = 1.f;
+    if (cw > 0) {
+      // ---- rows of the pass: key limits; q * 2^qexp as e4m3 hi + lo (exact
+      // for bf16 / fp16 q up to the last bits of elements 2^10 below the largest)
+      if (st < TN) {
+        const int n = pass_base + st;
+        const int K = S - (L - 1 - n / G);
+        s_lim[st] = (st < NQ && n < row_hi) ? min(ke_task, K) : kb;  // rows past the pass: padding
+        s_llo[st] = p.window > 0 ? max(0, K - p.window) : 0;
+        s_mref[st] = NEG_INF;
+        s_nm[st] = POS_INF;
+      }
+      if (st < 64)  // the block of e4m3 ones (0x38) read as every row of L's A operand
+        *reinterpret_cast<uint4*>(smb + (ones - base) + st * 16) =
+            make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
+      float qv[32];
+      const int qrow = st >> 2, qpart = st & 3;  // 32 head dims [32 qpart, +32) of row qrow
+      float amax = 0.f;
+      {
+        const int n = pass_base + qrow;
+        const int tok = n / G;
+        const bool ok = qrow < NQ && n < row_hi && row0 + tok < p.num_tokens;
+        const size_t qoff = ok ? (static_cast<size_t>(row0 + tok) * p.Hq + h * G + n % G) * D + 32 * qpart : 0;
+        const uint4* qp = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + qoff);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 w = ok ? qp[i] : make_uint4(0u, 0u, 0u, 0u);
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        for (int i = 0; i < 4; ++i) {
+          const uint4 w = ok ? qp[i] : make_uint4(0u, 0u, 0u, 0u);
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float2 f;
-          if (p.out_f16) {
-            f = __half22float2(*reinterpret_cast<const __half2*>(&ws[j]));
-          } else {
-            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&ws[j]);
-            f = make_float2(__low2float(b), __high2float(b));
+          for (int j = 0; j < 4; ++j) {
+            float2 f;
+            if (p.out_f16) {
+              f = __half22float2(*reinterpret_cast<const __half2*>(&ws[j]));
+            } else {
+              const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&ws[j]);
+              f = make_float2(__low2float(b), __high2float(b));
+            }
+            qv[8 * i + 2 * j] = f.x;
+            qv[8 * i + 2 * j + 1] = f.y;
+            amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
           }
-          qv[8 * i + 2 * j] = f.x;
-          qv[8 * i + 2 * j + 1] = f.y;
-          amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
         }
       }
-    }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    if (lane == 0) s_red[cw * 32] = amax;
-    named_barrier_sync(1, 128);
-    amax = fmaxf(fmaxf(s_red[0], s_red[32]), fmaxf(s_red[64], s_red[96]));
-    int qexp = 0;  // q is scaled by 2^qexp: its largest element lands in [128, 256)
-    if (amax > 0.f) {
-      int x;
-      frexpf(amax, &x);
-      qexp = min(100, max(-100, 8 - x));
-    }
-    const float qs = exp2f(static_cast<float>(qexp));
-    if (qrow < TN) {
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      if (lane == 0) s_red[sw * 32] = amax;
+      named_barrier_sync(2, 128);
+      amax = fmaxf(fmaxf(s_red[0], s_red[32]), fmaxf(s_red[64], s_red[96]));
+      int qexp = 0;  // q is scaled by 2^qexp: its largest element lands in [128, 256)
+      if (amax > 0.f) {
+        int x;
+        frexpf(amax, &x);
+        qexp = min(100, max(-100, 8 - x));
+      }
+      qs = exp2f(static_cast<float>(qexp));
+      if (qrow < TN) {
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {  // two 16-byte chunks (16 dims each) of the row
-        uint32_t hw[4], lw[4];
+        for (int c = 0; c < 2; ++c) {  // two 16-byte chunks (16 dims each) of the row
+          uint32_t hw[4], lw[4];
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const int i = 16 * c + 4 * w;
-          const float a0 = qv[i] * qs, a1 = qv[i + 1] * qs, a2 = qv[i + 2] * qs, a3 = qv[i + 3] * qs;
-          const uint32_t h01 = f32x2_to_e4m3x2(a0, a1), h23 = f32x2_to_e4m3x2(a2, a3);
-          const float2 r01 = e4m3x2_to_f32x2(h01), r23 = e4m3x2_to_f32x2(h23);
-          const uint32_t l01 = f32x2_to_e4m3x2(a0 - r01.x, a1 - r01.y);
-          const uint32_t l23 = f32x2_to_e4m3x2(a2 - r23.x, a3 - r23.y);
-          hw[w] = h01 | (h23 << 16);
-          lw[w] = l01 | (l23 << 16);
+          for (int w = 0; w < 4; ++w) {
+            const int i = 16 * c + 4 * w;
+            const float a0 = qv[i] * qs, a1 = qv[i + 1] * qs, a2 = qv[i + 2] * qs, a3 = qv[i + 3] * qs;
+            const uint32_t h01 = f32x2_to_e4m3x2(a0, a1), h23 = f32x2_to_e4m3x2(a2, a3);
+            const float2 r01 = e4m3x2_to_f32x2(h01), r23 = e4m3x2_to_f32x2(h23);
+            const uint32_t l01 = f32x2_to_e4m3x2(a0 - r01.x, a1 - r01.y);
+            const uint32_t l23 = f32x2_to_e4m3x2(a2 - r23.x, a3 - r23.y);
+            hw[w] = h01 | (h23 << 16);
+            lw[w] = l01 | (l23 << 16);
+          }
+          const uint32_t off = static_cast<uint32_t>(qrow * 128 + (((2 * qpart + c) ^ (qrow & 7)) << 4));
+          *reinterpret_cast<uint4*>(smb + (q_hi - base) + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(smb + (q_lo - base) + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
-        const uint32_t off = static_cast<uint32_t>(qrow * 128 + (((2 * qpart + c) ^ (qrow & 7)) << 4));
-        *reinterpret_cast<uint4*>(smb + (q_hi - base) + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        *reinterpret_cast<uint4*>(smb + (q_lo - base) + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
       }
+      fence_proxy_async_smem();  // q and the ones are read by the tensor cores
     }
-    fence_proxy_async_smem();  // q is read by the tensor cores
-    named_barrier_sync(1, 128);
-    const float c2 = p.scale_log2 / qs;  // logit (log2 units) = S^T * c2
-    int vis_lo = 0, vis_hi = 0x7fffffff;  // keys every real row of the pass sees
-    for (int j = 0; j < TN; ++j) {
-      if (j < NQ && pass_base + j < row_hi) {
-        vis_lo = max(vis_lo, s_llo[j]);
-        vis_hi = min(vis_hi, s_lim[j]);
-      }
-    }
+    named_barrier_sync(1, 160);  // q, the ones and the row limits are written
 
-    float lp[TN];  // this thread's key lane's share of each row's sum of p
-#pragma unroll
-    for (int j = 0; j < TN; ++j) lp[j] = 0.f;
-    bool o_started = false;
-    for (int s = 0; s < nst; ++s) {
-      const int sit = it + s;
-      const int slot = sit % Cfg::NS;
-      const int sb = sit & 1;
-      const uint32_t kt = base + slot * Cfg::STAGE_BYTES;
-      const uint32_t vt = kt + Cfg::TILE_BYTES;
-      const int key0 = kb + s * Cfg::KS;
-      const int nkeys = min(Cfg::KS, ke - key0);
-      // ---- S^T = K q^T (hi, then lo)
-      if (issuer) {  // one lane: no warp-collective calls in here
-        if (*reinterpret_cast<volatile int*>(&s_abort) == 0) {
-          if (mbar_wait(bar_full + 8 * slot, (sit / Cfg::NS) & 1, p.plan.err, p.wait_ns)) {
-            tc_fence_after();
-            const uint32_t sd = tmem + static_cast<uint32_t>(sb * TN);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              tc_mma_e4m3(sd, tc_desc(kt + 32 * ks, 16, 1024), tc_desc(q_hi + 32 * ks, 16, 1024), kIdQK,
-                          ks > 0);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              tc_mma_e4m3(sd, tc_desc(kt + 32 * ks, 16, 1024), tc_desc(q_lo + 32 * ks, 16, 1024), kIdQK,
-                          true);
-            tc_commit(bar_s + 8 * sb);
-          } else {
-            *reinterpret_cast<volatile int*>(&s_abort) = 1;
+    if (cw == 0) {
+      // ------------------------------------------------------- MMA issuer
+      if (lane == 0 && nst > 0) {  // one lane: no warp-collective calls in here
+        const uint64_t dq = tc_desc(q_hi, 16, 1024);  // +2 per 32-byte step along K
+        const uint64_t d1 = tc_desc(ones, 16, 0);     // SBO 0: one 8-row block for all 128 rows
+        // S^T = K [q_hi; q_lo]^T once stage s has landed (wait) or if it has
+        // (test): 1 issued, 0 not landed yet, -1 the wait gave up
+        auto issue_s = [&](int s, bool wait) {
+          const int g = it + s;
+          const int slot = g % Cfg::NS;
+          const uint32_t par = (g / Cfg::NS) & 1;
+          if (wait) {
+            if (!mbar_wait_or_abort(bar_full + 8 * slot, par, p.plan.err, p.wait_ns, abort_flag)) return -1;
+          } else if (!mbar_test(bar_full + 8 * slot, par)) {
+            return 0;
           }
+          tc_fence_after();
+          const uint64_t dk = tc_desc(base + slot * Cfg::STAGE_BYTES, 16, 1024);
+          const uint32_t sd = tmem + static_cast<uint32_t>((g & 1) * TN2);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) tc_mma_e4m3(sd, dk + 2 * ks, dq + 2 * ks, kIdQK, ks > 0);
+          tc_commit(bar_s + 8 * (g & 1));
+          return 1;
+        };
+        bool ok = issue_s(0, true) == 1 && (nst < 2 || issue_s(1, true) == 1);
+        for (int s = 0; ok && s < nst; ++s) {
+          const int g = it + s;
+          const int slot = g % Cfg::NS;
+          ok = mbar_wait_or_abort(bar_p + 8 * (g & 1), (g >> 1) & 1, p.plan.err, p.wait_ns, abort_flag);
+          if (!ok) break;
+          // S(g + 2) first when its tile is already there: the softmax needs it next
+          const int early = s + 2 < nst ? issue_s(s + 2, false) : 1;
+          // ---- O^T += V^T P'^T and L^T += 1 P'^T; the commit frees the ring slot
+          tc_fence_after();
+          const uint32_t kt = base + slot * Cfg::STAGE_BYTES;
+          const uint64_t dv = tc_desc(kt + Cfg::TILE_BYTES, 16, 1024);  // +256 per 32 keys
+          const uint64_t dp = tc_desc(kt, 128, 2048, 0u);               // +32 per 32 keys
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            tc_mma_e4m3(tmem + kColO, dv + 256 * ks, dp + 32 * ks, kIdPV, s > 0 || ks > 0);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            tc_mma_e4m3(tmem + kColL, d1 + 2 * ks, dp + 32 * ks, kIdL, s > 0 || ks > 0);
+          tc_commit(bar_empty + 8 * slot);
+          tc_commit(bar_o + 8 * (g & 1));
+          if (early == 0) ok = issue_s(s + 2, true) == 1;
         }
-      }
-      __syncwarp();  // the issuing lane rejoins its warp before the warp-wide calls below
-      const bool live_w = !aborted() && wait_all(bar_s + 8 * sb, (sit >> 1) & 1);
-      // ---- probabilities of this thread's key for every row
-      float t[TN];
-      bool over = false;
-      if (live_w) {
-        tc_fence_after();
-        uint32_t sv[TN];
-        tc_ld<TN>(tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(sb * TN), sv);
-        const int kabs = key0 + kk;
-        const bool full = kk < nkeys && kabs >= vis_lo && kabs < vis_hi;
-#pragma unroll
-        for (int j = 0; j < TN; ++j) {
-          const bool vis = full || (kk < nkeys && kabs < s_lim[j] && kabs >= s_llo[j]);
-          t[j] = vis ? __uint_as_float(sv[j]) * c2 : NEG_INF;
-          over = over || t[j] > s_mref[j] + 0.8f;
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < TN; ++j) t[j] = NEG_INF;
-      }
-      // a stage some warp could not read is dropped by all (the pipeline aborts)
-      const bool dead = named_barrier_or(1, 128, !live_w);
-      if (dead && ct == 0) *reinterpret_cast<volatile int*>(&s_abort) = 1;
-      if (named_barrier_or(1, 128, over && !dead)) {
-        // a new reference per row: the running maximum; p, l and O rescaled
-#pragma unroll
-        for (int j = 0; j < TN; ++j) {
-          float m = t[j];
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-          if (lane == 0) s_red[cw * 32 + j] = m;
-        }
-        named_barrier_sync(1, 128);
-        if (ct < TN) {
-          const float ms = fmaxf(fmaxf(s_red[ct], s_red[32 + ct]), fmaxf(s_red[64 + ct], s_red[96 + ct]));
-          const float mo = s_mref[ct];
-          const float mn = fmaxf(mo, ms);
-          s_fac[ct] = (mo == NEG_INF) ? 0.f : fast_exp2(mo - mn);
-          s_mref[ct] = mn;
-        }
-        named_barrier_sync(1, 128);
-#pragma unroll
-        for (int j = 0; j < TN; ++j) lp[j] *= s_fac[j];
-        if (o_started) {
-          if (wait_all(bar_o, (n_o - 1) & 1)) {  // the previous stage's P V is complete
-            tc_fence_after();
-            uint32_t ov[TN];
-            tc_ld<TN>(tl + static_cast<uint32_t>(2 * TN), ov);
-#pragma unroll
-            for (int j = 0; j < TN; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * s_fac[j]);
-            tc_st<TN>(tl + static_cast<uint32_t>(2 * TN), ov);
-          }
-        }
-      }
-      // p' = 128 p (at most 2^7.8) as e4m3 hi + lo, rows [j][key] into the K tile
-      if (!dead) {
-        uint8_t* ph = smb + (kt - base);
-        uint8_t* pl = ph + TN * 128;
-        const uint32_t cbyte = static_cast<uint32_t>(kk & 15);
-        const int chunk = kk >> 4;
-#pragma unroll
-        for (int j = 0; j < TN; j += 2) {
-          const float m0 = s_mref[j], m1 = s_mref[j + 1];
-          const float p0 = (t[j] == NEG_INF) ? 0.f : fast_exp2(t[j] - m0);
-          const float p1 = (t[j + 1] == NEG_INF) ? 0.f : fast_exp2(t[j + 1] - m1);
-          lp[j] += p0;
-          lp[j + 1] += p1;
-          const float a0 = 128.f * p0, a1 = 128.f * p1;
-          const uint32_t hi = f32x2_to_e4m3x2(a0, a1);
-          const float2 hr = e4m3x2_to_f32x2(hi);
-          const uint32_t lo = f32x2_to_e4m3x2(a0 - hr.x, a1 - hr.y);
-          const uint32_t o0 = static_cast<uint32_t>(j * 128 + ((chunk ^ (j & 7)) << 4)) + cbyte;
-          const uint32_t o1 = static_cast<uint32_t>((j + 1) * 128 + ((chunk ^ ((j + 1) & 7)) << 4)) + cbyte;
-          ph[o0] = static_cast<uint8_t>(hi & 0xffu);
-          ph[o1] = static_cast<uint8_t>(hi >> 8);
-          pl[o0] = static_cast<uint8_t>(lo & 0xffu);
-          pl[o1] = static_cast<uint8_t>(lo >> 8);
-        }
-        if (kk >= nkeys) {  // keys past the piece: their V rows may hold anything (0 * NaN)
-          uint4* vr = reinterpret_cast<uint4*>(smb + (vt - base) + kk * 128);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) vr[i] = make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
-      fence_proxy_async_smem();  // P and the zeroed rows are read by the tensor cores
-      tc_fence_before();
-      named_barrier_sync(1, 128);
-      // ---- O^T += V^T P^T (hi, then lo); the commit frees the ring slot
-      if (issuer && !dead) {
-        tc_fence_after();
-        const uint32_t od = tmem + static_cast<uint32_t>(2 * TN);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          tc_mma_e4m3(od, tc_desc(vt + 4096 * ks, 16, 1024), tc_desc(kt + 32 * ks, 16, 1024), kIdPV,
-                      o_started || ks > 0);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          tc_mma_e4m3(od, tc_desc(vt + 4096 * ks, 16, 1024), tc_desc(kt + TN * 128 + 32 * ks, 16, 1024),
-                      kIdPV, true);
-        tc_commit(bar_empty + 8 * slot);
-        tc_commit(bar_o);
+        if (!ok) *reinterpret_cast<volatile int*>(&s_abort) = 1;
       }
       __syncwarp();
-      if (!dead) ++n_o;  // every consumer thread counts the P V commits (uniform)
-      o_started = o_started || !dead;
-    }
-    it += nst;
-
-    // ------------------------------------------------------------ epilogue
-    // the last P V is complete (or, after an abort, O is not read)
-    const bool ok_o = o_started && !aborted() && wait_all(bar_o, (n_o - 1) & 1);
-    const bool have_o = o_started && !named_barrier_or(1, 128, o_started && !ok_o);
-    tc_fence_after();
-#pragma unroll
-    for (int j = 0; j < TN; ++j) {
-      float x = lp[j];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-      if (lane == 0) s_red[cw * 32 + j] = x;
-    }
-    named_barrier_sync(1, 128);
-    if (ct < TN) s_fac[ct] = s_red[ct] + s_red[32 + ct] + s_red[64 + ct] + s_red[96 + ct];
-    named_barrier_sync(1, 128);
-    uint32_t ov[TN];
-    if (have_o) {
-      tc_ld<TN>(tl + static_cast<uint32_t>(2 * TN), ov);
     } else {
-#pragma unroll
-      for (int j = 0; j < TN; ++j) ov[j] = 0u;
-    }
-    const int d = kk;  // this thread's head dim
-#pragma unroll
-    for (int j = 0; j < TN; ++j) {
-      const int n = pass_base + j;
-      if (j >= NQ || n >= row_hi) continue;
-      const int tok = n / G;
-      const int hq = h * G + n % G;
-      const float M = s_mref[j];
-      float lsum = M != NEG_INF ? s_fac[j] : 0.f;
-      float v = M != NEG_INF ? __uint_as_float(ov[j]) : 0.f;
-      if (prow_base < 0) {
-        if (p.sinks) v *= add_sink(M, __ldg(p.sinks + hq) * 1.4426950408889634f, lsum);
-        const float inv = lsum > 0.f ? p.v_scale / (128.f * lsum) : 0.f;
-        const int trow = row0 + tok;
-        if (trow >= p.num_tokens) {
-          if (d == 0) atomicOr(p.plan.err, PA_DEVERR_PLAN_OVERFLOW);
-          continue;
+      // ----------------------------------------------------------- softmax
+      const float c2 = p.scale_log2 / qs;  // logit (log2 units) = S^T * c2
+      int vis_lo = 0, vis_hi = 0x7fffffff;  // keys every real row of the pass sees
+      for (int j = 0; j < TN; ++j) {
+        if (j < NQ && pass_base + j < row_hi) {
+          vis_lo = max(vis_lo, s_llo[j]);
+          vis_hi = min(vis_hi, s_lim[j]);
         }
-        const uint32_t pk = p.out_f16 ? pack2<false>(v * inv, 0.f) : pack2<true>(v * inv, 0.f);
-        static_cast<uint16_t*>(p.out)[(static_cast<size_t>(trow) * p.Hq + hq) * D + d] =
-            static_cast<uint16_t>(pk & 0xffffu);
-      } else {
-        const float inv = lsum > 0.f ? p.v_scale / (128.f * lsum) : 0.f;
-        const size_t prow = static_cast<size_t>(prow_base + tok) * p.Hq + hq;
-        p.plan.part_o[prow * D + d] = v * inv;
-        if (d == 0) p.plan.part_lse[prow] = lsum > 0.f ? M + __log2f(lsum) : NEG_INF;
+      }
+      // P' = 64 * 2^(logit - m_ref) = 2^(S * c2 + 6 - m_ref) for every row,
+      // as f16 pairs (rows 2i, 2i + 1); masked keys give 0.
+      auto make_p = [&](const float (&sv)[TN], bool sfull, int kabs, int nkeys, uint32_t (&ph)[TN / 2]) {
+        const float4* nm4 = reinterpret_cast<const float4*>(s_nm);
+#pragma unroll
+        for (int q4 = 0; q4 < TN / 4; ++q4) {
+          const float4 nm = nm4[q4];
+          float a[4] = {fmaf(sv[4 * q4], c2, nm.x), fmaf(sv[4 * q4 + 1], c2, nm.y),
+                        fmaf(sv[4 * q4 + 2], c2, nm.z), fmaf(sv[4 * q4 + 3], c2, nm.w)};
+          if (!sfull) {
+            const int4 lim = reinterpret_cast<const int4*>(s_lim)[q4];
+            const int4 llo = reinterpret_cast<const int4*>(s_llo)[q4];
+            const bool in = kk < nkeys;
+            if (!(in && kabs < lim.x && kabs >= llo.x)) a[0] = NEG_INF;
+            if (!(in && kabs < lim.y && kabs >= llo.y)) a[1] = NEG_INF;
+            if (!(in && kabs < lim.z && kabs >= llo.z)) a[2] = NEG_INF;
+            if (!(in && kabs < lim.w && kabs >= llo.w)) a[3] = NEG_INF;
+          }
+          ph[2 * q4] = ex2_f16x2(f32x2_to_f16x2(a[0], a[1]));
+          ph[2 * q4 + 1] = ex2_f16x2(f32x2_to_f16x2(a[2], a[3]));
+        }
+      };
+      for (int s = 0; s < nst; ++s) {
+        const int g = it + s;
+        const int slot = g % Cfg::NS;
+        const int sb = g & 1;
+        const uint32_t kt = base + slot * Cfg::STAGE_BYTES;
+        const uint32_t vt = kt + Cfg::TILE_BYTES;
+        const int key0 = kb + s * Cfg::KS;
+        const int nkeys = min(Cfg::KS, ke - key0);
+        const int kabs = key0 + kk;
+        // every key of the stage visible to every row: no masks
+        const bool sfull = nkeys == Cfg::KS && key0 >= vis_lo && key0 + Cfg::KS <= vis_hi;
+        const bool live = !aborted() && wait_sm(bar_s + 8 * sb, (g >> 1) & 1);
+        float sv[TN];
+        bool over = false;  // some P' would exceed 2^8.8 (e4m3's largest is 448)
+        if (live) {
+          tc_fence_after();
+          uint32_t a[TN2];
+          tc_ld<TN2>(tl + static_cast<uint32_t>(sb * TN2), a);
+#pragma unroll
+          for (int j = 0; j < TN; ++j) sv[j] = __uint_as_float(a[j]) + __uint_as_float(a[TN + j]);
+          const float4* nm4 = reinterpret_cast<const float4*>(s_nm);
+          float amax = NEG_INF;
+#pragma unroll
+          for (int q4 = 0; q4 < TN / 4; ++q4) {
+            const float4 nm = nm4[q4];
+            float x[4] = {fmaf(sv[4 * q4], c2, nm.x), fmaf(sv[4 * q4 + 1], c2, nm.y),
+                          fmaf(sv[4 * q4 + 2], c2, nm.z), fmaf(sv[4 * q4 + 3], c2, nm.w)};
+            if (!sfull) {
+              const int4 lim = reinterpret_cast<const int4*>(s_lim)[q4];
+              const int4 llo = reinterpret_cast<const int4*>(s_llo)[q4];
+              const bool in = kk < nkeys;
+              if (!(in && kabs < lim.x && kabs >= llo.x)) x[0] = NEG_INF;
+              if (!(in && kabs < lim.y && kabs >= llo.y)) x[1] = NEG_INF;
+              if (!(in && kabs < lim.z && kabs >= llo.z)) x[2] = NEG_INF;
+              if (!(in && kabs < lim.w && kabs >= llo.w)) x[3] = NEG_INF;
+            }
+            amax = fmaxf(amax, fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])));
+          }
+          over = amax > 8.8f;
+        } else {
+#pragma unroll
+          for (int j = 0; j < TN; ++j) sv[j] = 0.f;
+        }
+        if (named_barrier_or(2, 128, over)) {
+          // A new reference per row: the running maximum; O and L rescaled.
+          // Kept compact (it runs on few stages): the row maxima go through
+          // shared memory -- the stage's K tile, dead since S was computed
+          // and not yet overwritten by P' -- as [TN rows][128 keys] floats,
+          // 16-byte groups XOR-swizzled by the row so that the readers below
+          // (TN / 4 or TN / 8 rows per warp, 16 keys each per load) hit
+          // distinct banks.
+          float* tt = reinterpret_cast<float*>(smb + (kt - base));
+#pragma unroll
+          for (int j = 0; j < TN; ++j) {
+            bool vis = live && kk < nkeys;
+            if (!sfull) vis = vis && kabs < s_lim[j] && kabs >= s_llo[j];
+            tt[j * 128 + (kk ^ ((j & 7) << 2))] = vis ? sv[j] * c2 : NEG_INF;
+          }
+          named_barrier_sync(2, 128);
+          {
+            constexpr int PER = 128 / TN;          // threads per row
+            constexpr int NF4 = (128 / PER) / 4;   // float4 groups per thread
+            const int j = st / PER, part = st % PER;
+            float m = NEG_INF;
+#pragma unroll 1
+            for (int i = 0; i < NF4; ++i) {
+              const int f4 = (part * NF4 + i) ^ (j & 7);
+              const float4 v = reinterpret_cast<const float4*>(tt + j * 128)[f4];
+              m = fmaxf(m, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+            }
+#pragma unroll
+            for (int o = PER / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (part == 0) {
+              const float mo = s_mref[j];
+              const float mn = fmaxf(mo, m);
+              s_fac[j] = (mo == NEG_INF) ? 0.f : fast_exp2(mo - mn);
+              s_mref[j] = mn;
+              s_nm[j] = (mn == NEG_INF) ? POS_INF : 6.f - mn;
+            }
+          }
+          named_barrier_sync(2, 128);
+          // the previous stage's P V (the only one that can be outstanding)
+          if (s > 0 && wait_sm(bar_o + 8 * ((g - 1) & 1), ((g - 1) >> 1) & 1)) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int c0 = 0; c0 < 2 * TN2; c0 += 32) {  // O hi, O lo, L hi, L lo
+              uint32_t ov[32];
+              tc_ld<32>(tl + kColO + static_cast<uint32_t>(c0), ov);
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                ov[i] = __float_as_uint(__uint_as_float(ov[i]) * s_fac[(c0 + i) % TN]);
+              tc_st<32>(tl + kColO + static_cast<uint32_t>(c0), ov);
+            }
+          }
+        }
+        uint32_t ph[TN / 2];  // every P' is now at most 2^8.8
+        make_p(sv, sfull, kabs, nkeys, ph);
+        // P' as e4m3 hi + lo: 16 rows per 16-byte store
+        if (!aborted()) {
+#pragma unroll
+          for (int c = 0; c < TN / 16; ++c) {
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const uint32_t x0 = ph[8 * c + 2 * w], x1 = ph[8 * c + 2 * w + 1];
+              const uint32_t h0 = f16x2_to_e4m3x2(x0), h1 = f16x2_to_e4m3x2(x1);
+              const uint32_t l0 = f16x2_to_e4m3x2(sub_f16x2(x0, e4m3x2_to_f16x2(h0)));
+              const uint32_t l1 = f16x2_to_e4m3x2(sub_f16x2(x1, e4m3x2_to_f16x2(h1)));
+              hw[w] = h0 | (h1 << 16);
+              lw[w] = l0 | (l1 << 16);
+            }
+            const uint32_t off = (kt - base) + static_cast<uint32_t>(c * 2048 + kk * 16);
+            *reinterpret_cast<uint4*>(smb + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(smb + off + kPlo) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          }
+          if (kk >= nkeys) {  // keys past the piece: their V rows may hold anything (0 * NaN)
+            uint4* vr = reinterpret_cast<uint4*>(smb + (vt - base) + kk * 128);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) vr[i] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        fence_proxy_async_smem();  // P' and the zeroed rows are read by the tensor cores
+        tc_fence_before();         // the S reads (and O / L rescale) precede the MMAs that follow
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_p + 8 * sb);
+      }
+
+      // ---------------------------------------------------------- epilogue
+      // the last P V (and L) is complete, and with it every earlier one
+      const int gl = it + nst - 1;
+      const bool have_o = nst > 0 && !aborted() && wait_sm(bar_o + 8 * (gl & 1), (gl >> 1) & 1);
+      tc_fence_after();
+      if (sw == 0) {  // row sums: every lane of L holds them all
+        uint32_t a[TN2];
+        if (have_o) {
+          tc_ld<TN2>(tl + kColL, a);
+        } else {
+#pragma unroll
+          for (int j = 0; j < TN2; ++j) a[j] = 0u;
+        }
+        if (lane == 0) {
+#pragma unroll
+          for (int j = 0; j < TN; ++j) s_fac[j] = __uint_as_float(a[j]) + __uint_as_float(a[TN + j]);
+        }
+      }
+      named_barrier_sync(2, 128);
+      float ov[TN];
+      {
+        uint32_t a[TN2];
+        if (have_o) {
+          tc_ld<TN2>(tl + kColO, a);
+        } else {
+#pragma unroll
+          for (int j = 0; j < TN2; ++j) a[j] = 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < TN; ++j) ov[j] = __uint_as_float(a[j]) + __uint_as_float(a[TN + j]);
+      }
+      const int d = kk;  // this thread's head dim
+#pragma unroll
+      for (int j = 0; j < TN; ++j) {
+        const int n = pass_base + j;
+        if (j >= NQ || n >= row_hi) continue;
+        const int tok = n / G;
+        const int hq = h * G + n % G;
+        const float M = s_mref[j];
+        // L and O carry the factor 64 of P'
+        float lsum = M != NEG_INF ? s_fac[j] * (1.f / 64.f) : 0.f;
+        float v = M != NEG_INF ? ov[j] : 0.f;
+        if (prow_base < 0) {
+          if (p.sinks) v *= add_sink(M, __ldg(p.sinks + hq) * 1.4426950408889634f, lsum);
+          const float inv = lsum > 0.f ? p.v_scale / (64.f * lsum) : 0.f;
+          const int trow = row0 + tok;
+          if (trow >= p.num_tokens) {
+            if (d == 0) atomicOr(p.plan.err, PA_DEVERR_PLAN_OVERFLOW);
+            continue;
+          }
+          const uint32_t pk = p.out_f16 ? pack2<false>(v * inv, 0.f) : pack2<true>(v * inv, 0.f);
+          static_cast<uint16_t*>(p.out)[(static_cast<size_t>(trow) * p.Hq + hq) * D + d] =
+              static_cast<uint16_t>(pk & 0xffffu);
+        } else {
+          const float inv = lsum > 0.f ? p.v_scale / (64.f * lsum) : 0.f;
+          const size_t prow = static_cast<size_t>(prow_base + tok) * p.Hq + hq;
+          p.plan.part_o[prow * D + d] = v * inv;
+          if (d == 0) p.plan.part_lse[prow] = lsum > 0.f ? M + __log2f(lsum) : NEG_INF;
+        }
       }
     }
+    it += nst;
+    // Fused merge: the consumers of the CTA that finished a request's last
+    // piece (of a group) combine the pieces' partials.
+    if (p.fused && prow_base >= 0 && pass == npass - 1)
+      fused_merge<D>(p, r, h, prow_base, row0, ct, cw, Cfg::NCW, lane);
     tc_fence_before();
     __syncthreads();  // pairs with the producer's end-of-pass barrier
+    tc_fence_after();
   }
   } else {
   // -------------------------------------------------------------- consumers
@@ -1284,19 +1406,20 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
       mbar_wait(bar_full + 8 * (k % Cfg::NS), (k / Cfg::NS) & 1, p.plan.err, p.wait_ns);
   }
   if constexpr (Cfg::kTc) {
-    // Every MMA the issuing thread started has completed (a last, bounded
-    // commit) before the tensor memory is released.
+    // Every MMA the issuing thread started has completed (a last commit, on a
+    // barrier of its own, and a bounded wait) before the tensor memory is
+    // released.
     if (warp == Cfg::NPW) {
-      const uint32_t bar_o = base + Cfg::DATA_BYTES + Cfg::TC_ARR_OFF + 1024;
+      const uint32_t bar_drain = bar_full + 16 * Cfg::NS + 48;
       if (lane == 0) {
-        tc_commit(bar_o);
-        mbar_wait(bar_o, n_o & 1, p.plan.err, p.wait_ns);
+        tc_commit(bar_drain);
+        mbar_wait(bar_drain, 0, p.plan.err, p.wait_ns);
       }
       __syncwarp();
       tc_fence_after();
       tc_dealloc(*reinterpret_cast<volatile uint32_t*>(smem_raw + (base - raw) + Cfg::DATA_BYTES +
-                                                       Cfg::TC_ARR_OFF + 1032),
-                 128);
+                                                       Cfg::TC_TMEM_SLOT),
+                 Cfg::TC_COLS);
     }
   }
   // With the merge fused there is no merge kernel to reset the work counter

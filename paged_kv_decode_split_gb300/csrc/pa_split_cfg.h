@@ -31,9 +31,9 @@ struct SplitCfg {
   // Tensor-memory path (tcgen05): fp8 caches, head dim 128, K in rows, two to
   // four query-row groups (multi-token rows).  S^T = K Q^T and O^T += V^T P^T
   // run on tcgen05.mma (kind::f8f6f4) with the accumulators in TMEM, K and V^T
-  // read straight from the TMA tiles, q and P as exact e4m3 hi + lo pairs; one
-  // warpgroup does the softmax, one thread per key.  TN: the MMA's N (the
-  // pass's query rows, padded to 16 or 32).
+  // read straight from the TMA tiles, q and P as e4m3 hi + lo pairs; one warp
+  // issues the MMAs and one warpgroup does the softmax, one thread per key.
+  // TN: the MMA's N (the pass's query rows, padded to 16 or 32).
   static constexpr bool kTc = kFp8 && D == 128 && KL == 0 && WQ >= 2;
   static constexpr int TN = WQ <= 2 ? 16 : 32;
   static constexpr int DS = kWide ? (D % 256 == 0 ? 256 : 128) : D;  // head dims per consumer warp
@@ -45,11 +45,16 @@ struct SplitCfg {
   // Ring depth: 3 stages, or 2 where that lets two CTAs share an SM (wide
   // heads of 640 and 768 dims: 3 stages of 40-48 KB need more than half of
   // the SM's 228 KB of shared memory).
-  // kTc: barriers, then (1024-aligned) q as e4m3 hi and lo [32 rows][128 B]
-  // each, then per-row limits, reference maxima, factors, a reduction area and
-  // the tensor-memory address
-  static constexpr int TC_Q_OFF = 1024;                 // from DATA_BYTES
-  static constexpr int TC_ARR_OFF = TC_Q_OFF + 8192;
+  // kTc: the ring's barriers and seven more (S computed x2, P written x2,
+  // P V done x2, drain), the tensor-memory address and a reduction area, then
+  // (1024-aligned) q as e4m3 hi and lo [32 rows][128 B] each, per-row limits,
+  // references and factors, and a block of ones
+  static constexpr int TC_TMEM_SLOT = 128;              // from DATA_BYTES (after the barriers)
+  static constexpr int TC_RED_OFF = 512;                // reduction area [4][32] floats
+  static constexpr int TC_Q_OFF = 1024;
+  static constexpr int TC_ARR_OFF = TC_Q_OFF + 8192;    // row limits, references, factors
+  static constexpr int TC_ONES_OFF = TC_ARR_OFF + 1024;  // 1 KB of e4m3 ones, 1024-aligned
+  static constexpr int TC_COLS = 8 * TN;                // tensor-memory columns
   static constexpr int kFixedBytes = kTc ? 1024 + TC_ARR_OFF + 2048 : 1024 + 64 + SX_BYTES;
   static constexpr bool kTwoPerSm3 = 2 * (3 * 2 * KS * ROW + kFixedBytes + 1024) <= 228 * 1024;
   static constexpr bool kTwoPerSm2 = 2 * (2 * 2 * KS * ROW + kFixedBytes + 1024) <= 228 * 1024;
@@ -65,7 +70,8 @@ struct SplitCfg {
   // Every key warp consumes every stage, in order, so a warp never waits on a
   // ring slot's use u+1 before it consumed use u -- which keeps the
   // parity-based mbarrier waits unambiguous.
-  static constexpr int NCW = kTc ? 4 : WQ * WK * ND;  // consumer warps (kTc: one warpgroup)
+  // consumer warps (kTc: one MMA-issuing warp, then one softmax warpgroup)
+  static constexpr int NCW = kTc ? 5 : WQ * WK * ND;
   // Producer warps.  Issuing a stage's copies (one per lane) holds a warp
   // for about 100-140 cycles per 2 KB box, which capped a lone CTA near
   // 25 GB/s with 16-key pages.  Two producers (K copies from one, V copies
@@ -93,6 +99,7 @@ struct SplitCfg {
   static constexpr bool kPreIssue = kTc || kDirectEpi || kHoldSlot;
   // two CTAs per SM where the threads' registers and both rings fit (228 KB per SM)
   static constexpr int MIN_BLOCKS = (THREADS <= 224 && 2 * (SMEM_BYTES + 1024) <= 228 * 1024) ? 2 : 1;
+  static_assert(!kTc || (THREADS == 224 && MIN_BLOCKS == 2), "tcgen05 path: 7 warps, 2 CTAs per SM");
   static_assert(!kWide || (WK == 1 && T == 1 && CBS * SWB == DS * ESZ && WQ <= 2),
                 "sliced head dims: one key warp, one tile per stage, whole column blocks");
   static_assert(2 * NS * 8 <= 64, "mbarriers fit before the exchange area");
@@ -103,8 +110,10 @@ struct SplitCfg {
   static_assert(!kGroupedK || (16 * ROW) % 1024 == 0,
                 "grouped K: every 16-key box starts on a 1024-byte swizzle repeat");
   static_assert(kTc || EX_BYTES <= DATA_BYTES, "epilogue exchange reuses the stage ring");
-  static_assert(!kTc || (KS == 128 && SWB == 128 && CB == 1 && NS * 16 + 16 <= 64),
-                "tcgen05 path: 128-key stages of 128-byte rows; barriers fit before the q area");
+  static_assert(!kTc || (KS == 128 && SWB == 128 && CB == 1 && NS * 16 + 56 <= TC_TMEM_SLOT &&
+                         TC_ONES_OFF + 1024 <= kFixedBytes - 1024 && TC_ARR_OFF + 5 * 128 <= TC_ONES_OFF &&
+                         (DATA_BYTES + TC_ONES_OFF) % 1024 == 0),
+                "tcgen05 path: 128-key stages of 128-byte rows; the fixed area's layout");
   static_assert(D % 32 == 0, "head_dim is a multiple of 32");
 };
 

@@ -156,6 +156,10 @@ FUSED_CASES = {
     "three_levels": dict(lens=[40000, 9000, 300, 1], H=(8, 1), budget=4096),
     # one slot cut into pieces by the split kernel (budget 32: one partition each)
     "pieces": dict(lens=[40000] + [300 + 37 * i for i in range(15)], H=(8, 2), budget=32),
+    # 16 and 32 q heads per kv head: passes of two and four 8-row groups (on
+    # tensor memory for fp8)
+    "g16": dict(lens=[9000, 40, 2600, 300], H=(16, 1), budget=64),
+    "g32": dict(lens=[5000, 1, 700], H=(32, 2), budget=48),
 }
 
 
