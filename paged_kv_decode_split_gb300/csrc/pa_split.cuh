@@ -476,9 +476,11 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
   //   L^T[128 x 2TN] += 1 P'^T (A = a block of ones read for all 128 rows):
   //     L is every row's sum of the very weights O was accumulated with; the
   //     commit frees the ring slot.
-  // The issuing thread runs S(g + 2) as soon as P'(g) is written (S buffer
-  // g & 1 is then free), so the softmax of stage g + 1 works on an S computed
-  // while stage g's softmax ran.  A row's reference m_ref moves (O and L
+  // The issuing thread runs P V(g) as soon as P'(g) is written -- releasing
+  // the ring slot comes first -- and S(g + 2) as soon as that stage has
+  // landed and stage g's P' is written (S buffer g & 1 then free), so the
+  // softmax of stage g + 1 works on an S computed while stage g's softmax
+  // ran.  A row's reference m_ref moves (O and L
   // rescaled) only when a logit exceeds it by more than 2.8 (log2 units):
   // P' stays below 2^8.8, inside e4m3's range (448).
   // Barriers (by stage parity where two operations of a kind can be
@@ -613,47 +615,68 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
       if (lane == 0 && nst > 0) {  // one lane: no warp-collective calls in here
         const uint64_t dq = tc_desc(q_hi, 16, 1024);  // +2 per 32-byte step along K
         const uint64_t d1 = tc_desc(ones, 16, 0);     // SBO 0: one 8-row block for all 128 rows
-        // S^T = K [q_hi; q_lo]^T once stage s has landed (wait) or if it has
-        // (test): 1 issued, 0 not landed yet, -1 the wait gave up
-        auto issue_s = [&](int s, bool wait) {
-          const int g = it + s;
-          const int slot = g % Cfg::NS;
-          const uint32_t par = (g / Cfg::NS) & 1;
-          if (wait) {
-            if (!mbar_wait_or_abort(bar_full + 8 * slot, par, p.plan.err, p.wait_ns, abort_flag)) return -1;
-          } else if (!mbar_test(bar_full + 8 * slot, par)) {
-            return 0;
+        // Two kinds of work, taken as their inputs become ready, P V first
+        // (it frees a ring slot): P V(np) once P'(np) is written, and
+        // S(nq) = K [q_hi; q_lo]^T once stage nq has landed and S buffer
+        // nq & 1 is free (stage nq - 2's P' written, i.e. np >= nq - 1).
+        // Short suspending tries on both; a wait without progress for
+        // wait_ns gives up.
+        int np = 0, nq = 0;
+        bool ok = true;
+        unsigned long long t_idle = 0;
+        while (np < nst) {
+          bool did = false;
+          if (np < nq) {
+            const int g = it + np;
+            if (mbar_try_wait_hint(bar_p + 8 * (g & 1), (g >> 1) & 1, 20)) {
+              // ---- O^T += V^T P'^T and L^T += 1 P'^T; the commit frees the ring slot
+              tc_fence_after();
+              const int slot = g % Cfg::NS;
+              const uint32_t kt = base + slot * Cfg::STAGE_BYTES;
+              const uint64_t dv = tc_desc(kt + Cfg::TILE_BYTES, 16, 1024);  // +256 per 32 keys
+              const uint64_t dp = tc_desc(kt, 128, 2048, 0u);               // +32 per 32 keys
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks)
+                tc_mma_e4m3(tmem + kColO, dv + 256 * ks, dp + 32 * ks, kIdPV, np > 0 || ks > 0);
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks)
+                tc_mma_e4m3(tmem + kColL, d1 + 2 * ks, dp + 32 * ks, kIdL, np > 0 || ks > 0);
+              tc_commit(bar_empty + 8 * slot);
+              tc_commit(bar_o + 8 * (g & 1));
+              ++np;
+              did = true;
+            }
           }
-          tc_fence_after();
-          const uint64_t dk = tc_desc(base + slot * Cfg::STAGE_BYTES, 16, 1024);
-          const uint32_t sd = tmem + static_cast<uint32_t>((g & 1) * TN2);
+          if (!did && nq < nst && nq <= np + 1) {
+            const int g = it + nq;
+            const int slot = g % Cfg::NS;
+            if (mbar_try_wait_hint(bar_full + 8 * slot, (g / Cfg::NS) & 1, 20)) {
+              tc_fence_after();
+              const uint64_t dk = tc_desc(base + slot * Cfg::STAGE_BYTES, 16, 1024);
+              const uint32_t sd = tmem + static_cast<uint32_t>((g & 1) * TN2);
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) tc_mma_e4m3(sd, dk + 2 * ks, dq + 2 * ks, kIdQK, ks > 0);
-          tc_commit(bar_s + 8 * (g & 1));
-          return 1;
-        };
-        bool ok = issue_s(0, true) == 1 && (nst < 2 || issue_s(1, true) == 1);
-        for (int s = 0; ok && s < nst; ++s) {
-          const int g = it + s;
-          const int slot = g % Cfg::NS;
-          ok = mbar_wait_or_abort(bar_p + 8 * (g & 1), (g >> 1) & 1, p.plan.err, p.wait_ns, abort_flag);
-          if (!ok) break;
-          // S(g + 2) first when its tile is already there: the softmax needs it next
-          const int early = s + 2 < nst ? issue_s(s + 2, false) : 1;
-          // ---- O^T += V^T P'^T and L^T += 1 P'^T; the commit frees the ring slot
-          tc_fence_after();
-          const uint32_t kt = base + slot * Cfg::STAGE_BYTES;
-          const uint64_t dv = tc_desc(kt + Cfg::TILE_BYTES, 16, 1024);  // +256 per 32 keys
-          const uint64_t dp = tc_desc(kt, 128, 2048, 0u);               // +32 per 32 keys
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            tc_mma_e4m3(tmem + kColO, dv + 256 * ks, dp + 32 * ks, kIdPV, s > 0 || ks > 0);
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            tc_mma_e4m3(tmem + kColL, d1 + 2 * ks, dp + 32 * ks, kIdL, s > 0 || ks > 0);
-          tc_commit(bar_empty + 8 * slot);
-          tc_commit(bar_o + 8 * (g & 1));
-          if (early == 0) ok = issue_s(s + 2, true) == 1;
+              for (int ks = 0; ks < 4; ++ks) tc_mma_e4m3(sd, dk + 2 * ks, dq + 2 * ks, kIdQK, ks > 0);
+              tc_commit(bar_s + 8 * (g & 1));
+              ++nq;
+              did = true;
+            }
+          }
+          if (did) {
+            t_idle = 0;
+          } else {
+            if (*abort_flag) {
+              ok = false;
+              break;
+            }
+            const unsigned long long t = global_ns();
+            if (t_idle == 0) {
+              t_idle = t;
+            } else if (t - t_idle > p.wait_ns) {
+              atomicOr(p.plan.err, PA_DEVERR_TIMEOUT);
+              ok = false;
+              break;
+            }
+          }
         }
         if (!ok) *reinterpret_cast<volatile int*>(&s_abort) = 1;
       }
@@ -669,9 +692,12 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
         }
       }
       // P' = 64 * 2^(logit - m_ref) = 2^(S * c2 + 6 - m_ref) for every row,
-      // as f16 pairs (rows 2i, 2i + 1); masked keys give 0.
+      // as f16 pairs (rows 2i, 2i + 1); masked keys give 0.  Returns whether
+      // some P' exceeds 2^8.8 (e4m3's largest is 448): the reference must
+      // move first.
       auto make_p = [&](const float (&sv)[TN], bool sfull, int kabs, int nkeys, uint32_t (&ph)[TN / 2]) {
         const float4* nm4 = reinterpret_cast<const float4*>(s_nm);
+        uint32_t mx = 0u;
 #pragma unroll
         for (int q4 = 0; q4 < TN / 4; ++q4) {
           const float4 nm = nm4[q4];
@@ -688,7 +714,10 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
           }
           ph[2 * q4] = ex2_f16x2(f32x2_to_f16x2(a[0], a[1]));
           ph[2 * q4 + 1] = ex2_f16x2(f32x2_to_f16x2(a[2], a[3]));
+          mx = max_f16x2(mx, max_f16x2(ph[2 * q4], ph[2 * q4 + 1]));
         }
+        const float2 m2 = __half22float2(*reinterpret_cast<const __half2*>(&mx));
+        return fmaxf(m2.x, m2.y) > 445.f;
       };
       for (int s = 0; s < nst; ++s) {
         const int g = it + s;
@@ -703,6 +732,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
         const bool sfull = nkeys == Cfg::KS && key0 >= vis_lo && key0 + Cfg::KS <= vis_hi;
         const bool live = !aborted() && wait_sm(bar_s + 8 * sb, (g >> 1) & 1);
         float sv[TN];
+        uint32_t ph[TN / 2];
         bool over = false;  // some P' would exceed 2^8.8 (e4m3's largest is 448)
         if (live) {
           tc_fence_after();
@@ -710,28 +740,12 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
           tc_ld<TN2>(tl + static_cast<uint32_t>(sb * TN2), a);
 #pragma unroll
           for (int j = 0; j < TN; ++j) sv[j] = __uint_as_float(a[j]) + __uint_as_float(a[TN + j]);
-          const float4* nm4 = reinterpret_cast<const float4*>(s_nm);
-          float amax = NEG_INF;
-#pragma unroll
-          for (int q4 = 0; q4 < TN / 4; ++q4) {
-            const float4 nm = nm4[q4];
-            float x[4] = {fmaf(sv[4 * q4], c2, nm.x), fmaf(sv[4 * q4 + 1], c2, nm.y),
-                          fmaf(sv[4 * q4 + 2], c2, nm.z), fmaf(sv[4 * q4 + 3], c2, nm.w)};
-            if (!sfull) {
-              const int4 lim = reinterpret_cast<const int4*>(s_lim)[q4];
-              const int4 llo = reinterpret_cast<const int4*>(s_llo)[q4];
-              const bool in = kk < nkeys;
-              if (!(in && kabs < lim.x && kabs >= llo.x)) x[0] = NEG_INF;
-              if (!(in && kabs < lim.y && kabs >= llo.y)) x[1] = NEG_INF;
-              if (!(in && kabs < lim.z && kabs >= llo.z)) x[2] = NEG_INF;
-              if (!(in && kabs < lim.w && kabs >= llo.w)) x[3] = NEG_INF;
-            }
-            amax = fmaxf(amax, fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])));
-          }
-          over = amax > 8.8f;
+          over = make_p(sv, sfull, kabs, nkeys, ph);
         } else {
 #pragma unroll
           for (int j = 0; j < TN; ++j) sv[j] = 0.f;
+#pragma unroll
+          for (int j = 0; j < TN / 2; ++j) ph[j] = 0u;
         }
         if (named_barrier_or(2, 128, over)) {
           // A new reference per row: the running maximum; O and L rescaled.
@@ -784,9 +798,8 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
               tc_st<32>(tl + kColO + static_cast<uint32_t>(c0), ov);
             }
           }
+          make_p(sv, sfull, kabs, nkeys, ph);  // every P' is now at most 2^8.8
         }
-        uint32_t ph[TN / 2];  // every P' is now at most 2^8.8
-        make_p(sv, sfull, kabs, nkeys, ph);
         // P' as e4m3 hi + lo: 16 rows per 16-byte store
         if (!aborted()) {
 #pragma unroll
