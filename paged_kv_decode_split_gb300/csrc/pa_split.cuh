@@ -146,9 +146,9 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     return;
   }
   if constexpr (Cfg::kTc) {
-    // 8 TN columns of tensor memory: S^T buffers [0, 2 TN) and [2 TN, 4 TN),
-    // O^T [4 TN, 6 TN), L^T [6 TN, 8 TN) (each hi then lo); two CTAs per SM
-    // take at most the SM's 512
+    // Tensor memory: four regions of 2 TN columns (hi then lo) at multiples of
+    // 32 (16 rows) or 64 columns -- S^T buffers 0 and 1, O^T, L^T; two CTAs
+    // per SM take at most the SM's 512
     if (warp == Cfg::NPW) tc_alloc(base + Cfg::DATA_BYTES + Cfg::TC_TMEM_SLOT, Cfg::TC_COLS);
     tc_fence_before();
   }
@@ -469,9 +469,10 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
   //     tile, K-major; B = q * 2^qexp, K-major);
   //   P' = 64 * 2^(logit - m_ref) for every key and row (f16 exponential),
   //     as e4m3 hi and lo, written over the stage's K tile (dead once S is
-  //     computed): planes of 16 rows, key k's 16 bytes at k * 16 (MN-major,
-  //     no swizzle), hi planes then lo planes, so each softmax thread stores
-  //     whole 16-byte rows;
+  //     computed): the 2 TN bytes of key k -- hi for every row, then lo --
+  //     in chunks of 16 (16 of the MMA's N rows each), chunk c at c * 2048
+  //     + k * 16 (MN-major, no swizzle), so each softmax thread stores whole
+  //     16-byte rows;
   //   O^T[128 dims x 2TN] += V^T P'^T (A = the V tile read MN-major) and
   //   L^T[128 x 2TN] += 1 P'^T (A = a block of ones read for all 128 rows):
   //     L is every row's sum of the very weights O was accumulated with; the
@@ -512,11 +513,13 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
   const volatile int* abort_flag = reinterpret_cast<volatile int*>(&s_abort);
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smb + Cfg::DATA_BYTES + Cfg::TC_TMEM_SLOT);
   const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);  // this warp's lanes
-  constexpr uint32_t kColO = 2 * TN2, kColL = 3 * TN2;  // S buffers at 0 and TN2
+  // tensor-memory regions (each 2 TN columns, hi then lo) at multiples of CS:
+  // S buffers 0 and 1, O^T, L^T
+  constexpr int CS = TN2 <= 32 ? 32 : 64;
+  constexpr uint32_t kColO = 2 * CS, kColL = 3 * CS;
   constexpr uint32_t kIdQK = tc_idesc(0, 0, TN2, 128);  // K (K-major) x q (K-major)
   constexpr uint32_t kIdPV = tc_idesc(1, 1, TN2, 128);  // V^T (MN-major) x P' (MN-major)
   constexpr uint32_t kIdL = tc_idesc(0, 1, TN2, 128);   // ones (K-major) x P' (MN-major)
-  constexpr uint32_t kPlo = TN * 128;                   // P' lo planes, from the K tile
   // Softmax warps: a bounded wait that also ends once the pipeline aborted
   // (warp-uniform result; a failure raises the abort).
   auto wait_sm = [&](uint32_t bar, uint32_t parity) {
@@ -653,7 +656,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
             if (mbar_try_wait_hint(bar_full + 8 * slot, (g / Cfg::NS) & 1, 20)) {
               tc_fence_after();
               const uint64_t dk = tc_desc(base + slot * Cfg::STAGE_BYTES, 16, 1024);
-              const uint32_t sd = tmem + static_cast<uint32_t>((g & 1) * TN2);
+              const uint32_t sd = tmem + static_cast<uint32_t>((g & 1) * CS);
 #pragma unroll
               for (int ks = 0; ks < 4; ++ks) tc_mma_e4m3(sd, dk + 2 * ks, dq + 2 * ks, kIdQK, ks > 0);
               tc_commit(bar_s + 8 * (g & 1));
@@ -737,7 +740,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
         if (live) {
           tc_fence_after();
           uint32_t a[TN2];
-          tc_ld<TN2>(tl + static_cast<uint32_t>(sb * TN2), a);
+          tc_ld<TN2>(tl + static_cast<uint32_t>(sb * CS), a);
 #pragma unroll
           for (int j = 0; j < TN; ++j) sv[j] = __uint_as_float(a[j]) + __uint_as_float(a[TN + j]);
           over = make_p(sv, sfull, kabs, nkeys, ph);
@@ -753,8 +756,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
           // shared memory -- the stage's K tile, dead since S was computed
           // and not yet overwritten by P' -- as [TN rows][128 keys] floats,
           // 16-byte groups XOR-swizzled by the row so that the readers below
-          // (TN / 4 or TN / 8 rows per warp, 16 keys each per load) hit
-          // distinct banks.
+          // (8 rows per warp, 4 threads per row) hit distinct banks.
           float* tt = reinterpret_cast<float*>(smb + (kt - base));
 #pragma unroll
           for (int j = 0; j < TN; ++j) {
@@ -763,19 +765,17 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
             tt[j * 128 + (kk ^ ((j & 7) << 2))] = vis ? sv[j] * c2 : NEG_INF;
           }
           named_barrier_sync(2, 128);
-          {
-            constexpr int PER = 128 / TN;          // threads per row
-            constexpr int NF4 = (128 / PER) / 4;   // float4 groups per thread
-            const int j = st / PER, part = st % PER;
+          if (st < 4 * TN) {  // 4 threads per row, 32 keys (8 float4) each
+            const int j = st >> 2, part = st & 3;
             float m = NEG_INF;
 #pragma unroll 1
-            for (int i = 0; i < NF4; ++i) {
-              const int f4 = (part * NF4 + i) ^ (j & 7);
+            for (int i = 0; i < 8; ++i) {
+              const int f4 = (part * 8 + i) ^ (j & 7);
               const float4 v = reinterpret_cast<const float4*>(tt + j * 128)[f4];
               m = fmaxf(m, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
             }
-#pragma unroll
-            for (int o = PER / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
             if (part == 0) {
               const float mo = s_mref[j];
               const float mn = fmaxf(mo, m);
@@ -789,35 +789,35 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
           if (s > 0 && wait_sm(bar_o + 8 * ((g - 1) & 1), ((g - 1) >> 1) & 1)) {
             tc_fence_after();
 #pragma unroll 1
-            for (int c0 = 0; c0 < 2 * TN2; c0 += 32) {  // O hi, O lo, L hi, L lo
-              uint32_t ov[32];
-              tc_ld<32>(tl + kColO + static_cast<uint32_t>(c0), ov);
+            for (int c = 0; c < 2 * TN2; c += 16) {  // O hi, O lo, then L hi, L lo
+              const uint32_t col = (c < TN2 ? kColO + c : kColL + (c - TN2));
+              uint32_t ov[16];
+              tc_ld<16>(tl + col, ov);
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                ov[i] = __float_as_uint(__uint_as_float(ov[i]) * s_fac[(c0 + i) % TN]);
-              tc_st<32>(tl + kColO + static_cast<uint32_t>(c0), ov);
+              for (int i = 0; i < 16; ++i)
+                ov[i] = __float_as_uint(__uint_as_float(ov[i]) * s_fac[(c % TN2 + i) % TN]);
+              tc_st<16>(tl + col, ov);
             }
           }
           make_p(sv, sfull, kabs, nkeys, ph);  // every P' is now at most 2^8.8
         }
-        // P' as e4m3 hi + lo: 16 rows per 16-byte store
+        // P' as e4m3 hi + lo: the words of 4 rows' hi bytes, then of their lo
+        // bytes, 4 words per 16-byte store
         if (!aborted()) {
+          uint32_t pw[TN / 2];
 #pragma unroll
-          for (int c = 0; c < TN / 16; ++c) {
-            uint32_t hw[4], lw[4];
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              const uint32_t x0 = ph[8 * c + 2 * w], x1 = ph[8 * c + 2 * w + 1];
-              const uint32_t h0 = f16x2_to_e4m3x2(x0), h1 = f16x2_to_e4m3x2(x1);
-              const uint32_t l0 = f16x2_to_e4m3x2(sub_f16x2(x0, e4m3x2_to_f16x2(h0)));
-              const uint32_t l1 = f16x2_to_e4m3x2(sub_f16x2(x1, e4m3x2_to_f16x2(h1)));
-              hw[w] = h0 | (h1 << 16);
-              lw[w] = l0 | (l1 << 16);
-            }
-            const uint32_t off = (kt - base) + static_cast<uint32_t>(c * 2048 + kk * 16);
-            *reinterpret_cast<uint4*>(smb + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4*>(smb + off + kPlo) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          for (int w = 0; w < TN / 4; ++w) {
+            const uint32_t x0 = ph[2 * w], x1 = ph[2 * w + 1];
+            const uint32_t h0 = f16x2_to_e4m3x2(x0), h1 = f16x2_to_e4m3x2(x1);
+            const uint32_t l0 = f16x2_to_e4m3x2(sub_f16x2(x0, e4m3x2_to_f16x2(h0)));
+            const uint32_t l1 = f16x2_to_e4m3x2(sub_f16x2(x1, e4m3x2_to_f16x2(h1)));
+            pw[w] = h0 | (h1 << 16);
+            pw[TN / 4 + w] = l0 | (l1 << 16);
           }
+#pragma unroll
+          for (int c = 0; c < TN / 8; ++c)
+            *reinterpret_cast<uint4*>(smb + (kt - base) + static_cast<uint32_t>(c * 2048 + kk * 16)) =
+                make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
           if (kk >= nkeys) {  // keys past the piece: their V rows may hold anything (0 * NaN)
             uint4* vr = reinterpret_cast<uint4*>(smb + (vt - base) + kk * 128);
 #pragma unroll

@@ -33,9 +33,9 @@ struct SplitCfg {
   // run on tcgen05.mma (kind::f8f6f4) with the accumulators in TMEM, K and V^T
   // read straight from the TMA tiles, q and P as e4m3 hi + lo pairs; one warp
   // issues the MMAs and one warpgroup does the softmax, one thread per key.
-  // TN: the MMA's N (the pass's query rows, padded to 16 or 32).
+  // TN: the pass's query rows (16, 24 or 32); the MMAs' N is 2 TN.
   static constexpr bool kTc = kFp8 && D == 128 && KL == 0 && WQ >= 2;
-  static constexpr int TN = WQ <= 2 ? 16 : 32;
+  static constexpr int TN = 8 * WQ;
   static constexpr int DS = kWide ? (D % 256 == 0 ? 256 : 128) : D;  // head dims per consumer warp
   static constexpr int ND = D / DS;                   // dim slices
   static constexpr int CBS = DS * ESZ / SWB;          // column blocks per slice
@@ -54,7 +54,7 @@ struct SplitCfg {
   static constexpr int TC_Q_OFF = 1024;
   static constexpr int TC_ARR_OFF = TC_Q_OFF + 8192;    // row limits, references, factors
   static constexpr int TC_ONES_OFF = TC_ARR_OFF + 1024;  // 1 KB of e4m3 ones, 1024-aligned
-  static constexpr int TC_COLS = 8 * TN;                // tensor-memory columns
+  static constexpr int TC_COLS = TN == 16 ? 128 : 256;  // tensor-memory columns: 4 regions
   static constexpr int kFixedBytes = kTc ? 1024 + TC_ARR_OFF + 2048 : 1024 + 64 + SX_BYTES;
   static constexpr bool kTwoPerSm3 = 2 * (3 * 2 * KS * ROW + kFixedBytes + 1024) <= 228 * 1024;
   static constexpr bool kTwoPerSm2 = 2 * (2 * 2 * KS * ROW + kFixedBytes + 1024) <= 228 * 1024;
