@@ -473,10 +473,11 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
   //     in chunks of 16 (16 of the MMA's N rows each), chunk c at c * 2048
   //     + k * 16 (MN-major, no swizzle), so each softmax thread stores whole
   //     16-byte rows;
-  //   O^T[128 dims x 2TN] += V^T P'^T (A = the V tile read MN-major) and
-  //   L^T[128 x 2TN] += 1 P'^T (A = a block of ones read for all 128 rows):
-  //     L is every row's sum of the very weights O was accumulated with; the
-  //     commit frees the ring slot.
+  //   O^T[128 dims x 2TN] += V^T P'^T (A = the V tile read MN-major) and,
+  //   for 32-row passes, L^T[128 x 2TN] += 1 P'^T (A = a block of ones read
+  //     for all 128 rows): L is every row's sum of the very weights O was
+  //     accumulated with (for fewer rows each softmax thread sums its key's
+  //     share); the commit frees the ring slot.
   // The issuing thread runs P V(g) as soon as P'(g) is written -- releasing
   // the ring slot comes first -- and S(g + 2) as soon as that stage has
   // landed and stage g's P' is written (S buffer g & 1 then free), so the
@@ -520,6 +521,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
   constexpr uint32_t kIdQK = tc_idesc(0, 0, TN2, 128);  // K (K-major) x q (K-major)
   constexpr uint32_t kIdPV = tc_idesc(1, 1, TN2, 128);  // V^T (MN-major) x P' (MN-major)
   constexpr uint32_t kIdL = tc_idesc(0, 1, TN2, 128);   // ones (K-major) x P' (MN-major)
+  constexpr bool kRsMma = Cfg::kTcRowSumMma;            // row sums by MMA, else per thread
   // Softmax warps: a bounded wait that also ends once the pipeline aborted
   // (warp-uniform result; a failure raises the abort).
   auto wait_sm = [&](uint32_t bar, uint32_t parity) {
@@ -641,9 +643,11 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
 #pragma unroll
               for (int ks = 0; ks < 4; ++ks)
                 tc_mma_e4m3(tmem + kColO, dv + 256 * ks, dp + 32 * ks, kIdPV, np > 0 || ks > 0);
+              if constexpr (kRsMma) {
 #pragma unroll
-              for (int ks = 0; ks < 4; ++ks)
-                tc_mma_e4m3(tmem + kColL, d1 + 2 * ks, dp + 32 * ks, kIdL, np > 0 || ks > 0);
+                for (int ks = 0; ks < 4; ++ks)
+                  tc_mma_e4m3(tmem + kColL, d1 + 2 * ks, dp + 32 * ks, kIdL, np > 0 || ks > 0);
+              }
               tc_commit(bar_empty + 8 * slot);
               tc_commit(bar_o + 8 * (g & 1));
               ++np;
@@ -722,6 +726,9 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
         const float2 m2 = __half22float2(*reinterpret_cast<const __half2*>(&mx));
         return fmaxf(m2.x, m2.y) > 445.f;
       };
+      float lp[kRsMma ? 1 : TN];  // (row sums per thread) this key's share of each row's sum
+#pragma unroll
+      for (int j = 0; j < (kRsMma ? 1 : TN); ++j) lp[j] = 0.f;
       for (int s = 0; s < nst; ++s) {
         const int g = it + s;
         const int slot = g % Cfg::NS;
@@ -785,11 +792,22 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
             }
           }
           named_barrier_sync(2, 128);
+          if constexpr (!kRsMma) {
+            const float4* f4 = reinterpret_cast<const float4*>(s_fac);
+#pragma unroll
+            for (int q4 = 0; q4 < TN / 4; ++q4) {
+              const float4 f = f4[q4];
+              lp[4 * q4] *= f.x;
+              lp[4 * q4 + 1] *= f.y;
+              lp[4 * q4 + 2] *= f.z;
+              lp[4 * q4 + 3] *= f.w;
+            }
+          }
           // the previous stage's P V (the only one that can be outstanding)
           if (s > 0 && wait_sm(bar_o + 8 * ((g - 1) & 1), ((g - 1) >> 1) & 1)) {
             tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < 2 * TN2; c += 16) {  // O hi, O lo, then L hi, L lo
+            for (int c = 0; c < (kRsMma ? 2 : 1) * TN2; c += 16) {  // O hi, O lo (, L hi, L lo)
               const uint32_t col = (c < TN2 ? kColO + c : kColL + (c - TN2));
               uint32_t ov[16];
               tc_ld<16>(tl + col, ov);
@@ -800,6 +818,14 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
             }
           }
           make_p(sv, sfull, kabs, nkeys, ph);  // every P' is now at most 2^8.8
+        }
+        if constexpr (!kRsMma) {
+#pragma unroll
+          for (int i = 0; i < TN / 2; ++i) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ph[i]));
+            lp[2 * i] += f.x;
+            lp[2 * i + 1] += f.y;
+          }
         }
         // P' as e4m3 hi + lo: the words of 4 rows' hi bytes, then of their lo
         // bytes, 4 words per 16-byte store
@@ -835,20 +861,33 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
       const int gl = it + nst - 1;
       const bool have_o = nst > 0 && !aborted() && wait_sm(bar_o + 8 * (gl & 1), (gl >> 1) & 1);
       tc_fence_after();
-      if (sw == 0) {  // row sums: every lane of L holds them all
-        uint32_t a[TN2];
-        if (have_o) {
-          tc_ld<TN2>(tl + kColL, a);
-        } else {
+      if constexpr (kRsMma) {
+        if (sw == 0) {  // row sums: every lane of L holds them all
+          uint32_t a[TN2];
+          if (have_o) {
+            tc_ld<TN2>(tl + kColL, a);
+          } else {
 #pragma unroll
-          for (int j = 0; j < TN2; ++j) a[j] = 0u;
-        }
-        if (lane == 0) {
+            for (int j = 0; j < TN2; ++j) a[j] = 0u;
+          }
+          if (lane == 0) {
 #pragma unroll
-          for (int j = 0; j < TN; ++j) s_fac[j] = __uint_as_float(a[j]) + __uint_as_float(a[TN + j]);
+            for (int j = 0; j < TN; ++j) s_fac[j] = __uint_as_float(a[j]) + __uint_as_float(a[TN + j]);
+          }
         }
+        named_barrier_sync(2, 128);
+      } else {  // row sums: the threads' shares, over the warp, then the 4 warps
+#pragma unroll
+        for (int j = 0; j < TN; ++j) {
+          float x = lp[j];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+          if (lane == 0) s_red[sw * 32 + j] = x;
+        }
+        named_barrier_sync(2, 128);
+        if (st < TN) s_fac[st] = s_red[st] + s_red[32 + st] + s_red[64 + st] + s_red[96 + st];
+        named_barrier_sync(2, 128);
       }
-      named_barrier_sync(2, 128);
       float ov[TN];
       {
         uint32_t a[TN2];

@@ -36,6 +36,14 @@ struct SplitCfg {
   // TN: the pass's query rows (16, 24 or 32); the MMAs' N is 2 TN.
   static constexpr bool kTc = kFp8 && D == 128 && KL == 0 && WQ >= 2;
   static constexpr int TN = 8 * WQ;
+  // Row sums of P': by an MMA of a block of ones (32 rows: the per-thread
+  // sums would cost the softmax, there the bottleneck, registers and time)
+  // or summed by the softmax threads (16 and 24 rows: four fewer MMAs per
+  // stage for the issuing thread, about 90 cycles each, on the path that
+  // releases a ring slot).  Measured: 3-token verify 0.559 -> 0.575 of the
+  // copy peak and the skewed 3-token batch 90.6 -> 85.0 us with per-thread
+  // sums; 4 tokens 0.503 -> 0.486 (so 32 rows keep the MMA).
+  static constexpr bool kTcRowSumMma = TN >= 32;
   static constexpr int DS = kWide ? (D % 256 == 0 ? 256 : 128) : D;  // head dims per consumer warp
   static constexpr int ND = D / DS;                   // dim slices
   static constexpr int CBS = DS * ESZ / SWB;          // column blocks per slice
