@@ -424,13 +424,16 @@ def test_verify_row_groups(dev, ql):
 
 
 @pytest.mark.parametrize("D", [64, 128, 256])
-@pytest.mark.parametrize("ql,H", [(2, (8, 1)), (3, (8, 1)), (3, (6, 1)), (2, (12, 2))])
-@pytest.mark.parametrize("bs", [16, 64])
+@pytest.mark.parametrize("ql,H", [(2, (8, 1)), (3, (8, 1)), (3, (6, 1)), (2, (12, 2)), (4, (8, 1))])
+@pytest.mark.parametrize("bs", [16, 64, 128])
 def test_fp8_verify_rows(dev, D, ql, H, bs):
-    """fp8 caches with two or three query-row groups per pass (speculative
-    verify rows on an fp8 cache).  Ragged lengths (one-key requests, rows with
-    no visible key, a zero-length request), graph padding, fp16 and bf16 q,
-    against the oracle."""
+    """fp8 caches with two to four query-row groups per pass (speculative
+    verify rows on an fp8 cache; at D 128 the tensor-memory consumer, 16, 24
+    and 32 rows, row sums per thread and by the ones MMA; pages of 16 keys
+    (two producer warps), 64 and 128 (one copy per tensor and stage)).
+    Ragged lengths (one-key requests, rows with no visible key, a
+    zero-length request), graph padding, fp16 and bf16 q, against the
+    oracle."""
     lens = [5000, 900, 64, 1, 2, 257, 3000]
     q = "fp16" if (D + ql) % 2 else "bf16"
     w = batch(dev, lens, ql=[ql] * len(lens), H=H, D=D, bs=bs, kv="fp8", q=q, pad=3,
