@@ -553,19 +553,28 @@ def test_bad_page_is_reported_not_faulted(dev, grouped):
     assert max_diff(out[[1]], ref) <= TOL["bf16"]
 
 
-@pytest.mark.parametrize("case", ["d128", "d128_two_rows", "d512_slices"])
+@pytest.mark.parametrize("case", ["d128", "d128_two_rows", "d512_slices", "fp8_two_rows",
+                                  "fp8_four_rows"])
 def test_a_wait_that_runs_out_sets_the_timeout_bit(dev, case):
     """The timeout path, made to run on purpose: with a 100 us wait limit and
     the test hook that leaves every CTA's second pipeline stage un-issued, the
     consumers' bounded waits give up, PA_DEVERR_TIMEOUT is raised, the call
     returns (every barrier is still met on the abort path: the single-slice
-    kernel, the two-row-group exchange epilogue, and a 512-dim head whose
-    slice warps meet a named barrier per stage), and the next call on the same
-    plan, with the hook off and the default limit, is correct."""
+    kernel, the two-row-group exchange epilogue, a 512-dim head whose slice
+    warps meet a named barrier per stage, and the tensor-memory consumer --
+    its issuing thread gives up on the missing tile, the softmax warps on
+    its S, and the tensor memory is released after a last commit -- with
+    per-thread row sums (16 rows) and the ones MMA (32 rows)), and the next
+    call on the same plan, with the hook off and the default limit, is
+    correct."""
     if case == "d128":
         w = batch(dev, [3000, 800, 1200, 17], H=(8, 2), D=128, seed=71)
     elif case == "d128_two_rows":
         w = batch(dev, [3000, 800, 1200], ql=[2, 2, 2], H=(8, 1), D=128, pad=2, seed=72)
+    elif case.startswith("fp8"):
+        ql = 2 if case == "fp8_two_rows" else 4
+        w = batch(dev, [3000, 800, 1200], ql=[ql] * 3, H=(8, 1), D=128, kv="fp8", pad=2,
+                  seed=74 + ql)
     else:
         w = batch(dev, [3000, 800, 1200], H=(8, 1), D=512, seed=73)
     plan = binding.plan_for(w)
