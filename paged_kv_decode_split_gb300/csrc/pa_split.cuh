@@ -482,9 +482,9 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
   // the ring slot comes first -- and S(g + 2) as soon as that stage has
   // landed and stage g's P' is written (S buffer g & 1 then free), so the
   // softmax of stage g + 1 works on an S computed while stage g's softmax
-  // ran.  A row's reference m_ref moves (O and L
-  // rescaled) only when a logit exceeds it by more than 2.8 (log2 units):
-  // P' stays below 2^8.8, inside e4m3's range (448).
+  // ran.  A row's reference m_ref moves (O and L rescaled) only when a logit
+  // exceeds it by more than 2.8 (log2 units): P' stays below 2^8.8, inside
+  // e4m3's range (448).
   // Barriers (by stage parity where two operations of a kind can be
   // outstanding): S computed [2], P' written [2], P V done [2], and one for
   // the last commit before the tensor memory is released.
@@ -548,7 +548,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
         s_mref[st] = NEG_INF;
         s_nm[st] = POS_INF;
       }
-      if (st < 64)  // the block of e4m3 ones (0x38) read as every row of L's A operand
+      if (kRsMma && st < 64)  // the block of e4m3 ones (0x38) read as every row of L's A operand
         *reinterpret_cast<uint4*>(smb + (ones - base) + st * 16) =
             make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
       float qv[32];
