@@ -638,15 +638,17 @@ def profile_run(args, dev):
 
 
 def _fusable(w) -> bool:
-    """Whether a workload's plan can take the fused merge: one query row per
-    request, head dim at most 256, a GQA group of at most 32 rows."""
+    """Whether a workload's plan can take the fused merge: head dim at most
+    256, and every request's query rows (tokens x GQA group) in one work item
+    of at most 32 rows."""
     b = w.base if isinstance(w, wl.SparseWorkload) else w
-    if b.head_dim > 256 or b.num_q_heads // b.num_kv_heads > 32:
+    g = b.num_q_heads // b.num_kv_heads
+    if b.head_dim > 256 or g > 32:
         return False
     if b.cu_query_lens is None:
         return True
     cu = b.cu_query_lens.cpu()
-    return int((cu[1:] - cu[:-1]).max()) <= 1
+    return int((cu[1:] - cu[:-1]).max()) * g <= 32
 
 
 def _pct(xs, q):

@@ -208,11 +208,11 @@ int pa_plan_set_kv_dtype(pa_plan* plan, int kv_dtype);
  * group's last ticket (an atomic count, no waiting) and merges the group, up a
  * tree until the request's output rows are written -- and pa_decode launches
  * one kernel; enable = 0: a separate merge kernel runs after the split kernel.
- * The fused merge is possible for plans with one query row per request
- * (max_query_len 1), head_dim at most 256, whose GQA group fits one work item
- * of the split kernel;
- * every other plan keeps the merge kernel, where a request's many query rows
- * are better spread over many CTAs.  The default is 0 for every plan: on
+ * The fused merge is possible for plans whose requests' query rows
+ * (max_query_len x the GQA group) fit one work item of the split kernel (at
+ * most 32 rows) and whose head_dim is at most 256; every other plan keeps the
+ * merge kernel, where a request's many query rows are better spread over many
+ * CTAs.  The default is 0 for every plan: on
  * GB300 the merge kernel, chained to the split kernel by programmatic
  * dependent launch, measured 1.2-8 us faster per decode call on every batch
  * tried (the ticket round trip after each piece stalls that CTA's pipeline).

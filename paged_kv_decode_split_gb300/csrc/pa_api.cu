@@ -133,10 +133,10 @@ PlanLayout plan_layout(int num_seqs, int Hq, int Hkv, int D, int max_qlen, int m
   l.rpc = 8 * split_row_groups(max_qlen, G, D);
   l.max_extra = split_max_extra(G, l.rpc, l.rows_cap, max_tokens, max_qlen);
   // The split kernel can merge a request's partials itself when every query
-  // row of a request is in one work item, there is one row per request, and
-  // the head dim is at most 256 (the wide-head kernels are at their register
-  // limit and are built without the fused merge).
-  l.fused = (fused && max_qlen == 1 && G <= l.rpc && D <= 256) ? 1 : 0;
+  // row of a request (its tokens x G) is in one work item and the head dim is
+  // at most 256 (the wide-head kernels are at their register limit and are
+  // built without the fused merge).
+  l.fused = (fused && static_cast<long long>(max_qlen) * G <= l.rpc && D <= 256) ? 1 : 0;
   l.levels = 0;
   if (l.fused) {
     const long long kmax = static_cast<long long>(l.Q) * max_partitions;

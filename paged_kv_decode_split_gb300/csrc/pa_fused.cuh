@@ -3,8 +3,9 @@
 // work planner", section 6 item 5 and review item 7: the partial-softmax
 // reduce after the split attention tiles costs a second launch and ~14%).
 //
-// A request r with K >= 2 pieces leaves, per kv head h, K normalised fp32
-// partial rows (one per piece, G q heads each) and their log2-sum-exps.  Here
+// A request r of L query rows (tokens) with K >= 2 pieces leaves, per kv head
+// h, K x L normalised fp32 partial rows (piece k's row for token t at
+// base + k * L + t, G q heads each) and their log2-sum-exps.  Here
 // the CTAs that wrote them combine them, with no waits: pieces form groups of
 // kFusedFanIn consecutive ones; a CTA that finishes a piece takes a ticket of
 // its group (an atomic count per group, level and kv head), and the one that
@@ -33,23 +34,26 @@
 namespace pa {
 
 // Merges items [first, first + count) of `level` of request r's tree for kv
-// head h -- item i lives in partial row base + (i << 3*level) -- for the G q
-// heads of h, one warp per q head.  final: write the output row `orow`;
-// otherwise write the merged partial in place of item `first`.
+// head h -- item i's row for token t lives in partial row
+// base + (i << 3*level) * L + t -- for the L tokens and G q heads of h, one
+// warp per (token, q head).  final: write the output rows orow + t;
+// otherwise write the merged partials in place of item `first`.
 template <int D>
-__device__ __forceinline__ void fused_merge_group(const SplitParams& p, int h, int base, int first,
-                                                  int count, int level, bool final, int orow,
-                                                  int cw, int ncw, int lane) {
+__device__ __forceinline__ void fused_merge_group(const SplitParams& p, int h, int base, int L,
+                                                  int first, int count, int level, bool final,
+                                                  int orow, int cw, int ncw, int lane) {
   constexpr int VL = D / 32;            // outputs per lane
   constexpr int PB = VL <= 8 ? kFusedFanIn : (VL <= 16 ? 2 : 1);  // items loaded at once
   const float NEG_INF = -__int_as_float(0x7f800000);
   const int G = p.G, Hq = p.Hq;
   const int sh = kFusedLog2FanIn * level;
-  for (int gq = cw; gq < G; gq += ncw) {
+  for (int x = cw; x < L * G; x += ncw) {
+    const int t = x / G, gq = x - t * G;  // token, q head of h
     const int hq = h * G + gq;
     float lse = NEG_INF;
     if (lane < count)
-      lse = __ldcg(p.plan.part_lse + static_cast<long long>(base + ((first + lane) << sh)) * Hq + hq);
+      lse = __ldcg(p.plan.part_lse +
+                   static_cast<long long>(base + ((first + lane) << sh) * L + t) * Hq + hq);
     float M = lse;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
@@ -67,7 +71,7 @@ __device__ __forceinline__ void fused_merge_group(const SplitParams& p, int h, i
         const int j = j0 + k;
         if (j < count) {
           const float* src = p.plan.part_o +
-                             (static_cast<long long>(base + ((first + j) << sh)) * Hq + hq) * D +
+                             (static_cast<long long>(base + ((first + j) << sh) * L + t) * Hq + hq) * D +
                              lane * VL;
           if constexpr (VL % 4 == 0) {
 #pragma unroll
@@ -95,7 +99,7 @@ __device__ __forceinline__ void fused_merge_group(const SplitParams& p, int h, i
         for (int v = 0; v < VL; ++v) acc[v] += wj * o[k][v];
       }
     }
-    if (final && orow >= p.num_tokens) {  // a row past the call's rows: the plan was not
+    if (final && orow + t >= p.num_tokens) {  // a row past the call's rows: the plan was not
       if (lane == 0) atomicOr(p.plan.err, PA_DEVERR_PLAN_OVERFLOW);  // made for this call
     } else if (final) {
       if (p.sinks) {  // the head's sink joins the denominator once, at the last level
@@ -109,7 +113,7 @@ __device__ __forceinline__ void fused_merge_group(const SplitParams& p, int h, i
       for (int v = 0; v < VL; v += 2)
         pk[v / 2] = p.out_f16 ? pack2<false>(acc[v] * inv, acc[v + 1] * inv)
                               : pack2<true>(acc[v] * inv, acc[v + 1] * inv);
-      uint16_t* dst = static_cast<uint16_t*>(p.out) + (static_cast<size_t>(orow) * Hq + hq) * D +
+      uint16_t* dst = static_cast<uint16_t*>(p.out) + (static_cast<size_t>(orow + t) * Hq + hq) * D +
                       lane * VL;
       if constexpr (VL == 2) {
         *reinterpret_cast<uint32_t*>(dst) = pk[0];
@@ -124,7 +128,7 @@ __device__ __forceinline__ void fused_merge_group(const SplitParams& p, int h, i
       }
     } else {
       const float inv = W > 0.f ? 1.f / W : 0.f;
-      const long long prow = static_cast<long long>(base + (first << sh)) * Hq + hq;
+      const long long prow = static_cast<long long>(base + (first << sh) * L + t) * Hq + hq;
       float* dst = p.plan.part_o + prow * D + lane * VL;
 #pragma unroll
       for (int v = 0; v < VL; v += 2)
@@ -135,16 +139,17 @@ __device__ __forceinline__ void fused_merge_group(const SplitParams& p, int h, i
 }
 
 // Called by every consumer thread (ct in [0, ncw * 32), consumer warp cw) once
-// the item's partial rows (piece partial row `prow`, request r, kv head h) are
-// written.  Takes this piece's tickets up the tree and merges where it took a
-// group's last one; orow is the request's output row.
+// the item's partial rows (piece partial rows from `prow`, one per token of
+// the request's L; request r, kv head h) are written.  Takes this piece's
+// tickets up the tree and merges where it took a group's last one; orow is the
+// request's first output row.
 template <int D>
-__device__ __noinline__ void fused_merge(const SplitParams& p, int r, int h, int prow, int orow, int ct, int cw,
-                            int ncw, int lane) {
+__device__ __noinline__ void fused_merge(const SplitParams& p, int r, int h, int prow, int orow, int L,
+                                         int ct, int cw, int ncw, int lane) {
   __shared__ int s_last;
   const int2 pq = p.plan.preq[r];  // (first partial row, pieces)
   const int base = pq.x;
-  int k = prow - base;             // this piece's index, then its group's at each level
+  int k = (prow - base) / L;       // this piece's index, then its group's at each level
   int K = pq.y;                    // items at this level
   for (int level = 0;; ++level) {
     const int first = (k >> kFusedLog2FanIn) << kFusedLog2FanIn;
@@ -153,7 +158,7 @@ __device__ __noinline__ void fused_merge(const SplitParams& p, int r, int h, int
     if (ct == 0) {
       int* t = p.plan.tickets +
                (static_cast<long long>(level) * p.rows_cap +
-                (base + (first << (kFusedLog2FanIn * level)))) * p.Hkv + h;
+                (base + (first << (kFusedLog2FanIn * level)) * L)) * p.Hkv + h;
       fence_acq_rel_gpu();  // release: the CTA's partials above precede the ticket
       const int prev = atomicAdd(t, 1);
       const int last = prev == count - 1;
@@ -166,7 +171,7 @@ __device__ __noinline__ void fused_merge(const SplitParams& p, int r, int h, int
     named_barrier_sync(1, ncw * 32);
     if (!s_last) return;
     const bool final = K <= kFusedFanIn;
-    fused_merge_group<D>(p, h, base, first, count, level, final, orow, cw, ncw, lane);
+    fused_merge_group<D>(p, h, base, L, first, count, level, final, orow, cw, ncw, lane);
     if (final) return;
     k >>= kFusedLog2FanIn;
     K = (K + kFusedFanIn - 1) >> kFusedLog2FanIn;

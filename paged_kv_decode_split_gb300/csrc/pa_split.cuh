@@ -934,7 +934,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     // Fused merge: the consumers of the CTA that finished a request's last
     // piece (of a group) combine the pieces' partials.
     if (p.fused && prow_base >= 0 && pass == npass - 1)
-      fused_merge<D>(p, r, h, prow_base, row0, ct, cw, Cfg::NCW, lane);
+      fused_merge<D>(p, r, h, prow_base, row0, L, ct, cw, Cfg::NCW, lane);
     tc_fence_before();
     __syncthreads();  // pairs with the producer's end-of-pass barrier
     tc_fence_after();
@@ -1442,7 +1442,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
     // issues the next item's first stages.
     if constexpr (D <= 256) {  // wide heads keep the merge kernel (registers)
       if (p.fused && prow_base >= 0 && pass == npass - 1)
-        fused_merge<D>(p, r, h, prow_base, row0, ct, cw, Cfg::NCW, lane);
+        fused_merge<D>(p, r, h, prow_base, row0, L, ct, cw, Cfg::NCW, lane);
     }
     __syncthreads();  // pairs with the producer's end-of-pass barrier
   }

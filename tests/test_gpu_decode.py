@@ -160,17 +160,25 @@ FUSED_CASES = {
     # tensor memory for fp8)
     "g16": dict(lens=[9000, 40, 2600, 300], H=(16, 1), budget=64),
     "g32": dict(lens=[5000, 1, 700], H=(32, 2), budget=48),
+    # multi-token rows (tokens x G in one work item): 3 x 8 rows, 4 x 8 rows
+    # (on tensor memory for fp8), 3 x 6 rows at head dim 256 (MTP verify)
+    "verify3": dict(lens=[9000, 40, 2600, 300], ql=[3, 3, 1, 3], H=(8, 1), budget=64, pad=2),
+    "verify4": dict(lens=[40000, 700, 5000], ql=[4, 4, 4], H=(8, 1), budget=4096),
+    "verify3_d256": dict(lens=[16384, 3000, 40], ql=[3, 3, 3], H=(6, 1), D=256, bs=64, budget=304),
 }
 
 
 @pytest.mark.parametrize("case", list(FUSED_CASES))
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
 def test_fused_merge(dev, case, kv):
-    """Decode-only plans can merge the pieces' partials inside the split kernel
-    (ticket tree of fan-in 8) and launch no merge kernel: the result matches
-    the oracle, matches the separate merge kernel's within the bounds, and a
-    second call on the same plan gives the same bits (every ticket was reset).
-    Sharp queries (q std 6) so that a wrong weight or a lost piece shows."""
+    """Plans whose requests' query rows fit one work item (decode, and
+    multi-token verify rows) can merge the pieces' partials inside the split
+    kernel (ticket tree of fan-in 8, every token of the request merged by the
+    CTA that took the group's last ticket) and launch no merge kernel: the
+    result matches the oracle, matches the separate merge kernel's within the
+    bounds, and a second call on the same plan gives the same bits (every
+    ticket was reset).  Sharp queries (q std 6) so that a wrong weight or a
+    lost piece shows."""
     c = dict(FUSED_CASES[case])
     lens, H = c.pop("lens"), c.pop("H")
     w = batch(dev, lens, H=H, kv=kv, seed=81 + len(lens), q_std=6.0, **c)
@@ -179,7 +187,7 @@ def test_fused_merge(dev, case, kv):
     assert not plan.fused_merge  # the merge kernel is the default
     plan.set_fused_merge(True)
     assert plan.fused_merge and plan.kernels_per_decode() == 1
-    plan.refresh(w.context_lens)
+    plan.refresh(w.context_lens, w.cu_query_lens)
     a = binding.decode_workload(plan, w)
     b = binding.decode_workload(plan, w)
     torch.cuda.synchronize()
@@ -206,15 +214,21 @@ def test_fused_merge_with_window_and_sinks(dev, kv):
         assert plan.read_errors() == 0
 
 
-def test_multi_token_plans_keep_the_merge_kernel(dev):
-    plan = binding.Plan(3, 6, 1, 256, max_query_len=3, max_tokens=12, device=dev)
-    assert not plan.fused_merge and plan.kernels_per_decode() == 2
-    with pytest.raises(binding.PaError) as e:
-        plan.set_fused_merge(True)
-    assert e.value.status == binding.PA_ERR_UNSUPPORTED
-    # a GQA group of 64 rows is more than one work item holds: no fused merge either
-    plan = binding.Plan(3, 64, 1, 128, device=dev)
-    assert not plan.fused_merge
+def test_fused_merge_needs_one_work_item_per_request(dev):
+    """The fused merge needs every query row of a request (tokens x GQA group)
+    in one work item (at most 32 rows) and a head dim of at most 256."""
+    plan = binding.Plan(3, 6, 1, 256, max_query_len=3, max_tokens=12, device=dev)  # 18 rows
+    assert plan.kernels_per_decode() == 2
+    plan.set_fused_merge(True)
+    assert plan.fused_merge and plan.kernels_per_decode() == 1
+    for args, kw in (((3, 6, 1, 256), dict(max_query_len=6, max_tokens=18)),  # 36 rows
+                     ((3, 64, 1, 128), {}),                                     # a group of 64
+                     ((3, 8, 1, 512), {})):                                     # a wide head
+        plan = binding.Plan(*args, device=dev, **kw)
+        assert not plan.fused_merge and plan.kernels_per_decode() == 2
+        with pytest.raises(binding.PaError) as e:
+            plan.set_fused_merge(True)
+        assert e.value.status == binding.PA_ERR_UNSUPPORTED
 
 
 def test_set_kv_dtype_rejects_other_values(dev):
