@@ -212,10 +212,13 @@ int pa_plan_set_kv_dtype(pa_plan* plan, int kv_dtype);
  * (max_query_len x the GQA group) fit one work item of the split kernel (at
  * most 32 rows) and whose head_dim is at most 256; every other plan keeps the
  * merge kernel, where a request's many query rows are better spread over many
- * CTAs.  The default is 0 for every plan: on
- * GB300 the merge kernel, chained to the split kernel by programmatic
- * dependent launch, measured 1.2-8 us faster per decode call on every batch
- * tried (the ticket round trip after each piece stalls that CTA's pipeline).
+ * CTAs.  The default is 0 for every plan: on GB300 the merge kernel, chained
+ * to the split kernel by programmatic dependent launch, measured faster per
+ * decode call on every batch tried -- 1.2-8 us on one-row decode (the ticket
+ * round trip after each piece stalls that CTA's pipeline), 5-9 us on 2-4-token
+ * verify rows and 21 us on 3-token verify at head dim 256 (the CTA that takes
+ * a request's last ticket merges all L x G rows of its pieces with a few
+ * warps, where the merge kernel spreads them over many CTAs).
  * PA_ERR_UNSUPPORTED for enable = 1 on such a plan, PA_ERR_INVALID_ARG for
  * another value.  Takes effect at the next pa_decode.  No counterpart in the
  * pages beyond the cost they measured. */
