@@ -74,7 +74,7 @@ DESCRIBE = {
                     "Hq/Hkv 16/2, D 1024, page 16, fp8-e4m3 KV (scale 0.05), K grouped, "
                     "budget 296, cap 256",
 }
-SPLIT_SOURCES = ["pa_split.cuh", "pa_split_cfg.h", "pa_device.cuh"]
+SPLIT_SOURCES = ["pa_split.cuh", "pa_split_cfg.h", "pa_device.cuh", "pa_fused.cuh"]
 L2_BYTES = 129 * 1024 * 1024
 
 
