@@ -13,10 +13,11 @@ sum_r S_r * Hkv * D * 2 (K and V) * elem_bytes per step, over the measured step
 time; `us_per_decode_call` is the pa_decode call (split + merge, the refresh
 excluded; a graph of K calls) and `us_per_refresh` the refresh alone.  With the
 default workload the same line also carries the Large batch with an fp8 cache
-(`large_fp8`) and the skewed agentic batch over --seeds seeds (`skewed_seeds`:
+(`large_fp8`), the skewed agentic batch over --seeds seeds (`skewed_seeds`:
 median / p10 fraction of the measured HBM copy peak, and the uniform-split
 plan's time over the proportional plan's on the same kernel, L2 flushed before
-every step).  `--sweep all` adds one line per configuration (L2 flushed before
+every step) and two multi-token verify batches (`verify`: the skewed fp8 batch
+x 3 tokens and MTP verify, L2 flushed).  `--sweep all` adds one line per configuration (L2 flushed before
 every step) and a summary over the skewed batch's seeds.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
@@ -608,6 +609,16 @@ def run_native(args, world, rank, local):
         if args.seeds > 0:
             line["skewed_seeds"] = skewed_seeds(dev, args.seeds, min(args.steps, 50),
                                                 args.warmup, peak)
+        # multi-token verify rows (speculative decoding): the fp8 skewed batch x
+        # 3 tokens (tensor-memory consumer) and MTP verify (bf16, D 256), both
+        # plans, L2 flushed before every step
+        line["verify"] = {}
+        for name in ("skewed_mtp3", "mtp_verify"):
+            wv = wl.CONFIGS[name](0, dev)
+            line["verify"][name] = {"workload": DESCRIBE[name],
+                                    **plan_ab(wv, min(args.steps, 50), args.warmup, True, peak)}
+            del wv
+            torch.cuda.empty_cache()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         w = wl.CONFIGS[args.workload](0, dev)
         gbs, secs, cores, desc = oracle_sample(w, args.cpu_seconds)
@@ -770,7 +781,7 @@ def main(argv=None):
     ap.add_argument("--profile-run", action="store_true",
                     help="W + K plain steps of the workload for a profiler (no timing)")
     ap.add_argument("--no-extra", action="store_true",
-                    help="headline workload only (no large_fp8 / skewed_seeds keys)")
+                    help="headline workload only (no large_fp8 / skewed_seeds / verify keys)")
     args = ap.parse_args(argv)
     world, rank, local = dist_setup()
     if args.impl == "reference":

@@ -33,8 +33,11 @@ def test_native_line_has_the_contract_keys():
     assert d["value"] > 0 and d["ms_per_step"] > 0 and d["higher_is_better"] is True
     assert "workload" in d["config"]
     assert d["config"]["name"] == "large_bf16"  # the largest single-GPU configuration
-    for key in ("large_fp8", "skewed_seeds"):  # the target's evidence, in the same line
+    for key in ("large_fp8", "skewed_seeds", "verify"):  # the target's evidence, in the same line
         assert key in d, key
+    for name in ("skewed_mtp3", "mtp_verify"):  # multi-token verify rows
+        v = d["verify"][name]
+        assert v["us_per_decode_call"] > 0 and 0 < v["call_frac_of_measured"]
     sk = d["skewed_seeds"]
     assert sk["seeds"] == 2 and len(sk["per_seed"]) == 2
     for k in ("call_frac_of_measured", "split_frac_of_measured",
