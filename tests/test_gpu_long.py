@@ -181,25 +181,31 @@ def _drift_lens(n: int, seed: int) -> list[int]:
     return [int(x) for x in rng.integers(100_000, 130_001, n)]
 
 
-@pytest.mark.parametrize("n,q_std", [(1, 1.0), (1, SHARP), (8, 1.0), (8, SHARP), (24, 1.0)])
-def test_error_does_not_grow_with_split_count(dev, n, q_std):
+@pytest.mark.parametrize("n,q_std,kv,ql", [(1, 1.0, "bf16", 1), (1, SHARP, "bf16", 1),
+                                           (8, 1.0, "bf16", 1), (8, SHARP, "bf16", 1),
+                                           (24, 1.0, "bf16", 1), (8, 1.0, "fp8", 3),
+                                           (8, SHARP, "fp8", 3)])
+def test_error_does_not_grow_with_split_count(dev, n, q_std, kv, ql):
     """One batch, one fp64 reference; the planned GPU result for partition
     ceilings 8 ... 256 (budget n x P x Hkv, so a request of mean length gets P
     partitions).  ||gpu - ref|| / ||ref|| and max |gpu - ref| / max |ref| stay
     below the relative bounds at every P, and at P = 256 within 1.5x their
-    value at P = 8."""
-    w = batch(dev, _drift_lens(n, 60 + n), H=(8, 1), seed=61 + n, q_std=q_std)
+    value at P = 8.  The fp8 3-token cases (24 rows per pass) run on the
+    tensor-memory consumer."""
+    w = batch(dev, _drift_lens(n, 60 + n), ql=None if ql == 1 else [ql] * n, H=(8, 1), kv=kv,
+              seed=61 + n + ql, q_std=q_std)
     ref = oracle_decode(w.to("cpu"))
     rows = []
     for P in DRIFT_P:
         out, plan = run(w, budget=n * P * w.num_kv_heads, max_partitions=P)
-        e = parity(out, ref, None if q_std > 1 else "bf16", what=f"P={P}")
+        e = parity(out, ref, None if q_std > 1 else kv, what=f"P={P}")
         rows.append({"P": P, "max_parts": int(partitions(plan).max()), **e})
-    table = {"n": n, "q_std": q_std, "lens": w.context_lens.tolist()[:4], "rows": rows}
+    table = {"n": n, "q_std": q_std, "kv": kv, "ql": ql, "lens": w.context_lens.tolist()[:4],
+             "rows": rows}
     print("DRIFT " + json.dumps(table))
     out_dir = os.environ.get("PA_DRIFT_OUT")
     if out_dir:
-        with open(os.path.join(out_dir, f"drift_n{n}_q{q_std:g}.json"), "w") as f:
+        with open(os.path.join(out_dir, f"drift_n{n}_q{q_std:g}_{kv}_l{ql}.json"), "w") as f:
             json.dump(table, f)
     assert rows[-1]["max_parts"] == 256 or n > 1
     e8, e256 = rows[0], rows[-1]
