@@ -507,6 +507,8 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
   float* s_mref = reinterpret_cast<float*>(s_llo + 32);  // the row's reference m_ref
   float* s_nm = s_mref + 32;                             // 6 - m_ref (log2 of 64, less m_ref)
   float* s_fac = s_nm + 32;                              // rescale factors, then row sums
+  long long* s_off = reinterpret_cast<long long*>(s_fac + 32);  // epilogue: a row's element offset
+  float* s_scl = reinterpret_cast<float*>(s_off + 32);          // epilogue: a row's scale
   float* s_red = reinterpret_cast<float*>(smb + Cfg::DATA_BYTES + Cfg::TC_RED_OFF);  // [4 warps][32]
   const uint32_t bar_s = bar_full + 16 * Cfg::NS;
   const uint32_t bar_p = bar_s + 16;
@@ -876,17 +878,65 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
           }
         }
         named_barrier_sync(2, 128);
-      } else {  // row sums: the threads' shares, over the warp, then the 4 warps
+      } else {
+        // row sums: the threads' shares, over the warp by a transpose-reduce
+        // (each exchange halves the rows a lane holds: TNP - 1 shuffles in
+        // all, lane l ending with row l of TNP = 32, or row l / 2 of 16),
+        // then over the 4 warps
+        constexpr int TNP = TN <= 16 ? 16 : 32;
+        float v[TNP];
 #pragma unroll
-        for (int j = 0; j < TN; ++j) {
-          float x = lp[j];
+        for (int j = 0; j < TNP; ++j) v[j] = j < TN ? lp[j] : 0.f;
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-          if (lane == 0) s_red[sw * 32 + j] = x;
+        for (int o = 16, n = TNP; n > 1; o >>= 1, n >>= 1) {
+          const bool up = (lane & o) != 0;
+#pragma unroll
+          for (int i = 0; i < n / 2; ++i) {
+            const float send = up ? v[i] : v[i + n / 2];
+            const float keep = up ? v[i + n / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+          }
         }
+        if constexpr (TNP == 16) v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+        const int row = TNP == 32 ? lane : lane >> 1;
+        if (row < TN && (TNP == 32 || (lane & 1) == 0)) s_red[sw * 32 + row] = v[0];
         named_barrier_sync(2, 128);
         if (st < TN) s_fac[st] = s_red[st] + s_red[32 + st] + s_red[64 + st] + s_red[96 + st];
         named_barrier_sync(2, 128);
+      }
+      // Per row, once (thread st = row): where it goes and by what it is
+      // scaled (1 / l with the sink, v_scale, the factor 64 of P'; 0 for a
+      // row with no visible key), and a partial's log2-sum-exp.
+      if (st < TN) {
+        const int j = st;
+        const int n = pass_base + j;
+        long long off = -1;
+        float scl = 0.f;
+        if (j < NQ && n < row_hi) {
+          const int tok = n / G;
+          const int hq = h * G + n % G;
+          const float M = s_mref[j];
+          float lsum = M != NEG_INF ? s_fac[j] * (1.f / 64.f) : 0.f;  // the row sums carry the 64 of P'
+          if (prow_base < 0) {
+            float f = 1.f;
+            if (p.sinks) f = add_sink(M, __ldg(p.sinks + hq) * 1.4426950408889634f, lsum);
+            const float inv = lsum > 0.f ? p.v_scale / (64.f * lsum) : 0.f;
+            scl = M != NEG_INF ? f * inv : 0.f;
+            const int trow = row0 + tok;
+            if (trow >= p.num_tokens)
+              atomicOr(p.plan.err, PA_DEVERR_PLAN_OVERFLOW);
+            else
+              off = (static_cast<long long>(trow) * p.Hq + hq) * D;
+          } else {
+            const float inv = lsum > 0.f ? p.v_scale / (64.f * lsum) : 0.f;
+            scl = M != NEG_INF ? inv : 0.f;
+            const long long prow = static_cast<long long>(prow_base + tok) * p.Hq + hq;
+            off = prow * D;
+            p.plan.part_lse[prow] = lsum > 0.f ? M + __log2f(lsum) : NEG_INF;
+          }
+        }
+        s_off[j] = off;
+        s_scl[j] = scl;
       }
       float ov[TN];
       {
@@ -900,33 +950,23 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
 #pragma unroll
         for (int j = 0; j < TN; ++j) ov[j] = __uint_as_float(a[j]) + __uint_as_float(a[TN + j]);
       }
+      named_barrier_sync(2, 128);
       const int d = kk;  // this thread's head dim
+      if (prow_base < 0) {
+        uint16_t* o16 = static_cast<uint16_t*>(p.out) + d;
 #pragma unroll
-      for (int j = 0; j < TN; ++j) {
-        const int n = pass_base + j;
-        if (j >= NQ || n >= row_hi) continue;
-        const int tok = n / G;
-        const int hq = h * G + n % G;
-        const float M = s_mref[j];
-        // L and O carry the factor 64 of P'
-        float lsum = M != NEG_INF ? s_fac[j] * (1.f / 64.f) : 0.f;
-        float v = M != NEG_INF ? ov[j] : 0.f;
-        if (prow_base < 0) {
-          if (p.sinks) v *= add_sink(M, __ldg(p.sinks + hq) * 1.4426950408889634f, lsum);
-          const float inv = lsum > 0.f ? p.v_scale / (64.f * lsum) : 0.f;
-          const int trow = row0 + tok;
-          if (trow >= p.num_tokens) {
-            if (d == 0) atomicOr(p.plan.err, PA_DEVERR_PLAN_OVERFLOW);
-            continue;
-          }
-          const uint32_t pk = p.out_f16 ? pack2<false>(v * inv, 0.f) : pack2<true>(v * inv, 0.f);
-          static_cast<uint16_t*>(p.out)[(static_cast<size_t>(trow) * p.Hq + hq) * D + d] =
-              static_cast<uint16_t>(pk & 0xffffu);
-        } else {
-          const float inv = lsum > 0.f ? p.v_scale / (64.f * lsum) : 0.f;
-          const size_t prow = static_cast<size_t>(prow_base + tok) * p.Hq + hq;
-          p.plan.part_o[prow * D + d] = v * inv;
-          if (d == 0) p.plan.part_lse[prow] = lsum > 0.f ? M + __log2f(lsum) : NEG_INF;
+        for (int j = 0; j < TN; ++j) {
+          const long long off = s_off[j];
+          const float x = ov[j] * s_scl[j];
+          if (off >= 0)
+            o16[off] = static_cast<uint16_t>((p.out_f16 ? pack2<false>(x, 0.f) : pack2<true>(x, 0.f)) & 0xffffu);
+        }
+      } else {
+        float* po = p.plan.part_o + d;
+#pragma unroll
+        for (int j = 0; j < TN; ++j) {
+          const long long off = s_off[j];
+          if (off >= 0) po[off] = ov[j] * s_scl[j];
         }
       }
     }

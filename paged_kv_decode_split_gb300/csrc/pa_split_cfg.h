@@ -56,7 +56,8 @@ struct SplitCfg {
   // kTc: the ring's barriers and seven more (S computed x2, P written x2,
   // P V done x2, drain), the tensor-memory address and a reduction area, then
   // (1024-aligned) q as e4m3 hi and lo [32 rows][128 B] each, per-row limits,
-  // references and factors, and a block of ones
+  // references, factors and the epilogue's offsets and scales, and a block of
+  // ones
   static constexpr int TC_TMEM_SLOT = 128;              // from DATA_BYTES (after the barriers)
   static constexpr int TC_RED_OFF = 512;                // reduction area [4][32] floats
   static constexpr int TC_Q_OFF = 1024;
@@ -119,7 +120,8 @@ struct SplitCfg {
                 "grouped K: every 16-key box starts on a 1024-byte swizzle repeat");
   static_assert(kTc || EX_BYTES <= DATA_BYTES, "epilogue exchange reuses the stage ring");
   static_assert(!kTc || (KS == 128 && SWB == 128 && CB == 1 && NS * 16 + 56 <= TC_TMEM_SLOT &&
-                         TC_ONES_OFF + 1024 <= kFixedBytes - 1024 && TC_ARR_OFF + 5 * 128 <= TC_ONES_OFF &&
+                         TC_ONES_OFF + 1024 <= kFixedBytes - 1024 &&
+                         TC_ARR_OFF + 5 * 128 + 32 * 8 + 32 * 4 <= TC_ONES_OFF &&
                          (DATA_BYTES + TC_ONES_OFF) % 1024 == 0),
                 "tcgen05 path: 128-key stages of 128-byte rows; the fixed area's layout");
   static_assert(D % 32 == 0, "head_dim is a multiple of 32");
