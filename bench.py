@@ -75,6 +75,10 @@ DESCRIBE = {
                     "Hq/Hkv 16/2, D 1024, page 16, fp8-e4m3 KV (scale 0.05), K grouped, "
                     "budget 296, cap 256",
 }
+for _kv, _kvd in (("fp8", "fp8-e4m3 KV (scale 0.05)"), ("bf16", "bf16 KV")):
+    for _t in (1, 2, 3, 4):
+        DESCRIBE[f"rows_{_kv}_t{_t}"] = (f"verify rows: 16 seqs x {_t} query token(s) at 16384 ctx, "
+                                         f"Hq/Hkv 32/4, D 128, page 16, {_kvd}")
 SPLIT_SOURCES = ["pa_split.cuh", "pa_split_cfg.h", "pa_device.cuh", "pa_fused.cuh"]
 L2_BYTES = 129 * 1024 * 1024
 
@@ -610,10 +614,10 @@ def run_native(args, world, rank, local):
             line["skewed_seeds"] = skewed_seeds(dev, args.seeds, min(args.steps, 50),
                                                 args.warmup, peak)
         # multi-token verify rows (speculative decoding): the fp8 skewed batch x
-        # 3 tokens (tensor-memory consumer) and MTP verify (bf16, D 256), both
-        # plans, L2 flushed before every step
+        # 3 tokens and 16 x 16384 keys x 3 tokens (tensor-memory consumer), and
+        # MTP verify (bf16, D 256), both plans, L2 flushed before every step
         line["verify"] = {}
-        for name in ("skewed_mtp3", "mtp_verify"):
+        for name in ("skewed_mtp3", "rows_fp8_t3", "mtp_verify"):
             wv = wl.CONFIGS[name](0, dev)
             line["verify"][name] = {"workload": DESCRIBE[name],
                                     **plan_ab(wv, min(args.steps, 50), args.warmup, True, peak)}

@@ -231,6 +231,14 @@ def mixed_prompt(seed: int = 0, device="cpu", pad_tokens: int = 21) -> Workload:
                       "bf16", seed=seed, pad_tokens=pad_tokens, device=device)
 
 
+def verify_rows(kv_dtype: str, tokens: int, seed: int = 0, device="cpu") -> Workload:
+    """Verify rows at head dim 128: 16 requests x 16384 keys, `tokens` query
+    tokens each (per-token causal ranges), Hq/Hkv 32/4, page 16, bf16 or fp8
+    KV (scale 0.05)."""
+    return make_batch(f"rows_{kv_dtype}_t{tokens}", [16384] * 16, [tokens] * 16, 32, 4, 128, 16,
+                      kv_dtype, seed=seed, kv_scale=0.05, device=device)
+
+
 def large(kv_dtype: str = "bf16", seed: int = 0, device="cpu") -> Workload:
     """512 decodes, context lognormal(median 2048, sigma 1.2) clipped to [16, 65536],
     Hq/Hkv 64/8, D 128, page 128, bf16 or fp8 KV, budget 2 x SM, cap 256."""
@@ -331,6 +339,10 @@ CONFIGS["uniform_d1024"] = uniform_d1024
 CONFIGS["skewed_d1024"] = skewed_d1024
 CONFIGS["uniform_n64_h8"] = uniform_n64_h8
 CONFIGS["skewed_mtp3"] = skewed_mtp3
+for _kv in ("fp8", "bf16"):
+    for _t in (1, 2, 3, 4):
+        CONFIGS[f"rows_{_kv}_t{_t}"] = (lambda seed=0, device="cpu", kv=_kv, t=_t:
+                                        verify_rows(kv, t, seed, device))
 
 
 @dataclass

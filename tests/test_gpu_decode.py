@@ -768,7 +768,8 @@ def _pick(w, k=4):
 
 FULL = ["uniform", "skewed", "mtp_verify", "mixed_prompt", "large_bf16", "large_fp8",
         "uniform_w1024", "skewed_w4096", "uniform_k5", "skewed_k5", "uniform_d512",
-        "skewed_d1024", "uniform_d1024", "uniform_n64_h8", "skewed_mtp3"]
+        "skewed_d1024", "uniform_d1024", "uniform_n64_h8", "skewed_mtp3", "rows_fp8_t3",
+        "rows_bf16_t4"]
 
 
 @pytest.mark.parametrize("name", FULL)
