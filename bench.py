@@ -16,8 +16,9 @@ default workload the same line also carries the Large batch with an fp8 cache
 (`large_fp8`), the skewed agentic batch over --seeds seeds (`skewed_seeds`:
 median / p10 fraction of the measured HBM copy peak, and the uniform-split
 plan's time over the proportional plan's on the same kernel, L2 flushed before
-every step) and two multi-token verify batches (`verify`: the skewed fp8 batch
-x 3 tokens and MTP verify, L2 flushed).  `--sweep all` adds one line per configuration (L2 flushed before
+every step) and three multi-token verify batches (`verify`: the skewed fp8
+batch x 3 tokens, 16 x 16384 keys x 3 tokens in fp8, and MTP verify; L2
+flushed).  `--sweep all` adds one line per configuration (L2 flushed before
 every step) and a summary over the skewed batch's seeds.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]

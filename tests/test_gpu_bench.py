@@ -35,7 +35,7 @@ def test_native_line_has_the_contract_keys():
     assert d["config"]["name"] == "large_bf16"  # the largest single-GPU configuration
     for key in ("large_fp8", "skewed_seeds", "verify"):  # the target's evidence, in the same line
         assert key in d, key
-    for name in ("skewed_mtp3", "mtp_verify"):  # multi-token verify rows
+    for name in ("skewed_mtp3", "rows_fp8_t3", "mtp_verify"):  # multi-token verify rows
         v = d["verify"][name]
         assert v["us_per_decode_call"] > 0 and 0 < v["call_frac_of_measured"]
     sk = d["skewed_seeds"]
