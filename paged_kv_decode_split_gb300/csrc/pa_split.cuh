@@ -478,11 +478,11 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
   //     for all 128 rows): L is every row's sum of the very weights O was
   //     accumulated with (for fewer rows each softmax thread sums its key's
   //     share); the commit frees the ring slot.
-  // The issuing thread runs P V(g) as soon as P'(g) is written -- releasing
-  // the ring slot comes first -- and S(g + 2) as soon as that stage has
-  // landed and stage g's P' is written (S buffer g & 1 then free), so the
-  // softmax of stage g + 1 works on an S computed while stage g's softmax
-  // ran.  A row's reference m_ref moves (O and L rescaled) only when a logit
+  // The issuing thread runs S(g + 2) as soon as that stage has landed and
+  // stage g's P' is written (S buffer g & 1 then free) -- the softmax warps
+  // wait on it first -- and P V(g) as soon as P'(g) is written, which
+  // releases the ring slot; so the softmax of stage g + 1 works on an S
+  // computed while stage g's softmax ran.  A row's reference m_ref moves (O and L rescaled) only when a logit
   // exceeds it by more than 2.8 (log2 units): P' stays below 2^8.8, inside
   // e4m3's range (448).
   // Barriers (by stage parity where two operations of a kind can be
@@ -622,10 +622,11 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
       if (lane == 0 && nst > 0) {  // one lane: no warp-collective calls in here
         const uint64_t dq = tc_desc(q_hi, 16, 1024);  // +2 per 32-byte step along K
         const uint64_t d1 = tc_desc(ones, 16, 0);     // SBO 0: one 8-row block for all 128 rows
-        // Two kinds of work, taken as their inputs become ready, P V first
-        // (it frees a ring slot): P V(np) once P'(np) is written, and
-        // S(nq) = K [q_hi; q_lo]^T once stage nq has landed and S buffer
-        // nq & 1 is free (stage nq - 2's P' written, i.e. np >= nq - 1).
+        // Two kinds of work, taken as their inputs become ready, S first
+        // (the softmax warps wait on it): S(nq) = K [q_hi; q_lo]^T once
+        // stage nq has landed and S buffer nq & 1 is free (stage nq - 2's P'
+        // written, i.e. np >= nq - 1), and P V(np) once P'(np) is written
+        // (its commit frees the ring slot).
         // Short suspending tries on both; a wait without progress for
         // wait_ns gives up.
         int np = 0, nq = 0;
@@ -633,7 +634,21 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
         unsigned long long t_idle = 0;
         while (np < nst) {
           bool did = false;
-          if (np < nq) {
+          if (nq < nst && nq <= np + 1) {
+            const int g = it + nq;
+            const int slot = g % Cfg::NS;
+            if (mbar_try_wait_hint(bar_full + 8 * slot, (g / Cfg::NS) & 1, 20)) {
+              tc_fence_after();
+              const uint64_t dk = tc_desc(base + slot * Cfg::STAGE_BYTES, 16, 1024);
+              const uint32_t sd = tmem + static_cast<uint32_t>((g & 1) * CS);
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks) tc_mma_e4m3(sd, dk + 2 * ks, dq + 2 * ks, kIdQK, ks > 0);
+              tc_commit(bar_s + 8 * (g & 1));
+              ++nq;
+              did = true;
+            }
+          }
+          if (!did && np < nq) {
             const int g = it + np;
             if (mbar_try_wait_hint(bar_p + 8 * (g & 1), (g >> 1) & 1, 20)) {
               // ---- O^T += V^T P'^T and L^T += 1 P'^T; the commit frees the ring slot
@@ -653,20 +668,6 @@ __global__ void __launch_bounds__(SplitCfg<D, KVT, WQ, KL>::THREADS,
               tc_commit(bar_empty + 8 * slot);
               tc_commit(bar_o + 8 * (g & 1));
               ++np;
-              did = true;
-            }
-          }
-          if (!did && nq < nst && nq <= np + 1) {
-            const int g = it + nq;
-            const int slot = g % Cfg::NS;
-            if (mbar_try_wait_hint(bar_full + 8 * slot, (g / Cfg::NS) & 1, 20)) {
-              tc_fence_after();
-              const uint64_t dk = tc_desc(base + slot * Cfg::STAGE_BYTES, 16, 1024);
-              const uint32_t sd = tmem + static_cast<uint32_t>((g & 1) * CS);
-#pragma unroll
-              for (int ks = 0; ks < 4; ++ks) tc_mma_e4m3(sd, dk + 2 * ks, dq + 2 * ks, kIdQK, ks > 0);
-              tc_commit(bar_s + 8 * (g & 1));
-              ++nq;
               did = true;
             }
           }
